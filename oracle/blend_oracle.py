@@ -1,0 +1,479 @@
+"""CPU oracle for blended (selective KV-recompute) RAG prefill.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product path imports this module: only
+the tests, the smoke check of the package entry script and the CPU-baseline leg
+of the benchmark do.  It shares no code with the CUDA path.
+
+Plain numpy in float64, written to be read against the pages rather than to be
+fast.  Matrix products use numpy's matmul (a library primitive); everything else
+is written out step by step.  Where the pages are silent, the reading taken is
+stated next to the function.
+
+Sources (page title, section):
+  * CacheClip blog, "6.1 Shared prefix and position IDs", "6.2 Auxiliary-model-guided
+    token selection", "6.3 Sliding-window grouping" (with Figure 6 and its rule list).
+  * CacheClip paper (arXiv 2510.10129), "4.1 KV Cache Calibration with Shared Prefix",
+    "4.3 Sliding-Window Grouping and KV Cache Update".
+  * CacheBlend blog, "Prefill and the KV cache", "Selective KV recompute",
+    "Picking the tokens to recompute", "The chicken-and-egg problem", "Implementation".
+  * SpecCache notes, "2.2 Importance score estimation" (the I_i formula) and
+    "2.3 Semantic span completion" (TopK with K = ceil(rho N)).
+
+Parity pins (what each function is checked against, in tests/test_oracle_*.py):
+  rope / realign      : rotation composition R(d)R(p)x = R(p+d)x, identity at 0, closed
+                        form on basis vectors, relative-position invariance of q.k
+  rmsnorm / silu      : closed forms on constant vectors
+  attention           : single key -> that value row; two keys -> closed-form softmax
+                        weights with the 1/sqrt(d) scale; GQA with duplicated K/V heads
+                        equals MHA; causal mask by brute force
+  full_prefill        : causality (a prefix of the input gives the same rows)
+  assemble            : prefix kept once, chunk rows are the realigned pool rows
+  select              : the Figure 6 worked case (tests/golden), brute force over all
+                        candidate subsets on tiny inputs, monotonicity in the budget
+  blend_prefill       : rho=100 % equals full prefill; rho=0 leaves every chunk row at its
+                        realigned cache value; chunk 0 (shift 0) has zero layer-0 deviation
+  importance_scores   : closed form on constant hidden states
+"""
+from __future__ import annotations
+
+import math
+from typing import Optional
+
+import numpy as np
+
+F64 = np.float64
+
+
+# ----------------------------------------------------------------------------------
+# Rotary position embedding and KV realignment
+# ----------------------------------------------------------------------------------
+
+def rope_inv_freq(head_dim: int, theta: float) -> np.ndarray:
+    """theta^(-2i/d) for i = 0..d/2-1 (rotary embedding frequencies).
+
+    Reading: the pages only say RoPE (CacheBlend blog, "Selective KV recompute", the
+    footnote on positional correctness); we take the rotate-half pairing (i, i+d/2).
+    """
+    i = np.arange(head_dim // 2, dtype=F64)
+    return np.power(F64(theta), -2.0 * i / head_dim)
+
+
+def rope_rotate(x: np.ndarray, pos: np.ndarray, theta: float) -> np.ndarray:
+    """Rotate every head vector of x[..., n, heads, d] by the angle pos[n] * inv_freq.
+
+    Pair (i, i+d/2) is rotated by angle a: (x_i cos a - x_{i+d/2} sin a,
+    x_{i+d/2} cos a + x_i sin a).  pos may be any integer (negative allowed).
+    """
+    x = np.asarray(x, dtype=F64)
+    d = x.shape[-1]
+    h = d // 2
+    ang = np.asarray(pos, dtype=F64)[:, None] * rope_inv_freq(d, theta)[None, :]   # [n, d/2]
+    c = np.cos(ang)[:, None, :]
+    s = np.sin(ang)[:, None, :]
+    x1 = x[..., :h]
+    x2 = x[..., h:]
+    return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1)
+
+
+def realign_keys(k_cached: np.ndarray, delta: np.ndarray, theta: float) -> np.ndarray:
+    """Move cached keys by delta positions: one more rotation by delta * inv_freq.
+
+    Cached keys were rotated at their precompute position p; RoPE rotations compose,
+    so rotating by delta gives the key at p + delta (CacheBlend blog, "Selective KV
+    recompute", positional-correctness footnote; CacheClip "Position ID rearrangement").
+    """
+    return rope_rotate(k_cached, delta, theta)
+
+
+# ----------------------------------------------------------------------------------
+# Decoder layer pieces
+# ----------------------------------------------------------------------------------
+
+def rmsnorm(x: np.ndarray, g: np.ndarray, eps: float) -> np.ndarray:
+    """x / sqrt(mean(x^2) + eps) * g over the last axis."""
+    x = np.asarray(x, dtype=F64)
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    return x / np.sqrt(ms + eps) * np.asarray(g, dtype=F64)
+
+
+def silu(x: np.ndarray) -> np.ndarray:
+    return x / (1.0 + np.exp(-x))
+
+
+def attention(q: np.ndarray, qpos: np.ndarray, K: np.ndarray, V: np.ndarray) -> np.ndarray:
+    """Causal grouped-query attention of a set of query rows over a full KV.
+
+    q[n, hq, d] at positions qpos[n]; K, V [N, hkv, d] indexed by position.  Query
+    head h reads KV head h // (hq/hkv).  Row i attends keys 0..qpos[i] inclusive with
+    softmax(q.k / sqrt(d)).  Each row is complete even though only a few rows are
+    computed (CacheBlend blog, "Selective KV recompute": expand K and V back to full
+    length, then run ordinary attention).
+    """
+    n, hq, d = q.shape
+    hkv = K.shape[1]
+    group = hq // hkv
+    out = np.zeros((n, hq, d), dtype=F64)
+    scale = 1.0 / math.sqrt(d)
+    for i in range(n):
+        p = int(qpos[i])
+        qi = q[i].reshape(hkv, group, d)                       # head h = g*group + j
+        s = np.einsum("tgd,gjd->gjt", K[:p + 1], qi) * scale     # [hkv, group, p+1]
+        s = s - np.max(s, axis=-1, keepdims=True)
+        e = np.exp(s)
+        a = e / np.sum(e, axis=-1, keepdims=True)
+        out[i] = np.einsum("gjt,tgd->gjd", a, V[:p + 1]).reshape(hq, d)
+    return out
+
+
+def layer_kv(w: dict, cfg: dict, layer: int, x: np.ndarray, pos: np.ndarray,
+             K: np.ndarray, V: np.ndarray, dev_rows: Optional[np.ndarray] = None,
+             dev_mode: str = "kv"):
+    """First half of a pre-norm decoder layer on the rows x[n, H] at positions pos[n]:
+    RMSNorm, Q/K/V projection, RoPE at the blended positions, and the overwrite of this
+    layer's cache rows K[pos], V[pos] with the fresh keys and values.
+
+    These are the first steps of selective recompute (CacheBlend blog, "Selective KV
+    recompute"): the layer input is already reduced to the selected rows; they are
+    projected to Q, K, V; K and V are expanded back to full length with the reused
+    rows of the other tokens.
+
+    If dev_rows (bool[n]) is given, the KV deviation of those rows is returned: the
+    squared L2 distance between the fresh and the cached K and V rows at the same
+    position, taken before the overwrite (CacheBlend blog, "Selective KV recompute":
+    how far the cached KV sits from the recomputed one; "Implementation": the largest
+    deviation between newly computed and loaded KV).  dev_mode "v" compares V only
+    (CacheClip paper, "Related work": CacheBlend compares the value matrix).
+    Returns q [n, hq, d] and dev [n] (or None).
+    """
+    hq, hkv, d = cfg["n_q_heads"], cfg["n_kv_heads"], cfg["head_dim"]
+    eps, theta = cfg["rms_eps"], cfg["rope_theta"]
+    n = x.shape[0]
+    h = rmsnorm(x, w["attn_norm"][layer], eps)
+    q = (h @ w["wq"][layer].T).reshape(n, hq, d)
+    k = (h @ w["wk"][layer].T).reshape(n, hkv, d)
+    v = (h @ w["wv"][layer].T).reshape(n, hkv, d)
+    q = rope_rotate(q, pos, theta)
+    k = rope_rotate(k, pos, theta)
+    dev = None
+    if dev_rows is not None:
+        dk = (k - K[pos]).reshape(n, -1)
+        dv = (v - V[pos]).reshape(n, -1)
+        full = np.sum(dv * dv, axis=1)
+        if dev_mode == "kv":
+            full = full + np.sum(dk * dk, axis=1)
+        dev = np.where(dev_rows, full, 0.0)
+    K[pos] = k
+    V[pos] = v
+    return q, dev
+
+
+def layer_rest(w: dict, cfg: dict, layer: int, x: np.ndarray, q: np.ndarray, pos: np.ndarray,
+               K: np.ndarray, V: np.ndarray) -> np.ndarray:
+    """Second half of the layer for the rows that continue: causal attention of their
+    queries over this layer's full K, V, O-projection and residual, RMSNorm, SwiGLU MLP
+    and residual ("run the ordinary attention module to get the next layer's input")."""
+    hq, d = cfg["n_q_heads"], cfg["head_dim"]
+    eps = cfg["rms_eps"]
+    n = x.shape[0]
+    o = attention(q, pos, K, V).reshape(n, hq * d)
+    x = np.asarray(x, dtype=F64) + o @ w["wo"][layer].T
+    h2 = rmsnorm(x, w["mlp_norm"][layer], eps)
+    return x + (silu(h2 @ w["wg"][layer].T) * (h2 @ w["wu"][layer].T)) @ w["wd"][layer].T
+
+
+def layer_forward(w: dict, cfg: dict, layer: int, x: np.ndarray, pos: np.ndarray,
+                  K: np.ndarray, V: np.ndarray, dev_rows: Optional[np.ndarray] = None,
+                  dev_mode: str = "kv"):
+    """A whole decoder layer on rows x at positions pos (layer_kv then layer_rest)."""
+    q, dev = layer_kv(w, cfg, layer, x, pos, K, V, dev_rows, dev_mode)
+    return layer_rest(w, cfg, layer, x, q, pos, K, V), dev
+
+
+def full_prefill(w: dict, cfg: dict, tokens: np.ndarray):
+    """Standard causal prefill of every token (the quality reference, CacheBlend blog,
+    "Prefill and the KV cache").  Returns final-norm hidden rows, K, V [L, N, hkv, d]."""
+    N = len(tokens)
+    L, hkv, d = cfg["n_layers"], cfg["n_kv_heads"], cfg["head_dim"]
+    K = np.zeros((L, N, hkv, d), dtype=F64)
+    V = np.zeros((L, N, hkv, d), dtype=F64)
+    pos = np.arange(N)
+    x = np.asarray(w["embed"], dtype=F64)[np.asarray(tokens)]
+    for layer in range(L):
+        x, _ = layer_forward(w, cfg, layer, x, pos, K[layer], V[layer])
+    return rmsnorm(x, w["final_norm"], cfg["rms_eps"]), K, V
+
+
+def precompute_chunk(w: dict, cfg: dict, prefix_tokens, chunk_tokens):
+    """Offline encoding of [shared prefix + chunk] at positions 0..P+L-1 (CacheClip
+    "4.1 KV Cache Calibration with Shared Prefix").  Returns K, V [L, P+L, hkv, d]."""
+    toks = np.concatenate([np.asarray(prefix_tokens), np.asarray(chunk_tokens)])
+    _, K, V = full_prefill(w, cfg, toks)
+    return K, V
+
+
+# ----------------------------------------------------------------------------------
+# Cache preparation
+# ----------------------------------------------------------------------------------
+
+def assemble(entries_k, entries_v, chunk_ids, prefix_len: int, chunk_lens, query_len: int,
+             theta: float):
+    """Concatenate the retrieved chunk caches behind one prefix copy and realign keys.
+
+    entries_k[c], entries_v[c]: [L, P+L_c, hkv, d] of pool entry c (each holds its own
+    prefix copy).  Only the first chunk's prefix rows are kept (CacheClip "6.1 Shared
+    prefix and position IDs", steps 2-3).  Chunk j, precomputed at positions P..P+L_j-1,
+    moves to P+off_j..P+off_j+L_j-1 with off_j = sum of earlier chunk lengths, so its keys
+    are rotated by delta = off_j and its values copied (step 4; CacheClip "Position ID
+    rearrangement").  Query rows are left zero: they are always recomputed.
+    Returns K, V [L, N, hkv, d] with N = P + sum(L_j) + Q.
+    """
+    P = prefix_len
+    first = chunk_ids[0]
+    L, _, hkv, d = entries_k[first].shape
+    n_c = int(sum(chunk_lens))
+    N = P + n_c + query_len
+    K = np.zeros((L, N, hkv, d), dtype=F64)
+    V = np.zeros((L, N, hkv, d), dtype=F64)
+    K[:, :P] = entries_k[first][:, :P]
+    V[:, :P] = entries_v[first][:, :P]
+    off = 0
+    for c, lc in zip(chunk_ids, chunk_lens):
+        src_k = np.asarray(entries_k[c], dtype=F64)[:, P:P + lc]
+        src_v = np.asarray(entries_v[c], dtype=F64)[:, P:P + lc]
+        delta = np.full(lc, off)
+        for layer in range(L):
+            K[layer, P + off:P + off + lc] = realign_keys(src_k[layer], delta, theta)
+        V[:, P + off:P + off + lc] = src_v
+        off += lc
+    return K, V
+
+
+# ----------------------------------------------------------------------------------
+# Token selection
+# ----------------------------------------------------------------------------------
+
+def _order_key(score: float, t: int):
+    """Candidates are ranked by score (descending), ties by position (ascending).
+    -0.0 counts as +0.0; NaN ranks below every number (reading: pages are silent)."""
+    s = float(score)
+    if math.isnan(s):
+        return (1, 0.0, t)
+    if s == 0.0:
+        s = 0.0
+    return (0, -s, t)
+
+
+def topk(scores: np.ndarray, k: int, allowed: Optional[np.ndarray] = None) -> list:
+    """Positions of the k highest scores among the allowed ones (SpecCache 2.2,
+    TopK(I, K); CacheClip 6.2 step 6), ranked as in _order_key."""
+    n = len(scores)
+    idx = [t for t in range(n) if allowed is None or allowed[t]]
+    idx.sort(key=lambda t: _order_key(scores[t], t))
+    return idx[:max(0, min(k, len(idx)))]
+
+
+def group_windows(candidates, n: int, w: int, tau: int) -> set:
+    """CacheClip sliding-window grouping (blog "6.3 Sliding-window grouping", the rule
+    list and Figure 6; paper 4.3).  Scan window starts t = 0..n-w with step 1; a window
+    [t, t+w) is evaluated only if t is a candidate; if it holds at least tau candidates
+    every position in it joins the recompute set, gaps included.  Candidates not covered
+    by a passing window are dropped."""
+    cand = set(candidates)
+    out = set()
+    for t in range(n - w + 1):
+        if t not in cand:
+            continue
+        density = 0
+        for j in range(t, t + w):
+            if j in cand:
+                density += 1
+        if density >= tau:
+            out.update(range(t, t + w))
+    return out
+
+
+def select(scores: np.ndarray, budget: int, w: int, tau: int, budget_mode: str = "final",
+           allowed: Optional[np.ndarray] = None, base: int = 0) -> np.ndarray:
+    """Recompute set from per-token scores over the chunk region (positions base..base+n-1).
+
+    candidate mode: the top-`budget` scores are the candidates, grouped as above (the
+      CacheClip pseudocode literally: k = ratio x N candidates).
+    final mode: the largest k <= budget whose grouped set has at most `budget` rows, so
+      the ratio bounds the rows actually recomputed (CacheBlend: recomputing r % of the
+      tokens costs about r % of a prefill; SpecCache 2.3: a global budget after span
+      completion).  The grouped set grows with k, so the first k found scanning down
+      from the budget is the largest.
+    allowed (bool[n]): only these positions may be candidates or be returned (gradual
+      filtering never adds a token outside the previous stage's set).
+    Returns sorted absolute positions (int64).
+    """
+    n = len(scores)
+
+    def grouped(k):
+        s = group_windows(topk(scores, k, allowed), n, w, tau)
+        if allowed is not None:
+            s = {t for t in s if allowed[t]}
+        return s
+
+    if budget_mode == "candidate":
+        res = grouped(budget)
+    elif budget_mode == "final":
+        res = set()
+        k = budget
+        while k > 0:
+            s = grouped(k)
+            if len(s) <= budget:
+                res = s
+                break
+            k -= 1
+    else:
+        raise ValueError(budget_mode)
+    return np.array(sorted(base + t for t in res), dtype=np.int64)
+
+
+def select_final_bisect(scores, budget, w, tau, allowed=None, base=0) -> np.ndarray:
+    """Same result as select(..., 'final') using bisection on k (the grouped set grows
+    with k), for sizes where the linear scan is slow."""
+    n = len(scores)
+    order = topk(scores, n, allowed)
+    n_ok = len(order)
+
+    def grouped(k):
+        s = group_windows(order[:k], n, w, tau)
+        if allowed is not None:
+            s = {t for t in s if allowed[t]}
+        return s
+
+    lo, hi = 0, min(budget, n_ok)          # invariant: |grouped(lo)| <= budget
+    if len(grouped(hi)) <= budget:
+        lo = hi
+    else:
+        while hi - lo > 1:
+            mid = (lo + hi) // 2
+            if len(grouped(mid)) <= budget:
+                lo = mid
+            else:
+                hi = mid
+    return np.array(sorted(base + t for t in grouped(lo)), dtype=np.int64)
+
+
+def importance_scores(hidden: np.ndarray) -> np.ndarray:
+    """SpecCache 2.2: I_i = mean over the deep layers of ||h_i^(l)||_2.
+    hidden: [tokens, layers, dim] (the deep-layer slices of a small model)."""
+    h = np.asarray(hidden, dtype=F64)
+    return np.mean(np.sqrt(np.sum(h * h, axis=-1)), axis=-1)
+
+
+# ----------------------------------------------------------------------------------
+# Blended prefill
+# ----------------------------------------------------------------------------------
+
+def ceil_bp(rho_bp: int, n: int) -> int:
+    """ceil(rho * n) with rho in basis points (SpecCache 2.2, K = ceil(rho N))."""
+    return (rho_bp * n + 9999) // 10000
+
+
+CHECK_LAYERS = (1, 2)
+
+
+def blend_prefill(w: dict, cfg: dict, entries_k, entries_v, entry_tokens, prefix_tokens,
+                  chunk_ids, query_tokens, mode: str, rho_bp: int = 0, r1_bp: int = 0,
+                  window: int = 1, tau: int = 1, budget_mode: str = "final",
+                  scores: Optional[np.ndarray] = None, forced: Optional[list] = None,
+                  dev_mode: str = "kv"):
+    """Selective KV-recompute prefill of one request.
+
+    1. Assemble the blended cache (see assemble()).
+    2. Run every layer on a set of chunk rows plus the query rows (always recomputed),
+       in ascending position order.  The schedule is a list of stages
+       (first_layer, positions): from first_layer on, the rows that go through attention
+       and the MLP are `positions` + query.  A layer projects K, V for the rows that
+       entered it (the previous layer's rows) and writes them into the cache; when a
+       new stage starts at that layer, only the new (smaller) set continues.
+       * "ext":   one stage [(0, S)] with S = select(scores, ceil(rho N_c), w, tau, mode)
+                  from external per-chunk-token scores (CacheClip 6.2-6.3; SpecCache 2.2).
+       * "hkvd":  gradual filtering (CacheBlend blog, "The chicken-and-egg problem"; the
+                  CacheClip paper's summary: the first layer is recomputed in full, the
+                  second partially, and its fresh KV is compared with the loaded one).
+                  Stage 0 = every chunk row.  The first layer's K, V depend only on a
+                  token and its realigned position, so it has no deviation to rank; the
+                  checks are at layers 1 and 2 (CHECK_LAYERS, counted from 0):
+                  layer 1 ranks every chunk row by deviation and keeps the top
+                  ceil(r1 N_c) as C1; layer 2 ranks the C1 rows and keeps
+                  S = select(dev2 over C1, ceil(rho N_c), w, tau, mode), within C1.
+                  The set only shrinks; S is used from layer 2's attention onward.
+       * "forced": the caller's stages (deviations are still reported at the check layers).
+       * "full":  every row 0..N-1 at every layer (full prefill through the same steps).
+    3. Output the final RMSNorm of the query rows and the blended K, V of every layer.
+
+    Positions in sets are absolute positions in the blended sequence.
+    Returns a dict: hidden [Q, H], K, V [L, N, hkv, d], stages, dev1, dev2 ([N_c] each,
+    zero outside the rows checked).
+    """
+    L = cfg["n_layers"]
+    P = len(prefix_tokens)
+    lens = [len(entry_tokens[c]) for c in chunk_ids]
+    n_c = int(sum(lens))
+    Q = len(query_tokens)
+    N = P + n_c + Q
+    K, V = assemble(entries_k, entries_v, chunk_ids, P, lens, Q, cfg["rope_theta"])
+    tokens = np.concatenate([np.asarray(prefix_tokens)] + [np.asarray(entry_tokens[c]) for c in chunk_ids]
+                            + [np.asarray(query_tokens)])
+    lo, hi = P, P + n_c
+    qrows = np.arange(hi, N)
+    budget = ceil_bp(rho_bp, n_c)
+
+    if mode == "ext":
+        s = np.asarray(scores)
+        sel = (select(s, budget, window, tau, budget_mode, base=lo) if budget_mode == "candidate"
+               else select_final_bisect(s, budget, window, tau, base=lo))
+        stages = [(0, sel)]
+    elif mode == "hkvd":
+        stages = [(0, np.arange(lo, hi))]
+    elif mode == "forced":
+        stages = [(int(f), np.asarray(p, dtype=np.int64)) for f, p in forced]
+    elif mode == "full":
+        stages = [(0, np.arange(0, hi))]
+    else:
+        raise ValueError(mode)
+
+    def rows_at(layer):
+        cur = None
+        for f, p in stages:
+            if f <= layer:
+                cur = p
+        return np.concatenate([cur, qrows]).astype(np.int64)
+
+    devs = {}
+    rows = rows_at(0)
+    x = np.asarray(w["embed"], dtype=F64)[tokens[rows]]
+    for layer in range(L):
+        check = mode in ("hkvd", "forced") and layer in CHECK_LAYERS
+        dev_rows = ((rows >= lo) & (rows < hi)) if check else None
+        q, dev = layer_kv(w, cfg, layer, x, rows, K[layer], V[layer], dev_rows, dev_mode)
+        if dev is not None:
+            full = np.zeros(n_c, dtype=F64)
+            full[rows[dev_rows] - lo] = dev[dev_rows]
+            devs[layer] = full
+        if mode == "hkvd" and layer == CHECK_LAYERS[0]:
+            c1 = np.array(sorted(lo + t for t in topk(devs[layer], ceil_bp(r1_bp, n_c))), dtype=np.int64)
+            stages.append((layer, c1))
+        if mode == "hkvd" and layer == CHECK_LAYERS[1]:
+            allowed = np.zeros(n_c, dtype=bool)
+            allowed[stages[1][1] - lo] = True
+            dscore = np.where(allowed, devs[layer], -np.inf)
+            sel = (select(dscore, budget, window, tau, budget_mode, allowed=allowed, base=lo)
+                   if budget_mode == "candidate"
+                   else select_final_bisect(dscore, budget, window, tau, allowed=allowed, base=lo))
+            stages.append((layer, sel))
+        new_rows = rows_at(layer)
+        if not np.array_equal(new_rows, rows):
+            where = {int(p): i for i, p in enumerate(rows)}
+            keep = [where[int(p)] for p in new_rows]
+            x, q, rows = x[keep], q[keep], new_rows
+        x = layer_rest(w, cfg, layer, x, q, rows, K[layer], V[layer])
+    qi = np.searchsorted(rows, qrows)
+    hidden = rmsnorm(x[qi], w["final_norm"], cfg["rms_eps"])
+    return {"hidden": hidden, "K": K, "V": V, "stages": stages,
+            "dev1": devs.get(CHECK_LAYERS[0]), "dev2": devs.get(CHECK_LAYERS[1]),
+            "tokens": tokens, "N": N, "n_c": n_c}
