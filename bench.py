@@ -1,0 +1,439 @@
+"""Benchmark of blended (selective KV-recompute) prefill on one GB300 per rank.
+
+One step = the whole hot path for one request of the workload: SpecCache-style
+importance scores from the small model's hidden states, then blend_prefill (cache
+assembly with RoPE realignment, selection with window grouping, every layer's
+selective recompute of the chosen rows plus the query, final norm).  Inputs are
+seeded synthetic tensors with the workload's shapes; weights are random (no trained
+checkpoint).  `value` is blended context tokens per second (N / TTFT) with inputs
+already resident in HBM; `e2e` repeats the measurement through the same C ABI with the
+step's inputs copied from pinned host memory and the first-token hidden state copied
+back every step.
+
+--impl reference times the CPU oracle instead (the plain fp64 restatement of the
+method, on the host cores), on a bounded sample of the same workload.
+Under torchrun every rank runs its own replica of the workload (the path has no
+exchange step): scaling is weak and `value` sums the ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import dataclasses
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from rag_kv_cache_rope_gb300 import synth  # noqa: E402
+
+PEAKS = {"hbm_gbs": 6789.0, "bf16_tflops": 1874.3, "bf16_tflops_sustained": 1722.0}
+PEAKS_SRC = "fallback"
+try:
+    with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+        PEAKS.update({k: v for k, v in json.load(f).items() if k in PEAKS})
+        PEAKS_SRC = "measured"
+except OSError:
+    pass
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="qwen14b-16k-ext20")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--full-prefill-steps", type=int, default=0,
+                    help="also time full prefill of the same input (every row recomputed)")
+    return ap.parse_args()
+
+
+def workload(name: str) -> synth.Workload:
+    if name in synth.WORKLOADS:
+        return synth.WORKLOADS[name]
+    if name.startswith("sweep:"):
+        _, nc, rho = name.split(":")
+        return synth.sweep_workload(int(nc), int(rho))
+    raise SystemExit(f"unknown workload {name}")
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            p = [x.strip() for x in ln.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                mx.append(float(p[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, p[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- our arm
+class Setup:
+    """Device-resident inputs, weights, handle and outputs for one replica."""
+
+    def __init__(self, wl: synth.Workload, dev: torch.device, max_rows_full: bool):
+        from rag_kv_cache_rope_gb300 import binding as b
+        self.b = b
+        self.wl = wl
+        sh = wl.model
+        self.dev = dev
+        torch.manual_seed(wl.seed)
+        plain = synth.model_weights(sh, wl.seed, device=dev)
+        self.packed = b.pack_weights(plain)
+        del plain
+        torch.cuda.empty_cache()
+        pool_tok, reqs = synth.workload_tokens(wl)
+        assert wl.batch == 1, "bench times one request per step"
+        self.req_tok = reqs[0]
+        lens = [wl.chunk_len] * len(pool_tok.chunks)
+        self.pool_k, self.pool_v, row_off = synth.random_pool_kv(sh, wl.prefix_len, lens, wl.seed, device=dev)
+        tok = torch.cat([torch.cat([pool_tok.prefix, c]) for c in pool_tok.chunks]).to(dev)
+        self.pool = b.PoolRef(self.pool_k, self.pool_v, tok, wl.prefix_len, lens, row_off)
+        self.N = wl.n_ctx
+        self.n_c = wl.n_chunk_rows
+        self.Q = wl.query_len
+        max_rows = self.N if max_rows_full else self.n_c + self.Q
+        self.cfg = b.model_cfg(sh, self.N)
+        self.lim = b.Limits(max_rows, self.N, self.n_c, 1)
+        self.h = b.blend_init(self.cfg, self.packed, self.lim)
+        dt = synth.torch_dtype(sh)
+        L = sh.n_layers
+        self.query = self.req_tok.query.to(dev)
+        self.hidden_states = synth.hidden_states(self.n_c, wl.score_layers, wl.score_dim, wl.seed, device=dev,
+                                                 dtype=dt)
+        self.scores = torch.empty(self.n_c, dtype=torch.float32, device=dev)
+        self.out = b.OutputsRef(
+            k=torch.empty(L, self.N, sh.n_kv_heads, sh.head_dim, dtype=dt, device=dev),
+            v=torch.empty(L, self.N, sh.n_kv_heads, sh.head_dim, dtype=dt, device=dev),
+            hidden=torch.empty(self.Q, sh.hidden, dtype=dt, device=dev),
+            sel=torch.empty(self.n_c, dtype=torch.int32, device=dev),
+            n_sel=torch.zeros(b.MAX_BATCH, dtype=torch.int32, device=dev))
+        self.req = b.RequestRef(self.req_tok.chunk_ids, self.query, mode=wl.mode, rho_bp=wl.rho_bp,
+                                r1_bp=wl.r1_bp, window=wl.window, tau=wl.tau, budget_mode=wl.budget_mode,
+                                scores=self.scores)
+
+    def step(self, req=None):
+        b = self.b
+        b.importance_scores(self.hidden_states, self.n_c, self.wl.score_layers, self.wl.score_dim, self.scores)
+        b.blend_prefill(self.h, [req or self.req], self.pool, self.out)
+
+    def rows_and_pairs(self):
+        """Recomputed rows per layer and sum over them of (position + 1) for the last run."""
+        n = int(self.out["n_sel"][0].item())
+        sel = self.out["sel"][:n].to(torch.int64).cpu()
+        qpos = torch.arange(self.N - self.Q, self.N)
+        pos = torch.cat([sel, qpos])
+        return int(pos.numel()), int((pos + 1).sum().item())
+
+
+def algorithmic(sh: synth.ModelShape, rows: int, pairs: int, wl: synth.Workload) -> dict:
+    """Algorithmic work per launch of each stage (one launch = one layer)."""
+    H, d, F = sh.hidden, sh.head_dim, sh.ffn
+    qd, kvd = sh.n_q_heads * d, sh.n_kv_heads * d
+    es = 2 if sh.dtype == "bf16" else 4
+    asm_bytes = 2 * 2 * sh.n_layers * (wl.prefix_len + wl.n_chunk_rows) * kvd * es
+    return {
+        "gemm_qkv": ("tensor", 2.0 * rows * H * (qd + 2 * kvd)),
+        "gemm_o": ("tensor", 2.0 * rows * qd * H),
+        "gemm_gate_up": ("tensor", 2.0 * rows * H * 2 * F),
+        "gemm_down": ("tensor", 2.0 * rows * F * H),
+        "attention": ("tensor", 4.0 * d * sh.n_q_heads * pairs),
+        "assemble": ("hbm", float(asm_bytes)),
+    }
+
+
+def run_ours(args, wl, rank, world):
+    from rag_kv_cache_rope_gb300 import build as B
+    B.build()
+    from rag_kv_cache_rope_gb300 import binding as b
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    S = Setup(wl, dev, max_rows_full=args.full_prefill_steps > 0)
+    sh = wl.model
+    for _ in range(args.warmup):
+        S.step()
+    torch.cuda.synchronize()
+    rows, pairs = S.rows_and_pairs()
+    # timed region: K steps between barriers, per-stage events recorded live
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    l0 = b.blend_launch_count()
+    b.blend_profile(S.h, True)
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            S.step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    launches = b.blend_launch_count() - l0
+    prof = b.blend_profile_read(S.h)
+    b.blend_profile(S.h, False)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+        torch.distributed.barrier()
+    value = world * S.N / (ms / 1e3)
+
+    # roofline of the stage with the largest share of device time
+    work = algorithmic(sh, rows, pairs, wl)
+    shares = {k: v[0] for k, v in prof.items()}
+    total = sum(shares.values()) or 1.0
+    dom = max(shares, key=shares.get)
+    roof = None
+    if dom in work:
+        kind, units = work[dom]
+        n_launch = args.steps * (sh.n_layers if dom != "assemble" else 1)
+        avg_ms = prof[dom][0] / n_launch
+        if kind == "tensor":
+            peak = PEAKS["bf16_tflops_sustained"] if sh.dtype == "bf16" else None
+            ach = units / (avg_ms / 1e3) / 1e12
+            roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+                    "frac": (ach / peak) if peak else None, "traffic": None,
+                    "peak_source": f"{PEAKS_SRC} bf16 sustained", "avg_launch_ms": avg_ms}
+        else:
+            ach = units / (avg_ms / 1e3) / 1e9
+            roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": PEAKS["hbm_gbs"], "unit": "GB/s",
+                    "frac": ach / PEAKS["hbm_gbs"], "traffic": None, "peak_source": f"{PEAKS_SRC} hbm",
+                    "avg_launch_ms": avg_ms}
+    stages = {k: {"ms_per_step": v[0] / args.steps, "share": v[0] / total, "launches": v[1]}
+              for k, v in prof.items() if v[1]}
+    # whole-step roofline: ideal time of every GEMM/attention at the tensor peak plus the
+    # assembly at the HBM peak, over the measured step
+    tflop = sum(w[1] for k, w in work.items() if w[0] == "tensor") * sh.n_layers
+    ideal_ms = tflop / (PEAKS["bf16_tflops_sustained"] * 1e12) * 1e3 + \
+        work["assemble"][1] / (PEAKS["hbm_gbs"] * 1e9) * 1e3
+    line = {
+        "metric": "blended-prefill context tokens/s (16K ctx, 20% recompute), TTFT ms, % roofline",
+        "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "ttft_ms": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if sh.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded random weights, token ids, chunk-KV pool and small-model hidden states)",
+        "config": {"workload": wl.name, "model_shape": sh.name, "n_ctx": S.N, "prefix": wl.prefix_len,
+                   "chunks": f"{wl.n_chunks}x{wl.chunk_len}", "query": wl.query_len, "mode": wl.mode,
+                   "rho_bp": wl.rho_bp, "window": wl.window, "tau": wl.tau, "budget": wl.budget_mode,
+                   "rows_per_layer": rows, "layers": sh.n_layers, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (weights %.1f GB, chunk pool %.1f GB)" % (
+                       sum(t.numel() * t.element_size() for t in S.packed.values()) / 1e9,
+                       2 * S.pool_k.numel() * S.pool_k.element_size() / 1e9)},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+        "roofline": roof,
+        "step_roofline": {"ideal_ms": ideal_ms, "frac": ideal_ms / ms, "algorithmic_tflop": tflop / 1e12,
+                          "peaks": f"{PEAKS_SRC}: bf16 sustained {PEAKS['bf16_tflops_sustained']} TF/s, "
+                                   f"HBM {PEAKS['hbm_gbs']} GB/s"},
+        "stages": stages,
+        "tensor_cores": bool(b.blend_set_tensor_cores(S.h, True)),
+    }
+    if not args.no_e2e:
+        line["e2e"] = e2e(S, args, world)
+    if args.full_prefill_steps > 0:
+        full = b.RequestRef(S.req_tok.chunk_ids, S.query, mode="full")
+        S.step(full)
+        torch.cuda.synchronize()
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record()
+        for _ in range(args.full_prefill_steps):
+            S.step(full)
+        f1.record()
+        torch.cuda.synchronize()
+        fms = f0.elapsed_time(f1) / args.full_prefill_steps
+        line["full_prefill"] = {"ttft_ms": fms, "tokens_per_s": S.N / (fms / 1e3), "speedup_of_blend": fms / ms}
+    return line, S
+
+
+def e2e(S: Setup, args, world):
+    """Same step through the C ABI with host inputs: pinned H2D of query tokens and the
+    small model's hidden states, D2H of the first-token hidden state, every step."""
+    b = S.b
+    hs_host = S.hidden_states.cpu().pin_memory()
+    q_host = S.query.cpu().pin_memory()
+    out_host = torch.empty_like(S.out["hidden"], device="cpu").pin_memory()
+    h2d = hs_host.numel() * hs_host.element_size() + q_host.numel() * q_host.element_size()
+    d2h = out_host.numel() * out_host.element_size()
+
+    def one():
+        S.hidden_states.copy_(hs_host, non_blocking=True)
+        S.query.copy_(q_host, non_blocking=True)
+        S.step()
+        out_host.copy_(S.out["hidden"], non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(2):
+        one()
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    dt = (time.perf_counter() - t0) / args.steps
+    if world > 1:
+        t = torch.tensor([dt], device=S.dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        dt = float(t.item())
+    return {"value": world * S.N / dt, "unit": "tokens/s", "ttft_ms": dt * 1e3, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h}
+
+
+# ---------------------------------------------------------------- oracle (CPU) arm
+def oracle_sample(wl: synth.Workload, S=None):
+    """Times the CPU oracle on a bounded sample of one step and scales it to the whole
+    step: one layer's assembly (x layers), the full selection, and one layer of the
+    selective recompute on 64 of the recomputed rows spread over the context (x rows/64
+    x layers).  Weights of that layer are the same seeded random weights."""
+    from oracle import blend_oracle as O
+    sh = wl.model
+    one = dataclasses.replace(sh, n_layers=1)
+    cfg = dict(n_layers=1, hidden=sh.hidden, n_q_heads=sh.n_q_heads, n_kv_heads=sh.n_kv_heads,
+               head_dim=sh.head_dim, ffn=sh.ffn, vocab=sh.vocab, rope_theta=sh.rope_theta, rms_eps=sh.rms_eps)
+    w_t = synth.model_weights(one, wl.seed, device="cpu")
+    w = {k: v.double().numpy() for k, v in w_t.items()}
+    del w_t
+    pool_tok, reqs = synth.workload_tokens(wl)
+    lens = [wl.chunk_len] * len(pool_tok.chunks)
+    pk, pv, row_off = synth.random_pool_kv(one, wl.prefix_len, lens, wl.seed)
+    ek = [pk[:, o:o + wl.prefix_len + l].double().numpy() for o, l in zip(row_off, lens)]
+    ev = [pv[:, o:o + wl.prefix_len + l].double().numpy() for o, l in zip(row_off, lens)]
+    hs = synth.hidden_states(wl.n_chunk_rows, wl.score_layers, wl.score_dim, wl.seed)
+    ids = reqs[0].chunk_ids
+    P, n_c, Q = wl.prefix_len, wl.n_chunk_rows, wl.query_len
+    N = P + n_c + Q
+    t0 = time.perf_counter()
+    K, V = O.assemble(ek, ev, ids, P, [lens[c] for c in ids], Q, sh.rope_theta)
+    t_asm = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    s = O.importance_scores(hs.double().numpy()).astype(np.float32).astype(np.float64)
+    sel = O.select_final_bisect(s, O.ceil_bp(wl.rho_bp, n_c), wl.window, wl.tau, base=P)
+    t_sel = time.perf_counter() - t0
+    rows = np.concatenate([sel, np.arange(P + n_c, N)])
+    pick = rows[np.linspace(0, len(rows) - 1, 64).astype(int)]
+    tokens = np.concatenate([reqs[0].prefix.numpy()] + [pool_tok.chunks[c].numpy() for c in ids]
+                            + [reqs[0].query.numpy()])
+    x = w["embed"][tokens[pick]]
+    t0 = time.perf_counter()
+    O.layer_forward(w, cfg, 0, x, pick, K[0], V[0])
+    t_layer = time.perf_counter() - t0
+    est = sh.n_layers * t_asm + t_sel + sh.n_layers * t_layer * len(rows) / len(pick)
+    sample_s = t_asm + t_sel + t_layer
+    return {"est_step_s": est, "sample_s": sample_s, "N": N,
+            "sample": f"1 of {sh.n_layers} layers assembled (x{sh.n_layers}), full selection, one layer's "
+                      f"recompute of 64 of {len(rows)} rows spread over the context (x{len(rows) / 64:.1f} "
+                      f"x{sh.n_layers}); numpy fp64"}
+
+
+def cores():
+    for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(v):
+            return int(os.environ[v])
+    return os.cpu_count()
+
+
+def run_reference(args, wl, rank, world):
+    if rank != 0:
+        return None
+    for _ in range(args.warmup):
+        oracle_sample(wl)
+    ests = []
+    for _ in range(args.steps):
+        ests.append(oracle_sample(wl))
+    est = statistics.median(e["est_step_s"] for e in ests)
+    v = ests[0]["N"] / est
+    return {
+        "impl": "reference",
+        "metric": "blended-prefill context tokens/s (16K ctx, 20% recompute), TTFT ms, % roofline",
+        "value": v, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": est * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic", "config": {"workload": wl.name},
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores(), "kind": "oracle",
+                         "sample": ests[0]["sample"]},
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    wl = workload(args.workload)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, wl, rank, world)
+        if line:
+            print(json.dumps(line), flush=True)
+        return
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    line, S = run_ours(args, wl, rank, world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        del S
+        torch.cuda.empty_cache()
+        cb = oracle_sample(wl)
+        line["cpu_baseline"] = {"value": cb["N"] / cb["est_step_s"], "unit": "tokens/s", "cores": cores(),
+                                "kind": "oracle", "sample": cb["sample"], "sample_seconds": cb["sample_s"]}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

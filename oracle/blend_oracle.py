@@ -116,12 +116,12 @@ def attention(q: np.ndarray, qpos: np.ndarray, K: np.ndarray, V: np.ndarray) -> 
     scale = 1.0 / math.sqrt(d)
     for i in range(n):
         p = int(qpos[i])
-        qi = q[i].reshape(hkv, group, d)                       # head h = g*group + j
-        s = np.einsum("tgd,gjd->gjt", K[:p + 1], qi) * scale     # [hkv, group, p+1]
-        s = s - np.max(s, axis=-1, keepdims=True)
-        e = np.exp(s)
-        a = e / np.sum(e, axis=-1, keepdims=True)
-        out[i] = np.einsum("gjt,tgd->gjd", a, V[:p + 1]).reshape(hq, d)
+        for g in range(hkv):
+            heads = slice(g * group, (g + 1) * group)              # query heads of kv head g
+            s = (q[i, heads, :] @ K[:p + 1, g, :].T) * scale       # [group, p+1]
+            s = s - np.max(s, axis=1, keepdims=True)
+            e = np.exp(s)
+            out[i, heads, :] = (e / np.sum(e, axis=1, keepdims=True)) @ V[:p + 1, g, :]
     return out
 
 

@@ -1,0 +1,338 @@
+"""Thin Python binding of libblend's C ABI (include/blend.h).
+
+Functions carry the C names and only marshal arguments: torch tensors become device
+pointers, Python lists become host arrays, and a non-zero status raises BlendError.
+Every step of the method runs in the library's CUDA kernels.  If libblend.so is
+missing, lib() raises: there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from typing import Optional, Sequence
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libblend.so")
+
+OK, EINVAL, ENOMEM, ECUDA, EMISS, ETIMEOUT, EDEVICE, EUNSUPPORTED = 0, -1, -2, -3, -4, -5, -6, -7
+F32, BF16 = 0, 1
+SEL_EXT, SEL_HKVD, SEL_FORCED, SEL_FULL = 0, 1, 2, 3
+BUDGET_FINAL, BUDGET_CANDIDATE = 0, 1
+DEV_KV, DEV_V = 0, 1
+MAX_BATCH = 64
+GU_BLOCK = 16
+
+MODES = {"ext": SEL_EXT, "hkvd": SEL_HKVD, "forced": SEL_FORCED, "full": SEL_FULL}
+BUDGETS = {"final": BUDGET_FINAL, "candidate": BUDGET_CANDIDATE}
+DEVMODES = {"kv": DEV_KV, "v": DEV_V}
+
+
+class BlendError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"libblend error {code}: {msg}")
+        self.code = code
+
+
+# ---------------------------------------------------------------- C structs
+class ModelCfg(C.Structure):
+    _fields_ = [("n_layers", C.c_int32), ("hidden", C.c_int32), ("n_q_heads", C.c_int32),
+                ("n_kv_heads", C.c_int32), ("head_dim", C.c_int32), ("ffn", C.c_int32),
+                ("vocab", C.c_int32), ("dtype", C.c_int32), ("rope_theta", C.c_double),
+                ("rms_eps", C.c_float), ("max_pos", C.c_int32)]
+
+
+class Weights(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in ("embed", "attn_norm", "w_qkv", "w_o", "mlp_norm", "w_gu",
+                                          "w_down", "final_norm")]
+
+
+class Limits(C.Structure):
+    _fields_ = [("max_rows", C.c_int32), ("max_tokens", C.c_int32), ("max_chunk_rows", C.c_int32),
+                ("max_batch", C.c_int32)]
+
+
+class Pool(C.Structure):
+    _fields_ = [("n_entries", C.c_int32), ("prefix_len", C.c_int32),
+                ("entry_len", C.POINTER(C.c_int32)), ("entry_row", C.POINTER(C.c_int64)),
+                ("present", C.POINTER(C.c_uint8)), ("n_rows", C.c_int64), ("k", C.c_void_p),
+                ("v", C.c_void_p), ("tokens", C.c_void_p)]
+
+
+class Request(C.Structure):
+    _fields_ = [("n_chunks", C.c_int32), ("chunk_ids", C.POINTER(C.c_int32)),
+                ("query_len", C.c_int32), ("query_tokens", C.c_void_p), ("mode", C.c_int32),
+                ("rho_bp", C.c_int32), ("r1_bp", C.c_int32), ("window", C.c_int32),
+                ("tau", C.c_int32), ("budget_mode", C.c_int32), ("dev_mode", C.c_int32),
+                ("scores", C.c_void_p), ("n_stages", C.c_int32), ("stage_layer", C.c_int32 * 3),
+                ("stage_pos", C.c_void_p * 3), ("stage_n", C.c_int32 * 3)]
+
+
+class Outputs(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in ("k", "v", "hidden", "sel", "n_sel", "c1", "n_c1", "dev1",
+                                          "dev2")]
+
+
+_lib = None
+
+
+def lib() -> C.CDLL:
+    """Loads libblend.so (built by build.build()); raises if it is not there."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "rag_kv_cache_rope_gb300.build.build() (needs nvcc)")
+        L = C.CDLL(LIB_PATH)
+        vp, i32, i64 = C.c_void_p, C.c_int32, C.c_int64
+        sig = {
+            "blend_workspace_size": (C.c_size_t, [C.POINTER(ModelCfg), C.POINTER(Limits)]),
+            "blend_init": (C.c_int, [C.POINTER(ModelCfg), C.POINTER(Weights), C.POINTER(Limits), vp,
+                                     C.c_size_t, vp, C.POINTER(vp)]),
+            "blend_destroy": (C.c_int, [vp]),
+            "blend_last_error": (C.c_char_p, [vp]),
+            "blend_device_status": (C.c_int, [vp, vp]),
+            "blend_set_tensor_cores": (C.c_int, [vp, C.c_int]),
+            "rope_realign": (C.c_int, [vp, vp, vp, i32, vp, i32, i64, i64, vp]),
+            "blend_assemble": (C.c_int, [vp, i32, C.POINTER(Request), C.POINTER(Pool),
+                                         C.POINTER(Outputs), vp]),
+            "kv_deviation": (C.c_int, [vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, vp]),
+            "topk_select_dilate": (C.c_int, [vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp]),
+            "gather_rows": (C.c_int, [vp, i64, vp, vp, i32, vp, vp]),
+            "scatter_kv": (C.c_int, [vp, vp, vp, vp, vp, i32, vp, vp, vp]),
+            "selective_layer": (C.c_int, [vp, i32, vp, vp, i32, vp, vp, i32, vp, i32, vp]),
+            "blend_prefill": (C.c_int, [vp, i32, C.POINTER(Request), C.POINTER(Pool),
+                                        C.POINTER(Outputs), vp]),
+            "importance_scores": (C.c_int, [vp, i32, i32, i32, i32, vp, vp]),
+            "blend_profile": (C.c_int, [vp, C.c_int]),
+            "blend_profile_read": (C.c_int, [vp, C.POINTER(C.c_double), C.POINTER(C.c_int64), i32]),
+            "blend_profile_name": (C.c_char_p, [i32]),
+            "blend_launch_count": (C.c_int64, []),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+EXPORTED = ("blend_workspace_size", "blend_init", "blend_destroy", "blend_last_error",
+            "blend_device_status", "blend_set_tensor_cores", "rope_realign", "blend_assemble",
+            "kv_deviation", "topk_select_dilate", "gather_rows", "scatter_kv", "selective_layer",
+            "blend_prefill", "importance_scores", "blend_profile", "blend_profile_read",
+            "blend_profile_name", "blend_launch_count")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    return C.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(stream.cuda_stream)
+
+
+def _check(rc: int, h=None):
+    if rc != OK:
+        msg = lib().blend_last_error(h.ptr if h is not None else None)
+        raise BlendError(rc, msg.decode() if msg else "")
+    return rc
+
+
+# ---------------------------------------------------------------- handle
+class Handle:
+    """A libblend handle plus the tensors it points into (kept alive here)."""
+
+    def __init__(self, ptr, cfg: ModelCfg, lim: Limits, keep):
+        self.ptr = ptr
+        self.cfg = cfg
+        self.lim = lim
+        self._keep = keep
+
+    def __del__(self):
+        if getattr(self, "ptr", None) and _lib is not None:
+            _lib.blend_destroy(self.ptr)
+            self.ptr = None
+
+
+def model_cfg(shape, max_pos: int) -> ModelCfg:
+    return ModelCfg(shape.n_layers, shape.hidden, shape.n_q_heads, shape.n_kv_heads, shape.head_dim,
+                    shape.ffn, shape.vocab, F32 if shape.dtype == "f32" else BF16,
+                    float(shape.rope_theta), float(shape.rms_eps), int(max_pos))
+
+
+def blend_workspace_size(cfg: ModelCfg, lim: Limits) -> int:
+    return int(lib().blend_workspace_size(C.byref(cfg), C.byref(lim)))
+
+
+def blend_init(cfg: ModelCfg, packed: dict, lim: Limits, workspace: Optional[torch.Tensor] = None,
+               stream=None) -> Handle:
+    need = blend_workspace_size(cfg, lim)
+    if need == 0:
+        raise BlendError(EINVAL, "bad model configuration or limits")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=packed["embed"].device)
+    w = Weights(*[packed[k].data_ptr() for k in ("embed", "attn_norm", "w_qkv", "w_o", "mlp_norm",
+                                                  "w_gu", "w_down", "final_norm")])
+    out = C.c_void_p()
+    rc = lib().blend_init(C.byref(cfg), C.byref(w), C.byref(lim), _ptr(workspace), workspace.numel(),
+                          _stream(stream), C.byref(out))
+    _check(rc)
+    return Handle(out, cfg, lim, (packed, workspace))
+
+
+def blend_destroy(h: Handle):
+    if h.ptr:
+        _check(lib().blend_destroy(h.ptr))
+        h.ptr = None
+
+
+def blend_device_status(h: Handle, stream=None) -> int:
+    return _check(lib().blend_device_status(h.ptr, _stream(stream)), h)
+
+
+def blend_set_tensor_cores(h: Handle, on: bool) -> int:
+    return int(lib().blend_set_tensor_cores(h.ptr, 1 if on else 0))
+
+
+def blend_profile(h: Handle, enable: bool):
+    _check(lib().blend_profile(h.ptr, 1 if enable else 0), h)
+
+
+def blend_profile_read(h: Handle) -> dict:
+    """{stage: (total ms, kernel launches)} since blend_profile(h, True)."""
+    n = 32
+    ms = (C.c_double * n)()
+    cnt = (C.c_int64 * n)()
+    k = lib().blend_profile_read(h.ptr, ms, cnt, n)
+    if k < 0:
+        _check(k, h)
+    return {lib().blend_profile_name(i).decode(): (ms[i], int(cnt[i])) for i in range(k)}
+
+
+def blend_launch_count() -> int:
+    return int(lib().blend_launch_count())
+
+
+def rope_realign(h, k_src, k_dst, n_rows, delta, n_layers, src_layer_rows, dst_layer_rows, stream=None):
+    _check(lib().rope_realign(h.ptr, _ptr(k_src), _ptr(k_dst), n_rows, _ptr(delta), n_layers,
+                              src_layer_rows, dst_layer_rows, _stream(stream)), h)
+
+
+def kv_deviation(h, k_new, v_new, k_cache, v_cache, pos, n_rows, max_rows, mode, dev_out, stream=None):
+    _check(lib().kv_deviation(h.ptr, _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(pos),
+                              _ptr(n_rows), max_rows, mode, _ptr(dev_out), _stream(stream)), h)
+
+
+def topk_select_dilate(h, scores, n, base, budget, window, tau, budget_mode, allowed, idx_out, n_out,
+                       stream=None):
+    _check(lib().topk_select_dilate(h.ptr, _ptr(scores), n, base, budget, window, tau, budget_mode,
+                                    _ptr(allowed), _ptr(idx_out), _ptr(n_out), _stream(stream)), h)
+
+
+def gather_rows(src, row_bytes, idx, n, max_n, dst, stream=None):
+    _check(lib().gather_rows(_ptr(src), row_bytes, _ptr(idx), _ptr(n), max_n, _ptr(dst), _stream(stream)))
+
+
+def scatter_kv(h, k_new, v_new, pos, n, max_n, k_cache, v_cache, stream=None):
+    _check(lib().scatter_kv(h.ptr, _ptr(k_new), _ptr(v_new), _ptr(pos), _ptr(n), max_n, _ptr(k_cache),
+                            _ptr(v_cache), _stream(stream)), h)
+
+
+def selective_layer(h, layer, x, pos, n, k_cache, v_cache, n_ctx, dev_out=None, dev_mode=DEV_KV,
+                    stream=None):
+    _check(lib().selective_layer(h.ptr, layer, _ptr(x), _ptr(pos), n, _ptr(k_cache), _ptr(v_cache),
+                                 n_ctx, _ptr(dev_out), dev_mode, _stream(stream)), h)
+
+
+def importance_scores(hidden, n, n_layers, dim, out, stream=None):
+    dt = BF16 if hidden.dtype == torch.bfloat16 else F32
+    _check(lib().importance_scores(_ptr(hidden), n, n_layers, dim, dt, _ptr(out), _stream(stream)))
+
+
+# ---------------------------------------------------------------- pool / requests / outputs
+class PoolRef:
+    """Host-side description of a device chunk-KV pool (see blend_pool)."""
+
+    def __init__(self, k, v, tokens, prefix_len, entry_len, entry_row, present=None):
+        self.k, self.v, self.tokens = k, v, tokens
+        self._len = (C.c_int32 * len(entry_len))(*entry_len)
+        self._row = (C.c_int64 * len(entry_row))(*entry_row)
+        self._present = None if present is None else (C.c_uint8 * len(present))(*present)
+        self.c = Pool(len(entry_len), prefix_len, self._len, self._row, self._present, k.shape[1],
+                      k.data_ptr(), v.data_ptr(), tokens.data_ptr())
+        self.entry_len = list(entry_len)
+        self.prefix_len = prefix_len
+
+
+class RequestRef:
+    def __init__(self, chunk_ids: Sequence[int], query_tokens: torch.Tensor, mode: str = "ext",
+                 rho_bp: int = 0, r1_bp: int = 0, window: int = 1, tau: int = 1,
+                 budget_mode: str = "final", dev_mode: str = "kv", scores: Optional[torch.Tensor] = None,
+                 stages: Optional[list] = None):
+        self.chunk_ids = list(chunk_ids)
+        self._ids = (C.c_int32 * len(self.chunk_ids))(*self.chunk_ids)
+        self.query = query_tokens
+        self.scores = scores
+        self.stages = stages or []
+        st_layer = (C.c_int32 * 3)(*([int(f) for f, _ in self.stages] + [0] * (3 - len(self.stages))))
+        st_pos = (C.c_void_p * 3)(*([p.data_ptr() if p.numel() else None for _, p in self.stages]
+                                     + [None] * (3 - len(self.stages))))
+        st_n = (C.c_int32 * 3)(*([int(p.numel()) for _, p in self.stages] + [0] * (3 - len(self.stages))))
+        self.c = Request(len(self.chunk_ids), self._ids, int(query_tokens.numel()), query_tokens.data_ptr(),
+                         MODES[mode], rho_bp, r1_bp, window, tau, BUDGETS[budget_mode], DEVMODES[dev_mode],
+                         scores.data_ptr() if scores is not None else None, len(self.stages), st_layer,
+                         st_pos, st_n)
+
+
+class OutputsRef:
+    def __init__(self, k, v, hidden, sel=None, n_sel=None, c1=None, n_c1=None, dev1=None, dev2=None):
+        self.t = dict(k=k, v=v, hidden=hidden, sel=sel, n_sel=n_sel, c1=c1, n_c1=n_c1, dev1=dev1, dev2=dev2)
+        self.c = Outputs(*[None if self.t[n] is None else self.t[n].data_ptr()
+                           for n in ("k", "v", "hidden", "sel", "n_sel", "c1", "n_c1", "dev1", "dev2")])
+
+    def __getitem__(self, k):
+        return self.t[k]
+
+
+def _req_array(reqs):
+    arr = (Request * len(reqs))()
+    for i, r in enumerate(reqs):
+        arr[i] = r.c
+    return arr
+
+
+def blend_assemble(h, reqs: Sequence[RequestRef], pool: PoolRef, out: OutputsRef, stream=None):
+    _check(lib().blend_assemble(h.ptr, len(reqs), _req_array(reqs), C.byref(pool.c), C.byref(out.c),
+                                _stream(stream)), h)
+
+
+def blend_prefill(h, reqs: Sequence[RequestRef], pool: PoolRef, out: OutputsRef, stream=None):
+    _check(lib().blend_prefill(h.ptr, len(reqs), _req_array(reqs), C.byref(pool.c), C.byref(out.c),
+                               _stream(stream)), h)
+
+
+# ---------------------------------------------------------------- weight layout
+def pack_weights(w: dict, device=None) -> dict:
+    """Plain per-layer weights (synth.model_weights layout) -> the layout blend_weights
+    documents: fused [q; k; v] rows, gate/up rows interleaved in blocks of GU_BLOCK."""
+    dev = device or w["embed"].device
+    wq, wk, wv = w["wq"], w["wk"], w["wv"]
+    L, F, H = w["wg"].shape
+    gu = torch.stack([w["wg"].reshape(L, F // GU_BLOCK, GU_BLOCK, H),
+                      w["wu"].reshape(L, F // GU_BLOCK, GU_BLOCK, H)], dim=2).reshape(L, 2 * F, H)
+    return {
+        "embed": w["embed"].to(dev).contiguous(),
+        "attn_norm": w["attn_norm"].to(dev).contiguous(),
+        "w_qkv": torch.cat([wq, wk, wv], dim=1).to(dev).contiguous(),
+        "w_o": w["wo"].to(dev).contiguous(),
+        "mlp_norm": w["mlp_norm"].to(dev).contiguous(),
+        "w_gu": gu.to(dev).contiguous(),
+        "w_down": w["wd"].to(dev).contiguous(),
+        "final_norm": w["final_norm"].to(dev).contiguous(),
+    }

@@ -1,0 +1,189 @@
+// Shared device helpers and internal launch interfaces of libblend.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/blend.h"
+
+namespace blend {
+
+using bf16 = __nv_bfloat16;
+
+template <typename T> __device__ __forceinline__ float to_f(T x);
+template <> __device__ __forceinline__ float to_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ float to_f<bf16>(bf16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f(float x);
+template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ bf16 from_f<bf16>(float x) { return __float2bfloat16_rn(x); }
+
+// 16-byte vector of T: 4 floats or 8 bf16.
+template <typename T> struct Vec {
+    static constexpr int N = 16 / sizeof(T);
+    uint4 raw;
+    __device__ __forceinline__ float get(int i) const {
+        const T* p = reinterpret_cast<const T*>(&raw);
+        return to_f<T>(p[i]);
+    }
+    __device__ __forceinline__ void set(int i, float v) {
+        T* p = reinterpret_cast<T*>(&raw);
+        p[i] = from_f<T>(v);
+    }
+};
+
+template <typename T> __device__ __forceinline__ Vec<T> ld16(const T* p) {
+    Vec<T> v;
+    v.raw = *reinterpret_cast<const uint4*>(p);
+    return v;
+}
+template <typename T> __device__ __forceinline__ void st16(T* p, const Vec<T>& v) {
+    *reinterpret_cast<uint4*>(p) = v.raw;
+}
+
+// Counts kernel launches made by the library (process-wide; read by blend_launch_count).
+void note_launch(int n = 1);
+
+// Records the first device-side failure (code, where) in the handle's error word.
+__device__ __forceinline__ void set_error(int32_t* err, int32_t code) {
+    if (err) atomicCAS(err, 0, code);
+}
+
+// Deterministic block-wide sum (fixed tree order) of one float per thread.
+// `red` must hold blockDim.x floats; blockDim.x a power of two <= 1024.
+__device__ __forceinline__ float block_sum(float v, float* red) {
+    const int t = threadIdx.x;
+    red[t] = v;
+    __syncthreads();
+    for (int s = blockDim.x >> 1; s > 0; s >>= 1) {
+        if (t < s) red[t] += red[t + s];
+        __syncthreads();
+    }
+    float r = red[0];
+    __syncthreads();
+    return r;
+}
+
+// Per-request description of a batch, passed to kernels by value.
+struct ReqDesc {
+    int32_t tok_off;  // first blended token of the request in the batch K/V
+    int32_t P;        // prefix rows
+    int32_t n_c;      // chunk rows
+    int32_t Q;        // query rows
+    int32_t nc_off;   // first chunk row of the request in per-chunk-row arrays
+    int32_t q_off;    // first query row of the request in the hidden output
+};
+struct BatchDesc {
+    int32_t n_req;
+    ReqDesc r[BLEND_MAX_BATCH];
+};
+
+// Assembly segment: n_rows pool rows from src_row go to blended tokens dst_tok..,
+// keys rotated by delta positions.
+struct Seg {
+    int32_t row0;     // first linear row of this segment (sum of earlier n_rows)
+    int32_t src_row;
+    int32_t dst_tok;
+    int32_t n_rows;
+    int32_t delta;
+};
+struct SegTable {
+    int32_t n_seg;
+    int32_t total_rows;
+    Seg s[BLEND_MAX_CHUNKS + BLEND_MAX_BATCH];
+};
+struct QueryTable {
+    int32_t n;
+    const int32_t* ptr[BLEND_MAX_BATCH];
+    int32_t dst_tok[BLEND_MAX_BATCH];
+    int32_t len[BLEND_MAX_BATCH];
+};
+
+// Stage set of every request: positions at set + nc_off[r], count at count[r];
+// iota 1: the set is every chunk row P..P+n_c-1; iota 2: every row 0..P+n_c-1.
+struct StageDesc {
+    const int32_t* set;
+    const int32_t* count;
+    int32_t iota;
+};
+
+// ------------------------------ launchers (kernels_mem.cu) -------------------------
+// dev_out of launch_rope_qkv: per chunk row of each request (dev_by_row = 0, indexed
+// nc_off + pos - P, other rows skipped) or per recomputed row (dev_by_row = 1).
+void launch_rope_table(float2* tab, int max_pos, int head_dim, double theta, cudaStream_t s);
+void launch_realign(int dtype, const void* src, void* dst, int n_rows, const int32_t* delta,
+                    int n_layers, long long src_layer_rows, long long dst_layer_rows, int hkv, int d,
+                    const float2* tab, int max_pos, int32_t* err, cudaStream_t s);
+void launch_assemble(int dtype, const SegTable& segs, const void* pool_k, const void* pool_v,
+                     long long pool_rows, void* out_k, void* out_v, long long out_tokens,
+                     int n_layers, int hkv, int d, const float2* tab, int max_pos, int32_t* err,
+                     cudaStream_t s);
+void launch_tokens(const SegTable& segs, const QueryTable& qt, const int32_t* pool_tokens,
+                   int32_t* out_tokens, cudaStream_t s);
+void launch_rmsnorm(int dtype, const float* x, const void* g, void* out, int H, float eps,
+                    const int32_t* M_dev, int M_max, cudaStream_t s);
+void launch_embed(int dtype, const void* embed, const int32_t* tokens, const int32_t* row_tok,
+                  float* x, int H, int vocab, const int32_t* M_dev, int M_max, int32_t* err,
+                  cudaStream_t s);
+void launch_gather(const void* src, long long row_bytes, const int32_t* idx, const int32_t* n_dev,
+                   int max_n, void* dst, cudaStream_t s);
+void launch_rope_qkv(int dtype, const float* qkv, const int32_t* row_pos, const int32_t* row_tok,
+                     const int32_t* row_req, const int32_t* M_dev, int M_max, const BatchDesc& bd,
+                     int hq, int hkv, int d, const float2* tab, void* q_out, void* k_cache,
+                     void* v_cache, float* dev_out, int dev_mode, int dev_by_row, cudaStream_t s);
+void launch_deviation(int dtype, const void* k_new, const void* v_new, const void* k_cache,
+                      const void* v_cache, const int32_t* pos, const int32_t* n_dev, int max_rows,
+                      int kv_elems, int mode, float* dev_out, cudaStream_t s);
+void launch_scatter(int dtype, const void* k_new, const void* v_new, const int32_t* pos,
+                    const int32_t* n_dev, int max_n, int kv_elems, void* k_cache, void* v_cache,
+                    cudaStream_t s);
+void launch_final_norm(int dtype, const float* x, const void* g, void* hidden, int H, float eps,
+                       const BatchDesc& bd, const int32_t* req_row_end, cudaStream_t s);
+void launch_importance(int dtype, const void* hidden, int n, int n_layers, int dim, float* out,
+                       cudaStream_t s);
+// With old_row_tok/old_M (the previous plan) set, row_src receives each new row's row in
+// the previous plan; positions missing from the previous plan are reported in err.
+void launch_plan(const BatchDesc& bd, const StageDesc& st, int32_t* row_pos, int32_t* row_tok,
+                 int32_t* row_req, int32_t* row_src, int32_t* pos2row, int32_t* M_dev,
+                 int32_t* req_row_end, const int32_t* old_row_tok, const int32_t* old_M, int32_t* err,
+                 cudaStream_t s);
+void launch_set_mask(const BatchDesc& bd, const int32_t* set, const int32_t* count, uint8_t* mask,
+                     cudaStream_t s);
+void launch_fill_i32(int32_t* p, int32_t v, long long n, cudaStream_t s);
+void launch_copy_sets(const BatchDesc& bd, const int32_t* src, const int32_t* src_n, int32_t* dst,
+                      int32_t* dst_n, cudaStream_t s);
+
+// ------------------------------ selection (select.cu) ------------------------------
+struct SelectJob {
+    const float* scores;   // [n]
+    const uint8_t* allowed;  // [n] or null
+    int32_t* out;          // [n]
+    int32_t* out_n;        // scalar
+    int32_t n;
+    int32_t base;
+    int32_t budget;
+    int32_t rank_off;      // offset of this job's rank scratch
+};
+struct SelectBatch {
+    int32_t n_job;
+    int32_t window, tau, budget_mode;
+    SelectJob j[BLEND_MAX_BATCH];
+};
+void launch_select(const SelectBatch& sb, int32_t* rank_scratch, int max_n, cudaStream_t s);
+
+// ------------------------------ GEMM (gemm_simt.cu) --------------------------------
+enum Epi { EPI_STORE_F32 = 0, EPI_ADD_F32 = 1, EPI_SWIGLU = 2 };
+// C = A[M,K] . B[N,K]^T with A, B of the model dtype; epilogue:
+//   EPI_STORE_F32: C fp32 [M][ldc] = acc
+//   EPI_ADD_F32:   C fp32 [M][ldc] += acc
+//   EPI_SWIGLU:    C dtype [M][N/2]: gate/up interleaved in blocks of BLEND_GU_BLOCK
+void launch_gemm_simt(int dtype, const void* A, int lda, const void* B, int ldb, int K, int N,
+                      const int32_t* M_dev, int M_max, int epi, void* C, int ldc, cudaStream_t s);
+
+// ------------------------------ attention (attn_simt.cu) ---------------------------
+void launch_attn_simt(int dtype, const void* q, const int32_t* row_pos, const int32_t* row_tok,
+                      const int32_t* M_dev, int M_max, const void* k_cache, const void* v_cache,
+                      void* o, int hq, int hkv, int d, cudaStream_t s);
+
+}  // namespace blend

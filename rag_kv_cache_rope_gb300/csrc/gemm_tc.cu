@@ -1,0 +1,376 @@
+// Tensor-core GEMM for the gathered-row projections: C = A . B^T, A [M][K] bf16
+// (recomputed rows), B [N][K] bf16 (weights, nn.Linear layout), fp32 accumulation in
+// TMEM, fused epilogues (fp32 store, fp32 residual add, SwiGLU).
+//
+// Persistent kernel, one CTA per SM, 6 warps:
+//   warp 0      TMA producer: 128x64 A tile + 256x64 B tile per stage (128-byte swizzle)
+//   warp 1      TMEM allocator and MMA issuer: tcgen05.mma kind::f16, M=128 N=256 K=16,
+//               4 per stage; tcgen05.commit frees the stage / publishes the accumulator
+//   warps 2..5  epilogue: tcgen05.ld of their 32 TMEM lanes (one output row per thread)
+// Two 256-column fp32 accumulators (all 512 TMEM columns) let the epilogue of one tile
+// overlap the main loop of the next.  M is read from the device; tiles past it are
+// skipped.  Every mbarrier wait is bounded: on expiry the kernel records
+// BLEND_ETIMEOUT in the error word, stops issuing work, drains its own copies and
+// frees TMEM before returning.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "gemm_tc.cuh"
+
+namespace blend {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+constexpr int B_BYTES = BN * BK * 2;  // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int TMEM_COLS = 2 * BN;
+constexpr int THREADS = 192;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;  // + alignment slack
+constexpr long long SPIN_LIMIT = 1ll << 24;
+
+__device__ __forceinline__ uint32_t su32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t* b, int count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(su32(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait for the phase of parity `parity`; false if it did not complete in time
+// or another role gave up.
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort_flag) {
+    for (long long i = 0; i < SPIN_LIMIT; ++i) {
+        if (mbar_try(b, parity)) return true;
+        if ((i & 255) == 255 && *abort_flag) return false;
+    }
+    return false;
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0,
+                                            int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(su32(dst)),
+        "l"((uint64_t)map), "r"(su32(bar)), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major tile stored with the 128-byte swizzle
+// (rows of 64 bf16 = 128 bytes, 8-row groups 1024 bytes apart).
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFF) >> 4);  // start address
+    d |= (uint64_t)1 << 16;                   // leading byte offset (unused with swizzle)
+    d |= (uint64_t)(1024 >> 4) << 32;         // stride byte offset: 8 rows x 128 B
+    d |= (uint64_t)1 << 46;                   // descriptor version for tcgen05
+    d |= (uint64_t)2 << 61;                   // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor, kind::f16: bf16 A and B (K-major), fp32 D, M=128, N=256.
+constexpr uint32_t IDESC = (1u << 4)            // D format f32
+                           | (1u << 7)          // A format bf16
+                           | (1u << 10)         // B format bf16
+                           | ((BN >> 3) << 17)  // N / 8
+                           | ((BM >> 4) << 24); // M / 16
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(IDESC), "r"(acc)
+        : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     su32(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+#define TMEM_LD32(taddr, r)                                                                        \
+    asm volatile(                                                                                  \
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14," \
+        "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"           \
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),   \
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), \
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),           \
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),           \
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])            \
+        : "r"(taddr))
+
+template <int EPI>
+__global__ void __launch_bounds__(THREADS, 1)
+    k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB, int K,
+              int N, const int32_t* __restrict__ M_dev, void* __restrict__ Cv, int ldc,
+              int32_t* __restrict__ err) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2];
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ volatile int abort_flag;
+    __shared__ int pending[STAGES];  // parity a stage's last issued load completes with, or -1
+
+    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int M = *M_dev;
+    const int m_tiles = (M + BM - 1) / BM, n_tiles = N / BN;
+    const int n_total = m_tiles * n_tiles;
+    const int kblocks = K / BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+            pending[s] = -1;
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 4 * 32);
+        }
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         su32(&tmem_base_sh)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = tmem_base_sh;
+
+    if (warp == 0 && lane == 0) {
+        // ---------------- TMA producer
+        int s = 0;
+        uint32_t ph = 0;
+        for (int t = blockIdx.x; t < n_total && !abort_flag; t += gridDim.x) {
+            const int mt = t % m_tiles, nt = t / m_tiles;
+            for (int kb = 0; kb < kblocks; ++kb) {
+                if (!mbar_wait(&empty[s], ph ^ 1, &abort_flag)) {
+                    abort_flag = 1;
+                    set_error(err, BLEND_ETIMEOUT);
+                    break;
+                }
+                uint8_t* st = smem + s * STAGE_BYTES;
+                mbar_expect_tx(&full[s], STAGE_BYTES);
+                pending[s] = (int)ph;
+                tma_load_2d(st, &mapA, &full[s], kb * BK, mt * BM);
+                tma_load_2d(st + A_BYTES, &mapB, &full[s], kb * BK, nt * BN);
+                if (++s == STAGES) {
+                    s = 0;
+                    ph ^= 1;
+                }
+            }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---------------- MMA issuer
+        int s = 0, b = 0;
+        uint32_t ph = 0, tph = 0;
+        for (int t = blockIdx.x; t < n_total && !abort_flag; t += gridDim.x) {
+            if (!mbar_wait(&tempty[b], tph ^ 1, &abort_flag)) {
+                abort_flag = 1;
+                set_error(err, BLEND_ETIMEOUT);
+                break;
+            }
+            tc_fence_after();
+            const uint32_t d = tbase + (uint32_t)(b * BN);
+            for (int kb = 0; kb < kblocks; ++kb) {
+                if (!mbar_wait(&full[s], ph, &abort_flag)) {
+                    abort_flag = 1;
+                    set_error(err, BLEND_ETIMEOUT);
+                    break;
+                }
+                tc_fence_after();
+                pending[s] = -1;
+                const uint32_t a_addr = su32(smem + s * STAGE_BYTES);
+                const uint32_t b_addr = a_addr + A_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk)
+                    umma_bf16(d, sdesc_sw128(a_addr + kk * 32), sdesc_sw128(b_addr + kk * 32),
+                              (kb | kk) != 0);
+                umma_commit(&empty[s]);
+                if (++s == STAGES) {
+                    s = 0;
+                    ph ^= 1;
+                }
+            }
+            umma_commit(&tfull[b]);
+            b ^= 1;
+            if (b == 0) tph ^= 1;
+        }
+    } else if (warp >= 2) {
+        // ---------------- epilogue: thread = one row of the 128-row tile
+        const int sp = warp & 3;  // TMEM lane quarter this warp may access
+        const int r_in = sp * 32 + lane;
+        int b = 0;
+        uint32_t tph = 0;
+        for (int t = blockIdx.x; t < n_total; t += gridDim.x) {
+            const int mt = t % m_tiles, nt = t / m_tiles;
+            // every lane waits; the warp continues only if all saw the accumulator
+            // (tcgen05.ld below is .sync.aligned and must not run in a diverged warp)
+            const bool ok = __all_sync(0xffffffffu, mbar_wait(&tfull[b], tph, &abort_flag));
+            if (!ok) {
+                abort_flag = 1;
+                if (lane == 0) set_error(err, BLEND_ETIMEOUT);
+                break;
+            }
+            tc_fence_after();
+            const int row = mt * BM + r_in;
+            const uint32_t tl = tbase + ((uint32_t)(sp * 32) << 16) + (uint32_t)(b * BN);
+#pragma unroll 1
+            for (int c = 0; c < BN; c += 32) {
+                uint32_t r[32];
+                TMEM_LD32(tl + c, r);
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                if (row < M) {
+                    const int col = nt * BN + c;
+                    if (EPI == EPI_STORE_F32 || EPI == EPI_ADD_F32) {
+                        float4* p = reinterpret_cast<float4*>((float*)Cv + (long long)row * ldc + col);
+#pragma unroll
+                        for (int v = 0; v < 8; ++v) {
+                            float4 o = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                                   __uint_as_float(r[4 * v + 2]),
+                                                   __uint_as_float(r[4 * v + 3]));
+                            if (EPI == EPI_ADD_F32) {
+                                float4 x = p[v];
+                                o.x += x.x;
+                                o.y += x.y;
+                                o.z += x.z;
+                                o.w += x.w;
+                            }
+                            p[v] = o;
+                        }
+                    } else {
+                        // 32 columns = 16 gate + 16 up of the same hidden units
+                        __align__(16) bf16 h[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float g = __uint_as_float(r[i]), u = __uint_as_float(r[16 + i]);
+                            h[i] = __float2bfloat16_rn(g / (1.f + expf(-g)) * u);
+                        }
+                        uint4* p = reinterpret_cast<uint4*>((bf16*)Cv + (long long)row * ldc + col / 2);
+                        p[0] = reinterpret_cast<const uint4*>(h)[0];
+                        p[1] = reinterpret_cast<const uint4*>(h)[1];
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&tempty[b]);
+            b ^= 1;
+            if (b == 0) tph ^= 1;
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && abort_flag) {
+        // drain loads still in flight so no copy lands in shared memory after exit
+        for (int s = 0; s < STAGES; ++s)
+            if (pending[s] >= 0) {
+                for (long long i = 0; i < SPIN_LIMIT && !mbar_try(&full[s], (uint32_t)pending[s]); ++i) {
+                }
+            }
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(TMEM_COLS)
+                     : "memory");
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+int g_tc_state = -1;  // -1 unknown, 0 unavailable, 1 available
+int g_num_sms = 0;
+
+bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+               uint32_t box_outer) {
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * 2};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                          box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+int tc_available() {
+    if (g_tc_state >= 0) return g_tc_state;
+    g_tc_state = 0;
+    int dev = 0;
+    cudaDeviceProp prop;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaGetDeviceProperties(&prop, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    if (!(prop.major == 10 && prop.minor == 3)) return 0;  // built for sm_103a only
+    g_num_sms = prop.multiProcessorCount;
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn) {
+        cudaGetLastError();
+        return 0;
+    }
+    g_encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+    cudaFuncSetAttribute(k_gemm_tc<EPI_STORE_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    cudaFuncSetAttribute(k_gemm_tc<EPI_ADD_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    cudaFuncSetAttribute(k_gemm_tc<EPI_SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    g_tc_state = 1;
+    return 1;
+}
+
+bool tc_gemm_supported(int K, int N, int epi, int ldc, int M_cap) {
+    (void)epi;
+    return K >= BK && K % BK == 0 && N >= BN && N % BN == 0 && ldc % 8 == 0 && M_cap >= BM;
+}
+
+int launch_gemm_tc(const void* A, int K, int M_cap, const void* B, int N, const int32_t* M_dev, int M_max,
+                   int epi, void* C, int ldc, int32_t* err, cudaStream_t s) {
+    if (M_max <= 0) return BLEND_OK;
+    CUtensorMap ma, mb;
+    if (!encode_2d(&ma, A, (uint64_t)K, (uint64_t)M_cap, BK, BM) ||
+        !encode_2d(&mb, B, (uint64_t)K, (uint64_t)N, BK, BN))
+        return BLEND_EUNSUPPORTED;  // the operands cannot be described to the TMA unit
+    const int tiles = ((M_max + BM - 1) / BM) * (N / BN);
+    const int grid = tiles < g_num_sms ? tiles : g_num_sms;
+    if (epi == EPI_STORE_F32)
+        k_gemm_tc<EPI_STORE_F32><<<grid, THREADS, SMEM_BYTES, s>>>(ma, mb, K, N, M_dev, C, ldc, err);
+    else if (epi == EPI_ADD_F32)
+        k_gemm_tc<EPI_ADD_F32><<<grid, THREADS, SMEM_BYTES, s>>>(ma, mb, K, N, M_dev, C, ldc, err);
+    else
+        k_gemm_tc<EPI_SWIGLU><<<grid, THREADS, SMEM_BYTES, s>>>(ma, mb, K, N, M_dev, C, ldc, err);
+    note_launch(1);
+    return BLEND_OK;
+}
+
+}  // namespace blend

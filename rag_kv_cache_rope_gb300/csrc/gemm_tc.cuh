@@ -1,0 +1,17 @@
+// Tensor-core (tcgen05) GEMM interface: C = A[M,K] . B[N,K]^T in bf16 with fp32
+// accumulation and the epilogues of Epi (common.cuh).
+#pragma once
+#include "common.cuh"
+
+namespace blend {
+// 1 when the current device is an sm_103 GPU and the TMA descriptor encoder is
+// reachable; also sets the kernels' shared-memory limits.
+int tc_available();
+// Shapes the tensor-core kernel takes: K % 64 == 0, N % 256 == 0, ldc % 8 == 0, and an A
+// buffer of at least 128 rows (M_cap).
+bool tc_gemm_supported(int K, int N, int epi, int ldc, int M_cap);
+// A: [M_cap][K] bf16 buffer whose first *M_dev rows are used; B: [N][K] bf16.
+// Returns BLEND_OK or BLEND_EUNSUPPORTED (operands not describable by a tensor map).
+int launch_gemm_tc(const void* A, int K, int M_cap, const void* B, int N, const int32_t* M_dev, int M_max,
+                   int epi, void* C, int ldc, int32_t* err, cudaStream_t s);
+}  // namespace blend

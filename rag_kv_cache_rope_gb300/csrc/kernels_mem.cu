@@ -1,0 +1,629 @@
+// HBM-bound kernels of blended prefill: RoPE table, key realignment and cache
+// assembly, fused RoPE + deviation + K/V scatter, RMSNorm, row gather, row plans.
+//
+// Rows are streamed with 16-byte vector accesses so a warp touches contiguous
+// 512-byte spans; reductions run in a fixed order (no floating-point atomics) so
+// results are bitwise reproducible run to run.
+#include "common.cuh"
+
+namespace blend {
+
+// ---------------------------------------------------------------- RoPE table
+// tab[p][i] = (cos a, sin a) with a = p * theta^(-2i/d), evaluated in fp64 and rounded
+// to fp32 (an fp32 angle would be off by ~1e-3 rad at position 32K).
+__global__ void k_rope_table(float2* tab, int max_pos, int half, double theta, int d) {
+    long long total = (long long)max_pos * half;
+    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        int p = (int)(idx / half);
+        int i = (int)(idx % half);
+        double inv = pow(theta, -2.0 * (double)i / (double)d);
+        double a = (double)p * inv;
+        double s, c;
+        sincos(a, &s, &c);
+        tab[idx] = make_float2((float)c, (float)s);
+    }
+}
+
+void launch_rope_table(float2* tab, int max_pos, int head_dim, double theta, cudaStream_t s) {
+    int half = head_dim / 2;
+    long long total = (long long)max_pos * half;
+    long long blocks = (total + 255) / 256;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    k_rope_table<<<(int)blocks, 256, 0, s>>>(tab, max_pos, half, theta, head_dim);
+    note_launch(1);
+}
+
+// Rotates the pair vectors (row[i0..i0+V), row[i0+d/2..i0+d/2+V)) by `delta` positions:
+// (x1, x2) -> (x1 cos - x2 sin, x2 cos + x1 sin); a negative delta flips sin.
+template <typename T>
+__device__ __forceinline__ void rotate_pair(const T* src, T* dst, int i0, int half, int delta,
+                                            const float2* tab) {
+    Vec<T> a = ld16(src + i0);
+    Vec<T> b = ld16(src + i0 + half);
+    const int ad = delta < 0 ? -delta : delta;
+    const float sg = delta < 0 ? -1.f : 1.f;
+    const float2* cs = tab + (long long)ad * half + i0;
+    Vec<T> oa, ob;
+#pragma unroll
+    for (int e = 0; e < Vec<T>::N; ++e) {
+        float2 t = cs[e];
+        float c = t.x, s = sg * t.y;
+        float x1 = a.get(e), x2 = b.get(e);
+        oa.set(e, x1 * c - x2 * s);
+        ob.set(e, x2 * c + x1 * s);
+    }
+    st16(dst + i0, oa);
+    st16(dst + i0 + half, ob);
+}
+
+// ---------------------------------------------------------------- realign (per-row shift)
+template <typename T>
+__global__ void k_realign(const T* src, T* dst, int n_rows, const int32_t* delta, long long src_lr,
+                          long long dst_lr, int hkv, int d, const float2* tab, int max_pos,
+                          int32_t* err) {
+    const int layer = blockIdx.y;
+    const int row = blockIdx.x;
+    if (row >= n_rows) return;
+    const int dl = delta[row];
+    if (dl <= -max_pos || dl >= max_pos) {
+        set_error(err, BLEND_EINVAL);
+        return;
+    }
+    const int half = d / 2;
+    const int VN = Vec<T>::N;
+    const int per_head = half / VN;
+    const long long re = (long long)hkv * d;
+    const T* s = src + ((long long)layer * src_lr + row) * re;
+    T* o = dst + ((long long)layer * dst_lr + row) * re;
+    for (int j = threadIdx.x; j < hkv * per_head; j += blockDim.x) {
+        int g = j / per_head, i0 = (j % per_head) * VN;
+        rotate_pair(s + g * d, o + g * d, i0, half, dl, tab);
+    }
+}
+
+void launch_realign(int dtype, const void* src, void* dst, int n_rows, const int32_t* delta,
+                    int n_layers, long long src_lr, long long dst_lr, int hkv, int d,
+                    const float2* tab, int max_pos, int32_t* err, cudaStream_t s) {
+    if (n_rows <= 0 || n_layers <= 0) return;
+    dim3 grid(n_rows, n_layers);
+    if (dtype == BLEND_BF16)
+        k_realign<bf16><<<grid, 128, 0, s>>>((const bf16*)src, (bf16*)dst, n_rows, delta, src_lr,
+                                             dst_lr, hkv, d, tab, max_pos, err);
+    else
+        k_realign<float><<<grid, 128, 0, s>>>((const float*)src, (float*)dst, n_rows, delta,
+                                              src_lr, dst_lr, hkv, d, tab, max_pos, err);
+    note_launch(1);
+}
+
+// ---------------------------------------------------------------- assemble
+// Concatenation + prefix drop + key realignment for every layer of a batch.  The
+// segment table lists, in order, the prefix rows of each request (shift 0) and each
+// chunk's rows (shift = offset of the chunk among the request's chunks).  One CTA
+// handles ASM_ROWS consecutive rows of one layer (blockIdx.y).
+constexpr int ASM_ROWS = 8;
+
+template <typename T>
+__global__ void __launch_bounds__(256)
+    k_assemble(const __grid_constant__ SegTable segs, const T* __restrict__ pk,
+               const T* __restrict__ pv, long long pool_rows, T* __restrict__ ok,
+               T* __restrict__ ov, long long out_tokens, int hkv, int d,
+               const float2* __restrict__ tab, int max_pos, int32_t* err) {
+    const int layer = blockIdx.y;
+    const int half = d / 2;
+    const int VN = Vec<T>::N;
+    const int per_head = half / VN;
+    const int nk = hkv * per_head;  // K pair items per row
+    const int nv = hkv * d / VN;    // V vector items per row
+    const long long re = (long long)hkv * d;
+    for (int rr = 0; rr < ASM_ROWS; ++rr) {
+        const int r = blockIdx.x * ASM_ROWS + rr;
+        if (r >= segs.total_rows) return;
+        int lo = 0, hi = segs.n_seg - 1;  // last segment with row0 <= r
+        while (lo < hi) {
+            int mid = (lo + hi + 1) >> 1;
+            if (segs.s[mid].row0 <= r) lo = mid;
+            else hi = mid - 1;
+        }
+        const Seg sg = segs.s[lo];
+        const int k = r - sg.row0;
+        const long long srow = (long long)sg.src_row + k;
+        const long long drow = (long long)sg.dst_tok + k;
+        const int dl = sg.delta;
+        if (dl < 0 || dl >= max_pos || srow >= pool_rows || drow >= out_tokens) {
+            set_error(err, BLEND_EINVAL);
+            continue;
+        }
+        const T* sk = pk + ((long long)layer * pool_rows + srow) * re;
+        const T* sv = pv + ((long long)layer * pool_rows + srow) * re;
+        T* dk = ok + ((long long)layer * out_tokens + drow) * re;
+        T* dv = ov + ((long long)layer * out_tokens + drow) * re;
+        for (int j = threadIdx.x; j < nk + nv; j += blockDim.x) {
+            if (j < nk) {
+                int g = j / per_head, i0 = (j % per_head) * VN;
+                rotate_pair(sk + g * d, dk + g * d, i0, half, dl, tab);
+            } else {
+                int e = (j - nk) * VN;
+                st16(dv + e, ld16(sv + e));
+            }
+        }
+    }
+}
+
+void launch_assemble(int dtype, const SegTable& segs, const void* pool_k, const void* pool_v,
+                     long long pool_rows, void* out_k, void* out_v, long long out_tokens,
+                     int n_layers, int hkv, int d, const float2* tab, int max_pos, int32_t* err,
+                     cudaStream_t s) {
+    if (segs.total_rows <= 0 || n_layers <= 0) return;
+    dim3 grid((segs.total_rows + ASM_ROWS - 1) / ASM_ROWS, n_layers);
+    const int items = hkv * (d / 2) / (16 / (dtype == BLEND_BF16 ? 2 : 4)) +
+                      hkv * d / (16 / (dtype == BLEND_BF16 ? 2 : 4));
+    int threads = items >= 256 ? 256 : ((items + 31) / 32) * 32;
+    if (dtype == BLEND_BF16)
+        k_assemble<bf16><<<grid, threads, 0, s>>>(segs, (const bf16*)pool_k, (const bf16*)pool_v,
+                                                  pool_rows, (bf16*)out_k, (bf16*)out_v,
+                                                  out_tokens, hkv, d, tab, max_pos, err);
+    else
+        k_assemble<float><<<grid, threads, 0, s>>>(segs, (const float*)pool_k,
+                                                   (const float*)pool_v, pool_rows, (float*)out_k,
+                                                   (float*)out_v, out_tokens, hkv, d, tab, max_pos,
+                                                   err);
+    note_launch(1);
+}
+
+// Token id of every blended token: prefix and chunk rows from the pool, query rows
+// from each request's query tokens.
+__global__ void k_tokens(const __grid_constant__ SegTable segs,
+                         const __grid_constant__ QueryTable qt, const int32_t* pool_tokens,
+                         int32_t* out) {
+    for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < segs.total_rows;
+         r += gridDim.x * blockDim.x) {
+        int lo = 0, hi = segs.n_seg - 1;
+        while (lo < hi) {
+            int mid = (lo + hi + 1) >> 1;
+            if (segs.s[mid].row0 <= r) lo = mid;
+            else hi = mid - 1;
+        }
+        const Seg sg = segs.s[lo];
+        const int k = r - sg.row0;
+        out[sg.dst_tok + k] = pool_tokens[sg.src_row + k];
+    }
+    for (int q = 0; q < qt.n; ++q)
+        for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < qt.len[q];
+             i += gridDim.x * blockDim.x)
+            out[qt.dst_tok[q] + i] = qt.ptr[q][i];
+}
+
+void launch_tokens(const SegTable& segs, const QueryTable& qt, const int32_t* pool_tokens,
+                   int32_t* out_tokens, cudaStream_t s) {
+    int blocks = (segs.total_rows + 255) / 256;
+    if (blocks < 1) blocks = 1;
+    if (blocks > 1024) blocks = 1024;
+    k_tokens<<<blocks, 256, 0, s>>>(segs, qt, pool_tokens, out_tokens);
+    note_launch(1);
+}
+
+// ---------------------------------------------------------------- RMSNorm
+// out[row] = x[row] / sqrt(mean(x^2) + eps) * g, x fp32, out in the model dtype.
+template <typename T>
+__global__ void __launch_bounds__(256) k_rmsnorm(const float* __restrict__ x, const T* __restrict__ g,
+                                                 T* __restrict__ out, int H, float eps,
+                                                 const int32_t* M_dev) {
+    __shared__ float red[256];
+    const int row = blockIdx.x;
+    if (row >= *M_dev) return;
+    const float* xr = x + (long long)row * H;
+    float ss = 0.f;
+    for (int j = threadIdx.x; j < H; j += blockDim.x) {
+        float v = xr[j];
+        ss += v * v;
+    }
+    ss = block_sum(ss, red);
+    const float r = rsqrtf(ss / (float)H + eps);
+    T* o = out + (long long)row * H;
+    for (int j = threadIdx.x; j < H; j += blockDim.x) o[j] = from_f<T>(xr[j] * r * to_f<T>(g[j]));
+}
+
+void launch_rmsnorm(int dtype, const float* x, const void* g, void* out, int H, float eps,
+                    const int32_t* M_dev, int M_max, cudaStream_t s) {
+    if (M_max <= 0) return;
+    if (dtype == BLEND_BF16)
+        k_rmsnorm<bf16><<<M_max, 256, 0, s>>>(x, (const bf16*)g, (bf16*)out, H, eps, M_dev);
+    else
+        k_rmsnorm<float><<<M_max, 256, 0, s>>>(x, (const float*)g, (float*)out, H, eps, M_dev);
+    note_launch(1);
+}
+
+// Final norm of every request's query rows (the last Q rows of its block of rows).
+template <typename T>
+__global__ void __launch_bounds__(256)
+    k_final_norm(const float* __restrict__ x, const T* __restrict__ g, T* __restrict__ hidden,
+                 int H, float eps, const __grid_constant__ BatchDesc bd, const int32_t* req_row_end) {
+    __shared__ float red[256];
+    const int r = blockIdx.y;
+    const int j = blockIdx.x;
+    if (j >= bd.r[r].Q) return;
+    const long long row = (long long)req_row_end[r] - bd.r[r].Q + j;
+    const float* xr = x + row * H;
+    float ss = 0.f;
+    for (int c = threadIdx.x; c < H; c += blockDim.x) {
+        float v = xr[c];
+        ss += v * v;
+    }
+    ss = block_sum(ss, red);
+    const float rr = rsqrtf(ss / (float)H + eps);
+    T* o = hidden + ((long long)bd.r[r].q_off + j) * H;
+    for (int c = threadIdx.x; c < H; c += blockDim.x) o[c] = from_f<T>(xr[c] * rr * to_f<T>(g[c]));
+}
+
+void launch_final_norm(int dtype, const float* x, const void* g, void* hidden, int H, float eps,
+                       const BatchDesc& bd, const int32_t* req_row_end, cudaStream_t s) {
+    int maxq = 0;
+    for (int r = 0; r < bd.n_req; ++r) maxq = bd.r[r].Q > maxq ? bd.r[r].Q : maxq;
+    if (maxq == 0) return;
+    dim3 grid(maxq, bd.n_req);
+    if (dtype == BLEND_BF16)
+        k_final_norm<bf16><<<grid, 256, 0, s>>>(x, (const bf16*)g, (bf16*)hidden, H, eps, bd,
+                                                req_row_end);
+    else
+        k_final_norm<float><<<grid, 256, 0, s>>>(x, (const float*)g, (float*)hidden, H, eps, bd,
+                                                 req_row_end);
+    note_launch(1);
+}
+
+// ---------------------------------------------------------------- embeddings, gather
+template <typename T>
+__global__ void k_embed(const T* __restrict__ embed, const int32_t* __restrict__ tokens,
+                        const int32_t* __restrict__ row_tok, float* __restrict__ x, int H, int vocab,
+                        const int32_t* M_dev, int32_t* err) {
+    const int row = blockIdx.x;
+    if (row >= *M_dev) return;
+    long long tok = tokens[row_tok[row]];
+    if (tok < 0 || tok >= vocab) {  // token id outside the vocabulary: reported, row 0 used
+        if (threadIdx.x == 0) set_error(err, BLEND_EDEVICE);
+        tok = 0;
+    }
+    const T* e = embed + tok * H;
+    float* o = x + (long long)row * H;
+    for (int j = threadIdx.x; j < H; j += blockDim.x) o[j] = to_f<T>(e[j]);
+}
+
+void launch_embed(int dtype, const void* embed, const int32_t* tokens, const int32_t* row_tok,
+                  float* x, int H, int vocab, const int32_t* M_dev, int M_max, int32_t* err,
+                  cudaStream_t s) {
+    if (M_max <= 0) return;
+    if (dtype == BLEND_BF16)
+        k_embed<bf16><<<M_max, 256, 0, s>>>((const bf16*)embed, tokens, row_tok, x, H, vocab, M_dev, err);
+    else
+        k_embed<float><<<M_max, 256, 0, s>>>((const float*)embed, tokens, row_tok, x, H, vocab, M_dev, err);
+    note_launch(1);
+}
+
+// dst[i] = src[idx[i]], rows of row_bytes (multiple of 16).
+__global__ void k_gather(const uint4* __restrict__ src, long long row_vec,
+                         const int32_t* __restrict__ idx, const int32_t* n_dev, uint4* __restrict__ dst) {
+    const int i = blockIdx.x;
+    if (i >= *n_dev) return;
+    const long long s = (long long)idx[i] * row_vec;
+    const long long d = (long long)i * row_vec;
+    for (long long j = threadIdx.x; j < row_vec; j += blockDim.x) dst[d + j] = src[s + j];
+}
+
+void launch_gather(const void* src, long long row_bytes, const int32_t* idx, const int32_t* n_dev,
+                   int max_n, void* dst, cudaStream_t s) {
+    if (max_n <= 0) return;
+    long long rv = row_bytes / 16;
+    int threads = rv >= 256 ? 256 : (int)(((rv + 31) / 32) * 32);
+    k_gather<<<max_n, threads, 0, s>>>((const uint4*)src, rv, idx, n_dev, (uint4*)dst);
+    note_launch(1);
+}
+
+// ---------------------------------------------------------------- fused RoPE + deviation + scatter
+// For each recomputed row (one CTA per row): rotate q and k at the row's blended
+// position, store q for attention, compare the fresh k, v (fp32, before rounding) with
+// the cached rows at that position (deviation, optional), then overwrite the cache rows.
+template <typename T>
+__global__ void __launch_bounds__(256)
+    k_rope_qkv(const float* __restrict__ qkv, const int32_t* __restrict__ row_pos,
+               const int32_t* __restrict__ row_tok, const int32_t* __restrict__ row_req,
+               const int32_t* M_dev, const __grid_constant__ BatchDesc bd, int hq, int hkv, int d,
+               const float2* __restrict__ tab, T* __restrict__ q_out, T* __restrict__ kc,
+               T* __restrict__ vc, float* __restrict__ dev_out, int dev_mode, int dev_by_row) {
+    __shared__ float red[256];
+    const int row = blockIdx.x;
+    if (row >= *M_dev) return;
+    const int pos = row_pos[row];
+    const long long tok = row_tok[row];
+    const int half = d / 2;
+    const int width = (hq + 2 * hkv) * d;
+    const float* src = qkv + (long long)row * width;
+    const float2* cs = tab + (long long)pos * half;
+    T* qo = q_out + (long long)row * hq * d;
+    for (int j = threadIdx.x; j < hq * half; j += blockDim.x) {
+        int h = j / half, i = j % half;
+        float x1 = src[h * d + i], x2 = src[h * d + i + half];
+        float2 t = cs[i];
+        qo[h * d + i] = from_f<T>(x1 * t.x - x2 * t.y);
+        qo[h * d + i + half] = from_f<T>(x2 * t.x + x1 * t.y);
+    }
+    float acc = 0.f;
+    const float* ks = src + hq * d;
+    T* kr = kc + tok * hkv * d;
+    for (int j = threadIdx.x; j < hkv * half; j += blockDim.x) {
+        int g = j / half, i = j % half;
+        float x1 = ks[g * d + i], x2 = ks[g * d + i + half];
+        float2 t = cs[i];
+        float r1 = x1 * t.x - x2 * t.y, r2 = x2 * t.x + x1 * t.y;
+        if (dev_out && dev_mode == BLEND_DEV_KV) {
+            float o1 = to_f<T>(kr[g * d + i]) - r1, o2 = to_f<T>(kr[g * d + i + half]) - r2;
+            acc += o1 * o1 + o2 * o2;
+        }
+        kr[g * d + i] = from_f<T>(r1);
+        kr[g * d + i + half] = from_f<T>(r2);
+    }
+    const float* vs = src + (hq + hkv) * d;
+    T* vr = vc + tok * hkv * d;
+    for (int j = threadIdx.x; j < hkv * d; j += blockDim.x) {
+        float v = vs[j];
+        if (dev_out) {
+            float o = to_f<T>(vr[j]) - v;
+            acc += o * o;
+        }
+        vr[j] = from_f<T>(v);
+    }
+    if (dev_out) {
+        float dv = block_sum(acc, red);
+        const ReqDesc rd = bd.r[row_req[row]];
+        if (threadIdx.x == 0) {
+            if (dev_by_row) dev_out[row] = dv;
+            else if (pos >= rd.P && pos < rd.P + rd.n_c) dev_out[rd.nc_off + pos - rd.P] = dv;
+        }
+    }
+}
+
+void launch_rope_qkv(int dtype, const float* qkv, const int32_t* row_pos, const int32_t* row_tok,
+                     const int32_t* row_req, const int32_t* M_dev, int M_max, const BatchDesc& bd,
+                     int hq, int hkv, int d, const float2* tab, void* q_out, void* k_cache,
+                     void* v_cache, float* dev_out, int dev_mode, int dev_by_row, cudaStream_t s) {
+    if (M_max <= 0) return;
+    if (dtype == BLEND_BF16)
+        k_rope_qkv<bf16><<<M_max, 256, 0, s>>>(qkv, row_pos, row_tok, row_req, M_dev, bd, hq, hkv,
+                                               d, tab, (bf16*)q_out, (bf16*)k_cache,
+                                               (bf16*)v_cache, dev_out, dev_mode, dev_by_row);
+    else
+        k_rope_qkv<float><<<M_max, 256, 0, s>>>(qkv, row_pos, row_tok, row_req, M_dev, bd, hq, hkv,
+                                                d, tab, (float*)q_out, (float*)k_cache,
+                                                (float*)v_cache, dev_out, dev_mode, dev_by_row);
+    note_launch(1);
+}
+
+// ---------------------------------------------------------------- standalone deviation / scatter
+template <typename T>
+__global__ void __launch_bounds__(256)
+    k_deviation(const T* __restrict__ kn, const T* __restrict__ vn, const T* __restrict__ kc,
+                const T* __restrict__ vc, const int32_t* __restrict__ pos, const int32_t* n_dev,
+                int kv_elems, int mode, float* __restrict__ dev) {
+    __shared__ float red[256];
+    const int i = blockIdx.x;
+    if (i >= *n_dev) return;
+    const long long a = (long long)i * kv_elems, b = (long long)pos[i] * kv_elems;
+    float acc = 0.f;
+    for (int j = threadIdx.x; j < kv_elems; j += blockDim.x) {
+        float dv = to_f<T>(vn[a + j]) - to_f<T>(vc[b + j]);
+        acc += dv * dv;
+        if (mode == BLEND_DEV_KV) {
+            float dk = to_f<T>(kn[a + j]) - to_f<T>(kc[b + j]);
+            acc += dk * dk;
+        }
+    }
+    float s = block_sum(acc, red);
+    if (threadIdx.x == 0) dev[i] = s;
+}
+
+void launch_deviation(int dtype, const void* k_new, const void* v_new, const void* k_cache,
+                      const void* v_cache, const int32_t* pos, const int32_t* n_dev, int max_rows,
+                      int kv_elems, int mode, float* dev_out, cudaStream_t s) {
+    if (max_rows <= 0) return;
+    if (dtype == BLEND_BF16)
+        k_deviation<bf16><<<max_rows, 256, 0, s>>>((const bf16*)k_new, (const bf16*)v_new,
+                                                   (const bf16*)k_cache, (const bf16*)v_cache, pos,
+                                                   n_dev, kv_elems, mode, dev_out);
+    else
+        k_deviation<float><<<max_rows, 256, 0, s>>>((const float*)k_new, (const float*)v_new,
+                                                    (const float*)k_cache, (const float*)v_cache,
+                                                    pos, n_dev, kv_elems, mode, dev_out);
+    note_launch(1);
+}
+
+__global__ void k_scatter(const uint4* __restrict__ kn, const uint4* __restrict__ vn,
+                          const int32_t* __restrict__ pos, const int32_t* n_dev, long long row_vec,
+                          uint4* __restrict__ kc, uint4* __restrict__ vc) {
+    const int i = blockIdx.x;
+    if (i >= *n_dev) return;
+    const long long a = (long long)i * row_vec, b = (long long)pos[i] * row_vec;
+    for (long long j = threadIdx.x; j < row_vec; j += blockDim.x) {
+        kc[b + j] = kn[a + j];
+        vc[b + j] = vn[a + j];
+    }
+}
+
+void launch_scatter(int dtype, const void* k_new, const void* v_new, const int32_t* pos,
+                    const int32_t* n_dev, int max_n, int kv_elems, void* k_cache, void* v_cache,
+                    cudaStream_t s) {
+    if (max_n <= 0) return;
+    long long rv = (long long)kv_elems * (dtype == BLEND_BF16 ? 2 : 4) / 16;
+    int threads = rv >= 128 ? 128 : (int)(((rv + 31) / 32) * 32);
+    k_scatter<<<max_n, threads, 0, s>>>((const uint4*)k_new, (const uint4*)v_new, pos, n_dev, rv,
+                                        (uint4*)k_cache, (uint4*)v_cache);
+    note_launch(1);
+}
+
+// ---------------------------------------------------------------- importance scores
+// SpecCache 2.2: out[i] = mean over layers of the L2 norm of hidden[i][l].
+template <typename T>
+__global__ void __launch_bounds__(256) k_importance(const T* __restrict__ h, int n_layers, int dim,
+                                                    float* __restrict__ out) {
+    __shared__ float red[256];
+    const long long i = blockIdx.x;
+    float acc = 0.f;
+    for (int l = 0; l < n_layers; ++l) {
+        const T* r = h + (i * n_layers + l) * dim;
+        float ss = 0.f;
+        for (int j = threadIdx.x; j < dim; j += blockDim.x) {
+            float v = to_f<T>(r[j]);
+            ss += v * v;
+        }
+        ss = block_sum(ss, red);
+        acc += sqrtf(ss);
+    }
+    if (threadIdx.x == 0) out[i] = acc / (float)n_layers;
+}
+
+void launch_importance(int dtype, const void* hidden, int n, int n_layers, int dim, float* out,
+                       cudaStream_t s) {
+    if (n <= 0) return;
+    if (dtype == BLEND_BF16)
+        k_importance<bf16><<<n, 256, 0, s>>>((const bf16*)hidden, n_layers, dim, out);
+    else
+        k_importance<float><<<n, 256, 0, s>>>((const float*)hidden, n_layers, dim, out);
+    note_launch(1);
+}
+
+// ---------------------------------------------------------------- row plans
+// Rows of request r = its stage set (ascending) followed by its Q query positions;
+// requests are laid out one after another.  Also records, for a new plan, the row each
+// position held in the previous plan (row_src; the new set is a subset of the old
+// one), then updates the position -> row map.  Positions outside a request's chunk
+// region (or not increasing) are reported in err and replaced by the first query
+// position, so no access leaves the request's rows.
+__global__ void __launch_bounds__(1024)
+    k_plan(const __grid_constant__ BatchDesc bd, StageDesc st, int32_t* row_pos, int32_t* row_tok,
+           int32_t* row_req, int32_t* row_src, int32_t* pos2row, int32_t* M_dev,
+           int32_t* req_row_end, const int32_t* old_row_tok, const int32_t* old_M, int32_t* err) {
+    __shared__ int off[BLEND_MAX_BATCH + 1];
+    __shared__ int cnt[BLEND_MAX_BATCH];
+    if (threadIdx.x == 0) {
+        off[0] = 0;
+        for (int r = 0; r < bd.n_req; ++r) {
+            const ReqDesc rd = bd.r[r];
+            const int cap = st.iota == 2 ? (rd.P + rd.n_c) : rd.n_c;
+            int n = st.iota ? cap : st.count[r];
+            if (n < 0 || n > cap) {
+                set_error(err, BLEND_EDEVICE);
+                n = n < 0 ? 0 : cap;
+            }
+            cnt[r] = n;
+            off[r + 1] = off[r] + n + rd.Q;
+        }
+    }
+    __syncthreads();
+    for (int r = 0; r < bd.n_req; ++r) {
+        const ReqDesc rd = bd.r[r];
+        const int n = cnt[r];
+        for (int i = threadIdx.x; i < n + rd.Q; i += blockDim.x) {
+            int pos;
+            if (i < n) {
+                if (st.iota) {
+                    pos = st.iota == 2 ? i : rd.P + i;
+                } else {
+                    pos = st.set[rd.nc_off + i];
+                    bool ok = pos >= rd.P && pos < rd.P + rd.n_c;
+                    if (ok && i > 0) ok = st.set[rd.nc_off + i - 1] < pos;
+                    if (!ok) {
+                        set_error(err, BLEND_EDEVICE);
+                        pos = rd.Q > 0 ? rd.P + rd.n_c : rd.P;  // a valid row of this request
+                    }
+                }
+            } else {
+                pos = rd.P + rd.n_c + (i - n);
+            }
+            const int row = off[r] + i;
+            const int tok = rd.tok_off + pos;
+            row_pos[row] = pos;
+            row_tok[row] = tok;
+            row_req[row] = r;
+            if (old_row_tok) {
+                // the new set must be part of the previous one: its row there holds tok
+                int src = pos2row[tok];
+                if (src < 0 || src >= *old_M || old_row_tok[src] != tok) {
+                    set_error(err, BLEND_EDEVICE);
+                    src = 0;
+                }
+                row_src[row] = src;
+            }
+        }
+    }
+    __syncthreads();
+    for (int r = 0; r < bd.n_req; ++r) {
+        const int base = off[r];
+        const int m = off[r + 1] - base;
+        for (int i = threadIdx.x; i < m; i += blockDim.x) pos2row[row_tok[base + i]] = base + i;
+    }
+    if (threadIdx.x == 0) {
+        *M_dev = off[bd.n_req];
+        for (int r = 0; r < bd.n_req; ++r) req_row_end[r] = off[r + 1];
+    }
+}
+
+void launch_plan(const BatchDesc& bd, const StageDesc& st, int32_t* row_pos, int32_t* row_tok,
+                 int32_t* row_req, int32_t* row_src, int32_t* pos2row, int32_t* M_dev,
+                 int32_t* req_row_end, const int32_t* old_row_tok, const int32_t* old_M, int32_t* err,
+                 cudaStream_t s) {
+    k_plan<<<1, 1024, 0, s>>>(bd, st, row_pos, row_tok, row_req, row_src, pos2row, M_dev,
+                              req_row_end, old_row_tok, old_M, err);
+    note_launch(1);
+}
+
+// mask[nc_off + pos - P] = 1 for every position of request r's set (one CTA per request).
+__global__ void __launch_bounds__(1024)
+    k_set_mask(const __grid_constant__ BatchDesc bd, const int32_t* set, const int32_t* count,
+               uint8_t* mask) {
+    const ReqDesc rd = bd.r[blockIdx.x];
+    for (int i = threadIdx.x; i < rd.n_c; i += blockDim.x) mask[rd.nc_off + i] = 0;
+    __syncthreads();
+    const int n = count[blockIdx.x];
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        int p = set[rd.nc_off + i] - rd.P;
+        if (p >= 0 && p < rd.n_c) mask[rd.nc_off + p] = 1;
+    }
+}
+
+void launch_set_mask(const BatchDesc& bd, const int32_t* set, const int32_t* count, uint8_t* mask,
+                     cudaStream_t s) {
+    k_set_mask<<<bd.n_req, 1024, 0, s>>>(bd, set, count, mask);
+    note_launch(1);
+}
+
+__global__ void k_fill_i32(int32_t* p, int32_t v, long long n) {
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+         i += (long long)gridDim.x * blockDim.x)
+        p[i] = v;
+}
+
+void launch_fill_i32(int32_t* p, int32_t v, long long n, cudaStream_t s) {
+    if (n <= 0) return;
+    long long b = (n + 255) / 256;
+    if (b > 4096) b = 4096;
+    k_fill_i32<<<(int)b, 256, 0, s>>>(p, v, n);
+    note_launch(1);
+}
+
+// Copies each request's set (and count) from the workspace to the caller's outputs;
+// with src == nullptr the set is every chunk row P..P+n_c-1.  Unused slots get -1.
+__global__ void k_copy_sets(const __grid_constant__ BatchDesc bd, const int32_t* src,
+                            const int32_t* src_n, int32_t* dst, int32_t* dst_n) {
+    const ReqDesc rd = bd.r[blockIdx.x];
+    const int n = src ? src_n[blockIdx.x] : rd.n_c;
+    if (dst)
+        for (int i = threadIdx.x; i < rd.n_c; i += blockDim.x)
+            dst[rd.nc_off + i] = i < n ? (src ? src[rd.nc_off + i] : rd.P + i) : -1;
+    if (dst_n && threadIdx.x == 0) dst_n[blockIdx.x] = n;
+}
+
+void launch_copy_sets(const BatchDesc& bd, const int32_t* src, const int32_t* src_n, int32_t* dst,
+                      int32_t* dst_n, cudaStream_t s) {
+    k_copy_sets<<<bd.n_req, 256, 0, s>>>(bd, src, src_n, dst, dst_n);
+    note_launch(1);
+}
+
+}  // namespace blend
