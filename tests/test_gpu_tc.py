@@ -1,0 +1,66 @@
+"""The tcgen05 tensor-core GEMM path against the oracle and against the CUDA-core path.
+
+One decoder layer through selective_layer with the tensor cores on and off: row
+counts that span several 128-row tiles with a ragged tail, widths that give several
+256-column tiles and many 64-wide k-blocks per tile, and more tiles than SMs.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import blend_oracle as O
+from rag_kv_cache_rope_gb300 import binding as b
+from rag_kv_cache_rope_gb300 import build as B
+from rag_kv_cache_rope_gb300 import synth
+
+from blendcase import GpuRunner, f64, make_case, maxrel, oracle_cfg
+
+pytestmark = pytest.mark.gpu
+
+TOL_BF16 = 2e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    B.build()
+    b.lib()
+
+
+SHAPES = [
+    (synth.ModelShape("tc-small", 2, 512, 8, 2, 128, 1024, 300, 1e6), 300, 700),
+    (synth.ModelShape("tc-wide", 2, 2048, 16, 4, 128, 5632, 300, 1e6), 1000, 1500),
+]
+
+
+@pytest.mark.parametrize("shape,n,n_ctx", SHAPES, ids=[s[0].name for s in SHAPES])
+def test_layer_tensor_cores_match_oracle_and_cuda_cores(shape, n, n_ctx):
+    dev = torch.device("cuda:0")
+    case = make_case(shape, 4, [8], pool="random")
+    r = GpuRunner(case, max(n, 128), n_ctx, 64, max_pos=n_ctx)
+    assert b.blend_set_tensor_cores(r.h, True) == 1, "tcgen05 path unavailable on this GPU"
+    g = torch.Generator().manual_seed(11)
+    dt = synth.torch_dtype(shape)
+    kc = (0.5 * torch.randn(n_ctx, shape.n_kv_heads, shape.head_dim, generator=g)).to(dt)
+    vc = (0.5 * torch.randn(n_ctx, shape.n_kv_heads, shape.head_dim, generator=g)).to(dt)
+    x = torch.randn(n, shape.hidden, generator=g)
+    pos = torch.sort(torch.randperm(n_ctx, generator=g)[:n]).values.to(torch.int32)
+    outs = {}
+    for tc in (True, False):
+        b.blend_set_tensor_cores(r.h, tc)
+        xg, kg, vg = x.to(dev), kc.to(dev), vc.to(dev)
+        dv = torch.zeros(n, device=dev)
+        b.selective_layer(r.h, 1, xg, pos.to(dev), n, kg, vg, n_ctx, dv)
+        b.blend_device_status(r.h)
+        outs[tc] = (f64(xg), f64(kg), f64(vg), f64(dv))
+    K, V = f64(kc), f64(vc)
+    xo, dref = O.layer_forward(case.w_np, oracle_cfg(shape), 1, f64(x), pos.numpy(), K, V,
+                               np.ones(n, dtype=bool))
+    for tc, (xg, kg, vg, dv) in outs.items():
+        assert maxrel(kg, K) <= TOL_BF16, tc
+        assert maxrel(vg, V) <= TOL_BF16, tc
+        assert maxrel(xg, xo) <= TOL_BF16, tc
+        assert maxrel(dv, dref) <= TOL_BF16, tc
+    # the two GPU paths differ only by fp32 summation order
+    assert maxrel(outs[True][0], outs[False][0]) <= 1e-2
