@@ -265,20 +265,27 @@ void gemm(blend_handle* h, const void* A, int K, const void* B, int N, int epi, 
         launch_gemm_simt(h->cfg.dtype, A, K, B, K, K, N, M_dev, M_max, epi, C, ldc, s);
 }
 
-void attention(blend_handle* h, const Plan& p, int M_max, const void* kc, const void* vc, cudaStream_t s) {
+void attention(blend_handle* h, const Plan& p, int n_req, int M_max, const void* kc, const void* vc,
+               long long n_tokens, cudaStream_t s) {
     const blend_model_cfg& c = h->cfg;
-    launch_attn_simt(c.dtype, h->q, p.row_pos, p.row_tok, p.M, M_max, kc, vc, h->o, c.n_q_heads,
-                     c.n_kv_heads, c.head_dim, s);
+    if (c.dtype == BLEND_BF16 && h->use_tc && tc_attn_supported(c.head_dim)) {
+        int rc = launch_attn_tc(h->q, h->lim.max_rows, n_req, p.req_row_end, p.row_pos, p.row_tok, M_max, kc, vc,
+                                n_tokens, h->o, c.n_q_heads, c.n_kv_heads, h->err, s);
+        if (rc != BLEND_OK && h->host_rc == BLEND_OK) h->host_rc = rc;
+        return;
+    }
+    launch_attn_simt(c.dtype, h->q, h->lim.max_rows, p.row_pos, p.row_tok, p.M, M_max, kc, vc, h->o,
+                     c.n_q_heads, c.n_kv_heads, c.head_dim, s);
 }
 
 // The part of a layer after the K/V write: attention, O-proj + residual, RMSNorm,
 // SwiGLU MLP + residual, on the rows of plan p (x holds those rows).
-void layer_rest(blend_handle* h, int l, float* x, const Plan& p, int M_max, const void* kc,
-                const void* vc, cudaStream_t s) {
+void layer_rest(blend_handle* h, int l, float* x, const Plan& p, int n_req, int M_max, const void* kc,
+                const void* vc, long long n_tokens, cudaStream_t s) {
     const blend_model_cfg& c = h->cfg;
     const LayerW lw = layer_w(h, l);
     const int H = c.hidden, qd = c.n_q_heads * c.head_dim, F = c.ffn;
-    { ProfScope ps(h, PROF_ATTN, s); attention(h, p, M_max, kc, vc, s); }
+    { ProfScope ps(h, PROF_ATTN, s); attention(h, p, n_req, M_max, kc, vc, n_tokens, s); }
     { ProfScope ps(h, PROF_GEMM_O, s); gemm(h, h->o, qd, lw.w_o, H, EPI_ADD_F32, x, H, p.M, M_max, s); }
     { ProfScope ps(h, PROF_NORM, s); launch_rmsnorm(c.dtype, x, lw.mlp_norm, h->xn, H, c.rms_eps, p.M, M_max, s); }
     { ProfScope ps(h, PROF_GEMM_GU, s); gemm(h, h->xn, H, lw.w_gu, 2 * F, EPI_SWIGLU, h->hmlp, F, p.M, M_max, s); }
@@ -298,7 +305,7 @@ void layer_kv(blend_handle* h, int l, const float* x, const Plan& p, const int32
     { ProfScope ps(h, PROF_GEMM_QKV, s); gemm(h, h->xn, H, lw.w_qkv, width, EPI_STORE_F32, h->qkv, width, p.M, M_max, s); }
     ProfScope ps(h, PROF_ROPE_KV, s);
     launch_rope_qkv(c.dtype, h->qkv, p.row_pos, p.row_tok, row_req, p.M, M_max, bd, c.n_q_heads,
-                    c.n_kv_heads, d, h->rope, h->q, kc, vc, dev, dev_mode, dev_by_row, s);
+                    c.n_kv_heads, d, h->lim.max_rows, h->rope, h->q, kc, vc, dev, dev_mode, dev_by_row, s);
 }
 
 }  // namespace
@@ -540,7 +547,7 @@ int selective_layer(blend_handle* h, int32_t layer, float* x, const int32_t* pos
     launch_plan(bd, st, p.row_pos, p.row_tok, p.row_req, h->row_src, h->pos2row, p.M, p.req_row_end,
                 nullptr, nullptr, h->err, s);
     layer_kv(h, layer, x, p, p.row_req, n, bd, k_cache, v_cache, dev_out, dev_mode, 1, s);
-    layer_rest(h, layer, x, p, n, k_cache, v_cache, s);
+    layer_rest(h, layer, x, p, 1, n, k_cache, v_cache, n_ctx, s);
     return finish(h, "selective_layer");
 }
 
@@ -810,7 +817,14 @@ extern "C" int blend_prefill(blend_handle* h, int32_t n_req, const blend_request
             launch_plan(bd, st, np.row_pos, np.row_tok, np.row_req, h->row_src, h->pos2row, np.M,
                         np.req_row_end, h->plan[cur].row_tok, h->plan[cur].M, h->err, s);
             launch_gather(x, (long long)c.hidden * 4, h->row_src, np.M, M_max, x_alt, s);
-            launch_gather(h->q, (long long)c.n_q_heads * c.head_dim * es, h->row_src, np.M, M_max, h->q2, s);
+            {
+                // q is stored per kv head: compact each head's slab of [rows][group][d]
+                const int group = c.n_q_heads / c.n_kv_heads;
+                const size_t slab = (size_t)h->lim.max_rows * group * c.head_dim * es;
+                for (int g = 0; g < c.n_kv_heads; ++g)
+                    launch_gather((const char*)h->q + g * slab, (long long)group * c.head_dim * es, h->row_src,
+                                  np.M, M_max, (char*)h->q2 + g * slab, s);
+            }
             float* tx = x;
             x = x_alt;
             x_alt = tx;
@@ -819,7 +833,7 @@ extern "C" int blend_prefill(blend_handle* h, int32_t n_req, const blend_request
             h->q2 = tq;
             cur = 1 - cur;
         }
-        layer_rest(h, l, x, h->plan[cur], M_max, kc, vc, s);
+        layer_rest(h, l, x, h->plan[cur], n_req, M_max, kc, vc, tok, s);
     }
     // ---- 4. final norm of the query rows
     ProfScope ps_final(h, PROF_FINAL, s);

@@ -12,7 +12,7 @@
 namespace blend {
 
 template <typename T>
-__global__ void k_attn_simt(const T* __restrict__ q, const int32_t* __restrict__ row_pos,
+__global__ void k_attn_simt(const T* __restrict__ q, int m_cap, const int32_t* __restrict__ row_pos,
                             const int32_t* __restrict__ row_tok, const int32_t* M_dev,
                             const T* __restrict__ Kc, const T* __restrict__ Vc, T* __restrict__ o,
                             int hq, int hkv, int d, float scale_log2) {
@@ -28,7 +28,7 @@ __global__ void k_attn_simt(const T* __restrict__ q, const int32_t* __restrict__
     float* Ks = sm;                 // [32][d+1]
     float* Vs = Ks + 32 * (d + 1);  // [32][d]
     float* qs = Vs + 32 * d;        // [group][d]
-    const T* qr = q + (long long)row * hq * d + (long long)g * group * d;
+    const T* qr = q + ((long long)g * m_cap + row) * group * d;
     for (int e = threadIdx.x; e < group * d; e += blockDim.x) qs[e] = to_f<T>(qr[e]);
     const int nd = d / 32;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -86,7 +86,7 @@ __global__ void k_attn_simt(const T* __restrict__ q, const int32_t* __restrict__
         if (u < nd) orow[lane + 32 * u] = from_f<T>(acc[u] * inv);
 }
 
-void launch_attn_simt(int dtype, const void* q, const int32_t* row_pos, const int32_t* row_tok,
+void launch_attn_simt(int dtype, const void* q, int m_cap, const int32_t* row_pos, const int32_t* row_tok,
                       const int32_t* M_dev, int M_max, const void* k_cache, const void* v_cache,
                       void* o, int hq, int hkv, int d, cudaStream_t s) {
     if (M_max <= 0) return;
@@ -96,12 +96,12 @@ void launch_attn_simt(int dtype, const void* q, const int32_t* row_pos, const in
     const float scale_log2 = (float)(1.4426950408889634 / sqrt((double)d));
     if (dtype == BLEND_BF16) {
         cudaFuncSetAttribute(k_attn_simt<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        k_attn_simt<bf16><<<grid, 32 * group, smem, s>>>((const bf16*)q, row_pos, row_tok, M_dev,
+        k_attn_simt<bf16><<<grid, 32 * group, smem, s>>>((const bf16*)q, m_cap, row_pos, row_tok, M_dev,
                                                          (const bf16*)k_cache, (const bf16*)v_cache,
                                                          (bf16*)o, hq, hkv, d, scale_log2);
     } else {
         cudaFuncSetAttribute(k_attn_simt<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        k_attn_simt<float><<<grid, 32 * group, smem, s>>>((const float*)q, row_pos, row_tok, M_dev,
+        k_attn_simt<float><<<grid, 32 * group, smem, s>>>((const float*)q, m_cap, row_pos, row_tok, M_dev,
                                                           (const float*)k_cache,
                                                           (const float*)v_cache, (float*)o, hq, hkv,
                                                           d, scale_log2);

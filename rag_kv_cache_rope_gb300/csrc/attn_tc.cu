@@ -1,0 +1,488 @@
+// Tensor-core causal GQA attention of the recomputed rows over the full blended KV
+// (CacheBlend blog, "Selective KV recompute": only the selected rows' attention rows
+// are computed, each over every earlier token, reused or fresh).
+//
+// Work item: one kv head g and 128 consecutive (row, head-of-group) pairs of one
+// request (q is stored per kv head as [pair][d], pair = row * group + j, so a tile is
+// one TMA box and each K/V block is shared by the whole head group).  Items run
+// longest first on persistent CTAs.  Per 64-key block:
+//   S  = Q . K^T      tcgen05.mma M128 N64 K16 x8  -> TMEM (two buffers)
+//   P  = softmax part  4 warps, one pair row per thread: mask keys past the row's
+//                      position, online max/sum in base 2, bf16 P into swizzled smem
+//   PV = P . V        tcgen05.mma M128 N128 K16 x4 (V as an MN-major operand) -> TMEM
+//   O  = O * c + PV   in the softmax threads' registers, one block behind, so the
+//                      tensor core computes S of block j+1 and PV of block j while the
+//                      threads work on block j+1.
+// Warps: 0 TMA producer, 1 TMEM owner + MMA issuer, 2..5 softmax + output.
+// All mbarrier waits are bounded (error word BLEND_ETIMEOUT, drain, free TMEM).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "gemm_tc.cuh"
+
+namespace blend {
+namespace {
+
+constexpr int D = 128;
+constexpr int BQ = 128;
+constexpr int BKV = 64;
+constexpr int KV_STAGES = 3;
+constexpr int Q_BYTES = BQ * D * 2;   // 32 KB: two 16 KB column halves (d 0-63, 64-127)
+constexpr int KH_BYTES = BKV * 64 * 2;  // 8 KB: one column half of a K or V block
+constexpr int KV_BYTES = 4 * KH_BYTES;  // K halves, then V halves
+constexpr int P_BYTES = BQ * BKV * 2;   // 16 KB
+constexpr int SMEM_BYTES = Q_BYTES + KV_STAGES * KV_BYTES + 2 * P_BYTES + 1024;
+constexpr int TMEM_COLS = 512;  // S0 [0,64) S1 [64,128) O0 [128,256) O1 [256,384)
+constexpr int THREADS = 192;
+constexpr long long SPIN_LIMIT = 1ll << 24;
+
+__device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ void mbar_init(uint64_t* b, int c) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(c) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t n) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(n) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t par) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(su32(b)), "r"(par)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t par, volatile int* abort_flag) {
+    for (long long i = 0; i < SPIN_LIMIT; ++i) {
+        if (mbar_try(b, par)) return true;
+        if ((i & 255) == 255 && *abort_flag) return false;
+    }
+    return false;
+}
+__device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* m, uint64_t* bar, int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+            su32(dst)),
+        "l"((uint64_t)m), "r"(su32(bar)), "r"(c0), "r"(c1)
+        : "memory");
+}
+__device__ __forceinline__ void tma_3d(void* dst, const CUtensorMap* m, uint64_t* bar, int c0, int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(
+            su32(dst)),
+        "l"((uint64_t)m), "r"(su32(bar)), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+// K-major operand, 128-byte swizzle: rows of 128 B, 8-row groups 1024 B apart.
+__device__ __forceinline__ uint64_t desc_k(uint32_t a) {
+    return (uint64_t)((a & 0x3FFFF) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// MN-major operand (V as B of P.V), 128-byte swizzle: each key row holds 64 d values
+// (128 B); 8-key groups 1024 B apart (stride byte offset); the second 64-wide d half
+// 8 KB further (leading byte offset).
+__device__ __forceinline__ uint64_t desc_mn(uint32_t a) {
+    return (uint64_t)((a & 0x3FFFF) >> 4) | ((uint64_t)(KH_BYTES >> 4) << 16) |
+           ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+constexpr uint32_t IDESC_S = (1u << 4) | (1u << 7) | (1u << 10) | ((BKV >> 3) << 17) | ((BQ >> 4) << 24);
+constexpr uint32_t IDESC_PV =
+    (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) /* B MN-major */ | ((D >> 3) << 17) | ((BQ >> 4) << 24);
+
+__device__ __forceinline__ void umma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+__device__ __forceinline__ void commit(uint64_t* b) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(b))
+                 : "memory");
+}
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+#define TMEM_LD32(taddr, r)                                                                          \
+    asm volatile(                                                                                    \
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"   \
+        "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"             \
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),     \
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),   \
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),             \
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),             \
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])              \
+        : "r"(taddr))
+
+struct Tile {
+    int g, row0, pair0, npairs, max_pos, tok_base, nblk;
+};
+
+// Work item w -> tile.  Items of request r: hkv * ceil(rows_r * group / 128), the
+// tiles with the largest positions (the longest KV ranges) first.
+__device__ __forceinline__ bool get_tile(int w, int n_req, const int32_t* req_row_end, const int32_t* row_pos,
+                                         const int32_t* row_tok, int group, int hkv, Tile& t) {
+    int row0 = 0;
+    for (int r = 0; r < n_req; ++r) {
+        const int row1 = req_row_end[r];
+        const int np = (row1 - row0) * group;
+        const int tiles = (np + BQ - 1) / BQ;
+        if (w < tiles * hkv) {
+            const int ti = tiles - 1 - w / hkv;
+            t.g = w % hkv;
+            t.row0 = row0;
+            t.pair0 = ti * BQ;
+            t.npairs = np;
+            const int last = min(t.pair0 + BQ, np) - 1;
+            const int lrow = row0 + last / group;
+            t.max_pos = row_pos[lrow];
+            t.tok_base = row_tok[lrow] - t.max_pos;
+            t.nblk = t.max_pos / BKV + 1;
+            return true;
+        }
+        w -= tiles * hkv;
+        row0 = row1;
+    }
+    return false;
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
+              const __grid_constant__ CUtensorMap mapV, int n_req, const int32_t* __restrict__ req_row_end,
+              const int32_t* __restrict__ row_pos, const int32_t* __restrict__ row_tok, int group, int hkv,
+              int m_cap, float scale_log2, bf16* __restrict__ out, int32_t* __restrict__ err) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t q_full, q_empty, kv_full[KV_STAGES], kv_empty[KV_STAGES], s_full[2],
+        s_empty[2], p_full[2], o_full[2], o_empty[2];
+    __shared__ uint32_t tmem_sh;
+    __shared__ volatile int abort_flag;
+    __shared__ int pend_kv[KV_STAGES];
+    __shared__ int pend_q;
+
+    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t* sQ = smem;
+    uint8_t* sKV = smem + Q_BYTES;
+    uint8_t* sP = sKV + KV_STAGES * KV_BYTES;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+    int total = 0;
+    {
+        int row0 = 0;
+        for (int r = 0; r < n_req; ++r) {
+            const int row1 = req_row_end[r];
+            total += hkv * (((row1 - row0) * group + BQ - 1) / BQ);
+            row0 = row1;
+        }
+    }
+    if (threadIdx.x == 0) {
+        mbar_init(&q_full, 1);
+        mbar_init(&q_empty, 1);
+        for (int s = 0; s < KV_STAGES; ++s) {
+            mbar_init(&kv_full[s], 1);
+            mbar_init(&kv_empty[s], 1);
+            pend_kv[s] = -1;
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&s_full[b], 1);
+            mbar_init(&s_empty[b], 128);
+            mbar_init(&p_full[b], 128);
+            mbar_init(&o_full[b], 1);
+            mbar_init(&o_empty[b], 128);
+        }
+        pend_q = -1;
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&tmem_sh)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tb = tmem_sh;
+    const int qslab = m_cap * group;  // pair rows per kv head in q
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------ TMA producer
+        uint32_t it = 0, tl = 0;
+        for (int w = blockIdx.x; w < total && !abort_flag; w += gridDim.x, ++tl) {
+            Tile t;
+            get_tile(w, n_req, req_row_end, row_pos, row_tok, group, hkv, t);
+            if (!mbar_wait(&q_empty, (tl & 1) ^ 1, &abort_flag)) {
+                abort_flag = 1;
+                set_error(err, BLEND_ETIMEOUT);
+                break;
+            }
+            mbar_expect_tx(&q_full, Q_BYTES);
+            pend_q = (int)(tl & 1);
+            const int qrow = t.g * qslab + t.row0 * group + t.pair0;
+            tma_2d(sQ, &mapQ, &q_full, 0, qrow);
+            tma_2d(sQ + Q_BYTES / 2, &mapQ, &q_full, 64, qrow);
+            for (int kb = 0; kb < t.nblk; ++kb, ++it) {
+                const int st = it % KV_STAGES;
+                if (!mbar_wait(&kv_empty[st], ((it / KV_STAGES) & 1) ^ 1, &abort_flag)) {
+                    abort_flag = 1;
+                    set_error(err, BLEND_ETIMEOUT);
+                    break;
+                }
+                uint8_t* b = sKV + st * KV_BYTES;
+                mbar_expect_tx(&kv_full[st], KV_BYTES);
+                pend_kv[st] = (int)((it / KV_STAGES) & 1);
+                const int tok = t.tok_base + kb * BKV;
+                tma_3d(b, &mapK, &kv_full[st], 0, t.g, tok);
+                tma_3d(b + KH_BYTES, &mapK, &kv_full[st], 64, t.g, tok);
+                tma_3d(b + 2 * KH_BYTES, &mapV, &kv_full[st], 0, t.g, tok);
+                tma_3d(b + 3 * KH_BYTES, &mapV, &kv_full[st], 64, t.g, tok);
+            }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------ MMA issuer
+        uint32_t it = 0, tl = 0;
+        auto do_pv = [&](uint32_t j) -> bool {
+            const int pb = j & 1;
+            if (!mbar_wait(&p_full[pb], (j >> 1) & 1, &abort_flag)) return false;
+            if (!mbar_wait(&o_empty[pb], ((j >> 1) & 1) ^ 1, &abort_flag)) return false;
+            fence_after();
+            const uint32_t pa = su32(sP + pb * P_BYTES);
+            const uint32_t va = su32(sKV + (j % KV_STAGES) * KV_BYTES + 2 * KH_BYTES);
+            const uint32_t od = tb + 128 + pb * 128;
+#pragma unroll
+            for (int kk = 0; kk < BKV / 16; ++kk) umma(od, desc_k(pa + kk * 32), desc_mn(va + kk * 2048), IDESC_PV, kk);
+            commit(&o_full[pb]);
+            commit(&kv_empty[j % KV_STAGES]);
+            return true;
+        };
+        bool ok = true;
+        for (int w = blockIdx.x; w < total && ok && !abort_flag; w += gridDim.x, ++tl) {
+            Tile t;
+            get_tile(w, n_req, req_row_end, row_pos, row_tok, group, hkv, t);
+            if (!mbar_wait(&q_full, tl & 1, &abort_flag)) {
+                ok = false;
+                break;
+            }
+            pend_q = -1;
+            fence_after();
+            const uint32_t qa = su32(sQ);
+            for (int kb = 0; kb < t.nblk; ++kb, ++it) {
+                const int st = it % KV_STAGES;
+                const int sb = it & 1;
+                if (!mbar_wait(&kv_full[st], (it / KV_STAGES) & 1, &abort_flag) ||
+                    !mbar_wait(&s_empty[sb], ((it >> 1) & 1) ^ 1, &abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                pend_kv[st] = -1;
+                fence_after();
+                const uint32_t ka = su32(sKV + st * KV_BYTES);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk & 3) * 32;
+                    const uint32_t half = (kk >> 2);
+                    umma(tb + sb * 64, desc_k(qa + half * (Q_BYTES / 2) + off), desc_k(ka + half * KH_BYTES + off),
+                         IDESC_S, kk);
+                }
+                commit(&s_full[sb]);
+                if (kb > 0 && !do_pv(it - 1)) {
+                    ok = false;
+                    break;
+                }
+            }
+            if (!ok || !do_pv(it - 1)) {
+                ok = false;
+                break;
+            }
+            commit(&q_empty);
+        }
+        if (!ok) {
+            abort_flag = 1;
+            set_error(err, BLEND_ETIMEOUT);
+        }
+    } else if (warp >= 2) {
+        // ------------------------------------------------ softmax + output
+        const int sp = warp & 3;
+        const int r_in = sp * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(sp * 32) << 16;
+        uint32_t it = 0;
+        bool ok = true;
+        for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+            Tile t;
+            get_tile(w, n_req, req_row_end, row_pos, row_tok, group, hkv, t);
+            const int p = t.pair0 + r_in;
+            const bool valid = p < t.npairs;
+            const int row = t.row0 + (valid ? p / group : 0);
+            const int my_pos = valid ? row_pos[row] : t.max_pos;
+            float o[D];
+#pragma unroll
+            for (int c = 0; c < D; ++c) o[c] = 0.f;
+            float m = -INFINITY, l = 0.f, corr_prev = 0.f;
+            auto accumulate = [&](uint32_t j, float c) -> bool {
+                const int ob = j & 1;
+                if (!__all_sync(0xffffffffu, mbar_wait(&o_full[ob], (j >> 1) & 1, &abort_flag))) return false;
+                fence_after();
+#pragma unroll
+                for (int cc = 0; cc < D; cc += 32) {
+                    uint32_t v[32];
+                    TMEM_LD32(tb + lane_off + 128 + ob * 128 + cc, v);
+                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[cc + i] = fmaf(o[cc + i], c, __uint_as_float(v[i]));
+                }
+                fence_before();
+                mbar_arrive(&o_empty[ob]);
+                return true;
+            };
+            for (int kb = 0; kb < t.nblk; ++kb, ++it) {
+                const int sb = it & 1;
+                if (!__all_sync(0xffffffffu, mbar_wait(&s_full[sb], (it >> 1) & 1, &abort_flag))) {
+                    ok = false;
+                    break;
+                }
+                fence_after();
+                uint32_t s0[32], s1[32];
+                TMEM_LD32(tb + lane_off + sb * 64, s0);
+                TMEM_LD32(tb + lane_off + sb * 64 + 32, s1);
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                fence_before();
+                mbar_arrive(&s_empty[sb]);
+                const int k0 = kb * BKV;
+                float mx = m;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    float a = k0 + i <= my_pos ? __uint_as_float(s0[i]) * scale_log2 : -INFINITY;
+                    float b2 = k0 + 32 + i <= my_pos ? __uint_as_float(s1[i]) * scale_log2 : -INFINITY;
+                    s0[i] = __float_as_uint(a);
+                    s1[i] = __float_as_uint(b2);
+                    mx = fmaxf(mx, fmaxf(a, b2));
+                }
+                const float corr = ex2(m - mx);
+                float sum = 0.f;
+                // P row r_in: 8 chunks of 8 keys, chunk c stored at chunk slot c ^ (r_in & 7)
+                uint8_t* prow = sP + sb * P_BYTES + r_in * 128;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    __align__(16) bf16 h[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int i = c * 8 + e;
+                        const float sv = __uint_as_float(i < 32 ? s0[i] : s1[i - 32]);
+                        const float pv = ex2(sv - mx);
+                        sum += pv;
+                        h[e] = __float2bfloat16_rn(pv);
+                    }
+                    *reinterpret_cast<uint4*>(prow + ((c ^ (r_in & 7)) * 16)) = *reinterpret_cast<const uint4*>(h);
+                }
+                l = l * corr + sum;
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                mbar_arrive(&p_full[sb]);
+                if (kb > 0 && !accumulate(it - 1, corr_prev)) {
+                    ok = false;
+                    break;
+                }
+                corr_prev = corr;
+                m = mx;
+            }
+            if (!ok || !accumulate(it - 1, corr_prev)) {
+                ok = false;
+                break;
+            }
+            if (valid) {
+                const int j = p % group;
+                const float inv = 1.f / l;
+                bf16* dst = out + (long long)row * (hkv * group * D) + (long long)(t.g * group + j) * D;
+#pragma unroll
+                for (int c = 0; c < D; c += 8) {
+                    __align__(16) bf16 h[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) h[e] = __float2bfloat16_rn(o[c + e] * inv);
+                    *reinterpret_cast<uint4*>(dst + c) = *reinterpret_cast<const uint4*>(h);
+                }
+            }
+        }
+        if (!ok) {
+            abort_flag = 1;
+            if (lane == 0) set_error(err, BLEND_ETIMEOUT);
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && abort_flag) {
+        // let every load still in flight land before the shared memory is released
+        for (int s = 0; s < KV_STAGES; ++s)
+            if (pend_kv[s] >= 0)
+                for (long long i = 0; i < SPIN_LIMIT && !mbar_try(&kv_full[s], (uint32_t)pend_kv[s]); ++i) {
+                }
+        if (pend_q >= 0)
+            for (long long i = 0; i < SPIN_LIMIT && !mbar_try(&q_full, (uint32_t)pend_q); ++i) {
+            }
+    }
+    __syncthreads();
+    if (warp == 1) {
+        fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tb), "r"(TMEM_COLS) : "memory");
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_enc = nullptr;
+int g_sms = 0;
+
+bool encode(CUtensorMap* map, int rank, const void* base, const cuuint64_t* dims, const cuuint64_t* strides,
+            const cuuint32_t* box) {
+    cuuint32_t es[3] = {1, 1, 1};
+    return g_enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box, es,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool tc_attn_supported(int head_dim) { return head_dim == D && tc_available(); }
+
+int launch_attn_tc(const void* q, int m_cap, int n_req, const int32_t* req_row_end, const int32_t* row_pos,
+                   const int32_t* row_tok, int M_max, const void* k_cache, const void* v_cache, long long n_tokens,
+                   void* o, int hq, int hkv, int32_t* err, cudaStream_t s) {
+    if (M_max <= 0) return BLEND_OK;
+    if (!g_enc) {
+        cudaDriverEntryPointQueryResult qr;
+        void* fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &qr) !=
+                cudaSuccess ||
+            qr != cudaDriverEntryPointSuccess || !fn)
+            return BLEND_EUNSUPPORTED;
+        g_enc = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaFuncSetAttribute(k_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    }
+    const int group = hq / hkv;
+    CUtensorMap mq, mk, mv;
+    cuuint64_t qd[2] = {(cuuint64_t)D, (cuuint64_t)hkv * m_cap * group};
+    cuuint64_t qs[1] = {(cuuint64_t)D * 2};
+    cuuint32_t qb[2] = {64, BQ};
+    cuuint64_t kd[3] = {(cuuint64_t)D, (cuuint64_t)hkv, (cuuint64_t)n_tokens};
+    cuuint64_t ks[2] = {(cuuint64_t)D * 2, (cuuint64_t)hkv * D * 2};
+    cuuint32_t kbx[3] = {64, 1, BKV};
+    if (!encode(&mq, 2, q, qd, qs, qb) || !encode(&mk, 3, k_cache, kd, ks, kbx) || !encode(&mv, 3, v_cache, kd, ks, kbx))
+        return BLEND_EUNSUPPORTED;
+    const long long items = (long long)hkv * ((((long long)M_max * group) + BQ - 1) / BQ + n_req);
+    const int grid = (int)(items < g_sms ? items : g_sms);
+    const float scale_log2 = (float)(1.4426950408889634 / 11.313708498984761);  // log2(e) / sqrt(128)
+    k_attn_tc<<<grid, THREADS, SMEM_BYTES, s>>>(mq, mk, mv, n_req, req_row_end, row_pos, row_tok, group, hkv,
+                                                m_cap, scale_log2, (bf16*)o, err);
+    note_launch(1);
+    return BLEND_OK;
+}
+
+}  // namespace blend

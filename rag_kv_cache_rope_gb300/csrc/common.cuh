@@ -130,7 +130,7 @@ void launch_gather(const void* src, long long row_bytes, const int32_t* idx, con
                    int max_n, void* dst, cudaStream_t s);
 void launch_rope_qkv(int dtype, const float* qkv, const int32_t* row_pos, const int32_t* row_tok,
                      const int32_t* row_req, const int32_t* M_dev, int M_max, const BatchDesc& bd,
-                     int hq, int hkv, int d, const float2* tab, void* q_out, void* k_cache,
+                     int hq, int hkv, int d, int m_cap, const float2* tab, void* q_out, void* k_cache,
                      void* v_cache, float* dev_out, int dev_mode, int dev_by_row, cudaStream_t s);
 void launch_deviation(int dtype, const void* k_new, const void* v_new, const void* k_cache,
                       const void* v_cache, const int32_t* pos, const int32_t* n_dev, int max_rows,
@@ -182,7 +182,8 @@ void launch_gemm_simt(int dtype, const void* A, int lda, const void* B, int ldb,
                       const int32_t* M_dev, int M_max, int epi, void* C, int ldc, cudaStream_t s);
 
 // ------------------------------ attention (attn_simt.cu) ---------------------------
-void launch_attn_simt(int dtype, const void* q, const int32_t* row_pos, const int32_t* row_tok,
+// q: per kv head g a slab [m_cap][group][d]; o: [M][hq*d].
+void launch_attn_simt(int dtype, const void* q, int m_cap, const int32_t* row_pos, const int32_t* row_tok,
                       const int32_t* M_dev, int M_max, const void* k_cache, const void* v_cache,
                       void* o, int hq, int hkv, int d, cudaStream_t s);
 

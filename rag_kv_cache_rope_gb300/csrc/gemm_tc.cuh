@@ -14,4 +14,11 @@ bool tc_gemm_supported(int K, int N, int epi, int ldc, int M_cap);
 // Returns BLEND_OK or BLEND_EUNSUPPORTED (operands not describable by a tensor map).
 int launch_gemm_tc(const void* A, int K, int M_cap, const void* B, int N, const int32_t* M_dev, int M_max,
                    int epi, void* C, int ldc, int32_t* err, cudaStream_t s);
+// Tensor-core attention (attn_tc.cu): head_dim 128, bf16.
+bool tc_attn_supported(int head_dim);
+// q: per kv head a slab [m_cap][group][128]; rows of request r are
+// req_row_end[r-1]..req_row_end[r]-1 (device); caches: this layer's [n_tokens][hkv][128].
+int launch_attn_tc(const void* q, int m_cap, int n_req, const int32_t* req_row_end, const int32_t* row_pos,
+                   const int32_t* row_tok, int M_max, const void* k_cache, const void* v_cache, long long n_tokens,
+                   void* o, int hq, int hkv, int32_t* err, cudaStream_t s);
 }  // namespace blend

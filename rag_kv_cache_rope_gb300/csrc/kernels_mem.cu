@@ -327,7 +327,7 @@ __global__ void __launch_bounds__(256)
     k_rope_qkv(const float* __restrict__ qkv, const int32_t* __restrict__ row_pos,
                const int32_t* __restrict__ row_tok, const int32_t* __restrict__ row_req,
                const int32_t* M_dev, const __grid_constant__ BatchDesc bd, int hq, int hkv, int d,
-               const float2* __restrict__ tab, T* __restrict__ q_out, T* __restrict__ kc,
+               int m_cap, const float2* __restrict__ tab, T* __restrict__ q_out, T* __restrict__ kc,
                T* __restrict__ vc, float* __restrict__ dev_out, int dev_mode, int dev_by_row) {
     __shared__ float red[256];
     const int row = blockIdx.x;
@@ -338,13 +338,15 @@ __global__ void __launch_bounds__(256)
     const int width = (hq + 2 * hkv) * d;
     const float* src = qkv + (long long)row * width;
     const float2* cs = tab + (long long)pos * half;
-    T* qo = q_out + (long long)row * hq * d;
+    // q layout: per kv head g a slab of [m_cap rows][group][d] (pair = row * group + j)
+    const int group = hq / hkv;
     for (int j = threadIdx.x; j < hq * half; j += blockDim.x) {
         int h = j / half, i = j % half;
         float x1 = src[h * d + i], x2 = src[h * d + i + half];
         float2 t = cs[i];
-        qo[h * d + i] = from_f<T>(x1 * t.x - x2 * t.y);
-        qo[h * d + i + half] = from_f<T>(x2 * t.x + x1 * t.y);
+        T* qo = q_out + (((long long)(h / group) * m_cap + row) * group + (h % group)) * d;
+        qo[i] = from_f<T>(x1 * t.x - x2 * t.y);
+        qo[i + half] = from_f<T>(x2 * t.x + x1 * t.y);
     }
     float acc = 0.f;
     const float* ks = src + hq * d;
@@ -383,16 +385,16 @@ __global__ void __launch_bounds__(256)
 
 void launch_rope_qkv(int dtype, const float* qkv, const int32_t* row_pos, const int32_t* row_tok,
                      const int32_t* row_req, const int32_t* M_dev, int M_max, const BatchDesc& bd,
-                     int hq, int hkv, int d, const float2* tab, void* q_out, void* k_cache,
+                     int hq, int hkv, int d, int m_cap, const float2* tab, void* q_out, void* k_cache,
                      void* v_cache, float* dev_out, int dev_mode, int dev_by_row, cudaStream_t s) {
     if (M_max <= 0) return;
     if (dtype == BLEND_BF16)
         k_rope_qkv<bf16><<<M_max, 256, 0, s>>>(qkv, row_pos, row_tok, row_req, M_dev, bd, hq, hkv,
-                                               d, tab, (bf16*)q_out, (bf16*)k_cache,
+                                               d, m_cap, tab, (bf16*)q_out, (bf16*)k_cache,
                                                (bf16*)v_cache, dev_out, dev_mode, dev_by_row);
     else
         k_rope_qkv<float><<<M_max, 256, 0, s>>>(qkv, row_pos, row_tok, row_req, M_dev, bd, hq, hkv,
-                                                d, tab, (float*)q_out, (float*)k_cache,
+                                                d, m_cap, tab, (float*)q_out, (float*)k_cache,
                                                 (float*)v_cache, dev_out, dev_mode, dev_by_row);
     note_launch(1);
 }

@@ -1,4 +1,5 @@
-"""The tcgen05 tensor-core GEMM path against the oracle and against the CUDA-core path.
+"""The tcgen05 tensor-core path (GEMMs and attention) against the oracle and against the
+CUDA-core path.
 
 One decoder layer through selective_layer with the tensor cores on and off: row
 counts that span several 128-row tiles with a ragged tail, widths that give several
@@ -31,6 +32,8 @@ def built():
 SHAPES = [
     (synth.ModelShape("tc-small", 2, 512, 8, 2, 128, 1024, 300, 1e6), 300, 700),
     (synth.ModelShape("tc-wide", 2, 2048, 16, 4, 128, 5632, 300, 1e6), 1000, 1500),
+    # 5 query heads per kv head (the 14B grouping), contexts spanning ~60 key blocks
+    (synth.ModelShape("tc-gqa5", 2, 1280, 10, 2, 128, 2560, 300, 1e6), 700, 4000),
 ]
 
 
