@@ -45,6 +45,27 @@ except OSError:
     pass
 
 
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
+# capture of each kernel (profiles/), valid only while the kernel's source is unchanged.
+TRAFFIC = {
+    "attention": {"bytes": 140.736768e6 + 17.628416e6, "source": "rag_kv_cache_rope_gb300/csrc/attn_tc.cu",
+                  "sha256_16": "fcb6aa23b2958d4d", "profile": "profiles/attn_tc_qwen14b_16k_layer.md"},
+}
+
+
+def traffic_for(stage: str):
+    import hashlib
+    t = TRAFFIC.get(stage)
+    if not t:
+        return None
+    try:
+        with open(os.path.join(ROOT, t["source"]), "rb") as f:
+            h = hashlib.sha256(f.read()).hexdigest()[:16]
+    except OSError:
+        return None
+    return t["bytes"] if h == t["sha256_16"] else None
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -54,6 +75,8 @@ def parse():
     ap.add_argument("--workload", default="qwen14b-16k-ext20")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="truncate the model to this many layers (profiling captures only; not a headline)")
     ap.add_argument("--full-prefill-steps", type=int, default=0,
                     help="also time full prefill of the same input (every row recomputed)")
     return ap.parse_args()
@@ -249,12 +272,12 @@ def run_ours(args, wl, rank, world):
             peak = PEAKS["bf16_tflops_sustained"] if sh.dtype == "bf16" else None
             ach = units / (avg_ms / 1e3) / 1e12
             roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
-                    "frac": (ach / peak) if peak else None, "traffic": None,
+                    "frac": (ach / peak) if peak else None, "traffic": traffic_for(dom),
                     "peak_source": f"{PEAKS_SRC} bf16 sustained", "avg_launch_ms": avg_ms}
         else:
             ach = units / (avg_ms / 1e3) / 1e9
             roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": PEAKS["hbm_gbs"], "unit": "GB/s",
-                    "frac": ach / PEAKS["hbm_gbs"], "traffic": None, "peak_source": f"{PEAKS_SRC} hbm",
+                    "frac": ach / PEAKS["hbm_gbs"], "traffic": traffic_for(dom), "peak_source": f"{PEAKS_SRC} hbm",
                     "avg_launch_ms": avg_ms}
     stages = {k: {"ms_per_step": v[0] / args.steps, "share": v[0] / total, "launches": v[1]}
               for k, v in prof.items() if v[1]}
@@ -413,6 +436,9 @@ def run_reference(args, wl, rank, world):
 def main():
     args = parse()
     wl = workload(args.workload)
+    if args.layers:
+        wl = dataclasses.replace(wl, name=f"{wl.name}-{args.layers}L",
+                                 model=dataclasses.replace(wl.model, n_layers=args.layers))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":

@@ -185,6 +185,7 @@ bool cfg_ok(const blend_model_cfg* c, std::string* why) {
     }
     if (c->head_dim != 64 && c->head_dim != 128) { *why = "head_dim must be 64 or 128"; return false; }
     if (c->n_q_heads / c->n_kv_heads > 32) { *why = "more than 32 query heads per kv head"; return false; }
+    if (c->hidden > 8192) { *why = "hidden size above 8192"; return false; }
     return true;
 }
 

@@ -204,33 +204,77 @@ void launch_tokens(const SegTable& segs, const QueryTable& qt, const int32_t* po
 }
 
 // ---------------------------------------------------------------- RMSNorm
-// out[row] = x[row] / sqrt(mean(x^2) + eps) * g, x fp32, out in the model dtype.
+// out[row] = x[row] / sqrt(mean(x^2) + eps) * g, x fp32, out in the model dtype.  One
+// CTA per row; the row stays in registers (float4, up to RMS_V per thread) between the
+// sum of squares and the scaling, so x is read once.  The block sum is a fixed-order
+// shuffle tree plus a fixed-order sum of the warp partials (bitwise reproducible).
+constexpr int RMS_THREADS = 256;
+constexpr int RMS_V = 8;  // H <= 4 * RMS_V * RMS_THREADS = 8192
+
+__device__ __forceinline__ float block_sum_fast(float v, float* warp_part) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    const int w = threadIdx.x / 32;
+    if ((threadIdx.x & 31) == 0) warp_part[w] = v;
+    __syncthreads();
+    float r = 0.f;
+    for (int i = 0; i < (int)(blockDim.x / 32); ++i) r += warp_part[i];
+    return r;
+}
+
 template <typename T>
-__global__ void __launch_bounds__(256) k_rmsnorm(const float* __restrict__ x, const T* __restrict__ g,
-                                                 T* __restrict__ out, int H, float eps,
-                                                 const int32_t* M_dev) {
-    __shared__ float red[256];
+__device__ __forceinline__ void store4(T* p, float a, float b, float c, float d);
+template <>
+__device__ __forceinline__ void store4<float>(float* p, float a, float b, float c, float d) {
+    *reinterpret_cast<float4*>(p) = make_float4(a, b, c, d);
+}
+template <>
+__device__ __forceinline__ void store4<bf16>(bf16* p, float a, float b, float c, float d) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(a, b), hi = __floats2bfloat162_rn(c, d);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&lo);
+    u.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(p) = u;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(RMS_THREADS)
+    k_rmsnorm(const float* __restrict__ x, const T* __restrict__ g, T* __restrict__ out, int H, float eps,
+              const int32_t* M_dev) {
+    __shared__ float part[RMS_THREADS / 32];
     const int row = blockIdx.x;
     if (row >= *M_dev) return;
-    const float* xr = x + (long long)row * H;
+    const float4* xr = reinterpret_cast<const float4*>(x + (long long)row * H);
+    const int nv = H / 4;
+    float4 v[RMS_V];
     float ss = 0.f;
-    for (int j = threadIdx.x; j < H; j += blockDim.x) {
-        float v = xr[j];
-        ss += v * v;
+#pragma unroll
+    for (int k = 0; k < RMS_V; ++k) {
+        const int i = threadIdx.x + k * RMS_THREADS;
+        v[k] = i < nv ? xr[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+        ss += v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z + v[k].w * v[k].w;
     }
-    ss = block_sum(ss, red);
+    ss = block_sum_fast(ss, part);
     const float r = rsqrtf(ss / (float)H + eps);
     T* o = out + (long long)row * H;
-    for (int j = threadIdx.x; j < H; j += blockDim.x) o[j] = from_f<T>(xr[j] * r * to_f<T>(g[j]));
+#pragma unroll
+    for (int k = 0; k < RMS_V; ++k) {
+        const int i = threadIdx.x + k * RMS_THREADS;
+        if (i < nv) {
+            const int c = 4 * i;
+            store4<T>(o + c, v[k].x * r * to_f<T>(g[c]), v[k].y * r * to_f<T>(g[c + 1]),
+                      v[k].z * r * to_f<T>(g[c + 2]), v[k].w * r * to_f<T>(g[c + 3]));
+        }
+    }
 }
 
 void launch_rmsnorm(int dtype, const float* x, const void* g, void* out, int H, float eps,
                     const int32_t* M_dev, int M_max, cudaStream_t s) {
     if (M_max <= 0) return;
     if (dtype == BLEND_BF16)
-        k_rmsnorm<bf16><<<M_max, 256, 0, s>>>(x, (const bf16*)g, (bf16*)out, H, eps, M_dev);
+        k_rmsnorm<bf16><<<M_max, RMS_THREADS, 0, s>>>(x, (const bf16*)g, (bf16*)out, H, eps, M_dev);
     else
-        k_rmsnorm<float><<<M_max, 256, 0, s>>>(x, (const float*)g, (float*)out, H, eps, M_dev);
+        k_rmsnorm<float><<<M_max, RMS_THREADS, 0, s>>>(x, (const float*)g, (float*)out, H, eps, M_dev);
     note_launch(1);
 }
 
