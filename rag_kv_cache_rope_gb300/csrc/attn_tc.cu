@@ -2,19 +2,24 @@
 // (CacheBlend blog, "Selective KV recompute": only the selected rows' attention rows
 // are computed, each over every earlier token, reused or fresh).
 //
-// Work item: one kv head g and 128 consecutive (row, head-of-group) pairs of one
-// request (q is stored per kv head as [pair][d], pair = row * group + j, so a tile is
-// one TMA box and each K/V block is shared by the whole head group).  Items run
-// longest first on persistent CTAs.  Per 64-key block:
-//   S  = Q . K^T      tcgen05.mma M128 N64 K16 x8  -> TMEM (two buffers)
-//   P  = softmax part  4 warps, one pair row per thread: mask keys past the row's
-//                      position, online max/sum in base 2, bf16 P into swizzled smem
-//   PV = P . V        tcgen05.mma M128 N128 K16 x4 (V as an MN-major operand) -> TMEM
-//   O  = O * c + PV   in the softmax threads' registers, one block behind, so the
-//                      tensor core computes S of block j+1 and PV of block j while the
-//                      threads work on block j+1.
-// Warps: 0 TMA producer, 1 TMEM owner + MMA issuer, 2..5 softmax + output.
-// All mbarrier waits are bounded (error word BLEND_ETIMEOUT, drain, free TMEM).
+// q is stored per kv head as [pair][d] with pair = row * group + j, so 128 consecutive
+// (row, head-of-group) pairs of one kv head form one TMA box and every K/V block is
+// shared by the whole head group.  A work item is two consecutive 128-pair tiles (A
+// and B) of one kv head and one request; items run longest first on persistent CTAs,
+// and the two tiles share every K/V block.  Per 64-key block, for each tile:
+//   S = Q . K^T      tcgen05.mma M128 N64 K16 x8 -> TMEM (two buffers per tile)
+//   P                one softmax warpgroup per tile, one pair row per thread: causal
+//                    mask on boundary blocks, base-2 scores with the scale folded into
+//                    one FFMA, bf16 P written to 128-byte-swizzled shared memory
+//   O += P . V       tcgen05.mma M128 N128 K16 x4, V as an MN-major operand, O kept in
+//                    TMEM for the whole item.
+// The running maximum used for P is raised only when a row's maximum grows by more
+// than 2^8; then that warp rescales its rows of O in TMEM (ld, scale, st) between two
+// P.V products.  The sum l uses the same maximum, so O / l is exact.
+// Warps: 0 TMA producer, 1 TMEM owner + MMA issuer, 2..5 softmax of tile A, 6..9 of
+// tile B.  The tensor core interleaves S_A, S_B, PV_A, PV_B so one tile's softmax
+// overlaps the other tile's products.  All mbarrier waits are bounded (error word
+// BLEND_ETIMEOUT, loads drained, TMEM freed).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -27,13 +32,14 @@ constexpr int D = 128;
 constexpr int BQ = 128;
 constexpr int BKV = 64;
 constexpr int KV_STAGES = 3;
-constexpr int Q_BYTES = BQ * D * 2;   // 32 KB: two 16 KB column halves (d 0-63, 64-127)
-constexpr int KH_BYTES = BKV * 64 * 2;  // 8 KB: one column half of a K or V block
+constexpr int QT_BYTES = BQ * D * 2;    // 32 KB per tile: two 16 KB column halves
+constexpr int KH_BYTES = BKV * 64 * 2;  // 8 KB: one 64-wide column half of a K or V block
 constexpr int KV_BYTES = 4 * KH_BYTES;  // K halves, then V halves
 constexpr int P_BYTES = BQ * BKV * 2;   // 16 KB
-constexpr int SMEM_BYTES = Q_BYTES + KV_STAGES * KV_BYTES + 2 * P_BYTES + 1024;
-constexpr int TMEM_COLS = 512;  // S0 [0,64) S1 [64,128) O0 [128,256) O1 [256,384)
-constexpr int THREADS = 192;
+constexpr int SMEM_BYTES = 2 * QT_BYTES + KV_STAGES * KV_BYTES + 4 * P_BYTES + 1024;
+constexpr int TMEM_COLS = 512;  // tile t: S0 t*256+[0,64), S1 t*256+[64,128), O t*256+[128,256)
+constexpr int THREADS = 320;
+constexpr float RESCALE_LOG2 = 8.f;
 constexpr long long SPIN_LIMIT = 1ll << 24;
 
 __device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -62,6 +68,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t par, volatile in
         if ((i & 255) == 255 && *abort_flag) return false;
     }
     return false;
+}
+// Warp-uniform bounded wait (every lane polls; the warp proceeds only if all saw it).
+__device__ __forceinline__ bool warp_wait(uint64_t* b, uint32_t par, volatile int* abort_flag) {
+    return __all_sync(0xffffffffu, mbar_wait(b, par, abort_flag));
 }
 __device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* m, uint64_t* bar, int c0, int c1) {
     asm volatile(
@@ -122,34 +132,48 @@ __device__ __forceinline__ float ex2(float x) {
           "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),             \
           "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])              \
         : "r"(taddr))
+#define TMEM_ST32(taddr, r)                                                                          \
+    asm volatile(                                                                                    \
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14," \
+        "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),   \
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),      \
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), \
+        "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]),           \
+        "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]),           \
+        "r"(r[30]), "r"(r[31])                                                                       \
+        : "memory")
 
-struct Tile {
-    int g, row0, pair0, npairs, max_pos, tok_base, nblk;
+struct Item {
+    int g, row0, npairs, pair0[2], max_pos, tok_base, nblk;
 };
 
-// Work item w -> tile.  Items of request r: hkv * ceil(rows_r * group / 128), the
-// tiles with the largest positions (the longest KV ranges) first.
-__device__ __forceinline__ bool get_tile(int w, int n_req, const int32_t* req_row_end, const int32_t* row_pos,
-                                         const int32_t* row_tok, int group, int hkv, Tile& t) {
+// Work item w -> two tiles.  Request r has tiles_r = ceil(rows_r * group / 128) tiles per
+// kv head, paired from the top (largest positions, longest KV range) down; items of the
+// first pair of every kv head come first.
+__device__ __forceinline__ bool get_item(int w, int n_req, const int32_t* req_row_end, const int32_t* row_pos,
+                                         const int32_t* row_tok, int group, int hkv, Item& it) {
     int row0 = 0;
     for (int r = 0; r < n_req; ++r) {
         const int row1 = req_row_end[r];
         const int np = (row1 - row0) * group;
         const int tiles = (np + BQ - 1) / BQ;
-        if (w < tiles * hkv) {
-            const int ti = tiles - 1 - w / hkv;
-            t.g = w % hkv;
-            t.row0 = row0;
-            t.pair0 = ti * BQ;
-            t.npairs = np;
-            const int last = min(t.pair0 + BQ, np) - 1;
+        const int items = (tiles + 1) / 2;
+        if (w < items * hkv) {
+            const int ta = tiles - 1 - 2 * (w / hkv);
+            const int tb = ta - 1;
+            it.g = w % hkv;
+            it.row0 = row0;
+            it.npairs = np;
+            it.pair0[0] = ta * BQ;
+            it.pair0[1] = tb >= 0 ? tb * BQ : -1;
+            const int last = min(ta * BQ + BQ, np) - 1;
             const int lrow = row0 + last / group;
-            t.max_pos = row_pos[lrow];
-            t.tok_base = row_tok[lrow] - t.max_pos;
-            t.nblk = t.max_pos / BKV + 1;
+            it.max_pos = row_pos[lrow];
+            it.tok_base = row_tok[lrow] - it.max_pos;
+            it.nblk = it.max_pos / BKV + 1;
             return true;
         }
-        w -= tiles * hkv;
+        w -= items * hkv;
         row0 = row1;
     }
     return false;
@@ -161,17 +185,17 @@ __global__ void __launch_bounds__(THREADS, 1)
               const int32_t* __restrict__ row_pos, const int32_t* __restrict__ row_tok, int group, int hkv,
               int m_cap, float scale_log2, bf16* __restrict__ out, int32_t* __restrict__ err) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t q_full, q_empty, kv_full[KV_STAGES], kv_empty[KV_STAGES], s_full[2],
-        s_empty[2], p_full[2], o_full[2], o_empty[2];
+    __shared__ __align__(8) uint64_t q_full, q_empty, kv_full[KV_STAGES], kv_empty[KV_STAGES], s_full[2][2],
+        s_empty[2][2], p_full[2][2], pv_done[2][2], o_free[2];
     __shared__ uint32_t tmem_sh;
     __shared__ volatile int abort_flag;
     __shared__ int pend_kv[KV_STAGES];
     __shared__ int pend_q;
 
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    uint8_t* sQ = smem;
-    uint8_t* sKV = smem + Q_BYTES;
-    uint8_t* sP = sKV + KV_STAGES * KV_BYTES;
+    uint8_t* sQ = smem;                               // tile t at t * QT_BYTES
+    uint8_t* sKV = smem + 2 * QT_BYTES;               // stage s at s * KV_BYTES
+    uint8_t* sP = sKV + KV_STAGES * KV_BYTES;         // tile t, buffer b at (2t + b) * P_BYTES
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
     int total = 0;
@@ -179,7 +203,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         int row0 = 0;
         for (int r = 0; r < n_req; ++r) {
             const int row1 = req_row_end[r];
-            total += hkv * (((row1 - row0) * group + BQ - 1) / BQ);
+            const int tiles = ((row1 - row0) * group + BQ - 1) / BQ;
+            total += hkv * ((tiles + 1) / 2);
             row0 = row1;
         }
     }
@@ -191,12 +216,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(&kv_empty[s], 1);
             pend_kv[s] = -1;
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&s_full[b], 1);
-            mbar_init(&s_empty[b], 128);
-            mbar_init(&p_full[b], 128);
-            mbar_init(&o_full[b], 1);
-            mbar_init(&o_empty[b], 128);
+        for (int t = 0; t < 2; ++t) {
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(&s_full[t][b], 1);
+                mbar_init(&s_empty[t][b], 128);
+                mbar_init(&p_full[t][b], 128);
+                mbar_init(&pv_done[t][b], 1);
+            }
+            mbar_init(&o_free[t], 128);
         }
         pend_q = -1;
         abort_flag = 0;
@@ -219,19 +246,23 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ------------------------------------------------ TMA producer
         uint32_t it = 0, tl = 0;
         for (int w = blockIdx.x; w < total && !abort_flag; w += gridDim.x, ++tl) {
-            Tile t;
-            get_tile(w, n_req, req_row_end, row_pos, row_tok, group, hkv, t);
+            Item m;
+            get_item(w, n_req, req_row_end, row_pos, row_tok, group, hkv, m);
             if (!mbar_wait(&q_empty, (tl & 1) ^ 1, &abort_flag)) {
                 abort_flag = 1;
                 set_error(err, BLEND_ETIMEOUT);
                 break;
             }
-            mbar_expect_tx(&q_full, Q_BYTES);
+            mbar_expect_tx(&q_full, 2 * QT_BYTES);
             pend_q = (int)(tl & 1);
-            const int qrow = t.g * qslab + t.row0 * group + t.pair0;
-            tma_2d(sQ, &mapQ, &q_full, 0, qrow);
-            tma_2d(sQ + Q_BYTES / 2, &mapQ, &q_full, 64, qrow);
-            for (int kb = 0; kb < t.nblk; ++kb, ++it) {
+            for (int t = 0; t < 2; ++t) {
+                // an absent second tile reloads the first (finite data, never stored)
+                const int p0 = m.pair0[t] >= 0 ? m.pair0[t] : m.pair0[0];
+                const int qrow = m.g * qslab + m.row0 * group + p0;
+                tma_2d(sQ + t * QT_BYTES, &mapQ, &q_full, 0, qrow);
+                tma_2d(sQ + t * QT_BYTES + QT_BYTES / 2, &mapQ, &q_full, 64, qrow);
+            }
+            for (int kb = 0; kb < m.nblk; ++kb, ++it) {
                 const int st = it % KV_STAGES;
                 if (!mbar_wait(&kv_empty[st], ((it / KV_STAGES) & 1) ^ 1, &abort_flag)) {
                     abort_flag = 1;
@@ -241,66 +272,70 @@ __global__ void __launch_bounds__(THREADS, 1)
                 uint8_t* b = sKV + st * KV_BYTES;
                 mbar_expect_tx(&kv_full[st], KV_BYTES);
                 pend_kv[st] = (int)((it / KV_STAGES) & 1);
-                const int tok = t.tok_base + kb * BKV;
-                tma_3d(b, &mapK, &kv_full[st], 0, t.g, tok);
-                tma_3d(b + KH_BYTES, &mapK, &kv_full[st], 64, t.g, tok);
-                tma_3d(b + 2 * KH_BYTES, &mapV, &kv_full[st], 0, t.g, tok);
-                tma_3d(b + 3 * KH_BYTES, &mapV, &kv_full[st], 64, t.g, tok);
+                const int tok = m.tok_base + kb * BKV;
+                tma_3d(b, &mapK, &kv_full[st], 0, m.g, tok);
+                tma_3d(b + KH_BYTES, &mapK, &kv_full[st], 64, m.g, tok);
+                tma_3d(b + 2 * KH_BYTES, &mapV, &kv_full[st], 0, m.g, tok);
+                tma_3d(b + 3 * KH_BYTES, &mapV, &kv_full[st], 64, m.g, tok);
             }
         }
     } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------ MMA issuer
         uint32_t it = 0, tl = 0;
-        auto do_pv = [&](uint32_t j) -> bool {
-            const int pb = j & 1;
-            if (!mbar_wait(&p_full[pb], (j >> 1) & 1, &abort_flag)) return false;
-            if (!mbar_wait(&o_empty[pb], ((j >> 1) & 1) ^ 1, &abort_flag)) return false;
-            fence_after();
-            const uint32_t pa = su32(sP + pb * P_BYTES);
+        bool ok = true;
+        // P.V of global block j (local block index kb) for both tiles, then release its K/V stage
+        auto pv = [&](uint32_t j, int kb) -> bool {
             const uint32_t va = su32(sKV + (j % KV_STAGES) * KV_BYTES + 2 * KH_BYTES);
-            const uint32_t od = tb + 128 + pb * 128;
+            for (int t = 0; t < 2; ++t) {
+                if (!mbar_wait(&p_full[t][j & 1], (j >> 1) & 1, &abort_flag)) return false;
+                if (kb == 0 && !mbar_wait(&o_free[t], (tl & 1) ^ 1, &abort_flag)) return false;
+                fence_after();
+                const uint32_t pa = su32(sP + (2 * t + (j & 1)) * P_BYTES);
+                const uint32_t od = tb + t * 256 + 128;
 #pragma unroll
-            for (int kk = 0; kk < BKV / 16; ++kk) umma(od, desc_k(pa + kk * 32), desc_mn(va + kk * 2048), IDESC_PV, kk);
-            commit(&o_full[pb]);
+                for (int kk = 0; kk < BKV / 16; ++kk)
+                    umma(od, desc_k(pa + kk * 32), desc_mn(va + kk * 2048), IDESC_PV, (kb > 0 || kk > 0) ? 1u : 0u);
+                commit(&pv_done[t][j & 1]);
+            }
             commit(&kv_empty[j % KV_STAGES]);
             return true;
         };
-        bool ok = true;
         for (int w = blockIdx.x; w < total && ok && !abort_flag; w += gridDim.x, ++tl) {
-            Tile t;
-            get_tile(w, n_req, req_row_end, row_pos, row_tok, group, hkv, t);
+            Item m;
+            get_item(w, n_req, req_row_end, row_pos, row_tok, group, hkv, m);
             if (!mbar_wait(&q_full, tl & 1, &abort_flag)) {
                 ok = false;
                 break;
             }
             pend_q = -1;
             fence_after();
-            const uint32_t qa = su32(sQ);
-            for (int kb = 0; kb < t.nblk; ++kb, ++it) {
+            for (int kb = 0; kb < m.nblk && ok; ++kb, ++it) {
                 const int st = it % KV_STAGES;
-                const int sb = it & 1;
-                if (!mbar_wait(&kv_full[st], (it / KV_STAGES) & 1, &abort_flag) ||
-                    !mbar_wait(&s_empty[sb], ((it >> 1) & 1) ^ 1, &abort_flag)) {
+                if (!mbar_wait(&kv_full[st], (it / KV_STAGES) & 1, &abort_flag)) {
                     ok = false;
                     break;
                 }
                 pend_kv[st] = -1;
-                fence_after();
                 const uint32_t ka = su32(sKV + st * KV_BYTES);
+                for (int t = 0; t < 2; ++t) {
+                    if (!mbar_wait(&s_empty[t][it & 1], ((it >> 1) & 1) ^ 1, &abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_after();
+                    const uint32_t qa = su32(sQ + t * QT_BYTES);
+                    const uint32_t sd = tb + t * 256 + (it & 1) * 64;
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk & 3) * 32;
-                    const uint32_t half = (kk >> 2);
-                    umma(tb + sb * 64, desc_k(qa + half * (Q_BYTES / 2) + off), desc_k(ka + half * KH_BYTES + off),
-                         IDESC_S, kk);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk & 3) * 32, half = kk >> 2;
+                        umma(sd, desc_k(qa + half * (QT_BYTES / 2) + off), desc_k(ka + half * KH_BYTES + off), IDESC_S,
+                             kk > 0 ? 1u : 0u);
+                    }
+                    commit(&s_full[t][it & 1]);
                 }
-                commit(&s_full[sb]);
-                if (kb > 0 && !do_pv(it - 1)) {
-                    ok = false;
-                    break;
-                }
+                if (ok && kb > 0 && !pv(it - 1, kb - 1)) ok = false;
             }
-            if (!ok || !do_pv(it - 1)) {
+            if (!ok || !pv(it - 1, m.nblk - 1)) {
                 ok = false;
                 break;
             }
@@ -311,105 +346,126 @@ __global__ void __launch_bounds__(THREADS, 1)
             set_error(err, BLEND_ETIMEOUT);
         }
     } else if (warp >= 2) {
-        // ------------------------------------------------ softmax + output
-        const int sp = warp & 3;
+        // ------------------------------------------------ softmax (tile t) + output
+        const int t = (warp - 2) / 4;
+        const int sp = warp & 3;  // TMEM lane quarter of this warp
         const int r_in = sp * 32 + lane;
         const uint32_t lane_off = (uint32_t)(sp * 32) << 16;
+        const uint32_t s_col = tb + lane_off + t * 256;
+        const uint32_t o_col = s_col + 128;
+        uint8_t* prow_base = sP + 2 * t * P_BYTES + r_in * 128;
         uint32_t it = 0;
         bool ok = true;
         for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
-            Tile t;
-            get_tile(w, n_req, req_row_end, row_pos, row_tok, group, hkv, t);
-            const int p = t.pair0 + r_in;
-            const bool valid = p < t.npairs;
-            const int row = t.row0 + (valid ? p / group : 0);
-            const int my_pos = valid ? row_pos[row] : t.max_pos;
-            float o[D];
-#pragma unroll
-            for (int c = 0; c < D; ++c) o[c] = 0.f;
-            float m = -INFINITY, l = 0.f, corr_prev = 0.f;
-            auto accumulate = [&](uint32_t j, float c) -> bool {
-                const int ob = j & 1;
-                if (!__all_sync(0xffffffffu, mbar_wait(&o_full[ob], (j >> 1) & 1, &abort_flag))) return false;
-                fence_after();
-#pragma unroll
-                for (int cc = 0; cc < D; cc += 32) {
-                    uint32_t v[32];
-                    TMEM_LD32(tb + lane_off + 128 + ob * 128 + cc, v);
-                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) o[cc + i] = fmaf(o[cc + i], c, __uint_as_float(v[i]));
-                }
-                fence_before();
-                mbar_arrive(&o_empty[ob]);
-                return true;
-            };
-            for (int kb = 0; kb < t.nblk; ++kb, ++it) {
-                const int sb = it & 1;
-                if (!__all_sync(0xffffffffu, mbar_wait(&s_full[sb], (it >> 1) & 1, &abort_flag))) {
+            Item m;
+            get_item(w, n_req, req_row_end, row_pos, row_tok, group, hkv, m);
+            const bool have = m.pair0[t] >= 0;
+            const int p = (have ? m.pair0[t] : 0) + r_in;
+            const bool valid = have && p < m.npairs;
+            const int row = m.row0 + (valid ? p / group : 0);
+            const int my_pos = valid ? row_pos[row] : m.max_pos;
+            float m_used = -INFINITY, l = 0.f;
+            for (int kb = 0; kb < m.nblk; ++kb, ++it) {
+                const int b = it & 1;
+                if (!warp_wait(&s_full[t][b], (it >> 1) & 1, &abort_flag)) {
                     ok = false;
                     break;
                 }
                 fence_after();
-                uint32_t s0[32], s1[32];
-                TMEM_LD32(tb + lane_off + sb * 64, s0);
-                TMEM_LD32(tb + lane_off + sb * 64 + 32, s1);
+                uint32_t s[64];
+                TMEM_LD32(s_col + b * 64, s);
+                TMEM_LD32(s_col + b * 64 + 32, (s + 32));
                 asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
                 fence_before();
-                mbar_arrive(&s_empty[sb]);
+                mbar_arrive(&s_empty[t][b]);
                 const int k0 = kb * BKV;
-                float mx = m;
+                float mx = -INFINITY;
+                if (k0 + BKV - 1 <= my_pos) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    float a = k0 + i <= my_pos ? __uint_as_float(s0[i]) * scale_log2 : -INFINITY;
-                    float b2 = k0 + 32 + i <= my_pos ? __uint_as_float(s1[i]) * scale_log2 : -INFINITY;
-                    s0[i] = __float_as_uint(a);
-                    s1[i] = __float_as_uint(b2);
-                    mx = fmaxf(mx, fmaxf(a, b2));
+                    for (int i = 0; i < 64; ++i) mx = fmaxf(mx, __uint_as_float(s[i]));
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) {
+                        const float v = k0 + i <= my_pos ? __uint_as_float(s[i]) : -INFINITY;
+                        s[i] = __float_as_uint(v);
+                        mx = fmaxf(mx, v);
+                    }
                 }
-                const float corr = ex2(m - mx);
+                const float mxs = mx * scale_log2;
+                const bool need = mxs > m_used + RESCALE_LOG2;
+                if (__any_sync(0xffffffffu, need)) {
+                    const float m_new = need ? mxs : m_used;
+                    const float corr = ex2(m_used - m_new);
+                    if (kb > 0) {
+                        // O holds blocks 0..kb-1 once P.V of block kb-1 is done
+                        if (!warp_wait(&pv_done[t][(it - 1) & 1], ((it - 1) >> 1) & 1, &abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        fence_after();
+#pragma unroll
+                        for (int c = 0; c < D; c += 32) {
+                            uint32_t o[32];
+                            TMEM_LD32(o_col + c, o);
+                            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
+                            TMEM_ST32(o_col + c, o);
+                        }
+                        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                    }
+                    l *= corr;
+                    m_used = m_new;
+                }
+                // the P buffer b was last read by P.V of global block it-2
+                if (it >= 2 && !warp_wait(&pv_done[t][b], ((it - 2) >> 1) & 1, &abort_flag)) {
+                    ok = false;
+                    break;
+                }
                 float sum = 0.f;
-                // P row r_in: 8 chunks of 8 keys, chunk c stored at chunk slot c ^ (r_in & 7)
-                uint8_t* prow = sP + sb * P_BYTES + r_in * 128;
+                uint8_t* prow = prow_base + b * P_BYTES;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     __align__(16) bf16 h[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
-                        const int i = c * 8 + e;
-                        const float sv = __uint_as_float(i < 32 ? s0[i] : s1[i - 32]);
-                        const float pv = ex2(sv - mx);
+                        const float pv = ex2(fmaf(__uint_as_float(s[c * 8 + e]), scale_log2, -m_used));
                         sum += pv;
                         h[e] = __float2bfloat16_rn(pv);
                     }
                     *reinterpret_cast<uint4*>(prow + ((c ^ (r_in & 7)) * 16)) = *reinterpret_cast<const uint4*>(h);
                 }
-                l = l * corr + sum;
+                l += sum;
+                fence_before();
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                mbar_arrive(&p_full[sb]);
-                if (kb > 0 && !accumulate(it - 1, corr_prev)) {
-                    ok = false;
-                    break;
-                }
-                corr_prev = corr;
-                m = mx;
+                mbar_arrive(&p_full[t][b]);
             }
-            if (!ok || !accumulate(it - 1, corr_prev)) {
+            if (!ok) break;
+            // O of this tile is final once P.V of its last block is done
+            if (!warp_wait(&pv_done[t][(it - 1) & 1], ((it - 1) >> 1) & 1, &abort_flag)) {
                 ok = false;
                 break;
             }
-            if (valid) {
-                const int j = p % group;
-                const float inv = 1.f / l;
-                bf16* dst = out + (long long)row * (hkv * group * D) + (long long)(t.g * group + j) * D;
+            fence_after();
+            const float inv = 1.f / l;
+            bf16* dst = out + (long long)row * (hkv * group * D) + (long long)(m.g * group + (valid ? p % group : 0)) * D;
 #pragma unroll
-                for (int c = 0; c < D; c += 8) {
-                    __align__(16) bf16 h[8];
+            for (int c = 0; c < D; c += 32) {
+                uint32_t o[32];
+                TMEM_LD32(o_col + c, o);
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                if (valid) {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) h[e] = __float2bfloat16_rn(o[c + e] * inv);
-                    *reinterpret_cast<uint4*>(dst + c) = *reinterpret_cast<const uint4*>(h);
+                    for (int v = 0; v < 4; ++v) {
+                        __align__(16) bf16 h[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) h[e] = __float2bfloat16_rn(__uint_as_float(o[v * 8 + e]) * inv);
+                        *reinterpret_cast<uint4*>(dst + c + v * 8) = *reinterpret_cast<const uint4*>(h);
+                    }
                 }
             }
+            fence_before();
+            mbar_arrive(&o_free[t]);
         }
         if (!ok) {
             abort_flag = 1;
@@ -476,7 +532,8 @@ int launch_attn_tc(const void* q, int m_cap, int n_req, const int32_t* req_row_e
     cuuint32_t kbx[3] = {64, 1, BKV};
     if (!encode(&mq, 2, q, qd, qs, qb) || !encode(&mk, 3, k_cache, kd, ks, kbx) || !encode(&mv, 3, v_cache, kd, ks, kbx))
         return BLEND_EUNSUPPORTED;
-    const long long items = (long long)hkv * ((((long long)M_max * group) + BQ - 1) / BQ + n_req);
+    const long long tiles = (((long long)M_max * group) + BQ - 1) / BQ + n_req;
+    const long long items = (long long)hkv * ((tiles + 1) / 2 + n_req);
     const int grid = (int)(items < g_sms ? items : g_sms);
     const float scale_log2 = (float)(1.4426950408889634 / 11.313708498984761);  // log2(e) / sqrt(128)
     k_attn_tc<<<grid, THREADS, SMEM_BYTES, s>>>(mq, mk, mv, n_req, req_row_end, row_pos, row_tok, group, hkv,

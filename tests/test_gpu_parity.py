@@ -306,8 +306,8 @@ def test_prefill_full_equals_rho_100():
         assert maxrel(f64(o["v"]), ref_v) <= TOL_BF16
 
 
-def test_prefill_batch_of_requests_matches_single_runs():
-    sh = SMALL_BF16_D64
+@pytest.mark.parametrize("sh", [SMALL_BF16_D64, SMALL_BF16], ids=["d64-cuda-cores", "d128-tensor-cores"])
+def test_prefill_batch_of_requests_matches_single_runs(sh):
     lens = [64, 48, 64, 32, 64]
     P, Q = 8, 12
     case = make_case(sh, P, lens, seed=5)
