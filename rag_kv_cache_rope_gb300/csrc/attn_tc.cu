@@ -16,6 +16,8 @@
 // The running maximum used for P is raised only when a row's maximum grows by more
 // than 2^8; then that warp rescales its rows of O in TMEM (ld, scale, st) between two
 // P.V products.  The sum l uses the same maximum, so O / l is exact.
+// Half of the exponentials run on the FMA pipe (ex2_fma) to relieve the MUFU unit.
+// Items are dealt to CTAs in snake order to balance their total KV length.
 // Warps: 0 TMA producer, 1 TMEM owner + MMA issuer, 2..5 softmax of tile A, 6..9 of
 // tile B.  The tensor core interleaves S_A, S_B, PV_A, PV_B so one tile's softmax
 // overlaps the other tile's products.  All mbarrier waits are bounded (error word
@@ -69,9 +71,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t par, volatile in
     }
     return false;
 }
-// Warp-uniform bounded wait (every lane polls; the warp proceeds only if all saw it).
+// Warp-level bounded wait: lane 0 polls, the result is broadcast, and __syncwarp orders
+// the other lanes after lane 0's acquire.
 __device__ __forceinline__ bool warp_wait(uint64_t* b, uint32_t par, volatile int* abort_flag) {
-    return __all_sync(0xffffffffu, mbar_wait(b, par, abort_flag));
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(b, par, abort_flag);
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    __syncwarp();
+    return ok;
+}
+// Warp-level arrive (barriers count warps): __syncwarp orders every lane's prior work
+// before lane 0's release-arrive.
+__device__ __forceinline__ void warp_arrive(uint64_t* b) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(b);
 }
 __device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* m, uint64_t* bar, int c0, int c1) {
     asm volatile(
@@ -116,10 +129,31 @@ __device__ __forceinline__ void commit(uint64_t* b) {
 }
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// Two fp32 values to one register of two bf16 (round to nearest even), lo in bits 0-15.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// 2^x on the FMA pipe, for part of the scores so the MUFU unit is not the only source of
+// exponentials: x = n + f with n = round(x) (1.5 * 2^23 rounding trick, no conversion
+// instruction), 2^f by a cubic fitted here to minimise the relative error on
+// [-0.5, 0.5] (7.5e-5; 1.4e-4 with fp32 rounding), 2^n added to the exponent bits.
+// x below -126 (masked scores are -inf) gives exactly 0.
+__device__ __forceinline__ float ex2_fma(float x) {
+    const float xc = fmaxf(x, -127.f);
+    const float t = xc + 12582912.f;
+    const int n = __float_as_int(t) - 0x4B400000;
+    const float f = xc - (t - 12582912.f);
+    const float p = fmaf(fmaf(fmaf(0.055170551f, f, 0.24260864f), f, 0.69326095f), f, 0.99992825f);
+    const float r = __int_as_float(__float_as_int(p) + (n << 23));
+    return x < -126.f ? 0.f : r;
 }
 
 #define TMEM_LD32(taddr, r)                                                                          \
@@ -143,8 +177,30 @@ __device__ __forceinline__ float ex2(float x) {
         "r"(r[30]), "r"(r[31])                                                                       \
         : "memory")
 
+// P.V of global block j (local block index kb of item tl) for both tiles, then release
+// the block's K/V stage.  Issued by the single MMA thread.
+__device__ __forceinline__ bool issue_pv(uint32_t j, int kb, uint32_t tl, uint8_t* sKV, uint8_t* sP, uint32_t tb,
+                                         uint64_t (*p_full)[2], uint64_t* o_free, uint64_t (*pv_done)[2],
+                                         uint64_t* kv_empty, volatile int* abort_flag) {
+    const uint32_t va = su32(sKV + (j % KV_STAGES) * KV_BYTES + 2 * KH_BYTES);
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        if (!mbar_wait(&p_full[t][j & 1], (j >> 1) & 1, abort_flag)) return false;
+        if (kb == 0 && !mbar_wait(&o_free[t], (tl & 1) ^ 1, abort_flag)) return false;
+        fence_after();
+        const uint32_t pa = su32(sP + (2 * t + (j & 1)) * P_BYTES);
+        const uint32_t od = tb + t * 256 + 128;
+#pragma unroll
+        for (int kk = 0; kk < BKV / 16; ++kk)
+            umma(od, desc_k(pa + kk * 32), desc_mn(va + kk * 2048), IDESC_PV, (kb > 0 || kk > 0) ? 1u : 0u);
+        commit(&pv_done[t][j & 1]);
+    }
+    commit(&kv_empty[j % KV_STAGES]);
+    return true;
+}
+
 struct Item {
-    int g, row0, npairs, pair0[2], max_pos, tok_base, nblk;
+    int g, row0, npairs, pair0_a, pair0_b, max_pos, tok_base, nblk;
 };
 
 // Work item w -> two tiles.  Request r has tiles_r = ceil(rows_r * group / 128) tiles per
@@ -164,8 +220,8 @@ __device__ __forceinline__ bool get_item(int w, int n_req, const int32_t* req_ro
             it.g = w % hkv;
             it.row0 = row0;
             it.npairs = np;
-            it.pair0[0] = ta * BQ;
-            it.pair0[1] = tb >= 0 ? tb * BQ : -1;
+            it.pair0_a = ta * BQ;
+            it.pair0_b = tb >= 0 ? tb * BQ : -1;
             const int last = min(ta * BQ + BQ, np) - 1;
             const int lrow = row0 + last / group;
             it.max_pos = row_pos[lrow];
@@ -219,11 +275,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int t = 0; t < 2; ++t) {
             for (int b = 0; b < 2; ++b) {
                 mbar_init(&s_full[t][b], 1);
-                mbar_init(&s_empty[t][b], 128);
-                mbar_init(&p_full[t][b], 128);
+                mbar_init(&s_empty[t][b], 4);
+                mbar_init(&p_full[t][b], 4);
                 mbar_init(&pv_done[t][b], 1);
             }
-            mbar_init(&o_free[t], 128);
+            mbar_init(&o_free[t], 4);
         }
         pend_q = -1;
         abort_flag = 0;
@@ -241,11 +297,18 @@ __global__ void __launch_bounds__(THREADS, 1)
     fence_after();
     const uint32_t tb = tmem_sh;
     const int qslab = m_cap * group;  // pair rows per kv head in q
+    // items are sorted longest first; round k gives CTA b item k*G + b (k even) or
+    // k*G + G-1-b (k odd), which evens out the total length per CTA
+    auto item_of = [&](int k) -> int {
+        return k * (int)gridDim.x + ((k & 1) ? (int)gridDim.x - 1 - (int)blockIdx.x : (int)blockIdx.x);
+    };
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------ TMA producer
         uint32_t it = 0, tl = 0;
-        for (int w = blockIdx.x; w < total && !abort_flag; w += gridDim.x, ++tl) {
+        for (int k = 0; !abort_flag; ++k, ++tl) {
+            const int w = item_of(k);
+            if (w >= total) break;
             Item m;
             get_item(w, n_req, req_row_end, row_pos, row_tok, group, hkv, m);
             if (!mbar_wait(&q_empty, (tl & 1) ^ 1, &abort_flag)) {
@@ -255,9 +318,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             mbar_expect_tx(&q_full, 2 * QT_BYTES);
             pend_q = (int)(tl & 1);
+#pragma unroll
             for (int t = 0; t < 2; ++t) {
                 // an absent second tile reloads the first (finite data, never stored)
-                const int p0 = m.pair0[t] >= 0 ? m.pair0[t] : m.pair0[0];
+                const int p0 = (t == 0 || m.pair0_b < 0) ? m.pair0_a : m.pair0_b;
                 const int qrow = m.g * qslab + m.row0 * group + p0;
                 tma_2d(sQ + t * QT_BYTES, &mapQ, &q_full, 0, qrow);
                 tma_2d(sQ + t * QT_BYTES + QT_BYTES / 2, &mapQ, &q_full, 64, qrow);
@@ -283,24 +347,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ------------------------------------------------ MMA issuer
         uint32_t it = 0, tl = 0;
         bool ok = true;
-        // P.V of global block j (local block index kb) for both tiles, then release its K/V stage
-        auto pv = [&](uint32_t j, int kb) -> bool {
-            const uint32_t va = su32(sKV + (j % KV_STAGES) * KV_BYTES + 2 * KH_BYTES);
-            for (int t = 0; t < 2; ++t) {
-                if (!mbar_wait(&p_full[t][j & 1], (j >> 1) & 1, &abort_flag)) return false;
-                if (kb == 0 && !mbar_wait(&o_free[t], (tl & 1) ^ 1, &abort_flag)) return false;
-                fence_after();
-                const uint32_t pa = su32(sP + (2 * t + (j & 1)) * P_BYTES);
-                const uint32_t od = tb + t * 256 + 128;
-#pragma unroll
-                for (int kk = 0; kk < BKV / 16; ++kk)
-                    umma(od, desc_k(pa + kk * 32), desc_mn(va + kk * 2048), IDESC_PV, (kb > 0 || kk > 0) ? 1u : 0u);
-                commit(&pv_done[t][j & 1]);
-            }
-            commit(&kv_empty[j % KV_STAGES]);
-            return true;
-        };
-        for (int w = blockIdx.x; w < total && ok && !abort_flag; w += gridDim.x, ++tl) {
+        for (int k = 0; ok && !abort_flag; ++k, ++tl) {
+            const int w = item_of(k);
+            if (w >= total) break;
             Item m;
             get_item(w, n_req, req_row_end, row_pos, row_tok, group, hkv, m);
             if (!mbar_wait(&q_full, tl & 1, &abort_flag)) {
@@ -333,9 +382,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                     commit(&s_full[t][it & 1]);
                 }
-                if (ok && kb > 0 && !pv(it - 1, kb - 1)) ok = false;
+                if (ok && kb > 0 &&
+                    !issue_pv(it - 1, kb - 1, tl, sKV, sP, tb, p_full, o_free, pv_done, kv_empty, &abort_flag))
+                    ok = false;
             }
-            if (!ok || !pv(it - 1, m.nblk - 1)) {
+            if (!ok ||
+                !issue_pv(it - 1, m.nblk - 1, tl, sKV, sP, tb, p_full, o_free, pv_done, kv_empty, &abort_flag)) {
                 ok = false;
                 break;
             }
@@ -356,11 +408,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint8_t* prow_base = sP + 2 * t * P_BYTES + r_in * 128;
         uint32_t it = 0;
         bool ok = true;
-        for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+        for (int k = 0; ok; ++k) {
+            const int w = item_of(k);
+            if (w >= total) break;
             Item m;
             get_item(w, n_req, req_row_end, row_pos, row_tok, group, hkv, m);
-            const bool have = m.pair0[t] >= 0;
-            const int p = (have ? m.pair0[t] : 0) + r_in;
+            const int my_pair0 = t == 0 ? m.pair0_a : m.pair0_b;
+            const bool have = my_pair0 >= 0;
+            const int p = (have ? my_pair0 : 0) + r_in;
             const bool valid = have && p < m.npairs;
             const int row = m.row0 + (valid ? p / group : 0);
             const int my_pos = valid ? row_pos[row] : m.max_pos;
@@ -377,19 +432,26 @@ __global__ void __launch_bounds__(THREADS, 1)
                 TMEM_LD32(s_col + b * 64 + 32, (s + 32));
                 asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
                 fence_before();
-                mbar_arrive(&s_empty[t][b]);
+                warp_arrive(&s_empty[t][b]);
                 const int k0 = kb * BKV;
-                float mx = -INFINITY;
-                if (k0 + BKV - 1 <= my_pos) {
+                if (k0 + BKV - 1 > my_pos) {
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) mx = fmaxf(mx, __uint_as_float(s[i]));
-                } else {
+                    for (int i = 0; i < 64; ++i)
+                        if (k0 + i > my_pos) s[i] = __float_as_uint(-INFINITY);
+                }
+                float mx;
+                {
+                    // max by a tree (short dependency chains)
+                    float a[16];
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) {
-                        const float v = k0 + i <= my_pos ? __uint_as_float(s[i]) : -INFINITY;
-                        s[i] = __float_as_uint(v);
-                        mx = fmaxf(mx, v);
-                    }
+                    for (int i = 0; i < 16; ++i)
+                        a[i] = fmaxf(fmaxf(__uint_as_float(s[i]), __uint_as_float(s[i + 16])),
+                                     fmaxf(__uint_as_float(s[i + 32]), __uint_as_float(s[i + 48])));
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) a[i] = fmaxf(a[i], a[i + 8]);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) a[i] = fmaxf(a[i], a[i + 4]);
+                    mx = fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3]));
                 }
                 const float mxs = mx * scale_log2;
                 const bool need = mxs > m_used + RESCALE_LOG2;
@@ -422,23 +484,25 @@ __global__ void __launch_bounds__(THREADS, 1)
                     ok = false;
                     break;
                 }
-                float sum = 0.f;
+                float sum4[4] = {0.f, 0.f, 0.f, 0.f};
                 uint8_t* prow = prow_base + b * P_BYTES;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
-                    __align__(16) bf16 h[8];
+                    uint32_t w4[4];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float pv = ex2(fmaf(__uint_as_float(s[c * 8 + e]), scale_log2, -m_used));
-                        sum += pv;
-                        h[e] = __float2bfloat16_rn(pv);
+                    for (int e = 0; e < 4; ++e) {
+                        // even keys on the MUFU unit, odd keys on the FMA pipe
+                        const float p0 = ex2(fmaf(__uint_as_float(s[c * 8 + 2 * e]), scale_log2, -m_used));
+                        const float p1 = ex2_fma(fmaf(__uint_as_float(s[c * 8 + 2 * e + 1]), scale_log2, -m_used));
+                        sum4[e] += p0 + p1;
+                        w4[e] = pack_bf16x2(p0, p1);
                     }
-                    *reinterpret_cast<uint4*>(prow + ((c ^ (r_in & 7)) * 16)) = *reinterpret_cast<const uint4*>(h);
+                    *reinterpret_cast<uint4*>(prow + ((c ^ (r_in & 7)) * 16)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                 }
-                l += sum;
+                l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
                 fence_before();
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                mbar_arrive(&p_full[t][b]);
+                warp_arrive(&p_full[t][b]);
             }
             if (!ok) break;
             // O of this tile is final once P.V of its last block is done
@@ -457,15 +521,17 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (valid) {
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {
-                        __align__(16) bf16 h[8];
+                        uint32_t w4[4];
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) h[e] = __float2bfloat16_rn(__uint_as_float(o[v * 8 + e]) * inv);
-                        *reinterpret_cast<uint4*>(dst + c + v * 8) = *reinterpret_cast<const uint4*>(h);
+                        for (int e = 0; e < 4; ++e)
+                            w4[e] = pack_bf16x2(__uint_as_float(o[v * 8 + 2 * e]) * inv,
+                                                __uint_as_float(o[v * 8 + 2 * e + 1]) * inv);
+                        *reinterpret_cast<uint4*>(dst + c + v * 8) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                     }
                 }
             }
             fence_before();
-            mbar_arrive(&o_free[t]);
+            warp_arrive(&o_free[t]);
         }
         if (!ok) {
             abort_flag = 1;

@@ -104,6 +104,12 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
                      su32(bar))
                  : "memory");
 }
+// Two fp32 values to one register of two bf16 (round to nearest even), lo in bits 0-15.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -148,7 +154,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
-            mbar_init(&tempty[b], 4 * 32);
+            mbar_init(&tempty[b], 4);  // one arrival per epilogue warp
         }
         abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -233,9 +239,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t tph = 0;
         for (int t = blockIdx.x; t < n_total; t += gridDim.x) {
             const int mt = t % m_tiles, nt = t / m_tiles;
-            // every lane waits; the warp continues only if all saw the accumulator
-            // (tcgen05.ld below is .sync.aligned and must not run in a diverged warp)
-            const bool ok = __all_sync(0xffffffffu, mbar_wait(&tfull[b], tph, &abort_flag));
+            // lane 0 waits and broadcasts; the warp stays converged for the .sync.aligned
+            // tcgen05.ld below
+            bool ok = true;
+            if (lane == 0) ok = mbar_wait(&tfull[b], tph, &abort_flag);
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            __syncwarp();
             if (!ok) {
                 abort_flag = 1;
                 if (lane == 0) set_error(err, BLEND_ETIMEOUT);
@@ -269,20 +278,22 @@ __global__ void __launch_bounds__(THREADS, 1)
                         }
                     } else {
                         // 32 columns = 16 gate + 16 up of the same hidden units
-                        __align__(16) bf16 h[16];
+                        uint32_t w8[8];
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const float g = __uint_as_float(r[i]), u = __uint_as_float(r[16 + i]);
-                            h[i] = __float2bfloat16_rn(g / (1.f + expf(-g)) * u);
+                        for (int i = 0; i < 8; ++i) {
+                            const float g0 = __uint_as_float(r[2 * i]), u0 = __uint_as_float(r[16 + 2 * i]);
+                            const float g1 = __uint_as_float(r[2 * i + 1]), u1 = __uint_as_float(r[17 + 2 * i]);
+                            w8[i] = pack_bf16x2(g0 / (1.f + expf(-g0)) * u0, g1 / (1.f + expf(-g1)) * u1);
                         }
                         uint4* p = reinterpret_cast<uint4*>((bf16*)Cv + (long long)row * ldc + col / 2);
-                        p[0] = reinterpret_cast<const uint4*>(h)[0];
-                        p[1] = reinterpret_cast<const uint4*>(h)[1];
+                        p[0] = make_uint4(w8[0], w8[1], w8[2], w8[3]);
+                        p[1] = make_uint4(w8[4], w8[5], w8[6], w8[7]);
                     }
                 }
             }
             tc_fence_before();
-            mbar_arrive(&tempty[b]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[b]);
             b ^= 1;
             if (b == 0) tph ^= 1;
         }
