@@ -184,6 +184,26 @@ int blend_device_status(blend_handle* h, void* stream);
  * and on GPUs without tcgen05). */
 int blend_set_tensor_cores(blend_handle* h, int on);
 
+/* Allocation-free variant of topk_select_dilate (same arguments, same result, no
+ * handle).  The pages have no counterpart: this call exists for callers that cannot
+ * allocate device memory when they select tokens - for example a serving loop that
+ * reserves all HBM for its KV pool at start-up, or one that must not call cudaMalloc /
+ * cudaFree on its hot path because those calls can synchronise the device or fail
+ * under fragmentation.  The call uses a fixed scratch array of 32768 ranks (128 KB)
+ * in device memory that every GPU which loads the library holds until the process
+ * exits; it never allocates or frees memory.
+ *   - n above 32768 is rejected with BLEND_EINVAL (nothing is launched).
+ *   - The first call on each device looks up the array's device address (with that
+ *     device current); make that first call before any stream capture.
+ *   - Every call shares the one array: calls whose work overlaps on the GPU (on
+ *     different streams, or on several host threads) race and give wrong sets.
+ *     Each call rewrites every scratch entry it reads, so nothing needs clearing.
+ * Errors: as topk_select_dilate; the text is in blend_last_error(NULL). */
+int topk_select_dilate_noalloc(const float* scores, int32_t n, int32_t base, int32_t budget,
+                               int32_t window, int32_t tau, int32_t budget_mode,
+                               const uint8_t* allowed, int32_t* idx_out, int32_t* n_out,
+                               void* stream);
+
 /* ---- tracing --------------------------------------------------------------- */
 /* Per-stage timing with CUDA events recorded on the caller's stream around each stage
  * of blend_prefill / selective_layer (assemble, select, plan_gather, rmsnorm,

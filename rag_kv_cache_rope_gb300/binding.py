@@ -109,6 +109,7 @@ def lib() -> C.CDLL:
             "blend_profile_read": (C.c_int, [vp, C.POINTER(C.c_double), C.POINTER(C.c_int64), i32]),
             "blend_profile_name": (C.c_char_p, [i32]),
             "blend_launch_count": (C.c_int64, []),
+            "topk_select_dilate_noalloc": (C.c_int, [vp, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -122,7 +123,7 @@ EXPORTED = ("blend_workspace_size", "blend_init", "blend_destroy", "blend_last_e
             "blend_device_status", "blend_set_tensor_cores", "rope_realign", "blend_assemble",
             "kv_deviation", "topk_select_dilate", "gather_rows", "scatter_kv", "selective_layer",
             "blend_prefill", "importance_scores", "blend_profile", "blend_profile_read",
-            "blend_profile_name", "blend_launch_count")
+            "blend_profile_name", "blend_launch_count", "topk_select_dilate_noalloc")
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -233,6 +234,14 @@ def topk_select_dilate(h, scores, n, base, budget, window, tau, budget_mode, all
                        stream=None):
     _check(lib().topk_select_dilate(h.ptr, _ptr(scores), n, base, budget, window, tau, budget_mode,
                                     _ptr(allowed), _ptr(idx_out), _ptr(n_out), _stream(stream)), h)
+
+
+def topk_select_dilate_noalloc(scores, n, base, budget, window, tau, budget_mode, allowed, idx_out, n_out,
+                               stream=None):
+    """topk_select_dilate without a handle or any allocation (fixed 32768-entry device
+    scratch shared by every call; see include/blend.h)."""
+    _check(lib().topk_select_dilate_noalloc(_ptr(scores), n, base, budget, window, tau, budget_mode,
+                                            _ptr(allowed), _ptr(idx_out), _ptr(n_out), _stream(stream)))
 
 
 def gather_rows(src, row_bytes, idx, n, max_n, dst, stream=None):

@@ -14,16 +14,22 @@
 #include "common.cuh"
 #include "gemm_tc.cuh"
 
+namespace {
+thread_local std::string g_err;
+}  // namespace
+
 namespace blend {
 static std::atomic<long long> g_launches{0};
 void note_launch(int n) { g_launches += n; }
+int report_error(int code, const char* msg) {
+    g_err = msg;
+    return code;
+}
 }  // namespace blend
 
 using namespace blend;
 
 namespace {
-
-thread_local std::string g_err;
 
 // Stages timed by the profiler (CUDA events on the caller's stream).
 enum ProfCat {

@@ -44,6 +44,8 @@ template <typename T> __device__ __forceinline__ void st16(T* p, const Vec<T>& v
 
 // Counts kernel launches made by the library (process-wide; read by blend_launch_count).
 void note_launch(int n = 1);
+// Records `msg` as the text blend_last_error(NULL) returns and returns `code`.
+int report_error(int code, const char* msg);
 
 // Records the first device-side failure (code, where) in the handle's error word.
 __device__ __forceinline__ void set_error(int32_t* err, int32_t code) {

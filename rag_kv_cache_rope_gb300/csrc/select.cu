@@ -15,6 +15,8 @@
 // k, so the answer is either the bound itself or the (budget+1)-th smallest cover
 // value.  All arithmetic is integer, so the result is exact.
 #include <climits>
+#include <cstring>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -189,4 +191,65 @@ void launch_select(const SelectBatch& sb, int32_t* rank_scratch, int max_n, cuda
     note_launch(2);
 }
 
+// ---------------------------------------------------------------- allocation-free variant
+// Rank scratch of topk_select_dilate_noalloc: a fixed array in device memory, so the
+// call needs neither a handle nor any allocation.  Every GPU that loads the library
+// holds these 128 KB until the process exits.
+constexpr int NOALLOC_MAX_N = 32768;
+static __device__ __align__(256) int32_t g_noalloc_rank[NOALLOC_MAX_N];
+
+namespace {
+constexpr int NOALLOC_MAX_DEVICES = 64;
+std::mutex g_noalloc_mu;
+int32_t* g_noalloc_ptr[NOALLOC_MAX_DEVICES] = {};
+
+// Device address of g_noalloc_rank on the current device (looked up once per device;
+// the host-side name of the array is only a stand-in and must not reach a kernel).
+int noalloc_scratch(int32_t** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return BLEND_ECUDA;
+    if (dev < 0 || dev >= NOALLOC_MAX_DEVICES) return BLEND_EUNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_rank) != cudaSuccess || p == nullptr) return BLEND_ECUDA;
+        g_noalloc_ptr[dev] = static_cast<int32_t*>(p);
+    }
+    *out = g_noalloc_ptr[dev];
+    return BLEND_OK;
+}
+}  // namespace
+
 }  // namespace blend
+
+extern "C" int topk_select_dilate_noalloc(const float* scores, int32_t n, int32_t base, int32_t budget,
+                                          int32_t window, int32_t tau, int32_t budget_mode,
+                                          const uint8_t* allowed, int32_t* idx_out, int32_t* n_out,
+                                          void* stream) {
+    using namespace blend;
+    if (!scores || !idx_out || !n_out) return report_error(BLEND_EINVAL, "topk_select_dilate_noalloc: NULL pointer");
+    if (n < 0 || n > NOALLOC_MAX_N)
+        return report_error(BLEND_EINVAL, "topk_select_dilate_noalloc: n outside 0..32768 (size of its fixed scratch)");
+    if (budget < 0 || window < 1 || window > BLEND_MAX_WINDOW || tau < 1 || tau > window)
+        return report_error(BLEND_EINVAL, "topk_select_dilate_noalloc: bad budget/window/tau");
+    if (budget_mode != BLEND_BUDGET_FINAL && budget_mode != BLEND_BUDGET_CANDIDATE)
+        return report_error(BLEND_EINVAL, "topk_select_dilate_noalloc: bad budget_mode");
+    int32_t* rank = nullptr;
+    int rc = noalloc_scratch(&rank);
+    if (rc != BLEND_OK) {
+        cudaGetLastError();
+        return report_error(rc, "topk_select_dilate_noalloc: cannot get the device address of the fixed scratch");
+    }
+    SelectBatch sb;
+    memset(&sb, 0, sizeof sb);
+    sb.n_job = 1;
+    sb.window = window;
+    sb.tau = tau;
+    sb.budget_mode = budget_mode;
+    sb.j[0] = SelectJob{scores, allowed, idx_out, n_out, n, base, budget, 0};
+    // every rank entry the call reads is written by the call first: nothing to clear
+    launch_select(sb, rank, n, (cudaStream_t)stream);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return report_error(BLEND_ECUDA, cudaGetErrorString(e));
+    return BLEND_OK;
+}
