@@ -24,6 +24,14 @@ def f64(t: torch.Tensor) -> np.ndarray:
     return t.detach().to("cpu", torch.float64).numpy()
 
 
+def relerr(got, ref) -> float:
+    """Norm-wise relative error ||got - ref||_2 / ||ref||_2."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    den = np.sqrt(np.sum(ref * ref))
+    return float(np.sqrt(np.sum((got - ref) ** 2)) / (den if den > 0 else 1.0))
+
+
 def maxrel(got, ref) -> float:
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)

@@ -1,0 +1,233 @@
+"""Parity at the workloads' full sizes, in the launch configuration bench.py times.
+
+Each case keeps the workload's exact shapes (hidden size, heads, context, chunk
+layout, recompute ratio, window) and truncates only the depth, so every kernel runs
+with the same grids and tiles as in the benchmark; the oracle then checks every
+output.  The pools are Gaussian (the oracle cannot precompute 14B chunk caches in
+seconds) except for the HKVD case, whose deviations need real precomputed caches.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import blend_oracle as O
+from rag_kv_cache_rope_gb300 import binding as b
+from rag_kv_cache_rope_gb300 import build as B
+from rag_kv_cache_rope_gb300 import synth
+
+from blendcase import f64, maxrel, oracle_cfg, relerr, set_diff_is_near_tie, stages_to_device
+
+pytestmark = pytest.mark.gpu
+
+# bf16 outputs: norm-wise relative error within the 2e-2 bar, and a max-norm guard
+# (max|d| / max|ref|) that catches a wrong row or head the 2-norm would dilute.  The
+# guard is 2e-2 up to two layers deep; three layers of bf16 intermediates reach ~2.0e-2
+# on the 8B shape (an oracle copy rounding at the same points to bf16 shows the same
+# RMS error), so there it is 3e-2.
+TOL_BF16 = 2e-2
+TOL_BF16_MAX_DEEP = 3e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    B.build()
+    b.lib()
+
+
+def dev():
+    return torch.device("cuda:0")
+
+
+class FullCase:
+    """Weights on the device (torch generator on cuda) and their float64 copies."""
+
+    def __init__(self, wl: synth.Workload, layers: int, pool: str = "random", real_prefix: bool = False):
+        self.wl = dataclasses.replace(wl, model=dataclasses.replace(wl.model, n_layers=layers))
+        sh = self.wl.model
+        self.sh = sh
+        w = synth.model_weights(sh, wl.seed, device=dev())
+        self.w_np = {k: f64(v) for k, v in w.items()}
+        self.packed = b.pack_weights(w)
+        del w
+        self.pool_tok, self.reqs = synth.workload_tokens(self.wl)
+        n_entries = len(self.pool_tok.chunks)
+        lens = [wl.chunk_len] * n_entries
+        P = wl.prefix_len
+        self.chunks = [c.numpy() for c in self.pool_tok.chunks]
+        self.prefix = self.pool_tok.prefix.numpy()
+        if pool == "random":
+            k, v, row_off = synth.random_pool_kv(sh, P, lens, wl.seed, device=dev())
+            if real_prefix:
+                # the model's own prefix rows (any [prefix + chunk] precompute starts with them)
+                _, pk, pv = O.full_prefill(self.w_np, oracle_cfg(sh), self.prefix)
+                pk = torch.from_numpy(pk).to(torch.bfloat16).to(dev())
+                pv = torch.from_numpy(pv).to(torch.bfloat16).to(dev())
+                for o in row_off:
+                    k[:, o:o + P] = pk
+                    v[:, o:o + P] = pv
+            self.entries_k = [f64(k[:, o:o + P + L]) for o, L in zip(row_off, lens)]
+            self.entries_v = [f64(v[:, o:o + P + L]) for o, L in zip(row_off, lens)]
+        else:
+            cfg = oracle_cfg(sh)
+            ks, vs = [], []
+            for c in self.chunks:
+                kk, vv = O.precompute_chunk(self.w_np, cfg, self.prefix, c)
+                ks.append(torch.from_numpy(kk).to(torch.bfloat16))
+                vs.append(torch.from_numpy(vv).to(torch.bfloat16))
+            self.entries_k = [f64(t) for t in ks]
+            self.entries_v = [f64(t) for t in vs]
+            k = torch.cat(ks, dim=1).to(dev())
+            v = torch.cat(vs, dim=1).to(dev())
+            row_off = [i * (P + wl.chunk_len) for i in range(n_entries)]
+        tok = torch.cat([torch.cat([self.pool_tok.prefix, c]) for c in self.pool_tok.chunks]).to(dev())
+        self.pool = b.PoolRef(k, v, tok, P, lens, row_off)
+        self.N = self.wl.n_ctx
+        self.n_c = self.wl.n_chunk_rows
+        self.Q = self.wl.query_len
+
+    def handle(self, max_rows, batch=1):
+        N = self.N * batch
+        return b.blend_init(b.model_cfg(self.sh, self.N), self.packed,
+                            b.Limits(max_rows, N, self.n_c, batch))
+
+    def outputs(self, batch=1):
+        sh, L = self.sh, self.sh.n_layers
+        d = dev()
+        return b.OutputsRef(
+            k=torch.zeros(L, self.N * batch, sh.n_kv_heads, sh.head_dim, dtype=torch.bfloat16, device=d),
+            v=torch.zeros(L, self.N * batch, sh.n_kv_heads, sh.head_dim, dtype=torch.bfloat16, device=d),
+            hidden=torch.zeros(self.Q * batch, sh.hidden, dtype=torch.bfloat16, device=d),
+            sel=torch.full((self.n_c * batch,), -1, dtype=torch.int32, device=d),
+            n_sel=torch.zeros(b.MAX_BATCH, dtype=torch.int32, device=d),
+            c1=torch.full((self.n_c * batch,), -1, dtype=torch.int32, device=d),
+            n_c1=torch.zeros(b.MAX_BATCH, dtype=torch.int32, device=d),
+            dev1=torch.zeros(self.n_c * batch, dtype=torch.float32, device=d),
+            dev2=torch.zeros(self.n_c * batch, dtype=torch.float32, device=d))
+
+    def oracle(self, r, **kw):
+        req = self.reqs[r]
+        return O.blend_prefill(self.w_np, oracle_cfg(self.sh), self.entries_k, self.entries_v, self.chunks,
+                               self.prefix, req.chunk_ids, req.query.numpy(), **kw)
+
+
+def check(name, got, ref, tol_max=TOL_BF16):
+    g = f64(got) if isinstance(got, torch.Tensor) else got
+    e2, em = relerr(g, ref), maxrel(g, ref)
+    print(f"[fullsize] {name}: relative error {e2:.3e} (bar {TOL_BF16:.0e}), max-norm {em:.3e} (bar {tol_max:.0e})")
+    assert e2 <= TOL_BF16 and em <= tol_max, (name, e2, em)
+
+
+def ext_scores(n_c, seed):
+    h = synth.hidden_states(n_c, 4, 2048, seed)
+    return O.importance_scores(f64(h)).astype(np.float32)
+
+
+def test_qwen14b_16k_ext20_two_layers():
+    wl = synth.WORKLOADS["qwen14b-16k-ext20"]
+    fc = FullCase(wl, layers=2)
+    h = fc.handle(fc.n_c + fc.Q)
+    scores = ext_scores(fc.n_c, wl.seed)
+    req = fc.reqs[0]
+    kw = dict(mode="ext", rho_bp=wl.rho_bp, window=wl.window, tau=wl.tau, budget_mode=wl.budget_mode)
+    out = fc.outputs()
+    b.blend_prefill(h, [b.RequestRef(req.chunk_ids, req.query.to(dev()), scores=torch.from_numpy(scores).to(dev()),
+                                     **kw)], fc.pool, out)
+    b.blend_device_status(h)
+    ref = fc.oracle(0, scores=scores.astype(np.float64), **kw)
+    sel = ref["stages"][0][1]
+    n = int(out["n_sel"][0].item())
+    assert n == len(sel) and n <= O.ceil_bp(wl.rho_bp, fc.n_c)
+    assert out["sel"][:n].cpu().numpy().tolist() == sel.tolist()
+    check("14B 16K K", out["k"], ref["K"])
+    check("14B 16K V", out["v"], ref["V"])
+    check("14B 16K hidden", out["hidden"], ref["hidden"])
+    # the GPU's own score kernel on the same hidden states
+    hs = synth.hidden_states(fc.n_c, 4, 2048, wl.seed)
+    got = torch.empty(fc.n_c, device=dev())
+    b.importance_scores(hs.to(dev()), fc.n_c, 4, 2048, got)
+    torch.cuda.synchronize()
+    assert maxrel(f64(got), O.importance_scores(f64(hs))) <= 1e-5
+
+
+def test_llama8b_3k_hkvd15_three_layers():
+    wl = synth.WORKLOADS["llama8b-3k-hkvd15"]
+    fc = FullCase(wl, layers=3, pool="oracle")
+    h = fc.handle(fc.n_c + fc.Q)
+    req = fc.reqs[0]
+    kw = dict(rho_bp=wl.rho_bp, r1_bp=wl.r1_bp, window=wl.window, tau=wl.tau, budget_mode=wl.budget_mode)
+    ref = fc.oracle(0, mode="hkvd", **kw)
+    qd = req.query.to(dev())
+    out = fc.outputs()
+    b.blend_prefill(h, [b.RequestRef(req.chunk_ids, qd, mode="hkvd", **kw)], fc.pool, out)
+    b.blend_device_status(h)
+    check("8B HKVD dev1", out["dev1"], ref["dev1"])
+    c1_ref = ref["stages"][1][1]
+    n1 = int(out["n_c1"][0].item())
+    assert n1 == len(c1_ref) == O.ceil_bp(wl.r1_bp, fc.n_c)
+    P = wl.prefix_len
+    assert set_diff_is_near_tie(out["c1"][:n1].cpu().numpy() - P, c1_ref - P, ref["dev1"], n1, rel=TOL_BF16)
+    ns = int(out["n_sel"][0].item())
+    assert ns <= O.ceil_bp(wl.rho_bp, fc.n_c)
+    assert set(out["sel"][:ns].cpu().numpy().tolist()) <= set(out["c1"][:n1].cpu().numpy().tolist())
+    # values with the GPU forced onto the oracle's stage sets
+    out2 = fc.outputs()
+    b.blend_prefill(h, [b.RequestRef(req.chunk_ids, qd, mode="forced",
+                                     stages=stages_to_device(ref["stages"], dev()))], fc.pool, out2)
+    b.blend_device_status(h)
+    for k, rk in (("k", "K"), ("v", "V"), ("hidden", "hidden")):
+        check(f"8B HKVD forced {k}", out2[k], ref[rk], tol_max=TOL_BF16_MAX_DEEP)
+    check("8B HKVD forced dev2", out2["dev2"], ref["dev2"])
+
+
+def test_mistral7b_batch8_ext15_two_layers():
+    wl = synth.WORKLOADS["mistral7b-b8-ext15"]
+    fc = FullCase(wl, layers=2)
+    Bn = wl.batch
+    budget = O.ceil_bp(wl.rho_bp, fc.n_c)
+    h = fc.handle(Bn * (budget + fc.Q), batch=Bn)
+    reqs, scores = [], []
+    for r in range(Bn):
+        s = ext_scores(fc.n_c, wl.seed + r)
+        scores.append(s)
+        reqs.append(b.RequestRef(fc.reqs[r].chunk_ids, fc.reqs[r].query.to(dev()), mode="ext", rho_bp=wl.rho_bp,
+                                 window=wl.window, tau=wl.tau, scores=torch.from_numpy(s).to(dev())))
+    out = fc.outputs(batch=Bn)
+    b.blend_prefill(h, reqs, fc.pool, out)
+    b.blend_device_status(h)
+    assert len(set(tuple(r.chunk_ids) for r in fc.reqs)) > 1       # Zipf draws differ per request
+    for r in range(Bn):
+        ref = fc.oracle(r, mode="ext", rho_bp=wl.rho_bp, window=wl.window, tau=wl.tau,
+                        scores=scores[r].astype(np.float64))
+        t0, q0, c0 = r * fc.N, r * fc.Q, r * fc.n_c
+        ns = int(out["n_sel"][r].item())
+        assert out["sel"][c0:c0 + ns].cpu().numpy().tolist() == ref["stages"][0][1].tolist()
+        check(f"7B batch req{r} K", out["k"][:, t0:t0 + fc.N], ref["K"])
+        check(f"7B batch req{r} V", out["v"][:, t0:t0 + fc.N], ref["V"])
+        check(f"7B batch req{r} hidden", out["hidden"][q0:q0 + fc.Q], ref["hidden"])
+
+
+def test_qwen14b_sweep_100_percent_equals_full_prefill():
+    """The sweep's 100 % point (4K context): every chunk row recomputed equals a full
+    prefill of the same tokens (the pages' invariant), and FULL mode does too."""
+    wl = synth.sweep_workload(7, 10000)
+    fc = FullCase(wl, layers=2, real_prefix=True)
+    h = fc.handle(fc.N)
+    req = fc.reqs[0]
+    qd = req.query.to(dev())
+    scores = torch.from_numpy(ext_scores(fc.n_c, 9)).to(dev())
+    toks = np.concatenate([fc.prefix] + [fc.chunks[c] for c in req.chunk_ids] + [req.query.numpy()])
+    hf, kf, vf = O.full_prefill(fc.w_np, oracle_cfg(fc.sh), toks)
+    for mode in ("ext", "full"):
+        o = fc.outputs()
+        b.blend_prefill(h, [b.RequestRef(req.chunk_ids, qd, mode=mode, rho_bp=10000, window=wl.window,
+                                         scores=scores)], fc.pool, o)
+        b.blend_device_status(h)
+        if mode == "ext":
+            assert int(o["n_sel"][0].item()) == fc.n_c
+        check(f"14B 4K rho100 {mode} hidden", o["hidden"], hf[-fc.Q:])
+        check(f"14B 4K rho100 {mode} K", o["k"], kf)
+        check(f"14B 4K rho100 {mode} V", o["v"], vf)
