@@ -6,22 +6,26 @@
 // (row, head-of-group) pairs of one kv head form one TMA box and every K/V block is
 // shared by the whole head group.  A work item is two consecutive 128-pair tiles (A
 // and B) of one kv head and one request; items run longest first on persistent CTAs,
-// and the two tiles share every K/V block.  Per 64-key block, for each tile:
-//   S = Q . K^T      tcgen05.mma M128 N64 K16 x8 -> TMEM (two buffers per tile)
-//   P                one softmax warpgroup per tile, one pair row per thread: causal
-//                    mask on boundary blocks, base-2 scores with the scale folded into
-//                    one FFMA, bf16 P written to 128-byte-swizzled shared memory
-//   O += P . V       tcgen05.mma M128 N128 K16 x4, V as an MN-major operand, O kept in
-//                    TMEM for the whole item.
-// The running maximum used for P is raised only when a row's maximum grows by more
-// than 2^8; then that warp rescales its rows of O in TMEM (ld, scale, st) between two
-// P.V products.  The sum l uses the same maximum, so O / l is exact.
-// Half of the exponentials run on the FMA pipe (ex2_fma) to relieve the MUFU unit.
-// Items are dealt to CTAs in snake order to balance their total KV length.
+// dealt in snake order, and the two tiles share every K/V block.  Per 128-key block,
+// for each tile:
+//   S = Q . K^T   tcgen05.mma M128 N128 K16 x8, shared-memory operands -> TMEM
+//   P             one softmax warpgroup per tile, one pair row per thread: the row's 128
+//                 scores come to registers in one TMEM round trip; row maximum (causal mask
+//                 on boundary blocks), then bf16 P (base 2, scale folded into one FFMA, half
+//                 of the exponentials on the FMA pipe) written back over S's first 64 TMEM
+//                 columns in one more round trip
+//   O += P . V    tcgen05.mma M128 N128 K16 x8 with A = P read from TMEM and V an
+//                 MN-major shared-memory operand; O stays in TMEM for the whole item.
+// Per tile the products run S(j), PV(j), S(j+1): the tensor core executes one CTA's
+// MMAs in order, so S(j+1) cannot overwrite P(j) before PV(j) has read it, and the
+// completion of S(j) implies that of PV(j-1), which lets the softmax rescale O right
+// after S(j) arrives.  The running maximum used for P is raised only when a row's
+// maximum grows by more than 2^8 (then that warp rescales its rows of O in TMEM); the
+// sum l uses the same maximum, so O / l is exact.  While one tile's softmax runs, the
+// tensor core works on the other tile.
 // Warps: 0 TMA producer, 1 TMEM owner + MMA issuer, 2..5 softmax of tile A, 6..9 of
-// tile B.  The tensor core interleaves S_A, S_B, PV_A, PV_B so one tile's softmax
-// overlaps the other tile's products.  All mbarrier waits are bounded (error word
-// BLEND_ETIMEOUT, loads drained, TMEM freed).
+// tile B.  All mbarrier waits are bounded (error word BLEND_ETIMEOUT, loads drained,
+// TMEM freed).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -32,14 +36,13 @@ namespace {
 
 constexpr int D = 128;
 constexpr int BQ = 128;
-constexpr int BKV = 64;
-constexpr int KV_STAGES = 3;
-constexpr int QT_BYTES = BQ * D * 2;    // 32 KB per tile: two 16 KB column halves
-constexpr int KH_BYTES = BKV * 64 * 2;  // 8 KB: one 64-wide column half of a K or V block
-constexpr int KV_BYTES = 4 * KH_BYTES;  // K halves, then V halves
-constexpr int P_BYTES = BQ * BKV * 2;   // 16 KB
-constexpr int SMEM_BYTES = 2 * QT_BYTES + KV_STAGES * KV_BYTES + 4 * P_BYTES + 1024;
-constexpr int TMEM_COLS = 512;  // tile t: S0 t*256+[0,64), S1 t*256+[64,128), O t*256+[128,256)
+constexpr int BKV = 128;
+constexpr int KV_STAGES = 2;
+constexpr int QT_BYTES = BQ * D * 2;     // 32 KB per tile: two 16 KB column halves
+constexpr int KH_BYTES = BKV * 64 * 2;   // 16 KB: one 64-wide column half of a K or V block
+constexpr int KV_BYTES = 4 * KH_BYTES;   // K halves, then V halves
+constexpr int SMEM_BYTES = 2 * QT_BYTES + KV_STAGES * KV_BYTES + 1024;
+constexpr int TMEM_COLS = 512;  // tile t: S (and P over its first 64 columns) t*256+[0,128), O t*256+[128,256)
 constexpr int THREADS = 320;
 constexpr float RESCALE_LOG2 = 8.f;
 constexpr long long SPIN_LIMIT = 1ll << 24;
@@ -107,20 +110,30 @@ __device__ __forceinline__ uint64_t desc_k(uint32_t a) {
 }
 // MN-major operand (V as B of P.V), 128-byte swizzle: each key row holds 64 d values
 // (128 B); 8-key groups 1024 B apart (stride byte offset); the second 64-wide d half
-// 8 KB further (leading byte offset).
+// 16 KB further (leading byte offset).
 __device__ __forceinline__ uint64_t desc_mn(uint32_t a) {
     return (uint64_t)((a & 0x3FFFF) >> 4) | ((uint64_t)(KH_BYTES >> 4) << 16) |
            ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
+// kind::f16, bf16 inputs, fp32 accumulate, M128 N128; PV additionally reads B MN-major.
 constexpr uint32_t IDESC_S = (1u << 4) | (1u << 7) | (1u << 10) | ((BKV >> 3) << 17) | ((BQ >> 4) << 24);
 constexpr uint32_t IDESC_PV =
     (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) /* B MN-major */ | ((D >> 3) << 17) | ((BQ >> 4) << 24);
 
-__device__ __forceinline__ void umma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+// D (TMEM) op= A (shared-memory descriptor) . B (shared-memory descriptor)
+__device__ __forceinline__ void umma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d),
         "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+// D (TMEM) op= A (TMEM: lane = row, two bf16 per column) . B (shared-memory descriptor)
+__device__ __forceinline__ void umma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
         : "memory");
 }
 __device__ __forceinline__ void commit(uint64_t* b) {
@@ -140,7 +153,6 @@ __device__ __forceinline__ float ex2(float x) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
-
 // 2^x on the FMA pipe, for part of the scores so the MUFU unit is not the only source of
 // exponentials: x = n + f with n = round(x) (1.5 * 2^23 rounding trick, no conversion
 // instruction), 2^f by a cubic fitted here to minimise the relative error on
@@ -176,28 +188,13 @@ __device__ __forceinline__ float ex2_fma(float x) {
         "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]),           \
         "r"(r[30]), "r"(r[31])                                                                       \
         : "memory")
-
-// P.V of global block j (local block index kb of item tl) for both tiles, then release
-// the block's K/V stage.  Issued by the single MMA thread.
-__device__ __forceinline__ bool issue_pv(uint32_t j, int kb, uint32_t tl, uint8_t* sKV, uint8_t* sP, uint32_t tb,
-                                         uint64_t (*p_full)[2], uint64_t* o_free, uint64_t (*pv_done)[2],
-                                         uint64_t* kv_empty, volatile int* abort_flag) {
-    const uint32_t va = su32(sKV + (j % KV_STAGES) * KV_BYTES + 2 * KH_BYTES);
-#pragma unroll
-    for (int t = 0; t < 2; ++t) {
-        if (!mbar_wait(&p_full[t][j & 1], (j >> 1) & 1, abort_flag)) return false;
-        if (kb == 0 && !mbar_wait(&o_free[t], (tl & 1) ^ 1, abort_flag)) return false;
-        fence_after();
-        const uint32_t pa = su32(sP + (2 * t + (j & 1)) * P_BYTES);
-        const uint32_t od = tb + t * 256 + 128;
-#pragma unroll
-        for (int kk = 0; kk < BKV / 16; ++kk)
-            umma(od, desc_k(pa + kk * 32), desc_mn(va + kk * 2048), IDESC_PV, (kb > 0 || kk > 0) ? 1u : 0u);
-        commit(&pv_done[t][j & 1]);
-    }
-    commit(&kv_empty[j % KV_STAGES]);
-    return true;
-}
+#define TMEM_ST16(taddr, r)                                                                          \
+    asm volatile(                                                                                    \
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14," \
+        "%15,%16};" ::"r"(taddr),                                                                    \
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),      \
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]) \
+        : "memory")
 
 struct Item {
     int g, row0, npairs, pair0_a, pair0_b, max_pos, tok_base, nblk;
@@ -235,23 +232,41 @@ __device__ __forceinline__ bool get_item(int w, int n_req, const int32_t* req_ro
     return false;
 }
 
+// S of tile t (into its TMEM region) for the K block at ka.
+__device__ __forceinline__ void issue_s(uint32_t tb, int t, uint32_t qa, uint32_t ka) {
+    const uint32_t sd = tb + t * 256;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk & 3) * 32, half = kk >> 2;
+        umma_ss(sd, desc_k(qa + half * (QT_BYTES / 2) + off), desc_k(ka + half * KH_BYTES + off), IDESC_S,
+                kk > 0 ? 1u : 0u);
+    }
+}
+// O of tile t += P (TMEM, first 64 columns of its S region) . V (block at va).
+__device__ __forceinline__ void issue_pv(uint32_t tb, int t, uint32_t va, bool first) {
+    const uint32_t od = tb + t * 256 + 128;
+    const uint32_t pa = tb + t * 256;
+#pragma unroll
+    for (int kk = 0; kk < BKV / 16; ++kk)
+        umma_ts(od, pa + kk * 8, desc_mn(va + kk * 2048), IDESC_PV, (!first || kk > 0) ? 1u : 0u);
+}
+
 __global__ void __launch_bounds__(THREADS, 1)
     k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
               const __grid_constant__ CUtensorMap mapV, int n_req, const int32_t* __restrict__ req_row_end,
               const int32_t* __restrict__ row_pos, const int32_t* __restrict__ row_tok, int group, int hkv,
               int m_cap, float scale_log2, bf16* __restrict__ out, int32_t* __restrict__ err) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t q_full, q_empty, kv_full[KV_STAGES], kv_empty[KV_STAGES], s_full[2][2],
-        s_empty[2][2], p_full[2][2], pv_done[2][2], o_free[2];
+    __shared__ __align__(8) uint64_t q_full, q_empty, kv_full[KV_STAGES], kv_empty[KV_STAGES], s_full[2], p_full[2],
+        o_full[2], o_free[2];
     __shared__ uint32_t tmem_sh;
     __shared__ volatile int abort_flag;
     __shared__ int pend_kv[KV_STAGES];
     __shared__ int pend_q;
 
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    uint8_t* sQ = smem;                               // tile t at t * QT_BYTES
-    uint8_t* sKV = smem + 2 * QT_BYTES;               // stage s at s * KV_BYTES
-    uint8_t* sP = sKV + KV_STAGES * KV_BYTES;         // tile t, buffer b at (2t + b) * P_BYTES
+    uint8_t* sQ = smem;                  // tile t at t * QT_BYTES
+    uint8_t* sKV = smem + 2 * QT_BYTES;  // stage s at s * KV_BYTES
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
     int total = 0;
@@ -273,12 +288,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             pend_kv[s] = -1;
         }
         for (int t = 0; t < 2; ++t) {
-            for (int b = 0; b < 2; ++b) {
-                mbar_init(&s_full[t][b], 1);
-                mbar_init(&s_empty[t][b], 4);
-                mbar_init(&p_full[t][b], 4);
-                mbar_init(&pv_done[t][b], 1);
-            }
+            mbar_init(&s_full[t], 1);
+            mbar_init(&p_full[t], 4);
+            mbar_init(&o_full[t], 1);
             mbar_init(&o_free[t], 4);
         }
         pend_q = -1;
@@ -347,50 +359,59 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ------------------------------------------------ MMA issuer
         uint32_t it = 0, tl = 0;
         bool ok = true;
+        const uint32_t qa0 = su32(sQ), qa1 = su32(sQ + QT_BYTES);
         for (int k = 0; ok && !abort_flag; ++k, ++tl) {
             const int w = item_of(k);
             if (w >= total) break;
             Item m;
             get_item(w, n_req, req_row_end, row_pos, row_tok, group, hkv, m);
-            if (!mbar_wait(&q_full, tl & 1, &abort_flag)) {
+            if (!mbar_wait(&q_full, tl & 1, &abort_flag) ||
+                !mbar_wait(&kv_full[it % KV_STAGES], (it / KV_STAGES) & 1, &abort_flag)) {
                 ok = false;
                 break;
             }
             pend_q = -1;
+            pend_kv[it % KV_STAGES] = -1;
             fence_after();
+            {
+                const uint32_t ka = su32(sKV + (it % KV_STAGES) * KV_BYTES);
+                issue_s(tb, 0, qa0, ka);
+                commit(&s_full[0]);
+                issue_s(tb, 1, qa1, ka);
+                commit(&s_full[1]);
+            }
             for (int kb = 0; kb < m.nblk && ok; ++kb, ++it) {
                 const int st = it % KV_STAGES;
-                if (!mbar_wait(&kv_full[st], (it / KV_STAGES) & 1, &abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                pend_kv[st] = -1;
-                const uint32_t ka = su32(sKV + st * KV_BYTES);
+                const uint32_t va = su32(sKV + st * KV_BYTES + 2 * KH_BYTES);
+                const bool more = kb + 1 < m.nblk;
                 for (int t = 0; t < 2; ++t) {
-                    if (!mbar_wait(&s_empty[t][it & 1], ((it >> 1) & 1) ^ 1, &abort_flag)) {
+                    if (!mbar_wait(&p_full[t], it & 1, &abort_flag) ||
+                        (kb == 0 && !mbar_wait(&o_free[t], (tl & 1) ^ 1, &abort_flag))) {
                         ok = false;
                         break;
                     }
                     fence_after();
-                    const uint32_t qa = su32(sQ + t * QT_BYTES);
-                    const uint32_t sd = tb + t * 256 + (it & 1) * 64;
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk & 3) * 32, half = kk >> 2;
-                        umma(sd, desc_k(qa + half * (QT_BYTES / 2) + off), desc_k(ka + half * KH_BYTES + off), IDESC_S,
-                             kk > 0 ? 1u : 0u);
+                    issue_pv(tb, t, va, kb == 0);
+                    if (more) {
+                        const int nst = (it + 1) % KV_STAGES;
+                        if (t == 0) {
+                            if (!mbar_wait(&kv_full[nst], ((it + 1) / KV_STAGES) & 1, &abort_flag)) {
+                                ok = false;
+                                break;
+                            }
+                            pend_kv[nst] = -1;
+                            fence_after();
+                        }
+                        issue_s(tb, t, t == 0 ? qa0 : qa1, su32(sKV + nst * KV_BYTES));
+                        commit(&s_full[t]);
+                    } else {
+                        commit(&o_full[t]);
                     }
-                    commit(&s_full[t][it & 1]);
                 }
-                if (ok && kb > 0 &&
-                    !issue_pv(it - 1, kb - 1, tl, sKV, sP, tb, p_full, o_free, pv_done, kv_empty, &abort_flag))
-                    ok = false;
+                if (!ok) break;
+                commit(&kv_empty[st]);  // both tiles' S and PV of this block are issued
             }
-            if (!ok ||
-                !issue_pv(it - 1, m.nblk - 1, tl, sKV, sP, tb, p_full, o_free, pv_done, kv_empty, &abort_flag)) {
-                ok = false;
-                break;
-            }
+            if (!ok) break;
             commit(&q_empty);
         }
         if (!ok) {
@@ -405,10 +426,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t lane_off = (uint32_t)(sp * 32) << 16;
         const uint32_t s_col = tb + lane_off + t * 256;
         const uint32_t o_col = s_col + 128;
-        uint8_t* prow_base = sP + 2 * t * P_BYTES + r_in * 128;
-        uint32_t it = 0;
+        uint32_t it = 0, tl = 0;
         bool ok = true;
-        for (int k = 0; ok; ++k) {
+        for (int k = 0; ok; ++k, ++tl) {
             const int w = item_of(k);
             if (w >= total) break;
             Item m;
@@ -421,92 +441,78 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int my_pos = valid ? row_pos[row] : m.max_pos;
             float m_used = -INFINITY, l = 0.f;
             for (int kb = 0; kb < m.nblk; ++kb, ++it) {
-                const int b = it & 1;
-                if (!warp_wait(&s_full[t][b], (it >> 1) & 1, &abort_flag)) {
+                if (!warp_wait(&s_full[t], it & 1, &abort_flag)) {
                     ok = false;
                     break;
                 }
                 fence_after();
-                uint32_t s[64];
-                TMEM_LD32(s_col + b * 64, s);
-                TMEM_LD32(s_col + b * 64 + 32, (s + 32));
-                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-                fence_before();
-                warp_arrive(&s_empty[t][b]);
                 const int k0 = kb * BKV;
+                // all 128 scores of the row in registers with a single TMEM round trip
+                uint32_t s[128];
+                TMEM_LD32(s_col, s);
+                TMEM_LD32(s_col + 32, (s + 32));
+                TMEM_LD32(s_col + 64, (s + 64));
+                TMEM_LD32(s_col + 96, (s + 96));
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
                 if (k0 + BKV - 1 > my_pos) {
 #pragma unroll
-                    for (int i = 0; i < 64; ++i)
+                    for (int i = 0; i < 128; ++i)
                         if (k0 + i > my_pos) s[i] = __float_as_uint(-INFINITY);
                 }
                 float mx;
                 {
-                    // max by a tree (short dependency chains)
-                    float a[16];
+                    // row maximum: 8 independent chains, then a short tree
+                    float a[8];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        a[i] = fmaxf(fmaxf(__uint_as_float(s[i]), __uint_as_float(s[i + 16])),
-                                     fmaxf(__uint_as_float(s[i + 32]), __uint_as_float(s[i + 48])));
+                    for (int i = 0; i < 8; ++i) a[i] = __uint_as_float(s[i]);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) a[i] = fmaxf(a[i], a[i + 8]);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) a[i] = fmaxf(a[i], a[i + 4]);
-                    mx = fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3]));
+                    for (int i = 8; i < 128; ++i) a[i & 7] = fmaxf(a[i & 7], __uint_as_float(s[i]));
+                    mx = fmaxf(fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])), fmaxf(fmaxf(a[4], a[5]), fmaxf(a[6], a[7])));
                 }
                 const float mxs = mx * scale_log2;
                 const bool need = mxs > m_used + RESCALE_LOG2;
-                if (__any_sync(0xffffffffu, need)) {
+                const bool rescale = __any_sync(0xffffffffu, need);
+                float corr = 1.f;
+                if (rescale) {
                     const float m_new = need ? mxs : m_used;
-                    const float corr = ex2(m_used - m_new);
-                    if (kb > 0) {
-                        // O holds blocks 0..kb-1 once P.V of block kb-1 is done
-                        if (!warp_wait(&pv_done[t][(it - 1) & 1], ((it - 1) >> 1) & 1, &abort_flag)) {
-                            ok = false;
-                            break;
-                        }
-                        fence_after();
-#pragma unroll
-                        for (int c = 0; c < D; c += 32) {
-                            uint32_t o[32];
-                            TMEM_LD32(o_col + c, o);
-                            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
-                            TMEM_ST32(o_col + c, o);
-                        }
-                        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-                    }
+                    corr = ex2(m_used - m_new);
                     l *= corr;
                     m_used = m_new;
                 }
-                // the P buffer b was last read by P.V of global block it-2
-                if (it >= 2 && !warp_wait(&pv_done[t][b], ((it - 2) >> 1) & 1, &abort_flag)) {
-                    ok = false;
-                    break;
-                }
+                // P = 2^(s * scale - m_used) as bf16 pairs, packed in place: word e (keys 2e,
+                // 2e+1) lands in s[e], whose own score was consumed at step e/2
                 float sum4[4] = {0.f, 0.f, 0.f, 0.f};
-                uint8_t* prow = prow_base + b * P_BYTES;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    uint32_t w4[4];
+                for (int e = 0; e < 64; ++e) {
+                    // even keys on the MUFU unit, odd keys on the FMA pipe
+                    const float p0 = ex2(fmaf(__uint_as_float(s[2 * e]), scale_log2, -m_used));
+                    const float p1 = ex2_fma(fmaf(__uint_as_float(s[2 * e + 1]), scale_log2, -m_used));
+                    sum4[e & 3] += p0 + p1;
+                    s[e] = pack_bf16x2(p0, p1);
+                }
+                TMEM_ST32(s_col, s);
+                TMEM_ST32(s_col + 32, (s + 32));
+                if (rescale && kb > 0) {
+                    // S of this block completed after P.V of the previous one, so O is settled;
+                    // bring it to the new maximum before this block's P.V adds to it
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        // even keys on the MUFU unit, odd keys on the FMA pipe
-                        const float p0 = ex2(fmaf(__uint_as_float(s[c * 8 + 2 * e]), scale_log2, -m_used));
-                        const float p1 = ex2_fma(fmaf(__uint_as_float(s[c * 8 + 2 * e + 1]), scale_log2, -m_used));
-                        sum4[e] += p0 + p1;
-                        w4[e] = pack_bf16x2(p0, p1);
+                    for (int c = 0; c < D; c += 32) {
+                        uint32_t o[32];
+                        TMEM_LD32(o_col + c, o);
+                        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
+                        TMEM_ST32(o_col + c, o);
                     }
-                    *reinterpret_cast<uint4*>(prow + ((c ^ (r_in & 7)) * 16)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                 }
                 l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 fence_before();
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                warp_arrive(&p_full[t][b]);
+                warp_arrive(&p_full[t]);
             }
             if (!ok) break;
-            // O of this tile is final once P.V of its last block is done
-            if (!warp_wait(&pv_done[t][(it - 1) & 1], ((it - 1) >> 1) & 1, &abort_flag)) {
+            // O of this tile is final once the last P.V has completed
+            if (!warp_wait(&o_full[t], tl & 1, &abort_flag)) {
                 ok = false;
                 break;
             }

@@ -20,14 +20,21 @@
 namespace blend {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int BM = 128, BK = 64;
 constexpr int A_BYTES = BM * BK * 2;  // 16 KB
-constexpr int B_BYTES = BN * BK * 2;  // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int TMEM_COLS = 2 * BN;
 constexpr int THREADS = 192;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;  // + alignment slack
 constexpr long long SPIN_LIMIT = 1ll << 24;
+// Tile shape per N-tile width: 128x256 tiles with 4 stages of 48 KB, or 128x128 tiles
+// with 6 stages of 32 KB (used where 256-wide tiles leave the last wave mostly empty).
+template <int BN> struct TileCfg {
+    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = BN == 256 ? 4 : 6;
+    static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;  // + alignment slack
+    // kind::f16 instruction descriptor: bf16 A and B (K-major), fp32 D, M=128, N=BN
+    static constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((BN >> 3) << 17) | ((BM >> 4) << 24);
+};
 
 __device__ __forceinline__ uint32_t su32(const void* p) {
     return (uint32_t)__cvta_generic_to_shared(p);
@@ -84,19 +91,12 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
     return d;
 }
 
-// Instruction descriptor, kind::f16: bf16 A and B (K-major), fp32 D, M=128, N=256.
-constexpr uint32_t IDESC = (1u << 4)            // D format f32
-                           | (1u << 7)          // A format bf16
-                           | (1u << 10)         // B format bf16
-                           | ((BN >> 3) << 17)  // N / 8
-                           | ((BM >> 4) << 24); // M / 16
-
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t acc) {
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(IDESC), "r"(acc)
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
         : "memory");
 }
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
@@ -128,11 +128,15 @@ __device__ __forceinline__ void tc_fence_after() {
           "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])            \
         : "r"(taddr))
 
-template <int EPI>
+template <int EPI, int BN>
 __global__ void __launch_bounds__(THREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB, int K,
               int N, const int32_t* __restrict__ M_dev, void* __restrict__ Cv, int ldc,
               int32_t* __restrict__ err) {
+    using TC = TileCfg<BN>;
+    constexpr int STAGES = TC::STAGES;
+    constexpr int STAGE_BYTES = TC::STAGE_BYTES;
+    constexpr int TMEM_COLS = TC::TMEM_COLS;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2];
     __shared__ uint32_t tmem_base_sh;
@@ -219,7 +223,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const uint32_t b_addr = a_addr + A_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk)
-                    umma_bf16(d, sdesc_sw128(a_addr + kk * 32), sdesc_sw128(b_addr + kk * 32),
+                    umma_bf16(d, sdesc_sw128(a_addr + kk * 32), sdesc_sw128(b_addr + kk * 32), TC::IDESC,
                               (kb | kk) != 0);
                 umma_commit(&empty[s]);
                 if (++s == STAGES) {
@@ -353,33 +357,61 @@ int tc_available() {
         return 0;
     }
     g_encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
-    cudaFuncSetAttribute(k_gemm_tc<EPI_STORE_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    cudaFuncSetAttribute(k_gemm_tc<EPI_ADD_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    cudaFuncSetAttribute(k_gemm_tc<EPI_SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    cudaFuncSetAttribute(k_gemm_tc<EPI_STORE_F32, 256>, cudaFuncAttributeMaxDynamicSharedMemorySize, TileCfg<256>::SMEM_BYTES);
+    cudaFuncSetAttribute(k_gemm_tc<EPI_ADD_F32, 256>, cudaFuncAttributeMaxDynamicSharedMemorySize, TileCfg<256>::SMEM_BYTES);
+    cudaFuncSetAttribute(k_gemm_tc<EPI_SWIGLU, 256>, cudaFuncAttributeMaxDynamicSharedMemorySize, TileCfg<256>::SMEM_BYTES);
+    cudaFuncSetAttribute(k_gemm_tc<EPI_STORE_F32, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, TileCfg<128>::SMEM_BYTES);
+    cudaFuncSetAttribute(k_gemm_tc<EPI_ADD_F32, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, TileCfg<128>::SMEM_BYTES);
+    cudaFuncSetAttribute(k_gemm_tc<EPI_SWIGLU, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, TileCfg<128>::SMEM_BYTES);
     g_tc_state = 1;
     return 1;
 }
 
 bool tc_gemm_supported(int K, int N, int epi, int ldc, int M_cap) {
     (void)epi;
-    return K >= BK && K % BK == 0 && N >= BN && N % BN == 0 && ldc % 8 == 0 && M_cap >= BM;
+    return K >= BK && K % BK == 0 && N >= 128 && N % 128 == 0 && ldc % 8 == 0 && M_cap >= BM;
+}
+
+// N-tile width: 256 unless N is not a multiple of 256.  (128-wide tiles fill the last
+// wave better for N = 5120 at ~3.3K rows, but measured 30-40 % slower per FLOP.)
+int pick_bn(int M_max, int N) {
+    if (N % 256 != 0) return 128;
+    const long long m_tiles = (M_max + BM - 1) / BM;
+    auto fill = [&](int bn) {
+        const long long tiles = m_tiles * (N / bn);
+        const long long waves = (tiles + g_num_sms - 1) / g_num_sms;
+        return (double)tiles / (double)(waves * g_num_sms);
+    };
+    (void)fill;
+    return 256;  // 128x128 tiles measured slower even with better wave fill
+}
+
+template <int BN>
+void launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, int K, int N, const int32_t* M_dev, int M_max,
+               int epi, void* C, int ldc, int32_t* err, cudaStream_t s) {
+    const int tiles = ((M_max + BM - 1) / BM) * (N / BN);
+    const int grid = tiles < g_num_sms ? tiles : g_num_sms;
+    constexpr int SM = TileCfg<BN>::SMEM_BYTES;
+    if (epi == EPI_STORE_F32)
+        k_gemm_tc<EPI_STORE_F32, BN><<<grid, THREADS, SM, s>>>(ma, mb, K, N, M_dev, C, ldc, err);
+    else if (epi == EPI_ADD_F32)
+        k_gemm_tc<EPI_ADD_F32, BN><<<grid, THREADS, SM, s>>>(ma, mb, K, N, M_dev, C, ldc, err);
+    else
+        k_gemm_tc<EPI_SWIGLU, BN><<<grid, THREADS, SM, s>>>(ma, mb, K, N, M_dev, C, ldc, err);
 }
 
 int launch_gemm_tc(const void* A, int K, int M_cap, const void* B, int N, const int32_t* M_dev, int M_max,
                    int epi, void* C, int ldc, int32_t* err, cudaStream_t s) {
     if (M_max <= 0) return BLEND_OK;
+    const int bn = pick_bn(M_max, N);
     CUtensorMap ma, mb;
     if (!encode_2d(&ma, A, (uint64_t)K, (uint64_t)M_cap, BK, BM) ||
-        !encode_2d(&mb, B, (uint64_t)K, (uint64_t)N, BK, BN))
+        !encode_2d(&mb, B, (uint64_t)K, (uint64_t)N, BK, (uint32_t)bn))
         return BLEND_EUNSUPPORTED;  // the operands cannot be described to the TMA unit
-    const int tiles = ((M_max + BM - 1) / BM) * (N / BN);
-    const int grid = tiles < g_num_sms ? tiles : g_num_sms;
-    if (epi == EPI_STORE_F32)
-        k_gemm_tc<EPI_STORE_F32><<<grid, THREADS, SMEM_BYTES, s>>>(ma, mb, K, N, M_dev, C, ldc, err);
-    else if (epi == EPI_ADD_F32)
-        k_gemm_tc<EPI_ADD_F32><<<grid, THREADS, SMEM_BYTES, s>>>(ma, mb, K, N, M_dev, C, ldc, err);
+    if (bn == 256)
+        launch_bn<256>(ma, mb, K, N, M_dev, M_max, epi, C, ldc, err, s);
     else
-        k_gemm_tc<EPI_SWIGLU><<<grid, THREADS, SMEM_BYTES, s>>>(ma, mb, K, N, M_dev, C, ldc, err);
+        launch_bn<128>(ma, mb, K, N, M_dev, M_max, epi, C, ldc, err, s);
     note_launch(1);
     return BLEND_OK;
 }
