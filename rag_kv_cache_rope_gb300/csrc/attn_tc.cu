@@ -11,9 +11,10 @@
 //   S = Q . K^T   tcgen05.mma M128 N128 K16 x8, shared-memory operands -> TMEM
 //   P             one softmax warpgroup per tile, one pair row per thread: the row's 128
 //                 scores come to registers in one TMEM round trip; row maximum (causal mask
-//                 on boundary blocks), then bf16 P (base 2, scale folded into one FFMA, half
-//                 of the exponentials on the FMA pipe) written back over S's first 64 TMEM
-//                 columns in one more round trip
+//                 on boundary blocks), then bf16 P (base 2, scale folded into one FFMA)
+//                 written back over S's first 64 TMEM columns in one more round trip.  (A
+//                 polynomial 2^x on the FMA pipe for part of the keys was measured slower:
+//                 the softmax is bound by issue slots, not by the MUFU unit.)
 //   O += P . V    tcgen05.mma M128 N128 K16 x8 with A = P read from TMEM and V an
 //                 MN-major shared-memory operand; O stays in TMEM for the whole item.
 // Per tile the products run S(j), PV(j), S(j+1): the tensor core executes one CTA's
@@ -153,21 +154,6 @@ __device__ __forceinline__ float ex2(float x) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
-// 2^x on the FMA pipe, for part of the scores so the MUFU unit is not the only source of
-// exponentials: x = n + f with n = round(x) (1.5 * 2^23 rounding trick, no conversion
-// instruction), 2^f by a cubic fitted here to minimise the relative error on
-// [-0.5, 0.5] (7.5e-5; 1.4e-4 with fp32 rounding), 2^n added to the exponent bits.
-// x below -126 (masked scores are -inf) gives exactly 0.
-__device__ __forceinline__ float ex2_fma(float x) {
-    const float xc = fmaxf(x, -127.f);
-    const float t = xc + 12582912.f;
-    const int n = __float_as_int(t) - 0x4B400000;
-    const float f = xc - (t - 12582912.f);
-    const float p = fmaf(fmaf(fmaf(0.055170551f, f, 0.24260864f), f, 0.69326095f), f, 0.99992825f);
-    const float r = __int_as_float(__float_as_int(p) + (n << 23));
-    return x < -126.f ? 0.f : r;
-}
-
 #define TMEM_LD32(taddr, r)                                                                          \
     asm volatile(                                                                                    \
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"   \
@@ -484,9 +470,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 float sum4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int e = 0; e < 64; ++e) {
-                    // even keys on the MUFU unit, odd keys on the FMA pipe
                     const float p0 = ex2(fmaf(__uint_as_float(s[2 * e]), scale_log2, -m_used));
-                    const float p1 = ex2_fma(fmaf(__uint_as_float(s[2 * e + 1]), scale_log2, -m_used));
+                    const float p1 = ex2(fmaf(__uint_as_float(s[2 * e + 1]), scale_log2, -m_used));
                     sum4[e & 3] += p0 + p1;
                     s[e] = pack_bf16x2(p0, p1);
                 }
