@@ -309,6 +309,18 @@ void layer_kv(blend_handle* h, int l, const float* x, const Plan& p, const int32
     const int H = c.hidden, d = c.head_dim;
     const int width = (c.n_q_heads + 2 * c.n_kv_heads) * d;
     { ProfScope ps(h, PROF_NORM, s); launch_rmsnorm(c.dtype, x, lw.attn_norm, h->xn, H, c.rms_eps, p.M, M_max, s); }
+    const bool fused = dev == nullptr && c.dtype == BLEND_BF16 && h->use_tc && d == 128 && width % 256 == 0 &&
+                       tc_gemm_supported(H, width, EPI_QKV_ROPE, width, h->lim.max_rows);
+    if (fused) {
+        // projection, RoPE, q layout and the K/V cache write in one kernel
+        ProfScope ps(h, PROF_GEMM_QKV, s);
+        QkvEpi qe{p.row_pos, p.row_tok, h->rope, (bf16*)h->q, (bf16*)kc, (bf16*)vc, h->lim.max_rows,
+                  c.n_q_heads / c.n_kv_heads, c.n_q_heads, c.n_kv_heads};
+        int rc = launch_gemm_tc(h->xn, H, h->lim.max_rows, lw.w_qkv, width, p.M, M_max, EPI_QKV_ROPE, nullptr, 0,
+                                h->err, s, &qe);
+        if (rc != BLEND_OK && h->host_rc == BLEND_OK) h->host_rc = rc;
+        return;
+    }
     { ProfScope ps(h, PROF_GEMM_QKV, s); gemm(h, h->xn, H, lw.w_qkv, width, EPI_STORE_F32, h->qkv, width, p.M, M_max, s); }
     ProfScope ps(h, PROF_ROPE_KV, s);
     launch_rope_qkv(c.dtype, h->qkv, p.row_pos, p.row_tok, row_req, p.M, M_max, bd, c.n_q_heads,

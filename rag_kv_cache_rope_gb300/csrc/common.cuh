@@ -175,7 +175,19 @@ struct SelectBatch {
 void launch_select(const SelectBatch& sb, int32_t* rank_scratch, int max_n, cudaStream_t s);
 
 // ------------------------------ GEMM (gemm_simt.cu) --------------------------------
-enum Epi { EPI_STORE_F32 = 0, EPI_ADD_F32 = 1, EPI_SWIGLU = 2 };
+enum Epi { EPI_STORE_F32 = 0, EPI_ADD_F32 = 1, EPI_SWIGLU = 2, EPI_QKV_ROPE = 3 };
+// Extra arguments of the fused QKV epilogue (tensor-core GEMM, head_dim 128): rotate q and
+// k at each row's blended position, store q per kv head ([m_cap][group][128] slabs) and
+// k, v straight into this layer's cache rows [tok][hkv][128].
+struct QkvEpi {
+    const int32_t* row_pos;
+    const int32_t* row_tok;
+    const float2* rope;  // [max_pos][64] (cos, sin)
+    bf16* q;
+    bf16* k_cache;
+    bf16* v_cache;
+    int m_cap, group, hq, hkv;
+};
 // C = A[M,K] . B[N,K]^T with A, B of the model dtype; epilogue:
 //   EPI_STORE_F32: C fp32 [M][ldc] = acc
 //   EPI_ADD_F32:   C fp32 [M][ldc] += acc

@@ -6,7 +6,9 @@
 //   warp 0      TMA producer: 128x64 A tile + 256x64 B tile per stage (128-byte swizzle)
 //   warp 1      TMEM allocator and MMA issuer: tcgen05.mma kind::f16, M=128 N=256 K=16,
 //               4 per stage; tcgen05.commit frees the stage / publishes the accumulator
-//   warps 2..5  epilogue: tcgen05.ld of their 32 TMEM lanes (one output row per thread)
+//   warps 2..5  epilogue: tcgen05.ld of their 32 TMEM lanes (one output row per thread);
+//               fp32 store, fp32 residual add, SwiGLU, or the QKV epilogue (RoPE at each
+//               row's position, q to its per-kv-head slab, k and v into the KV cache)
 // Two 256-column fp32 accumulators (all 512 TMEM columns) let the epilogue of one tile
 // overlap the main loop of the next.  M is read from the device; tiles past it are
 // skipped.  Every mbarrier wait is bounded: on expiry the kernel records
@@ -132,7 +134,7 @@ template <int EPI, int BN>
 __global__ void __launch_bounds__(THREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB, int K,
               int N, const int32_t* __restrict__ M_dev, void* __restrict__ Cv, int ldc,
-              int32_t* __restrict__ err) {
+              int32_t* __restrict__ err, const __grid_constant__ QkvEpi qe) {
     using TC = TileCfg<BN>;
     constexpr int STAGES = TC::STAGES;
     constexpr int STAGE_BYTES = TC::STAGE_BYTES;
@@ -257,6 +259,62 @@ __global__ void __launch_bounds__(THREADS, 1)
             tc_fence_after();
             const int row = mt * BM + r_in;
             const uint32_t tl = tbase + ((uint32_t)(sp * 32) << 16) + (uint32_t)(b * BN);
+            if (EPI == EPI_QKV_ROPE) {
+                // the tile holds BN/128 whole heads of this row: q and k heads are rotated at
+                // the row's position (pairs i, i+64), then q goes to its per-kv-head slab and
+                // k, v to the cache row of the row's token
+                const bool live = row < M;
+                const int pos = live ? qe.row_pos[row] : 0;
+                const long long tok = live ? qe.row_tok[row] : 0;
+#pragma unroll 1
+                for (int hh = 0; hh < BN / 128; ++hh) {
+                    const int head = nt * (BN / 128) + hh;
+                    bf16* dst;
+                    bool rotate = true;
+                    if (head < qe.hq) {
+                        dst = qe.q + (((long long)(head / qe.group) * qe.m_cap + row) * qe.group + head % qe.group) * 128;
+                    } else if (head < qe.hq + qe.hkv) {
+                        dst = qe.k_cache + (tok * qe.hkv + (head - qe.hq)) * 128;
+                    } else {
+                        dst = qe.v_cache + (tok * qe.hkv + (head - qe.hq - qe.hkv)) * 128;
+                        rotate = false;
+                    }
+#pragma unroll 1
+                    for (int c = 0; c < 64; c += 32) {
+                        uint32_t x1[32], x2[32];
+                        TMEM_LD32(tl + hh * 128 + c, x1);
+                        TMEM_LD32(tl + hh * 128 + 64 + c, x2);
+                        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                        if (live) {
+                            uint32_t w1[16], w2[16];
+                            if (rotate) {
+                                const float4* cs = reinterpret_cast<const float4*>(qe.rope + (long long)pos * 64 + c);
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) {
+                                    const float4 t = cs[i];  // (cos, sin) of pairs 2i and 2i+1
+                                    const float a0 = __uint_as_float(x1[2 * i]), b0 = __uint_as_float(x2[2 * i]);
+                                    const float a1 = __uint_as_float(x1[2 * i + 1]), b1 = __uint_as_float(x2[2 * i + 1]);
+                                    w1[i] = pack_bf16x2(a0 * t.x - b0 * t.y, a1 * t.z - b1 * t.w);
+                                    w2[i] = pack_bf16x2(b0 * t.x + a0 * t.y, b1 * t.z + a1 * t.w);
+                                }
+                            } else {
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) {
+                                    w1[i] = pack_bf16x2(__uint_as_float(x1[2 * i]), __uint_as_float(x1[2 * i + 1]));
+                                    w2[i] = pack_bf16x2(__uint_as_float(x2[2 * i]), __uint_as_float(x2[2 * i + 1]));
+                                }
+                            }
+                            uint4* d1 = reinterpret_cast<uint4*>(dst + c);
+                            uint4* d2 = reinterpret_cast<uint4*>(dst + 64 + c);
+#pragma unroll
+                            for (int v = 0; v < 4; ++v) {
+                                d1[v] = make_uint4(w1[4 * v], w1[4 * v + 1], w1[4 * v + 2], w1[4 * v + 3]);
+                                d2[v] = make_uint4(w2[4 * v], w2[4 * v + 1], w2[4 * v + 2], w2[4 * v + 3]);
+                            }
+                        }
+                    }
+                }
+            } else {
 #pragma unroll 1
             for (int c = 0; c < BN; c += 32) {
                 uint32_t r[32];
@@ -294,6 +352,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         p[1] = make_uint4(w8[4], w8[5], w8[6], w8[7]);
                     }
                 }
+            }
             }
             tc_fence_before();
             __syncwarp();
@@ -360,9 +419,11 @@ int tc_available() {
     cudaFuncSetAttribute(k_gemm_tc<EPI_STORE_F32, 256>, cudaFuncAttributeMaxDynamicSharedMemorySize, TileCfg<256>::SMEM_BYTES);
     cudaFuncSetAttribute(k_gemm_tc<EPI_ADD_F32, 256>, cudaFuncAttributeMaxDynamicSharedMemorySize, TileCfg<256>::SMEM_BYTES);
     cudaFuncSetAttribute(k_gemm_tc<EPI_SWIGLU, 256>, cudaFuncAttributeMaxDynamicSharedMemorySize, TileCfg<256>::SMEM_BYTES);
+    cudaFuncSetAttribute(k_gemm_tc<EPI_QKV_ROPE, 256>, cudaFuncAttributeMaxDynamicSharedMemorySize, TileCfg<256>::SMEM_BYTES);
     cudaFuncSetAttribute(k_gemm_tc<EPI_STORE_F32, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, TileCfg<128>::SMEM_BYTES);
     cudaFuncSetAttribute(k_gemm_tc<EPI_ADD_F32, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, TileCfg<128>::SMEM_BYTES);
     cudaFuncSetAttribute(k_gemm_tc<EPI_SWIGLU, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, TileCfg<128>::SMEM_BYTES);
+    cudaFuncSetAttribute(k_gemm_tc<EPI_QKV_ROPE, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, TileCfg<128>::SMEM_BYTES);
     g_tc_state = 1;
     return 1;
 }
@@ -388,30 +449,35 @@ int pick_bn(int M_max, int N) {
 
 template <int BN>
 void launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, int K, int N, const int32_t* M_dev, int M_max,
-               int epi, void* C, int ldc, int32_t* err, cudaStream_t s) {
+               int epi, void* C, int ldc, int32_t* err, cudaStream_t s, const QkvEpi& qe) {
     const int tiles = ((M_max + BM - 1) / BM) * (N / BN);
     const int grid = tiles < g_num_sms ? tiles : g_num_sms;
     constexpr int SM = TileCfg<BN>::SMEM_BYTES;
     if (epi == EPI_STORE_F32)
-        k_gemm_tc<EPI_STORE_F32, BN><<<grid, THREADS, SM, s>>>(ma, mb, K, N, M_dev, C, ldc, err);
+        k_gemm_tc<EPI_STORE_F32, BN><<<grid, THREADS, SM, s>>>(ma, mb, K, N, M_dev, C, ldc, err, qe);
     else if (epi == EPI_ADD_F32)
-        k_gemm_tc<EPI_ADD_F32, BN><<<grid, THREADS, SM, s>>>(ma, mb, K, N, M_dev, C, ldc, err);
+        k_gemm_tc<EPI_ADD_F32, BN><<<grid, THREADS, SM, s>>>(ma, mb, K, N, M_dev, C, ldc, err, qe);
+    else if (epi == EPI_SWIGLU)
+        k_gemm_tc<EPI_SWIGLU, BN><<<grid, THREADS, SM, s>>>(ma, mb, K, N, M_dev, C, ldc, err, qe);
     else
-        k_gemm_tc<EPI_SWIGLU, BN><<<grid, THREADS, SM, s>>>(ma, mb, K, N, M_dev, C, ldc, err);
+        k_gemm_tc<EPI_QKV_ROPE, BN><<<grid, THREADS, SM, s>>>(ma, mb, K, N, M_dev, C, ldc, err, qe);
 }
 
 int launch_gemm_tc(const void* A, int K, int M_cap, const void* B, int N, const int32_t* M_dev, int M_max,
-                   int epi, void* C, int ldc, int32_t* err, cudaStream_t s) {
+                   int epi, void* C, int ldc, int32_t* err, cudaStream_t s, const QkvEpi* qkv) {
     if (M_max <= 0) return BLEND_OK;
     const int bn = pick_bn(M_max, N);
+    if (epi == EPI_QKV_ROPE && (qkv == nullptr || bn != 256)) return BLEND_EUNSUPPORTED;
+    QkvEpi qe{};
+    if (qkv) qe = *qkv;
     CUtensorMap ma, mb;
     if (!encode_2d(&ma, A, (uint64_t)K, (uint64_t)M_cap, BK, BM) ||
         !encode_2d(&mb, B, (uint64_t)K, (uint64_t)N, BK, (uint32_t)bn))
         return BLEND_EUNSUPPORTED;  // the operands cannot be described to the TMA unit
     if (bn == 256)
-        launch_bn<256>(ma, mb, K, N, M_dev, M_max, epi, C, ldc, err, s);
+        launch_bn<256>(ma, mb, K, N, M_dev, M_max, epi, C, ldc, err, s, qe);
     else
-        launch_bn<128>(ma, mb, K, N, M_dev, M_max, epi, C, ldc, err, s);
+        launch_bn<128>(ma, mb, K, N, M_dev, M_max, epi, C, ldc, err, s, qe);
     note_launch(1);
     return BLEND_OK;
 }

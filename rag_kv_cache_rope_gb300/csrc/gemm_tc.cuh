@@ -13,7 +13,7 @@ bool tc_gemm_supported(int K, int N, int epi, int ldc, int M_cap);
 // A: [M_cap][K] bf16 buffer whose first *M_dev rows are used; B: [N][K] bf16.
 // Returns BLEND_OK or BLEND_EUNSUPPORTED (operands not describable by a tensor map).
 int launch_gemm_tc(const void* A, int K, int M_cap, const void* B, int N, const int32_t* M_dev, int M_max,
-                   int epi, void* C, int ldc, int32_t* err, cudaStream_t s);
+                   int epi, void* C, int ldc, int32_t* err, cudaStream_t s, const QkvEpi* qkv = nullptr);
 // Tensor-core attention (attn_tc.cu): head_dim 128, bf16.
 bool tc_attn_supported(int head_dim);
 // q: per kv head a slab [m_cap][group][128]; rows of request r are

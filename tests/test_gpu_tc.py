@@ -57,6 +57,12 @@ def test_layer_tensor_cores_match_oracle_and_cuda_cores(shape, n, n_ctx):
         b.selective_layer(r.h, 1, xg, pos.to(dev), n, kg, vg, n_ctx, dv)
         b.blend_device_status(r.h)
         outs[tc] = (f64(xg), f64(kg), f64(vg), f64(dv))
+    # without a deviation output the projection, RoPE and cache write run as one fused kernel
+    b.blend_set_tensor_cores(r.h, True)
+    xg, kg, vg = x.to(dev), kc.to(dev), vc.to(dev)
+    b.selective_layer(r.h, 1, xg, pos.to(dev), n, kg, vg, n_ctx, None)
+    b.blend_device_status(r.h)
+    fused = (f64(xg), f64(kg), f64(vg))
     K, V = f64(kc), f64(vc)
     xo, dref = O.layer_forward(case.w_np, oracle_cfg(shape), 1, f64(x), pos.numpy(), K, V,
                                np.ones(n, dtype=bool))
@@ -65,5 +71,8 @@ def test_layer_tensor_cores_match_oracle_and_cuda_cores(shape, n, n_ctx):
         assert maxrel(vg, V) <= TOL_BF16, tc
         assert maxrel(xg, xo) <= TOL_BF16, tc
         assert maxrel(dv, dref) <= TOL_BF16, tc
-    # the two GPU paths differ only by fp32 summation order
+    assert maxrel(fused[1], K) <= TOL_BF16 and maxrel(fused[2], V) <= TOL_BF16
+    assert maxrel(fused[0], xo) <= TOL_BF16
+    # the GPU paths differ only by fp32 summation order and where bf16 rounding happens
     assert maxrel(outs[True][0], outs[False][0]) <= 1e-2
+    assert maxrel(fused[0], outs[True][0]) <= 1e-2
