@@ -11,10 +11,9 @@
 //   S = Q . K^T   tcgen05.mma M128 N128 K16 x8, shared-memory operands -> TMEM
 //   P             one softmax warpgroup per tile, one pair row per thread: the row's 128
 //                 scores come to registers in one TMEM round trip; row maximum (causal mask
-//                 on boundary blocks), then bf16 P (base 2, scale folded into one FFMA)
-//                 written back over S's first 64 TMEM columns in one more round trip.  (A
-//                 polynomial 2^x on the FMA pipe for part of the keys was measured slower:
-//                 the softmax is bound by issue slots, not by the MUFU unit.)
+//                 on boundary blocks; three-input max), then bf16 P (base 2, scale folded
+//                 into paired FMAs, sums in paired adds, 2^x on the MUFU unit) written back
+//                 over S's first 64 TMEM columns in one more round trip.
 //   O += P . V    tcgen05.mma M128 N128 K16 x8 with A = P read from TMEM and V an
 //                 MN-major shared-memory operand; O stays in TMEM for the whole item.
 // Per tile the products run S(j), PV(j), S(j+1): the tensor core executes one CTA's
@@ -75,14 +74,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t par, volatile in
     }
     return false;
 }
-// Warp-level bounded wait: lane 0 polls, the result is broadcast, and __syncwarp orders
-// the other lanes after lane 0's acquire.
+// Warp-level bounded wait: every lane polls (a convergent loop, no lane-0 divergence)
+// until all lanes have seen the phase complete.
 __device__ __forceinline__ bool warp_wait(uint64_t* b, uint32_t par, volatile int* abort_flag) {
-    bool ok = true;
-    if ((threadIdx.x & 31) == 0) ok = mbar_wait(b, par, abort_flag);
-    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-    __syncwarp();
-    return ok;
+    for (long long i = 0; i < SPIN_LIMIT; ++i) {
+        if (__all_sync(0xffffffffu, mbar_try(b, par))) return true;
+        if ((i & 255) == 255 && __any_sync(0xffffffffu, *abort_flag != 0)) return false;
+    }
+    return false;
 }
 // Warp-level arrive (barriers count warps): __syncwarp orders every lane's prior work
 // before lane 0's release-arrive.
@@ -148,6 +147,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
+}
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
 }
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -218,23 +222,25 @@ __device__ __forceinline__ bool get_item(int w, int n_req, const int32_t* req_ro
     return false;
 }
 
-// S of tile t (into its TMEM region) for the K block at ka.
-__device__ __forceinline__ void issue_s(uint32_t tb, int t, uint32_t qa, uint32_t ka) {
+// S of tile t (into its TMEM region) for the K block whose descriptor base is kd; the
+// start-address field of a descriptor holds address / 16, so operand steps are added to
+// the descriptor itself (shared addresses stay below 2^18, so the field never carries).
+__device__ __forceinline__ void issue_s(uint32_t tb, int t, uint64_t qd, uint64_t kd) {
     const uint32_t sd = tb + t * 256;
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (kk & 3) * 32, half = kk >> 2;
-        umma_ss(sd, desc_k(qa + half * (QT_BYTES / 2) + off), desc_k(ka + half * KH_BYTES + off), IDESC_S,
+        umma_ss(sd, qd + ((half * (QT_BYTES / 2) + off) >> 4), kd + ((half * KH_BYTES + off) >> 4), IDESC_S,
                 kk > 0 ? 1u : 0u);
     }
 }
-// O of tile t += P (TMEM, first 64 columns of its S region) . V (block at va).
-__device__ __forceinline__ void issue_pv(uint32_t tb, int t, uint32_t va, bool first) {
+// O of tile t += P (TMEM, first 64 columns of its S region) . V (block descriptor base vd).
+__device__ __forceinline__ void issue_pv(uint32_t tb, int t, uint64_t vd, bool first) {
     const uint32_t od = tb + t * 256 + 128;
     const uint32_t pa = tb + t * 256;
 #pragma unroll
     for (int kk = 0; kk < BKV / 16; ++kk)
-        umma_ts(od, pa + kk * 8, desc_mn(va + kk * 2048), IDESC_PV, (!first || kk > 0) ? 1u : 0u);
+        umma_ts(od, pa + kk * 8, vd + ((kk * 2048) >> 4), IDESC_PV, (!first || kk > 0) ? 1u : 0u);
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
@@ -345,7 +351,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ------------------------------------------------ MMA issuer
         uint32_t it = 0, tl = 0;
         bool ok = true;
-        const uint32_t qa0 = su32(sQ), qa1 = su32(sQ + QT_BYTES);
+        const uint64_t qd0 = desc_k(su32(sQ)), qd1 = desc_k(su32(sQ + QT_BYTES));
         for (int k = 0; ok && !abort_flag; ++k, ++tl) {
             const int w = item_of(k);
             if (w >= total) break;
@@ -360,15 +366,15 @@ __global__ void __launch_bounds__(THREADS, 1)
             pend_kv[it % KV_STAGES] = -1;
             fence_after();
             {
-                const uint32_t ka = su32(sKV + (it % KV_STAGES) * KV_BYTES);
-                issue_s(tb, 0, qa0, ka);
+                const uint64_t kd = desc_k(su32(sKV + (it % KV_STAGES) * KV_BYTES));
+                issue_s(tb, 0, qd0, kd);
                 commit(&s_full[0]);
-                issue_s(tb, 1, qa1, ka);
+                issue_s(tb, 1, qd1, kd);
                 commit(&s_full[1]);
             }
             for (int kb = 0; kb < m.nblk && ok; ++kb, ++it) {
                 const int st = it % KV_STAGES;
-                const uint32_t va = su32(sKV + st * KV_BYTES + 2 * KH_BYTES);
+                const uint64_t vd = desc_mn(su32(sKV + st * KV_BYTES + 2 * KH_BYTES));
                 const bool more = kb + 1 < m.nblk;
                 for (int t = 0; t < 2; ++t) {
                     if (!mbar_wait(&p_full[t], it & 1, &abort_flag) ||
@@ -377,7 +383,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         break;
                     }
                     fence_after();
-                    issue_pv(tb, t, va, kb == 0);
+                    issue_pv(tb, t, vd, kb == 0);
                     if (more) {
                         const int nst = (it + 1) % KV_STAGES;
                         if (t == 0) {
@@ -388,7 +394,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                             pend_kv[nst] = -1;
                             fence_after();
                         }
-                        issue_s(tb, t, t == 0 ? qa0 : qa1, su32(sKV + nst * KV_BYTES));
+                        issue_s(tb, t, t == 0 ? qd0 : qd1, desc_k(su32(sKV + nst * KV_BYTES)));
                         commit(&s_full[t]);
                     } else {
                         commit(&o_full[t]);
@@ -450,10 +456,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                     // row maximum: 8 independent chains, then a short tree
                     float a[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) a[i] = __uint_as_float(s[i]);
+                    for (int i = 0; i < 8; ++i) a[i] = fmaxf(__uint_as_float(s[i]), __uint_as_float(s[i + 8]));
 #pragma unroll
-                    for (int i = 8; i < 128; ++i) a[i & 7] = fmaxf(a[i & 7], __uint_as_float(s[i]));
-                    mx = fmaxf(fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])), fmaxf(fmaxf(a[4], a[5]), fmaxf(a[6], a[7])));
+                    for (int i = 16; i < 128; i += 16)
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) a[c] = max3f(a[c], __uint_as_float(s[i + c]), __uint_as_float(s[i + 8 + c]));
+                    mx = max3f(max3f(a[0], a[1], a[2]), max3f(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
                 }
                 const float mxs = mx * scale_log2;
                 const bool need = mxs > m_used + RESCALE_LOG2;
@@ -467,14 +475,16 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 // P = 2^(s * scale - m_used) as bf16 pairs, packed in place: word e (keys 2e,
                 // 2e+1) lands in s[e], whose own score was consumed at step e/2
-                float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+                float2 acc2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                const float2 sc2 = make_float2(scale_log2, scale_log2), nm2 = make_float2(-m_used, -m_used);
 #pragma unroll
                 for (int e = 0; e < 64; ++e) {
-                    const float p0 = ex2(fmaf(__uint_as_float(s[2 * e]), scale_log2, -m_used));
-                    const float p1 = ex2(fmaf(__uint_as_float(s[2 * e + 1]), scale_log2, -m_used));
-                    sum4[e & 3] += p0 + p1;
+                    const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1])), sc2, nm2);
+                    const float p0 = ex2(x.x), p1 = ex2(x.y);
+                    acc2[e & 1] = __fadd2_rn(acc2[e & 1], make_float2(p0, p1));
                     s[e] = pack_bf16x2(p0, p1);
                 }
+                const float2 accs = __fadd2_rn(acc2[0], acc2[1]);
                 TMEM_ST32(s_col, s);
                 TMEM_ST32(s_col + 32, (s + 32));
                 if (rescale && kb > 0) {
@@ -490,7 +500,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         TMEM_ST32(o_col + c, o);
                     }
                 }
-                l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+                l += accs.x + accs.y;
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 fence_before();
                 warp_arrive(&p_full[t]);
