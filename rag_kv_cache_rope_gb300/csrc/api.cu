@@ -82,6 +82,8 @@ struct blend_handle {
     uint8_t* mask;
     float* dev[2];
     int32_t* scratch_n;
+    float* split_ws;     // tensor-core GEMM: partials of last-wave tiles run as K halves
+    int32_t* split_cnt;  // their arrival counters (zero between launches)
     int use_tc;  // tensor-core GEMM for bf16
     int host_rc = 0;  // first failure of an internal launch during the current call
     std::string last_error;
@@ -238,6 +240,8 @@ Layout make_layout(const blend_model_cfg* c, const blend_limits* l) {
     L.add(nc * 4);                                         // 31 dev1
     L.add(nc * 4);                                         // 32 dev2
     L.add(16);                                             // 33 scratch count
+    L.add(c->dtype == BLEND_BF16 ? GEMM_SPLIT_WS_FLOATS * 4 : 0);  // 34 GEMM split partials
+    L.add(GEMM_SPLIT_CNT_INTS * 4);                        // 35 GEMM split counters
     return L;
 }
 
@@ -266,7 +270,8 @@ LayerW layer_w(const blend_handle* h, int l) {
 void gemm(blend_handle* h, const void* A, int K, const void* B, int N, int epi, void* C, int ldc,
           const int32_t* M_dev, int M_max, cudaStream_t s) {
     if (h->cfg.dtype == BLEND_BF16 && h->use_tc && tc_gemm_supported(K, N, epi, ldc, h->lim.max_rows)) {
-        int rc = launch_gemm_tc(A, K, h->lim.max_rows, B, N, M_dev, M_max, epi, C, ldc, h->err, s);
+        int rc = launch_gemm_tc(A, K, h->lim.max_rows, B, N, M_dev, M_max, epi, C, ldc, h->err, s, nullptr,
+                                h->split_ws, h->split_cnt);
         if (rc != BLEND_OK && h->host_rc == BLEND_OK) h->host_rc = rc;
     } else
         launch_gemm_simt(h->cfg.dtype, A, K, B, K, K, N, M_dev, M_max, epi, C, ldc, s);
@@ -390,9 +395,13 @@ int blend_init(const blend_model_cfg* cfg, const blend_weights* w, const blend_l
     h->dev[0] = (float*)(b + L.off[i++]);
     h->dev[1] = (float*)(b + L.off[i++]);
     h->scratch_n = (int32_t*)(b + L.off[i++]);
+    h->split_ws = cfg->dtype == BLEND_BF16 ? (float*)(b + L.off[i]) : nullptr;
+    ++i;
+    h->split_cnt = (int32_t*)(b + L.off[i++]);
     h->use_tc = cfg->dtype == BLEND_BF16 ? tc_available() : 0;
     cudaStream_t s = (cudaStream_t)stream;
     cudaMemsetAsync(h->err, 0, 16, s);
+    cudaMemsetAsync(h->split_cnt, 0, GEMM_SPLIT_CNT_INTS * 4, s);
     launch_rope_table(h->rope, cfg->max_pos, cfg->head_dim, cfg->rope_theta, s);
     int rc = check_cuda(h, "blend_init");
     if (rc != BLEND_OK) {
@@ -420,6 +429,8 @@ int blend_device_status(blend_handle* h, void* stream) {
         return check_cuda(h, "blend_device_status");
     if (e != 0) {
         cudaMemset(h->err, 0, 4);
+        // an interrupted GEMM may have left split-tile counters raised
+        cudaMemset(h->split_cnt, 0, GEMM_SPLIT_CNT_INTS * 4);
         return fail(h, e == BLEND_ETIMEOUT ? BLEND_ETIMEOUT : BLEND_EDEVICE,
                     "device-side check failed (code %d)", e);
     }

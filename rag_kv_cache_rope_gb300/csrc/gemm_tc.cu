@@ -11,7 +11,14 @@
 //               row's position, q to its per-kv-head slab, k and v into the KV cache)
 // Two 256-column fp32 accumulators (all 512 TMEM columns) let the epilogue of one tile
 // overlap the main loop of the next.  M is read from the device; tiles past it are
-// skipped.  Every mbarrier wait is bounded: on expiry the kernel records
+// skipped.
+// Tail split: tiles are dealt to the persistent CTAs in waves of gridDim.x.  When the
+// last wave is at most half full, each of its tiles is cut into two K halves run by two
+// CTAs, so that wave takes half a tile's time.  Each half writes its fp32 partial to a
+// workspace slab and counts in on a per-(tile, lane quarter) counter; the warp that
+// counts second adds the other partial to its own (a commutative sum of two terms, so
+// the result does not depend on which half finished first), runs the epilogue on the
+// sum and resets the counter.  No thread waits for another CTA.  Every mbarrier wait is bounded: on expiry the kernel records
 // BLEND_ETIMEOUT in the error word, stops issuing work, drains its own copies and
 // frees TMEM before returning.
 #include <cuda.h>
@@ -106,6 +113,42 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
                      su32(bar))
                  : "memory");
 }
+// Work unit u -> tile, K-block range and, for a split unit, its half and split index.
+struct Unit {
+    int t, k0, k1, half, sidx;
+};
+struct Sched {
+    int full;   // units dealt as whole tiles
+    int split;  // split tiles (each two units), 0 when the last wave is more than half full
+    int units;
+};
+__device__ __forceinline__ Sched make_sched(int n_total, int grid, bool can_split) {
+    Sched sc;
+    const int rem = n_total % grid;
+    sc.split = (can_split && rem > 0 && 2 * rem <= grid && rem <= GEMM_MAX_SPLIT_TILES) ? rem : 0;
+    sc.full = n_total - sc.split;
+    sc.units = sc.full + 2 * sc.split;
+    return sc;
+}
+__device__ __forceinline__ Unit unit_of(int u, const Sched& sc, int kblocks) {
+    Unit r;
+    if (u < sc.full) {
+        r.t = u;
+        r.k0 = 0;
+        r.k1 = kblocks;
+        r.half = -1;
+        r.sidx = -1;
+    } else {
+        const int v = u - sc.full;
+        r.sidx = v >> 1;
+        r.half = v & 1;
+        r.t = sc.full + r.sidx;
+        r.k0 = r.half ? kblocks / 2 : 0;
+        r.k1 = r.half ? kblocks : kblocks / 2;
+    }
+    return r;
+}
+
 // Two fp32 values to one register of two bf16 (round to nearest even), lo in bits 0-15.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
@@ -130,11 +173,46 @@ __device__ __forceinline__ void tc_fence_after() {
           "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])            \
         : "r"(taddr))
 
+// Epilogue of 32 accumulator columns of one row (fp32 store, fp32 residual add, or
+// SwiGLU of 16 gate + 16 up columns to 16 bf16 outputs).
+template <int EPI>
+__device__ __forceinline__ void epi_chunk(const uint32_t* r, int row, int col, void* Cv, int ldc) {
+    if (EPI == EPI_STORE_F32 || EPI == EPI_ADD_F32) {
+        float4* p = reinterpret_cast<float4*>((float*)Cv + (long long)row * ldc + col);
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+            float4 o = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]), __uint_as_float(r[4 * v + 2]),
+                                   __uint_as_float(r[4 * v + 3]));
+            if (EPI == EPI_ADD_F32) {
+                const float4 x = p[v];
+                o.x += x.x;
+                o.y += x.y;
+                o.z += x.z;
+                o.w += x.w;
+            }
+            p[v] = o;
+        }
+    } else {
+        // 32 columns = 16 gate + 16 up of the same hidden units
+        uint32_t w8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float g0 = __uint_as_float(r[2 * i]), u0 = __uint_as_float(r[16 + 2 * i]);
+            const float g1 = __uint_as_float(r[2 * i + 1]), u1 = __uint_as_float(r[17 + 2 * i]);
+            w8[i] = pack_bf16x2(g0 / (1.f + expf(-g0)) * u0, g1 / (1.f + expf(-g1)) * u1);
+        }
+        uint4* p = reinterpret_cast<uint4*>((bf16*)Cv + (long long)row * ldc + col / 2);
+        p[0] = make_uint4(w8[0], w8[1], w8[2], w8[3]);
+        p[1] = make_uint4(w8[4], w8[5], w8[6], w8[7]);
+    }
+}
+
 template <int EPI, int BN>
 __global__ void __launch_bounds__(THREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB, int K,
               int N, const int32_t* __restrict__ M_dev, void* __restrict__ Cv, int ldc,
-              int32_t* __restrict__ err, const __grid_constant__ QkvEpi qe) {
+              int32_t* __restrict__ err, const __grid_constant__ QkvEpi qe, float* __restrict__ split_ws,
+              int32_t* __restrict__ split_cnt) {
     using TC = TileCfg<BN>;
     constexpr int STAGES = TC::STAGES;
     constexpr int STAGE_BYTES = TC::STAGE_BYTES;
@@ -151,6 +229,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int m_tiles = (M + BM - 1) / BM, n_tiles = N / BN;
     const int n_total = m_tiles * n_tiles;
     const int kblocks = K / BK;
+    const Sched sc = make_sched(n_total, gridDim.x, EPI != EPI_QKV_ROPE && split_ws != nullptr && kblocks >= 2);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -182,9 +261,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ---------------- TMA producer
         int s = 0;
         uint32_t ph = 0;
-        for (int t = blockIdx.x; t < n_total && !abort_flag; t += gridDim.x) {
-            const int mt = t % m_tiles, nt = t / m_tiles;
-            for (int kb = 0; kb < kblocks; ++kb) {
+        for (int u = blockIdx.x; u < sc.units && !abort_flag; u += gridDim.x) {
+            const Unit un = unit_of(u, sc, kblocks);
+            const int mt = un.t % m_tiles, nt = un.t / m_tiles;
+            for (int kb = un.k0; kb < un.k1; ++kb) {
                 if (!mbar_wait(&empty[s], ph ^ 1, &abort_flag)) {
                     abort_flag = 1;
                     set_error(err, BLEND_ETIMEOUT);
@@ -205,7 +285,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ---------------- MMA issuer
         int s = 0, b = 0;
         uint32_t ph = 0, tph = 0;
-        for (int t = blockIdx.x; t < n_total && !abort_flag; t += gridDim.x) {
+        for (int u = blockIdx.x; u < sc.units && !abort_flag; u += gridDim.x) {
+            const Unit un = unit_of(u, sc, kblocks);
             if (!mbar_wait(&tempty[b], tph ^ 1, &abort_flag)) {
                 abort_flag = 1;
                 set_error(err, BLEND_ETIMEOUT);
@@ -213,7 +294,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             tc_fence_after();
             const uint32_t d = tbase + (uint32_t)(b * BN);
-            for (int kb = 0; kb < kblocks; ++kb) {
+            for (int kb = un.k0; kb < un.k1; ++kb) {
                 if (!mbar_wait(&full[s], ph, &abort_flag)) {
                     abort_flag = 1;
                     set_error(err, BLEND_ETIMEOUT);
@@ -226,7 +307,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk)
                     umma_bf16(d, sdesc_sw128(a_addr + kk * 32), sdesc_sw128(b_addr + kk * 32), TC::IDESC,
-                              (kb | kk) != 0);
+                              (kb != un.k0 || kk != 0) ? 1u : 0u);
                 umma_commit(&empty[s]);
                 if (++s == STAGES) {
                     s = 0;
@@ -243,8 +324,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int r_in = sp * 32 + lane;
         int b = 0;
         uint32_t tph = 0;
-        for (int t = blockIdx.x; t < n_total; t += gridDim.x) {
-            const int mt = t % m_tiles, nt = t / m_tiles;
+        for (int u = blockIdx.x; u < sc.units; u += gridDim.x) {
+            const Unit un = unit_of(u, sc, kblocks);
+            const int mt = un.t % m_tiles, nt = un.t / m_tiles;
             // lane 0 waits and broadcasts; the warp stays converged for the .sync.aligned
             // tcgen05.ld below
             bool ok = true;
@@ -314,45 +396,59 @@ __global__ void __launch_bounds__(THREADS, 1)
                         }
                     }
                 }
-            } else {
+            } else if (un.half < 0) {
 #pragma unroll 1
-            for (int c = 0; c < BN; c += 32) {
-                uint32_t r[32];
-                TMEM_LD32(tl + c, r);
-                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-                if (row < M) {
-                    const int col = nt * BN + c;
-                    if (EPI == EPI_STORE_F32 || EPI == EPI_ADD_F32) {
-                        float4* p = reinterpret_cast<float4*>((float*)Cv + (long long)row * ldc + col);
+                for (int c = 0; c < BN; c += 32) {
+                    uint32_t r[32];
+                    TMEM_LD32(tl + c, r);
+                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                    if (row < M) epi_chunk<EPI>(r, row, nt * BN + c, Cv, ldc);
+                }
+            } else {
+                // split tile: publish this half's partial rows, then the second arrival
+                // for these rows finishes them
+                float* own = split_ws + ((long long)(un.sidx * 2 + un.half) * BM + r_in) * BN;
+                const float* other = split_ws + ((long long)(un.sidx * 2 + (un.half ^ 1)) * BM + r_in) * BN;
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 32) {
+                    uint32_t r[32];
+                    TMEM_LD32(tl + c, r);
+                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                    if (row < M) {
+                        float4* p = reinterpret_cast<float4*>(own + c);
 #pragma unroll
-                        for (int v = 0; v < 8; ++v) {
-                            float4 o = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                                                   __uint_as_float(r[4 * v + 2]),
-                                                   __uint_as_float(r[4 * v + 3]));
-                            if (EPI == EPI_ADD_F32) {
-                                float4 x = p[v];
-                                o.x += x.x;
-                                o.y += x.y;
-                                o.z += x.z;
-                                o.w += x.w;
-                            }
-                            p[v] = o;
-                        }
-                    } else {
-                        // 32 columns = 16 gate + 16 up of the same hidden units
-                        uint32_t w8[8];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const float g0 = __uint_as_float(r[2 * i]), u0 = __uint_as_float(r[16 + 2 * i]);
-                            const float g1 = __uint_as_float(r[2 * i + 1]), u1 = __uint_as_float(r[17 + 2 * i]);
-                            w8[i] = pack_bf16x2(g0 / (1.f + expf(-g0)) * u0, g1 / (1.f + expf(-g1)) * u1);
-                        }
-                        uint4* p = reinterpret_cast<uint4*>((bf16*)Cv + (long long)row * ldc + col / 2);
-                        p[0] = make_uint4(w8[0], w8[1], w8[2], w8[3]);
-                        p[1] = make_uint4(w8[4], w8[5], w8[6], w8[7]);
+                        for (int v = 0; v < 8; ++v)
+                            p[v] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                               __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
                     }
                 }
-            }
+                __threadfence();
+                __syncwarp();
+                int order = 0;
+                if (lane == 0) order = atomicAdd(split_cnt + un.sidx * 4 + sp, 1);
+                order = __shfl_sync(0xffffffffu, order, 0);
+                if (order == 1) {
+                    __threadfence();
+                    if (lane == 0) split_cnt[un.sidx * 4 + sp] = 0;  // ready for the next launch
+#pragma unroll 1
+                    for (int c = 0; c < BN; c += 32) {
+                        uint32_t r[32];
+                        TMEM_LD32(tl + c, r);
+                        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                        if (row < M) {
+                            const float4* q = reinterpret_cast<const float4*>(other + c);
+#pragma unroll
+                            for (int v = 0; v < 8; ++v) {
+                                const float4 o = __ldcg(q + v);
+                                r[4 * v] = __float_as_uint(__uint_as_float(r[4 * v]) + o.x);
+                                r[4 * v + 1] = __float_as_uint(__uint_as_float(r[4 * v + 1]) + o.y);
+                                r[4 * v + 2] = __float_as_uint(__uint_as_float(r[4 * v + 2]) + o.z);
+                                r[4 * v + 3] = __float_as_uint(__uint_as_float(r[4 * v + 3]) + o.w);
+                            }
+                            epi_chunk<EPI>(r, row, nt * BN + c, Cv, ldc);
+                        }
+                    }
+                }
             }
             tc_fence_before();
             __syncwarp();
@@ -449,22 +545,25 @@ int pick_bn(int M_max, int N) {
 
 template <int BN>
 void launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, int K, int N, const int32_t* M_dev, int M_max,
-               int epi, void* C, int ldc, int32_t* err, cudaStream_t s, const QkvEpi& qe) {
+               int epi, void* C, int ldc, int32_t* err, cudaStream_t s, const QkvEpi& qe, float* ws, int32_t* cnt) {
     const int tiles = ((M_max + BM - 1) / BM) * (N / BN);
-    const int grid = tiles < g_num_sms ? tiles : g_num_sms;
+    int grid = tiles < g_num_sms ? tiles : g_num_sms;
+    // fewer tiles than half the SMs: every tile runs as two K halves on two CTAs
+    if (ws != nullptr && epi != EPI_QKV_ROPE && K / BK >= 2 && 2 * tiles <= g_num_sms) grid = 2 * tiles;
     constexpr int SM = TileCfg<BN>::SMEM_BYTES;
     if (epi == EPI_STORE_F32)
-        k_gemm_tc<EPI_STORE_F32, BN><<<grid, THREADS, SM, s>>>(ma, mb, K, N, M_dev, C, ldc, err, qe);
+        k_gemm_tc<EPI_STORE_F32, BN><<<grid, THREADS, SM, s>>>(ma, mb, K, N, M_dev, C, ldc, err, qe, ws, cnt);
     else if (epi == EPI_ADD_F32)
-        k_gemm_tc<EPI_ADD_F32, BN><<<grid, THREADS, SM, s>>>(ma, mb, K, N, M_dev, C, ldc, err, qe);
+        k_gemm_tc<EPI_ADD_F32, BN><<<grid, THREADS, SM, s>>>(ma, mb, K, N, M_dev, C, ldc, err, qe, ws, cnt);
     else if (epi == EPI_SWIGLU)
-        k_gemm_tc<EPI_SWIGLU, BN><<<grid, THREADS, SM, s>>>(ma, mb, K, N, M_dev, C, ldc, err, qe);
+        k_gemm_tc<EPI_SWIGLU, BN><<<grid, THREADS, SM, s>>>(ma, mb, K, N, M_dev, C, ldc, err, qe, ws, cnt);
     else
-        k_gemm_tc<EPI_QKV_ROPE, BN><<<grid, THREADS, SM, s>>>(ma, mb, K, N, M_dev, C, ldc, err, qe);
+        k_gemm_tc<EPI_QKV_ROPE, BN><<<grid, THREADS, SM, s>>>(ma, mb, K, N, M_dev, C, ldc, err, qe, ws, cnt);
 }
 
 int launch_gemm_tc(const void* A, int K, int M_cap, const void* B, int N, const int32_t* M_dev, int M_max,
-                   int epi, void* C, int ldc, int32_t* err, cudaStream_t s, const QkvEpi* qkv) {
+                   int epi, void* C, int ldc, int32_t* err, cudaStream_t s, const QkvEpi* qkv, float* split_ws,
+                   int32_t* split_cnt) {
     if (M_max <= 0) return BLEND_OK;
     const int bn = pick_bn(M_max, N);
     if (epi == EPI_QKV_ROPE && (qkv == nullptr || bn != 256)) return BLEND_EUNSUPPORTED;
@@ -474,10 +573,11 @@ int launch_gemm_tc(const void* A, int K, int M_cap, const void* B, int N, const 
     if (!encode_2d(&ma, A, (uint64_t)K, (uint64_t)M_cap, BK, BM) ||
         !encode_2d(&mb, B, (uint64_t)K, (uint64_t)N, BK, (uint32_t)bn))
         return BLEND_EUNSUPPORTED;  // the operands cannot be described to the TMA unit
+    if (split_cnt == nullptr) split_ws = nullptr;
     if (bn == 256)
-        launch_bn<256>(ma, mb, K, N, M_dev, M_max, epi, C, ldc, err, s, qe);
+        launch_bn<256>(ma, mb, K, N, M_dev, M_max, epi, C, ldc, err, s, qe, split_ws, split_cnt);
     else
-        launch_bn<128>(ma, mb, K, N, M_dev, M_max, epi, C, ldc, err, s, qe);
+        launch_bn<128>(ma, mb, K, N, M_dev, M_max, epi, C, ldc, err, s, qe, split_ws, split_cnt);
     note_launch(1);
     return BLEND_OK;
 }

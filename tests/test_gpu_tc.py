@@ -76,3 +76,28 @@ def test_layer_tensor_cores_match_oracle_and_cuda_cores(shape, n, n_ctx):
     # the GPU paths differ only by fp32 summation order and where bf16 rounding happens
     assert maxrel(outs[True][0], outs[False][0]) <= 1e-2
     assert maxrel(fused[0], outs[True][0]) <= 1e-2
+
+
+@pytest.mark.parametrize("shape,n,n_ctx", SHAPES[:2], ids=[s[0].name for s in SHAPES[:2]])
+def test_split_tail_gemm_is_deterministic(shape, n, n_ctx):
+    """Shapes whose projections run as K halves (fewer tiles than half the SMs, or a last
+    wave at most half full): two runs of the same layer give bitwise identical outputs,
+    whichever half of a split tile finishes first."""
+    dev = torch.device("cuda:0")
+    case = make_case(shape, 4, [8], pool="random")
+    r = GpuRunner(case, max(n, 128), n_ctx, 64, max_pos=n_ctx)
+    g = torch.Generator().manual_seed(12)
+    dt = synth.torch_dtype(shape)
+    kc = (0.5 * torch.randn(n_ctx, shape.n_kv_heads, shape.head_dim, generator=g)).to(dt)
+    vc = (0.5 * torch.randn(n_ctx, shape.n_kv_heads, shape.head_dim, generator=g)).to(dt)
+    x = torch.randn(n, shape.hidden, generator=g)
+    pos = torch.sort(torch.randperm(n_ctx, generator=g)[:n]).values.to(torch.int32).to(dev)
+    runs = []
+    for _ in range(3):
+        xg, kg, vg = x.to(dev), kc.to(dev), vc.to(dev)
+        b.selective_layer(r.h, 1, xg, pos, n, kg, vg, n_ctx, None)
+        b.blend_device_status(r.h)
+        runs.append((xg.cpu(), kg.cpu(), vg.cpu()))
+    for other in runs[1:]:
+        for a, c in zip(runs[0], other):
+            assert torch.equal(a, c)
