@@ -48,8 +48,16 @@ except OSError:
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
 # capture of each kernel (profiles/), valid only while the kernel's source is unchanged.
 TRAFFIC = {
-    "attention": {"bytes": 140.736768e6 + 17.628416e6, "source": "rag_kv_cache_rope_gb300/csrc/attn_tc.cu",
-                  "sha256_16": "fcb6aa23b2958d4d", "profile": "profiles/attn_tc_qwen14b_16k_layer.md"},
+    "gemm_qkv": {"bytes": 116.266240e6 + 30.864896e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
+                 "sha256_16": "f2027e01e0765111", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
+    "gemm_o": {"bytes": 162.874624e6 + 42.884096e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
+               "sha256_16": "f2027e01e0765111", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
+    "gemm_gate_up": {"bytes": 323.675904e6 + 86.671872e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
+                     "sha256_16": "f2027e01e0765111", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
+    "gemm_down": {"bytes": 591.546624e6 + 62.978816e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
+                  "sha256_16": "f2027e01e0765111", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
+    "attention": {"bytes": 132.513792e6 + 13.233664e6, "source": "rag_kv_cache_rope_gb300/csrc/attn_tc.cu",
+                  "sha256_16": "7d325c2c8d0b527d", "profile": "profiles/attn_tc_qwen14b_16k_layer.md"},
 }
 
 
@@ -77,8 +85,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--layers", type=int, default=0,
                     help="truncate the model to this many layers (profiling captures only; not a headline)")
-    ap.add_argument("--full-prefill-steps", type=int, default=0,
-                    help="also time full prefill of the same input (every row recomputed)")
+    ap.add_argument("--full-prefill-steps", type=int, default=2,
+                    help="also time full prefill of the same input (every row recomputed; 0 skips it)")
     return ap.parse_args()
 
 
@@ -227,7 +235,7 @@ def run_ours(args, wl, rank, world):
     from rag_kv_cache_rope_gb300 import binding as b
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    S = Setup(wl, dev, max_rows_full=args.full_prefill_steps > 0)
+    S = Setup(wl, dev, max_rows_full=False)
     sh = wl.model
     for _ in range(args.warmup):
         S.step()
@@ -310,18 +318,24 @@ def run_ours(args, wl, rank, world):
     }
     if not args.no_e2e:
         line["e2e"] = e2e(S, args, world)
-    if args.full_prefill_steps > 0:
+    if args.full_prefill_steps > 0 and world == 1:
+        # the same input with every row recomputed, on a handle sized for all N rows
+        hf = b.blend_init(S.cfg, S.packed, b.Limits(S.N, S.N, S.n_c, 1))
         full = b.RequestRef(S.req_tok.chunk_ids, S.query, mode="full")
-        S.step(full)
+        b.blend_prefill(hf, [full], S.pool, S.out)
         torch.cuda.synchronize()
         f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         f0.record()
         for _ in range(args.full_prefill_steps):
-            S.step(full)
+            b.blend_prefill(hf, [full], S.pool, S.out)
         f1.record()
         torch.cuda.synchronize()
+        b.blend_device_status(hf)
+        del hf
+        torch.cuda.empty_cache()
         fms = f0.elapsed_time(f1) / args.full_prefill_steps
-        line["full_prefill"] = {"ttft_ms": fms, "tokens_per_s": S.N / (fms / 1e3), "speedup_of_blend": fms / ms}
+        line["full_prefill"] = {"ttft_ms": fms, "tokens_per_s": S.N / (fms / 1e3), "speedup_of_blend": fms / ms,
+                                "steps": args.full_prefill_steps}
     return line, S
 
 
@@ -359,49 +373,79 @@ def e2e(S: Setup, args, world):
 
 
 # ---------------------------------------------------------------- oracle (CPU) arm
-def oracle_sample(wl: synth.Workload, S=None):
+class OracleSample:
     """Times the CPU oracle on a bounded sample of one step and scales it to the whole
     step: one layer's assembly (x layers), the full selection, and one layer of the
-    selective recompute on 64 of the recomputed rows spread over the context (x rows/64
-    x layers).  Weights of that layer are the same seeded random weights."""
-    from oracle import blend_oracle as O
-    sh = wl.model
-    one = dataclasses.replace(sh, n_layers=1)
-    cfg = dict(n_layers=1, hidden=sh.hidden, n_q_heads=sh.n_q_heads, n_kv_heads=sh.n_kv_heads,
-               head_dim=sh.head_dim, ffn=sh.ffn, vocab=sh.vocab, rope_theta=sh.rope_theta, rms_eps=sh.rms_eps)
-    w_t = synth.model_weights(one, wl.seed, device="cpu")
-    w = {k: v.double().numpy() for k, v in w_t.items()}
-    del w_t
-    pool_tok, reqs = synth.workload_tokens(wl)
-    lens = [wl.chunk_len] * len(pool_tok.chunks)
-    pk, pv, row_off = synth.random_pool_kv(one, wl.prefix_len, lens, wl.seed)
-    ek = [pk[:, o:o + wl.prefix_len + l].double().numpy() for o, l in zip(row_off, lens)]
-    ev = [pv[:, o:o + wl.prefix_len + l].double().numpy() for o, l in zip(row_off, lens)]
-    hs = synth.hidden_states(wl.n_chunk_rows, wl.score_layers, wl.score_dim, wl.seed)
-    ids = reqs[0].chunk_ids
-    P, n_c, Q = wl.prefix_len, wl.n_chunk_rows, wl.query_len
-    N = P + n_c + Q
-    t0 = time.perf_counter()
-    K, V = O.assemble(ek, ev, ids, P, [lens[c] for c in ids], Q, sh.rope_theta)
-    t_asm = time.perf_counter() - t0
-    t0 = time.perf_counter()
-    s = O.importance_scores(hs.double().numpy()).astype(np.float32).astype(np.float64)
-    sel = O.select_final_bisect(s, O.ceil_bp(wl.rho_bp, n_c), wl.window, wl.tau, base=P)
-    t_sel = time.perf_counter() - t0
-    rows = np.concatenate([sel, np.arange(P + n_c, N)])
-    pick = rows[np.linspace(0, len(rows) - 1, 64).astype(int)]
-    tokens = np.concatenate([reqs[0].prefix.numpy()] + [pool_tok.chunks[c].numpy() for c in ids]
-                            + [reqs[0].query.numpy()])
-    x = w["embed"][tokens[pick]]
-    t0 = time.perf_counter()
-    O.layer_forward(w, cfg, 0, x, pick, K[0], V[0])
-    t_layer = time.perf_counter() - t0
-    est = sh.n_layers * t_asm + t_sel + sh.n_layers * t_layer * len(rows) / len(pick)
-    sample_s = t_asm + t_sel + t_layer
-    return {"est_step_s": est, "sample_s": sample_s, "N": N,
-            "sample": f"1 of {sh.n_layers} layers assembled (x{sh.n_layers}), full selection, one layer's "
-                      f"recompute of 64 of {len(rows)} rows spread over the context (x{len(rows) / 64:.1f} "
-                      f"x{sh.n_layers}); numpy fp64"}
+    selective recompute on a subset of the recomputed rows spread over the context
+    (x rows/subset x layers).  rows_for() sizes the subset for a wanted sample time.
+    Weights of that layer are the same seeded random weights."""
+
+    def __init__(self, wl: synth.Workload):
+        from oracle import blend_oracle as O
+        self.O = O
+        self.wl = wl
+        sh = wl.model
+        one = dataclasses.replace(sh, n_layers=1)
+        self.cfg = dict(n_layers=1, hidden=sh.hidden, n_q_heads=sh.n_q_heads, n_kv_heads=sh.n_kv_heads,
+                        head_dim=sh.head_dim, ffn=sh.ffn, vocab=sh.vocab, rope_theta=sh.rope_theta,
+                        rms_eps=sh.rms_eps)
+        w_t = synth.model_weights(one, wl.seed, device="cpu")
+        self.w = {k: v.double().numpy() for k, v in w_t.items()}
+        del w_t
+        pool_tok, reqs = synth.workload_tokens(wl)
+        self.lens = [wl.chunk_len] * len(pool_tok.chunks)
+        pk, pv, row_off = synth.random_pool_kv(one, wl.prefix_len, self.lens, wl.seed)
+        self.ek = [pk[:, o:o + wl.prefix_len + n].double().numpy() for o, n in zip(row_off, self.lens)]
+        self.ev = [pv[:, o:o + wl.prefix_len + n].double().numpy() for o, n in zip(row_off, self.lens)]
+        self.hs = synth.hidden_states(wl.n_chunk_rows, wl.score_layers, wl.score_dim, wl.seed).double().numpy()
+        self.ids = reqs[0].chunk_ids
+        self.tokens = np.concatenate([reqs[0].prefix.numpy()] + [pool_tok.chunks[c].numpy() for c in self.ids]
+                                     + [reqs[0].query.numpy()])
+        self.per_row, self.fixed_s, self.n_rows = 1.0, 0.0, 1
+
+    def run(self, n_pick: int):
+        """One sample with a recompute subset of n_pick rows."""
+        O, wl = self.O, self.wl
+        sh = wl.model
+        P, n_c, Q = wl.prefix_len, wl.n_chunk_rows, wl.query_len
+        N = P + n_c + Q
+        t0 = time.perf_counter()
+        K, V = O.assemble(self.ek, self.ev, self.ids, P, [self.lens[c] for c in self.ids], Q, sh.rope_theta)
+        t_asm = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        s = O.importance_scores(self.hs).astype(np.float32).astype(np.float64)
+        sel = O.select_final_bisect(s, O.ceil_bp(wl.rho_bp, n_c), wl.window, wl.tau, base=P)
+        t_sel = time.perf_counter() - t0
+        rows = np.concatenate([sel, np.arange(P + n_c, N)])
+        pick = rows[np.linspace(0, len(rows) - 1, max(1, min(n_pick, len(rows)))).astype(int)]
+        x = self.w["embed"][self.tokens[pick]]
+        t0 = time.perf_counter()
+        O.layer_forward(self.w, self.cfg, 0, x, pick, K[0], V[0])
+        t_layer = time.perf_counter() - t0
+        self.per_row = t_layer / len(pick)
+        self.fixed_s = t_asm + t_sel
+        self.n_rows = len(rows)
+        if wl.mode == "hkvd":
+            # layer 0 recomputes every chunk row, layer 1 the first candidates, the rest the final set
+            c1 = O.ceil_bp(wl.r1_bp, n_c)
+            row_layers = (n_c + Q) + (c1 + Q) + (sh.n_layers - 2) * len(rows)
+        else:
+            row_layers = sh.n_layers * len(rows)
+        est = sh.n_layers * t_asm + t_sel + self.per_row * row_layers
+        sample = (f"1 of {sh.n_layers} layers assembled (x{sh.n_layers}), full selection, one layer's recompute "
+                  f"of {len(pick)} of {len(rows)} rows spread over the context, scaled to {row_layers} "
+                  f"row-layers; numpy fp64")
+        return {"est_step_s": est, "sample_s": t_asm + t_sel + t_layer, "N": N, "sample": sample}
+
+    def rows_for(self, target_s: float) -> int:
+        """Row subset that makes one sample take about target_s seconds (after calibrate)."""
+        return int(max(16, min(self.n_rows, round(max(1e-3, target_s - self.fixed_s) / max(self.per_row, 1e-6)))))
+
+    def calibrate(self):
+        """Two small samples: the first touches every array once, the second gives a warm
+        per-row time for rows_for."""
+        self.run(32)
+        self.run(32)
 
 
 def cores():
@@ -414,11 +458,14 @@ def cores():
 def run_reference(args, wl, rank, world):
     if rank != 0:
         return None
+    osm = OracleSample(wl)
+    osm.calibrate()
+    n_pick = osm.rows_for(12.0)
     for _ in range(args.warmup):
-        oracle_sample(wl)
+        osm.run(osm.rows_for(3.0))
     ests = []
     for _ in range(args.steps):
-        ests.append(oracle_sample(wl))
+        ests.append(osm.run(n_pick))
     est = statistics.median(e["est_step_s"] for e in ests)
     v = ests[0]["N"] / est
     return {
@@ -452,7 +499,9 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         del S
         torch.cuda.empty_cache()
-        cb = oracle_sample(wl)
+        osm = OracleSample(wl)
+        osm.calibrate()
+        cb = osm.run(osm.rows_for(15.0))
         line["cpu_baseline"] = {"value": cb["N"] / cb["est_step_s"], "unit": "tokens/s", "cores": cores(),
                                 "kind": "oracle", "sample": cb["sample"], "sample_seconds": cb["sample_s"]}
     if rank == 0:
