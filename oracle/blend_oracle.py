@@ -16,8 +16,9 @@ Sources (page title, section):
     "4.3 Sliding-Window Grouping and KV Cache Update".
   * CacheBlend blog, "Prefill and the KV cache", "Selective KV recompute",
     "Picking the tokens to recompute", "The chicken-and-egg problem", "Implementation".
-  * SpecCache notes, "2.2 Importance score estimation" (the I_i formula) and
-    "2.3 Semantic span completion" (TopK with K = ceil(rho N)).
+  * SpecCache notes, "2.2 Importance score estimation" (the I_i formula and TopK with
+    K = ceil(rho N)), "2.3 Semantic span completion" (span segmentation, coverage,
+    global budget control) and "2.4 Cross-tokenizer alignment".
 
 Parity pins (what each function is checked against, in tests/test_oracle_*.py):
   rope / realign      : rotation composition R(d)R(p)x = R(p+d)x, identity at 0, closed
@@ -33,6 +34,11 @@ Parity pins (what each function is checked against, in tests/test_oracle_*.py):
   blend_prefill       : rho=100 % equals full prefill; rho=0 leaves every chunk row at its
                         realigned cache value; chunk 0 (shift 0) has zero layer-0 deviation
   importance_scores   : closed form on constant hidden states
+  span_segments /     : a hand-worked case (tests/golden/span_completion.json), closed-form
+  span_complete /       span lengths on a smooth ramp, invariants (T_init inside T, every
+  span_select           covered span complete, nothing else added), degenerate thresholds,
+                        budget cap and final-budget maximality
+  align_expand        : identity alignment, one-to-two splits, overlapping ranges
 """
 from __future__ import annotations
 
@@ -355,6 +361,107 @@ def select_final_bisect(scores, budget, w, tau, allowed=None, base=0) -> np.ndar
             else:
                 hi = mid
     return np.array(sorted(base + t for t in grouped(lo)), dtype=np.int64)
+
+
+# ----------------------------------------------------------------------------------
+# SpecCache semantic span completion (SpecCache notes, "2.3 Semantic span completion")
+# and cross-tokenizer alignment ("2.4 Cross-tokenizer alignment")
+# ----------------------------------------------------------------------------------
+
+F32 = np.float32
+
+
+def span_segments(scores: np.ndarray, tau_smooth: float, max_span: int) -> list:
+    """Spans [u, v] (inclusive) of SpecCache 2.3, left to right.
+
+    Scores are min-max normalised, I~_i = (I_i - min I) / (max I - min I); the relative
+    change to the next token is delta_i = |I~_{i+1} - I~_i| / I~_i, and token i+1 joins
+    the span of token i while delta_i < tau_smooth, up to max_span tokens per span.
+    Readings (the pages are silent): every step is one fp32 operation rounded to
+    nearest (the scores are fp32), so a GPU kernel can take each merge decision
+    identically; -0 counts as +0; min and max skip NaN; a NaN or infinite delta
+    (I~_i = 0, or all scores equal) is not below the threshold, so it ends the span;
+    a span that reaches max_span tokens ends there and the next token starts a new one.
+    """
+    x = np.asarray(scores, dtype=F32).copy()
+    x[x == 0] = F32(0.0)
+    n = len(x)
+    if n == 0:
+        return []
+    finite = x[~np.isnan(x)]
+    lo = F32(np.min(finite)) if len(finite) else F32(np.nan)
+    hi = F32(np.max(finite)) if len(finite) else F32(np.nan)
+    rng = F32(hi - lo)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        norm = [F32(F32(x[i] - lo) / rng) for i in range(n)]
+        spans = []
+        u = 0
+        for i in range(n - 1):
+            delta = F32(F32(abs(F32(norm[i + 1] - norm[i]))) / norm[i])
+            merge = bool(delta < F32(tau_smooth))
+            if not merge or (i + 1 - u) >= max_span:
+                spans.append((u, i))
+                u = i + 1
+        spans.append((u, n - 1))
+    return spans
+
+
+def span_complete(scores: np.ndarray, k: int, tau_smooth: float, tau_cover_bp: int, max_span: int) -> set:
+    """T = T_init U (every span p_j with coverage r_j >= tau_cover), SpecCache 2.3, with
+    T_init = the top-k scores (2.2; ranked as in _order_key).  The coverage test
+    |T_init n p_j| / |p_j| >= tau_cover is taken exactly in integers with tau_cover in
+    basis points: count * 10000 >= tau_cover_bp * |p_j|."""
+    init = set(topk(scores, k))
+    out = set(init)
+    for u, v in span_segments(scores, tau_smooth, max_span):
+        members = range(u, v + 1)
+        count = sum(1 for t in members if t in init)
+        if count * 10000 >= tau_cover_bp * (v - u + 1):
+            out.update(members)
+    return out
+
+
+def span_select(scores: np.ndarray, budget: int, tau_smooth: float, tau_cover_bp: int, max_span: int,
+                budget_mode: str = "final", cap: Optional[int] = None, base: int = 0) -> np.ndarray:
+    """SpecCache selection with its global budget control (2.3, last paragraph).
+
+    candidate mode: T_init = top-`budget`, spans completed, then if |T| > cap only the
+      cap tokens of T with the highest scores are kept (the pages' "maximum size limit";
+      reading: a caller-given cap >= budget, since a cap equal to the TopK size would
+      undo every completion).
+    final mode (reading, as for window grouping): the largest k <= budget whose completed
+      set has at most `budget` tokens, so the ratio bounds the rows recomputed; the
+      completed set grows with k, so scanning k down from the budget finds it.
+    Returns sorted absolute positions (int64)."""
+    n = len(scores)
+    if budget_mode == "candidate":
+        res = span_complete(scores, min(budget, n), tau_smooth, tau_cover_bp, max_span)
+        c = budget if cap is None else cap
+        if len(res) > c:
+            keep = sorted(res, key=lambda t: _order_key(scores[t], t))[:c]
+            res = set(keep)
+    elif budget_mode == "final":
+        res = set()
+        k = min(budget, n)
+        while k > 0:
+            s = span_complete(scores, k, tau_smooth, tau_cover_bp, max_span)
+            if len(s) <= budget:
+                res = s
+                break
+            k -= 1
+    else:
+        raise ValueError(budget_mode)
+    return np.array(sorted(base + t for t in res), dtype=np.int64)
+
+
+def align_expand(selected, a_start, a_end) -> np.ndarray:
+    """SpecCache 2.4: T = union over selected speculative tokens i of Psi(i), where
+    Psi(i) = target tokens a_start[i] .. a_end[i]-1 (the target sub-tokens covering the
+    same text).  Returns the sorted distinct target indices."""
+    out = set()
+    for i in selected:
+        out.update(range(int(a_start[i]), int(a_end[i])))
+    return np.array(sorted(out), dtype=np.int64)
 
 
 def importance_scores(hidden: np.ndarray) -> np.ndarray:
