@@ -187,7 +187,7 @@ class Setup:
         L = sh.n_layers
         self.query = self.req_tok.query.to(dev)
         self.hidden_states = synth.hidden_states(self.n_c, wl.score_layers, wl.score_dim, wl.seed, device=dev,
-                                                 dtype=dt)
+                                                 dtype=dt, phrase_max=wl.score_phrase_max)
         self.scores = torch.empty(self.n_c, dtype=torch.float32, device=dev)
         self.out = b.OutputsRef(
             k=torch.empty(L, self.N, sh.n_kv_heads, sh.head_dim, dtype=dt, device=dev),
@@ -197,7 +197,7 @@ class Setup:
             n_sel=torch.zeros(b.MAX_BATCH, dtype=torch.int32, device=dev))
         self.req = b.RequestRef(self.req_tok.chunk_ids, self.query, mode=wl.mode, rho_bp=wl.rho_bp,
                                 r1_bp=wl.r1_bp, window=wl.window, tau=wl.tau, budget_mode=wl.budget_mode,
-                                scores=self.scores)
+                                scores=self.scores, group_rule=wl.group_rule)
 
     def step(self, req=None):
         b = self.b
@@ -303,6 +303,7 @@ def run_ours(args, wl, rank, world):
         "config": {"workload": wl.name, "model_shape": sh.name, "n_ctx": S.N, "prefix": wl.prefix_len,
                    "chunks": f"{wl.n_chunks}x{wl.chunk_len}", "query": wl.query_len, "mode": wl.mode,
                    "rho_bp": wl.rho_bp, "window": wl.window, "tau": wl.tau, "budget": wl.budget_mode,
+                   "group_rule": wl.group_rule,
                    "rows_per_layer": rows, "layers": sh.n_layers, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (weights %.1f GB, chunk pool %.1f GB)" % (
                        sum(t.numel() * t.element_size() for t in S.packed.values()) / 1e9,
@@ -397,7 +398,8 @@ class OracleSample:
         pk, pv, row_off = synth.random_pool_kv(one, wl.prefix_len, self.lens, wl.seed)
         self.ek = [pk[:, o:o + wl.prefix_len + n].double().numpy() for o, n in zip(row_off, self.lens)]
         self.ev = [pv[:, o:o + wl.prefix_len + n].double().numpy() for o, n in zip(row_off, self.lens)]
-        self.hs = synth.hidden_states(wl.n_chunk_rows, wl.score_layers, wl.score_dim, wl.seed).double().numpy()
+        self.hs = synth.hidden_states(wl.n_chunk_rows, wl.score_layers, wl.score_dim, wl.seed,
+                                      phrase_max=wl.score_phrase_max).double().numpy()
         self.ids = reqs[0].chunk_ids
         self.tokens = np.concatenate([reqs[0].prefix.numpy()] + [pool_tok.chunks[c].numpy() for c in self.ids]
                                      + [reqs[0].query.numpy()])
@@ -414,7 +416,10 @@ class OracleSample:
         t_asm = time.perf_counter() - t0
         t0 = time.perf_counter()
         s = O.importance_scores(self.hs).astype(np.float32).astype(np.float64)
-        sel = O.select_final_bisect(s, O.ceil_bp(wl.rho_bp, n_c), wl.window, wl.tau, base=P)
+        if wl.group_rule == "span":
+            sel = O.span_select_final_bisect(s, O.ceil_bp(wl.rho_bp, n_c), 0.4, 7000, 16, base=P)
+        else:
+            sel = O.select_final_bisect(s, O.ceil_bp(wl.rho_bp, n_c), wl.window, wl.tau, base=P)
         t_sel = time.perf_counter() - t0
         rows = np.concatenate([sel, np.arange(P + n_c, N)])
         pick = rows[np.linspace(0, len(rows) - 1, max(1, min(n_pick, len(rows)))).astype(int)]

@@ -63,12 +63,19 @@ extern "C" {
 #define BLEND_BUDGET_FINAL 0     /* at most ceil(rho*N_c) rows after grouping */
 #define BLEND_BUDGET_CANDIDATE 1 /* ceil(rho*N_c) candidates, then grouping */
 
+/* EXT selection rule applied after TopK: CacheClip window grouping (window, tau) or
+ * SpecCache span completion (tau_smooth, tau_cover_bp, max_span, cap_bp). */
+#define BLEND_GROUP_WINDOW 0
+#define BLEND_GROUP_SPAN 1
+
 #define BLEND_DEV_KV 0 /* deviation = |k-k'|^2 + |v-v'|^2 */
 #define BLEND_DEV_V 1  /* deviation = |v-v'|^2 */
 
 #define BLEND_MAX_BATCH 64
 #define BLEND_MAX_CHUNKS 1024 /* chunks over all requests of one call */
 #define BLEND_MAX_WINDOW 64
+#define BLEND_MAX_SPAN 64              /* longest span of the span rule */
+#define BLEND_MAX_ALIGN_TARGETS 131072 /* target tokens of one align_expand call */
 #define BLEND_GU_BLOCK 16 /* gate/up row interleave of w_gu, see blend_weights */
 
 /* ---- model ----------------------------------------------------------------- */
@@ -146,6 +153,14 @@ typedef struct {
     int32_t stage_layer[3];
     const int32_t* stage_pos[3];
     int32_t stage_n[3];
+    /* EXT only: BLEND_GROUP_WINDOW (0, the fields window/tau above) or BLEND_GROUP_SPAN
+     * (SpecCache 2.3: spans of smooth importance, completed when covered enough). */
+    int32_t group_rule;
+    float tau_smooth;            /* SPAN: merge while the relative change is below this (0.4) */
+    int32_t tau_cover_bp;        /* SPAN: complete a span at this coverage, basis points (7000) */
+    int32_t max_span;            /* SPAN: longest span, 1..BLEND_MAX_SPAN (16) */
+    int32_t cap_bp;              /* SPAN + CANDIDATE: most rows kept after completion, basis
+                                  * points of N_c (rho_bp..10000); FINAL: the budget is the cap */
 } blend_request;
 
 /* Outputs of a batch.  Request r owns tokens tok_r .. tok_r+N_r-1 of k, v with
@@ -256,6 +271,36 @@ int kv_deviation(blend_handle* h, const void* k_new, const void* v_new, const vo
 int topk_select_dilate(blend_handle* h, const float* scores, int32_t n, int32_t base,
                        int32_t budget, int32_t window, int32_t tau, int32_t budget_mode,
                        const uint8_t* allowed, int32_t* idx_out, int32_t* n_out, void* stream);
+
+/* SpecCache selection (SpecCache notes, "2.2 Importance score estimation" TopK and
+ * "2.3 Semantic span completion" with its global budget control).  scores: device [n]
+ * fp32 for positions base..base+n-1, ranked as in topk_select_dilate.  Normalised
+ * scores n~ = (s - min)/(max - min) (fp32, -0 as +0, NaN skipped by min/max); token i+1
+ * joins token i's span while |n~(i+1) - n~(i)| / n~(i) < tau_smooth (each step one fp32
+ * operation; a NaN or infinite change ends the span), at most max_span tokens per span.
+ * A span joins the set when (#TopK members in it) * 10000 >= tau_cover_bp * length.
+ * CANDIDATE: TopK size = budget, then at most `cap` tokens, those of highest score.
+ * FINAL: the largest TopK size <= budget whose completed set has <= budget tokens
+ * (`cap` unused).  Writes the set ascending (absolute positions) to idx_out (device [n])
+ * and its size to *n_out (device).  n <= 32768 and within the handle's chunk-row
+ * capacity; 0 <= tau_smooth (finite), 1 <= tau_cover_bp <= 10000,
+ * 1 <= max_span <= BLEND_MAX_SPAN, cap >= 0, else BLEND_EINVAL.  Uses the handle's
+ * workspace; calls on one handle must not overlap. */
+int span_select(blend_handle* h, const float* scores, int32_t n, int32_t base, int32_t budget, int32_t cap,
+                float tau_smooth, int32_t tau_cover_bp, int32_t max_span, int32_t budget_mode,
+                int32_t* idx_out, int32_t* n_out, void* stream);
+
+/* Cross-tokenizer alignment (SpecCache notes, "2.4 Cross-tokenizer alignment"): the
+ * selected speculative-model tokens sel[0..*n_sel) (device, values sel_base..sel_base+
+ * n_spec-1; *n_sel clamped to 0..max_sel) are expanded to every target-model token
+ * a_start[i]..a_end[i]-1 (device [n_spec] each) of token i = sel[k] - sel_base; the
+ * distinct target tokens are written ascending, plus out_base, to idx_out (device,
+ * room for n_target) and their count to *n_out (device).  0 <= n_target <=
+ * BLEND_MAX_ALIGN_TARGETS.  A selected index or a range outside its bounds is skipped
+ * and reported by blend_device_status as BLEND_EDEVICE. */
+int align_expand(blend_handle* h, const int32_t* sel, const int32_t* n_sel, int32_t max_sel, int32_t sel_base,
+                 const int32_t* a_start, const int32_t* a_end, int32_t n_spec, int32_t n_target,
+                 int32_t out_base, int32_t* idx_out, int32_t* n_out, void* stream);
 
 /* Row gather: dst[i] = src[idx[i]] for i < *n (device scalar), rows of row_bytes
  * (a multiple of 16; src, dst 16-byte aligned).  max_n bounds *n. */

@@ -454,6 +454,29 @@ def span_select(scores: np.ndarray, budget: int, tau_smooth: float, tau_cover_bp
     return np.array(sorted(base + t for t in res), dtype=np.int64)
 
 
+def span_select_final_bisect(scores: np.ndarray, budget: int, tau_smooth: float, tau_cover_bp: int,
+                             max_span: int, base: int = 0) -> np.ndarray:
+    """Same result as span_select(..., 'final') using bisection on k (the completed set
+    grows with k), for sizes where the linear scan is slow."""
+    n = len(scores)
+
+    def size(k):
+        return len(span_complete(scores, k, tau_smooth, tau_cover_bp, max_span))
+
+    lo, hi = 0, min(budget, n)               # invariant: size(lo) <= budget
+    if size(hi) <= budget:
+        lo = hi
+    else:
+        while hi - lo > 1:
+            mid = (lo + hi) // 2
+            if size(mid) <= budget:
+                lo = mid
+            else:
+                hi = mid
+    res = span_complete(scores, lo, tau_smooth, tau_cover_bp, max_span)
+    return np.array(sorted(base + t for t in res), dtype=np.int64)
+
+
 def align_expand(selected, a_start, a_end) -> np.ndarray:
     """SpecCache 2.4: T = union over selected speculative tokens i of Psi(i), where
     Psi(i) = target tokens a_start[i] .. a_end[i]-1 (the target sub-tokens covering the
@@ -487,7 +510,8 @@ def blend_prefill(w: dict, cfg: dict, entries_k, entries_v, entry_tokens, prefix
                   chunk_ids, query_tokens, mode: str, rho_bp: int = 0, r1_bp: int = 0,
                   window: int = 1, tau: int = 1, budget_mode: str = "final",
                   scores: Optional[np.ndarray] = None, forced: Optional[list] = None,
-                  dev_mode: str = "kv"):
+                  dev_mode: str = "kv", group_rule: str = "window", tau_smooth: float = 0.4,
+                  tau_cover_bp: int = 7000, max_span: int = 16, cap_bp: int = 0):
     """Selective KV-recompute prefill of one request.
 
     1. Assemble the blended cache (see assemble()).
@@ -498,7 +522,9 @@ def blend_prefill(w: dict, cfg: dict, entries_k, entries_v, entry_tokens, prefix
        entered it (the previous layer's rows) and writes them into the cache; when a
        new stage starts at that layer, only the new (smaller) set continues.
        * "ext":   one stage [(0, S)] with S = select(scores, ceil(rho N_c), w, tau, mode)
-                  from external per-chunk-token scores (CacheClip 6.2-6.3; SpecCache 2.2).
+                  from external per-chunk-token scores (CacheClip 6.2-6.3; SpecCache 2.2),
+                  or with group_rule "span" S = span_select(...) (SpecCache 2.3; in
+                  candidate mode the cap is ceil(cap_bp N_c)).
        * "hkvd":  gradual filtering (CacheBlend blog, "The chicken-and-egg problem"; the
                   CacheClip paper's summary: the first layer is recomputed in full, the
                   second partially, and its fresh KV is compared with the loaded one).
@@ -530,7 +556,13 @@ def blend_prefill(w: dict, cfg: dict, entries_k, entries_v, entry_tokens, prefix
     qrows = np.arange(hi, N)
     budget = ceil_bp(rho_bp, n_c)
 
-    if mode == "ext":
+    if mode == "ext" and group_rule == "span":
+        s = np.asarray(scores)
+        sel = (span_select(s, budget, tau_smooth, tau_cover_bp, max_span, "candidate",
+                           cap=ceil_bp(cap_bp, n_c), base=lo) if budget_mode == "candidate"
+               else span_select_final_bisect(s, budget, tau_smooth, tau_cover_bp, max_span, base=lo))
+        stages = [(0, sel)]
+    elif mode == "ext":
         s = np.asarray(scores)
         sel = (select(s, budget, window, tau, budget_mode, base=lo) if budget_mode == "candidate"
                else select_final_bisect(s, budget, window, tau, base=lo))

@@ -21,12 +21,16 @@ F32, BF16 = 0, 1
 SEL_EXT, SEL_HKVD, SEL_FORCED, SEL_FULL = 0, 1, 2, 3
 BUDGET_FINAL, BUDGET_CANDIDATE = 0, 1
 DEV_KV, DEV_V = 0, 1
+GROUP_WINDOW, GROUP_SPAN = 0, 1
 MAX_BATCH = 64
+MAX_SPAN = 64
+MAX_ALIGN_TARGETS = 131072
 GU_BLOCK = 16
 
 MODES = {"ext": SEL_EXT, "hkvd": SEL_HKVD, "forced": SEL_FORCED, "full": SEL_FULL}
 BUDGETS = {"final": BUDGET_FINAL, "candidate": BUDGET_CANDIDATE}
 DEVMODES = {"kv": DEV_KV, "v": DEV_V}
+GROUP_RULES = {"window": GROUP_WINDOW, "span": GROUP_SPAN}
 
 
 class BlendError(RuntimeError):
@@ -66,7 +70,9 @@ class Request(C.Structure):
                 ("rho_bp", C.c_int32), ("r1_bp", C.c_int32), ("window", C.c_int32),
                 ("tau", C.c_int32), ("budget_mode", C.c_int32), ("dev_mode", C.c_int32),
                 ("scores", C.c_void_p), ("n_stages", C.c_int32), ("stage_layer", C.c_int32 * 3),
-                ("stage_pos", C.c_void_p * 3), ("stage_n", C.c_int32 * 3)]
+                ("stage_pos", C.c_void_p * 3), ("stage_n", C.c_int32 * 3), ("group_rule", C.c_int32),
+                ("tau_smooth", C.c_float), ("tau_cover_bp", C.c_int32), ("max_span", C.c_int32),
+                ("cap_bp", C.c_int32)]
 
 
 class Outputs(C.Structure):
@@ -110,6 +116,8 @@ def lib() -> C.CDLL:
             "blend_profile_name": (C.c_char_p, [i32]),
             "blend_launch_count": (C.c_int64, []),
             "topk_select_dilate_noalloc": (C.c_int, [vp, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp]),
+            "span_select": (C.c_int, [vp, vp, i32, i32, i32, i32, C.c_float, i32, i32, i32, vp, vp, vp]),
+            "align_expand": (C.c_int, [vp, vp, vp, i32, i32, vp, vp, i32, i32, i32, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -123,7 +131,8 @@ EXPORTED = ("blend_workspace_size", "blend_init", "blend_destroy", "blend_last_e
             "blend_device_status", "blend_set_tensor_cores", "rope_realign", "blend_assemble",
             "kv_deviation", "topk_select_dilate", "gather_rows", "scatter_kv", "selective_layer",
             "blend_prefill", "importance_scores", "blend_profile", "blend_profile_read",
-            "blend_profile_name", "blend_launch_count", "topk_select_dilate_noalloc")
+            "blend_profile_name", "blend_launch_count", "topk_select_dilate_noalloc", "span_select",
+            "align_expand")
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -230,6 +239,18 @@ def kv_deviation(h, k_new, v_new, k_cache, v_cache, pos, n_rows, max_rows, mode,
                               _ptr(n_rows), max_rows, mode, _ptr(dev_out), _stream(stream)), h)
 
 
+def span_select(h, scores, n, base, budget, cap, tau_smooth, tau_cover_bp, max_span, budget_mode, idx_out,
+                n_out, stream=None):
+    _check(lib().span_select(h.ptr, _ptr(scores), n, base, budget, cap, float(tau_smooth), tau_cover_bp, max_span,
+                             budget_mode, _ptr(idx_out), _ptr(n_out), _stream(stream)), h)
+
+
+def align_expand(h, sel, n_sel, max_sel, sel_base, a_start, a_end, n_spec, n_target, out_base, idx_out, n_out,
+                 stream=None):
+    _check(lib().align_expand(h.ptr, _ptr(sel), _ptr(n_sel), max_sel, sel_base, _ptr(a_start), _ptr(a_end), n_spec,
+                              n_target, out_base, _ptr(idx_out), _ptr(n_out), _stream(stream)), h)
+
+
 def topk_select_dilate(h, scores, n, base, budget, window, tau, budget_mode, allowed, idx_out, n_out,
                        stream=None):
     _check(lib().topk_select_dilate(h.ptr, _ptr(scores), n, base, budget, window, tau, budget_mode,
@@ -283,7 +304,8 @@ class RequestRef:
     def __init__(self, chunk_ids: Sequence[int], query_tokens: torch.Tensor, mode: str = "ext",
                  rho_bp: int = 0, r1_bp: int = 0, window: int = 1, tau: int = 1,
                  budget_mode: str = "final", dev_mode: str = "kv", scores: Optional[torch.Tensor] = None,
-                 stages: Optional[list] = None):
+                 stages: Optional[list] = None, group_rule: str = "window", tau_smooth: float = 0.4,
+                 tau_cover_bp: int = 7000, max_span: int = 16, cap_bp: int = 0):
         self.chunk_ids = list(chunk_ids)
         self._ids = (C.c_int32 * len(self.chunk_ids))(*self.chunk_ids)
         self.query = query_tokens
@@ -296,7 +318,7 @@ class RequestRef:
         self.c = Request(len(self.chunk_ids), self._ids, int(query_tokens.numel()), query_tokens.data_ptr(),
                          MODES[mode], rho_bp, r1_bp, window, tau, BUDGETS[budget_mode], DEVMODES[dev_mode],
                          scores.data_ptr() if scores is not None else None, len(self.stages), st_layer,
-                         st_pos, st_n)
+                         st_pos, st_n, GROUP_RULES[group_rule], float(tau_smooth), tau_cover_bp, max_span, cap_bp)
 
 
 class OutputsRef:

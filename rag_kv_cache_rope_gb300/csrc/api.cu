@@ -8,6 +8,7 @@
 #include <string.h>
 
 #include <atomic>
+#include <cmath>
 #include <string>
 #include <vector>
 
@@ -524,6 +525,46 @@ int topk_select_dilate(blend_handle* h, const float* scores, int32_t n, int32_t 
     return check_cuda(h, "topk_select_dilate");
 }
 
+int span_select(blend_handle* h, const float* scores, int32_t n, int32_t base, int32_t budget, int32_t cap,
+                float tau_smooth, int32_t tau_cover_bp, int32_t max_span, int32_t budget_mode,
+                int32_t* idx_out, int32_t* n_out, void* stream) {
+    if (!h) return fail(nullptr, BLEND_EINVAL, "handle is NULL");
+    if (!scores || !idx_out || !n_out) return fail(h, BLEND_EINVAL, "NULL pointer");
+    if (n < 0 || n > 32768 || (long long)n > (long long)h->lim.max_batch * h->lim.max_chunk_rows)
+        return fail(h, BLEND_EINVAL, "n=%d outside 0..min(32768, workspace capacity)", n);
+    if (budget < 0 || cap < 0 || !std::isfinite(tau_smooth) || tau_smooth < 0.f || tau_cover_bp < 1 ||
+        tau_cover_bp > 10000 || max_span < 1 || max_span > BLEND_MAX_SPAN)
+        return fail(h, BLEND_EINVAL, "bad budget/cap/tau_smooth/tau_cover_bp/max_span");
+    if (budget_mode != BLEND_BUDGET_FINAL && budget_mode != BLEND_BUDGET_CANDIDATE)
+        return fail(h, BLEND_EINVAL, "bad budget_mode");
+    SelectBatch sb;
+    memset(&sb, 0, sizeof sb);
+    sb.n_job = 1;
+    sb.window = 1;
+    sb.tau = 1;
+    sb.budget_mode = budget_mode;
+    sb.rule = BLEND_GROUP_SPAN;
+    sb.tau_smooth = tau_smooth;
+    sb.tau_cover_bp = tau_cover_bp;
+    sb.max_span = max_span;
+    sb.j[0] = SelectJob{scores, nullptr, idx_out, n_out, n, base, budget, 0, cap};
+    launch_select(sb, h->rank, n, (cudaStream_t)stream);
+    return check_cuda(h, "span_select");
+}
+
+int align_expand(blend_handle* h, const int32_t* sel, const int32_t* n_sel, int32_t max_sel, int32_t sel_base,
+                 const int32_t* a_start, const int32_t* a_end, int32_t n_spec, int32_t n_target,
+                 int32_t out_base, int32_t* idx_out, int32_t* n_out, void* stream) {
+    if (!h) return fail(nullptr, BLEND_EINVAL, "handle is NULL");
+    if (!sel || !n_sel || !idx_out || !n_out || (n_spec > 0 && (!a_start || !a_end)))
+        return fail(h, BLEND_EINVAL, "NULL pointer");
+    if (max_sel < 0 || n_spec < 0 || n_target < 0 || n_target > BLEND_MAX_ALIGN_TARGETS)
+        return fail(h, BLEND_EINVAL, "bad sizes (max_sel %d, n_spec %d, n_target %d)", max_sel, n_spec, n_target);
+    launch_align_expand(sel, n_sel, max_sel, sel_base, a_start, a_end, n_spec, n_target, out_base, idx_out, n_out,
+                        h->err, (cudaStream_t)stream);
+    return check_cuda(h, "align_expand");
+}
+
 int gather_rows(const void* src, int64_t row_bytes, const int32_t* idx, const int32_t* n,
                 int32_t max_n, void* dst, void* stream) {
     if (!src || !idx || !n || !dst) return fail(nullptr, BLEND_EINVAL, "NULL pointer");
@@ -587,7 +628,7 @@ int selective_layer(blend_handle* h, int32_t layer, float* x, const int32_t* pos
 namespace {
 
 struct ReqInfo {
-    int P, n_c, Q, N, B, k1, max_rows;
+    int P, n_c, Q, N, B, k1, max_rows, cap;
 };
 
 int validate_batch(blend_handle* h, int n_req, const blend_request* reqs, const blend_pool* pool,
@@ -607,8 +648,22 @@ int validate_batch(blend_handle* h, int n_req, const blend_request* reqs, const 
     for (int r = 0; r < n_req; ++r) {
         const blend_request& q = reqs[r];
         if (q.mode != mode || q.window != reqs[0].window || q.tau != reqs[0].tau ||
-            q.budget_mode != reqs[0].budget_mode || q.dev_mode != reqs[0].dev_mode)
-            return fail(h, BLEND_EINVAL, "requests of one batch must share mode, window, tau, budget and deviation modes");
+            q.budget_mode != reqs[0].budget_mode || q.dev_mode != reqs[0].dev_mode ||
+            q.group_rule != reqs[0].group_rule)
+            return fail(h, BLEND_EINVAL, "requests of one batch must share mode, window, tau, budget, deviation and grouping rule");
+        if (q.group_rule != BLEND_GROUP_WINDOW && q.group_rule != BLEND_GROUP_SPAN)
+            return fail(h, BLEND_EINVAL, "request %d: bad group_rule %d", r, q.group_rule);
+        if (q.group_rule == BLEND_GROUP_SPAN) {
+            if (mode != BLEND_SEL_EXT) return fail(h, BLEND_EINVAL, "the span rule applies to EXT mode only");
+            if (q.tau_smooth != reqs[0].tau_smooth || q.tau_cover_bp != reqs[0].tau_cover_bp ||
+                q.max_span != reqs[0].max_span)
+                return fail(h, BLEND_EINVAL, "requests of one batch must share the span parameters");
+            if (!std::isfinite(q.tau_smooth) || q.tau_smooth < 0.f || q.tau_cover_bp < 1 || q.tau_cover_bp > 10000 ||
+                q.max_span < 1 || q.max_span > BLEND_MAX_SPAN)
+                return fail(h, BLEND_EINVAL, "request %d: bad tau_smooth/tau_cover_bp/max_span", r);
+            if (q.budget_mode == BLEND_BUDGET_CANDIDATE && (q.cap_bp < q.rho_bp || q.cap_bp > 10000))
+                return fail(h, BLEND_EINVAL, "request %d: cap_bp must be in rho_bp..10000", r);
+        }
         if (mode < BLEND_SEL_EXT || mode > BLEND_SEL_FULL) return fail(h, BLEND_EINVAL, "bad mode %d", mode);
         if (q.n_chunks < 1 || !q.chunk_ids || q.query_len < 1 || !q.query_tokens)
             return fail(h, BLEND_EINVAL, "request %d: needs >= 1 chunk and a non-empty query", r);
@@ -640,7 +695,14 @@ int validate_batch(blend_handle* h, int n_req, const blend_request* reqs, const 
         int chunk_rows = 0;
         if (mode == BLEND_SEL_EXT) {
             if (!q.scores) return fail(h, BLEND_EINVAL, "request %d: EXT mode needs scores", r);
-            chunk_rows = q.budget_mode == BLEND_BUDGET_FINAL ? (ri.B < ri.n_c ? ri.B : ri.n_c) : ri.n_c;
+            if (q.budget_mode == BLEND_BUDGET_FINAL) {
+                chunk_rows = ri.B < ri.n_c ? ri.B : ri.n_c;
+            } else if (q.group_rule == BLEND_GROUP_SPAN) {
+                ri.cap = ceil_bp(q.cap_bp, ri.n_c);
+                chunk_rows = ri.cap < ri.n_c ? ri.cap : ri.n_c;
+            } else {
+                chunk_rows = ri.n_c;
+            }
         } else if (mode == BLEND_SEL_HKVD) {
             if (q.r1_bp < q.rho_bp || q.r1_bp > 10000) return fail(h, BLEND_EINVAL, "request %d: r1_bp must be in rho_bp..10000", r);
             ri.k1 = ceil_bp(q.r1_bp, ri.n_c);
@@ -760,10 +822,14 @@ extern "C" int blend_prefill(blend_handle* h, int32_t n_req, const blend_request
         sb.window = reqs[0].window;
         sb.tau = reqs[0].tau;
         sb.budget_mode = reqs[0].budget_mode;
+        sb.rule = reqs[0].group_rule;
+        sb.tau_smooth = reqs[0].tau_smooth;
+        sb.tau_cover_bp = reqs[0].tau_cover_bp;
+        sb.max_span = reqs[0].max_span;
         int max_n = 0;
         for (int r = 0; r < n_req; ++r) {
             sb.j[r] = SelectJob{reqs[r].scores, nullptr, h->set[0] + bd.r[r].nc_off, h->set_n[0] + r,
-                                info[r].n_c, info[r].P, info[r].B, bd.r[r].nc_off};
+                                info[r].n_c, info[r].P, info[r].B, bd.r[r].nc_off, info[r].cap};
             max_n = info[r].n_c > max_n ? info[r].n_c : max_n;
         }
         ProfScope ps(h, PROF_SELECT, s);

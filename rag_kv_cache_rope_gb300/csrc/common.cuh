@@ -159,20 +159,31 @@ void launch_copy_sets(const BatchDesc& bd, const int32_t* src, const int32_t* sr
 // ------------------------------ selection (select.cu) ------------------------------
 struct SelectJob {
     const float* scores;   // [n]
-    const uint8_t* allowed;  // [n] or null
+    const uint8_t* allowed;  // [n] or null (window rule only)
     int32_t* out;          // [n]
     int32_t* out_n;        // scalar
     int32_t n;
     int32_t base;
     int32_t budget;
     int32_t rank_off;      // offset of this job's rank scratch
+    int32_t cap;           // span rule, CANDIDATE budget: most tokens kept after completion
 };
 struct SelectBatch {
     int32_t n_job;
     int32_t window, tau, budget_mode;
+    int32_t rule;          // BLEND_GROUP_WINDOW or BLEND_GROUP_SPAN
+    float tau_smooth;      // span rule: SpecCache 2.3 thresholds and span length
+    int32_t tau_cover_bp, max_span;
     SelectJob j[BLEND_MAX_BATCH];
 };
+// Ranks (select.cu), then the window rule (select.cu) or the span rule (span.cu).
 void launch_select(const SelectBatch& sb, int32_t* rank_scratch, int max_n, cudaStream_t s);
+void launch_rank(const SelectBatch& sb, int32_t* rank_scratch, int max_n, cudaStream_t s);
+void launch_span_finish(const SelectBatch& sb, const int32_t* rank_scratch, int max_n, cudaStream_t s);
+// SpecCache 2.4: sorted distinct union of [a_start[i], a_end[i]) over the selected i.
+void launch_align_expand(const int32_t* sel, const int32_t* n_sel, int32_t max_sel, int32_t sel_base,
+                         const int32_t* a_start, const int32_t* a_end, int32_t n_spec, int32_t n_target,
+                         int32_t out_base, int32_t* out, int32_t* n_out, int32_t* err, cudaStream_t s);
 
 // ------------------------------ GEMM (gemm_simt.cu) --------------------------------
 enum Epi { EPI_STORE_F32 = 0, EPI_ADD_F32 = 1, EPI_SWIGLU = 2, EPI_QKV_ROPE = 3 };

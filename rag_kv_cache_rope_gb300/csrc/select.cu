@@ -179,16 +179,27 @@ __global__ void __launch_bounds__(SEL_THREADS)
     if (threadIdx.x == SEL_THREADS - 1) *jb.out_n = red[SEL_THREADS - 1];
 }
 
-void launch_select(const SelectBatch& sb, int32_t* rank_scratch, int max_n, cudaStream_t s) {
+void launch_rank(const SelectBatch& sb, int32_t* rank_scratch, int max_n, cudaStream_t s) {
     if (sb.n_job <= 0) return;
     if (max_n <= 0) max_n = 1;
     dim3 g1((max_n + 255) / 256, sb.n_job);
     k_rank<<<g1, 256, 0, s>>>(sb, rank_scratch);
+    note_launch(1);
+}
+
+void launch_select(const SelectBatch& sb, int32_t* rank_scratch, int max_n, cudaStream_t s) {
+    if (sb.n_job <= 0) return;
+    if (max_n <= 0) max_n = 1;
+    launch_rank(sb, rank_scratch, max_n, s);
+    if (sb.rule == BLEND_GROUP_SPAN) {
+        launch_span_finish(sb, rank_scratch, max_n, s);
+        return;
+    }
     const size_t smem = (size_t)max_n * sizeof(int32_t);
     cudaFuncSetAttribute(k_select_finish, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          SEL_THREADS * SEL_MAX_PER_THREAD * (int)sizeof(int32_t));
     k_select_finish<<<sb.n_job, SEL_THREADS, smem, s>>>(sb, rank_scratch);
-    note_launch(2);
+    note_launch(1);
 }
 
 // ---------------------------------------------------------------- allocation-free variant
@@ -246,7 +257,7 @@ extern "C" int topk_select_dilate_noalloc(const float* scores, int32_t n, int32_
     sb.window = window;
     sb.tau = tau;
     sb.budget_mode = budget_mode;
-    sb.j[0] = SelectJob{scores, allowed, idx_out, n_out, n, base, budget, 0};
+    sb.j[0] = SelectJob{scores, allowed, idx_out, n_out, n, base, budget, 0, 0};
     // every rank entry the call reads is written by the call first: nothing to clear
     launch_select(sb, rank, n, (cudaStream_t)stream);
     cudaError_t e = cudaGetLastError();

@@ -77,6 +77,8 @@ class Workload:
     seed: int = 0
     score_layers: int = 4        # small-model hidden states [tokens, score_layers, score_dim]
     score_dim: int = 2048
+    score_phrase_max: int = 0    # >0: hidden-state scales shared within runs of 1..this many tokens
+    group_rule: str = "window"   # "window" (CacheClip grouping) | "span" (SpecCache span completion)
 
     @property
     def n_ctx(self) -> int:
@@ -104,6 +106,10 @@ WORKLOADS = {
                                    batch=8, pool_size=64, zipf_s=1.1, seed=3),
     # Qwen2.5-14B shape, 16K context (64 + 31 x 512 + 128), 20 % with window-4 dilation
     "qwen14b-16k-ext20": Workload("qwen14b-16k-ext20", QWEN14B, 64, 512, 31, 128, "ext", 2000, 0, 4, 1, seed=4),
+    # the same request selected by SpecCache span completion (tau_smooth 0.4, tau_cover 0.7,
+    # spans <= 16) over scores with phrase structure (runs of 1..8 tokens of similar scale)
+    "qwen14b-16k-span20": Workload("qwen14b-16k-span20", QWEN14B, 64, 512, 31, 128, "ext", 2000, 0, 1, 1, seed=4,
+                                   score_phrase_max=8, group_rule="span"),
 }
 
 
@@ -209,14 +215,22 @@ def workload_tokens(wl: Workload):
 
 
 def hidden_states(n_tokens: int, n_layers: int, dim: int, seed: int, device="cpu",
-                  dtype=torch.float32) -> torch.Tensor:
+                  dtype=torch.float32, phrase_max: int = 0) -> torch.Tensor:
     """Stand-in for a small model's deep-layer hidden states, [tokens, layers, dim].
 
     Each token gets its own scale (log-normal), so that the per-token norms spread
-    out the way importance scores do, plus unit Gaussian directions.
+    out the way importance scores do, plus unit Gaussian directions.  With phrase_max
+    > 0 the scale is shared within runs of 1..phrase_max tokens (a stand-in for
+    multi-token entities, SpecCache 2.3) with a 3 % per-token jitter.
     """
     g = _gen(2000 + seed, device)
     scale = torch.exp(0.5 * torch.randn(n_tokens, 1, 1, generator=g, device=device))
+    if phrase_max > 0:
+        gp = _gen(2500 + seed, "cpu")
+        lens = torch.randint(1, phrase_max + 1, (n_tokens,), generator=gp)
+        run = torch.repeat_interleave(torch.arange(n_tokens), lens)[:n_tokens].to(device)
+        jitter = 1.0 + 0.03 * torch.randn(n_tokens, 1, 1, generator=g, device=device)
+        scale = scale[run] * jitter
     h = torch.randn(n_tokens, n_layers, dim, generator=g, device=device) * scale
     return h.to(dtype)
 

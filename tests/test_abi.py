@@ -61,6 +61,8 @@ int main(void) {
   printf("blend_request %zu\n", sizeof(blend_request));
   P(blend_request, chunk_ids) P(blend_request, query_tokens) P(blend_request, scores)
   P(blend_request, n_stages) P(blend_request, stage_layer) P(blend_request, stage_pos) P(blend_request, stage_n)
+  P(blend_request, group_rule) P(blend_request, tau_smooth) P(blend_request, tau_cover_bp)
+  P(blend_request, max_span) P(blend_request, cap_bp)
   printf("blend_outputs %zu\n", sizeof(blend_outputs));
   return 0;
 }
@@ -128,6 +130,9 @@ def test_init_rejects_bad_arguments_without_a_gpu(lib):
     assert lib.gather_rows(C.c_void_p(1 << 20), 20, C.c_void_p(1 << 20), C.c_void_p(1 << 20), 1,
                            C.c_void_p(1 << 20), None) == b.EINVAL
     assert lib.importance_scores(C.c_void_p(1 << 20), 4, 0, 8, b.F32, C.c_void_p(1 << 20), None) == b.EINVAL
+    vp = C.c_void_p(1 << 20)
+    assert lib.span_select(None, vp, 8, 0, 4, 4, 0.4, 7000, 16, b.BUDGET_FINAL, vp, vp, None) == b.EINVAL
+    assert lib.align_expand(None, vp, vp, 4, 0, vp, vp, 4, 8, 0, vp, vp, None) == b.EINVAL
 
 
 def test_pack_weights_layout():

@@ -142,3 +142,13 @@ def test_align_expand():
     a0, a1 = np.array([0, 1, 1, 3]), np.array([1, 2, 3, 4])
     assert list(O.align_expand([1, 2], a0, a1)) == [1, 2]
     assert list(O.align_expand([], a0, a1)) == []
+
+
+def test_final_bisection_matches_linear_scan():
+    rng = np.random.default_rng(7)
+    for trial in range(12):
+        n = int(rng.integers(1, 160))
+        s = _rand_scores(rng, n, ["walk", "phrases", "iid"][trial % 3])
+        B = int(rng.integers(0, n + 1))
+        assert list(O.span_select_final_bisect(s, B, 0.4, 7000, 16, base=5)) == \
+            list(O.span_select(s, B, 0.4, 7000, 16, "final", base=5))
