@@ -11,7 +11,8 @@ stated next to the function.
 
 Sources (page title, section):
   * CacheClip blog, "6.1 Shared prefix and position IDs", "6.2 Auxiliary-model-guided
-    token selection", "6.3 Sliding-window grouping" (with Figure 6 and its rule list).
+    token selection" (steps 1-6 and the column-mean formula), "6.3 Sliding-window grouping"
+    (with Figure 6 and its rule list).
   * CacheClip paper (arXiv 2510.10129), "4.1 KV Cache Calibration with Shared Prefix",
     "4.3 Sliding-Window Grouping and KV Cache Update".
   * CacheBlend blog, "Prefill and the KV cache", "Selective KV recompute",
@@ -39,6 +40,10 @@ Parity pins (what each function is checked against, in tests/test_oracle_*.py):
   span_select           covered span complete, nothing else added), degenerate thresholds,
                         budget cap and final-budget maximality
   align_expand        : identity alignment, one-to-two splits, overlapping ranges
+  attention_probs /   : uniform weights for a zero query, the two-key logistic closed form,
+  column_mean_scores /  rows summing to one with zeros past the causal limit; a zero query
+  aux_attention_scores  projection gives closed-form column means; the query rows' final
+                        state equals blend_prefill on the same single-chunk request
 """
 from __future__ import annotations
 
@@ -128,6 +133,24 @@ def attention(q: np.ndarray, qpos: np.ndarray, K: np.ndarray, V: np.ndarray) -> 
             s = s - np.max(s, axis=1, keepdims=True)
             e = np.exp(s)
             out[i, heads, :] = (e / np.sum(e, axis=1, keepdims=True)) @ V[:p + 1, g, :]
+    return out
+
+
+def attention_probs(q: np.ndarray, qpos: np.ndarray, K: np.ndarray) -> np.ndarray:
+    """The attention weights behind attention(): P[n, hq, N] with P[i, h, j] =
+    softmax_j(q_i,h . K_j,g / sqrt(d)) over keys j <= qpos[i] (g = h // (hq/hkv)), and 0 for
+    j > qpos[i]."""
+    n, hq, d = q.shape
+    N, hkv = K.shape[0], K.shape[1]
+    group = hq // hkv
+    out = np.zeros((n, hq, N), dtype=F64)
+    scale = 1.0 / math.sqrt(d)
+    for i in range(n):
+        p = int(qpos[i])
+        for h in range(hq):
+            s = (K[:p + 1, h // group, :] @ q[i, h, :]) * scale
+            e = np.exp(s - np.max(s))
+            out[i, h, :p + 1] = e / np.sum(e)
     return out
 
 
@@ -485,6 +508,58 @@ def align_expand(selected, a_start, a_end) -> np.ndarray:
     for i in selected:
         out.update(range(int(a_start[i]), int(a_end[i])))
     return np.array(sorted(out), dtype=np.int64)
+
+
+def column_mean_scores(q: np.ndarray, qpos: np.ndarray, K: np.ndarray, col_lo: int, col_hi: int) -> np.ndarray:
+    """CacheClip blog 6.2, "the scoring step is just a column mean": score(j) = mean over the
+    query rows i (and, reading, over the heads) of the attention weight A[i, j], for the
+    columns j in [col_lo, col_hi)."""
+    probs = attention_probs(q, qpos, K)
+    return np.mean(probs[:, :, col_lo:col_hi], axis=(0, 1))
+
+
+def aux_query_forward(w: dict, cfg: dict, ek, ev, P: int, query_tokens):
+    """The auxiliary model on one [prefix + chunk + query] sequence whose prefix and chunk
+    rows are its precomputed cache ek, ev [L, P+L_c, hkv, d] (CacheClip blog 6.2 step 2: only
+    the query tokens are computed, the chunk side is loaded from cache).  The query rows go
+    through every layer at positions P+L_c ..; returns the last layer's query projections
+    q [Q, hq, d] (after RoPE) and its keys K [P+L_c+Q, hkv, d] (cache rows, then the query's)."""
+    L = cfg["n_layers"]
+    Q = len(query_tokens)
+    ek, ev = np.asarray(ek, dtype=F64), np.asarray(ev, dtype=F64)
+    Lc = ek.shape[1] - P
+    K = np.concatenate([ek, np.zeros((L, Q) + ek.shape[2:], dtype=F64)], axis=1)
+    V = np.concatenate([ev, np.zeros((L, Q) + ev.shape[2:], dtype=F64)], axis=1)
+    pos = np.arange(P + Lc, P + Lc + Q)
+    x = np.asarray(w["embed"], dtype=F64)[np.asarray(query_tokens)]
+    q = None
+    for layer in range(L):
+        q, _ = layer_kv(w, cfg, layer, x, pos, K[layer], V[layer])
+        if layer < L - 1:
+            x = layer_rest(w, cfg, layer, x, q, pos, K[layer], V[layer])
+    return q, K[L - 1]
+
+
+def aux_attention_scores(w: dict, cfg: dict, entries_k, entries_v, entry_tokens, prefix_tokens, chunk_ids,
+                         query_tokens) -> np.ndarray:
+    """Auxiliary-model importance scores (CacheClip blog "6.2 Auxiliary-model-guided token
+    selection", steps 1-5; CacheClip paper 4.2).
+
+    For every retrieved chunk c, in request order, the auxiliary model reads [prefix + chunk_c
+    + query] (aux_query_forward).  From the last layer's attention the query rows and chunk_c's
+    columns are kept (attention among query tokens and to the prefix is dropped after the
+    softmax, which covers all of them) and each column is averaged over the query rows and the
+    heads (reading: the pages speak of one attention matrix per layer; a multi-head model's is
+    taken as the mean over its heads).  Returns the scores of all chunk tokens [sum L_c].
+    """
+    P = len(prefix_tokens)
+    Q = len(query_tokens)
+    out = []
+    for c in chunk_ids:
+        Lc = len(entry_tokens[c])
+        q, K = aux_query_forward(w, cfg, entries_k[c], entries_v[c], P, query_tokens)
+        out.append(column_mean_scores(q, np.arange(P + Lc, P + Lc + Q), K, P, P + Lc))
+    return np.concatenate(out) if out else np.zeros(0, dtype=F64)
 
 
 def importance_scores(hidden: np.ndarray) -> np.ndarray:
