@@ -176,6 +176,8 @@ typedef struct {
     int32_t* n_c1;     /* device [n_req] or NULL */
     float* dev1;       /* device [sum N_c] or NULL: deviation at layer 1 (0 = not checked) */
     float* dev2;       /* device [sum N_c] or NULL: deviation at layer 2 */
+    void* q_last;      /* device [sum Q][hq][d] or NULL: the query rows' last-layer q after RoPE
+                        * (model dtype), read by aux_attention_scores */
 } blend_outputs;
 
 /* ---- handle ---------------------------------------------------------------- */
@@ -301,6 +303,19 @@ int span_select(blend_handle* h, const float* scores, int32_t n, int32_t base, i
 int align_expand(blend_handle* h, const int32_t* sel, const int32_t* n_sel, int32_t max_sel, int32_t sel_base,
                  const int32_t* a_start, const int32_t* a_end, int32_t n_spec, int32_t n_target,
                  int32_t out_base, int32_t* idx_out, int32_t* n_out, void* stream);
+
+/* Auxiliary-model importance scores (CacheClip blog, "6.2 Auxiliary-model-guided token
+ * selection", steps 3-5, and its formula score(j) = (1/|Q|) sum over query rows i of
+ * A_last[i, j]; CacheClip paper 4.2).  Call it after blend_prefill on the auxiliary model's
+ * handle with the same reqs, pool and out, where out->q_last was set: each request is one
+ * [prefix + chunk(s) + query] sequence, typically FORCED with an empty stage so that only
+ * the query rows are computed over the chunk's cached rows.  For every request r and chunk
+ * column j (the request's tokens P..P+N_c-1) writes scores[nc_r + j] = mean over its query
+ * rows and the model's hq heads of the last layer's softmax weight on key j, the softmax
+ * covering every key the row sees (prefix, chunks, query rows up to itself; fp32, scale
+ * 1/sqrt(d)).  scores: device [sum N_c] fp32.  Deterministic (fixed summation order). */
+int aux_attention_scores(blend_handle* h, int32_t n_req, const blend_request* reqs, const blend_pool* pool,
+                         const blend_outputs* out, float* scores, void* stream);
 
 /* Row gather: dst[i] = src[idx[i]] for i < *n (device scalar), rows of row_bytes
  * (a multiple of 16; src, dst 16-byte aligned).  max_n bounds *n. */

@@ -77,7 +77,7 @@ class Request(C.Structure):
 
 class Outputs(C.Structure):
     _fields_ = [(n, C.c_void_p) for n in ("k", "v", "hidden", "sel", "n_sel", "c1", "n_c1", "dev1",
-                                          "dev2")]
+                                          "dev2", "q_last")]
 
 
 _lib = None
@@ -117,6 +117,8 @@ def lib() -> C.CDLL:
             "blend_launch_count": (C.c_int64, []),
             "topk_select_dilate_noalloc": (C.c_int, [vp, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp]),
             "span_select": (C.c_int, [vp, vp, i32, i32, i32, i32, C.c_float, i32, i32, i32, vp, vp, vp]),
+            "aux_attention_scores": (C.c_int, [vp, i32, C.POINTER(Request), C.POINTER(Pool),
+                                               C.POINTER(Outputs), vp, vp]),
             "align_expand": (C.c_int, [vp, vp, vp, i32, i32, vp, vp, i32, i32, i32, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
@@ -132,7 +134,7 @@ EXPORTED = ("blend_workspace_size", "blend_init", "blend_destroy", "blend_last_e
             "kv_deviation", "topk_select_dilate", "gather_rows", "scatter_kv", "selective_layer",
             "blend_prefill", "importance_scores", "blend_profile", "blend_profile_read",
             "blend_profile_name", "blend_launch_count", "topk_select_dilate_noalloc", "span_select",
-            "align_expand")
+            "align_expand", "aux_attention_scores")
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -322,10 +324,13 @@ class RequestRef:
 
 
 class OutputsRef:
-    def __init__(self, k, v, hidden, sel=None, n_sel=None, c1=None, n_c1=None, dev1=None, dev2=None):
-        self.t = dict(k=k, v=v, hidden=hidden, sel=sel, n_sel=n_sel, c1=c1, n_c1=n_c1, dev1=dev1, dev2=dev2)
+    def __init__(self, k, v, hidden, sel=None, n_sel=None, c1=None, n_c1=None, dev1=None, dev2=None,
+                 q_last=None):
+        self.t = dict(k=k, v=v, hidden=hidden, sel=sel, n_sel=n_sel, c1=c1, n_c1=n_c1, dev1=dev1, dev2=dev2,
+                      q_last=q_last)
         self.c = Outputs(*[None if self.t[n] is None else self.t[n].data_ptr()
-                           for n in ("k", "v", "hidden", "sel", "n_sel", "c1", "n_c1", "dev1", "dev2")])
+                           for n in ("k", "v", "hidden", "sel", "n_sel", "c1", "n_c1", "dev1", "dev2",
+                                     "q_last")])
 
     def __getitem__(self, k):
         return self.t[k]
@@ -346,6 +351,12 @@ def blend_assemble(h, reqs: Sequence[RequestRef], pool: PoolRef, out: OutputsRef
 def blend_prefill(h, reqs: Sequence[RequestRef], pool: PoolRef, out: OutputsRef, stream=None):
     _check(lib().blend_prefill(h.ptr, len(reqs), _req_array(reqs), C.byref(pool.c), C.byref(out.c),
                                _stream(stream)), h)
+
+
+def aux_attention_scores(h, reqs: Sequence[RequestRef], pool: PoolRef, out: OutputsRef, scores: torch.Tensor,
+                         stream=None):
+    _check(lib().aux_attention_scores(h.ptr, len(reqs), _req_array(reqs), C.byref(pool.c), C.byref(out.c),
+                                      _ptr(scores), _stream(stream)), h)
 
 
 # ---------------------------------------------------------------- weight layout

@@ -83,6 +83,7 @@ struct blend_handle {
     uint8_t* mask;
     float* dev[2];
     int32_t* scratch_n;
+    float2* aux_stats;   // aux_attention_scores: softmax (max, sum) per query row and head
     float* split_ws;     // tensor-core GEMM: partials of last-wave tiles run as K halves
     int32_t* split_cnt;  // their arrival counters (zero between launches)
     int use_tc;  // tensor-core GEMM for bf16
@@ -243,6 +244,7 @@ Layout make_layout(const blend_model_cfg* c, const blend_limits* l) {
     L.add(16);                                             // 33 scratch count
     L.add(c->dtype == BLEND_BF16 ? GEMM_SPLIT_WS_FLOATS * 4 : 0);  // 34 GEMM split partials
     L.add(GEMM_SPLIT_CNT_INTS * 4);                        // 35 GEMM split counters
+    L.add(M * (size_t)c->n_q_heads * sizeof(float2));      // 36 aux score row statistics
     return L;
 }
 
@@ -283,7 +285,7 @@ void attention(blend_handle* h, const Plan& p, int n_req, int M_max, const void*
     const blend_model_cfg& c = h->cfg;
     if (c.dtype == BLEND_BF16 && h->use_tc && tc_attn_supported(c.head_dim)) {
         int rc = launch_attn_tc(h->q, h->lim.max_rows, n_req, p.req_row_end, p.row_pos, p.row_tok, M_max, kc, vc,
-                                n_tokens, h->o, c.n_q_heads, c.n_kv_heads, h->err, s);
+                                n_tokens, h->o, c.n_q_heads, c.n_kv_heads, c.head_dim, h->err, s);
         if (rc != BLEND_OK && h->host_rc == BLEND_OK) h->host_rc = rc;
         return;
     }
@@ -399,6 +401,7 @@ int blend_init(const blend_model_cfg* cfg, const blend_weights* w, const blend_l
     h->split_ws = cfg->dtype == BLEND_BF16 ? (float*)(b + L.off[i]) : nullptr;
     ++i;
     h->split_cnt = (int32_t*)(b + L.off[i++]);
+    h->aux_stats = (float2*)(b + L.off[i++]);
     h->use_tc = cfg->dtype == BLEND_BF16 ? tc_available() : 0;
     cudaStream_t s = (cudaStream_t)stream;
     cudaMemsetAsync(h->err, 0, 16, s);
@@ -929,6 +932,9 @@ extern "C" int blend_prefill(blend_handle* h, int32_t n_req, const blend_request
             h->q2 = tq;
             cur = 1 - cur;
         }
+        if (l == c.n_layers - 1 && out->q_last)
+            launch_gather_qlast(c.dtype, h->q, h->lim.max_rows, c.n_q_heads / c.n_kv_heads, c.n_kv_heads,
+                                c.head_dim, bd, h->plan[cur].req_row_end, out->q_last, qo, s);
         layer_rest(h, l, x, h->plan[cur], n_req, M_max, kc, vc, tok, s);
     }
     // ---- 4. final norm of the query rows
@@ -950,4 +956,31 @@ extern "C" int blend_prefill(blend_handle* h, int32_t n_req, const blend_request
     if (checks && out->dev1) cudaMemcpyAsync(out->dev1, h->dev[0], (size_t)nc_total * 4, cudaMemcpyDeviceToDevice, s);
     if (checks && out->dev2) cudaMemcpyAsync(out->dev2, h->dev[1], (size_t)nc_total * 4, cudaMemcpyDeviceToDevice, s);
     return finish(h, "blend_prefill");
+}
+
+extern "C" int aux_attention_scores(blend_handle* h, int32_t n_req, const blend_request* reqs, const blend_pool* pool,
+                         const blend_outputs* out, float* scores, void* stream) {
+    if (!h) return fail(nullptr, BLEND_EINVAL, "handle is NULL");
+    if (!out || !out->q_last || !scores) return fail(h, BLEND_EINVAL, "out->q_last and scores are required");
+    std::vector<ReqInfo> info;
+    int rc = validate_batch(h, n_req, reqs, pool, out, &info, false);
+    if (rc != BLEND_OK) return rc;
+    const blend_model_cfg& c = h->cfg;
+    BatchDesc bd;
+    memset(&bd, 0, sizeof bd);
+    bd.n_req = n_req;
+    int tok = 0, nc = 0, qo = 0, max_nc = 0;
+    for (int r = 0; r < n_req; ++r) {
+        bd.r[r] = ReqDesc{tok, info[r].P, info[r].n_c, info[r].Q, nc, qo};
+        tok += info[r].N;
+        nc += info[r].n_c;
+        qo += info[r].Q;
+        max_nc = info[r].n_c > max_nc ? info[r].n_c : max_nc;
+    }
+    if (qo > h->lim.max_rows) return fail(h, BLEND_ENOMEM, "%d query rows > limit %d", qo, h->lim.max_rows);
+    const size_t layer_elems = (size_t)tok * c.n_kv_heads * c.head_dim;
+    const void* k_last = (const char*)out->k + (size_t)(c.n_layers - 1) * layer_elems * elem_size(c.dtype);
+    launch_aux_scores(c.dtype, out->q_last, k_last, bd, c.n_q_heads, c.n_kv_heads, c.head_dim, qo, max_nc,
+                      h->aux_stats, scores, (cudaStream_t)stream);
+    return check_cuda(h, "aux_attention_scores");
 }

@@ -26,6 +26,8 @@
 // Warps: 0 TMA producer, 1 TMEM owner + MMA issuer, 2..5 softmax of tile A, 6..9 of
 // tile B.  All mbarrier waits are bounded (error word BLEND_ETIMEOUT, loads drained,
 // TMEM freed).
+#include <cmath>
+
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -34,14 +36,21 @@
 namespace blend {
 namespace {
 
-constexpr int D = 128;
 constexpr int BQ = 128;
 constexpr int BKV = 128;
 constexpr int KV_STAGES = 2;
-constexpr int QT_BYTES = BQ * D * 2;     // 32 KB per tile: two 16 KB column halves
+constexpr int QH_BYTES = BQ * 64 * 2;    // 16 KB: one 64-wide column half of a Q tile
 constexpr int KH_BYTES = BKV * 64 * 2;   // 16 KB: one 64-wide column half of a K or V block
-constexpr int KV_BYTES = 4 * KH_BYTES;   // K halves, then V halves
-constexpr int SMEM_BYTES = 2 * QT_BYTES + KV_STAGES * KV_BYTES + 1024;
+// Per head dim D (64 or 128): a Q tile and a K or V block hold D/64 column halves.
+template <int D> struct AttnCfg {
+    static constexpr int NH = D / 64;
+    static constexpr int QT_BYTES = NH * QH_BYTES;          // one 128-pair Q tile
+    static constexpr int KV_BYTES = 2 * NH * KH_BYTES;      // K halves, then V halves
+    static constexpr int SMEM_BYTES = 2 * QT_BYTES + KV_STAGES * KV_BYTES + 1024;
+    // kind::f16, bf16 inputs, fp32 accumulate, M128 N=D, B (V) MN-major
+    static constexpr uint32_t IDESC_PV =
+        (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((D >> 3) << 17) | ((BQ >> 4) << 24);
+};
 constexpr int TMEM_COLS = 512;  // tile t: S (and P over its first 64 columns) t*256+[0,128), O t*256+[128,256)
 constexpr int THREADS = 320;
 constexpr float RESCALE_LOG2 = 8.f;
@@ -115,10 +124,8 @@ __device__ __forceinline__ uint64_t desc_mn(uint32_t a) {
     return (uint64_t)((a & 0x3FFFF) >> 4) | ((uint64_t)(KH_BYTES >> 4) << 16) |
            ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
-// kind::f16, bf16 inputs, fp32 accumulate, M128 N128; PV additionally reads B MN-major.
+// kind::f16, bf16 inputs, fp32 accumulate, M128 N128 (S = Q K^T over 128 keys).
 constexpr uint32_t IDESC_S = (1u << 4) | (1u << 7) | (1u << 10) | ((BKV >> 3) << 17) | ((BQ >> 4) << 24);
-constexpr uint32_t IDESC_PV =
-    (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) /* B MN-major */ | ((D >> 3) << 17) | ((BQ >> 4) << 24);
 
 // D (TMEM) op= A (shared-memory descriptor) . B (shared-memory descriptor)
 __device__ __forceinline__ void umma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
@@ -225,29 +232,35 @@ __device__ __forceinline__ bool get_item(int w, int n_req, const int32_t* req_ro
 // S of tile t (into its TMEM region) for the K block whose descriptor base is kd; the
 // start-address field of a descriptor holds address / 16, so operand steps are added to
 // the descriptor itself (shared addresses stay below 2^18, so the field never carries).
+template <int D>
 __device__ __forceinline__ void issue_s(uint32_t tb, int t, uint64_t qd, uint64_t kd) {
     const uint32_t sd = tb + t * 256;
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (kk & 3) * 32, half = kk >> 2;
-        umma_ss(sd, qd + ((half * (QT_BYTES / 2) + off) >> 4), kd + ((half * KH_BYTES + off) >> 4), IDESC_S,
+        umma_ss(sd, qd + ((half * QH_BYTES + off) >> 4), kd + ((half * KH_BYTES + off) >> 4), IDESC_S,
                 kk > 0 ? 1u : 0u);
     }
 }
 // O of tile t += P (TMEM, first 64 columns of its S region) . V (block descriptor base vd).
+template <int D>
 __device__ __forceinline__ void issue_pv(uint32_t tb, int t, uint64_t vd, bool first) {
     const uint32_t od = tb + t * 256 + 128;
     const uint32_t pa = tb + t * 256;
 #pragma unroll
     for (int kk = 0; kk < BKV / 16; ++kk)
-        umma_ts(od, pa + kk * 8, vd + ((kk * 2048) >> 4), IDESC_PV, (!first || kk > 0) ? 1u : 0u);
+        umma_ts(od, pa + kk * 8, vd + ((kk * 2048) >> 4), AttnCfg<D>::IDESC_PV, (!first || kk > 0) ? 1u : 0u);
 }
 
+template <int D>
 __global__ void __launch_bounds__(THREADS, 1)
     k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
               const __grid_constant__ CUtensorMap mapV, int n_req, const int32_t* __restrict__ req_row_end,
               const int32_t* __restrict__ row_pos, const int32_t* __restrict__ row_tok, int group, int hkv,
               int m_cap, float scale_log2, bf16* __restrict__ out, int32_t* __restrict__ err) {
+    constexpr int NH = AttnCfg<D>::NH;
+    constexpr int QT_BYTES = AttnCfg<D>::QT_BYTES;
+    constexpr int KV_BYTES = AttnCfg<D>::KV_BYTES;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t q_full, q_empty, kv_full[KV_STAGES], kv_empty[KV_STAGES], s_full[2], p_full[2],
         o_full[2], o_free[2];
@@ -327,8 +340,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 // an absent second tile reloads the first (finite data, never stored)
                 const int p0 = (t == 0 || m.pair0_b < 0) ? m.pair0_a : m.pair0_b;
                 const int qrow = m.g * qslab + m.row0 * group + p0;
-                tma_2d(sQ + t * QT_BYTES, &mapQ, &q_full, 0, qrow);
-                tma_2d(sQ + t * QT_BYTES + QT_BYTES / 2, &mapQ, &q_full, 64, qrow);
+#pragma unroll
+                for (int hh = 0; hh < NH; ++hh) tma_2d(sQ + t * QT_BYTES + hh * QH_BYTES, &mapQ, &q_full, hh * 64, qrow);
             }
             for (int kb = 0; kb < m.nblk; ++kb, ++it) {
                 const int st = it % KV_STAGES;
@@ -341,10 +354,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                 mbar_expect_tx(&kv_full[st], KV_BYTES);
                 pend_kv[st] = (int)((it / KV_STAGES) & 1);
                 const int tok = m.tok_base + kb * BKV;
-                tma_3d(b, &mapK, &kv_full[st], 0, m.g, tok);
-                tma_3d(b + KH_BYTES, &mapK, &kv_full[st], 64, m.g, tok);
-                tma_3d(b + 2 * KH_BYTES, &mapV, &kv_full[st], 0, m.g, tok);
-                tma_3d(b + 3 * KH_BYTES, &mapV, &kv_full[st], 64, m.g, tok);
+#pragma unroll
+                for (int hh = 0; hh < NH; ++hh) {
+                    tma_3d(b + hh * KH_BYTES, &mapK, &kv_full[st], hh * 64, m.g, tok);
+                    tma_3d(b + (NH + hh) * KH_BYTES, &mapV, &kv_full[st], hh * 64, m.g, tok);
+                }
             }
         }
     } else if (warp == 1 && lane == 0) {
@@ -367,14 +381,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             fence_after();
             {
                 const uint64_t kd = desc_k(su32(sKV + (it % KV_STAGES) * KV_BYTES));
-                issue_s(tb, 0, qd0, kd);
+                issue_s<D>(tb, 0, qd0, kd);
                 commit(&s_full[0]);
-                issue_s(tb, 1, qd1, kd);
+                issue_s<D>(tb, 1, qd1, kd);
                 commit(&s_full[1]);
             }
             for (int kb = 0; kb < m.nblk && ok; ++kb, ++it) {
                 const int st = it % KV_STAGES;
-                const uint64_t vd = desc_mn(su32(sKV + st * KV_BYTES + 2 * KH_BYTES));
+                const uint64_t vd = desc_mn(su32(sKV + st * KV_BYTES + NH * KH_BYTES));
                 const bool more = kb + 1 < m.nblk;
                 for (int t = 0; t < 2; ++t) {
                     if (!mbar_wait(&p_full[t], it & 1, &abort_flag) ||
@@ -383,7 +397,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         break;
                     }
                     fence_after();
-                    issue_pv(tb, t, vd, kb == 0);
+                    issue_pv<D>(tb, t, vd, kb == 0);
                     if (more) {
                         const int nst = (it + 1) % KV_STAGES;
                         if (t == 0) {
@@ -394,7 +408,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                             pend_kv[nst] = -1;
                             fence_after();
                         }
-                        issue_s(tb, t, t == 0 ? qd0 : qd1, desc_k(su32(sKV + nst * KV_BYTES)));
+                        issue_s<D>(tb, t, t == 0 ? qd0 : qd1, desc_k(su32(sKV + nst * KV_BYTES)));
                         commit(&s_full[t]);
                     } else {
                         commit(&o_full[t]);
@@ -570,25 +584,12 @@ bool encode(CUtensorMap* map, int rank, const void* base, const cuuint64_t* dims
 
 }  // namespace
 
-bool tc_attn_supported(int head_dim) { return head_dim == D && tc_available(); }
+bool tc_attn_supported(int head_dim) { return (head_dim == 64 || head_dim == 128) && tc_available(); }
 
-int launch_attn_tc(const void* q, int m_cap, int n_req, const int32_t* req_row_end, const int32_t* row_pos,
-                   const int32_t* row_tok, int M_max, const void* k_cache, const void* v_cache, long long n_tokens,
-                   void* o, int hq, int hkv, int32_t* err, cudaStream_t s) {
-    if (M_max <= 0) return BLEND_OK;
-    if (!g_enc) {
-        cudaDriverEntryPointQueryResult qr;
-        void* fn = nullptr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &qr) !=
-                cudaSuccess ||
-            qr != cudaDriverEntryPointSuccess || !fn)
-            return BLEND_EUNSUPPORTED;
-        g_enc = (PFN_cuTensorMapEncodeTiled_v12000)fn;
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
-        cudaFuncSetAttribute(k_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    }
+template <int D>
+int launch_attn_d(const void* q, int m_cap, int n_req, const int32_t* req_row_end, const int32_t* row_pos,
+                  const int32_t* row_tok, int M_max, const void* k_cache, const void* v_cache, long long n_tokens,
+                  void* o, int hq, int hkv, int32_t* err, cudaStream_t s) {
     const int group = hq / hkv;
     CUtensorMap mq, mk, mv;
     cuuint64_t qd[2] = {(cuuint64_t)D, (cuuint64_t)hkv * m_cap * group};
@@ -602,11 +603,38 @@ int launch_attn_tc(const void* q, int m_cap, int n_req, const int32_t* req_row_e
     const long long tiles = (((long long)M_max * group) + BQ - 1) / BQ + n_req;
     const long long items = (long long)hkv * ((tiles + 1) / 2 + n_req);
     const int grid = (int)(items < g_sms ? items : g_sms);
-    const float scale_log2 = (float)(1.4426950408889634 / 11.313708498984761);  // log2(e) / sqrt(128)
-    k_attn_tc<<<grid, THREADS, SMEM_BYTES, s>>>(mq, mk, mv, n_req, req_row_end, row_pos, row_tok, group, hkv,
-                                                m_cap, scale_log2, (bf16*)o, err);
+    const float scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));  // log2(e) / sqrt(d)
+    k_attn_tc<D><<<grid, THREADS, AttnCfg<D>::SMEM_BYTES, s>>>(mq, mk, mv, n_req, req_row_end, row_pos, row_tok,
+                                                               group, hkv, m_cap, scale_log2, (bf16*)o, err);
     note_launch(1);
     return BLEND_OK;
+}
+
+int launch_attn_tc(const void* q, int m_cap, int n_req, const int32_t* req_row_end, const int32_t* row_pos,
+                   const int32_t* row_tok, int M_max, const void* k_cache, const void* v_cache, long long n_tokens,
+                   void* o, int hq, int hkv, int head_dim, int32_t* err, cudaStream_t s) {
+    if (M_max <= 0) return BLEND_OK;
+    if (!g_enc) {
+        cudaDriverEntryPointQueryResult qr;
+        void* fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &qr) !=
+                cudaSuccess ||
+            qr != cudaDriverEntryPointSuccess || !fn)
+            return BLEND_EUNSUPPORTED;
+        g_enc = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaFuncSetAttribute(k_attn_tc<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnCfg<64>::SMEM_BYTES);
+        cudaFuncSetAttribute(k_attn_tc<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnCfg<128>::SMEM_BYTES);
+    }
+    if (head_dim == 64)
+        return launch_attn_d<64>(q, m_cap, n_req, req_row_end, row_pos, row_tok, M_max, k_cache, v_cache, n_tokens,
+                                 o, hq, hkv, err, s);
+    if (head_dim == 128)
+        return launch_attn_d<128>(q, m_cap, n_req, req_row_end, row_pos, row_tok, M_max, k_cache, v_cache, n_tokens,
+                                  o, hq, hkv, err, s);
+    return BLEND_EUNSUPPORTED;
 }
 
 }  // namespace blend

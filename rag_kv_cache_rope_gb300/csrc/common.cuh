@@ -180,6 +180,12 @@ struct SelectBatch {
 void launch_select(const SelectBatch& sb, int32_t* rank_scratch, int max_n, cudaStream_t s);
 void launch_rank(const SelectBatch& sb, int32_t* rank_scratch, int max_n, cudaStream_t s);
 void launch_span_finish(const SelectBatch& sb, const int32_t* rank_scratch, int max_n, cudaStream_t s);
+// CacheClip 6.2 auxiliary scores (aux.cu): the query rows' last-layer q out of the per-kv-head
+// slab, then per chunk column the mean attention weight over query rows and heads.
+void launch_gather_qlast(int dtype, const void* qslab, int m_cap, int group, int hkv, int d, const BatchDesc& bd,
+                         const int32_t* req_row_end, void* q_last, int n_qrows, cudaStream_t s);
+void launch_aux_scores(int dtype, const void* q_last, const void* K, const BatchDesc& bd, int hq, int hkv, int d,
+                       int n_qrows, int max_nc, float2* stats, float* scores, cudaStream_t s);
 // SpecCache 2.4: sorted distinct union of [a_start[i], a_end[i]) over the selected i.
 void launch_align_expand(const int32_t* sel, const int32_t* n_sel, int32_t max_sel, int32_t sel_base,
                          const int32_t* a_start, const int32_t* a_end, int32_t n_spec, int32_t n_target,

@@ -226,7 +226,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int M = *M_dev;
-    const int m_tiles = (M + BM - 1) / BM, n_tiles = N / BN;
+    const int m_tiles = (M + BM - 1) / BM, n_tiles = (N + BN - 1) / BN;  // the last N-tile may be partial
     const int n_total = m_tiles * n_tiles;
     const int kblocks = K / BK;
     const Sched sc = make_sched(n_total, gridDim.x, EPI != EPI_QKV_ROPE && split_ws != nullptr && kblocks >= 2);
@@ -402,7 +402,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     uint32_t r[32];
                     TMEM_LD32(tl + c, r);
                     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-                    if (row < M) epi_chunk<EPI>(r, row, nt * BN + c, Cv, ldc);
+                    if (row < M && nt * BN + c < N) epi_chunk<EPI>(r, row, nt * BN + c, Cv, ldc);
                 }
             } else {
                 // split tile: publish this half's partial rows, then the second arrival
@@ -435,7 +435,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         uint32_t r[32];
                         TMEM_LD32(tl + c, r);
                         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-                        if (row < M) {
+                        if (row < M && nt * BN + c < N) {
                             const float4* q = reinterpret_cast<const float4*>(other + c);
 #pragma unroll
                             for (int v = 0; v < 8; ++v) {
@@ -525,14 +525,17 @@ int tc_available() {
 }
 
 bool tc_gemm_supported(int K, int N, int epi, int ldc, int M_cap) {
-    (void)epi;
-    return K >= BK && K % BK == 0 && N >= 128 && N % 128 == 0 && ldc % 8 == 0 && M_cap >= BM;
+    if (epi == EPI_QKV_ROPE && N % 256 != 0) return false;
+    return K >= BK && K % BK == 0 && N >= 128 && N % 32 == 0 && ldc % 8 == 0 && M_cap >= BM;
 }
 
-// N-tile width: 256 unless N is not a multiple of 256.  (128-wide tiles fill the last
-// wave better for N = 5120 at ~3.3K rows, but measured 30-40 % slower per FLOP.)
+// N-tile width: 256, or 128 when N is a multiple of 128 but not of 256 or smaller than
+// 256 (the weight tensor must be at least one box high).  Otherwise the last 256-wide
+// tile is partial: the TMA fills the rows past N with zeros and the epilogue skips
+// those columns.  (128-wide tiles fill the last wave better for N = 5120 at ~3.3K rows,
+// but measured 30-40 % slower per FLOP.)
 int pick_bn(int M_max, int N) {
-    if (N % 256 != 0) return 128;
+    if (N < 256 || (N % 256 != 0 && N % 128 == 0)) return 128;
     const long long m_tiles = (M_max + BM - 1) / BM;
     auto fill = [&](int bn) {
         const long long tiles = m_tiles * (N / bn);
@@ -546,7 +549,7 @@ int pick_bn(int M_max, int N) {
 template <int BN>
 void launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, int K, int N, const int32_t* M_dev, int M_max,
                int epi, void* C, int ldc, int32_t* err, cudaStream_t s, const QkvEpi& qe, float* ws, int32_t* cnt) {
-    const int tiles = ((M_max + BM - 1) / BM) * (N / BN);
+    const int tiles = ((M_max + BM - 1) / BM) * ((N + BN - 1) / BN);
     int grid = tiles < g_num_sms ? tiles : g_num_sms;
     // fewer tiles than half the SMs: every tile runs as two K halves on two CTAs
     if (ws != nullptr && epi != EPI_QKV_ROPE && K / BK >= 2 && 2 * tiles <= g_num_sms) grid = 2 * tiles;

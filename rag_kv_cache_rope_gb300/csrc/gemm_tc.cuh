@@ -22,11 +22,11 @@ constexpr size_t GEMM_SPLIT_CNT_INTS = (size_t)GEMM_MAX_SPLIT_TILES * 4;
 int launch_gemm_tc(const void* A, int K, int M_cap, const void* B, int N, const int32_t* M_dev, int M_max,
                    int epi, void* C, int ldc, int32_t* err, cudaStream_t s, const QkvEpi* qkv = nullptr,
                    float* split_ws = nullptr, int32_t* split_cnt = nullptr);
-// Tensor-core attention (attn_tc.cu): head_dim 128, bf16.
+// Tensor-core attention (attn_tc.cu): head_dim 64 or 128, bf16.
 bool tc_attn_supported(int head_dim);
-// q: per kv head a slab [m_cap][group][128]; rows of request r are
-// req_row_end[r-1]..req_row_end[r]-1 (device); caches: this layer's [n_tokens][hkv][128].
+// q: per kv head a slab [m_cap][group][head_dim]; rows of request r are
+// req_row_end[r-1]..req_row_end[r]-1 (device); caches: this layer's [n_tokens][hkv][head_dim].
 int launch_attn_tc(const void* q, int m_cap, int n_req, const int32_t* req_row_end, const int32_t* row_pos,
                    const int32_t* row_tok, int M_max, const void* k_cache, const void* v_cache, long long n_tokens,
-                   void* o, int hq, int hkv, int32_t* err, cudaStream_t s);
+                   void* o, int hq, int hkv, int head_dim, int32_t* err, cudaStream_t s);
 }  // namespace blend

@@ -64,6 +64,7 @@ int main(void) {
   P(blend_request, group_rule) P(blend_request, tau_smooth) P(blend_request, tau_cover_bp)
   P(blend_request, max_span) P(blend_request, cap_bp)
   printf("blend_outputs %zu\n", sizeof(blend_outputs));
+  P(blend_outputs, dev2) P(blend_outputs, q_last)
   return 0;
 }
 """

@@ -34,6 +34,8 @@ SHAPES = [
     (synth.ModelShape("tc-wide", 2, 2048, 16, 4, 128, 5632, 300, 1e6), 1000, 1500),
     # 5 query heads per kv head (the 14B grouping), contexts spanning ~60 key blocks
     (synth.ModelShape("tc-gqa5", 2, 1280, 10, 2, 128, 2560, 300, 1e6), 700, 4000),
+    # SmolLM2-135M widths: projections of 960 and 576 columns end in partial 256-wide tiles
+    (synth.ModelShape("tc-smol", 2, 576, 9, 3, 64, 1536, 300, 1e5), 500, 900),
 ]
 
 
