@@ -87,6 +87,8 @@ def parse():
                     help="truncate the model to this many layers (profiling captures only; not a headline)")
     ap.add_argument("--full-prefill-steps", type=int, default=2,
                     help="also time full prefill of the same input (every row recomputed; 0 skips it)")
+    ap.add_argument("--pool", default="device", choices=["device", "host"],
+                    help="chunk-KV pool in HBM, or in pinned host memory read layer by layer (overlapped)")
     return ap.parse_args()
 
 
@@ -158,7 +160,7 @@ class ClockSampler:
 class Setup:
     """Device-resident inputs, weights, handle and outputs for one replica."""
 
-    def __init__(self, wl: synth.Workload, dev: torch.device, max_rows_full: bool):
+    def __init__(self, wl: synth.Workload, dev: torch.device, max_rows_full: bool, pool_loc: str = "device"):
         from rag_kv_cache_rope_gb300 import binding as b
         self.b = b
         self.wl = wl
@@ -175,7 +177,13 @@ class Setup:
         lens = [wl.chunk_len] * len(pool_tok.chunks)
         self.pool_k, self.pool_v, row_off = synth.random_pool_kv(sh, wl.prefix_len, lens, wl.seed, device=dev)
         tok = torch.cat([torch.cat([pool_tok.prefix, c]) for c in pool_tok.chunks]).to(dev)
-        self.pool = b.PoolRef(self.pool_k, self.pool_v, tok, wl.prefix_len, lens, row_off)
+        self.pool_loc = pool_loc
+        if pool_loc == "host":
+            # pinned host copies the GPU reads in place, layer by layer
+            self.pool_k, self.pool_v = self.pool_k.cpu().pin_memory(), self.pool_v.cpu().pin_memory()
+            tok = tok.cpu().pin_memory()
+            torch.cuda.empty_cache()
+        self.pool = b.PoolRef(self.pool_k, self.pool_v, tok, wl.prefix_len, lens, row_off, location=pool_loc)
         self.N = wl.n_ctx
         self.n_c = wl.n_chunk_rows
         self.Q = wl.query_len
@@ -235,7 +243,7 @@ def run_ours(args, wl, rank, world):
     from rag_kv_cache_rope_gb300 import binding as b
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    S = Setup(wl, dev, max_rows_full=False)
+    S = Setup(wl, dev, max_rows_full=False, pool_loc=args.pool)
     sh = wl.model
     for _ in range(args.warmup):
         S.step()
@@ -303,7 +311,7 @@ def run_ours(args, wl, rank, world):
         "config": {"workload": wl.name, "model_shape": sh.name, "n_ctx": S.N, "prefix": wl.prefix_len,
                    "chunks": f"{wl.n_chunks}x{wl.chunk_len}", "query": wl.query_len, "mode": wl.mode,
                    "rho_bp": wl.rho_bp, "window": wl.window, "tau": wl.tau, "budget": wl.budget_mode,
-                   "group_rule": wl.group_rule,
+                   "group_rule": wl.group_rule, "pool": args.pool,
                    "rows_per_layer": rows, "layers": sh.n_layers, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (weights %.1f GB, chunk pool %.1f GB)" % (
                        sum(t.numel() * t.element_size() for t in S.packed.values()) / 1e9,
@@ -337,7 +345,47 @@ def run_ours(args, wl, rank, world):
         fms = f0.elapsed_time(f1) / args.full_prefill_steps
         line["full_prefill"] = {"ttft_ms": fms, "tokens_per_s": S.N / (fms / 1e3), "speedup_of_blend": fms / ms,
                                 "steps": args.full_prefill_steps}
+        line["loading"] = loading(S, args, fms)
     return line, S
+
+
+def loading(S: Setup, args, full_ms: float) -> dict:
+    """The pool read alone (every layer's assembly, from HBM or from pinned host memory),
+    and the recompute ratio CacheBlend's loading controller picks from it and the measured
+    full prefill (CacheBlend blog, "Making the recompute free")."""
+    b = S.b
+    sh = S.wl.model
+    es = 2 if sh.dtype == "bf16" else 4
+    kv_bytes = 2.0 * sh.n_layers * (S.wl.prefix_len + S.n_c) * sh.n_kv_heads * sh.head_dim * es
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if S.pool_loc == "host":
+        # what the pipelined path does: copy-engine transfers of the pool into HBM
+        dk, dv = torch.empty_like(S.pool_k, device=S.dev), torch.empty_like(S.pool_v, device=S.dev)
+        kind = "host-to-device copies (copy engines) of the whole pool"
+        def once():
+            dk.copy_(S.pool_k, non_blocking=True)
+            dv.copy_(S.pool_v, non_blocking=True)
+    else:
+        kind = "assembly of every layer from the HBM pool"
+        def once():
+            b.blend_assemble(S.h, [S.req], S.pool, S.out)
+    once()
+    torch.cuda.synchronize()
+    a0.record()
+    for _ in range(3):
+        once()
+    a1.record()
+    torch.cuda.synchronize()
+    t = a0.elapsed_time(a1) / 3
+    if S.pool_loc == "host":
+        kv_bytes = float(dk.numel() * dk.element_size() * 2)
+        del dk, dv
+        torch.cuda.empty_cache()
+    bw = kv_bytes / (t / 1e3)
+    return {"pool": S.pool_loc, "measured": kind, "pool_read_bytes": kv_bytes, "pool_read_ms": t,
+            "pool_read_gbps": bw / 1e9,
+            "full_prefill_ms": full_ms,
+            "controller_rho_bp": b.blend_ratio_controller(full_ms / 1e3, kv_bytes, bw, 1500)}
 
 
 def e2e(S: Setup, args, world):

@@ -68,6 +68,9 @@ extern "C" {
 #define BLEND_GROUP_WINDOW 0
 #define BLEND_GROUP_SPAN 1
 
+#define BLEND_POOL_DEVICE 0
+#define BLEND_POOL_HOST 1
+
 #define BLEND_DEV_KV 0 /* deviation = |k-k'|^2 + |v-v'|^2 */
 #define BLEND_DEV_V 1  /* deviation = |v-v'|^2 */
 
@@ -131,6 +134,14 @@ typedef struct {
     const void* k;             /* device [L][n_rows][hkv][d] */
     const void* v;             /* device [L][n_rows][hkv][d] */
     const int32_t* tokens;     /* device [n_rows] token id of each row */
+    /* BLEND_POOL_DEVICE: k, v, tokens in device memory.  BLEND_POOL_HOST: in pinned host
+     * memory (cudaHostAlloc / cudaHostRegister).  blend_prefill then copies each layer's
+     * pool rows into one of two staging buffers with the copy engines on a side stream,
+     * two layers ahead, and realigns them into the blended cache just before that layer's
+     * recompute, which waits only for its own layer (CacheBlend blog, "Making the
+     * recompute free": loading and recompute overlap).  The pool rows one call reads must
+     * fit max_tokens (BLEND_ENOMEM otherwise). */
+    int32_t location;
 } blend_pool;
 
 /* ---- one request ----------------------------------------------------------- */
@@ -316,6 +327,23 @@ int align_expand(blend_handle* h, const int32_t* sel, const int32_t* n_sel, int3
  * 1/sqrt(d)).  scores: device [sum N_c] fp32.  Deterministic (fixed summation order). */
 int aux_attention_scores(blend_handle* h, int32_t n_req, const blend_request* reqs, const blend_pool* pool,
                          const blend_outputs* out, float* scores, void* stream);
+
+/* CacheBlend's loading controller (CacheBlend blog, "Making the recompute free").  The
+ * recompute delay is rho x full_prefill_s (the offline-profiled full prefill of the
+ * context); the load delay is kv_bytes / load_bytes_per_s.  rho is the ratio where the
+ * two are equal, raised to the quality floor floor_bp (15 % on the pages) and capped at
+ * 100 %: *rho_bp = min(10000, max(floor_bp, ceil(10000 * load / full_prefill_s)))
+ * (double arithmetic in that order).  Host arithmetic only; BLEND_EINVAL unless every
+ * time, size and rate is positive and finite and 0 <= floor_bp <= 10000. */
+int blend_ratio_controller(double full_prefill_s, double kv_bytes, double load_bytes_per_s, int32_t floor_bp,
+                           int32_t* rho_bp);
+/* The same estimators run backwards (CacheBlend blog, "Making the recompute free"): at
+ * the floor ratio, keep the storage devices whose load delay kv_bytes / bytes_per_s[i]
+ * is at most floor x full_prefill_s, and return in *best the index of the cheapest
+ * (lowest cost_per_byte[i]; the lower index on a tie), or -1 if none qualifies.  Host
+ * arrays of n_dev entries; host arithmetic only. */
+int blend_pick_storage(double full_prefill_s, double kv_bytes, int32_t floor_bp, int32_t n_dev,
+                       const double* bytes_per_s, const double* cost_per_byte, int32_t* best);
 
 /* Row gather: dst[i] = src[idx[i]] for i < *n (device scalar), rows of row_bytes
  * (a multiple of 16; src, dst 16-byte aligned).  max_n bounds *n. */

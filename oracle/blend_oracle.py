@@ -40,6 +40,8 @@ Parity pins (what each function is checked against, in tests/test_oracle_*.py):
   span_select           covered span complete, nothing else added), degenerate thresholds,
                         budget cap and final-budget maximality
   align_expand        : identity alignment, one-to-two splits, overlapping ranges
+  ratio_controller /  : hand-computed delays (matching ratio, the floor, the 100 % cap); the
+  pick_storage          cheapest device that hides the load, none when no device does
   attention_probs /   : uniform weights for a zero query, the two-key logistic closed form,
   column_mean_scores /  rows summing to one with zeros past the causal limit; a zero query
   aux_attention_scores  projection gives closed-form column means; the query rows' final
@@ -560,6 +562,32 @@ def aux_attention_scores(w: dict, cfg: dict, entries_k, entries_v, entry_tokens,
         q, K = aux_query_forward(w, cfg, entries_k[c], entries_v[c], P, query_tokens)
         out.append(column_mean_scores(q, np.arange(P + Lc, P + Lc + Q), K, P, P + Lc))
     return np.concatenate(out) if out else np.zeros(0, dtype=F64)
+
+
+# ----------------------------------------------------------------------------------
+# CacheBlend loading controller (CacheBlend blog, "Making the recompute free")
+# ----------------------------------------------------------------------------------
+
+def ratio_controller(full_prefill_s: float, kv_bytes: float, load_bytes_per_s: float, floor_bp: int) -> int:
+    """Recompute delay = rho x (offline-profiled full prefill time); load delay = KV size of
+    the context / the device's throughput.  rho is where the two delays are equal, then the
+    larger of that and the quality floor (15 % on the pages), at most 100 %.  Returned in
+    basis points, rounded up (reading: the pages give no rounding)."""
+    load_s = kv_bytes / load_bytes_per_s
+    r = math.ceil(10000.0 * (load_s / full_prefill_s))
+    return int(min(10000, max(floor_bp, r)))
+
+
+def pick_storage(full_prefill_s: float, kv_bytes: float, floor_bp: int, bytes_per_s, cost_per_byte) -> int:
+    """The estimators run backwards: fix the ratio at the floor, keep the devices on which
+    the recompute takes at least as long as the load, and take the cheapest survivor
+    (reading: ties go to the first listed).  -1 when none qualifies."""
+    budget_s = (floor_bp / 10000.0) * full_prefill_s
+    best = -1
+    for i, (bw, cost) in enumerate(zip(bytes_per_s, cost_per_byte)):
+        if kv_bytes / bw <= budget_s and (best < 0 or cost < cost_per_byte[best]):
+            best = i
+    return best
 
 
 def importance_scores(hidden: np.ndarray) -> np.ndarray:

@@ -22,6 +22,7 @@ SEL_EXT, SEL_HKVD, SEL_FORCED, SEL_FULL = 0, 1, 2, 3
 BUDGET_FINAL, BUDGET_CANDIDATE = 0, 1
 DEV_KV, DEV_V = 0, 1
 GROUP_WINDOW, GROUP_SPAN = 0, 1
+POOL_DEVICE, POOL_HOST = 0, 1
 MAX_BATCH = 64
 MAX_SPAN = 64
 MAX_ALIGN_TARGETS = 131072
@@ -61,7 +62,7 @@ class Pool(C.Structure):
     _fields_ = [("n_entries", C.c_int32), ("prefix_len", C.c_int32),
                 ("entry_len", C.POINTER(C.c_int32)), ("entry_row", C.POINTER(C.c_int64)),
                 ("present", C.POINTER(C.c_uint8)), ("n_rows", C.c_int64), ("k", C.c_void_p),
-                ("v", C.c_void_p), ("tokens", C.c_void_p)]
+                ("v", C.c_void_p), ("tokens", C.c_void_p), ("location", C.c_int32)]
 
 
 class Request(C.Structure):
@@ -119,6 +120,9 @@ def lib() -> C.CDLL:
             "span_select": (C.c_int, [vp, vp, i32, i32, i32, i32, C.c_float, i32, i32, i32, vp, vp, vp]),
             "aux_attention_scores": (C.c_int, [vp, i32, C.POINTER(Request), C.POINTER(Pool),
                                                C.POINTER(Outputs), vp, vp]),
+            "blend_ratio_controller": (C.c_int, [C.c_double, C.c_double, C.c_double, i32, C.POINTER(i32)]),
+            "blend_pick_storage": (C.c_int, [C.c_double, C.c_double, i32, i32, C.POINTER(C.c_double),
+                                             C.POINTER(C.c_double), C.POINTER(i32)]),
             "align_expand": (C.c_int, [vp, vp, vp, i32, i32, vp, vp, i32, i32, i32, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
@@ -134,7 +138,7 @@ EXPORTED = ("blend_workspace_size", "blend_init", "blend_destroy", "blend_last_e
             "kv_deviation", "topk_select_dilate", "gather_rows", "scatter_kv", "selective_layer",
             "blend_prefill", "importance_scores", "blend_profile", "blend_profile_read",
             "blend_profile_name", "blend_launch_count", "topk_select_dilate_noalloc", "span_select",
-            "align_expand", "aux_attention_scores")
+            "align_expand", "aux_attention_scores", "blend_ratio_controller", "blend_pick_storage")
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -289,15 +293,17 @@ def importance_scores(hidden, n, n_layers, dim, out, stream=None):
 
 # ---------------------------------------------------------------- pool / requests / outputs
 class PoolRef:
-    """Host-side description of a device chunk-KV pool (see blend_pool)."""
+    """Host-side description of a chunk-KV pool (see blend_pool): tensors on the GPU, or
+    pinned CPU tensors (location "host") that the GPU reads in place."""
 
-    def __init__(self, k, v, tokens, prefix_len, entry_len, entry_row, present=None):
+    def __init__(self, k, v, tokens, prefix_len, entry_len, entry_row, present=None, location: str = "device"):
         self.k, self.v, self.tokens = k, v, tokens
         self._len = (C.c_int32 * len(entry_len))(*entry_len)
         self._row = (C.c_int64 * len(entry_row))(*entry_row)
         self._present = None if present is None else (C.c_uint8 * len(present))(*present)
         self.c = Pool(len(entry_len), prefix_len, self._len, self._row, self._present, k.shape[1],
-                      k.data_ptr(), v.data_ptr(), tokens.data_ptr())
+                      k.data_ptr(), v.data_ptr(), tokens.data_ptr(),
+                      {"device": POOL_DEVICE, "host": POOL_HOST}[location])
         self.entry_len = list(entry_len)
         self.prefix_len = prefix_len
 
@@ -357,6 +363,22 @@ def aux_attention_scores(h, reqs: Sequence[RequestRef], pool: PoolRef, out: Outp
                          stream=None):
     _check(lib().aux_attention_scores(h.ptr, len(reqs), _req_array(reqs), C.byref(pool.c), C.byref(out.c),
                                       _ptr(scores), _stream(stream)), h)
+
+
+def blend_ratio_controller(full_prefill_s: float, kv_bytes: float, load_bytes_per_s: float,
+                           floor_bp: int = 1500) -> int:
+    out = C.c_int32()
+    _check(lib().blend_ratio_controller(full_prefill_s, kv_bytes, load_bytes_per_s, floor_bp, C.byref(out)))
+    return out.value
+
+
+def blend_pick_storage(full_prefill_s: float, kv_bytes: float, floor_bp: int, bytes_per_s, cost_per_byte) -> int:
+    n = len(bytes_per_s)
+    bw = (C.c_double * max(n, 1))(*bytes_per_s)
+    cost = (C.c_double * max(n, 1))(*cost_per_byte)
+    out = C.c_int32()
+    _check(lib().blend_pick_storage(full_prefill_s, kv_bytes, floor_bp, n, bw, cost, C.byref(out)))
+    return out.value
 
 
 # ---------------------------------------------------------------- weight layout

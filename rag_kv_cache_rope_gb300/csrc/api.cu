@@ -7,6 +7,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <string>
@@ -84,6 +85,13 @@ struct blend_handle {
     float* dev[2];
     int32_t* scratch_n;
     float2* aux_stats;   // aux_attention_scores: softmax (max, sum) per query row and head
+    // host-memory pool: per-layer copies into two staging buffers on a side stream (copy
+    // engines), one event per layer, one per staging buffer
+    void* stage[4];  // K0, V0, K1, V1
+    cudaStream_t side = nullptr;
+    cudaEvent_t ev_start = nullptr;
+    cudaEvent_t ev_free[2] = {nullptr, nullptr};
+    std::vector<cudaEvent_t> ev_layer;
     float* split_ws;     // tensor-core GEMM: partials of last-wave tiles run as K halves
     int32_t* split_cnt;  // their arrival counters (zero between launches)
     int use_tc;  // tensor-core GEMM for bf16
@@ -96,6 +104,11 @@ struct blend_handle {
     size_t ev_used = 0;
     ~blend_handle() {
         for (cudaEvent_t e : ev_pool) cudaEventDestroy(e);
+        for (cudaEvent_t e : ev_layer) cudaEventDestroy(e);
+        if (ev_start) cudaEventDestroy(ev_start);
+        for (cudaEvent_t e : ev_free)
+            if (e) cudaEventDestroy(e);
+        if (side) cudaStreamDestroy(side);
     }
     cudaEvent_t next_event() {
         if (ev_used == ev_pool.size()) {
@@ -245,6 +258,8 @@ Layout make_layout(const blend_model_cfg* c, const blend_limits* l) {
     L.add(c->dtype == BLEND_BF16 ? GEMM_SPLIT_WS_FLOATS * 4 : 0);  // 34 GEMM split partials
     L.add(GEMM_SPLIT_CNT_INTS * 4);                        // 35 GEMM split counters
     L.add(M * (size_t)c->n_q_heads * sizeof(float2));      // 36 aux score row statistics
+    for (int b = 0; b < 4; ++b)                            // 37..40 host-pool staging: K, V x 2 buffers
+        L.add((size_t)l->max_tokens * kvd * es);
     return L;
 }
 
@@ -402,6 +417,7 @@ int blend_init(const blend_model_cfg* cfg, const blend_weights* w, const blend_l
     ++i;
     h->split_cnt = (int32_t*)(b + L.off[i++]);
     h->aux_stats = (float2*)(b + L.off[i++]);
+    for (int q = 0; q < 4; ++q) h->stage[q] = b + L.off[i++];
     h->use_tc = cfg->dtype == BLEND_BF16 ? tc_available() : 0;
     cudaStream_t s = (cudaStream_t)stream;
     cudaMemsetAsync(h->err, 0, 16, s);
@@ -568,6 +584,37 @@ int align_expand(blend_handle* h, const int32_t* sel, const int32_t* n_sel, int3
     return check_cuda(h, "align_expand");
 }
 
+int blend_ratio_controller(double full_prefill_s, double kv_bytes, double load_bytes_per_s, int32_t floor_bp,
+                           int32_t* rho_bp) {
+    if (!rho_bp) return fail(nullptr, BLEND_EINVAL, "rho_bp is NULL");
+    if (!(std::isfinite(full_prefill_s) && full_prefill_s > 0) || !(std::isfinite(kv_bytes) && kv_bytes > 0) ||
+        !(std::isfinite(load_bytes_per_s) && load_bytes_per_s > 0) || floor_bp < 0 || floor_bp > 10000)
+        return fail(nullptr, BLEND_EINVAL, "controller inputs must be positive and finite, floor in 0..10000");
+    const double load_s = kv_bytes / load_bytes_per_s;
+    const double r = std::ceil(10000.0 * (load_s / full_prefill_s));
+    const double v = r > 10000.0 ? 10000.0 : (r < (double)floor_bp ? (double)floor_bp : r);
+    *rho_bp = (int32_t)v;
+    return BLEND_OK;
+}
+
+int blend_pick_storage(double full_prefill_s, double kv_bytes, int32_t floor_bp, int32_t n_dev,
+                       const double* bytes_per_s, const double* cost_per_byte, int32_t* best) {
+    if (!best || n_dev < 0 || (n_dev > 0 && (!bytes_per_s || !cost_per_byte)))
+        return fail(nullptr, BLEND_EINVAL, "NULL pointer or negative device count");
+    if (!(std::isfinite(full_prefill_s) && full_prefill_s > 0) || !(std::isfinite(kv_bytes) && kv_bytes > 0) ||
+        floor_bp < 0 || floor_bp > 10000)
+        return fail(nullptr, BLEND_EINVAL, "controller inputs must be positive and finite, floor in 0..10000");
+    const double budget_s = ((double)floor_bp / 10000.0) * full_prefill_s;
+    *best = -1;
+    for (int32_t i = 0; i < n_dev; ++i) {
+        if (!(bytes_per_s[i] > 0) || !std::isfinite(cost_per_byte[i]))
+            return fail(nullptr, BLEND_EINVAL, "device %d: throughput must be positive, cost finite", i);
+        const double load_s = kv_bytes / bytes_per_s[i];
+        if (load_s <= budget_s && (*best < 0 || cost_per_byte[i] < cost_per_byte[*best])) *best = i;
+    }
+    return BLEND_OK;
+}
+
 int gather_rows(const void* src, int64_t row_bytes, const int32_t* idx, const int32_t* n,
                 int32_t max_n, void* dst, void* stream) {
     if (!src || !idx || !n || !dst) return fail(nullptr, BLEND_EINVAL, "NULL pointer");
@@ -643,6 +690,20 @@ int validate_batch(blend_handle* h, int n_req, const blend_request* reqs, const 
         pool->prefix_len < 0 || pool->n_rows < 1)
         return fail(h, BLEND_EINVAL, "bad pool description");
     if (pool->n_rows >= (1LL << 31)) return fail(h, BLEND_EUNSUPPORTED, "pool rows per layer must be < 2^31");
+    if (pool->location != BLEND_POOL_DEVICE && pool->location != BLEND_POOL_HOST)
+        return fail(h, BLEND_EINVAL, "bad pool location %d", pool->location);
+    if (pool->location == BLEND_POOL_HOST) {
+        // the GPU reads the pool in place: it must be pinned (page-locked, mapped) host memory
+        const void* ptrs[3] = {pool->k, pool->v, pool->tokens};
+        for (const void* ptr : ptrs) {
+            cudaPointerAttributes a;
+            if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess || a.type != cudaMemoryTypeHost ||
+                a.devicePointer != ptr) {
+                cudaGetLastError();
+                return fail(h, BLEND_EINVAL, "a host pool must be pinned host memory the GPU can address directly");
+            }
+        }
+    }
     if (!out->k || !out->v || !out->hidden) return fail(h, BLEND_EINVAL, "outputs k, v and hidden are required");
     if (((uintptr_t)out->k | (uintptr_t)out->v | (uintptr_t)pool->k | (uintptr_t)pool->v) & 15)
         return fail(h, BLEND_EINVAL, "caches must be 16-byte aligned");
@@ -739,16 +800,11 @@ int validate_batch(blend_handle* h, int n_req, const blend_request* reqs, const 
 
 }  // namespace
 
-extern "C" int blend_assemble(blend_handle* h, int32_t n_req, const blend_request* reqs,
-                              const blend_pool* pool, const blend_outputs* out, void* stream) {
-    if (!h) return fail(nullptr, BLEND_EINVAL, "handle is NULL");
-    std::vector<ReqInfo> info;
-    int rc = validate_batch(h, n_req, reqs, pool, out, &info, false);
-    if (rc != BLEND_OK) return rc;
-    const blend_model_cfg& c = h->cfg;
-    cudaStream_t s = (cudaStream_t)stream;
-    static thread_local SegTable segs;
-    static thread_local QueryTable qt;
+namespace {
+// Segment table (prefix rows once, then each chunk's rows with its shift) and query table
+// of a validated batch.
+void build_segments(int n_req, const blend_request* reqs, const blend_pool* pool, const std::vector<ReqInfo>& info,
+                    SegTable& segs, QueryTable& qt, int* tok_out) {
     memset(&qt, 0, sizeof qt);
     segs.n_seg = 0;
     int row = 0, tok = 0;
@@ -775,6 +831,66 @@ extern "C" int blend_assemble(blend_handle* h, int32_t n_req, const blend_reques
         tok += info[r].N;
     }
     segs.total_rows = row;
+    *tok_out = tok;
+}
+
+// Host-pool staging: merged runs of pool rows [start, end) and their first staging row.
+struct Run {
+    long long start, end, stage;
+};
+thread_local SegTable hp_segs;
+thread_local QueryTable hp_qt;
+thread_local std::vector<Run> hp_runs;
+thread_local int hp_tok = 0;
+thread_local long long hp_staged = 0;
+
+// Copy engines: layer l's pool rows (every run, K and V) into staging buffer l % 2 on the
+// side stream, then mark layer l as landed.
+void stage_layer_copy(blend_handle* h, const blend_pool* pool, int l) {
+    const blend_model_cfg& c = h->cfg;
+    const size_t row_bytes = (size_t)c.n_kv_heads * c.head_dim * elem_size(c.dtype);
+    const char* pk = (const char*)pool->k + (size_t)l * pool->n_rows * row_bytes;
+    const char* pv = (const char*)pool->v + (size_t)l * pool->n_rows * row_bytes;
+    char* sk = (char*)h->stage[2 * (l & 1)];
+    char* sv = (char*)h->stage[2 * (l & 1) + 1];
+    for (const Run& r : hp_runs) {
+        const size_t n = (size_t)(r.end - r.start) * row_bytes;
+        cudaMemcpyAsync(sk + r.stage * row_bytes, pk + r.start * row_bytes, n, cudaMemcpyHostToDevice, h->side);
+        cudaMemcpyAsync(sv + r.stage * row_bytes, pv + r.start * row_bytes, n, cudaMemcpyHostToDevice, h->side);
+    }
+    cudaEventRecord(h->ev_layer[l], h->side);
+}
+
+// Side stream and per-layer events of the host-pool pipeline (created on first use).
+int ensure_pipeline(blend_handle* h) {
+    if (!h->side && cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) != cudaSuccess)
+        return check_cuda(h, "pipeline stream");
+    if (!h->ev_start && cudaEventCreateWithFlags(&h->ev_start, cudaEventDisableTiming) != cudaSuccess)
+        return check_cuda(h, "pipeline event");
+    for (cudaEvent_t& e : h->ev_free)
+        if (!e && cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess)
+            return check_cuda(h, "pipeline event");
+    while ((int)h->ev_layer.size() < h->cfg.n_layers) {
+        cudaEvent_t e;
+        if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return check_cuda(h, "pipeline event");
+        h->ev_layer.push_back(e);
+    }
+    return BLEND_OK;
+}
+}  // namespace
+
+extern "C" int blend_assemble(blend_handle* h, int32_t n_req, const blend_request* reqs,
+                              const blend_pool* pool, const blend_outputs* out, void* stream) {
+    if (!h) return fail(nullptr, BLEND_EINVAL, "handle is NULL");
+    std::vector<ReqInfo> info;
+    int rc = validate_batch(h, n_req, reqs, pool, out, &info, false);
+    if (rc != BLEND_OK) return rc;
+    const blend_model_cfg& c = h->cfg;
+    cudaStream_t s = (cudaStream_t)stream;
+    static thread_local SegTable segs;
+    static thread_local QueryTable qt;
+    int tok = 0;
+    build_segments(n_req, reqs, pool, info, segs, qt, &tok);
     launch_assemble(c.dtype, segs, pool->k, pool->v, pool->n_rows, out->k, out->v, tok, c.n_layers,
                     c.n_kv_heads, c.head_dim, h->rope, c.max_pos, h->err, s);
     launch_tokens(segs, qt, pool->tokens, h->tokens, s);
@@ -808,11 +924,49 @@ extern "C" int blend_prefill(blend_handle* h, int32_t n_req, const blend_request
     const size_t es = elem_size(c.dtype);
 
     // ---- 1. cache preparation (all layers) and token ids
-    {
+    const bool host_pool = pool->location == BLEND_POOL_HOST;
+    if (!host_pool) {
         ProfScope ps(h, PROF_ASSEMBLE, s);
         rc = blend_assemble(h, n_req, reqs, pool, out, stream);
-    }
-    if (rc != BLEND_OK) return rc;
+    } else {
+        rc = ensure_pipeline(h);
+        if (rc != BLEND_OK) return rc;
+        build_segments(n_req, reqs, pool, info, hp_segs, hp_qt, &hp_tok);
+        launch_tokens(hp_segs, hp_qt, pool->tokens, h->tokens, s);
+        // the pool rows this batch reads, as merged runs; each segment is re-pointed at its
+        // rows in the staging buffer
+        std::vector<std::pair<long long, long long>> iv;
+        for (int q = 0; q < hp_segs.n_seg; ++q)
+            iv.push_back({hp_segs.s[q].src_row, (long long)hp_segs.s[q].src_row + hp_segs.s[q].n_rows});
+        std::sort(iv.begin(), iv.end());
+        hp_runs.clear();
+        long long staged = 0;
+        for (auto& a : iv) {
+            if (!hp_runs.empty() && a.first <= hp_runs.back().end) {
+                if (a.second > hp_runs.back().end) {
+                    staged += a.second - hp_runs.back().end;
+                    hp_runs.back().end = a.second;
+                }
+            } else {
+                hp_runs.push_back(Run{a.first, a.second, staged});
+                staged += a.second - a.first;
+            }
+        }
+        if (staged > h->lim.max_tokens)
+            return fail(h, BLEND_ENOMEM, "%lld pool rows to stage > max_tokens %d", staged, h->lim.max_tokens);
+        hp_staged = staged;
+        for (int q = 0; q < hp_segs.n_seg; ++q) {
+            const long long src = hp_segs.s[q].src_row;
+            const Run* run = &hp_runs[0];
+            for (const Run& x : hp_runs)
+                if (x.start <= src && src < x.end) run = &x;
+            hp_segs.s[q].src_row = (int32_t)(run->stage + (src - run->start));
+        }
+        cudaEventRecord(h->ev_start, s);
+        cudaStreamWaitEvent(h->side, h->ev_start, 0);
+        for (int l = 0; l < c.n_layers && l < 2; ++l) stage_layer_copy(h, pool, l);
+        rc = check_cuda(h, "blend_prefill (pool loading)");
+    }    if (rc != BLEND_OK) return rc;
 
     // ---- 2. stage-0 rows
     StageDesc st0{h->set[0], h->set_n[0], 0};
@@ -877,6 +1031,21 @@ extern "C" int blend_prefill(blend_handle* h, int32_t n_req, const blend_request
         void* kc = (char*)out->k + (size_t)l * layer_elems * es;
         void* vc = (char*)out->v + (size_t)l * layer_elems * es;
         const Plan& p = h->plan[cur];
+        if (host_pool) {
+            // this layer's pool rows have landed in staging buffer l % 2: realign them into the
+            // blended cache, free the buffer, and start the copy of layer l + 2 into it
+            cudaStreamWaitEvent(s, h->ev_layer[l], 0);
+            {
+                ProfScope ps(h, PROF_ASSEMBLE, s);
+                launch_assemble(c.dtype, hp_segs, h->stage[2 * (l & 1)], h->stage[2 * (l & 1) + 1], hp_staged, kc, vc,
+                                tok, 1, c.n_kv_heads, c.head_dim, h->rope, c.max_pos, h->err, s, 0);
+            }
+            cudaEventRecord(h->ev_free[l & 1], s);
+            if (l + 2 < c.n_layers) {
+                cudaStreamWaitEvent(h->side, h->ev_free[l & 1], 0);
+                stage_layer_copy(h, pool, l + 2);
+            }
+        }
         float* dev = (checks && (l == 1 || l == 2)) ? h->dev[l - 1] : nullptr;
         layer_kv(h, l, x, p, p.row_req, M_max, bd, kc, vc, dev, reqs[0].dev_mode, 0, s);
         int new_stage = -1;

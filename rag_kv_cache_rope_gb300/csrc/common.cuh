@@ -120,7 +120,7 @@ void launch_realign(int dtype, const void* src, void* dst, int n_rows, const int
 void launch_assemble(int dtype, const SegTable& segs, const void* pool_k, const void* pool_v,
                      long long pool_rows, void* out_k, void* out_v, long long out_tokens,
                      int n_layers, int hkv, int d, const float2* tab, int max_pos, int32_t* err,
-                     cudaStream_t s);
+                     cudaStream_t s, int layer0 = 0);
 void launch_tokens(const SegTable& segs, const QueryTable& qt, const int32_t* pool_tokens,
                    int32_t* out_tokens, cudaStream_t s);
 void launch_rmsnorm(int dtype, const float* x, const void* g, void* out, int H, float eps,

@@ -97,10 +97,12 @@ void launch_realign(int dtype, const void* src, void* dst, int n_rows, const int
 }
 
 // ---------------------------------------------------------------- assemble
-// Concatenation + prefix drop + key realignment for every layer of a batch.  The
+// Concatenation + prefix drop + key realignment for layers layer0.. of a batch.  The
 // segment table lists, in order, the prefix rows of each request (shift 0) and each
 // chunk's rows (shift = offset of the chunk among the request's chunks).  One CTA
-// handles ASM_ROWS consecutive rows of one layer (blockIdx.y).
+// handles ASM_ROWS consecutive rows of one layer (layer0 + blockIdx.y).  The pool may
+// sit in pinned host memory that the GPU reads directly (on Grace-Blackwell over the
+// NVLink chip-to-chip link): the kernel only streams it.
 constexpr int ASM_ROWS = 8;
 
 template <typename T>
@@ -108,8 +110,8 @@ __global__ void __launch_bounds__(256)
     k_assemble(const __grid_constant__ SegTable segs, const T* __restrict__ pk,
                const T* __restrict__ pv, long long pool_rows, T* __restrict__ ok,
                T* __restrict__ ov, long long out_tokens, int hkv, int d,
-               const float2* __restrict__ tab, int max_pos, int32_t* err) {
-    const int layer = blockIdx.y;
+               const float2* __restrict__ tab, int max_pos, int32_t* err, int layer0) {
+    const int layer = layer0 + blockIdx.y;
     const int half = d / 2;
     const int VN = Vec<T>::N;
     const int per_head = half / VN;
@@ -153,7 +155,7 @@ __global__ void __launch_bounds__(256)
 void launch_assemble(int dtype, const SegTable& segs, const void* pool_k, const void* pool_v,
                      long long pool_rows, void* out_k, void* out_v, long long out_tokens,
                      int n_layers, int hkv, int d, const float2* tab, int max_pos, int32_t* err,
-                     cudaStream_t s) {
+                     cudaStream_t s, int layer0) {
     if (segs.total_rows <= 0 || n_layers <= 0) return;
     dim3 grid((segs.total_rows + ASM_ROWS - 1) / ASM_ROWS, n_layers);
     const int items = hkv * (d / 2) / (16 / (dtype == BLEND_BF16 ? 2 : 4)) +
@@ -162,12 +164,12 @@ void launch_assemble(int dtype, const SegTable& segs, const void* pool_k, const 
     if (dtype == BLEND_BF16)
         k_assemble<bf16><<<grid, threads, 0, s>>>(segs, (const bf16*)pool_k, (const bf16*)pool_v,
                                                   pool_rows, (bf16*)out_k, (bf16*)out_v,
-                                                  out_tokens, hkv, d, tab, max_pos, err);
+                                                  out_tokens, hkv, d, tab, max_pos, err, layer0);
     else
         k_assemble<float><<<grid, threads, 0, s>>>(segs, (const float*)pool_k,
                                                    (const float*)pool_v, pool_rows, (float*)out_k,
                                                    (float*)out_v, out_tokens, hkv, d, tab, max_pos,
-                                                   err);
+                                                   err, layer0);
     note_launch(1);
 }
 

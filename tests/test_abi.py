@@ -57,7 +57,7 @@ int main(void) {
   printf("blend_weights %zu\n", sizeof(blend_weights));
   printf("blend_limits %zu\n", sizeof(blend_limits));
   printf("blend_pool %zu\n", sizeof(blend_pool));
-  P(blend_pool, entry_len) P(blend_pool, n_rows) P(blend_pool, tokens)
+  P(blend_pool, entry_len) P(blend_pool, n_rows) P(blend_pool, tokens) P(blend_pool, location)
   printf("blend_request %zu\n", sizeof(blend_request));
   P(blend_request, chunk_ids) P(blend_request, query_tokens) P(blend_request, scores)
   P(blend_request, n_stages) P(blend_request, stage_layer) P(blend_request, stage_pos) P(blend_request, stage_n)
