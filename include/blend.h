@@ -59,6 +59,8 @@ extern "C" {
 #define BLEND_SEL_HKVD 1   /* KV-deviation gradual filtering (checks on layers 1 and 2) */
 #define BLEND_SEL_FORCED 2 /* caller-given stage sets */
 #define BLEND_SEL_FULL 3   /* recompute every row (full prefill through the same path) */
+#define BLEND_SEL_EPIC 4   /* static: the first epic_m tokens of every chunk (EPIC, as SpecCache
+                            * describes it) */
 
 #define BLEND_BUDGET_FINAL 0     /* at most ceil(rho*N_c) rows after grouping */
 #define BLEND_BUDGET_CANDIDATE 1 /* ceil(rho*N_c) candidates, then grouping */
@@ -172,6 +174,15 @@ typedef struct {
     int32_t max_span;            /* SPAN: longest span, 1..BLEND_MAX_SPAN (16) */
     int32_t cap_bp;              /* SPAN + CANDIDATE: most rows kept after completion, basis
                                   * points of N_c (rho_bp..10000); FINAL: the budget is the cap */
+    int32_t epic_m;              /* EPIC: tokens recomputed at the start of every chunk (>= 0) */
+    /* Early termination for unfocused chunks (Cache-Craft notes, 3.2.2), EXT and EPIC modes:
+     * with focus_bp > 0, at layer focus_layer (after its K/V projection) each chunk's share
+     * of the query rows' attention is measured (mean over query rows and heads of the
+     * softmax weight on its tokens, summed over the chunk); chunks whose share of the total
+     * is below focus_bp basis points stop being recomputed from that layer's attention on.
+     * The set after the filter is what out->sel receives. */
+    int32_t focus_layer;
+    int32_t focus_bp;
 } blend_request;
 
 /* Outputs of a batch.  Request r owns tokens tok_r .. tok_r+N_r-1 of k, v with

@@ -601,6 +601,27 @@ def importance_scores(hidden: np.ndarray) -> np.ndarray:
 # Blended prefill
 # ----------------------------------------------------------------------------------
 
+def epic_positions(prefix_len: int, chunk_lens, m: int) -> np.ndarray:
+    """EPIC's static selection (SpecCache notes, background: EPIC recomputes the first few
+    tokens of every chunk): blended positions P + off_j + t for t < min(m, L_j)."""
+    out, off = [], 0
+    for L in chunk_lens:
+        out.extend(prefix_len + off + t for t in range(min(m, L)))
+        off += L
+    return np.array(out, dtype=np.int64)
+
+
+def focused_chunks(scores: np.ndarray, chunk_lens, focus_bp: int) -> np.ndarray:
+    """Cache-Craft notes, 3.2.2 (adaptive early recomputation termination): the query's
+    attention identifies focused chunks and recomputation stops for the others.  Readings
+    (the notes give no formula): a chunk's question attention is the sum over its tokens of
+    the column-mean scores (column_mean_scores at the detection layer); it is focused when
+    that share of the total is at least focus_bp basis points."""
+    s = np.asarray(scores, dtype=F64)
+    mass = np.array([s[a:a + L].sum() for a, L in zip(np.cumsum([0] + list(chunk_lens)[:-1]), chunk_lens)])
+    return mass * 10000.0 >= focus_bp * mass.sum()
+
+
 def ceil_bp(rho_bp: int, n: int) -> int:
     """ceil(rho * n) with rho in basis points (SpecCache 2.2, K = ceil(rho N))."""
     return (rho_bp * n + 9999) // 10000
@@ -614,7 +635,8 @@ def blend_prefill(w: dict, cfg: dict, entries_k, entries_v, entry_tokens, prefix
                   window: int = 1, tau: int = 1, budget_mode: str = "final",
                   scores: Optional[np.ndarray] = None, forced: Optional[list] = None,
                   dev_mode: str = "kv", group_rule: str = "window", tau_smooth: float = 0.4,
-                  tau_cover_bp: int = 7000, max_span: int = 16, cap_bp: int = 0):
+                  tau_cover_bp: int = 7000, max_span: int = 16, cap_bp: int = 0, epic_m: int = 0,
+                  focus_layer: int = 0, focus_bp: int = 0):
     """Selective KV-recompute prefill of one request.
 
     1. Assemble the blended cache (see assemble()).
@@ -640,6 +662,11 @@ def blend_prefill(w: dict, cfg: dict, entries_k, entries_v, entry_tokens, prefix
                   The set only shrinks; S is used from layer 2's attention onward.
        * "forced": the caller's stages (deviations are still reported at the check layers).
        * "full":  every row 0..N-1 at every layer (full prefill through the same steps).
+       * "epic":  one stage [(0, S)] with S = the first epic_m tokens of every chunk
+                  (EPIC's static rule as SpecCache describes it: a fixed number of tokens at
+                  the start of each chunk is recomputed, the rest reused).
+       With focus_bp > 0 (ext and epic): early termination for unfocused chunks (Cache-Craft
+       notes, 3.2.2; see focused_chunks) at focus_layer, after that layer's K/V projection.
     3. Output the final RMSNorm of the query rows and the blended K, V of every layer.
 
     Positions in sets are absolute positions in the blended sequence.
@@ -676,6 +703,8 @@ def blend_prefill(w: dict, cfg: dict, entries_k, entries_v, entry_tokens, prefix
         stages = [(int(f), np.asarray(p, dtype=np.int64)) for f, p in forced]
     elif mode == "full":
         stages = [(0, np.arange(0, hi))]
+    elif mode == "epic":
+        stages = [(0, epic_positions(P, lens, epic_m))]
     else:
         raise ValueError(mode)
 
@@ -697,6 +726,14 @@ def blend_prefill(w: dict, cfg: dict, entries_k, entries_v, entry_tokens, prefix
             full = np.zeros(n_c, dtype=F64)
             full[rows[dev_rows] - lo] = dev[dev_rows]
             devs[layer] = full
+        if focus_bp > 0 and mode in ("ext", "epic") and layer == focus_layer:
+            qq = q[len(rows) - Q:]                     # the query rows are the last Q rows
+            sc = column_mean_scores(qq, qrows, K[layer], lo, hi)
+            keep = focused_chunks(sc, lens, focus_bp)
+            starts = np.cumsum([0] + lens[:-1])
+            crow = rows[rows < hi]
+            chunk_of = np.searchsorted(starts, crow - lo, side="right") - 1
+            stages.append((layer, crow[keep[chunk_of]].astype(np.int64)))
         if mode == "hkvd" and layer == CHECK_LAYERS[0]:
             c1 = np.array(sorted(lo + t for t in topk(devs[layer], ceil_bp(r1_bp, n_c))), dtype=np.int64)
             stages.append((layer, c1))

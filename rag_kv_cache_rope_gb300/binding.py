@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_PKG, "libblend.so")
 
 OK, EINVAL, ENOMEM, ECUDA, EMISS, ETIMEOUT, EDEVICE, EUNSUPPORTED = 0, -1, -2, -3, -4, -5, -6, -7
 F32, BF16 = 0, 1
-SEL_EXT, SEL_HKVD, SEL_FORCED, SEL_FULL = 0, 1, 2, 3
+SEL_EXT, SEL_HKVD, SEL_FORCED, SEL_FULL, SEL_EPIC = 0, 1, 2, 3, 4
 BUDGET_FINAL, BUDGET_CANDIDATE = 0, 1
 DEV_KV, DEV_V = 0, 1
 GROUP_WINDOW, GROUP_SPAN = 0, 1
@@ -28,7 +28,7 @@ MAX_SPAN = 64
 MAX_ALIGN_TARGETS = 131072
 GU_BLOCK = 16
 
-MODES = {"ext": SEL_EXT, "hkvd": SEL_HKVD, "forced": SEL_FORCED, "full": SEL_FULL}
+MODES = {"ext": SEL_EXT, "hkvd": SEL_HKVD, "forced": SEL_FORCED, "full": SEL_FULL, "epic": SEL_EPIC}
 BUDGETS = {"final": BUDGET_FINAL, "candidate": BUDGET_CANDIDATE}
 DEVMODES = {"kv": DEV_KV, "v": DEV_V}
 GROUP_RULES = {"window": GROUP_WINDOW, "span": GROUP_SPAN}
@@ -73,7 +73,8 @@ class Request(C.Structure):
                 ("scores", C.c_void_p), ("n_stages", C.c_int32), ("stage_layer", C.c_int32 * 3),
                 ("stage_pos", C.c_void_p * 3), ("stage_n", C.c_int32 * 3), ("group_rule", C.c_int32),
                 ("tau_smooth", C.c_float), ("tau_cover_bp", C.c_int32), ("max_span", C.c_int32),
-                ("cap_bp", C.c_int32)]
+                ("cap_bp", C.c_int32), ("epic_m", C.c_int32), ("focus_layer", C.c_int32),
+                ("focus_bp", C.c_int32)]
 
 
 class Outputs(C.Structure):
@@ -313,7 +314,8 @@ class RequestRef:
                  rho_bp: int = 0, r1_bp: int = 0, window: int = 1, tau: int = 1,
                  budget_mode: str = "final", dev_mode: str = "kv", scores: Optional[torch.Tensor] = None,
                  stages: Optional[list] = None, group_rule: str = "window", tau_smooth: float = 0.4,
-                 tau_cover_bp: int = 7000, max_span: int = 16, cap_bp: int = 0):
+                 tau_cover_bp: int = 7000, max_span: int = 16, cap_bp: int = 0, epic_m: int = 0,
+                 focus_layer: int = 0, focus_bp: int = 0):
         self.chunk_ids = list(chunk_ids)
         self._ids = (C.c_int32 * len(self.chunk_ids))(*self.chunk_ids)
         self.query = query_tokens
@@ -326,7 +328,8 @@ class RequestRef:
         self.c = Request(len(self.chunk_ids), self._ids, int(query_tokens.numel()), query_tokens.data_ptr(),
                          MODES[mode], rho_bp, r1_bp, window, tau, BUDGETS[budget_mode], DEVMODES[dev_mode],
                          scores.data_ptr() if scores is not None else None, len(self.stages), st_layer,
-                         st_pos, st_n, GROUP_RULES[group_rule], float(tau_smooth), tau_cover_bp, max_span, cap_bp)
+                         st_pos, st_n, GROUP_RULES[group_rule], float(tau_smooth), tau_cover_bp, max_span, cap_bp,
+                         epic_m, focus_layer, focus_bp)
 
 
 class OutputsRef:

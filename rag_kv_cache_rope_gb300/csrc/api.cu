@@ -717,6 +717,13 @@ int validate_batch(blend_handle* h, int n_req, const blend_request* reqs, const 
             return fail(h, BLEND_EINVAL, "requests of one batch must share mode, window, tau, budget, deviation and grouping rule");
         if (q.group_rule != BLEND_GROUP_WINDOW && q.group_rule != BLEND_GROUP_SPAN)
             return fail(h, BLEND_EINVAL, "request %d: bad group_rule %d", r, q.group_rule);
+        if (q.focus_bp != reqs[0].focus_bp || q.focus_layer != reqs[0].focus_layer)
+            return fail(h, BLEND_EINVAL, "requests of one batch must share focus_layer and focus_bp");
+        if (q.focus_bp < 0 || q.focus_bp > 10000)
+            return fail(h, BLEND_EINVAL, "request %d: focus_bp must be in 0..10000", r);
+        if (q.focus_bp > 0 && ((mode != BLEND_SEL_EXT && mode != BLEND_SEL_EPIC) || q.focus_layer < 0 ||
+                               q.focus_layer >= c.n_layers))
+            return fail(h, BLEND_EINVAL, "request %d: focus filtering needs EXT or EPIC mode and 0 <= focus_layer < L", r);
         if (q.group_rule == BLEND_GROUP_SPAN) {
             if (mode != BLEND_SEL_EXT) return fail(h, BLEND_EINVAL, "the span rule applies to EXT mode only");
             if (q.tau_smooth != reqs[0].tau_smooth || q.tau_cover_bp != reqs[0].tau_cover_bp ||
@@ -728,7 +735,7 @@ int validate_batch(blend_handle* h, int n_req, const blend_request* reqs, const 
             if (q.budget_mode == BLEND_BUDGET_CANDIDATE && (q.cap_bp < q.rho_bp || q.cap_bp > 10000))
                 return fail(h, BLEND_EINVAL, "request %d: cap_bp must be in rho_bp..10000", r);
         }
-        if (mode < BLEND_SEL_EXT || mode > BLEND_SEL_FULL) return fail(h, BLEND_EINVAL, "bad mode %d", mode);
+        if (mode < BLEND_SEL_EXT || mode > BLEND_SEL_EPIC) return fail(h, BLEND_EINVAL, "bad mode %d", mode);
         if (q.n_chunks < 1 || !q.chunk_ids || q.query_len < 1 || !q.query_tokens)
             return fail(h, BLEND_EINVAL, "request %d: needs >= 1 chunk and a non-empty query", r);
         if (q.rho_bp < 0 || q.rho_bp > 10000 || q.window < 1 || q.window > BLEND_MAX_WINDOW || q.tau < 1 ||
@@ -783,6 +790,12 @@ int validate_batch(blend_handle* h, int n_req, const blend_request* reqs, const 
                 if (q.n_stages != reqs[0].n_stages) return fail(h, BLEND_EINVAL, "requests must have the same number of stages");
             }
             chunk_rows = q.stage_n[0];
+        } else if (mode == BLEND_SEL_EPIC) {
+            if (q.epic_m < 0) return fail(h, BLEND_EINVAL, "request %d: epic_m must be >= 0", r);
+            for (int j = 0; j < q.n_chunks; ++j) {
+                const int L = pool->entry_len[q.chunk_ids[j]];
+                chunk_rows += q.epic_m < L ? q.epic_m : L;
+            }
         } else {
             chunk_rows = ri.P + ri.n_c;
         }
@@ -998,6 +1011,27 @@ extern "C" int blend_prefill(blend_handle* h, int32_t n_req, const blend_request
         stage_layer[2] = 2;
     } else if (mode == BLEND_SEL_FULL) {
         st0.iota = 2;
+    } else if (mode == BLEND_SEL_EPIC) {
+        static thread_local EpicTable et;
+        et.n_run = 0;
+        et.n_req = n_req;
+        for (int r = 0; r < n_req; ++r) {
+            int off = 0, cnt = 0;
+            for (int j = 0; j < reqs[r].n_chunks; ++j) {
+                const int L = pool->entry_len[reqs[r].chunk_ids[j]];
+                const int m = reqs[r].epic_m < L ? reqs[r].epic_m : L;
+                if (m > 0) {
+                    et.start[et.n_run] = info[r].P + off;
+                    et.count[et.n_run] = m;
+                    et.out[et.n_run] = bd.r[r].nc_off + cnt;
+                    ++et.n_run;
+                }
+                cnt += m;
+                off += L;
+            }
+            et.req_n[r] = cnt;
+        }
+        launch_epic_set(et, h->set[0], h->set_n[0], s);
     } else {
         n_stage = reqs[0].n_stages;
         for (int sidx = 0; sidx < n_stage; ++sidx) {
@@ -1008,6 +1042,27 @@ extern "C" int blend_prefill(blend_handle* h, int32_t n_req, const blend_request
                                     (size_t)reqs[r].stage_n[sidx] * 4, cudaMemcpyDeviceToDevice, s);
                 launch_fill_i32(h->set_n[sidx] + r, reqs[r].stage_n[sidx], 1, s);
             }
+        }
+    }
+    const bool focus = reqs[0].focus_bp > 0;
+    static thread_local FocusTable ft;
+    int max_nc = 0;
+    if (focus) {
+        n_stage = 2;
+        stage_layer[1] = reqs[0].focus_layer;
+        ft.n_req = n_req;
+        int ci = 0;
+        for (int r = 0; r < n_req; ++r) {
+            ft.chunk0[r] = ci;
+            ft.n_chunks[r] = reqs[r].n_chunks;
+            int off = 0;
+            for (int j = 0; j < reqs[r].n_chunks; ++j, ++ci) {
+                const int L = pool->entry_len[reqs[r].chunk_ids[j]];
+                ft.start[ci] = info[r].P + off;
+                ft.len[ci] = L;
+                off += L;
+            }
+            max_nc = info[r].n_c > max_nc ? info[r].n_c : max_nc;
         }
     }
     int cur = 0;
@@ -1078,6 +1133,16 @@ extern "C" int blend_prefill(blend_handle* h, int32_t n_req, const blend_request
                 }
                 ProfScope ps(h, PROF_SELECT, s);
                 launch_select(sb, h->rank, max_n, s);
+            } else if (focus) {
+                // the query rows' attention at this layer, per chunk: their q (into the free
+                // attention-output buffer), column means over chunk tokens, then the filter
+                ProfScope ps(h, PROF_SELECT, s);
+                launch_gather_qlast(c.dtype, h->q, h->lim.max_rows, c.n_q_heads / c.n_kv_heads, c.n_kv_heads,
+                                    c.head_dim, bd, h->plan[cur].req_row_end, h->o, qo, s);
+                launch_aux_scores(c.dtype, h->o, kc, bd, c.n_q_heads, c.n_kv_heads, c.head_dim, qo, max_nc,
+                                  h->aux_stats, h->dev[0], s);
+                launch_focus_filter(bd, ft, h->dev[0], reqs[0].focus_bp, h->set[0], h->set_n[0], h->set[1],
+                                    h->set_n[1], s);
             }
             ProfScope ps(h, PROF_PLAN, s);
             StageDesc st{h->set[new_stage], h->set_n[new_stage], 0};

@@ -130,7 +130,78 @@ __global__ void __launch_bounds__(CM_COLS * CM_GROUPS)
     }
 }
 
+// One CTA per request: each chunk's attention mass (its tokens' scores summed in order by
+// one thread), the total (fixed tree), the focused flags, then the ordered compaction of
+// the request's set to the rows of focused chunks.
+constexpr int FF_THREADS = 1024;
+__global__ void __launch_bounds__(FF_THREADS)
+    k_focus_filter(const __grid_constant__ BatchDesc bd, const __grid_constant__ FocusTable ft,
+                   const float* __restrict__ scores, int32_t focus_bp, const int32_t* __restrict__ set_in,
+                   const int32_t* __restrict__ n_in, int32_t* __restrict__ set_out, int32_t* __restrict__ n_out) {
+    __shared__ float mass[BLEND_MAX_CHUNKS];
+    __shared__ uint8_t focused[BLEND_MAX_CHUNKS];
+    __shared__ float red[FF_THREADS];
+    __shared__ int cnt[FF_THREADS];
+    const int r = blockIdx.x;
+    const ReqDesc& rd = bd.r[r];
+    const int c0 = ft.chunk0[r], nch = ft.n_chunks[r];
+    const float* sc = scores + rd.nc_off;
+    for (int j = threadIdx.x; j < nch; j += FF_THREADS) {
+        const int a = ft.start[c0 + j] - rd.P;  // chunk-row index of its first token
+        float m = 0.f;
+        for (int t = 0; t < ft.len[c0 + j]; ++t) m += sc[a + t];
+        mass[j] = m;
+    }
+    __syncthreads();
+    float part = 0.f;
+    for (int j = threadIdx.x; j < nch; j += FF_THREADS) part += mass[j];
+    red[threadIdx.x] = part;
+    __syncthreads();
+    for (int w = FF_THREADS / 2; w > 0; w >>= 1) {
+        if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+        __syncthreads();
+    }
+    const float total = red[0];
+    for (int j = threadIdx.x; j < nch; j += FF_THREADS)
+        focused[j] = (uint8_t)(mass[j] * 10000.f >= (float)focus_bp * total);
+    __syncthreads();
+    const int n = min(max(n_in[r], 0), rd.n_c);
+    const int32_t* in = set_in + rd.nc_off;
+    const int per = (n + FF_THREADS - 1) / FF_THREADS;
+    const int i0 = min(n, (int)threadIdx.x * per), i1 = min(n, i0 + per);
+    auto keep = [&](int p) -> bool {  // chunk of position p by binary search over the starts
+        int lo = 0, hi = nch - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (ft.start[c0 + mid] <= p) lo = mid;
+            else hi = mid - 1;
+        }
+        return nch > 0 && focused[lo];
+    };
+    int loc = 0;
+    for (int i = i0; i < i1; ++i) loc += keep(in[i]);
+    cnt[threadIdx.x] = loc;
+    __syncthreads();
+    for (int w = 1; w < FF_THREADS; w <<= 1) {
+        const int v = threadIdx.x >= w ? cnt[threadIdx.x - w] : 0;
+        __syncthreads();
+        cnt[threadIdx.x] += v;
+        __syncthreads();
+    }
+    int o = cnt[threadIdx.x] - loc;
+    for (int i = i0; i < i1; ++i)
+        if (keep(in[i])) set_out[rd.nc_off + o++] = in[i];
+    if (threadIdx.x == FF_THREADS - 1) n_out[r] = cnt[FF_THREADS - 1];
+}
+
 }  // namespace
+
+void launch_focus_filter(const BatchDesc& bd, const FocusTable& ft, const float* scores, int32_t focus_bp,
+                         const int32_t* set_in, const int32_t* n_in, int32_t* set_out, int32_t* n_out,
+                         cudaStream_t s) {
+    k_focus_filter<<<bd.n_req, FF_THREADS, 0, s>>>(bd, ft, scores, focus_bp, set_in, n_in, set_out, n_out);
+    note_launch(1);
+}
 
 void launch_gather_qlast(int dtype, const void* qslab, int m_cap, int group, int hkv, int d, const BatchDesc& bd,
                          const int32_t* req_row_end, void* q_last, int n_qrows, cudaStream_t s) {

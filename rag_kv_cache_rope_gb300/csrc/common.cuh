@@ -153,6 +153,29 @@ void launch_plan(const BatchDesc& bd, const StageDesc& st, int32_t* row_pos, int
 void launch_set_mask(const BatchDesc& bd, const int32_t* set, const int32_t* count, uint8_t* mask,
                      cudaStream_t s);
 void launch_fill_i32(int32_t* p, int32_t v, long long n, cudaStream_t s);
+// EPIC sets: run q writes positions start[q] .. start[q]+count[q]-1 at set + out[q]; request
+// r's set size is req_n[r].
+struct EpicTable {
+    int32_t n_run;
+    int32_t n_req;
+    int32_t start[BLEND_MAX_CHUNKS];
+    int32_t count[BLEND_MAX_CHUNKS];
+    int32_t out[BLEND_MAX_CHUNKS];
+    int32_t req_n[BLEND_MAX_BATCH];
+};
+void launch_epic_set(const EpicTable& et, int32_t* set, int32_t* set_n, cudaStream_t s);
+// Cache-Craft focus filter: request r's chunks are chunk0[r] .. chunk0[r]+n_chunks[r]-1 of the
+// tables (start = blended position of the chunk's first token, len = its tokens).
+struct FocusTable {
+    int32_t n_req;
+    int32_t chunk0[BLEND_MAX_BATCH];
+    int32_t n_chunks[BLEND_MAX_BATCH];
+    int32_t start[BLEND_MAX_CHUNKS];
+    int32_t len[BLEND_MAX_CHUNKS];
+};
+void launch_focus_filter(const BatchDesc& bd, const FocusTable& ft, const float* scores, int32_t focus_bp,
+                         const int32_t* set_in, const int32_t* n_in, int32_t* set_out, int32_t* n_out,
+                         cudaStream_t s);
 void launch_copy_sets(const BatchDesc& bd, const int32_t* src, const int32_t* src_n, int32_t* dst,
                       int32_t* dst_n, cudaStream_t s);
 

@@ -173,6 +173,21 @@ void launch_assemble(int dtype, const SegTable& segs, const void* pool_k, const 
     note_launch(1);
 }
 
+// EPIC's static selection: the first m tokens of every chunk, written run by run.
+__global__ void k_epic_set(const __grid_constant__ EpicTable et, int32_t* __restrict__ set,
+                           int32_t* __restrict__ set_n) {
+    const int q = blockIdx.x;
+    if (q < et.n_run)
+        for (int t = threadIdx.x; t < et.count[q]; t += blockDim.x) set[et.out[q] + t] = et.start[q] + t;
+    if (q == 0)
+        for (int r = threadIdx.x; r < et.n_req; r += blockDim.x) set_n[r] = et.req_n[r];
+}
+
+void launch_epic_set(const EpicTable& et, int32_t* set, int32_t* set_n, cudaStream_t s) {
+    k_epic_set<<<et.n_run > 0 ? et.n_run : 1, 128, 0, s>>>(et, set, set_n);
+    note_launch(1);
+}
+
 // Token id of every blended token: prefix and chunk rows from the pool, query rows
 // from each request's query tokens.
 __global__ void k_tokens(const __grid_constant__ SegTable segs,

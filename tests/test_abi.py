@@ -62,7 +62,8 @@ int main(void) {
   P(blend_request, chunk_ids) P(blend_request, query_tokens) P(blend_request, scores)
   P(blend_request, n_stages) P(blend_request, stage_layer) P(blend_request, stage_pos) P(blend_request, stage_n)
   P(blend_request, group_rule) P(blend_request, tau_smooth) P(blend_request, tau_cover_bp)
-  P(blend_request, max_span) P(blend_request, cap_bp)
+  P(blend_request, max_span) P(blend_request, cap_bp) P(blend_request, epic_m)
+  P(blend_request, focus_layer) P(blend_request, focus_bp)
   printf("blend_outputs %zu\n", sizeof(blend_outputs));
   P(blend_outputs, dev2) P(blend_outputs, q_last)
   return 0;
