@@ -205,11 +205,47 @@ class Setup:
             n_sel=torch.zeros(b.MAX_BATCH, dtype=torch.int32, device=dev))
         self.req = b.RequestRef(self.req_tok.chunk_ids, self.query, mode=wl.mode, rho_bp=wl.rho_bp,
                                 r1_bp=wl.r1_bp, window=wl.window, tau=wl.tau, budget_mode=wl.budget_mode,
-                                scores=self.scores, group_rule=wl.group_rule)
+                                scores=self.scores, group_rule=wl.group_rule, epic_m=wl.epic_m,
+                                focus_layer=wl.focus_layer, focus_bp=wl.focus_bp)
+        self.aux = None
+        if wl.aux_model is not None:
+            self._setup_aux(pool_tok, lens, dev)
+
+    def _setup_aux(self, pool_tok, lens, dev):
+        """CacheClip's auxiliary step: the small model's own chunk-KV pool (same token ids),
+        one [prefix + chunk + query] request per retrieved chunk with only the query rows
+        computed (FORCED, empty stage), the last-layer q exported for the scorer."""
+        b, wl = self.b, self.wl
+        ash = wl.model if wl.aux_model is None else wl.aux_model
+        aw = synth.model_weights(ash, wl.seed + 100, device=dev)
+        self.aux_packed = b.pack_weights(aw)
+        del aw
+        ak, av, arow = synth.random_pool_kv(ash, wl.prefix_len, lens, wl.seed + 100, device=dev)
+        tok = torch.cat([torch.cat([pool_tok.prefix, c]) for c in pool_tok.chunks]).to(dev)
+        self.aux_pool = b.PoolRef(ak, av, tok, wl.prefix_len, lens, arow)
+        ids = self.req_tok.chunk_ids
+        nreq = len(ids)
+        Q = self.Q
+        n_tok = sum(wl.prefix_len + lens[c] + Q for c in ids)
+        self.aux_h = b.blend_init(b.model_cfg(ash, wl.prefix_len + max(lens) + Q), self.aux_packed,
+                                  b.Limits(nreq * Q, n_tok, max(lens), nreq))
+        empty = torch.zeros(0, dtype=torch.int32, device=dev)
+        self.aux_reqs = [b.RequestRef([c], self.query, mode="forced", stages=[(0, empty)]) for c in ids]
+        dt = synth.torch_dtype(ash)
+        self.aux_out = b.OutputsRef(
+            k=torch.empty(ash.n_layers, n_tok, ash.n_kv_heads, ash.head_dim, dtype=dt, device=dev),
+            v=torch.empty(ash.n_layers, n_tok, ash.n_kv_heads, ash.head_dim, dtype=dt, device=dev),
+            hidden=torch.empty(nreq * Q, ash.hidden, dtype=dt, device=dev),
+            q_last=torch.empty(nreq * Q, ash.n_q_heads, ash.head_dim, dtype=dt, device=dev))
+        self.aux = ash
 
     def step(self, req=None):
         b = self.b
-        b.importance_scores(self.hidden_states, self.n_c, self.wl.score_layers, self.wl.score_dim, self.scores)
+        if self.aux is not None:
+            b.blend_prefill(self.aux_h, self.aux_reqs, self.aux_pool, self.aux_out)
+            b.aux_attention_scores(self.aux_h, self.aux_reqs, self.aux_pool, self.aux_out, self.scores)
+        else:
+            b.importance_scores(self.hidden_states, self.n_c, self.wl.score_layers, self.wl.score_dim, self.scores)
         b.blend_prefill(self.h, [req or self.req], self.pool, self.out)
 
     def rows_and_pairs(self):
@@ -222,7 +258,8 @@ class Setup:
 
 
 def algorithmic(sh: synth.ModelShape, rows: int, pairs: int, wl: synth.Workload) -> dict:
-    """Algorithmic work per launch of each stage (one launch = one layer)."""
+    """Algorithmic work of one launch of each stage (one launch = one layer) at `rows`
+    recomputed rows whose causal pairs sum to `pairs`."""
     H, d, F = sh.hidden, sh.head_dim, sh.ffn
     qd, kvd = sh.n_q_heads * d, sh.n_kv_heads * d
     es = 2 if sh.dtype == "bf16" else 4
@@ -237,6 +274,30 @@ def algorithmic(sh: synth.ModelShape, rows: int, pairs: int, wl: synth.Workload)
     }
 
 
+def step_work(wl: synth.Workload, rows0: int, pairs0: int, rows1: int, pairs1: int, aux_rp=None) -> dict:
+    """{stage: (bound, algorithmic units per step, launches per step)} for one step.  Layers
+    before the focus layer run the first set (rows0, pairs0), later ones the filtered set; the
+    focus layer projects K/V for the first set and runs attention and MLP on the second.
+    aux_rp = (rows, pairs) of the auxiliary model's layers, counted under aux_* names."""
+    sh = wl.model
+    L = sh.n_layers
+    fl = wl.focus_layer if wl.focus_bp else L
+    w0, w1 = algorithmic(sh, rows0, pairs0, wl), algorithmic(sh, rows1, pairs1, wl)
+    out = {}
+    for k in w0:
+        if k == "assemble":
+            out[k] = (w0[k][0], w0[k][1], 1)
+            continue
+        n0 = min(L, fl + 1) if k == "gemm_qkv" else min(L, fl)
+        out[k] = (w0[k][0], n0 * w0[k][1] + (L - n0) * w1[k][1], L)
+    if aux_rp is not None:
+        ash = wl.aux_model
+        wa = algorithmic(ash, aux_rp[0], aux_rp[1], wl)
+        for k in ("gemm_qkv", "gemm_o", "gemm_gate_up", "gemm_down", "attention"):
+            out["aux_" + k] = (wa[k][0], ash.n_layers * wa[k][1], ash.n_layers)
+    return out
+
+
 def run_ours(args, wl, rank, world):
     from rag_kv_cache_rope_gb300 import build as B
     B.build()
@@ -249,12 +310,34 @@ def run_ours(args, wl, rank, world):
         S.step()
     torch.cuda.synchronize()
     rows, pairs = S.rows_and_pairs()
+    rows0, pairs0 = rows, pairs
+    if wl.focus_bp:
+        # the set before the focus filter: the same request without it
+        nofocus = dataclasses.replace(wl, focus_bp=0)
+        S.req = b.RequestRef(S.req_tok.chunk_ids, S.query, mode=wl.mode, rho_bp=wl.rho_bp, r1_bp=wl.r1_bp,
+                             window=wl.window, tau=wl.tau, budget_mode=wl.budget_mode, scores=S.scores,
+                             group_rule=wl.group_rule, epic_m=wl.epic_m)
+        S.step()
+        torch.cuda.synchronize()
+        rows0, pairs0 = S.rows_and_pairs()
+        S.req = b.RequestRef(S.req_tok.chunk_ids, S.query, mode=wl.mode, rho_bp=wl.rho_bp, r1_bp=wl.r1_bp,
+                             window=wl.window, tau=wl.tau, budget_mode=wl.budget_mode, scores=S.scores,
+                             group_rule=wl.group_rule, epic_m=wl.epic_m, focus_layer=wl.focus_layer,
+                             focus_bp=wl.focus_bp)
+        del nofocus
+    aux_rp = None
+    if S.aux is not None:
+        nq = len(S.req_tok.chunk_ids) * S.Q
+        ctx = sum(wl.prefix_len + wl.chunk_len for _ in S.req_tok.chunk_ids)
+        aux_rp = (nq, S.Q * ctx + len(S.req_tok.chunk_ids) * S.Q * (S.Q + 1) // 2)
     # timed region: K steps between barriers, per-stage events recorded live
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     l0 = b.blend_launch_count()
     b.blend_profile(S.h, True)
+    if S.aux is not None:
+        b.blend_profile(S.aux_h, True)
     stream = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(dev.index) as clk:
@@ -267,6 +350,10 @@ def run_ours(args, wl, rank, world):
     launches = b.blend_launch_count() - l0
     prof = b.blend_profile_read(S.h)
     b.blend_profile(S.h, False)
+    if S.aux is not None:
+        for k, v in b.blend_profile_read(S.aux_h).items():
+            prof["aux_" + k] = v
+        b.blend_profile(S.aux_h, False)
     if world > 1:
         t = torch.tensor([ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -275,14 +362,15 @@ def run_ours(args, wl, rank, world):
     value = world * S.N / (ms / 1e3)
 
     # roofline of the stage with the largest share of device time
-    work = algorithmic(sh, rows, pairs, wl)
+    work = step_work(wl, rows0, pairs0, rows, pairs, aux_rp)
     shares = {k: v[0] for k, v in prof.items()}
     total = sum(shares.values()) or 1.0
     dom = max(shares, key=shares.get)
     roof = None
     if dom in work:
-        kind, units = work[dom]
-        n_launch = args.steps * (sh.n_layers if dom != "assemble" else 1)
+        kind, step_units, per_step = work[dom]
+        units = step_units / per_step  # average work of one launch
+        n_launch = args.steps * per_step
         avg_ms = prof[dom][0] / n_launch
         if kind == "tensor":
             peak = PEAKS["bf16_tflops_sustained"] if sh.dtype == "bf16" else None
@@ -299,7 +387,7 @@ def run_ours(args, wl, rank, world):
               for k, v in prof.items() if v[1]}
     # whole-step roofline: ideal time of every GEMM/attention at the tensor peak plus the
     # assembly at the HBM peak, over the measured step
-    tflop = sum(w[1] for k, w in work.items() if w[0] == "tensor") * sh.n_layers
+    tflop = sum(w[1] for k, w in work.items() if w[0] == "tensor")
     ideal_ms = tflop / (PEAKS["bf16_tflops_sustained"] * 1e12) * 1e3 + \
         work["assemble"][1] / (PEAKS["hbm_gbs"] * 1e9) * 1e3
     line = {
@@ -311,8 +399,11 @@ def run_ours(args, wl, rank, world):
         "config": {"workload": wl.name, "model_shape": sh.name, "n_ctx": S.N, "prefix": wl.prefix_len,
                    "chunks": f"{wl.n_chunks}x{wl.chunk_len}", "query": wl.query_len, "mode": wl.mode,
                    "rho_bp": wl.rho_bp, "window": wl.window, "tau": wl.tau, "budget": wl.budget_mode,
-                   "group_rule": wl.group_rule, "pool": args.pool,
-                   "rows_per_layer": rows, "layers": sh.n_layers, "parallelism": f"replicas x{world}",
+                   "group_rule": wl.group_rule, "pool": args.pool, "epic_m": wl.epic_m,
+                   "focus": [wl.focus_layer, wl.focus_bp] if wl.focus_bp else None,
+                   "aux_model": wl.aux_model.name if wl.aux_model else None,
+                   "rows_per_layer": rows, "rows_before_focus": rows0 if wl.focus_bp else None,
+                   "layers": sh.n_layers, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (weights %.1f GB, chunk pool %.1f GB)" % (
                        sum(t.numel() * t.element_size() for t in S.packed.values()) / 1e9,
                        2 * S.pool_k.numel() * S.pool_k.element_size() / 1e9)},
@@ -392,14 +483,16 @@ def e2e(S: Setup, args, world):
     """Same step through the C ABI with host inputs: pinned H2D of query tokens and the
     small model's hidden states, D2H of the first-token hidden state, every step."""
     b = S.b
-    hs_host = S.hidden_states.cpu().pin_memory()
+    aux = S.aux is not None  # the auxiliary model scores on the GPU: no hidden states come in
+    hs_host = None if aux else S.hidden_states.cpu().pin_memory()
     q_host = S.query.cpu().pin_memory()
     out_host = torch.empty_like(S.out["hidden"], device="cpu").pin_memory()
-    h2d = hs_host.numel() * hs_host.element_size() + q_host.numel() * q_host.element_size()
+    h2d = (0 if aux else hs_host.numel() * hs_host.element_size()) + q_host.numel() * q_host.element_size()
     d2h = out_host.numel() * out_host.element_size()
 
     def one():
-        S.hidden_states.copy_(hs_host, non_blocking=True)
+        if not aux:
+            S.hidden_states.copy_(hs_host, non_blocking=True)
         S.query.copy_(q_host, non_blocking=True)
         S.step()
         out_host.copy_(S.out["hidden"], non_blocking=True)
@@ -452,6 +545,17 @@ class OracleSample:
         self.tokens = np.concatenate([reqs[0].prefix.numpy()] + [pool_tok.chunks[c].numpy() for c in self.ids]
                                      + [reqs[0].query.numpy()])
         self.per_row, self.fixed_s, self.n_rows = 1.0, 0.0, 1
+        self.aux = None
+        if wl.aux_model is not None:
+            ash = wl.aux_model
+            self.aux_cfg = dict(n_layers=ash.n_layers, hidden=ash.hidden, n_q_heads=ash.n_q_heads,
+                                n_kv_heads=ash.n_kv_heads, head_dim=ash.head_dim, ffn=ash.ffn, vocab=ash.vocab,
+                                rope_theta=ash.rope_theta, rms_eps=ash.rms_eps)
+            aw = synth.model_weights(ash, wl.seed + 100, device="cpu")
+            self.aux_w = {k: v.double().numpy() for k, v in aw.items()}
+            del aw
+            ak, av, _ = synth.random_pool_kv(ash, wl.prefix_len, [wl.chunk_len], wl.seed + 100)
+            self.aux = (ak.double().numpy(), av.double().numpy())
 
     def run(self, n_pick: int):
         """One sample with a recompute subset of n_pick rows."""
@@ -463,12 +567,23 @@ class OracleSample:
         K, V = O.assemble(self.ek, self.ev, self.ids, P, [self.lens[c] for c in self.ids], Q, sh.rope_theta)
         t_asm = time.perf_counter() - t0
         t0 = time.perf_counter()
+        t_aux = 0.0
+        if self.aux is not None:
+            # one chunk's auxiliary scoring, scaled by the chunks; the scores themselves come
+            # from the hidden-state stand-in (the selection's cost does not depend on them)
+            ta = time.perf_counter()
+            qa, Ka = O.aux_query_forward(self.aux_w, self.aux_cfg, self.aux[0], self.aux[1], P,
+                                         self.tokens[-Q:] % wl.aux_model.vocab)
+            O.column_mean_scores(qa, np.arange(P + wl.chunk_len, P + wl.chunk_len + Q), Ka, P, P + wl.chunk_len)
+            t_aux = (time.perf_counter() - ta) * wl.n_chunks
         s = O.importance_scores(self.hs).astype(np.float32).astype(np.float64)
-        if wl.group_rule == "span":
+        if wl.mode == "epic":
+            sel = O.epic_positions(P, [wl.chunk_len] * wl.n_chunks, wl.epic_m)
+        elif wl.group_rule == "span":
             sel = O.span_select_final_bisect(s, O.ceil_bp(wl.rho_bp, n_c), 0.4, 7000, 16, base=P)
         else:
             sel = O.select_final_bisect(s, O.ceil_bp(wl.rho_bp, n_c), wl.window, wl.tau, base=P)
-        t_sel = time.perf_counter() - t0
+        t_sel = time.perf_counter() - t0 + t_aux - (t_aux / wl.n_chunks if self.aux is not None else 0.0)
         rows = np.concatenate([sel, np.arange(P + n_c, N)])
         pick = rows[np.linspace(0, len(rows) - 1, max(1, min(n_pick, len(rows)))).astype(int)]
         x = self.w["embed"][self.tokens[pick]]
@@ -488,6 +603,10 @@ class OracleSample:
         sample = (f"1 of {sh.n_layers} layers assembled (x{sh.n_layers}), full selection, one layer's recompute "
                   f"of {len(pick)} of {len(rows)} rows spread over the context, scaled to {row_layers} "
                   f"row-layers; numpy fp64")
+        if self.aux is not None:
+            sample += f"; auxiliary scoring of 1 of {wl.n_chunks} chunks (x{wl.n_chunks})"
+        if wl.focus_bp:
+            sample += "; the focus filter is not modelled (every layer at the first set)"
         return {"est_step_s": est, "sample_s": t_asm + t_sel + t_layer, "N": N, "sample": sample}
 
     def rows_for(self, target_s: float) -> int:

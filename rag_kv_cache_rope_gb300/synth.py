@@ -54,6 +54,8 @@ TINY4 = dataclasses.replace(TINY, name="tiny-4L", n_layers=4)
 LLAMA8B = ModelShape("llama3-8b-shape", 32, 4096, 32, 8, 128, 14336, 128256, 5e5)
 MISTRAL7B = ModelShape("mistral-7b-shape", 32, 4096, 32, 8, 128, 14336, 32000, 1e6)
 QWEN14B = ModelShape("qwen2.5-14b-shape", 48, 5120, 40, 8, 128, 13824, 152064, 1e6)
+# CacheClip's auxiliary model (SmolLM2-135M widths: 30 layers, H 576, 9/3 heads of 64)
+SMOL135M = ModelShape("smollm2-135m-shape", 30, 576, 9, 3, 64, 1536, 49152, 1e5)
 
 
 @dataclasses.dataclass(frozen=True)
@@ -79,6 +81,10 @@ class Workload:
     score_dim: int = 2048
     score_phrase_max: int = 0    # >0: hidden-state scales shared within runs of 1..this many tokens
     group_rule: str = "window"   # "window" (CacheClip grouping) | "span" (SpecCache span completion)
+    epic_m: int = 0              # mode "epic": tokens recomputed at the start of every chunk
+    focus_layer: int = 0         # focus_bp > 0: Cache-Craft early termination at this layer
+    focus_bp: int = 0
+    aux_model: Optional["ModelShape"] = None  # CacheClip: scores from this auxiliary model
 
     @property
     def n_ctx(self) -> int:
@@ -110,6 +116,17 @@ WORKLOADS = {
     # spans <= 16) over scores with phrase structure (runs of 1..8 tokens of similar scale)
     "qwen14b-16k-span20": Workload("qwen14b-16k-span20", QWEN14B, 64, 512, 31, 128, "ext", 2000, 0, 1, 1, seed=4,
                                    score_phrase_max=8, group_rule="span"),
+    # the same context with EPIC's static rule: the first 103 tokens (~20 %) of every chunk
+    "qwen14b-16k-epic20": Workload("qwen14b-16k-epic20", QWEN14B, 64, 512, 31, 128, "epic", 2000, seed=4,
+                                   epic_m=103),
+    # the main request plus Cache-Craft early termination: at layer 16 chunks under a 3 %
+    # share of the question attention stop being recomputed
+    "qwen14b-16k-ext20-focus": Workload("qwen14b-16k-ext20-focus", QWEN14B, 64, 512, 31, 128, "ext", 2000, 0, 4, 1,
+                                        seed=4, focus_layer=16, focus_bp=300),
+    # CacheClip end to end: scores from the auxiliary model's last-layer attention (one
+    # [prefix + chunk + query] sequence per chunk), window 8, density 5, final budget 20 %
+    "qwen14b-16k-aux20": Workload("qwen14b-16k-aux20", QWEN14B, 64, 512, 31, 128, "ext", 2000, 0, 8, 5, seed=4,
+                                  aux_model=SMOL135M),
 }
 
 
