@@ -48,16 +48,16 @@ except OSError:
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
 # capture of each kernel (profiles/), valid only while the kernel's source is unchanged.
 TRAFFIC = {
-    "gemm_qkv": {"bytes": 116.266240e6 + 30.864896e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
-                 "sha256_16": "f2027e01e0765111", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
-    "gemm_o": {"bytes": 162.874624e6 + 42.884096e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
-               "sha256_16": "f2027e01e0765111", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
-    "gemm_gate_up": {"bytes": 323.675904e6 + 86.671872e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
-                     "sha256_16": "f2027e01e0765111", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
-    "gemm_down": {"bytes": 591.546624e6 + 62.978816e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
-                  "sha256_16": "f2027e01e0765111", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
-    "attention": {"bytes": 132.513792e6 + 13.233664e6, "source": "rag_kv_cache_rope_gb300/csrc/attn_tc.cu",
-                  "sha256_16": "7d325c2c8d0b527d", "profile": "profiles/attn_tc_qwen14b_16k_layer.md"},
+    "gemm_qkv": {"bytes": 116.457216e6 + 31.288320e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
+                 "sha256_16": "c92029abd008d826", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
+    "gemm_o": {"bytes": 163.003904e6 + 42.863360e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
+               "sha256_16": "c92029abd008d826", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
+    "gemm_gate_up": {"bytes": 322.974464e6 + 86.359552e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
+                     "sha256_16": "c92029abd008d826", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
+    "gemm_down": {"bytes": 591.620608e6 + 62.934784e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
+                  "sha256_16": "c92029abd008d826", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
+    "attention": {"bytes": 132.046848e6 + 13.367808e6, "source": "rag_kv_cache_rope_gb300/csrc/attn_tc.cu",
+                  "sha256_16": "95b92778a50a28c1", "profile": "profiles/attn_tc_qwen14b_16k_layer.md"},
 }
 
 
