@@ -85,6 +85,9 @@ struct blend_handle {
     float* dev[2];
     int32_t* scratch_n;
     float2* aux_stats;   // aux_attention_scores: softmax (max, sum) per query row and head
+    float* ssq;          // folded RMSNorm: per-row partial sums of squares [rows][ssq_parts]
+    bool xn_scaled = false;  // xn holds bf16(x * g) of the next layer's attention norm, ssq its partials
+    int ssq_parts = 0;
     // host-memory pool: per-layer copies into two staging buffers on a side stream (copy
     // engines), one event per layer, one per staging buffer
     void* stage[4];  // K0, V0, K1, V1
@@ -260,6 +263,7 @@ Layout make_layout(const blend_model_cfg* c, const blend_limits* l) {
     L.add(M * (size_t)c->n_q_heads * sizeof(float2));      // 36 aux score row statistics
     for (int b = 0; b < 4; ++b)                            // 37..40 host-pool staging: K, V x 2 buffers
         L.add((size_t)l->max_tokens * kvd * es);
+    L.add(M * 64 * sizeof(float));                         // 41 folded-RMSNorm partial sums of squares
     return L;
 }
 
@@ -285,11 +289,16 @@ LayerW layer_w(const blend_handle* h, int l) {
 }
 
 // C[M, N] (epi) A[M, K] . B[N, K]^T: tensor cores for bf16, CUDA cores for fp32.
+bool gemm_on_tc(const blend_handle* h, int K, int N, int epi, int ldc) {
+    return h->cfg.dtype == BLEND_BF16 && h->use_tc && tc_gemm_supported(K, N, epi, ldc, h->lim.max_rows);
+}
+
+// ne: folded-RMSNorm sides (tensor-core path only; callers pass it only when gemm_on_tc).
 void gemm(blend_handle* h, const void* A, int K, const void* B, int N, int epi, void* C, int ldc,
-          const int32_t* M_dev, int M_max, cudaStream_t s) {
-    if (h->cfg.dtype == BLEND_BF16 && h->use_tc && tc_gemm_supported(K, N, epi, ldc, h->lim.max_rows)) {
+          const int32_t* M_dev, int M_max, cudaStream_t s, const NormEpi* ne = nullptr) {
+    if (gemm_on_tc(h, K, N, epi, ldc)) {
         int rc = launch_gemm_tc(A, K, h->lim.max_rows, B, N, M_dev, M_max, epi, C, ldc, h->err, s, nullptr,
-                                h->split_ws, h->split_cnt);
+                                h->split_ws, h->split_cnt, ne);
         if (rc != BLEND_OK && h->host_rc == BLEND_OK) h->host_rc = rc;
     } else
         launch_gemm_simt(h->cfg.dtype, A, K, B, K, K, N, M_dev, M_max, epi, C, ldc, s);
@@ -310,16 +319,59 @@ void attention(blend_handle* h, const Plan& p, int n_req, int M_max, const void*
 
 // The part of a layer after the K/V write: attention, O-proj + residual, RMSNorm,
 // SwiGLU MLP + residual, on the rows of plan p (x holds those rows).
+// Producer and consumer sides of the folded RMSNorm (RMSNorm(x) . W = (1/rms(x)) ((x * g) . W)):
+// the residual-add GEMM writes bf16(x * g) and per-tile sums of squares, the next GEMM
+// scales its rows.
+NormEpi norm_producer(blend_handle* h, const void* g, int M_max) {
+    const int H = h->cfg.hidden;
+    NormEpi ne{};
+    ne.x_out = (bf16*)h->xn;
+    ne.g = (const bf16*)g;
+    ne.ssq_out = h->ssq;
+    ne.ssq_stride = gemm_tc_ntiles(M_max, H);
+    ne.ldx = H;
+    return ne;
+}
+NormEpi norm_consumer(blend_handle* h, int parts) {
+    NormEpi ne{};
+    ne.ssq_in = h->ssq;
+    ne.n_part = parts;
+    ne.inv_h = 1.f / (float)h->cfg.hidden;
+    ne.eps = h->cfg.rms_eps;
+    return ne;
+}
+
+// The rest of a layer.  next_follows: the next layer's QKV projection runs right after on
+// the same rows, so the down projection may hand it normalised input.
 void layer_rest(blend_handle* h, int l, float* x, const Plan& p, int n_req, int M_max, const void* kc,
-                const void* vc, long long n_tokens, cudaStream_t s) {
+                const void* vc, long long n_tokens, cudaStream_t s, bool next_follows) {
     const blend_model_cfg& c = h->cfg;
     const LayerW lw = layer_w(h, l);
     const int H = c.hidden, qd = c.n_q_heads * c.head_dim, F = c.ffn;
+    const int width = (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
     { ProfScope ps(h, PROF_ATTN, s); attention(h, p, n_req, M_max, kc, vc, n_tokens, s); }
-    { ProfScope ps(h, PROF_GEMM_O, s); gemm(h, h->o, qd, lw.w_o, H, EPI_ADD_F32, x, H, p.M, M_max, s); }
-    { ProfScope ps(h, PROF_NORM, s); launch_rmsnorm(c.dtype, x, lw.mlp_norm, h->xn, H, c.rms_eps, p.M, M_max, s); }
-    { ProfScope ps(h, PROF_GEMM_GU, s); gemm(h, h->xn, H, lw.w_gu, 2 * F, EPI_SWIGLU, h->hmlp, F, p.M, M_max, s); }
-    { ProfScope ps(h, PROF_GEMM_DOWN, s); gemm(h, h->hmlp, F, lw.w_down, H, EPI_ADD_F32, x, H, p.M, M_max, s); }
+    const bool fold_mlp = gemm_on_tc(h, qd, H, EPI_ADD_F32, H) && gemm_on_tc(h, H, 2 * F, EPI_SWIGLU, F) &&
+                          H <= 64 * 128;
+    if (fold_mlp) {
+        const NormEpi prod = norm_producer(h, lw.mlp_norm, M_max);
+        { ProfScope ps(h, PROF_GEMM_O, s); gemm(h, h->o, qd, lw.w_o, H, EPI_ADD_F32, x, H, p.M, M_max, s, &prod); }
+        const NormEpi cons = norm_consumer(h, prod.ssq_stride);
+        { ProfScope ps(h, PROF_GEMM_GU, s); gemm(h, h->xn, H, lw.w_gu, 2 * F, EPI_SWIGLU, h->hmlp, F, p.M, M_max, s, &cons); }
+    } else {
+        { ProfScope ps(h, PROF_GEMM_O, s); gemm(h, h->o, qd, lw.w_o, H, EPI_ADD_F32, x, H, p.M, M_max, s); }
+        { ProfScope ps(h, PROF_NORM, s); launch_rmsnorm(c.dtype, x, lw.mlp_norm, h->xn, H, c.rms_eps, p.M, M_max, s); }
+        { ProfScope ps(h, PROF_GEMM_GU, s); gemm(h, h->xn, H, lw.w_gu, 2 * F, EPI_SWIGLU, h->hmlp, F, p.M, M_max, s); }
+    }
+    const bool fold_next = next_follows && l + 1 < c.n_layers && gemm_on_tc(h, F, H, EPI_ADD_F32, H) &&
+                           gemm_on_tc(h, H, width, EPI_STORE_F32, width) && H <= 64 * 128;
+    if (fold_next) {
+        const NormEpi prod = norm_producer(h, layer_w(h, l + 1).attn_norm, M_max);
+        { ProfScope ps(h, PROF_GEMM_DOWN, s); gemm(h, h->hmlp, F, lw.w_down, H, EPI_ADD_F32, x, H, p.M, M_max, s, &prod); }
+        h->xn_scaled = true;
+        h->ssq_parts = prod.ssq_stride;
+    } else {
+        { ProfScope ps(h, PROF_GEMM_DOWN, s); gemm(h, h->hmlp, F, lw.w_down, H, EPI_ADD_F32, x, H, p.M, M_max, s); }
+    }
 }
 
 // The part of a layer up to the K/V write: RMSNorm, QKV projection, RoPE, optional
@@ -331,7 +383,17 @@ void layer_kv(blend_handle* h, int l, const float* x, const Plan& p, const int32
     const LayerW lw = layer_w(h, l);
     const int H = c.hidden, d = c.head_dim;
     const int width = (c.n_q_heads + 2 * c.n_kv_heads) * d;
-    { ProfScope ps(h, PROF_NORM, s); launch_rmsnorm(c.dtype, x, lw.attn_norm, h->xn, H, c.rms_eps, p.M, M_max, s); }
+    // xn already holds bf16(x * g) from the previous down projection (folded RMSNorm), or
+    // the norm runs here
+    const bool folded = h->xn_scaled && gemm_on_tc(h, H, width, EPI_STORE_F32, width);
+    h->xn_scaled = false;
+    NormEpi cons{};
+    if (folded)
+        cons = norm_consumer(h, h->ssq_parts);
+    else {
+        ProfScope ps(h, PROF_NORM, s);
+        launch_rmsnorm(c.dtype, x, lw.attn_norm, h->xn, H, c.rms_eps, p.M, M_max, s);
+    }
     const bool fused = dev == nullptr && c.dtype == BLEND_BF16 && h->use_tc && d == 128 && width % 256 == 0 &&
                        tc_gemm_supported(H, width, EPI_QKV_ROPE, width, h->lim.max_rows);
     if (fused) {
@@ -340,11 +402,14 @@ void layer_kv(blend_handle* h, int l, const float* x, const Plan& p, const int32
         QkvEpi qe{p.row_pos, p.row_tok, h->rope, (bf16*)h->q, (bf16*)kc, (bf16*)vc, h->lim.max_rows,
                   c.n_q_heads / c.n_kv_heads, c.n_q_heads, c.n_kv_heads};
         int rc = launch_gemm_tc(h->xn, H, h->lim.max_rows, lw.w_qkv, width, p.M, M_max, EPI_QKV_ROPE, nullptr, 0,
-                                h->err, s, &qe);
+                                h->err, s, &qe, nullptr, nullptr, &cons);
         if (rc != BLEND_OK && h->host_rc == BLEND_OK) h->host_rc = rc;
         return;
     }
-    { ProfScope ps(h, PROF_GEMM_QKV, s); gemm(h, h->xn, H, lw.w_qkv, width, EPI_STORE_F32, h->qkv, width, p.M, M_max, s); }
+    {
+        ProfScope ps(h, PROF_GEMM_QKV, s);
+        gemm(h, h->xn, H, lw.w_qkv, width, EPI_STORE_F32, h->qkv, width, p.M, M_max, s, folded ? &cons : nullptr);
+    }
     ProfScope ps(h, PROF_ROPE_KV, s);
     launch_rope_qkv(c.dtype, h->qkv, p.row_pos, p.row_tok, row_req, p.M, M_max, bd, c.n_q_heads,
                     c.n_kv_heads, d, h->lim.max_rows, h->rope, h->q, kc, vc, dev, dev_mode, dev_by_row, s);
@@ -418,6 +483,7 @@ int blend_init(const blend_model_cfg* cfg, const blend_weights* w, const blend_l
     h->split_cnt = (int32_t*)(b + L.off[i++]);
     h->aux_stats = (float2*)(b + L.off[i++]);
     for (int q = 0; q < 4; ++q) h->stage[q] = b + L.off[i++];
+    h->ssq = (float*)(b + L.off[i++]);
     h->use_tc = cfg->dtype == BLEND_BF16 ? tc_available() : 0;
     cudaStream_t s = (cudaStream_t)stream;
     cudaMemsetAsync(h->err, 0, 16, s);
@@ -667,8 +733,9 @@ int selective_layer(blend_handle* h, int32_t layer, float* x, const int32_t* pos
     Plan& p = h->plan[0];
     launch_plan(bd, st, p.row_pos, p.row_tok, p.row_req, h->row_src, h->pos2row, p.M, p.req_row_end,
                 nullptr, nullptr, h->err, s);
+    h->xn_scaled = false;
     layer_kv(h, layer, x, p, p.row_req, n, bd, k_cache, v_cache, dev_out, dev_mode, 1, s);
-    layer_rest(h, layer, x, p, 1, n, k_cache, v_cache, n_ctx, s);
+    layer_rest(h, layer, x, p, 1, n, k_cache, v_cache, n_ctx, s, false);
     return finish(h, "selective_layer");
 }
 
@@ -1080,6 +1147,7 @@ extern "C" int blend_prefill(blend_handle* h, int32_t n_req, const blend_request
         cudaMemsetAsync(h->dev[1], 0, (size_t)nc_total * 4, s);
     }
     // ---- 3. layers
+    h->xn_scaled = false;
     float* x = h->x;
     float* x_alt = h->x2;
     for (int l = 0; l < c.n_layers; ++l) {
@@ -1169,7 +1237,7 @@ extern "C" int blend_prefill(blend_handle* h, int32_t n_req, const blend_request
         if (l == c.n_layers - 1 && out->q_last)
             launch_gather_qlast(c.dtype, h->q, h->lim.max_rows, c.n_q_heads / c.n_kv_heads, c.n_kv_heads,
                                 c.head_dim, bd, h->plan[cur].req_row_end, out->q_last, qo, s);
-        layer_rest(h, l, x, h->plan[cur], n_req, M_max, kc, vc, tok, s);
+        layer_rest(h, l, x, h->plan[cur], n_req, M_max, kc, vc, tok, s, true);
     }
     // ---- 4. final norm of the query rows
     ProfScope ps_final(h, PROF_FINAL, s);

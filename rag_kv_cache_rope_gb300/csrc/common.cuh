@@ -232,6 +232,23 @@ struct QkvEpi {
 //   EPI_STORE_F32: C fp32 [M][ldc] = acc
 //   EPI_ADD_F32:   C fp32 [M][ldc] += acc
 //   EPI_SWIGLU:    C dtype [M][N/2]: gate/up interleaved in blocks of BLEND_GU_BLOCK
+// RMSNorm folded into the tensor-core GEMMs: RMSNorm(x) . W = (1 / rms(x)) ((x * g) . W).
+// Producer side (a residual-add GEMM, x_out set): besides the fp32 rows it writes
+// bf16(x * g) to x_out [rows][ldx] (g: the next norm's gain, per column) and each row's sum
+// of squares over the tile's columns to ssq_out[row * ssq_stride + n_tile].  Consumer side
+// (ssq_in set): every accumulator of a row is scaled by 1 / sqrt(sum of its n_part partials
+// * inv_h + eps) before the epilogue.
+struct NormEpi {
+    const float* ssq_in;
+    int n_part;
+    float inv_h, eps;
+    bf16* x_out;
+    const bf16* g;
+    float* ssq_out;
+    int ssq_stride;
+    int ldx;
+};
+
 void launch_gemm_simt(int dtype, const void* A, int lda, const void* B, int ldb, int K, int N,
                       const int32_t* M_dev, int M_max, int epi, void* C, int ldc, cudaStream_t s);
 

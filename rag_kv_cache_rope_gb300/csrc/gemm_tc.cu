@@ -173,32 +173,67 @@ __device__ __forceinline__ void tc_fence_after() {
           "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])            \
         : "r"(taddr))
 
+// Row scale of the consumer side of NormEpi (1 when the GEMM reads normalised rows).
+__device__ __forceinline__ float row_scale(const NormEpi& ne, int row) {
+    if (ne.ssq_in == nullptr) return 1.f;
+    float t = 0.f;
+    for (int q = 0; q < ne.n_part; ++q) t += ne.ssq_in[(long long)row * ne.n_part + q];
+    return 1.f / sqrtf(t * ne.inv_h + ne.eps);
+}
+
 // Epilogue of 32 accumulator columns of one row (fp32 store, fp32 residual add, or
-// SwiGLU of 16 gate + 16 up columns to 16 bf16 outputs).
+// SwiGLU of 16 gate + 16 up columns to 16 bf16 outputs), after the row scale rs.  A
+// residual add with ne.x_out also writes bf16(x * g) and adds the squares of the new row
+// values to ssq (in column order).
 template <int EPI>
-__device__ __forceinline__ void epi_chunk(const uint32_t* r, int row, int col, void* Cv, int ldc) {
+__device__ __forceinline__ void epi_chunk(const uint32_t* r, int row, int col, void* Cv, int ldc, float rs,
+                                          const NormEpi& ne, float& ssq) {
     if (EPI == EPI_STORE_F32 || EPI == EPI_ADD_F32) {
         float4* p = reinterpret_cast<float4*>((float*)Cv + (long long)row * ldc + col);
+        float o[32];
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
-            float4 o = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]), __uint_as_float(r[4 * v + 2]),
-                                   __uint_as_float(r[4 * v + 3]));
+            float4 w = make_float4(__uint_as_float(r[4 * v]) * rs, __uint_as_float(r[4 * v + 1]) * rs,
+                                   __uint_as_float(r[4 * v + 2]) * rs, __uint_as_float(r[4 * v + 3]) * rs);
             if (EPI == EPI_ADD_F32) {
                 const float4 x = p[v];
-                o.x += x.x;
-                o.y += x.y;
-                o.z += x.z;
-                o.w += x.w;
+                w.x += x.x;
+                w.y += x.y;
+                w.z += x.z;
+                w.w += x.w;
             }
-            p[v] = o;
+            p[v] = w;
+            o[4 * v] = w.x;
+            o[4 * v + 1] = w.y;
+            o[4 * v + 2] = w.z;
+            o[4 * v + 3] = w.w;
+        }
+        if (EPI == EPI_ADD_F32 && ne.x_out != nullptr) {
+            const uint4* gp = reinterpret_cast<const uint4*>(ne.g + col);
+            uint4* xp = reinterpret_cast<uint4*>(ne.x_out + (long long)row * ne.ldx + col);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                const uint4 gv = gp[v];
+                const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+                uint32_t xw[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float a = o[8 * v + 2 * e], b = o[8 * v + 2 * e + 1];
+                    ssq = fmaf(a, a, ssq);
+                    ssq = fmaf(b, b, ssq);
+                    const float ga = __uint_as_float(gw[e] << 16), gb = __uint_as_float(gw[e] & 0xffff0000u);
+                    xw[e] = pack_bf16x2(a * ga, b * gb);
+                }
+                xp[v] = make_uint4(xw[0], xw[1], xw[2], xw[3]);
+            }
         }
     } else {
         // 32 columns = 16 gate + 16 up of the same hidden units
         uint32_t w8[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const float g0 = __uint_as_float(r[2 * i]), u0 = __uint_as_float(r[16 + 2 * i]);
-            const float g1 = __uint_as_float(r[2 * i + 1]), u1 = __uint_as_float(r[17 + 2 * i]);
+            const float g0 = __uint_as_float(r[2 * i]) * rs, u0 = __uint_as_float(r[16 + 2 * i]) * rs;
+            const float g1 = __uint_as_float(r[2 * i + 1]) * rs, u1 = __uint_as_float(r[17 + 2 * i]) * rs;
             w8[i] = pack_bf16x2(g0 / (1.f + expf(-g0)) * u0, g1 / (1.f + expf(-g1)) * u1);
         }
         uint4* p = reinterpret_cast<uint4*>((bf16*)Cv + (long long)row * ldc + col / 2);
@@ -212,7 +247,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB, int K,
               int N, const int32_t* __restrict__ M_dev, void* __restrict__ Cv, int ldc,
               int32_t* __restrict__ err, const __grid_constant__ QkvEpi qe, float* __restrict__ split_ws,
-              int32_t* __restrict__ split_cnt) {
+              int32_t* __restrict__ split_cnt, const __grid_constant__ NormEpi ne) {
     using TC = TileCfg<BN>;
     constexpr int STAGES = TC::STAGES;
     constexpr int STAGE_BYTES = TC::STAGE_BYTES;
@@ -341,6 +376,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             tc_fence_after();
             const int row = mt * BM + r_in;
             const uint32_t tl = tbase + ((uint32_t)(sp * 32) << 16) + (uint32_t)(b * BN);
+            const float rs = row < M ? row_scale(ne, row) : 1.f;
+            float ssq = 0.f;
+            bool ssq_done = false;  // this thread produced the tile's values of its row
             if (EPI == EPI_QKV_ROPE) {
                 // the tile holds BN/128 whole heads of this row: q and k heads are rotated at
                 // the row's position (pairs i, i+64), then q goes to its per-kv-head slab and
@@ -374,16 +412,17 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                                 for (int i = 0; i < 16; ++i) {
                                     const float4 t = cs[i];  // (cos, sin) of pairs 2i and 2i+1
-                                    const float a0 = __uint_as_float(x1[2 * i]), b0 = __uint_as_float(x2[2 * i]);
-                                    const float a1 = __uint_as_float(x1[2 * i + 1]), b1 = __uint_as_float(x2[2 * i + 1]);
+                                    const float a0 = __uint_as_float(x1[2 * i]) * rs, b0 = __uint_as_float(x2[2 * i]) * rs;
+                                    const float a1 = __uint_as_float(x1[2 * i + 1]) * rs;
+                                    const float b1 = __uint_as_float(x2[2 * i + 1]) * rs;
                                     w1[i] = pack_bf16x2(a0 * t.x - b0 * t.y, a1 * t.z - b1 * t.w);
                                     w2[i] = pack_bf16x2(b0 * t.x + a0 * t.y, b1 * t.z + a1 * t.w);
                                 }
                             } else {
 #pragma unroll
                                 for (int i = 0; i < 16; ++i) {
-                                    w1[i] = pack_bf16x2(__uint_as_float(x1[2 * i]), __uint_as_float(x1[2 * i + 1]));
-                                    w2[i] = pack_bf16x2(__uint_as_float(x2[2 * i]), __uint_as_float(x2[2 * i + 1]));
+                                    w1[i] = pack_bf16x2(__uint_as_float(x1[2 * i]) * rs, __uint_as_float(x1[2 * i + 1]) * rs);
+                                    w2[i] = pack_bf16x2(__uint_as_float(x2[2 * i]) * rs, __uint_as_float(x2[2 * i + 1]) * rs);
                                 }
                             }
                             uint4* d1 = reinterpret_cast<uint4*>(dst + c);
@@ -402,8 +441,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                     uint32_t r[32];
                     TMEM_LD32(tl + c, r);
                     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-                    if (row < M && nt * BN + c < N) epi_chunk<EPI>(r, row, nt * BN + c, Cv, ldc);
+                    if (row < M && nt * BN + c < N) epi_chunk<EPI>(r, row, nt * BN + c, Cv, ldc, rs, ne, ssq);
                 }
+                ssq_done = true;
             } else {
                 // split tile: publish this half's partial rows, then the second arrival
                 // for these rows finishes them
@@ -445,11 +485,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                                 r[4 * v + 2] = __float_as_uint(__uint_as_float(r[4 * v + 2]) + o.z);
                                 r[4 * v + 3] = __float_as_uint(__uint_as_float(r[4 * v + 3]) + o.w);
                             }
-                            epi_chunk<EPI>(r, row, nt * BN + c, Cv, ldc);
+                            epi_chunk<EPI>(r, row, nt * BN + c, Cv, ldc, rs, ne, ssq);
                         }
                     }
+                    ssq_done = true;
                 }
             }
+            if (EPI == EPI_ADD_F32 && ne.x_out != nullptr && ssq_done && row < M)
+                ne.ssq_out[(long long)row * ne.ssq_stride + nt] = ssq;
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[b]);
@@ -546,41 +589,51 @@ int pick_bn(int M_max, int N) {
     return 256;  // 128x128 tiles measured slower even with better wave fill
 }
 
+int gemm_tc_ntiles(int M_max, int N) {
+    const int bn = pick_bn(M_max, N);
+    return (N + bn - 1) / bn;
+}
+
 template <int BN>
 void launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, int K, int N, const int32_t* M_dev, int M_max,
-               int epi, void* C, int ldc, int32_t* err, cudaStream_t s, const QkvEpi& qe, float* ws, int32_t* cnt) {
+               int epi, void* C, int ldc, int32_t* err, cudaStream_t s, const QkvEpi& qe, float* ws, int32_t* cnt,
+               const NormEpi& ne) {
     const int tiles = ((M_max + BM - 1) / BM) * ((N + BN - 1) / BN);
     int grid = tiles < g_num_sms ? tiles : g_num_sms;
     // fewer tiles than half the SMs: every tile runs as two K halves on two CTAs
     if (ws != nullptr && epi != EPI_QKV_ROPE && K / BK >= 2 && 2 * tiles <= g_num_sms) grid = 2 * tiles;
     constexpr int SM = TileCfg<BN>::SMEM_BYTES;
     if (epi == EPI_STORE_F32)
-        k_gemm_tc<EPI_STORE_F32, BN><<<grid, THREADS, SM, s>>>(ma, mb, K, N, M_dev, C, ldc, err, qe, ws, cnt);
+        k_gemm_tc<EPI_STORE_F32, BN><<<grid, THREADS, SM, s>>>(ma, mb, K, N, M_dev, C, ldc, err, qe, ws, cnt, ne);
     else if (epi == EPI_ADD_F32)
-        k_gemm_tc<EPI_ADD_F32, BN><<<grid, THREADS, SM, s>>>(ma, mb, K, N, M_dev, C, ldc, err, qe, ws, cnt);
+        k_gemm_tc<EPI_ADD_F32, BN><<<grid, THREADS, SM, s>>>(ma, mb, K, N, M_dev, C, ldc, err, qe, ws, cnt, ne);
     else if (epi == EPI_SWIGLU)
-        k_gemm_tc<EPI_SWIGLU, BN><<<grid, THREADS, SM, s>>>(ma, mb, K, N, M_dev, C, ldc, err, qe, ws, cnt);
+        k_gemm_tc<EPI_SWIGLU, BN><<<grid, THREADS, SM, s>>>(ma, mb, K, N, M_dev, C, ldc, err, qe, ws, cnt, ne);
     else
-        k_gemm_tc<EPI_QKV_ROPE, BN><<<grid, THREADS, SM, s>>>(ma, mb, K, N, M_dev, C, ldc, err, qe, ws, cnt);
+        k_gemm_tc<EPI_QKV_ROPE, BN><<<grid, THREADS, SM, s>>>(ma, mb, K, N, M_dev, C, ldc, err, qe, ws, cnt, ne);
 }
 
 int launch_gemm_tc(const void* A, int K, int M_cap, const void* B, int N, const int32_t* M_dev, int M_max,
                    int epi, void* C, int ldc, int32_t* err, cudaStream_t s, const QkvEpi* qkv, float* split_ws,
-                   int32_t* split_cnt) {
+                   int32_t* split_cnt, const NormEpi* norm) {
     if (M_max <= 0) return BLEND_OK;
     const int bn = pick_bn(M_max, N);
     if (epi == EPI_QKV_ROPE && (qkv == nullptr || bn != 256)) return BLEND_EUNSUPPORTED;
     QkvEpi qe{};
     if (qkv) qe = *qkv;
+    NormEpi ne{};
+    if (norm) ne = *norm;
+    if (ne.x_out && (epi != EPI_ADD_F32 || ne.ssq_out == nullptr || ne.g == nullptr || ne.ldx % 8 != 0))
+        return BLEND_EUNSUPPORTED;
     CUtensorMap ma, mb;
     if (!encode_2d(&ma, A, (uint64_t)K, (uint64_t)M_cap, BK, BM) ||
         !encode_2d(&mb, B, (uint64_t)K, (uint64_t)N, BK, (uint32_t)bn))
         return BLEND_EUNSUPPORTED;  // the operands cannot be described to the TMA unit
     if (split_cnt == nullptr) split_ws = nullptr;
     if (bn == 256)
-        launch_bn<256>(ma, mb, K, N, M_dev, M_max, epi, C, ldc, err, s, qe, split_ws, split_cnt);
+        launch_bn<256>(ma, mb, K, N, M_dev, M_max, epi, C, ldc, err, s, qe, split_ws, split_cnt, ne);
     else
-        launch_bn<128>(ma, mb, K, N, M_dev, M_max, epi, C, ldc, err, s, qe, split_ws, split_cnt);
+        launch_bn<128>(ma, mb, K, N, M_dev, M_max, epi, C, ldc, err, s, qe, split_ws, split_cnt, ne);
     note_launch(1);
     return BLEND_OK;
 }

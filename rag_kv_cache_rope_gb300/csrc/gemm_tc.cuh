@@ -21,7 +21,9 @@ constexpr size_t GEMM_SPLIT_CNT_INTS = (size_t)GEMM_MAX_SPLIT_TILES * 4;
 // tensor map).
 int launch_gemm_tc(const void* A, int K, int M_cap, const void* B, int N, const int32_t* M_dev, int M_max,
                    int epi, void* C, int ldc, int32_t* err, cudaStream_t s, const QkvEpi* qkv = nullptr,
-                   float* split_ws = nullptr, int32_t* split_cnt = nullptr);
+                   float* split_ws = nullptr, int32_t* split_cnt = nullptr, const NormEpi* norm = nullptr);
+// N-tiles of an N-wide tensor-core GEMM at up to M_max rows (the partials a producer writes).
+int gemm_tc_ntiles(int M_max, int N);
 // Tensor-core attention (attn_tc.cu): head_dim 64 or 128, bf16.
 bool tc_attn_supported(int head_dim);
 // q: per kv head a slab [m_cap][group][head_dim]; rows of request r are
