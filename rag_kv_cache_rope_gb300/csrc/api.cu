@@ -95,8 +95,6 @@ struct blend_handle {
     cudaEvent_t ev_start = nullptr;
     cudaEvent_t ev_free[2] = {nullptr, nullptr};
     std::vector<cudaEvent_t> ev_layer;
-    float* split_ws;     // tensor-core GEMM: partials of last-wave tiles run as K halves
-    int32_t* split_cnt;  // their arrival counters (zero between launches)
     int use_tc;  // tensor-core GEMM for bf16
     int host_rc = 0;  // first failure of an internal launch during the current call
     std::string last_error;
@@ -225,6 +223,9 @@ bool lim_ok(const blend_limits* l, std::string* why) {
     return true;
 }
 
+// Folded RMSNorm: at most this many partial sums of squares per row (hidden <= 8192).
+constexpr int NORM_PARTS_MAX = 64;
+
 Layout make_layout(const blend_model_cfg* c, const blend_limits* l) {
     Layout L;
     const size_t es = elem_size(c->dtype);
@@ -258,12 +259,10 @@ Layout make_layout(const blend_model_cfg* c, const blend_limits* l) {
     L.add(nc * 4);                                         // 31 dev1
     L.add(nc * 4);                                         // 32 dev2
     L.add(16);                                             // 33 scratch count
-    L.add(c->dtype == BLEND_BF16 ? GEMM_SPLIT_WS_FLOATS * 4 : 0);  // 34 GEMM split partials
-    L.add(GEMM_SPLIT_CNT_INTS * 4);                        // 35 GEMM split counters
-    L.add(M * (size_t)c->n_q_heads * sizeof(float2));      // 36 aux score row statistics
-    for (int b = 0; b < 4; ++b)                            // 37..40 host-pool staging: K, V x 2 buffers
+    L.add(M * (size_t)c->n_q_heads * sizeof(float2));      // 34 aux score row statistics
+    for (int b = 0; b < 4; ++b)                            // 35..38 host-pool staging: K, V x 2 buffers
         L.add((size_t)l->max_tokens * kvd * es);
-    L.add(M * 64 * sizeof(float));                         // 41 folded-RMSNorm partial sums of squares
+    L.add(M * NORM_PARTS_MAX * sizeof(float));             // 39 folded-RMSNorm partial sums of squares
     return L;
 }
 
@@ -297,8 +296,8 @@ bool gemm_on_tc(const blend_handle* h, int K, int N, int epi, int ldc) {
 void gemm(blend_handle* h, const void* A, int K, const void* B, int N, int epi, void* C, int ldc,
           const int32_t* M_dev, int M_max, cudaStream_t s, const NormEpi* ne = nullptr) {
     if (gemm_on_tc(h, K, N, epi, ldc)) {
-        int rc = launch_gemm_tc(A, K, h->lim.max_rows, B, N, M_dev, M_max, epi, C, ldc, h->err, s, nullptr,
-                                h->split_ws, h->split_cnt, ne);
+        int rc = launch_gemm_tc(A, K, h->lim.max_rows, B, N, M_dev, M_max, epi, C, ldc, h->err, s, nullptr, true,
+                                ne);
         if (rc != BLEND_OK && h->host_rc == BLEND_OK) h->host_rc = rc;
     } else
         launch_gemm_simt(h->cfg.dtype, A, K, B, K, K, N, M_dev, M_max, epi, C, ldc, s);
@@ -322,13 +321,13 @@ void attention(blend_handle* h, const Plan& p, int n_req, int M_max, const void*
 // Producer and consumer sides of the folded RMSNorm (RMSNorm(x) . W = (1/rms(x)) ((x * g) . W)):
 // the residual-add GEMM writes bf16(x * g) and per-tile sums of squares, the next GEMM
 // scales its rows.
-NormEpi norm_producer(blend_handle* h, const void* g, int M_max) {
+NormEpi norm_producer(blend_handle* h, const void* g) {
     const int H = h->cfg.hidden;
     NormEpi ne{};
     ne.x_out = (bf16*)h->xn;
     ne.g = (const bf16*)g;
     ne.ssq_out = h->ssq;
-    ne.ssq_stride = gemm_tc_ntiles(M_max, H);
+    ne.ssq_stride = gemm_tc_norm_parts(H);
     ne.ldx = H;
     return ne;
 }
@@ -351,9 +350,9 @@ void layer_rest(blend_handle* h, int l, float* x, const Plan& p, int n_req, int 
     const int width = (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
     { ProfScope ps(h, PROF_ATTN, s); attention(h, p, n_req, M_max, kc, vc, n_tokens, s); }
     const bool fold_mlp = gemm_on_tc(h, qd, H, EPI_ADD_F32, H) && gemm_on_tc(h, H, 2 * F, EPI_SWIGLU, F) &&
-                          H <= 64 * 128;
+                          gemm_tc_norm_parts(H) <= NORM_PARTS_MAX;
     if (fold_mlp) {
-        const NormEpi prod = norm_producer(h, lw.mlp_norm, M_max);
+        const NormEpi prod = norm_producer(h, lw.mlp_norm);
         { ProfScope ps(h, PROF_GEMM_O, s); gemm(h, h->o, qd, lw.w_o, H, EPI_ADD_F32, x, H, p.M, M_max, s, &prod); }
         const NormEpi cons = norm_consumer(h, prod.ssq_stride);
         { ProfScope ps(h, PROF_GEMM_GU, s); gemm(h, h->xn, H, lw.w_gu, 2 * F, EPI_SWIGLU, h->hmlp, F, p.M, M_max, s, &cons); }
@@ -363,9 +362,9 @@ void layer_rest(blend_handle* h, int l, float* x, const Plan& p, int n_req, int 
         { ProfScope ps(h, PROF_GEMM_GU, s); gemm(h, h->xn, H, lw.w_gu, 2 * F, EPI_SWIGLU, h->hmlp, F, p.M, M_max, s); }
     }
     const bool fold_next = next_follows && l + 1 < c.n_layers && gemm_on_tc(h, F, H, EPI_ADD_F32, H) &&
-                           gemm_on_tc(h, H, width, EPI_STORE_F32, width) && H <= 64 * 128;
+                           gemm_on_tc(h, H, width, EPI_STORE_F32, width) && gemm_tc_norm_parts(H) <= NORM_PARTS_MAX;
     if (fold_next) {
-        const NormEpi prod = norm_producer(h, layer_w(h, l + 1).attn_norm, M_max);
+        const NormEpi prod = norm_producer(h, layer_w(h, l + 1).attn_norm);
         { ProfScope ps(h, PROF_GEMM_DOWN, s); gemm(h, h->hmlp, F, lw.w_down, H, EPI_ADD_F32, x, H, p.M, M_max, s, &prod); }
         h->xn_scaled = true;
         h->ssq_parts = prod.ssq_stride;
@@ -402,7 +401,7 @@ void layer_kv(blend_handle* h, int l, const float* x, const Plan& p, const int32
         QkvEpi qe{p.row_pos, p.row_tok, h->rope, (bf16*)h->q, (bf16*)kc, (bf16*)vc, h->lim.max_rows,
                   c.n_q_heads / c.n_kv_heads, c.n_q_heads, c.n_kv_heads};
         int rc = launch_gemm_tc(h->xn, H, h->lim.max_rows, lw.w_qkv, width, p.M, M_max, EPI_QKV_ROPE, nullptr, 0,
-                                h->err, s, &qe, nullptr, nullptr, &cons);
+                                h->err, s, &qe, false, &cons);
         if (rc != BLEND_OK && h->host_rc == BLEND_OK) h->host_rc = rc;
         return;
     }
@@ -478,16 +477,12 @@ int blend_init(const blend_model_cfg* cfg, const blend_weights* w, const blend_l
     h->dev[0] = (float*)(b + L.off[i++]);
     h->dev[1] = (float*)(b + L.off[i++]);
     h->scratch_n = (int32_t*)(b + L.off[i++]);
-    h->split_ws = cfg->dtype == BLEND_BF16 ? (float*)(b + L.off[i]) : nullptr;
-    ++i;
-    h->split_cnt = (int32_t*)(b + L.off[i++]);
     h->aux_stats = (float2*)(b + L.off[i++]);
     for (int q = 0; q < 4; ++q) h->stage[q] = b + L.off[i++];
     h->ssq = (float*)(b + L.off[i++]);
     h->use_tc = cfg->dtype == BLEND_BF16 ? tc_available() : 0;
     cudaStream_t s = (cudaStream_t)stream;
     cudaMemsetAsync(h->err, 0, 16, s);
-    cudaMemsetAsync(h->split_cnt, 0, GEMM_SPLIT_CNT_INTS * 4, s);
     launch_rope_table(h->rope, cfg->max_pos, cfg->head_dim, cfg->rope_theta, s);
     int rc = check_cuda(h, "blend_init");
     if (rc != BLEND_OK) {
@@ -515,8 +510,6 @@ int blend_device_status(blend_handle* h, void* stream) {
         return check_cuda(h, "blend_device_status");
     if (e != 0) {
         cudaMemset(h->err, 0, 4);
-        // an interrupted GEMM may have left split-tile counters raised
-        cudaMemset(h->split_cnt, 0, GEMM_SPLIT_CNT_INTS * 4);
         return fail(h, e == BLEND_ETIMEOUT ? BLEND_ETIMEOUT : BLEND_EDEVICE,
                     "device-side check failed (code %d)", e);
     }

@@ -13,14 +13,13 @@
 // overlap the main loop of the next.  M is read from the device; tiles past it are
 // skipped.
 // Tail split: tiles are dealt to the persistent CTAs in waves of gridDim.x.  When the
-// last wave is at most half full, each of its tiles is cut into two K halves run by two
-// CTAs, so that wave takes half a tile's time.  Each half writes its fp32 partial to a
-// workspace slab and counts in on a per-(tile, lane quarter) counter; the warp that
-// counts second adds the other partial to its own (a commutative sum of two terms, so
-// the result does not depend on which half finished first), runs the epilogue on the
-// sum and resets the counter.  No thread waits for another CTA.  Every mbarrier wait is bounded: on expiry the kernel records
-// BLEND_ETIMEOUT in the error word, stops issuing work, drains its own copies and
-// frees TMEM before returning.
+// last wave is at most half full, each of its tiles is cut into two column halves
+// (N = BN/2 MMAs over the whole K) run by two CTAs, so that wave takes half a tile's
+// time and each half runs its own epilogue: no partial sums, no CTA waits for another.
+// Residual-add epilogues of warps whose 32 rows are all live stage each 32-column chunk
+// in shared memory and leave it as tensor stores.  Every mbarrier wait is bounded: on
+// expiry the kernel records BLEND_ETIMEOUT in the error word, stops issuing work, drains
+// its own copies and frees TMEM before returning.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -41,9 +40,20 @@ template <int BN> struct TileCfg {
     static constexpr int STAGES = BN == 256 ? 4 : 6;
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;  // + alignment slack
-    // kind::f16 instruction descriptor: bf16 A and B (K-major), fp32 D, M=128, N=BN
+    // kind::f16 instruction descriptors: bf16 A and B (K-major), fp32 D, M=128, N=BN for a
+    // whole tile and N=BN/2 for a column half of a split tile
     static constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((BN >> 3) << 17) | ((BM >> 4) << 24);
+    static constexpr uint32_t IDESC_H =
+        (1u << 4) | (1u << 7) | (1u << 10) | (((BN / 2) >> 3) << 17) | ((BM >> 4) << 24);
 };
+// Residual-add epilogue staging: per epilogue warp one 32-row x 32-column chunk of the
+// fp32 sum (4 KB, 128-byte swizzle) and of bf16(x * g) (2 KB, 64-byte swizzle), which the
+// TMA unit stores while the warp computes the next chunk.
+constexpr int OUT_F32_BYTES = 32 * 32 * 4;
+constexpr int OUT_WARP_BYTES = OUT_F32_BYTES + 32 * 32 * 2;
+template <int EPI, int BN> constexpr int smem_bytes() {
+    return TileCfg<BN>::SMEM_BYTES + (EPI == EPI_ADD_F32 ? 4 * OUT_WARP_BYTES : 0);
+}
 
 __device__ __forceinline__ uint32_t su32(const void* p) {
     return (uint32_t)__cvta_generic_to_shared(p);
@@ -88,6 +98,15 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
         : "memory");
 }
 
+// Tensor store of a shared-memory box to global memory (bulk async-group of the
+// issuing thread).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int c0, int c1) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     (uint64_t)map),
+                 "r"(su32(src)), "r"(c0), "r"(c1)
+                 : "memory");
+}
+
 // Shared-memory matrix descriptor of a K-major tile stored with the 128-byte swizzle
 // (rows of 64 bf16 = 128 bytes, 8-row groups 1024 bytes apart).
 __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
@@ -113,9 +132,9 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
                      su32(bar))
                  : "memory");
 }
-// Work unit u -> tile, K-block range and, for a split unit, its half and split index.
+// Work unit u -> tile and, for a unit of a split tile, which column half (-1: whole tile).
 struct Unit {
-    int t, k0, k1, half, sidx;
+    int t, half;
 };
 struct Sched {
     int full;   // units dealt as whole tiles
@@ -125,26 +144,20 @@ struct Sched {
 __device__ __forceinline__ Sched make_sched(int n_total, int grid, bool can_split) {
     Sched sc;
     const int rem = n_total % grid;
-    sc.split = (can_split && rem > 0 && 2 * rem <= grid && rem <= GEMM_MAX_SPLIT_TILES) ? rem : 0;
+    sc.split = (can_split && rem > 0 && 2 * rem <= grid) ? rem : 0;
     sc.full = n_total - sc.split;
     sc.units = sc.full + 2 * sc.split;
     return sc;
 }
-__device__ __forceinline__ Unit unit_of(int u, const Sched& sc, int kblocks) {
+__device__ __forceinline__ Unit unit_of(int u, const Sched& sc) {
     Unit r;
     if (u < sc.full) {
         r.t = u;
-        r.k0 = 0;
-        r.k1 = kblocks;
         r.half = -1;
-        r.sidx = -1;
     } else {
         const int v = u - sc.full;
-        r.sidx = v >> 1;
+        r.t = sc.full + (v >> 1);
         r.half = v & 1;
-        r.t = sc.full + r.sidx;
-        r.k0 = r.half ? kblocks / 2 : 0;
-        r.k1 = r.half ? kblocks : kblocks / 2;
     }
     return r;
 }
@@ -242,12 +255,75 @@ __device__ __forceinline__ void epi_chunk(const uint32_t* r, int row, int col, v
     }
 }
 
+// Residual-add epilogue of 32 accumulator columns of the warp's 32 rows (row0 + lane)
+// through the warp's staging chunk cb: the fp32 sum x + rs * acc and, with ne.x_out,
+// bf16(sum * g) are written to shared memory in the TMA unit's swizzled layout and leave
+// as tensor stores of whole 32 x 32 boxes (full lines, no per-thread global stores).  xr
+// holds the thread's 32 residual values.  The chunk is reused once the previous stores
+// have read it.
+__device__ __forceinline__ void add_chunk_tma(const uint32_t* r, const float4* xr, int row0, int col, float rs,
+                                              const NormEpi& ne, uint8_t* cb, const CUtensorMap* mapC,
+                                              const CUtensorMap* mapX, float& ssq) {
+    const int lane = threadIdx.x & 31;
+    float o[32];
+#pragma unroll
+    for (int v = 0; v < 8; ++v) {
+        float4 w = make_float4(__uint_as_float(r[4 * v]) * rs, __uint_as_float(r[4 * v + 1]) * rs,
+                               __uint_as_float(r[4 * v + 2]) * rs, __uint_as_float(r[4 * v + 3]) * rs);
+        w.x += xr[v].x;
+        w.y += xr[v].y;
+        w.z += xr[v].z;
+        w.w += xr[v].w;
+        o[4 * v] = w.x;
+        o[4 * v + 1] = w.y;
+        o[4 * v + 2] = w.z;
+        o[4 * v + 3] = w.w;
+    }
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+    __syncwarp();
+    // 128-byte swizzle: 16-byte piece j of row i sits at piece j ^ (i % 8)
+    uint8_t* rowp = cb + lane * 128;
+#pragma unroll
+    for (int v = 0; v < 8; ++v)
+        *reinterpret_cast<float4*>(rowp + ((v ^ (lane & 7)) << 4)) =
+            make_float4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+    const bool has_x = ne.x_out != nullptr;
+    if (has_x) {
+        // 64-byte swizzle over 64-byte rows: piece j of row i sits at piece j ^ ((i / 2) % 4)
+        const uint4* gp = reinterpret_cast<const uint4*>(ne.g + col);
+        uint8_t* xrow = cb + OUT_F32_BYTES + lane * 64;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            const uint4 gv = gp[v];
+            const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+            uint32_t xw[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float a = o[8 * v + 2 * e], b = o[8 * v + 2 * e + 1];
+                ssq = fmaf(a, a, ssq);
+                ssq = fmaf(b, b, ssq);
+                const float ga = __uint_as_float(gw[e] << 16), gb = __uint_as_float(gw[e] & 0xffff0000u);
+                xw[e] = pack_bf16x2(a * ga, b * gb);
+            }
+            *reinterpret_cast<uint4*>(xrow + ((v ^ ((lane >> 1) & 3)) << 4)) = make_uint4(xw[0], xw[1], xw[2], xw[3]);
+        }
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) {
+        tma_store_2d(mapC, cb, col, row0);
+        if (has_x) tma_store_2d(mapX, cb + OUT_F32_BYTES, col, row0);
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    }
+}
+
 template <int EPI, int BN>
 __global__ void __launch_bounds__(THREADS, 1)
-    k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB, int K,
-              int N, const int32_t* __restrict__ M_dev, void* __restrict__ Cv, int ldc,
-              int32_t* __restrict__ err, const __grid_constant__ QkvEpi qe, float* __restrict__ split_ws,
-              int32_t* __restrict__ split_cnt, const __grid_constant__ NormEpi ne) {
+    k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+              const __grid_constant__ CUtensorMap mapBh, int K, int N, const int32_t* __restrict__ M_dev,
+              void* __restrict__ Cv, int ldc, int32_t* __restrict__ err, const __grid_constant__ QkvEpi qe,
+              int can_split, const __grid_constant__ NormEpi ne, const __grid_constant__ CUtensorMap mapC,
+              const __grid_constant__ CUtensorMap mapX, int tma_out) {
     using TC = TileCfg<BN>;
     constexpr int STAGES = TC::STAGES;
     constexpr int STAGE_BYTES = TC::STAGE_BYTES;
@@ -264,7 +340,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int m_tiles = (M + BM - 1) / BM, n_tiles = (N + BN - 1) / BN;  // the last N-tile may be partial
     const int n_total = m_tiles * n_tiles;
     const int kblocks = K / BK;
-    const Sched sc = make_sched(n_total, gridDim.x, EPI != EPI_QKV_ROPE && split_ws != nullptr && kblocks >= 2);
+    constexpr int HALF = BN / 2;
+    const Sched sc = make_sched(n_total, gridDim.x, EPI != EPI_QKV_ROPE && can_split != 0);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -297,19 +374,23 @@ __global__ void __launch_bounds__(THREADS, 1)
         int s = 0;
         uint32_t ph = 0;
         for (int u = blockIdx.x; u < sc.units && !abort_flag; u += gridDim.x) {
-            const Unit un = unit_of(u, sc, kblocks);
+            const Unit un = unit_of(u, sc);
             const int mt = un.t % m_tiles, nt = un.t / m_tiles;
-            for (int kb = un.k0; kb < un.k1; ++kb) {
+            // a column half loads only its BN/2 weight rows
+            const CUtensorMap* mb = un.half < 0 ? &mapB : &mapBh;
+            const int brow = nt * BN + (un.half > 0 ? HALF : 0);
+            const uint32_t bytes = un.half < 0 ? STAGE_BYTES : A_BYTES + TC::B_BYTES / 2;
+            for (int kb = 0; kb < kblocks; ++kb) {
                 if (!mbar_wait(&empty[s], ph ^ 1, &abort_flag)) {
                     abort_flag = 1;
                     set_error(err, BLEND_ETIMEOUT);
                     break;
                 }
                 uint8_t* st = smem + s * STAGE_BYTES;
-                mbar_expect_tx(&full[s], STAGE_BYTES);
+                mbar_expect_tx(&full[s], bytes);
                 pending[s] = (int)ph;
                 tma_load_2d(st, &mapA, &full[s], kb * BK, mt * BM);
-                tma_load_2d(st + A_BYTES, &mapB, &full[s], kb * BK, nt * BN);
+                tma_load_2d(st + A_BYTES, mb, &full[s], kb * BK, brow);
                 if (++s == STAGES) {
                     s = 0;
                     ph ^= 1;
@@ -321,7 +402,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         int s = 0, b = 0;
         uint32_t ph = 0, tph = 0;
         for (int u = blockIdx.x; u < sc.units && !abort_flag; u += gridDim.x) {
-            const Unit un = unit_of(u, sc, kblocks);
+            const Unit un = unit_of(u, sc);
+            const uint32_t idesc = un.half < 0 ? TC::IDESC : TC::IDESC_H;
             if (!mbar_wait(&tempty[b], tph ^ 1, &abort_flag)) {
                 abort_flag = 1;
                 set_error(err, BLEND_ETIMEOUT);
@@ -329,7 +411,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             tc_fence_after();
             const uint32_t d = tbase + (uint32_t)(b * BN);
-            for (int kb = un.k0; kb < un.k1; ++kb) {
+            for (int kb = 0; kb < kblocks; ++kb) {
                 if (!mbar_wait(&full[s], ph, &abort_flag)) {
                     abort_flag = 1;
                     set_error(err, BLEND_ETIMEOUT);
@@ -341,8 +423,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const uint32_t b_addr = a_addr + A_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk)
-                    umma_bf16(d, sdesc_sw128(a_addr + kk * 32), sdesc_sw128(b_addr + kk * 32), TC::IDESC,
-                              (kb != un.k0 || kk != 0) ? 1u : 0u);
+                    umma_bf16(d, sdesc_sw128(a_addr + kk * 32), sdesc_sw128(b_addr + kk * 32), idesc,
+                              (kb != 0 || kk != 0) ? 1u : 0u);
                 umma_commit(&empty[s]);
                 if (++s == STAGES) {
                     s = 0;
@@ -360,7 +442,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         int b = 0;
         uint32_t tph = 0;
         for (int u = blockIdx.x; u < sc.units; u += gridDim.x) {
-            const Unit un = unit_of(u, sc, kblocks);
+            const Unit un = unit_of(u, sc);
             const int mt = un.t % m_tiles, nt = un.t / m_tiles;
             // lane 0 waits and broadcasts; the warp stays converged for the .sync.aligned
             // tcgen05.ld below
@@ -377,8 +459,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int row = mt * BM + r_in;
             const uint32_t tl = tbase + ((uint32_t)(sp * 32) << 16) + (uint32_t)(b * BN);
             const float rs = row < M ? row_scale(ne, row) : 1.f;
-            float ssq = 0.f;
-            bool ssq_done = false;  // this thread produced the tile's values of its row
+            // residual add of a warp whose 32 rows are all live: through shared memory and
+            // tensor stores (warp-uniform)
+            const int row0 = mt * BM + sp * 32;
+            const bool tma_rows = EPI == EPI_ADD_F32 && tma_out != 0 && row0 + 32 <= M;
+            uint8_t* cb = smem + STAGES * STAGE_BYTES + sp * OUT_WARP_BYTES;
             if (EPI == EPI_QKV_ROPE) {
                 // the tile holds BN/128 whole heads of this row: q and k heads are rotated at
                 // the row's position (pairs i, i+64), then q goes to its per-kv-head slab and
@@ -435,70 +520,45 @@ __global__ void __launch_bounds__(THREADS, 1)
                         }
                     }
                 }
-            } else if (un.half < 0) {
-#pragma unroll 1
-                for (int c = 0; c < BN; c += 32) {
-                    uint32_t r[32];
-                    TMEM_LD32(tl + c, r);
-                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-                    if (row < M && nt * BN + c < N) epi_chunk<EPI>(r, row, nt * BN + c, Cv, ldc, rs, ne, ssq);
-                }
-                ssq_done = true;
             } else {
-                // split tile: publish this half's partial rows, then the second arrival
-                // for these rows finishes them
-                float* own = split_ws + ((long long)(un.sidx * 2 + un.half) * BM + r_in) * BN;
-                const float* other = split_ws + ((long long)(un.sidx * 2 + (un.half ^ 1)) * BM + r_in) * BN;
+                // a whole tile, or one column half of a split tile; the folded-norm sums of
+                // squares are kept per BN/2 columns
+                const int cbase = nt * BN + (un.half > 0 ? HALF : 0);
+                const int n_half = un.half < 0 ? 2 : 1;
 #pragma unroll 1
-                for (int c = 0; c < BN; c += 32) {
-                    uint32_t r[32];
-                    TMEM_LD32(tl + c, r);
-                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-                    if (row < M) {
-                        float4* p = reinterpret_cast<float4*>(own + c);
-#pragma unroll
-                        for (int v = 0; v < 8; ++v)
-                            p[v] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                                               __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
-                    }
-                }
-                __threadfence();
-                __syncwarp();
-                int order = 0;
-                if (lane == 0) order = atomicAdd(split_cnt + un.sidx * 4 + sp, 1);
-                order = __shfl_sync(0xffffffffu, order, 0);
-                if (order == 1) {
-                    __threadfence();
-                    if (lane == 0) split_cnt[un.sidx * 4 + sp] = 0;  // ready for the next launch
+                for (int hh = 0; hh < n_half; ++hh) {
+                    float ssq = 0.f;
 #pragma unroll 1
-                    for (int c = 0; c < BN; c += 32) {
+                    for (int c = hh * HALF; c < (hh + 1) * HALF; c += 32) {
                         uint32_t r[32];
                         TMEM_LD32(tl + c, r);
-                        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-                        if (row < M && nt * BN + c < N) {
-                            const float4* q = reinterpret_cast<const float4*>(other + c);
+                        const int col = cbase + c;
+                        if (EPI == EPI_ADD_F32 && tma_rows && col < N) {
+                            float4 xr[8];
+                            const float4* xp =
+                                reinterpret_cast<const float4*>((const float*)Cv + (long long)row * ldc + col);
 #pragma unroll
-                            for (int v = 0; v < 8; ++v) {
-                                const float4 o = __ldcg(q + v);
-                                r[4 * v] = __float_as_uint(__uint_as_float(r[4 * v]) + o.x);
-                                r[4 * v + 1] = __float_as_uint(__uint_as_float(r[4 * v + 1]) + o.y);
-                                r[4 * v + 2] = __float_as_uint(__uint_as_float(r[4 * v + 2]) + o.z);
-                                r[4 * v + 3] = __float_as_uint(__uint_as_float(r[4 * v + 3]) + o.w);
-                            }
-                            epi_chunk<EPI>(r, row, nt * BN + c, Cv, ldc, rs, ne, ssq);
+                            for (int v = 0; v < 8; ++v) xr[v] = xp[v];
+                            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                            add_chunk_tma(r, xr, row0, col, rs, ne, cb, &mapC, &mapX, ssq);
+                        } else {
+                            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                            if (row < M && col < N) epi_chunk<EPI>(r, row, col, Cv, ldc, rs, ne, ssq);
                         }
                     }
-                    ssq_done = true;
+                    const int col0 = cbase + hh * HALF;
+                    if (EPI == EPI_ADD_F32 && ne.x_out != nullptr && row < M && col0 < N)
+                        ne.ssq_out[(long long)row * ne.ssq_stride + col0 / HALF] = ssq;
                 }
             }
-            if (EPI == EPI_ADD_F32 && ne.x_out != nullptr && ssq_done && row < M)
-                ne.ssq_out[(long long)row * ne.ssq_stride + nt] = ssq;
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[b]);
             b ^= 1;
             if (b == 0) tph ^= 1;
         }
+        // the staging chunk belongs to this CTA: its last stores must be done before exit
+        if (EPI == EPI_ADD_F32 && lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     }
     __syncthreads();
     if (threadIdx.x == 0 && abort_flag) {
@@ -533,6 +593,20 @@ bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t oute
     return r == CUDA_SUCCESS;
 }
 
+// Output map of the residual-add epilogue: [outer][inner] elements of `bytes` each with a
+// row stride of ld elements, 32 x 32 boxes, the given swizzle.
+bool encode_out(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int bytes, uint64_t inner,
+                uint64_t outer, uint64_t ld, CUtensorMapSwizzle sw) {
+    if (((uintptr_t)base & 15) != 0 || (ld * bytes) % 16 != 0) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {ld * bytes};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          sw, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 int tc_available() {
@@ -555,14 +629,17 @@ int tc_available() {
         return 0;
     }
     g_encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
-    cudaFuncSetAttribute(k_gemm_tc<EPI_STORE_F32, 256>, cudaFuncAttributeMaxDynamicSharedMemorySize, TileCfg<256>::SMEM_BYTES);
-    cudaFuncSetAttribute(k_gemm_tc<EPI_ADD_F32, 256>, cudaFuncAttributeMaxDynamicSharedMemorySize, TileCfg<256>::SMEM_BYTES);
-    cudaFuncSetAttribute(k_gemm_tc<EPI_SWIGLU, 256>, cudaFuncAttributeMaxDynamicSharedMemorySize, TileCfg<256>::SMEM_BYTES);
-    cudaFuncSetAttribute(k_gemm_tc<EPI_QKV_ROPE, 256>, cudaFuncAttributeMaxDynamicSharedMemorySize, TileCfg<256>::SMEM_BYTES);
-    cudaFuncSetAttribute(k_gemm_tc<EPI_STORE_F32, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, TileCfg<128>::SMEM_BYTES);
-    cudaFuncSetAttribute(k_gemm_tc<EPI_ADD_F32, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, TileCfg<128>::SMEM_BYTES);
-    cudaFuncSetAttribute(k_gemm_tc<EPI_SWIGLU, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, TileCfg<128>::SMEM_BYTES);
-    cudaFuncSetAttribute(k_gemm_tc<EPI_QKV_ROPE, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, TileCfg<128>::SMEM_BYTES);
+#define SET_SMEM(E, N) \
+    cudaFuncSetAttribute(k_gemm_tc<E, N>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<E, N>())
+    SET_SMEM(EPI_STORE_F32, 256);
+    SET_SMEM(EPI_ADD_F32, 256);
+    SET_SMEM(EPI_SWIGLU, 256);
+    SET_SMEM(EPI_QKV_ROPE, 256);
+    SET_SMEM(EPI_STORE_F32, 128);
+    SET_SMEM(EPI_ADD_F32, 128);
+    SET_SMEM(EPI_SWIGLU, 128);
+    SET_SMEM(EPI_QKV_ROPE, 128);
+#undef SET_SMEM
     g_tc_state = 1;
     return 1;
 }
@@ -575,65 +652,72 @@ bool tc_gemm_supported(int K, int N, int epi, int ldc, int M_cap) {
 // N-tile width: 256, or 128 when N is a multiple of 128 but not of 256 or smaller than
 // 256 (the weight tensor must be at least one box high).  Otherwise the last 256-wide
 // tile is partial: the TMA fills the rows past N with zeros and the epilogue skips
-// those columns.  (128-wide tiles fill the last wave better for N = 5120 at ~3.3K rows,
-// but measured 30-40 % slower per FLOP.)
-int pick_bn(int M_max, int N) {
-    if (N < 256 || (N % 256 != 0 && N % 128 == 0)) return 128;
-    const long long m_tiles = (M_max + BM - 1) / BM;
-    auto fill = [&](int bn) {
-        const long long tiles = m_tiles * (N / bn);
-        const long long waves = (tiles + g_num_sms - 1) / g_num_sms;
-        return (double)tiles / (double)(waves * g_num_sms);
-    };
-    (void)fill;
-    return 256;  // 128x128 tiles measured slower even with better wave fill
-}
+// those columns.  (128-wide tiles everywhere fill the waves better for N = 5120 at ~3.3K
+// rows, but measured 30-40 % slower per FLOP; only a half-full last wave runs as halves.)
+int pick_bn(int N) { return (N < 256 || (N % 256 != 0 && N % 128 == 0)) ? 128 : 256; }
 
-int gemm_tc_ntiles(int M_max, int N) {
-    const int bn = pick_bn(M_max, N);
-    return (N + bn - 1) / bn;
+int gemm_tc_norm_parts(int N) {
+    const int half = pick_bn(N) / 2;
+    return (N + half - 1) / half;
 }
 
 template <int BN>
-void launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, int K, int N, const int32_t* M_dev, int M_max,
-               int epi, void* C, int ldc, int32_t* err, cudaStream_t s, const QkvEpi& qe, float* ws, int32_t* cnt,
-               const NormEpi& ne) {
+void launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mbh, int K, int N,
+               const int32_t* M_dev, int M_max, int epi, void* C, int ldc, int32_t* err, cudaStream_t s,
+               const QkvEpi& qe, bool split, const NormEpi& ne, const CUtensorMap& mc, const CUtensorMap& mx,
+               int tma_out) {
     const int tiles = ((M_max + BM - 1) / BM) * ((N + BN - 1) / BN);
     int grid = tiles < g_num_sms ? tiles : g_num_sms;
-    // fewer tiles than half the SMs: every tile runs as two K halves on two CTAs
-    if (ws != nullptr && epi != EPI_QKV_ROPE && K / BK >= 2 && 2 * tiles <= g_num_sms) grid = 2 * tiles;
-    constexpr int SM = TileCfg<BN>::SMEM_BYTES;
+    split = split && epi != EPI_QKV_ROPE;
+    // fewer tiles than half the SMs: every tile runs as two column halves on two CTAs
+    if (split && 2 * tiles <= g_num_sms) grid = 2 * tiles;
+    const int cs = split ? 1 : 0;
+#define LAUNCH(E)                                                                                      \
+    k_gemm_tc<E, BN><<<grid, THREADS, smem_bytes<E, BN>(), s>>>(ma, mb, mbh, K, N, M_dev, C, ldc, err, qe, cs, \
+                                                               ne, mc, mx, tma_out)
     if (epi == EPI_STORE_F32)
-        k_gemm_tc<EPI_STORE_F32, BN><<<grid, THREADS, SM, s>>>(ma, mb, K, N, M_dev, C, ldc, err, qe, ws, cnt, ne);
+        LAUNCH(EPI_STORE_F32);
     else if (epi == EPI_ADD_F32)
-        k_gemm_tc<EPI_ADD_F32, BN><<<grid, THREADS, SM, s>>>(ma, mb, K, N, M_dev, C, ldc, err, qe, ws, cnt, ne);
+        LAUNCH(EPI_ADD_F32);
     else if (epi == EPI_SWIGLU)
-        k_gemm_tc<EPI_SWIGLU, BN><<<grid, THREADS, SM, s>>>(ma, mb, K, N, M_dev, C, ldc, err, qe, ws, cnt, ne);
+        LAUNCH(EPI_SWIGLU);
     else
-        k_gemm_tc<EPI_QKV_ROPE, BN><<<grid, THREADS, SM, s>>>(ma, mb, K, N, M_dev, C, ldc, err, qe, ws, cnt, ne);
+        LAUNCH(EPI_QKV_ROPE);
+#undef LAUNCH
 }
 
 int launch_gemm_tc(const void* A, int K, int M_cap, const void* B, int N, const int32_t* M_dev, int M_max,
-                   int epi, void* C, int ldc, int32_t* err, cudaStream_t s, const QkvEpi* qkv, float* split_ws,
-                   int32_t* split_cnt, const NormEpi* norm) {
+                   int epi, void* C, int ldc, int32_t* err, cudaStream_t s, const QkvEpi* qkv, bool split,
+                   const NormEpi* norm) {
     if (M_max <= 0) return BLEND_OK;
-    const int bn = pick_bn(M_max, N);
+    const int bn = pick_bn(N);
     if (epi == EPI_QKV_ROPE && (qkv == nullptr || bn != 256)) return BLEND_EUNSUPPORTED;
     QkvEpi qe{};
     if (qkv) qe = *qkv;
     NormEpi ne{};
     if (norm) ne = *norm;
-    if (ne.x_out && (epi != EPI_ADD_F32 || ne.ssq_out == nullptr || ne.g == nullptr || ne.ldx % 8 != 0))
+    if (ne.x_out && (epi != EPI_ADD_F32 || ne.ssq_out == nullptr || ne.g == nullptr || ne.ldx % 8 != 0 ||
+                     ne.ssq_stride != gemm_tc_norm_parts(N)))
         return BLEND_EUNSUPPORTED;
-    CUtensorMap ma, mb;
+    CUtensorMap ma, mb, mbh;
     if (!encode_2d(&ma, A, (uint64_t)K, (uint64_t)M_cap, BK, BM) ||
-        !encode_2d(&mb, B, (uint64_t)K, (uint64_t)N, BK, (uint32_t)bn))
+        !encode_2d(&mb, B, (uint64_t)K, (uint64_t)N, BK, (uint32_t)bn) ||
+        !encode_2d(&mbh, B, (uint64_t)K, (uint64_t)N, BK, (uint32_t)bn / 2))
         return BLEND_EUNSUPPORTED;  // the operands cannot be described to the TMA unit
-    if (split_cnt == nullptr) split_ws = nullptr;
+    // residual add: the sum (and bf16(x * g)) of warps with 32 live rows leave as tensor
+    // stores; the maps span the M_max rows the launch may write
+    CUtensorMap mc{}, mx{};
+    int tma_out = 0;
+    if (epi == EPI_ADD_F32) {
+        tma_out = encode_out(&mc, C, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (uint64_t)N, (uint64_t)M_max, (uint64_t)ldc,
+                             CU_TENSOR_MAP_SWIZZLE_128B) &&
+                  (ne.x_out == nullptr || encode_out(&mx, ne.x_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)N,
+                                                     (uint64_t)M_max, (uint64_t)ne.ldx, CU_TENSOR_MAP_SWIZZLE_64B));
+    }
     if (bn == 256)
-        launch_bn<256>(ma, mb, K, N, M_dev, M_max, epi, C, ldc, err, s, qe, split_ws, split_cnt, ne);
+        launch_bn<256>(ma, mb, mbh, K, N, M_dev, M_max, epi, C, ldc, err, s, qe, split, ne, mc, mx, tma_out);
     else
-        launch_bn<128>(ma, mb, K, N, M_dev, M_max, epi, C, ldc, err, s, qe, split_ws, split_cnt, ne);
+        launch_bn<128>(ma, mb, mbh, K, N, M_dev, M_max, epi, C, ldc, err, s, qe, split, ne, mc, mx, tma_out);
     note_launch(1);
     return BLEND_OK;
 }

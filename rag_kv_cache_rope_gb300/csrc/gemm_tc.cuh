@@ -7,23 +7,20 @@ namespace blend {
 // 1 when the current device is an sm_103 GPU and the TMA descriptor encoder is
 // reachable; also sets the kernels' shared-memory limits.
 int tc_available();
-// Shapes the tensor-core kernel takes: K % 64 == 0, N % 256 == 0, ldc % 8 == 0, and an A
-// buffer of at least 128 rows (M_cap).
+// Shapes the tensor-core kernel takes: K % 64 == 0, N >= 128 and N % 32 == 0 (N % 256 == 0
+// for EPI_QKV_ROPE), ldc % 8 == 0, and an A buffer of at least 128 rows (M_cap).
 bool tc_gemm_supported(int K, int N, int epi, int ldc, int M_cap);
-// Split tiles of the last wave: at most this many, each with two fp32 partial slabs of
-// 128 x 256 values (split_ws) and four arrival counters (split_cnt, zero between launches).
-constexpr int GEMM_MAX_SPLIT_TILES = 128;
-constexpr size_t GEMM_SPLIT_WS_FLOATS = (size_t)GEMM_MAX_SPLIT_TILES * 2 * 128 * 256;
-constexpr size_t GEMM_SPLIT_CNT_INTS = (size_t)GEMM_MAX_SPLIT_TILES * 4;
 // A: [M_cap][K] bf16 buffer whose first *M_dev rows are used; B: [N][K] bf16.  With
-// split_ws / split_cnt (not for EPI_QKV_ROPE) a last wave that is at most half full runs
-// as K halves.  Returns BLEND_OK or BLEND_EUNSUPPORTED (operands not describable by a
-// tensor map).
+// split (not for EPI_QKV_ROPE) a last wave that is at most half full runs as column
+// halves.  A folded-norm producer (norm->x_out) writes gemm_tc_norm_parts(N) partial sums
+// of squares per row (norm->ssq_stride must equal it).  Returns BLEND_OK or
+// BLEND_EUNSUPPORTED (operands not describable by a tensor map).
 int launch_gemm_tc(const void* A, int K, int M_cap, const void* B, int N, const int32_t* M_dev, int M_max,
                    int epi, void* C, int ldc, int32_t* err, cudaStream_t s, const QkvEpi* qkv = nullptr,
-                   float* split_ws = nullptr, int32_t* split_cnt = nullptr, const NormEpi* norm = nullptr);
-// N-tiles of an N-wide tensor-core GEMM at up to M_max rows (the partials a producer writes).
-int gemm_tc_ntiles(int M_max, int N);
+                   bool split = true, const NormEpi* norm = nullptr);
+// Partial sums of squares per row that a folded-norm producer of width N writes (one per
+// half N-tile).
+int gemm_tc_norm_parts(int N);
 // Tensor-core attention (attn_tc.cu): head_dim 64 or 128, bf16.
 bool tc_attn_supported(int head_dim);
 // q: per kv head a slab [m_cap][group][head_dim]; rows of request r are

@@ -82,9 +82,9 @@ def test_layer_tensor_cores_match_oracle_and_cuda_cores(shape, n, n_ctx):
 
 @pytest.mark.parametrize("shape,n,n_ctx", SHAPES[:2], ids=[s[0].name for s in SHAPES[:2]])
 def test_split_tail_gemm_is_deterministic(shape, n, n_ctx):
-    """Shapes whose projections run as K halves (fewer tiles than half the SMs, or a last
-    wave at most half full): two runs of the same layer give bitwise identical outputs,
-    whichever half of a split tile finishes first."""
+    """Shapes whose projections run as column halves (fewer tiles than half the SMs, or a
+    last wave at most half full): two runs of the same layer give bitwise identical
+    outputs."""
     dev = torch.device("cuda:0")
     case = make_case(shape, 4, [8], pool="random")
     r = GpuRunner(case, max(n, 128), n_ctx, 64, max_pos=n_ctx)
