@@ -48,14 +48,14 @@ except OSError:
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
 # capture of each kernel (profiles/), valid only while the kernel's source is unchanged.
 TRAFFIC = {
-    "gemm_qkv": {"bytes": 116.745472e6 + 30.549504e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
-                 "sha256_16": "5077d32d26dc86f8", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
-    "gemm_o": {"bytes": 176.485120e6 + 68.064000e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
-               "sha256_16": "5077d32d26dc86f8", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
-    "gemm_gate_up": {"bytes": 322.683136e6 + 86.141952e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
-                     "sha256_16": "5077d32d26dc86f8", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
-    "gemm_down": {"bytes": 592.334848e6 + 89.107456e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
-                  "sha256_16": "5077d32d26dc86f8", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
+    "gemm_qkv": {"bytes": 116.443392e6 + 30.369792e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
+                 "sha256_16": "e88f4921132bf23d", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
+    "gemm_o": {"bytes": 201.924096e6 + 67.400960e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
+               "sha256_16": "e88f4921132bf23d", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
+    "gemm_gate_up": {"bytes": 326.870016e6 + 82.691584e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
+                     "sha256_16": "e88f4921132bf23d", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
+    "gemm_down": {"bytes": 597.856512e6 + 93.054464e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
+                  "sha256_16": "e88f4921132bf23d", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
     "attention": {"bytes": 132.768256e6 + 13.124352e6, "source": "rag_kv_cache_rope_gb300/csrc/attn_tc.cu",
                   "sha256_16": "95b92778a50a28c1", "profile": "profiles/attn_tc_qwen14b_16k_layer.md"},
 }
