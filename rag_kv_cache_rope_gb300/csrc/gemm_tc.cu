@@ -34,25 +34,30 @@ constexpr int THREADS = 192;
 constexpr long long SPIN_LIMIT = 1ll << 24;
 // Tile shape per N-tile width: 128x256 tiles with 4 stages of 48 KB, or 128x128 tiles
 // with 6 stages of 32 KB (used where 256-wide tiles leave the last wave mostly empty).
-template <int BN> struct TileCfg {
-    static constexpr int B_BYTES = BN * BK * 2;
+// PAIR: a cluster of two CTAs computes a 256x256 tile with cta_group::2 MMAs; each CTA
+// stages its own 128 rows of A and half of the tile's weight rows (6 stages of 32 KB),
+// so per SM the operand bytes per FLOP are two thirds of the single-CTA tile's.
+template <int BN, bool PAIR = false> struct TileCfg {
+    static constexpr int TM = PAIR ? 2 * BM : BM;     // tile rows
+    static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // weight rows one CTA stages for a whole tile
+    static constexpr int B_BYTES = B_ROWS * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = BN == 256 ? 4 : 6;
+    static constexpr int STAGES = (PAIR || BN != 256) ? 6 : 4;
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;  // + alignment slack
-    // kind::f16 instruction descriptors: bf16 A and B (K-major), fp32 D, M=128, N=BN for a
-    // whole tile and N=BN/2 for a column half of a split tile
-    static constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((BN >> 3) << 17) | ((BM >> 4) << 24);
+    // kind::f16 instruction descriptors: bf16 A and B (K-major), fp32 D, M = TM, N = BN for
+    // a whole tile and N = BN/2 for a column half of a split tile
+    static constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((BN >> 3) << 17) | ((TM >> 4) << 24);
     static constexpr uint32_t IDESC_H =
-        (1u << 4) | (1u << 7) | (1u << 10) | (((BN / 2) >> 3) << 17) | ((BM >> 4) << 24);
+        (1u << 4) | (1u << 7) | (1u << 10) | (((BN / 2) >> 3) << 17) | ((TM >> 4) << 24);
 };
 // Residual-add epilogue staging: per epilogue warp one 32-row x 32-column chunk of the
 // fp32 sum (4 KB, 128-byte swizzle) and of bf16(x * g) (2 KB, 64-byte swizzle), which the
 // TMA unit stores while the warp computes the next chunk.
 constexpr int OUT_F32_BYTES = 32 * 32 * 4;
 constexpr int OUT_WARP_BYTES = OUT_F32_BYTES + 32 * 32 * 2;
-template <int EPI, int BN> constexpr int smem_bytes() {
-    return TileCfg<BN>::SMEM_BYTES + (EPI == EPI_ADD_F32 ? 4 * OUT_WARP_BYTES : 0);
+template <int EPI, int BN, bool PAIR = false> constexpr int smem_bytes() {
+    return TileCfg<BN, PAIR>::SMEM_BYTES + (EPI == EPI_ADD_F32 ? 4 * OUT_WARP_BYTES : 0);
 }
 
 __device__ __forceinline__ uint32_t su32(const void* p) {
@@ -79,16 +84,6 @@ __device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Bounded wait for the phase of parity `parity`; false if it did not complete in time
-// or another role gave up.
-__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort_flag) {
-    for (long long i = 0; i < SPIN_LIMIT; ++i) {
-        if (mbar_try(b, parity)) return true;
-        if ((i & 255) == 255 && *abort_flag) return false;
-    }
-    return false;
-}
-
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0,
                                             int c1) {
     asm volatile(
@@ -132,6 +127,70 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
                      su32(bar))
                  : "memory");
 }
+// ---- CTA-pair forms (cluster of two CTAs, rank 0 leads)
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// shared::cluster address of the same variable in the leading CTA
+__device__ __forceinline__ uint32_t leader_addr(const void* p) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(r) : "r"(su32(p)));
+    return r;
+}
+// tensor load into this CTA's shared memory whose bytes count on the leader's barrier
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, uint32_t bar, int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(su32(dst)),
+        "l"((uint64_t)map), "r"(bar), "r"(c0), "r"(c1)
+        : "memory");
+}
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+// arrive on the barrier at this address in both CTAs once the issued MMAs complete
+__device__ __forceinline__ void umma_commit_pair(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            su32(bar)),
+        "h"((uint16_t)3)
+        : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_cluster(uint64_t* b, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(su32(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait for the phase of parity `parity`; false if it did not complete in time or
+// another role gave up.  PAIR waits acquire at cluster scope (the other CTA's arrivals
+// and copies).
+template <bool PAIR>
+__device__ __forceinline__ bool mbar_wait_t(uint64_t* b, uint32_t parity, volatile int* abort_flag) {
+    for (long long i = 0; i < SPIN_LIMIT; ++i) {
+        if (PAIR ? mbar_try_cluster(b, parity) : mbar_try(b, parity)) return true;
+        if ((i & 255) == 255 && *abort_flag) return false;
+    }
+    return false;
+}
+
 // Work unit u -> tile and, for a unit of a split tile, which column half (-1: whole tile).
 struct Unit {
     int t, half;
@@ -317,14 +376,14 @@ __device__ __forceinline__ void add_chunk_tma(const uint32_t* r, const float4* x
     }
 }
 
-template <int EPI, int BN>
+template <int EPI, int BN, bool PAIR>
 __global__ void __launch_bounds__(THREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
               const __grid_constant__ CUtensorMap mapBh, int K, int N, const int32_t* __restrict__ M_dev,
               void* __restrict__ Cv, int ldc, int32_t* __restrict__ err, const __grid_constant__ QkvEpi qe,
               int can_split, const __grid_constant__ NormEpi ne, const __grid_constant__ CUtensorMap mapC,
               const __grid_constant__ CUtensorMap mapX, int tma_out) {
-    using TC = TileCfg<BN>;
+    using TC = TileCfg<BN, PAIR>;
     constexpr int STAGES = TC::STAGES;
     constexpr int STAGE_BYTES = TC::STAGE_BYTES;
     constexpr int TMEM_COLS = TC::TMEM_COLS;
@@ -336,12 +395,16 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    // a CTA pair works as one unit: units are dealt per cluster, rank 1 takes rows 128..255
+    const int rank = PAIR ? (int)cluster_rank() : 0;
+    const int grp = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int n_grp = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
     const int M = *M_dev;
-    const int m_tiles = (M + BM - 1) / BM, n_tiles = (N + BN - 1) / BN;  // the last N-tile may be partial
+    const int m_tiles = (M + TC::TM - 1) / TC::TM, n_tiles = (N + BN - 1) / BN;  // the last N-tile may be partial
     const int n_total = m_tiles * n_tiles;
     const int kblocks = K / BK;
     constexpr int HALF = BN / 2;
-    const Sched sc = make_sched(n_total, gridDim.x, EPI != EPI_QKV_ROPE && can_split != 0);
+    const Sched sc = make_sched(n_total, n_grp, EPI != EPI_QKV_ROPE && can_split != 0);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -351,21 +414,32 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
-            mbar_init(&tempty[b], 4);  // one arrival per epilogue warp
+            mbar_init(&tempty[b], PAIR ? 8 : 4);  // one arrival per epilogue warp (of both CTAs)
         }
         abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         su32(&tmem_base_sh)),
-                     "r"(TMEM_COLS)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        // a pair allocates collectively: one warp of each CTA, the same columns in both
+        if (PAIR) {
+            asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                             su32(&tmem_base_sh)),
+                         "r"(TMEM_COLS)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+        } else {
+            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                             su32(&tmem_base_sh)),
+                         "r"(TMEM_COLS)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        }
     }
     tc_fence_before();
     __syncthreads();
+    // both CTAs' barriers are initialised before either signals the other's
+    if (PAIR) cluster_sync();
     tc_fence_after();
     const uint32_t tbase = tmem_base_sh;
 
@@ -373,38 +447,51 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ---------------- TMA producer
         int s = 0;
         uint32_t ph = 0;
-        for (int u = blockIdx.x; u < sc.units && !abort_flag; u += gridDim.x) {
+        for (int u = grp; u < sc.units && !abort_flag; u += n_grp) {
             const Unit un = unit_of(u, sc);
             const int mt = un.t % m_tiles, nt = un.t / m_tiles;
-            // a column half loads only its BN/2 weight rows
+            // this CTA's A rows and its share of the weight rows (a column half loads half)
             const CUtensorMap* mb = un.half < 0 ? &mapB : &mapBh;
-            const int brow = nt * BN + (un.half > 0 ? HALF : 0);
-            const uint32_t bytes = un.half < 0 ? STAGE_BYTES : A_BYTES + TC::B_BYTES / 2;
+            const int bshare = un.half < 0 ? TC::B_ROWS : TC::B_ROWS / 2;
+            const int brow = nt * BN + (un.half > 0 ? HALF : 0) + rank * bshare;
+            const int arow = mt * TC::TM + rank * BM;
+            const uint32_t bytes = (uint32_t)(A_BYTES + bshare * BK * 2);
             for (int kb = 0; kb < kblocks; ++kb) {
-                if (!mbar_wait(&empty[s], ph ^ 1, &abort_flag)) {
+                if (!mbar_wait_t<PAIR>(&empty[s], ph ^ 1, &abort_flag)) {
                     abort_flag = 1;
                     set_error(err, BLEND_ETIMEOUT);
                     break;
                 }
                 uint8_t* st = smem + s * STAGE_BYTES;
-                mbar_expect_tx(&full[s], bytes);
-                pending[s] = (int)ph;
-                tma_load_2d(st, &mapA, &full[s], kb * BK, mt * BM);
-                tma_load_2d(st + A_BYTES, mb, &full[s], kb * BK, brow);
+                if (PAIR) {
+                    // both CTAs' copies count on the leader's barrier, which expects them all
+                    if (rank == 0) {
+                        mbar_expect_tx(&full[s], 2 * bytes);
+                        pending[s] = (int)ph;
+                    }
+                    const uint32_t fb = leader_addr(&full[s]);
+                    tma_load_2d_pair(st, &mapA, fb, kb * BK, arow);
+                    tma_load_2d_pair(st + A_BYTES, mb, fb, kb * BK, brow);
+                } else {
+                    mbar_expect_tx(&full[s], bytes);
+                    pending[s] = (int)ph;
+                    tma_load_2d(st, &mapA, &full[s], kb * BK, arow);
+                    tma_load_2d(st + A_BYTES, mb, &full[s], kb * BK, brow);
+                }
                 if (++s == STAGES) {
                     s = 0;
                     ph ^= 1;
                 }
             }
         }
-    } else if (warp == 1 && lane == 0) {
-        // ---------------- MMA issuer
+    } else if (warp == 1 && lane == 0 && rank == 0) {
+        // ---------------- MMA issuer (the leading CTA of a pair issues for both)
         int s = 0, b = 0;
         uint32_t ph = 0, tph = 0;
-        for (int u = blockIdx.x; u < sc.units && !abort_flag; u += gridDim.x) {
+        for (int u = grp; u < sc.units && !abort_flag; u += n_grp) {
             const Unit un = unit_of(u, sc);
             const uint32_t idesc = un.half < 0 ? TC::IDESC : TC::IDESC_H;
-            if (!mbar_wait(&tempty[b], tph ^ 1, &abort_flag)) {
+            if (!mbar_wait_t<PAIR>(&tempty[b], tph ^ 1, &abort_flag)) {
                 abort_flag = 1;
                 set_error(err, BLEND_ETIMEOUT);
                 break;
@@ -412,7 +499,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             tc_fence_after();
             const uint32_t d = tbase + (uint32_t)(b * BN);
             for (int kb = 0; kb < kblocks; ++kb) {
-                if (!mbar_wait(&full[s], ph, &abort_flag)) {
+                if (!mbar_wait_t<PAIR>(&full[s], ph, &abort_flag)) {
                     abort_flag = 1;
                     set_error(err, BLEND_ETIMEOUT);
                     break;
@@ -422,16 +509,27 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const uint32_t a_addr = su32(smem + s * STAGE_BYTES);
                 const uint32_t b_addr = a_addr + A_BYTES;
 #pragma unroll
-                for (int kk = 0; kk < BK / 16; ++kk)
-                    umma_bf16(d, sdesc_sw128(a_addr + kk * 32), sdesc_sw128(b_addr + kk * 32), idesc,
-                              (kb != 0 || kk != 0) ? 1u : 0u);
-                umma_commit(&empty[s]);
+                for (int kk = 0; kk < BK / 16; ++kk) {
+                    if (PAIR)
+                        umma_bf16_pair(d, sdesc_sw128(a_addr + kk * 32), sdesc_sw128(b_addr + kk * 32), idesc,
+                                       (kb != 0 || kk != 0) ? 1u : 0u);
+                    else
+                        umma_bf16(d, sdesc_sw128(a_addr + kk * 32), sdesc_sw128(b_addr + kk * 32), idesc,
+                                  (kb != 0 || kk != 0) ? 1u : 0u);
+                }
+                if (PAIR)
+                    umma_commit_pair(&empty[s]);
+                else
+                    umma_commit(&empty[s]);
                 if (++s == STAGES) {
                     s = 0;
                     ph ^= 1;
                 }
             }
-            umma_commit(&tfull[b]);
+            if (PAIR)
+                umma_commit_pair(&tfull[b]);
+            else
+                umma_commit(&tfull[b]);
             b ^= 1;
             if (b == 0) tph ^= 1;
         }
@@ -441,13 +539,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int r_in = sp * 32 + lane;
         int b = 0;
         uint32_t tph = 0;
-        for (int u = blockIdx.x; u < sc.units; u += gridDim.x) {
+        for (int u = grp; u < sc.units; u += n_grp) {
             const Unit un = unit_of(u, sc);
             const int mt = un.t % m_tiles, nt = un.t / m_tiles;
             // lane 0 waits and broadcasts; the warp stays converged for the .sync.aligned
             // tcgen05.ld below
             bool ok = true;
-            if (lane == 0) ok = mbar_wait(&tfull[b], tph, &abort_flag);
+            if (lane == 0) ok = mbar_wait_t<PAIR>(&tfull[b], tph, &abort_flag);
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             __syncwarp();
             if (!ok) {
@@ -456,12 +554,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                 break;
             }
             tc_fence_after();
-            const int row = mt * BM + r_in;
+            const int row = mt * TC::TM + rank * BM + r_in;
             const uint32_t tl = tbase + ((uint32_t)(sp * 32) << 16) + (uint32_t)(b * BN);
             const float rs = row < M ? row_scale(ne, row) : 1.f;
             // residual add of a warp whose 32 rows are all live: through shared memory and
             // tensor stores (warp-uniform)
-            const int row0 = mt * BM + sp * 32;
+            const int row0 = mt * TC::TM + rank * BM + sp * 32;
             const bool tma_rows = EPI == EPI_ADD_F32 && tma_out != 0 && row0 + 32 <= M;
             uint8_t* cb = smem + STAGES * STAGE_BYTES + sp * OUT_WARP_BYTES;
             if (EPI == EPI_QKV_ROPE) {
@@ -553,7 +651,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[b]);
+            if (lane == 0) {
+                if (PAIR)
+                    mbar_arrive_cluster(leader_addr(&tempty[b]));  // the leader reuses the columns
+                else
+                    mbar_arrive(&tempty[b]);
+            }
             b ^= 1;
             if (b == 0) tph ^= 1;
         }
@@ -569,11 +672,18 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             }
     }
+    tc_fence_before();
     __syncthreads();
+    // neither CTA of a pair leaves while the other may still signal its barriers
+    if (PAIR) cluster_sync();
     if (warp == 1) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(TMEM_COLS)
-                     : "memory");
+        if (PAIR)
+            asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(TMEM_COLS)
+                         : "memory");
+        else
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(TMEM_COLS)
+                         : "memory");
     }
 }
 
@@ -629,16 +739,20 @@ int tc_available() {
         return 0;
     }
     g_encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
-#define SET_SMEM(E, N) \
-    cudaFuncSetAttribute(k_gemm_tc<E, N>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<E, N>())
-    SET_SMEM(EPI_STORE_F32, 256);
-    SET_SMEM(EPI_ADD_F32, 256);
-    SET_SMEM(EPI_SWIGLU, 256);
-    SET_SMEM(EPI_QKV_ROPE, 256);
-    SET_SMEM(EPI_STORE_F32, 128);
-    SET_SMEM(EPI_ADD_F32, 128);
-    SET_SMEM(EPI_SWIGLU, 128);
-    SET_SMEM(EPI_QKV_ROPE, 128);
+#define SET_SMEM(E, N, P) \
+    cudaFuncSetAttribute(k_gemm_tc<E, N, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<E, N, P>())
+    SET_SMEM(EPI_STORE_F32, 256, false);
+    SET_SMEM(EPI_ADD_F32, 256, false);
+    SET_SMEM(EPI_SWIGLU, 256, false);
+    SET_SMEM(EPI_QKV_ROPE, 256, false);
+    SET_SMEM(EPI_STORE_F32, 128, false);
+    SET_SMEM(EPI_ADD_F32, 128, false);
+    SET_SMEM(EPI_SWIGLU, 128, false);
+    SET_SMEM(EPI_QKV_ROPE, 128, false);
+    SET_SMEM(EPI_STORE_F32, 256, true);
+    SET_SMEM(EPI_ADD_F32, 256, true);
+    SET_SMEM(EPI_SWIGLU, 256, true);
+    SET_SMEM(EPI_QKV_ROPE, 256, true);
 #undef SET_SMEM
     g_tc_state = 1;
     return 1;
@@ -661,20 +775,77 @@ int gemm_tc_norm_parts(int N) {
     return (N + half - 1) / half;
 }
 
-template <int BN>
+template <int BN, bool PAIR>
 void launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mbh, int K, int N,
                const int32_t* M_dev, int M_max, int epi, void* C, int ldc, int32_t* err, cudaStream_t s,
                const QkvEpi& qe, bool split, const NormEpi& ne, const CUtensorMap& mc, const CUtensorMap& mx,
                int tma_out) {
-    const int tiles = ((M_max + BM - 1) / BM) * ((N + BN - 1) / BN);
-    int grid = tiles < g_num_sms ? tiles : g_num_sms;
+    // one work unit per CTA, or per cluster of two CTAs: as many as can be resident at once
+    int slots = g_num_sms;
+    if (PAIR) {
+        static int max_clusters[4] = {0, 0, 0, 0};
+        int& mc = max_clusters[epi & 3];
+        if (mc == 0) {
+            cudaLaunchConfig_t q = {};
+            q.gridDim = dim3(g_num_sms);
+            q.blockDim = dim3(THREADS);
+            cudaLaunchAttribute qa[1];
+            qa[0].id = cudaLaunchAttributeClusterDimension;
+            qa[0].val.clusterDim.x = 2;
+            qa[0].val.clusterDim.y = 1;
+            qa[0].val.clusterDim.z = 1;
+            q.attrs = qa;
+            q.numAttrs = 1;
+            int n = 0;
+            cudaError_t e = cudaSuccess;
+            switch (epi) {
+                case EPI_STORE_F32:
+                    q.dynamicSmemBytes = smem_bytes<EPI_STORE_F32, BN, PAIR>();
+                    e = cudaOccupancyMaxActiveClusters(&n, k_gemm_tc<EPI_STORE_F32, BN, PAIR>, &q);
+                    break;
+                case EPI_ADD_F32:
+                    q.dynamicSmemBytes = smem_bytes<EPI_ADD_F32, BN, PAIR>();
+                    e = cudaOccupancyMaxActiveClusters(&n, k_gemm_tc<EPI_ADD_F32, BN, PAIR>, &q);
+                    break;
+                case EPI_SWIGLU:
+                    q.dynamicSmemBytes = smem_bytes<EPI_SWIGLU, BN, PAIR>();
+                    e = cudaOccupancyMaxActiveClusters(&n, k_gemm_tc<EPI_SWIGLU, BN, PAIR>, &q);
+                    break;
+                default:
+                    q.dynamicSmemBytes = smem_bytes<EPI_QKV_ROPE, BN, PAIR>();
+                    e = cudaOccupancyMaxActiveClusters(&n, k_gemm_tc<EPI_QKV_ROPE, BN, PAIR>, &q);
+            }
+            if (e != cudaSuccess || n <= 0) {
+                cudaGetLastError();
+                n = g_num_sms / 2;
+            }
+            mc = n < g_num_sms / 2 ? n : g_num_sms / 2;
+        }
+        slots = mc;
+    }
+    const int tiles = ((M_max + TileCfg<BN, PAIR>::TM - 1) / TileCfg<BN, PAIR>::TM) * ((N + BN - 1) / BN);
+    int groups = tiles < slots ? tiles : slots;
     split = split && epi != EPI_QKV_ROPE;
-    // fewer tiles than half the SMs: every tile runs as two column halves on two CTAs
-    if (split && 2 * tiles <= g_num_sms) grid = 2 * tiles;
+    // fewer tiles than half the slots: every tile runs as two column halves
+    if (split && 2 * tiles <= slots) groups = 2 * tiles;
     const int cs = split ? 1 : 0;
-#define LAUNCH(E)                                                                                      \
-    k_gemm_tc<E, BN><<<grid, THREADS, smem_bytes<E, BN>(), s>>>(ma, mb, mbh, K, N, M_dev, C, ldc, err, qe, cs, \
-                                                               ne, mc, mx, tma_out)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(PAIR ? 2 * groups : groups);
+    cfg.blockDim = dim3(THREADS);
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = PAIR ? 2 : 1;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+#define LAUNCH(E)                                                                                              \
+    do {                                                                                                       \
+        cfg.dynamicSmemBytes = smem_bytes<E, BN, PAIR>();                                                      \
+        cudaLaunchKernelEx(&cfg, k_gemm_tc<E, BN, PAIR>, ma, mb, mbh, K, N, M_dev, C, ldc, err, qe, cs, ne, mc, mx, \
+                           tma_out);                                                                           \
+    } while (0)
     if (epi == EPI_STORE_F32)
         LAUNCH(EPI_STORE_F32);
     else if (epi == EPI_ADD_F32)
@@ -699,10 +870,14 @@ int launch_gemm_tc(const void* A, int K, int M_cap, const void* B, int N, const 
     if (ne.x_out && (epi != EPI_ADD_F32 || ne.ssq_out == nullptr || ne.g == nullptr || ne.ldx % 8 != 0 ||
                      ne.ssq_stride != gemm_tc_norm_parts(N)))
         return BLEND_EUNSUPPORTED;
+    // 256-wide tiles over more than one 128-row block run on CTA pairs (256x256 tiles);
+    // each CTA of a pair stages half of a tile's weight rows
+    const bool pair = bn == 256 && M_max > BM && g_num_sms >= 2;
+    const uint32_t brows = pair ? (uint32_t)bn / 2 : (uint32_t)bn;
     CUtensorMap ma, mb, mbh;
     if (!encode_2d(&ma, A, (uint64_t)K, (uint64_t)M_cap, BK, BM) ||
-        !encode_2d(&mb, B, (uint64_t)K, (uint64_t)N, BK, (uint32_t)bn) ||
-        !encode_2d(&mbh, B, (uint64_t)K, (uint64_t)N, BK, (uint32_t)bn / 2))
+        !encode_2d(&mb, B, (uint64_t)K, (uint64_t)N, BK, brows) ||
+        !encode_2d(&mbh, B, (uint64_t)K, (uint64_t)N, BK, brows / 2))
         return BLEND_EUNSUPPORTED;  // the operands cannot be described to the TMA unit
     // residual add: the sum (and bf16(x * g)) of warps with 32 live rows leave as tensor
     // stores; the maps span the M_max rows the launch may write
@@ -714,10 +889,12 @@ int launch_gemm_tc(const void* A, int K, int M_cap, const void* B, int N, const 
                   (ne.x_out == nullptr || encode_out(&mx, ne.x_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)N,
                                                      (uint64_t)M_max, (uint64_t)ne.ldx, CU_TENSOR_MAP_SWIZZLE_64B));
     }
-    if (bn == 256)
-        launch_bn<256>(ma, mb, mbh, K, N, M_dev, M_max, epi, C, ldc, err, s, qe, split, ne, mc, mx, tma_out);
+    if (pair)
+        launch_bn<256, true>(ma, mb, mbh, K, N, M_dev, M_max, epi, C, ldc, err, s, qe, split, ne, mc, mx, tma_out);
+    else if (bn == 256)
+        launch_bn<256, false>(ma, mb, mbh, K, N, M_dev, M_max, epi, C, ldc, err, s, qe, split, ne, mc, mx, tma_out);
     else
-        launch_bn<128>(ma, mb, mbh, K, N, M_dev, M_max, epi, C, ldc, err, s, qe, split, ne, mc, mx, tma_out);
+        launch_bn<128, false>(ma, mb, mbh, K, N, M_dev, M_max, epi, C, ldc, err, s, qe, split, ne, mc, mx, tma_out);
     note_launch(1);
     return BLEND_OK;
 }
