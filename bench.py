@@ -48,14 +48,14 @@ except OSError:
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
 # capture of each kernel (profiles/), valid only while the kernel's source is unchanged.
 TRAFFIC = {
-    "gemm_qkv": {"bytes": 116.443392e6 + 30.369792e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
-                 "sha256_16": "e88f4921132bf23d", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
-    "gemm_o": {"bytes": 201.924096e6 + 67.400960e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
-               "sha256_16": "e88f4921132bf23d", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
-    "gemm_gate_up": {"bytes": 326.870016e6 + 82.691584e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
-                     "sha256_16": "e88f4921132bf23d", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
-    "gemm_down": {"bytes": 597.856512e6 + 93.054464e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
-                  "sha256_16": "e88f4921132bf23d", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
+    "gemm_qkv": {"bytes": 126.855680e6 + 31.247616e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
+                 "sha256_16": "2106f78a5fd04d97", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
+    "gemm_o": {"bytes": 210.922496e6 + 66.523648e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
+               "sha256_16": "2106f78a5fd04d97", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
+    "gemm_gate_up": {"bytes": 373.736960e6 + 84.323072e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
+                     "sha256_16": "2106f78a5fd04d97", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
+    "gemm_down": {"bytes": 598.224384e6 + 92.883968e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
+                  "sha256_16": "2106f78a5fd04d97", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
     "attention": {"bytes": 132.768256e6 + 13.124352e6, "source": "rag_kv_cache_rope_gb300/csrc/attn_tc.cu",
                   "sha256_16": "95b92778a50a28c1", "profile": "profiles/attn_tc_qwen14b_16k_layer.md"},
 }
@@ -115,7 +115,7 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -136,7 +136,7 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
+        sm, mx, pw, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             p = [x.strip() for x in ln.split(",")]
@@ -147,13 +147,17 @@ class ClockSampler:
                 mx.append(float(p[2]))
             except ValueError:
                 continue
+            try:
+                pw.append(float(p[3]))
+            except ValueError:
+                pass
             for n, v in zip(names, p[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "power_w": statistics.median(pw) if pw else None}
 
 
 # ---------------------------------------------------------------- our arm
