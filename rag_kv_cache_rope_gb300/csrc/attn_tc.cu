@@ -571,6 +571,468 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 }
 
+// ---------------------------------------------------------------- CTA-pair kernel (D = 128)
+// The two CTAs of a cluster take the two tiles of one work item.  Each holds its own Q
+// tile, and per 128-key block each stages half of the block's keys (for S) and half of
+// V's d columns (for P.V), so every block is loaded once for both tiles and each SM
+// reads a third less operand data per FLOP.  The leading CTA issues, for both:
+//   S = Q . K^T   tcgen05.mma.cta_group::2 M256 N128 K16 x8 (A: each CTA's Q tile; B:
+//                 each CTA's 64 keys) into the S buffer of the block's parity
+//   O += P . V    tcgen05.mma.cta_group::2 M256 N128 K16 x8 (A: each CTA's P in TMEM;
+//                 B: each CTA's 64 d columns of V, MN-major)
+// S is double-buffered in TMEM: S(j+1) is issued before P(j) is ready and S(j+2) right
+// after P.V(j), so a softmax goes from block to block without waiting for the tensor
+// core.  The completion of every P.V is committed, and a softmax that must rescale O
+// (running maximum up by more than 2^8) first waits for the previous block's P.V.  The
+// softmax is the single-tile one of k_attn_tc, one pair row per thread.
+namespace pairk {
+constexpr int THREADS2 = 192;  // warp 0 TMA, 1 TMEM + MMA issue (leader), 2..5 softmax
+constexpr int STAGES2 = 4;
+constexpr int KQ_BYTES = 64 * 64 * 2;                  // 64 keys x one 64-wide d half
+constexpr int VH_BYTES = BKV * 64 * 2;                 // 128 keys x this CTA's 64 d columns
+constexpr int STAGE_BYTES = 2 * KQ_BYTES + VH_BYTES;   // 32 KB
+constexpr int QT_BYTES = 2 * QH_BYTES;                 // one 128-pair tile, two d halves
+constexpr int SMEM_BYTES = 2 * QT_BYTES + STAGES2 * STAGE_BYTES + 1024;
+constexpr int COLS2 = 512;  // S buffers at 0 and 128, O at 256
+constexpr uint32_t O_COL = 256;
+// kind::f16, bf16 inputs, fp32 accumulate, M256 (the pair) N128; P.V with B MN-major
+constexpr uint32_t IDESC_S2 = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((256u >> 4) << 24);
+constexpr uint32_t IDESC_PV2 = IDESC_S2 | (1u << 16);
+
+__device__ __forceinline__ uint32_t cta_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t leader_addr(const void* p) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(r) : "r"(su32(p)));
+    return r;
+}
+__device__ __forceinline__ void tma_2d_pair(void* dst, const CUtensorMap* m, uint32_t bar, int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
+        "%4}], [%2];" ::"r"(su32(dst)),
+        "l"((uint64_t)m), "r"(bar), "r"(c0), "r"(c1)
+        : "memory");
+}
+__device__ __forceinline__ void tma_3d_pair(void* dst, const CUtensorMap* m, uint32_t bar, int c0, int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
+        "%4, %5}], [%2];" ::"r"(su32(dst)),
+        "l"((uint64_t)m), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+__device__ __forceinline__ void umma_ss2(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+__device__ __forceinline__ void umma_ts2(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+// arrive on this barrier in both CTAs once the MMAs issued so far complete
+__device__ __forceinline__ void commit2(uint64_t* b) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            su32(b)),
+        "h"((uint16_t)3)
+        : "memory");
+}
+__device__ __forceinline__ bool try_cl(uint64_t* b, uint32_t par) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(su32(b)), "r"(par)
+        : "memory");
+    return ok != 0;
+}
+// Non-blocking test of the phase: a blocking try_wait on a barrier that the other CTA
+// arrives on was measured to resume up to ~1.5 K cycles after the phase completed.
+__device__ __forceinline__ bool test_cl(uint64_t* b, uint32_t par) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(su32(b)), "r"(par)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool wait_cl(uint64_t* b, uint32_t par, volatile int* abort_flag) {
+    for (long long i = 0; i < 64 * SPIN_LIMIT; ++i) {
+        if (test_cl(b, par)) return true;
+        if ((i & 1023) == 1023 && *abort_flag) return false;
+    }
+    return false;
+}
+__device__ __forceinline__ bool warp_wait_cl(uint64_t* b, uint32_t par, volatile int* abort_flag) {
+    for (long long i = 0; i < SPIN_LIMIT; ++i) {
+        if (__all_sync(0xffffffffu, try_cl(b, par))) return true;
+        if ((i & 255) == 255 && __any_sync(0xffffffffu, *abort_flag != 0)) return false;
+    }
+    return false;
+}
+// warp-level release-arrive on the leader's barrier (remote for rank 1)
+__device__ __forceinline__ void warp_arrive_leader(uint64_t* b) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0)
+        asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(leader_addr(b)) : "memory");
+}
+}  // namespace pairk
+
+__global__ void __launch_bounds__(pairk::THREADS2, 1)
+    k_attn_pair(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
+                const __grid_constant__ CUtensorMap mapV, int n_req, const int32_t* __restrict__ req_row_end,
+                const int32_t* __restrict__ row_pos, const int32_t* __restrict__ row_tok, int group, int hkv,
+                int m_cap, float scale_log2, bf16* __restrict__ out, int32_t* __restrict__ err) {
+    using namespace pairk;
+    constexpr int D = 128;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t q_full[2], q_empty[2], kv_full[STAGES2], kv_empty[STAGES2], s_full[2],
+        p_full[2], pv_done, o_full, o_free;
+    __shared__ uint32_t tmem_sh;
+    __shared__ volatile int abort_flag;
+    __shared__ int pend_kv[STAGES2];
+    __shared__ int pend_q[2];
+
+    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t* sQ = smem;                  // Q buffer qb at qb * QT_BYTES
+    uint8_t* sKV = smem + 2 * QT_BYTES;  // stage s at s * STAGE_BYTES: K d-half 0, K d-half 1, V half
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int rank = (int)cta_rank();
+    const int grp = (int)(blockIdx.x >> 1), n_grp = (int)(gridDim.x >> 1);
+
+    int total = 0;
+    {
+        int row0 = 0;
+        for (int r = 0; r < n_req; ++r) {
+            const int row1 = req_row_end[r];
+            const int tiles = ((row1 - row0) * group + BQ - 1) / BQ;
+            total += hkv * ((tiles + 1) / 2);
+            row0 = row1;
+        }
+    }
+    if (threadIdx.x == 0) {
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&q_full[b], 1);
+            mbar_init(&q_empty[b], 1);
+            mbar_init(&s_full[b], 1);
+            mbar_init(&p_full[b], 8);  // 4 softmax warps in each CTA
+            pend_q[b] = -1;
+        }
+        for (int s = 0; s < STAGES2; ++s) {
+            mbar_init(&kv_full[s], 1);
+            mbar_init(&kv_empty[s], 1);
+            pend_kv[s] = -1;
+        }
+        mbar_init(&pv_done, 1);
+        mbar_init(&o_full, 1);
+        mbar_init(&o_free, 8);
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        // allocated collectively: one warp of each CTA, the same columns in both
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&tmem_sh)),
+                     "r"(COLS2)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    fence_before();
+    __syncthreads();
+    cluster_sync();  // both CTAs' barriers exist before either signals the other's
+    fence_after();
+    const uint32_t tb = tmem_sh;
+    const int qslab = m_cap * group;
+    auto item_of = [&](int k) -> int { return k * n_grp + ((k & 1) ? n_grp - 1 - grp : grp); };
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------ TMA producer (both CTAs)
+        uint32_t it = 0;
+        for (int k = 0, tl = 0; !abort_flag; ++k, ++tl) {
+            const int w = item_of(k);
+            if (w >= total) break;
+            Item m;
+            get_item(w, n_req, req_row_end, row_pos, row_tok, group, hkv, m);
+            const int qb = tl & 1;
+            if (!wait_cl(&q_empty[qb], ((tl >> 1) & 1) ^ 1, &abort_flag)) {
+                abort_flag = 1;
+                set_error(err, BLEND_ETIMEOUT);
+                break;
+            }
+            if (rank == 0) {
+                mbar_expect_tx(&q_full[qb], 2 * QT_BYTES);  // both CTAs' tiles count here
+                pend_q[qb] = (tl >> 1) & 1;
+            }
+            {
+                // an absent second tile reloads the first (finite data, never stored)
+                const int p0 = (rank == 0 || m.pair0_b < 0) ? m.pair0_a : m.pair0_b;
+                const int qrow = m.g * qslab + m.row0 * group + p0;
+                const uint32_t qf = leader_addr(&q_full[qb]);
+                tma_2d_pair(sQ + qb * QT_BYTES, &mapQ, qf, 0, qrow);
+                tma_2d_pair(sQ + qb * QT_BYTES + QH_BYTES, &mapQ, qf, 64, qrow);
+            }
+            for (int kb = 0; kb < m.nblk; ++kb, ++it) {
+                const int st = it % STAGES2;
+                if (!wait_cl(&kv_empty[st], ((it / STAGES2) & 1) ^ 1, &abort_flag)) {
+                    abort_flag = 1;
+                    set_error(err, BLEND_ETIMEOUT);
+                    break;
+                }
+                uint8_t* b = sKV + st * STAGE_BYTES;
+                if (rank == 0) {
+                    mbar_expect_tx(&kv_full[st], 2 * STAGE_BYTES);
+                    pend_kv[st] = (int)((it / STAGES2) & 1);
+                }
+                const uint32_t kf = leader_addr(&kv_full[st]);
+                const int tok = m.tok_base + kb * BKV;
+                // this CTA's 64 keys (both d halves) and its 64 d columns of V (all keys)
+                tma_3d_pair(b, &mapK, kf, 0, m.g, tok + 64 * rank);
+                tma_3d_pair(b + KQ_BYTES, &mapK, kf, 64, m.g, tok + 64 * rank);
+                tma_3d_pair(b + 2 * KQ_BYTES, &mapV, kf, 64 * rank, m.g, tok);
+            }
+        }
+    } else if (warp == 1 && lane == 0 && rank == 0) {
+        // ------------------------------------------------ MMA issuer (leader, for both CTAs)
+        uint32_t it = 0;
+        bool ok = true;
+        auto issue_s2 = [&](uint32_t sd, uint64_t qd, uint64_t kd) {
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (kk & 3) * 32, half = kk >> 2;
+                umma_ss2(sd, qd + ((half * QH_BYTES + off) >> 4), kd + ((half * KQ_BYTES + off) >> 4), IDESC_S2,
+                         kk > 0 ? 1u : 0u);
+            }
+        };
+        for (int k = 0, tl = 0; ok && !abort_flag; ++k, ++tl) {
+            const int w = item_of(k);
+            if (w >= total) break;
+            Item m;
+            get_item(w, n_req, req_row_end, row_pos, row_tok, group, hkv, m);
+            const int qb = tl & 1;
+            if (!wait_cl(&q_full[qb], (tl >> 1) & 1, &abort_flag)) {
+                ok = false;
+                break;
+            }
+            pend_q[qb] = -1;
+            fence_after();
+            const uint64_t qd = desc_k(su32(sQ + qb * QT_BYTES));
+            // S of the item's first two blocks
+            for (int j = 0; j < 2 && j < m.nblk; ++j) {
+                const uint32_t g = it + j;
+                const int st = g % STAGES2;
+                if (!wait_cl(&kv_full[st], (g / STAGES2) & 1, &abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                pend_kv[st] = -1;
+                fence_after();
+                issue_s2(tb + (g & 1) * 128, qd, desc_k(su32(sKV + st * STAGE_BYTES)));
+                commit2(&s_full[g & 1]);
+            }
+            for (int kb = 0; kb < m.nblk && ok; ++kb, ++it) {
+                const int b = it & 1, st = it % STAGES2;
+                if (!wait_cl(&p_full[b], (it >> 1) & 1, &abort_flag) ||
+                    (kb == 0 && !wait_cl(&o_free, (tl & 1) ^ 1, &abort_flag))) {
+                    ok = false;
+                    break;
+                }
+                fence_after();
+                {
+                    const uint64_t vd = desc_mn(su32(sKV + st * STAGE_BYTES + 2 * KQ_BYTES));
+                    const uint32_t pa = tb + b * 128;
+#pragma unroll
+                    for (int kk = 0; kk < BKV / 16; ++kk)
+                        umma_ts2(tb + O_COL, pa + kk * 8, vd + ((kk * 2048) >> 4), IDESC_PV2,
+                                 (kb > 0 || kk > 0) ? 1u : 0u);
+                }
+                commit2(&pv_done);
+                commit2(&kv_empty[st]);  // S and P.V of this block are done with the stage
+                if (kb + 2 < m.nblk) {
+                    const uint32_t g = it + 2;
+                    const int st2 = g % STAGES2;
+                    if (!wait_cl(&kv_full[st2], (g / STAGES2) & 1, &abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    pend_kv[st2] = -1;
+                    fence_after();
+                    // into the buffer P(it) occupies: the tensor core runs it after P.V(it)
+                    issue_s2(tb + b * 128, qd, desc_k(su32(sKV + st2 * STAGE_BYTES)));
+                    commit2(&s_full[b]);
+                }
+            }
+            if (!ok) break;
+            commit2(&o_full);
+            commit2(&q_empty[qb]);
+        }
+        if (!ok) {
+            abort_flag = 1;
+            set_error(err, BLEND_ETIMEOUT);
+        }
+    } else if (warp >= 2) {
+        // ------------------------------------------------ softmax of this CTA's tile + output
+        const int sp = warp & 3;  // TMEM lane quarter of this warp
+        const int r_in = sp * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(sp * 32) << 16;
+        const uint32_t o_col = tb + lane_off + O_COL;
+        uint32_t it = 0;
+        bool ok = true;
+        for (int k = 0, tl = 0; ok; ++k, ++tl) {
+            const int w = item_of(k);
+            if (w >= total) break;
+            Item m;
+            get_item(w, n_req, req_row_end, row_pos, row_tok, group, hkv, m);
+            const int my_pair0 = rank == 0 ? m.pair0_a : m.pair0_b;
+            const bool have = my_pair0 >= 0;
+            const int p = (have ? my_pair0 : 0) + r_in;
+            const bool valid = have && p < m.npairs;
+            const int row = m.row0 + (valid ? p / group : 0);
+            const int my_pos = valid ? row_pos[row] : m.max_pos;
+            float m_used = -INFINITY, l = 0.f;
+            for (int kb = 0; kb < m.nblk; ++kb, ++it) {
+                const int b = it & 1;
+                const uint32_t s_col = tb + lane_off + b * 128;
+                if (!warp_wait_cl(&s_full[b], (it >> 1) & 1, &abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                fence_after();
+                const int k0 = kb * BKV;
+                uint32_t s[128];
+                TMEM_LD32(s_col, s);
+                TMEM_LD32(s_col + 32, (s + 32));
+                TMEM_LD32(s_col + 64, (s + 64));
+                TMEM_LD32(s_col + 96, (s + 96));
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                if (k0 + BKV - 1 > my_pos) {
+#pragma unroll
+                    for (int i = 0; i < 128; ++i)
+                        if (k0 + i > my_pos) s[i] = __float_as_uint(-INFINITY);
+                }
+                float mx;
+                {
+                    float a[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) a[i] = fmaxf(__uint_as_float(s[i]), __uint_as_float(s[i + 8]));
+#pragma unroll
+                    for (int i = 16; i < 128; i += 16)
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) a[c] = max3f(a[c], __uint_as_float(s[i + c]), __uint_as_float(s[i + 8 + c]));
+                    mx = max3f(max3f(a[0], a[1], a[2]), max3f(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
+                }
+                const float mxs = mx * scale_log2;
+                const bool need = mxs > m_used + RESCALE_LOG2;
+                const bool rescale = __any_sync(0xffffffffu, need);
+                float corr = 1.f;
+                if (rescale) {
+                    const float m_new = need ? mxs : m_used;
+                    corr = ex2(m_used - m_new);
+                    l *= corr;
+                    m_used = m_new;
+                }
+                float2 acc2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                const float2 sc2 = make_float2(scale_log2, scale_log2), nm2 = make_float2(-m_used, -m_used);
+#pragma unroll
+                for (int e = 0; e < 64; ++e) {
+                    const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1])), sc2, nm2);
+                    const float p0 = ex2(x.x), p1 = ex2(x.y);
+                    acc2[e & 1] = __fadd2_rn(acc2[e & 1], make_float2(p0, p1));
+                    s[e] = pack_bf16x2(p0, p1);
+                }
+                const float2 accs = __fadd2_rn(acc2[0], acc2[1]);
+                TMEM_ST32(s_col, s);
+                TMEM_ST32(s_col + 32, (s + 32));
+                if (rescale && kb > 0) {
+                    // O must hold every block before this one: wait for the previous P.V
+                    if (!warp_wait_cl(&pv_done, (it - 1) & 1, &abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_after();
+#pragma unroll
+                    for (int c = 0; c < D; c += 32) {
+                        uint32_t o[32];
+                        TMEM_LD32(o_col + c, o);
+                        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
+                        TMEM_ST32(o_col + c, o);
+                    }
+                }
+                l += accs.x + accs.y;
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                fence_before();
+                warp_arrive_leader(&p_full[b]);
+            }
+            if (!ok) break;
+            // O of this tile is final once the item's last P.V has completed
+            if (!warp_wait_cl(&o_full, tl & 1, &abort_flag)) {
+                ok = false;
+                break;
+            }
+            fence_after();
+            const float inv = 1.f / l;
+            bf16* dst = out + (long long)row * (hkv * group * D) + (long long)(m.g * group + (valid ? p % group : 0)) * D;
+#pragma unroll
+            for (int c = 0; c < D; c += 32) {
+                uint32_t o[32];
+                TMEM_LD32(o_col + c, o);
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                if (valid) {
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        uint32_t w4[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            w4[e] = pack_bf16x2(__uint_as_float(o[v * 8 + 2 * e]) * inv,
+                                                __uint_as_float(o[v * 8 + 2 * e + 1]) * inv);
+                        *reinterpret_cast<uint4*>(dst + c + v * 8) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                    }
+                }
+            }
+            fence_before();
+            warp_arrive_leader(&o_free);
+        }
+        if (!ok) {
+            abort_flag = 1;
+            if (lane == 0) set_error(err, BLEND_ETIMEOUT);
+        }
+    }
+    fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0 && abort_flag && rank == 0) {
+        // let the copies still in flight land (both CTAs' bytes count on these barriers)
+        for (int s = 0; s < STAGES2; ++s)
+            if (pend_kv[s] >= 0)
+                for (long long i = 0; i < SPIN_LIMIT && !mbar_try(&kv_full[s], (uint32_t)pend_kv[s]); ++i) {
+                }
+        for (int b = 0; b < 2; ++b)
+            if (pend_q[b] >= 0)
+                for (long long i = 0; i < SPIN_LIMIT && !mbar_try(&q_full[b], (uint32_t)pend_q[b]); ++i) {
+                }
+    }
+    __syncthreads();
+    cluster_sync();  // neither CTA leaves while the other may still signal its barriers
+    if (warp == 1) {
+        fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tb), "r"(COLS2) : "memory");
+    }
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 g_enc = nullptr;
 int g_sms = 0;
 
@@ -610,6 +1072,60 @@ int launch_attn_d(const void* q, int m_cap, int n_req, const int32_t* req_row_en
     return BLEND_OK;
 }
 
+// D = 128 on CTA pairs: clusters of two CTAs, one tile each (k_attn_pair).  Returns
+// BLEND_EUNSUPPORTED when no cluster of two such CTAs fits on the device.
+int launch_attn_pair(const void* q, int m_cap, int n_req, const int32_t* req_row_end, const int32_t* row_pos,
+                     const int32_t* row_tok, int M_max, const void* k_cache, const void* v_cache, long long n_tokens,
+                     void* o, int hq, int hkv, int32_t* err, cudaStream_t s) {
+    constexpr int D = 128;
+    static int max_clusters = -1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(pairk::THREADS2);
+    cfg.dynamicSmemBytes = pairk::SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    if (max_clusters < 0) {
+        cudaFuncSetAttribute(k_attn_pair, cudaFuncAttributeMaxDynamicSharedMemorySize, pairk::SMEM_BYTES);
+        cfg.gridDim = dim3(g_sms);
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, k_attn_pair, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            n = 0;
+        }
+        max_clusters = n < g_sms / 2 ? n : g_sms / 2;
+    }
+    if (max_clusters <= 0) return BLEND_EUNSUPPORTED;
+    const int group = hq / hkv;
+    CUtensorMap mq, mk, mv;
+    cuuint64_t qd[2] = {(cuuint64_t)D, (cuuint64_t)hkv * m_cap * group};
+    cuuint64_t qs[1] = {(cuuint64_t)D * 2};
+    cuuint32_t qb[2] = {64, BQ};
+    cuuint64_t kd[3] = {(cuuint64_t)D, (cuuint64_t)hkv, (cuuint64_t)n_tokens};
+    cuuint64_t ks[2] = {(cuuint64_t)D * 2, (cuuint64_t)hkv * D * 2};
+    cuuint32_t kbx[3] = {64, 1, 64};   // this CTA's 64 keys of a block, one d half
+    cuuint32_t vbx[3] = {64, 1, BKV};  // all 128 keys of a block, this CTA's d half
+    if (!encode(&mq, 2, q, qd, qs, qb) || !encode(&mk, 3, k_cache, kd, ks, kbx) || !encode(&mv, 3, v_cache, kd, ks, vbx))
+        return BLEND_EUNSUPPORTED;
+    const long long tiles = (((long long)M_max * group) + BQ - 1) / BQ + n_req;
+    const long long items = (long long)hkv * ((tiles + 1) / 2 + n_req);
+    const int clusters = (int)(items < max_clusters ? items : max_clusters);
+    cfg.gridDim = dim3(2 * clusters);
+    const float scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));  // log2(e) / sqrt(d)
+    if (cudaLaunchKernelEx(&cfg, k_attn_pair, mq, mk, mv, n_req, req_row_end, row_pos, row_tok, group, hkv, m_cap,
+                           scale_log2, (bf16*)o, err) != cudaSuccess) {
+        cudaGetLastError();  // a configuration the device refuses: the single-CTA kernel takes over
+        return BLEND_EUNSUPPORTED;
+    }
+    note_launch(1);
+    return BLEND_OK;
+}
+
 int launch_attn_tc(const void* q, int m_cap, int n_req, const int32_t* req_row_end, const int32_t* row_pos,
                    const int32_t* row_tok, int M_max, const void* k_cache, const void* v_cache, long long n_tokens,
                    void* o, int hq, int hkv, int head_dim, int32_t* err, cudaStream_t s) {
@@ -631,9 +1147,13 @@ int launch_attn_tc(const void* q, int m_cap, int n_req, const int32_t* req_row_e
     if (head_dim == 64)
         return launch_attn_d<64>(q, m_cap, n_req, req_row_end, row_pos, row_tok, M_max, k_cache, v_cache, n_tokens,
                                  o, hq, hkv, err, s);
-    if (head_dim == 128)
+    if (head_dim == 128) {
+        const int rc = launch_attn_pair(q, m_cap, n_req, req_row_end, row_pos, row_tok, M_max, k_cache, v_cache,
+                                        n_tokens, o, hq, hkv, err, s);
+        if (rc != BLEND_EUNSUPPORTED) return rc;
         return launch_attn_d<128>(q, m_cap, n_req, req_row_end, row_pos, row_tok, M_max, k_cache, v_cache, n_tokens,
                                   o, hq, hkv, err, s);
+    }
     return BLEND_EUNSUPPORTED;
 }
 

@@ -169,10 +169,13 @@ __device__ __forceinline__ void umma_commit_pair(uint64_t* bar) {
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
 }
-__device__ __forceinline__ bool mbar_try_cluster(uint64_t* b, uint32_t parity) {
+// Non-blocking test of the phase at cluster scope: a blocking try_wait on a barrier that
+// the other CTA signals was measured to resume up to ~1.5 K cycles after the phase
+// completed.
+__device__ __forceinline__ bool mbar_test_cluster(uint64_t* b, uint32_t parity) {
     uint32_t ok;
     asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}\n"
         : "=r"(ok)
         : "r"(su32(b)), "r"(parity)
@@ -180,13 +183,13 @@ __device__ __forceinline__ bool mbar_try_cluster(uint64_t* b, uint32_t parity) {
     return ok != 0;
 }
 // Bounded wait for the phase of parity `parity`; false if it did not complete in time or
-// another role gave up.  PAIR waits acquire at cluster scope (the other CTA's arrivals
-// and copies).
+// another role gave up.  PAIR polls at cluster scope (the other CTA's arrivals and copies).
 template <bool PAIR>
 __device__ __forceinline__ bool mbar_wait_t(uint64_t* b, uint32_t parity, volatile int* abort_flag) {
-    for (long long i = 0; i < SPIN_LIMIT; ++i) {
-        if (PAIR ? mbar_try_cluster(b, parity) : mbar_try(b, parity)) return true;
-        if ((i & 255) == 255 && *abort_flag) return false;
+    const long long limit = PAIR ? 64 * SPIN_LIMIT : SPIN_LIMIT;
+    for (long long i = 0; i < limit; ++i) {
+        if (PAIR ? mbar_test_cluster(b, parity) : mbar_try(b, parity)) return true;
+        if ((i & 1023) == 1023 && *abort_flag) return false;
     }
     return false;
 }
