@@ -582,8 +582,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 //                 B: each CTA's 64 d columns of V, MN-major)
 // S is double-buffered in TMEM: S(j+1) is issued before P(j) is ready and S(j+2) right
 // after P.V(j), so a softmax goes from block to block without waiting for the tensor
-// core.  The completion of every P.V is committed, and a softmax that must rescale O
-// (running maximum up by more than 2^8) first waits for the previous block's P.V.  The
+// core.  A softmax that must rescale O (running maximum up by more than 2^8) first waits
+// for the previous block's P.V, whose completion releases that block's K/V stage.  The
 // softmax is the single-tile one of k_attn_tc, one pair row per thread.
 namespace pairk {
 constexpr int THREADS2 = 192;  // warp 0 TMA, 1 TMEM + MMA issue (leader), 2..5 softmax
@@ -684,11 +684,17 @@ __device__ __forceinline__ bool warp_wait_cl(uint64_t* b, uint32_t par, volatile
     }
     return false;
 }
-// warp-level release-arrive on the leader's barrier (remote for rank 1)
-__device__ __forceinline__ void warp_arrive_leader(uint64_t* b) {
+// Warp-level arrive on the leader's barrier: local in the leader, remote from rank 1
+// (default semantics: a cluster-scope release here was measured to cost ~1 K cycles per
+// block; the TMEM stores it follows are complete by tcgen05.wait::st).
+__device__ __forceinline__ void warp_arrive_leader(uint64_t* b, int rank) {
     __syncwarp();
-    if ((threadIdx.x & 31) == 0)
-        asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(leader_addr(b)) : "memory");
+    if ((threadIdx.x & 31) == 0) {
+        if (rank == 0)
+            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
+        else
+            asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(leader_addr(b)) : "memory");
+    }
 }
 }  // namespace pairk
 
@@ -701,7 +707,7 @@ __global__ void __launch_bounds__(pairk::THREADS2, 1)
     constexpr int D = 128;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t q_full[2], q_empty[2], kv_full[STAGES2], kv_empty[STAGES2], s_full[2],
-        p_full[2], pv_done, o_full, o_free;
+        p_full[2], o_full, o_free;
     __shared__ uint32_t tmem_sh;
     __shared__ volatile int abort_flag;
     __shared__ int pend_kv[STAGES2];
@@ -737,7 +743,6 @@ __global__ void __launch_bounds__(pairk::THREADS2, 1)
             mbar_init(&kv_empty[s], 1);
             pend_kv[s] = -1;
         }
-        mbar_init(&pv_done, 1);
         mbar_init(&o_full, 1);
         mbar_init(&o_free, 8);
         abort_flag = 0;
@@ -859,7 +864,6 @@ __global__ void __launch_bounds__(pairk::THREADS2, 1)
                         umma_ts2(tb + O_COL, pa + kk * 8, vd + ((kk * 2048) >> 4), IDESC_PV2,
                                  (kb > 0 || kk > 0) ? 1u : 0u);
                 }
-                commit2(&pv_done);
                 commit2(&kv_empty[st]);  // S and P.V of this block are done with the stage
                 if (kb + 2 < m.nblk) {
                     const uint32_t g = it + 2;
@@ -958,7 +962,10 @@ __global__ void __launch_bounds__(pairk::THREADS2, 1)
                 TMEM_ST32(s_col + 32, (s + 32));
                 if (rescale && kb > 0) {
                     // O must hold every block before this one: wait for the previous P.V
-                    if (!warp_wait_cl(&pv_done, (it - 1) & 1, &abort_flag)) {
+                    // (the previous block's stage is released when its P.V completes, at most
+                    // one use of that stage behind)
+                    const uint32_t pv = it - 1;
+                    if (!warp_wait_cl(&kv_empty[pv % STAGES2], (pv / STAGES2) & 1, &abort_flag)) {
                         ok = false;
                         break;
                     }
@@ -976,7 +983,7 @@ __global__ void __launch_bounds__(pairk::THREADS2, 1)
                 l += accs.x + accs.y;
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 fence_before();
-                warp_arrive_leader(&p_full[b]);
+                warp_arrive_leader(&p_full[b], rank);
             }
             if (!ok) break;
             // O of this tile is final once the item's last P.V has completed
@@ -1005,7 +1012,7 @@ __global__ void __launch_bounds__(pairk::THREADS2, 1)
                 }
             }
             fence_before();
-            warp_arrive_leader(&o_free);
+            warp_arrive_leader(&o_free, rank);
         }
         if (!ok) {
             abort_flag = 1;
