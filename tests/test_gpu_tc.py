@@ -36,6 +36,12 @@ SHAPES = [
     (synth.ModelShape("tc-gqa5", 2, 1280, 10, 2, 128, 2560, 300, 1e6), 700, 4000),
     # SmolLM2-135M widths: projections of 960 and 576 columns end in partial 256-wide tiles
     (synth.ModelShape("tc-smol", 2, 576, 9, 3, 64, 1536, 300, 1e5), 500, 900),
+    # CTA pairs at their edges: 90 rows x 4 heads = 3 attention tiles per kv head, so the
+    # last item has no second tile; 129 rows put one live row in the second CTA of a 256-row
+    # GEMM tile; 257 rows leave the second 256-row tile one row
+    (synth.ModelShape("tc-pair-odd", 2, 512, 8, 2, 128, 1024, 300, 1e6), 90, 300),
+    (synth.ModelShape("tc-pair-129", 2, 512, 8, 2, 128, 1024, 300, 1e6), 129, 500),
+    (synth.ModelShape("tc-pair-257", 2, 1280, 10, 2, 128, 2560, 300, 1e6), 257, 2000),
 ]
 
 
