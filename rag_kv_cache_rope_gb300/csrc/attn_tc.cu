@@ -582,12 +582,13 @@ __global__ void __launch_bounds__(THREADS, 1)
 //                 B: each CTA's 64 d columns of V, MN-major)
 // S is double-buffered in TMEM: S(j+1) is issued before P(j) is ready and S(j+2) right
 // after P.V(j), so a softmax goes from block to block without waiting for the tensor
-// core.  A softmax that must rescale O (running maximum up by more than 2^8) first waits
+// core.  One commit after P.V(j) and S(j+2) both releases block j's K/V stage and tells
+// the softmax that S(j+2) is there (an item's first two S products have their own).  A softmax that must rescale O (running maximum up by more than 2^8) first waits
 // for the previous block's P.V, whose completion releases that block's K/V stage.  The
 // softmax is the single-tile one of k_attn_tc, one pair row per thread.
 namespace pairk {
 constexpr int THREADS2 = 192;  // warp 0 TMA, 1 TMEM + MMA issue (leader), 2..5 softmax
-constexpr int STAGES2 = 4;
+constexpr int STAGES2 = 5;
 constexpr int KQ_BYTES = 64 * 64 * 2;                  // 64 keys x one 64-wide d half
 constexpr int VH_BYTES = BKV * 64 * 2;                 // 128 keys x this CTA's 64 d columns
 constexpr int STAGE_BYTES = 2 * KQ_BYTES + VH_BYTES;   // 32 KB
@@ -864,7 +865,6 @@ __global__ void __launch_bounds__(pairk::THREADS2, 1)
                         umma_ts2(tb + O_COL, pa + kk * 8, vd + ((kk * 2048) >> 4), IDESC_PV2,
                                  (kb > 0 || kk > 0) ? 1u : 0u);
                 }
-                commit2(&kv_empty[st]);  // S and P.V of this block are done with the stage
                 if (kb + 2 < m.nblk) {
                     const uint32_t g = it + 2;
                     const int st2 = g % STAGES2;
@@ -876,8 +876,9 @@ __global__ void __launch_bounds__(pairk::THREADS2, 1)
                     fence_after();
                     // into the buffer P(it) occupies: the tensor core runs it after P.V(it)
                     issue_s2(tb + b * 128, qd, desc_k(su32(sKV + st2 * STAGE_BYTES)));
-                    commit2(&s_full[b]);
                 }
+                // completes with P.V(it) and S(it + 2): block it's stage is free, S(it + 2) ready
+                commit2(&kv_empty[st]);
             }
             if (!ok) break;
             commit2(&o_full);
@@ -894,6 +895,7 @@ __global__ void __launch_bounds__(pairk::THREADS2, 1)
         const uint32_t lane_off = (uint32_t)(sp * 32) << 16;
         const uint32_t o_col = tb + lane_off + O_COL;
         uint32_t it = 0;
+        uint32_t s_uses0 = 0, s_uses1 = 0;  // completions of s_full[0], [1] so far (an item's first two S)
         bool ok = true;
         for (int k = 0, tl = 0; ok; ++k, ++tl) {
             const int w = item_of(k);
@@ -910,7 +912,18 @@ __global__ void __launch_bounds__(pairk::THREADS2, 1)
             for (int kb = 0; kb < m.nblk; ++kb, ++it) {
                 const int b = it & 1;
                 const uint32_t s_col = tb + lane_off + b * 128;
-                if (!warp_wait_cl(&s_full[b], (it >> 1) & 1, &abort_flag)) {
+                bool got;
+                if (kb < 2) {
+                    got = warp_wait_cl(&s_full[b], (b ? s_uses1 : s_uses0) & 1, &abort_flag);
+                    if (b) ++s_uses1;
+                    else ++s_uses0;
+                } else {
+                    // S(it) came with the commit after P.V(it - 2) (at most one use of that
+                    // stage behind)
+                    const uint32_t pv = it - 2;
+                    got = warp_wait_cl(&kv_empty[pv % STAGES2], (pv / STAGES2) & 1, &abort_flag);
+                }
+                if (!got) {
                     ok = false;
                     break;
                 }
