@@ -84,7 +84,7 @@ struct blend_handle {
     uint8_t* mask;
     float* dev[2];
     int32_t* scratch_n;
-    float2* aux_stats;   // aux_attention_scores: softmax (max, sum) per query row and head
+    float2* aux_stats;   // aux_attention_scores: softmax (max, sum) per query row, head and key span
     float* ssq;          // folded RMSNorm: per-row partial sums of squares [rows][ssq_parts]
     bool xn_scaled = false;  // xn holds bf16(x * g) of the next layer's attention norm, ssq its partials
     int ssq_parts = 0;
@@ -259,7 +259,7 @@ Layout make_layout(const blend_model_cfg* c, const blend_limits* l) {
     L.add(nc * 4);                                         // 31 dev1
     L.add(nc * 4);                                         // 32 dev2
     L.add(16);                                             // 33 scratch count
-    L.add(M * (size_t)c->n_q_heads * sizeof(float2));      // 34 aux score row statistics
+    L.add(M * (size_t)c->n_q_heads * tc_score_spans(l->max_tokens) * sizeof(float2));  // 34 aux score row statistics
     for (int b = 0; b < 4; ++b)                            // 35..38 host-pool staging: K, V x 2 buffers
         L.add((size_t)l->max_tokens * kvd * es);
     L.add(M * NORM_PARTS_MAX * sizeof(float));             // 39 folded-RMSNorm partial sums of squares
@@ -1201,7 +1201,7 @@ extern "C" int blend_prefill(blend_handle* h, int32_t n_req, const blend_request
                 launch_gather_qlast(c.dtype, h->q, h->lim.max_rows, c.n_q_heads / c.n_kv_heads, c.n_kv_heads,
                                     c.head_dim, bd, h->plan[cur].req_row_end, h->o, qo, s);
                 launch_aux_scores(c.dtype, h->o, kc, bd, c.n_q_heads, c.n_kv_heads, c.head_dim, qo, max_nc,
-                                  h->aux_stats, h->dev[0], s);
+                                  h->aux_stats, tc_score_spans(h->lim.max_tokens), h->dev[0], h->err, h->use_tc != 0, s);
                 launch_focus_filter(bd, ft, h->dev[0], reqs[0].focus_bp, h->set[0], h->set_n[0], h->set[1],
                                     h->set_n[1], s);
             }
@@ -1276,6 +1276,7 @@ extern "C" int aux_attention_scores(blend_handle* h, int32_t n_req, const blend_
     const size_t layer_elems = (size_t)tok * c.n_kv_heads * c.head_dim;
     const void* k_last = (const char*)out->k + (size_t)(c.n_layers - 1) * layer_elems * elem_size(c.dtype);
     launch_aux_scores(c.dtype, out->q_last, k_last, bd, c.n_q_heads, c.n_kv_heads, c.head_dim, qo, max_nc,
-                      h->aux_stats, scores, (cudaStream_t)stream);
+                      h->aux_stats, tc_score_spans(h->lim.max_tokens), scores, h->err, h->use_tc != 0,
+                      (cudaStream_t)stream);
     return check_cuda(h, "aux_attention_scores");
 }

@@ -5,8 +5,8 @@
 // only the query rows are computed, over the chunk's cached rows); it leaves the last
 // layer's keys in the blended cache and, on request, the query rows' last-layer q.
 //
-// Two passes, both on CUDA cores (the work is ~Q x hq x N_c dot products of length d,
-// far below a tensor-core problem):
+// bf16 models with head_dim 64 or 128 take the tensor-core form of these two passes
+// (score_tc.cu); the CUDA-core passes below serve the rest:
 //   k_aux_row_stats : per (query row, head) the softmax maximum m and sum l over every key
 //                     the row sees (prefix, chunk and the query rows up to itself); one
 //                     warp per (row, head), lane j takes keys j, j+32, ..., then a fixed
@@ -228,8 +228,16 @@ void aux_scores_t(const void* q_last, const void* K, const BatchDesc& bd, int hq
 }
 
 void launch_aux_scores(int dtype, const void* q_last, const void* K, const BatchDesc& bd, int hq, int hkv, int d,
-                       int n_qrows, int max_nc, float2* stats, float* scores, cudaStream_t s) {
+                       int n_qrows, int max_nc, float2* stats, int n_spans, float* scores, int32_t* err,
+                       bool tensor_cores, cudaStream_t s) {
     if (n_qrows <= 0 || max_nc <= 0) return;
+    if (dtype == BLEND_BF16 && tensor_cores) {
+        // tensor cores where they apply (score_tc.cu), else the CUDA-core passes below
+        const ReqDesc& last = bd.r[bd.n_req - 1];
+        const long long n_tokens = (long long)last.tok_off + last.P + last.n_c + last.Q;
+        if (launch_scores_tc(q_last, K, n_tokens, bd, hq, hkv, d, n_spans, stats, scores, err, s) == BLEND_OK)
+            return;
+    }
     if (dtype == BLEND_BF16) {
         if (d == 64) aux_scores_t<bf16, 64>(q_last, K, bd, hq, hkv, n_qrows, max_nc, stats, scores, s);
         else aux_scores_t<bf16, 128>(q_last, K, bd, hq, hkv, n_qrows, max_nc, stats, scores, s);

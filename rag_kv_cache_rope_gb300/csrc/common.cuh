@@ -207,8 +207,18 @@ void launch_span_finish(const SelectBatch& sb, const int32_t* rank_scratch, int 
 // slab, then per chunk column the mean attention weight over query rows and heads.
 void launch_gather_qlast(int dtype, const void* qslab, int m_cap, int group, int hkv, int d, const BatchDesc& bd,
                          const int32_t* req_row_end, void* q_last, int n_qrows, cudaStream_t s);
+// stats: n_qrows * hq * n_spans pairs of floats (score_spans(max_tokens) spans per row
+// and head for the tensor-core path, one for the CUDA-core path).
 void launch_aux_scores(int dtype, const void* q_last, const void* K, const BatchDesc& bd, int hq, int hkv, int d,
-                       int n_qrows, int max_nc, float2* stats, float* scores, cudaStream_t s);
+                       int n_qrows, int max_nc, float2* stats, int n_spans, float* scores, int32_t* err,
+                       bool tensor_cores, cudaStream_t s);
+// Tensor-core form of the same two passes (score_tc.cu): bf16, head_dim 64 or 128.
+// Returns BLEND_EUNSUPPORTED when it cannot run here.
+int launch_scores_tc(const void* q_last, const void* K, long long n_tokens, const BatchDesc& bd, int hq, int hkv,
+                     int d, int n_spans, float2* part, float* scores, int32_t* err, cudaStream_t s);
+// Key spans per (query row, head) the tensor-core statistics pass writes for contexts of
+// up to max_tokens tokens.
+int tc_score_spans(long long max_tokens);
 // SpecCache 2.4: sorted distinct union of [a_start[i], a_end[i]) over the selected i.
 void launch_align_expand(const int32_t* sel, const int32_t* n_sel, int32_t max_sel, int32_t sel_base,
                          const int32_t* a_start, const int32_t* a_end, int32_t n_spec, int32_t n_target,
