@@ -46,11 +46,18 @@ def _outputs(sh, lens, P, Q, dev):
                         q_last=torch.zeros(n_req * Q, sh.n_q_heads, sh.head_dim, dtype=dt, device=dev))
 
 
-@pytest.mark.parametrize("dtype,d", [("f32", 64), ("bf16", 64), ("bf16", 128)])
-def test_column_mean_kernel_matches_oracle(dtype, d):
+# (dtype, d, P, chunk lengths, Q): short contexts, then contexts of several 1024-key spans
+# per row (the tensor-core statistics pass merges span partials) with more than 128
+# (row, head) pairs per kv head
+COLMEAN_CASES = [("f32", 64, 7, [40, 95, 33], 12), ("bf16", 64, 7, [40, 95, 33], 12),
+                 ("bf16", 128, 7, [40, 95, 33], 12), ("bf16", 128, 64, [2500, 700], 40),
+                 ("bf16", 64, 33, [1100, 3000, 9], 50)]
+
+
+@pytest.mark.parametrize("dtype,d,P,lens,Q", COLMEAN_CASES)
+def test_column_mean_kernel_matches_oracle(dtype, d, P, lens, Q):
     hq, hkv = (9, 3) if d == 64 else (8, 2)
     sh = synth.ModelShape("aux-k", 1, hq * d if d == 64 else 1024, hq, hkv, d, 1536, 64, 1e4, dtype=dtype)
-    P, lens, Q = 7, [40, 95, 33], 12
     case = make_case(sh, P, lens, pool="random")
     dev = torch.device("cuda:0")
     N = sum(P + n + Q for n in lens)
