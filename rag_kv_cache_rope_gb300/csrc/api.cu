@@ -96,6 +96,7 @@ struct blend_handle {
     cudaEvent_t ev_free[2] = {nullptr, nullptr};
     std::vector<cudaEvent_t> ev_layer;
     int use_tc;  // tensor-core GEMM for bf16
+    float* split_ws;  // tensor-core GEMM: K-half partials of last-wave tiles
     int host_rc = 0;  // first failure of an internal launch during the current call
     std::string last_error;
     // profiler
@@ -260,9 +261,10 @@ Layout make_layout(const blend_model_cfg* c, const blend_limits* l) {
     L.add(nc * 4);                                         // 32 dev2
     L.add(16);                                             // 33 scratch count
     L.add(M * (size_t)c->n_q_heads * tc_score_spans(l->max_tokens) * sizeof(float2));  // 34 aux score row statistics
-    for (int b = 0; b < 4; ++b)                            // 35..38 host-pool staging: K, V x 2 buffers
+    L.add(c->dtype == BLEND_BF16 ? GEMM_SPLIT_WS_FLOATS * 4 : 0);  // 35 GEMM split partials
+    for (int b = 0; b < 4; ++b)                            // 36..39 host-pool staging: K, V x 2 buffers
         L.add((size_t)l->max_tokens * kvd * es);
-    L.add(M * NORM_PARTS_MAX * sizeof(float));             // 39 folded-RMSNorm partial sums of squares
+    L.add(M * NORM_PARTS_MAX * sizeof(float));             // 40 folded-RMSNorm partial sums of squares
     return L;
 }
 
@@ -296,8 +298,8 @@ bool gemm_on_tc(const blend_handle* h, int K, int N, int epi, int ldc) {
 void gemm(blend_handle* h, const void* A, int K, const void* B, int N, int epi, void* C, int ldc,
           const int32_t* M_dev, int M_max, cudaStream_t s, const NormEpi* ne = nullptr) {
     if (gemm_on_tc(h, K, N, epi, ldc)) {
-        int rc = launch_gemm_tc(A, K, h->lim.max_rows, B, N, M_dev, M_max, epi, C, ldc, h->err, s, nullptr, true,
-                                ne);
+        int rc = launch_gemm_tc(A, K, h->lim.max_rows, B, N, M_dev, M_max, epi, C, ldc, h->err, s, nullptr,
+                                h->split_ws, ne);
         if (rc != BLEND_OK && h->host_rc == BLEND_OK) h->host_rc = rc;
     } else
         launch_gemm_simt(h->cfg.dtype, A, K, B, K, K, N, M_dev, M_max, epi, C, ldc, s);
@@ -401,7 +403,7 @@ void layer_kv(blend_handle* h, int l, const float* x, const Plan& p, const int32
         QkvEpi qe{p.row_pos, p.row_tok, h->rope, (bf16*)h->q, (bf16*)kc, (bf16*)vc, h->lim.max_rows,
                   c.n_q_heads / c.n_kv_heads, c.n_q_heads, c.n_kv_heads};
         int rc = launch_gemm_tc(h->xn, H, h->lim.max_rows, lw.w_qkv, width, p.M, M_max, EPI_QKV_ROPE, nullptr, 0,
-                                h->err, s, &qe, false, &cons);
+                                h->err, s, &qe, nullptr, &cons);
         if (rc != BLEND_OK && h->host_rc == BLEND_OK) h->host_rc = rc;
         return;
     }
@@ -478,6 +480,8 @@ int blend_init(const blend_model_cfg* cfg, const blend_weights* w, const blend_l
     h->dev[1] = (float*)(b + L.off[i++]);
     h->scratch_n = (int32_t*)(b + L.off[i++]);
     h->aux_stats = (float2*)(b + L.off[i++]);
+    h->split_ws = cfg->dtype == BLEND_BF16 ? (float*)(b + L.off[i]) : nullptr;
+    ++i;
     for (int q = 0; q < 4; ++q) h->stage[q] = b + L.off[i++];
     h->ssq = (float*)(b + L.off[i++]);
     h->use_tc = cfg->dtype == BLEND_BF16 ? tc_available() : 0;

@@ -12,10 +12,12 @@
 // Two 256-column fp32 accumulators (all 512 TMEM columns) let the epilogue of one tile
 // overlap the main loop of the next.  M is read from the device; tiles past it are
 // skipped.
-// Tail split: tiles are dealt to the persistent CTAs in waves of gridDim.x.  When the
-// last wave is at most half full, each of its tiles is cut into two column halves
-// (N = BN/2 MMAs over the whole K) run by two CTAs, so that wave takes half a tile's
-// time and each half runs its own epilogue: no partial sums, no CTA waits for another.
+// Tail split: tiles are dealt to the persistent CTAs (or CTA pairs) in waves.  When the
+// last wave is at most half full, each of its tiles is cut into two K halves run by two
+// units, so that wave takes half a tile's time.  Each half stores its raw fp32 partial
+// tile to a workspace with tensor stores; k_split_combine then adds the two partials in
+// a fixed order and runs the tile's epilogue (no CTA waits for another; column halves
+// were measured to take as long as whole tiles).
 // Residual-add epilogues of warps whose 32 rows are all live stage each 32-column chunk
 // in shared memory and leave it as tensor stores.  Every mbarrier wait is bounded: on
 // expiry the kernel records BLEND_ETIMEOUT in the error word, stops issuing work, drains
@@ -45,20 +47,21 @@ template <int BN, bool PAIR = false> struct TileCfg {
     static constexpr int STAGES = (PAIR || BN != 256) ? 6 : 4;
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;  // + alignment slack
-    // kind::f16 instruction descriptors: bf16 A and B (K-major), fp32 D, M = TM, N = BN for
-    // a whole tile and N = BN/2 for a column half of a split tile
+    // kind::f16 instruction descriptor: bf16 A and B (K-major), fp32 D, M = TM, N = BN
     static constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((BN >> 3) << 17) | ((TM >> 4) << 24);
-    static constexpr uint32_t IDESC_H =
-        (1u << 4) | (1u << 7) | (1u << 10) | (((BN / 2) >> 3) << 17) | ((TM >> 4) << 24);
 };
 // Residual-add epilogue staging: per epilogue warp one 32-row x 32-column chunk of the
 // fp32 sum (4 KB, 128-byte swizzle) and of bf16(x * g) (2 KB, 64-byte swizzle), which the
 // TMA unit stores while the warp computes the next chunk.
 constexpr int OUT_F32_BYTES = 32 * 32 * 4;
 constexpr int OUT_WARP_BYTES = OUT_F32_BYTES + 32 * 32 * 2;
+// staging for the residual-add epilogue and for the partials of split tiles
 template <int EPI, int BN, bool PAIR = false> constexpr int smem_bytes() {
-    return TileCfg<BN, PAIR>::SMEM_BYTES + (EPI == EPI_ADD_F32 ? 4 * OUT_WARP_BYTES : 0);
+    return TileCfg<BN, PAIR>::SMEM_BYTES + (EPI != EPI_QKV_ROPE ? 4 * OUT_WARP_BYTES : 0);
 }
+// Split-tile workspace: up to GEMM_SPLIT_SMS / 2 split tiles, two K halves each, of
+// 128 x 256 fp32 per 128-row block (a CTA pair's tile has two).
+constexpr int GEMM_SPLIT_SMS = 160;
 
 __device__ __forceinline__ uint32_t su32(const void* p) {
     return (uint32_t)__cvta_generic_to_shared(p);
@@ -196,9 +199,10 @@ __device__ __forceinline__ bool mbar_wait_t(uint64_t* b, uint32_t parity, volati
     return false;
 }
 
-// Work unit u -> tile and, for a unit of a split tile, which column half (-1: whole tile).
+// Work unit u -> tile, its K-block range and, for a unit of a split tile, which K half
+// (-1: whole tile) and the split tile's index.
 struct Unit {
-    int t, half;
+    int t, half, sidx, k0, k1;
 };
 struct Sched {
     int full;   // units dealt as whole tiles
@@ -213,15 +217,21 @@ __device__ __forceinline__ Sched make_sched(int n_total, int grid, bool can_spli
     sc.units = sc.full + 2 * sc.split;
     return sc;
 }
-__device__ __forceinline__ Unit unit_of(int u, const Sched& sc) {
+__device__ __forceinline__ Unit unit_of(int u, const Sched& sc, int kblocks) {
     Unit r;
     if (u < sc.full) {
         r.t = u;
         r.half = -1;
+        r.sidx = -1;
+        r.k0 = 0;
+        r.k1 = kblocks;
     } else {
         const int v = u - sc.full;
-        r.t = sc.full + (v >> 1);
+        r.sidx = v >> 1;
+        r.t = sc.full + r.sidx;
         r.half = v & 1;
+        r.k0 = r.half ? kblocks / 2 : 0;
+        r.k1 = r.half ? kblocks : kblocks / 2;
     }
     return r;
 }
@@ -381,13 +391,32 @@ __device__ __forceinline__ void add_chunk_tma(const uint32_t* r, const float4* x
     }
 }
 
+// Raw fp32 partial of 32 accumulator columns of the warp's 32 rows (a K half of a split
+// tile) through the warp's staging chunk into the split workspace (tensor store).
+__device__ __forceinline__ void part_chunk_tma(const uint32_t* r, int ws_row0, int col, uint8_t* cb,
+                                               const CUtensorMap* mapW) {
+    const int lane = threadIdx.x & 31;
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+    __syncwarp();
+    uint8_t* rowp = cb + lane * 128;
+#pragma unroll
+    for (int v = 0; v < 8; ++v)
+        *reinterpret_cast<uint4*>(rowp + ((v ^ (lane & 7)) << 4)) = make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) {
+        tma_store_2d(mapW, cb, col, ws_row0);
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    }
+}
+
 template <int EPI, int BN, bool PAIR>
 __global__ void __launch_bounds__(THREADS, 1)
-    k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
-              const __grid_constant__ CUtensorMap mapBh, int K, int N, const int32_t* __restrict__ M_dev,
+    k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB, int K, int N,
+              const int32_t* __restrict__ M_dev,
               void* __restrict__ Cv, int ldc, int32_t* __restrict__ err, const __grid_constant__ QkvEpi qe,
               int can_split, const __grid_constant__ NormEpi ne, const __grid_constant__ CUtensorMap mapC,
-              const __grid_constant__ CUtensorMap mapX, int tma_out) {
+              const __grid_constant__ CUtensorMap mapX, int tma_out, const __grid_constant__ CUtensorMap mapW) {
     using TC = TileCfg<BN, PAIR>;
     constexpr int STAGES = TC::STAGES;
     constexpr int STAGE_BYTES = TC::STAGE_BYTES;
@@ -409,7 +438,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int n_total = m_tiles * n_tiles;
     const int kblocks = K / BK;
     constexpr int HALF = BN / 2;
-    const Sched sc = make_sched(n_total, n_grp, EPI != EPI_QKV_ROPE && can_split != 0);
+    const Sched sc = make_sched(n_total, n_grp, EPI != EPI_QKV_ROPE && BN == 256 && kblocks >= 2 && can_split != 0);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -453,15 +482,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         int s = 0;
         uint32_t ph = 0;
         for (int u = grp; u < sc.units && !abort_flag; u += n_grp) {
-            const Unit un = unit_of(u, sc);
+            const Unit un = unit_of(u, sc, kblocks);
             const int mt = un.t % m_tiles, nt = un.t / m_tiles;
-            // this CTA's A rows and its share of the weight rows (a column half loads half)
-            const CUtensorMap* mb = un.half < 0 ? &mapB : &mapBh;
-            const int bshare = un.half < 0 ? TC::B_ROWS : TC::B_ROWS / 2;
-            const int brow = nt * BN + (un.half > 0 ? HALF : 0) + rank * bshare;
+            // this CTA's A rows and its share of the weight rows, over the unit's K range
+            const int brow = nt * BN + rank * TC::B_ROWS;
             const int arow = mt * TC::TM + rank * BM;
-            const uint32_t bytes = (uint32_t)(A_BYTES + bshare * BK * 2);
-            for (int kb = 0; kb < kblocks; ++kb) {
+            const uint32_t bytes = (uint32_t)(A_BYTES + TC::B_ROWS * BK * 2);
+            for (int kb = un.k0; kb < un.k1; ++kb) {
                 if (!mbar_wait_t<PAIR>(&empty[s], ph ^ 1, &abort_flag)) {
                     abort_flag = 1;
                     set_error(err, BLEND_ETIMEOUT);
@@ -476,12 +503,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                     const uint32_t fb = leader_addr(&full[s]);
                     tma_load_2d_pair(st, &mapA, fb, kb * BK, arow);
-                    tma_load_2d_pair(st + A_BYTES, mb, fb, kb * BK, brow);
+                    tma_load_2d_pair(st + A_BYTES, &mapB, fb, kb * BK, brow);
                 } else {
                     mbar_expect_tx(&full[s], bytes);
                     pending[s] = (int)ph;
                     tma_load_2d(st, &mapA, &full[s], kb * BK, arow);
-                    tma_load_2d(st + A_BYTES, mb, &full[s], kb * BK, brow);
+                    tma_load_2d(st + A_BYTES, &mapB, &full[s], kb * BK, brow);
                 }
                 if (++s == STAGES) {
                     s = 0;
@@ -494,8 +521,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         int s = 0, b = 0;
         uint32_t ph = 0, tph = 0;
         for (int u = grp; u < sc.units && !abort_flag; u += n_grp) {
-            const Unit un = unit_of(u, sc);
-            const uint32_t idesc = un.half < 0 ? TC::IDESC : TC::IDESC_H;
+            const Unit un = unit_of(u, sc, kblocks);
+            const uint32_t idesc = TC::IDESC;
             if (!mbar_wait_t<PAIR>(&tempty[b], tph ^ 1, &abort_flag)) {
                 abort_flag = 1;
                 set_error(err, BLEND_ETIMEOUT);
@@ -503,7 +530,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             tc_fence_after();
             const uint32_t d = tbase + (uint32_t)(b * BN);
-            for (int kb = 0; kb < kblocks; ++kb) {
+            for (int kb = un.k0; kb < un.k1; ++kb) {
                 if (!mbar_wait_t<PAIR>(&full[s], ph, &abort_flag)) {
                     abort_flag = 1;
                     set_error(err, BLEND_ETIMEOUT);
@@ -517,10 +544,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                 for (int kk = 0; kk < BK / 16; ++kk) {
                     if (PAIR)
                         umma_bf16_pair(d, sdesc_sw128(a_addr + kk * 32), sdesc_sw128(b_addr + kk * 32), idesc,
-                                       (kb != 0 || kk != 0) ? 1u : 0u);
+                                       (kb != un.k0 || kk != 0) ? 1u : 0u);
                     else
                         umma_bf16(d, sdesc_sw128(a_addr + kk * 32), sdesc_sw128(b_addr + kk * 32), idesc,
-                                  (kb != 0 || kk != 0) ? 1u : 0u);
+                                  (kb != un.k0 || kk != 0) ? 1u : 0u);
                 }
                 if (PAIR)
                     umma_commit_pair(&empty[s]);
@@ -545,7 +572,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         int b = 0;
         uint32_t tph = 0;
         for (int u = grp; u < sc.units; u += n_grp) {
-            const Unit un = unit_of(u, sc);
+            const Unit un = unit_of(u, sc, kblocks);
             const int mt = un.t % m_tiles, nt = un.t / m_tiles;
             // lane 0 waits and broadcasts; the warp stays converged for the .sync.aligned
             // tcgen05.ld below
@@ -623,13 +650,22 @@ __global__ void __launch_bounds__(THREADS, 1)
                         }
                     }
                 }
-            } else {
-                // a whole tile, or one column half of a split tile; the folded-norm sums of
-                // squares are kept per BN/2 columns
-                const int cbase = nt * BN + (un.half > 0 ? HALF : 0);
-                const int n_half = un.half < 0 ? 2 : 1;
+            } else if (un.half >= 0) {
+                // a K half of a split tile: its raw partial goes to the workspace rows of
+                // (split tile, half); k_split_combine finishes the tile
+                const int ws_row0 = (un.sidx * 2 + un.half) * TC::TM + rank * BM + sp * 32;
 #pragma unroll 1
-                for (int hh = 0; hh < n_half; ++hh) {
+                for (int c = 0; c < BN; c += 32) {
+                    uint32_t r[32];
+                    TMEM_LD32(tl + c, r);
+                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                    part_chunk_tma(r, ws_row0, c, cb, &mapW);
+                }
+            } else {
+                // a whole tile; the folded-norm sums of squares are kept per BN/2 columns
+                const int cbase = nt * BN;
+#pragma unroll 1
+                for (int hh = 0; hh < 2; ++hh) {
                     float ssq = 0.f;
 #pragma unroll 1
                     for (int c = hh * HALF; c < (hh + 1) * HALF; c += 32) {
@@ -666,7 +702,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (b == 0) tph ^= 1;
         }
         // the staging chunk belongs to this CTA: its last stores must be done before exit
-        if (EPI == EPI_ADD_F32 && lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+        if (EPI != EPI_QKV_ROPE && lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     }
     __syncthreads();
     if (threadIdx.x == 0 && abort_flag) {
@@ -689,6 +725,107 @@ __global__ void __launch_bounds__(THREADS, 1)
         else
             asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(TMEM_COLS)
                          : "memory");
+    }
+}
+
+// Finishes the split tiles of a k_gemm_tc launch (BN = 256): the two K-half partials of
+// every row of a split tile are added in a fixed order (half 0 + half 1), scaled by the
+// row's folded-norm factor, and the tile's epilogue runs on the sum: fp32 store, residual
+// add (with bf16(x * g) and the two per-128-column sums of squares of a norm producer) or
+// SwiGLU.  One warp per row, eight consecutive columns per lane.  The split set is the
+// kernel's own (same schedule from the device row count).
+template <int EPI, int TM>
+__global__ void __launch_bounds__(128)
+    k_split_combine(const float* __restrict__ ws, int K, int N, const int32_t* __restrict__ M_dev, int n_grp,
+                    void* __restrict__ Cv, int ldc, const __grid_constant__ NormEpi ne) {
+    const int M = *M_dev;
+    const int m_tiles = (M + TM - 1) / TM, n_tiles = (N + 255) / 256;
+    const Sched sc = make_sched(m_tiles * n_tiles, n_grp, K / BK >= 2);
+    const int sidx = blockIdx.x;
+    if (sidx >= sc.split) return;
+    const int t = sc.full + sidx, mt = t % m_tiles, nt = t / m_tiles;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int r_t = blockIdx.y * 4 + warp;  // row within the tile
+    const int row = mt * TM + r_t;
+    if (r_t >= TM || row >= M) return;
+    const float rs = row_scale(ne, row);
+    const int c0 = lane * 8, col = nt * 256 + c0;
+    const bool live = col < N;  // N % 32 == 0: a lane's eight columns are all in or all out
+    float v[8];
+    if (live) {
+        const float4* p0 = reinterpret_cast<const float4*>(ws + ((long long)(sidx * 2) * TM + r_t) * 256 + c0);
+        const float4* p1 = reinterpret_cast<const float4*>(ws + ((long long)(sidx * 2 + 1) * TM + r_t) * 256 + c0);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const float4 a = __ldcg(p0 + h), b = __ldcg(p1 + h);
+            v[4 * h] = (a.x + b.x) * rs;
+            v[4 * h + 1] = (a.y + b.y) * rs;
+            v[4 * h + 2] = (a.z + b.z) * rs;
+            v[4 * h + 3] = (a.w + b.w) * rs;
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = 0.f;
+    }
+    if (EPI == EPI_STORE_F32) {
+        if (live) {
+            float4* p = reinterpret_cast<float4*>((float*)Cv + (long long)row * ldc + col);
+            p[0] = make_float4(v[0], v[1], v[2], v[3]);
+            p[1] = make_float4(v[4], v[5], v[6], v[7]);
+        }
+    } else if (EPI == EPI_ADD_F32) {
+        float ssq = 0.f;
+        if (live) {
+            float4* p = reinterpret_cast<float4*>((float*)Cv + (long long)row * ldc + col);
+            const float4 x0 = p[0], x1 = p[1];
+            v[0] += x0.x;
+            v[1] += x0.y;
+            v[2] += x0.z;
+            v[3] += x0.w;
+            v[4] += x1.x;
+            v[5] += x1.y;
+            v[6] += x1.z;
+            v[7] += x1.w;
+            p[0] = make_float4(v[0], v[1], v[2], v[3]);
+            p[1] = make_float4(v[4], v[5], v[6], v[7]);
+            if (ne.x_out != nullptr) {
+                const uint4 gv = *reinterpret_cast<const uint4*>(ne.g + col);
+                const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+                uint32_t xw[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    ssq = fmaf(v[2 * e], v[2 * e], ssq);
+                    ssq = fmaf(v[2 * e + 1], v[2 * e + 1], ssq);
+                    xw[e] = pack_bf16x2(v[2 * e] * __uint_as_float(gw[e] << 16),
+                                        v[2 * e + 1] * __uint_as_float(gw[e] & 0xffff0000u));
+                }
+                *reinterpret_cast<uint4*>(ne.x_out + (long long)row * ne.ldx + col) = make_uint4(xw[0], xw[1], xw[2], xw[3]);
+            }
+        }
+        if (ne.x_out != nullptr) {
+            // sums of squares of the two 128-column halves: 16 lanes each, fixed tree
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) ssq += __shfl_xor_sync(0xffffffffu, ssq, o);
+            const int seg = lane >> 4;
+            if ((lane & 15) == 0 && nt * 256 + seg * 128 < N)
+                ne.ssq_out[(long long)row * ne.ssq_stride + 2 * nt + seg] = ssq;
+        }
+    } else if (EPI == EPI_SWIGLU) {
+        // a 32-column group holds 16 gate then 16 up columns of the same hidden units:
+        // lanes 4i, 4i+1 hold the gates, 4i+2, 4i+3 the matching ups
+        float u[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) u[e] = __shfl_down_sync(0xffffffffu, v[e], 2);
+        if (live && (lane & 3) < 2) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float g0 = v[2 * e], g1 = v[2 * e + 1];
+                w[e] = pack_bf16x2(g0 / (1.f + expf(-g0)) * u[2 * e], g1 / (1.f + expf(-g1)) * u[2 * e + 1]);
+            }
+            const int ocol = (nt * 256 + (lane >> 2) * 32) / 2 + (lane & 3) * 8;
+            *reinterpret_cast<uint4*>((bf16*)Cv + (long long)row * ldc + ocol) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
     }
 }
 
@@ -781,10 +918,9 @@ int gemm_tc_norm_parts(int N) {
 }
 
 template <int BN, bool PAIR>
-void launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mbh, int K, int N,
-               const int32_t* M_dev, int M_max, int epi, void* C, int ldc, int32_t* err, cudaStream_t s,
-               const QkvEpi& qe, bool split, const NormEpi& ne, const CUtensorMap& mc, const CUtensorMap& mx,
-               int tma_out) {
+void launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, int K, int N, const int32_t* M_dev, int M_max, int epi,
+               void* C, int ldc, int32_t* err, cudaStream_t s, const QkvEpi& qe, const float* split_ws,
+               const CUtensorMap& mw, const NormEpi& ne, const CUtensorMap& mc, const CUtensorMap& mx, int tma_out) {
     // one work unit per CTA, or per cluster of two CTAs: as many as can be resident at once
     int slots = g_num_sms;
     if (PAIR) {
@@ -830,8 +966,8 @@ void launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& 
     }
     const int tiles = ((M_max + TileCfg<BN, PAIR>::TM - 1) / TileCfg<BN, PAIR>::TM) * ((N + BN - 1) / BN);
     int groups = tiles < slots ? tiles : slots;
-    split = split && epi != EPI_QKV_ROPE;
-    // fewer tiles than half the slots: every tile runs as two column halves
+    const bool split = split_ws != nullptr && epi != EPI_QKV_ROPE && BN == 256 && K / BK >= 2;
+    // fewer tiles than half the slots: every tile runs as two K halves
     if (split && 2 * tiles <= slots) groups = 2 * tiles;
     const int cs = split ? 1 : 0;
     cudaLaunchConfig_t cfg = {};
@@ -848,8 +984,8 @@ void launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& 
 #define LAUNCH(E)                                                                                              \
     do {                                                                                                       \
         cfg.dynamicSmemBytes = smem_bytes<E, BN, PAIR>();                                                      \
-        cudaLaunchKernelEx(&cfg, k_gemm_tc<E, BN, PAIR>, ma, mb, mbh, K, N, M_dev, C, ldc, err, qe, cs, ne, mc, mx, \
-                           tma_out);                                                                           \
+        cudaLaunchKernelEx(&cfg, k_gemm_tc<E, BN, PAIR>, ma, mb, K, N, M_dev, C, ldc, err, qe, cs, ne, mc, mx,   \
+                           tma_out, mw);                                                                       \
     } while (0)
     if (epi == EPI_STORE_F32)
         LAUNCH(EPI_STORE_F32);
@@ -860,10 +996,22 @@ void launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& 
     else
         LAUNCH(EPI_QKV_ROPE);
 #undef LAUNCH
+    if (split) {
+        // the split tiles (if the device row count gives any) are finished here
+        constexpr int TM = TileCfg<BN, PAIR>::TM;
+        const dim3 grid(groups / 2 > 0 ? groups / 2 : 1, TM / 4);
+        if (epi == EPI_STORE_F32)
+            k_split_combine<EPI_STORE_F32, TM><<<grid, 128, 0, s>>>(split_ws, K, N, M_dev, groups, C, ldc, ne);
+        else if (epi == EPI_ADD_F32)
+            k_split_combine<EPI_ADD_F32, TM><<<grid, 128, 0, s>>>(split_ws, K, N, M_dev, groups, C, ldc, ne);
+        else
+            k_split_combine<EPI_SWIGLU, TM><<<grid, 128, 0, s>>>(split_ws, K, N, M_dev, groups, C, ldc, ne);
+        note_launch(1);
+    }
 }
 
 int launch_gemm_tc(const void* A, int K, int M_cap, const void* B, int N, const int32_t* M_dev, int M_max,
-                   int epi, void* C, int ldc, int32_t* err, cudaStream_t s, const QkvEpi* qkv, bool split,
+                   int epi, void* C, int ldc, int32_t* err, cudaStream_t s, const QkvEpi* qkv, float* split_ws,
                    const NormEpi* norm) {
     if (M_max <= 0) return BLEND_OK;
     const int bn = pick_bn(N);
@@ -879,11 +1027,16 @@ int launch_gemm_tc(const void* A, int K, int M_cap, const void* B, int N, const 
     // each CTA of a pair stages half of a tile's weight rows
     const bool pair = bn == 256 && M_max > BM && g_num_sms >= 2;
     const uint32_t brows = pair ? (uint32_t)bn / 2 : (uint32_t)bn;
-    CUtensorMap ma, mb, mbh;
+    CUtensorMap ma, mb;
     if (!encode_2d(&ma, A, (uint64_t)K, (uint64_t)M_cap, BK, BM) ||
-        !encode_2d(&mb, B, (uint64_t)K, (uint64_t)N, BK, brows) ||
-        !encode_2d(&mbh, B, (uint64_t)K, (uint64_t)N, BK, brows / 2))
+        !encode_2d(&mb, B, (uint64_t)K, (uint64_t)N, BK, brows))
         return BLEND_EUNSUPPORTED;  // the operands cannot be described to the TMA unit
+    // split workspace: rows (split tile, K half, tile row) of 256 fp32
+    CUtensorMap mw{};
+    if (split_ws != nullptr &&
+        (g_num_sms > GEMM_SPLIT_SMS || !encode_out(&mw, split_ws, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 256,
+                                                    (uint64_t)GEMM_SPLIT_WS_FLOATS / 256, 256, CU_TENSOR_MAP_SWIZZLE_128B)))
+        split_ws = nullptr;
     // residual add: the sum (and bf16(x * g)) of warps with 32 live rows leave as tensor
     // stores; the maps span the M_max rows the launch may write
     CUtensorMap mc{}, mx{};
@@ -895,11 +1048,11 @@ int launch_gemm_tc(const void* A, int K, int M_cap, const void* B, int N, const 
                                                      (uint64_t)M_max, (uint64_t)ne.ldx, CU_TENSOR_MAP_SWIZZLE_64B));
     }
     if (pair)
-        launch_bn<256, true>(ma, mb, mbh, K, N, M_dev, M_max, epi, C, ldc, err, s, qe, split, ne, mc, mx, tma_out);
+        launch_bn<256, true>(ma, mb, K, N, M_dev, M_max, epi, C, ldc, err, s, qe, split_ws, mw, ne, mc, mx, tma_out);
     else if (bn == 256)
-        launch_bn<256, false>(ma, mb, mbh, K, N, M_dev, M_max, epi, C, ldc, err, s, qe, split, ne, mc, mx, tma_out);
+        launch_bn<256, false>(ma, mb, K, N, M_dev, M_max, epi, C, ldc, err, s, qe, split_ws, mw, ne, mc, mx, tma_out);
     else
-        launch_bn<128, false>(ma, mb, mbh, K, N, M_dev, M_max, epi, C, ldc, err, s, qe, split, ne, mc, mx, tma_out);
+        launch_bn<128, false>(ma, mb, K, N, M_dev, M_max, epi, C, ldc, err, s, qe, split_ws, mw, ne, mc, mx, tma_out);
     note_launch(1);
     return BLEND_OK;
 }
