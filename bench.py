@@ -48,16 +48,16 @@ except OSError:
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
 # capture of each kernel (profiles/), valid only while the kernel's source is unchanged.
 TRAFFIC = {
-    "gemm_qkv": {"bytes": 128.365824e6 + 31.427584e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
-                 "sha256_16": "0932f777c8c471dc", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
-    "gemm_o": {"bytes": 215.511296e6 + 67.811840e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
-               "sha256_16": "0932f777c8c471dc", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
-    "gemm_gate_up": {"bytes": 383.073024e6 + 83.892224e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
-                     "sha256_16": "0932f777c8c471dc", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
-    "gemm_down": {"bytes": 598.299904e6 + 93.098752e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
-                  "sha256_16": "0932f777c8c471dc", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
-    "attention": {"bytes": 136.019456e6 + 14.218240e6, "source": "rag_kv_cache_rope_gb300/csrc/attn_tc.cu",
-                  "sha256_16": "a6f10f2b41353b9c", "profile": "profiles/attn_tc_qwen14b_16k_layer.md"},
+    "gemm_qkv": {"bytes": 128.797184e6 + 31.917312e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
+                 "sha256_16": "72ebd2892f3bc03b", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
+    "gemm_o": {"bytes": 199.343616e6 + 63.367168e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
+               "sha256_16": "72ebd2892f3bc03b", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
+    "gemm_gate_up": {"bytes": 378.926592e6 + 85.732352e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
+                     "sha256_16": "72ebd2892f3bc03b", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
+    "gemm_down": {"bytes": 586.231040e6 + 90.249216e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
+                  "sha256_16": "72ebd2892f3bc03b", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
+    "attention": {"bytes": 134.492160e6 + 14.339072e6, "source": "rag_kv_cache_rope_gb300/csrc/attn_tc.cu",
+                  "sha256_16": "b27fab638c49ecc3", "profile": "profiles/attn_tc_qwen14b_16k_layer.md"},
 }
 
 
