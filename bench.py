@@ -57,7 +57,7 @@ TRAFFIC = {
     "gemm_down": {"bytes": 586.231040e6 + 90.249216e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
                   "sha256_16": "72ebd2892f3bc03b", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
     "attention": {"bytes": 134.492160e6 + 14.339072e6, "source": "rag_kv_cache_rope_gb300/csrc/attn_tc.cu",
-                  "sha256_16": "b27fab638c49ecc3", "profile": "profiles/attn_tc_qwen14b_16k_layer.md"},
+                  "sha256_16": "92d135632b7ee5ff", "profile": "profiles/attn_tc_qwen14b_16k_layer.md"},
 }
 
 

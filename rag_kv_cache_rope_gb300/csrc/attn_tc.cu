@@ -1,6 +1,8 @@
 // Tensor-core causal GQA attention of the recomputed rows over the full blended KV
 // (CacheBlend blog, "Selective KV recompute": only the selected rows' attention rows
-// are computed, each over every earlier token, reused or fresh).
+// are computed, each over every earlier token, reused or fresh).  Head dim 128 runs on
+// CTA pairs (k_attn_pair, further below); k_attn_tc, described here, serves head dim 64
+// and any device where a pair does not fit.
 //
 // q is stored per kv head as [pair][d] with pair = row * group + j, so 128 consecutive
 // (row, head-of-group) pairs of one kv head form one TMA box and every K/V block is
