@@ -664,6 +664,38 @@ __global__ void __launch_bounds__(THREADS, 1)
             } else {
                 // a whole tile; the folded-norm sums of squares are kept per BN/2 columns
                 const int cbase = nt * BN;
+                if (EPI == EPI_ADD_F32 && tma_rows) {
+                    // residual add of 32 live rows: the next chunk's residual loads are in
+                    // flight while this chunk is added and stored
+                    const float* xrow = (const float*)Cv + (long long)row * ldc + cbase;
+                    float4 xn[8];
+                    if (cbase < N) {
+#pragma unroll
+                        for (int v = 0; v < 8; ++v) xn[v] = reinterpret_cast<const float4*>(xrow)[v];
+                    }
+                    float ssq = 0.f;
+#pragma unroll 1
+                    for (int c = 0; c < BN; c += 32) {
+                        const int col = cbase + c;
+                        uint32_t r[32];
+                        TMEM_LD32(tl + c, r);
+                        float4 xr[8];
+#pragma unroll
+                        for (int v = 0; v < 8; ++v) xr[v] = xn[v];
+                        if (c + 32 < BN && col + 32 < N) {
+#pragma unroll
+                            for (int v = 0; v < 8; ++v) xn[v] = reinterpret_cast<const float4*>(xrow + c + 32)[v];
+                        }
+                        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                        if (col < N) add_chunk_tma(r, xr, row0, col, rs, ne, cb, &mapC, &mapX, ssq);
+                        if (c + 32 == HALF || c + 32 == BN) {
+                            const int col0 = cbase + (c + 32 == HALF ? 0 : HALF);
+                            if (ne.x_out != nullptr && col0 < N)
+                                ne.ssq_out[(long long)row * ne.ssq_stride + col0 / HALF] = ssq;
+                            ssq = 0.f;
+                        }
+                    }
+                } else {
 #pragma unroll 1
                 for (int hh = 0; hh < 2; ++hh) {
                     float ssq = 0.f;
@@ -688,6 +720,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const int col0 = cbase + hh * HALF;
                     if (EPI == EPI_ADD_F32 && ne.x_out != nullptr && row < M && col0 < N)
                         ne.ssq_out[(long long)row * ne.ssq_stride + col0 / HALF] = ssq;
+                }
                 }
             }
             tc_fence_before();
