@@ -48,14 +48,14 @@ except OSError:
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
 # capture of each kernel (profiles/), valid only while the kernel's source is unchanged.
 TRAFFIC = {
-    "gemm_qkv": {"bytes": 128.797184e6 + 31.917312e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
-                 "sha256_16": "0000000000000000", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
-    "gemm_o": {"bytes": 199.343616e6 + 63.367168e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
-               "sha256_16": "0000000000000000", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
-    "gemm_gate_up": {"bytes": 378.926592e6 + 85.732352e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
-                     "sha256_16": "0000000000000000", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
-    "gemm_down": {"bytes": 586.231040e6 + 90.249216e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
-                  "sha256_16": "0000000000000000", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
+    "gemm_qkv": {"bytes": 128.005888e6 + 31.630080e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
+                 "sha256_16": "6655236c82fc5564", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
+    "gemm_o": {"bytes": 201.848576e6 + 63.539712e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
+               "sha256_16": "6655236c82fc5564", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
+    "gemm_gate_up": {"bytes": 376.398848e6 + 86.185472e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
+                     "sha256_16": "6655236c82fc5564", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
+    "gemm_down": {"bytes": 588.014336e6 + 91.328256e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
+                  "sha256_16": "6655236c82fc5564", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
     "attention": {"bytes": 134.492160e6 + 14.339072e6, "source": "rag_kv_cache_rope_gb300/csrc/attn_tc.cu",
                   "sha256_16": "92d135632b7ee5ff", "profile": "profiles/attn_tc_qwen14b_16k_layer.md"},
 }
