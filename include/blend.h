@@ -384,7 +384,9 @@ int blend_prefill(blend_handle* h, int32_t n_req, const blend_request* reqs,
                   const blend_pool* pool, const blend_outputs* out, void* stream);
 
 /* SpecCache 2.2 importance scores: out[i] = (1/n_layers) * sum_l ||hidden[i][l]||_2
- * for hidden device [n][n_layers][dim] of dtype (BLEND_F32 | BLEND_BF16); out fp32. */
+ * for hidden device [n][n_layers][dim] of dtype (BLEND_F32 | BLEND_BF16); out fp32.
+ * BLEND_EINVAL for a NULL pointer, n < 0, dim < 1, n_layers outside [1, 4096] or
+ * another dtype.  Any alignment of hidden is accepted (16-byte aligned rows read faster). */
 int importance_scores(const void* hidden, int32_t n, int32_t n_layers, int32_t dim,
                       int32_t dtype, float* out, void* stream);
 

@@ -702,7 +702,7 @@ int scatter_kv(blend_handle* h, const void* k_new, const void* v_new, const int3
 int importance_scores(const void* hidden, int32_t n, int32_t n_layers, int32_t dim, int32_t dtype,
                       float* out, void* stream) {
     if (!hidden || !out) return fail(nullptr, BLEND_EINVAL, "NULL pointer");
-    if (n < 0 || n_layers < 1 || dim < 1 || (dtype != BLEND_F32 && dtype != BLEND_BF16))
+    if (n < 0 || n_layers < 1 || n_layers > 4096 || dim < 1 || (dtype != BLEND_F32 && dtype != BLEND_BF16))
         return fail(nullptr, BLEND_EINVAL, "bad sizes or dtype");
     launch_importance(dtype, hidden, n, n_layers, dim, out, (cudaStream_t)stream);
     return check_cuda(nullptr, "importance_scores");

@@ -522,33 +522,64 @@ void launch_scatter(int dtype, const void* k_new, const void* v_new, const int32
 }
 
 // ---------------------------------------------------------------- importance scores
-// SpecCache 2.2: out[i] = mean over layers of the L2 norm of hidden[i][l].
+// SpecCache 2.2: out[i] = mean over layers of the L2 norm of hidden[i][l].  One warp per
+// (token, layer) row at a time: 16-byte loads when dim allows, a fixed shuffle tree for
+// the sum of squares.  A block of IMP_WARPS warps covers IMP_WARPS / w tokens with w =
+// min(n_layers, IMP_WARPS) warps each; the layer norms go to shared memory and are added
+// in layer order.
+constexpr int IMP_WARPS = 8;
 template <typename T>
-__global__ void __launch_bounds__(256) k_importance(const T* __restrict__ h, int n_layers, int dim,
-                                                    float* __restrict__ out) {
-    __shared__ float red[256];
-    const long long i = blockIdx.x;
-    float acc = 0.f;
-    for (int l = 0; l < n_layers; ++l) {
-        const T* r = h + (i * n_layers + l) * dim;
-        float ss = 0.f;
-        for (int j = threadIdx.x; j < dim; j += blockDim.x) {
-            float v = to_f<T>(r[j]);
-            ss += v * v;
+__global__ void __launch_bounds__(IMP_WARPS * 32) k_importance(const T* __restrict__ h, int n, int n_layers, int dim,
+                                                             float* __restrict__ out) {
+    extern __shared__ float norms[];  // [tokens per block][n_layers]
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int wpt = n_layers < IMP_WARPS ? n_layers : IMP_WARPS;
+    const int per_block = IMP_WARPS / wpt;
+    const int tb = warp / wpt;  // token within the block
+    const long long i = (long long)blockIdx.x * per_block + tb;
+    const bool live = tb < per_block && i < n;
+    const bool vec = dim % Vec<T>::N == 0 && ((uintptr_t)h & 15) == 0;
+    if (live) {
+        for (int l = warp % wpt; l < n_layers; l += wpt) {
+            const T* r = h + (i * n_layers + l) * dim;
+            float ss = 0.f;
+            if (vec) {
+#pragma unroll 4
+                for (int j = lane * Vec<T>::N; j < dim; j += 32 * Vec<T>::N) {
+                    const Vec<T> v = ld16(r + j);
+#pragma unroll
+                    for (int e = 0; e < Vec<T>::N; ++e) ss = fmaf(v.get(e), v.get(e), ss);
+                }
+            } else {
+                for (int j = lane; j < dim; j += 32) {
+                    const float v = to_f<T>(r[j]);
+                    ss = fmaf(v, v, ss);
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+            if (lane == 0) norms[tb * n_layers + l] = sqrtf(ss);
         }
-        ss = block_sum(ss, red);
-        acc += sqrtf(ss);
     }
-    if (threadIdx.x == 0) out[i] = acc / (float)n_layers;
+    __syncthreads();
+    if (live && warp % wpt == 0 && lane == 0) {
+        float acc = 0.f;
+        for (int l = 0; l < n_layers; ++l) acc += norms[tb * n_layers + l];
+        out[i] = acc / (float)n_layers;
+    }
 }
 
 void launch_importance(int dtype, const void* hidden, int n, int n_layers, int dim, float* out,
                        cudaStream_t s) {
     if (n <= 0) return;
+    const int wpt = n_layers < IMP_WARPS ? n_layers : IMP_WARPS;
+    const int per_block = IMP_WARPS / wpt;
+    const int grid = (n + per_block - 1) / per_block;
+    const size_t smem = (size_t)per_block * n_layers * sizeof(float);
     if (dtype == BLEND_BF16)
-        k_importance<bf16><<<n, 256, 0, s>>>((const bf16*)hidden, n_layers, dim, out);
+        k_importance<bf16><<<grid, IMP_WARPS * 32, smem, s>>>((const bf16*)hidden, n, n_layers, dim, out);
     else
-        k_importance<float><<<n, 256, 0, s>>>((const float*)hidden, n_layers, dim, out);
+        k_importance<float><<<grid, IMP_WARPS * 32, smem, s>>>((const float*)hidden, n, n_layers, dim, out);
     note_launch(1);
 }
 

@@ -132,6 +132,7 @@ def test_init_rejects_bad_arguments_without_a_gpu(lib):
     assert lib.gather_rows(C.c_void_p(1 << 20), 20, C.c_void_p(1 << 20), C.c_void_p(1 << 20), 1,
                            C.c_void_p(1 << 20), None) == b.EINVAL
     assert lib.importance_scores(C.c_void_p(1 << 20), 4, 0, 8, b.F32, C.c_void_p(1 << 20), None) == b.EINVAL
+    assert lib.importance_scores(C.c_void_p(1 << 20), 4, 4097, 8, b.F32, C.c_void_p(1 << 20), None) == b.EINVAL
     vp = C.c_void_p(1 << 20)
     assert lib.span_select(None, vp, 8, 0, 4, 4, 0.4, 7000, 16, b.BUDGET_FINAL, vp, vp, None) == b.EINVAL
     assert lib.align_expand(None, vp, vp, 4, 0, vp, vp, 4, 8, 0, vp, vp, None) == b.EINVAL

@@ -169,11 +169,28 @@ def test_deviation_scatter_gather(dtype):
     assert torch.equal(rows, kn)
 
 
-def test_importance_scores():
+# (tokens, layers, dim): the 4 x 2048 shape of the workloads, more layers than a block's
+# warps, a width without 16-byte vectors, a single layer
+@pytest.mark.parametrize("n,n_layers,dim", [(301, 4, 2048), (37, 11, 72), (19, 3, 70), (5, 1, 3)])
+def test_importance_scores(n, n_layers, dim):
     for dt in (torch.float32, torch.bfloat16):
-        h = synth.hidden_states(301, 4, 2048, seed=4, dtype=dt)
-        out = torch.empty(301, device=dev())
-        b.importance_scores(h.to(dev()), 301, 4, 2048, out)
+        h = synth.hidden_states(n, n_layers, dim, seed=4, dtype=dt)
+        out = torch.empty(n, device=dev())
+        b.importance_scores(h.to(dev()), n, n_layers, dim, out)
+        torch.cuda.synchronize()
+        assert maxrel(f64(out), O.importance_scores(f64(h))) <= 1e-5
+
+
+def test_importance_scores_unaligned():
+    """Rows that start off a 16-byte boundary take the scalar loads."""
+    n, n_layers, dim = 23, 4, 256
+    for dt in (torch.float32, torch.bfloat16):
+        h = synth.hidden_states(n, n_layers, dim, seed=6, dtype=dt)
+        buf = torch.zeros(h.numel() + 1, dtype=dt, device=dev())
+        buf[1:].copy_(h.reshape(-1).to(dev()))
+        hv = buf[1:].view(n, n_layers, dim)
+        out = torch.empty(n, device=dev())
+        b.importance_scores(hv, n, n_layers, dim, out)
         torch.cuda.synchronize()
         assert maxrel(f64(out), O.importance_scores(f64(h))) <= 1e-5
 
