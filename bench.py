@@ -89,6 +89,9 @@ def parse():
                     help="also time full prefill of the same input (every row recomputed; 0 skips it)")
     ap.add_argument("--pool", default="device", choices=["device", "host"],
                     help="chunk-KV pool in HBM, or in pinned host memory read layer by layer (overlapped)")
+    ap.add_argument("--sweep", default="",
+                    help="context x ratio sweep of the 14B shape instead of the headline line: "
+                         "'CHUNKS,...:PCT,...' (e.g. '7,15,31,63:5,10,20,40,100'); one JSON line per point")
     return ap.parse_args()
 
 
@@ -164,17 +167,20 @@ class ClockSampler:
 class Setup:
     """Device-resident inputs, weights, handle and outputs for one replica."""
 
-    def __init__(self, wl: synth.Workload, dev: torch.device, max_rows_full: bool, pool_loc: str = "device"):
+    def __init__(self, wl: synth.Workload, dev: torch.device, max_rows_full: bool, pool_loc: str = "device",
+                 packed=None):
         from rag_kv_cache_rope_gb300 import binding as b
         self.b = b
         self.wl = wl
         sh = wl.model
         self.dev = dev
         torch.manual_seed(wl.seed)
-        plain = synth.model_weights(sh, wl.seed, device=dev)
-        self.packed = b.pack_weights(plain)
-        del plain
-        torch.cuda.empty_cache()
+        if packed is None:  # else the caller's packed weights of this shape and seed
+            plain = synth.model_weights(sh, wl.seed, device=dev)
+            packed = b.pack_weights(plain)
+            del plain
+            torch.cuda.empty_cache()
+        self.packed = packed
         pool_tok, reqs = synth.workload_tokens(wl)
         assert wl.batch == 1, "bench times one request per step"
         self.req_tok = reqs[0]
@@ -263,26 +269,39 @@ class Setup:
 
 def algorithmic(sh: synth.ModelShape, rows: int, pairs: int, wl: synth.Workload) -> dict:
     """Algorithmic work of one launch of each stage (one launch = one layer) at `rows`
-    recomputed rows whose causal pairs sum to `pairs`."""
+    recomputed rows whose causal pairs sum to `pairs`: {stage: (bound, FLOP or bytes, the
+    least HBM bytes the launch must move)}.  The bytes of a contraction are its weights read
+    once, its input rows read once and its outputs written once (the fp32 residual read and
+    written by the O and down projections); attention reads the blended K/V of the layer once."""
     H, d, F = sh.hidden, sh.head_dim, sh.ffn
     qd, kvd = sh.n_q_heads * d, sh.n_kv_heads * d
     es = 2 if sh.dtype == "bf16" else 4
     asm_bytes = 2 * 2 * sh.n_layers * (wl.prefix_len + wl.n_chunk_rows) * kvd * es
     return {
-        "gemm_qkv": ("tensor", 2.0 * rows * H * (qd + 2 * kvd)),
-        "gemm_o": ("tensor", 2.0 * rows * qd * H),
-        "gemm_gate_up": ("tensor", 2.0 * rows * H * 2 * F),
-        "gemm_down": ("tensor", 2.0 * rows * F * H),
-        "attention": ("tensor", 4.0 * d * sh.n_q_heads * pairs),
-        "assemble": ("hbm", float(asm_bytes)),
+        "gemm_qkv": ("tensor", 2.0 * rows * H * (qd + 2 * kvd), es * (H * (qd + 2 * kvd) + rows * H + rows * (qd + 2 * kvd))),
+        "gemm_o": ("tensor", 2.0 * rows * qd * H, es * (qd * H + rows * qd) + rows * H * (8 + es)),
+        "gemm_gate_up": ("tensor", 2.0 * rows * H * 2 * F, es * (H * 2 * F + rows * H + rows * F)),
+        "gemm_down": ("tensor", 2.0 * rows * F * H, es * (F * H + rows * F) + rows * H * (8 + es)),
+        "attention": ("tensor", 4.0 * d * sh.n_q_heads * pairs, es * (2 * wl.n_ctx * kvd + 2 * rows * qd)),
+        "assemble": ("hbm", float(asm_bytes), float(asm_bytes)),
     }
 
 
+def ideal_launch_ms(entry) -> float:
+    """Roofline time of one launch: max(FLOP / tensor peak, bytes / HBM bandwidth) for a
+    contraction, bytes / HBM bandwidth for a memory-bound kernel (measured peaks)."""
+    kind, units, nbytes = entry
+    t_mem = nbytes / (PEAKS["hbm_gbs"] * 1e9)
+    t_cmp = units / (PEAKS["bf16_tflops_sustained"] * 1e12) if kind == "tensor" else 0.0
+    return max(t_cmp, t_mem) * 1e3
+
+
 def step_work(wl: synth.Workload, rows0: int, pairs0: int, rows1: int, pairs1: int, aux_rp=None) -> dict:
-    """{stage: (bound, algorithmic units per step, launches per step)} for one step.  Layers
-    before the focus layer run the first set (rows0, pairs0), later ones the filtered set; the
-    focus layer projects K/V for the first set and runs attention and MLP on the second.
-    aux_rp = (rows, pairs) of the auxiliary model's layers, counted under aux_* names."""
+    """{stage: (bound, algorithmic units per step, launches per step, roofline ms per step)}
+    for one step.  Layers before the focus layer run the first set (rows0, pairs0), later
+    ones the filtered set; the focus layer projects K/V for the first set and runs attention
+    and MLP on the second.  aux_rp = (rows, pairs) of the auxiliary model's layers, counted
+    under aux_* names."""
     sh = wl.model
     L = sh.n_layers
     fl = wl.focus_layer if wl.focus_bp else L
@@ -290,15 +309,16 @@ def step_work(wl: synth.Workload, rows0: int, pairs0: int, rows1: int, pairs1: i
     out = {}
     for k in w0:
         if k == "assemble":
-            out[k] = (w0[k][0], w0[k][1], 1)
+            out[k] = (w0[k][0], w0[k][1], 1, ideal_launch_ms(w0[k]))
             continue
         n0 = min(L, fl + 1) if k == "gemm_qkv" else min(L, fl)
-        out[k] = (w0[k][0], n0 * w0[k][1] + (L - n0) * w1[k][1], L)
+        out[k] = (w0[k][0], n0 * w0[k][1] + (L - n0) * w1[k][1], L,
+                  n0 * ideal_launch_ms(w0[k]) + (L - n0) * ideal_launch_ms(w1[k]))
     if aux_rp is not None:
         ash = wl.aux_model
         wa = algorithmic(ash, aux_rp[0], aux_rp[1], wl)
         for k in ("gemm_qkv", "gemm_o", "gemm_gate_up", "gemm_down", "attention"):
-            out["aux_" + k] = (wa[k][0], ash.n_layers * wa[k][1], ash.n_layers)
+            out["aux_" + k] = (wa[k][0], ash.n_layers * wa[k][1], ash.n_layers, ash.n_layers * ideal_launch_ms(wa[k]))
     return out
 
 
@@ -372,7 +392,7 @@ def run_ours(args, wl, rank, world):
     dom = max(shares, key=shares.get)
     roof = None
     if dom in work:
-        kind, step_units, per_step = work[dom]
+        kind, step_units, per_step, _ = work[dom]
         units = step_units / per_step  # average work of one launch
         n_launch = args.steps * per_step
         avg_ms = prof[dom][0] / n_launch
@@ -389,11 +409,10 @@ def run_ours(args, wl, rank, world):
                     "avg_launch_ms": avg_ms}
     stages = {k: {"ms_per_step": v[0] / args.steps, "share": v[0] / total, "launches": v[1]}
               for k, v in prof.items() if v[1]}
-    # whole-step roofline: ideal time of every GEMM/attention at the tensor peak plus the
-    # assembly at the HBM peak, over the measured step
+    # whole-step roofline: every GEMM/attention launch at max(FLOP / tensor peak, bytes /
+    # HBM bandwidth) plus the assembly at the HBM peak, over the measured step
     tflop = sum(w[1] for k, w in work.items() if w[0] == "tensor")
-    ideal_ms = tflop / (PEAKS["bf16_tflops_sustained"] * 1e12) * 1e3 + \
-        work["assemble"][1] / (PEAKS["hbm_gbs"] * 1e9) * 1e3
+    ideal_ms = sum(w[3] for w in work.values())
     line = {
         "metric": "blended-prefill context tokens/s (16K ctx, 20% recompute), TTFT ms, % roofline",
         "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -516,6 +535,56 @@ def e2e(S: Setup, args, world):
         dt = float(t.item())
     return {"value": world * S.N / dt, "unit": "tokens/s", "ttft_ms": dt * 1e3, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h}
+
+
+def run_sweep(args):
+    """The 14B-shaped context x ratio sweep: for every context (chunks of 512 behind a
+    64-token prefix, 128-token query) and every recompute ratio, TTFT, context tokens/s and
+    the step's fraction of its roofline, one JSON line per point.  The weights are drawn
+    once; each context gets its own pool, outputs and a handle sized for every row (the
+    100 % point recomputes all of them)."""
+    from rag_kv_cache_rope_gb300 import build as B
+    B.build()
+    from rag_kv_cache_rope_gb300 import binding as b
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    chunks, pcts = args.sweep.split(":")
+    chunks = [int(c) for c in chunks.split(",")]
+    rhos = [int(round(float(p) * 100)) for p in pcts.split(",")]
+    packed = None
+    for nc in chunks:
+        S = Setup(synth.sweep_workload(nc, rhos[0]), dev, max_rows_full=True, packed=packed)
+        packed = S.packed
+        for rho in rhos:
+            wl = synth.sweep_workload(nc, rho)
+            req = b.RequestRef(S.req_tok.chunk_ids, S.query, mode=wl.mode, rho_bp=wl.rho_bp, window=wl.window,
+                               tau=wl.tau, budget_mode=wl.budget_mode, scores=S.scores)
+            for _ in range(args.warmup):
+                S.step(req)
+            torch.cuda.synchronize()
+            rows, pairs = S.rows_and_pairs()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with ClockSampler(dev.index) as clk:
+                e0.record()
+                for _ in range(args.steps):
+                    S.step(req)
+                e1.record()
+                torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / args.steps
+            b.blend_device_status(S.h)
+            work = step_work(wl, rows, pairs, rows, pairs)
+            tflop = sum(w[1] for w in work.values() if w[0] == "tensor")
+            ideal_ms = sum(w[3] for w in work.values())
+            print(json.dumps({
+                "sweep": "qwen2.5-14b-shape context x recompute ratio", "workload": wl.name, "n_ctx": S.N,
+                "chunks": f"{nc}x{wl.chunk_len}", "rho_pct": rho / 100, "rows_per_layer": rows,
+                "ttft_ms": ms, "tokens_per_s": S.N / (ms / 1e3), "steps": args.steps, "warmup": args.warmup,
+                "step_roofline": {"ideal_ms": ideal_ms, "frac": ideal_ms / ms, "algorithmic_tflop": tflop / 1e12,
+                                  "peaks": f"{PEAKS_SRC}: bf16 sustained {PEAKS['bf16_tflops_sustained']} "
+                                           f"TF/s, HBM {PEAKS['hbm_gbs']} GB/s"},
+                "clocks": clk.summary()}), flush=True)
+        del S
+        torch.cuda.empty_cache()
 
 
 # ---------------------------------------------------------------- oracle (CPU) arm
@@ -668,6 +737,9 @@ def main():
         line = run_reference(args, wl, rank, world)
         if line:
             print(json.dumps(line), flush=True)
+        return
+    if args.sweep:
+        run_sweep(args)
         return
     if world > 1:
         torch.distributed.init_process_group("nccl")
