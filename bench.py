@@ -46,7 +46,9 @@ except OSError:
 
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
-# capture of each kernel (profiles/), valid only while the kernel's source is unchanged.
+# capture of each kernel (profiles/) on the 14B 16K 20 % request's shapes, valid only for
+# that request and while the kernel's source is unchanged.
+TRAFFIC_WORKLOAD = "qwen14b-16k-ext20"
 TRAFFIC = {
     "gemm_qkv": {"bytes": 128.005888e6 + 31.630080e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
                  "sha256_16": "6655236c82fc5564", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
@@ -61,10 +63,10 @@ TRAFFIC = {
 }
 
 
-def traffic_for(stage: str):
+def traffic_for(stage: str, workload: str):
     import hashlib
     t = TRAFFIC.get(stage)
-    if not t:
+    if not t or workload != TRAFFIC_WORKLOAD:
         return None
     try:
         with open(os.path.join(ROOT, t["source"]), "rb") as f:
@@ -182,8 +184,9 @@ class Setup:
             torch.cuda.empty_cache()
         self.packed = packed
         pool_tok, reqs = synth.workload_tokens(wl)
-        assert wl.batch == 1, "bench times one request per step"
+        self.req_toks = reqs
         self.req_tok = reqs[0]
+        self.batch = Bn = wl.batch
         lens = [wl.chunk_len] * len(pool_tok.chunks)
         self.pool_k, self.pool_v, row_off = synth.random_pool_kv(sh, wl.prefix_len, lens, wl.seed, device=dev)
         tok = torch.cat([torch.cat([pool_tok.prefix, c]) for c in pool_tok.chunks]).to(dev)
@@ -197,29 +200,47 @@ class Setup:
         self.N = wl.n_ctx
         self.n_c = wl.n_chunk_rows
         self.Q = wl.query_len
-        max_rows = self.N if max_rows_full else self.n_c + self.Q
+        max_rows = Bn * (self.N if max_rows_full else self.n_c + self.Q)
         self.cfg = b.model_cfg(sh, self.N)
-        self.lim = b.Limits(max_rows, self.N, self.n_c, 1)
+        self.lim = b.Limits(max_rows, Bn * self.N, self.n_c, Bn)
         self.h = b.blend_init(self.cfg, self.packed, self.lim)
         dt = synth.torch_dtype(sh)
         L = sh.n_layers
-        self.query = self.req_tok.query.to(dev)
-        self.hidden_states = synth.hidden_states(self.n_c, wl.score_layers, wl.score_dim, wl.seed, device=dev,
-                                                 dtype=dt, phrase_max=wl.score_phrase_max)
-        self.scores = torch.empty(self.n_c, dtype=torch.float32, device=dev)
+        # every request's query tokens and small-model hidden states in one tensor each
+        # (request r at rows r*Q and r*n_c), so the host copies of a step are one each
+        self.query = torch.cat([r.query for r in reqs]).to(dev)
+        self.hidden_states = torch.cat([
+            synth.hidden_states(self.n_c, wl.score_layers, wl.score_dim, wl.seed + r, device=dev, dtype=dt,
+                                phrase_max=wl.score_phrase_max) for r in range(Bn)])
+        self.scores = torch.empty(Bn * self.n_c, dtype=torch.float32, device=dev)
         self.out = b.OutputsRef(
-            k=torch.empty(L, self.N, sh.n_kv_heads, sh.head_dim, dtype=dt, device=dev),
-            v=torch.empty(L, self.N, sh.n_kv_heads, sh.head_dim, dtype=dt, device=dev),
-            hidden=torch.empty(self.Q, sh.hidden, dtype=dt, device=dev),
-            sel=torch.empty(self.n_c, dtype=torch.int32, device=dev),
-            n_sel=torch.zeros(b.MAX_BATCH, dtype=torch.int32, device=dev))
-        self.req = b.RequestRef(self.req_tok.chunk_ids, self.query, mode=wl.mode, rho_bp=wl.rho_bp,
-                                r1_bp=wl.r1_bp, window=wl.window, tau=wl.tau, budget_mode=wl.budget_mode,
-                                scores=self.scores, group_rule=wl.group_rule, epic_m=wl.epic_m,
-                                focus_layer=wl.focus_layer, focus_bp=wl.focus_bp)
+            k=torch.empty(L, Bn * self.N, sh.n_kv_heads, sh.head_dim, dtype=dt, device=dev),
+            v=torch.empty(L, Bn * self.N, sh.n_kv_heads, sh.head_dim, dtype=dt, device=dev),
+            hidden=torch.empty(Bn * self.Q, sh.hidden, dtype=dt, device=dev),
+            sel=torch.empty(Bn * self.n_c, dtype=torch.int32, device=dev),
+            n_sel=torch.zeros(b.MAX_BATCH, dtype=torch.int32, device=dev),
+            c1=torch.empty(Bn * self.n_c, dtype=torch.int32, device=dev),
+            n_c1=torch.zeros(b.MAX_BATCH, dtype=torch.int32, device=dev))
+        self.reqs = self.make_reqs()
+        # external scores: from the small model's hidden states (HKVD ranks deviations and
+        # EPIC takes fixed positions, so neither reads them)
+        self.uses_scores = wl.mode == "ext"
         self.aux = None
         if wl.aux_model is not None:
+            assert Bn == 1, "the auxiliary-model workload is one request"
             self._setup_aux(pool_tok, lens, dev)
+
+    def make_reqs(self, **over):
+        """One RequestRef per request of the batch, from the workload, with overrides."""
+        wl, b = self.wl, self.b
+        kw = dict(mode=wl.mode, rho_bp=wl.rho_bp, r1_bp=wl.r1_bp, window=wl.window, tau=wl.tau,
+                  budget_mode=wl.budget_mode, group_rule=wl.group_rule, epic_m=wl.epic_m,
+                  focus_layer=wl.focus_layer, focus_bp=wl.focus_bp)
+        kw.update(over)
+        Q, n_c = self.Q, self.n_c
+        return [b.RequestRef(rt.chunk_ids, self.query[r * Q:(r + 1) * Q],
+                             scores=None if kw["mode"] == "full" else self.scores[r * n_c:(r + 1) * n_c], **kw)
+                for r, rt in enumerate(self.req_toks)]
 
     def _setup_aux(self, pool_tok, lens, dev):
         """CacheClip's auxiliary step: the small model's own chunk-KV pool (same token ids),
@@ -249,22 +270,54 @@ class Setup:
             q_last=torch.empty(nreq * Q, ash.n_q_heads, ash.head_dim, dtype=dt, device=dev))
         self.aux = ash
 
-    def step(self, req=None):
+    def step(self, reqs=None):
         b = self.b
         if self.aux is not None:
             b.blend_prefill(self.aux_h, self.aux_reqs, self.aux_pool, self.aux_out)
             b.aux_attention_scores(self.aux_h, self.aux_reqs, self.aux_pool, self.aux_out, self.scores)
-        else:
-            b.importance_scores(self.hidden_states, self.n_c, self.wl.score_layers, self.wl.score_dim, self.scores)
-        b.blend_prefill(self.h, [req or self.req], self.pool, self.out)
+        elif self.uses_scores:
+            b.importance_scores(self.hidden_states, self.batch * self.n_c, self.wl.score_layers,
+                                self.wl.score_dim, self.scores)
+        b.blend_prefill(self.h, reqs or self.reqs, self.pool, self.out)
+
+    def _rows_pairs(self, key_sel, key_n, with_all=False):
+        """(rows, sum of position + 1) over the batch for the set in out[key_sel] plus the
+        query rows; with_all: every chunk row plus the query rows."""
+        rows, pairs = 0, 0
+        for r in range(self.batch):
+            if with_all:
+                pos = torch.arange(self.wl.prefix_len, self.N)
+            else:
+                n = int(self.out[key_n][r].item())
+                sel = self.out[key_sel][r * self.n_c:r * self.n_c + n].to(torch.int64).cpu()
+                pos = torch.cat([sel, torch.arange(self.N - self.Q, self.N)])
+            rows += int(pos.numel())
+            pairs += int((pos + 1).sum().item())
+        return rows, pairs
 
     def rows_and_pairs(self):
-        """Recomputed rows per layer and sum over them of (position + 1) for the last run."""
-        n = int(self.out["n_sel"][0].item())
-        sel = self.out["sel"][:n].to(torch.int64).cpu()
-        qpos = torch.arange(self.N - self.Q, self.N)
-        pos = torch.cat([sel, qpos])
-        return int(pos.numel()), int((pos + 1).sum().item())
+        """Recomputed rows per layer and sum over them of (position + 1) for the last run
+        (the final set, summed over the batch)."""
+        return self._rows_pairs("sel", "n_sel")
+
+    def layer_sets(self, focus_rp=None):
+        """Per layer (rows whose K/V are projected, rows of attention and MLP, their causal
+        pairs) for the last run.  HKVD: layer 0 recomputes every chunk row, layer 1 projects
+        every row and continues with the first candidates C1, layer 2 projects C1 and
+        continues with the final set; the focus filter projects the first set at its layer
+        and continues with the filtered one (focus_rp = rows, pairs before the filter)."""
+        L = self.wl.model.n_layers
+        r2, p2 = self.rows_and_pairs()
+        if self.wl.mode == "hkvd":
+            r0, p0 = self._rows_pairs(None, None, with_all=True)
+            r1, p1 = self._rows_pairs("c1", "n_c1")
+            seq = [(r0, r0, p0), (r0, r1, p1), (r1, r2, p2)] + [(r2, r2, p2)] * (L - 3)
+            return seq[:L]
+        if focus_rp is not None and self.wl.focus_bp:
+            fl = self.wl.focus_layer
+            r0, p0 = focus_rp
+            return [(r0, r0, p0) if l < fl else (r0, r2, p2) if l == fl else (r2, r2, p2) for l in range(L)]
+        return [(r2, r2, p2)] * L
 
 
 def algorithmic(sh: synth.ModelShape, rows: int, pairs: int, wl: synth.Workload) -> dict:
@@ -276,13 +329,13 @@ def algorithmic(sh: synth.ModelShape, rows: int, pairs: int, wl: synth.Workload)
     H, d, F = sh.hidden, sh.head_dim, sh.ffn
     qd, kvd = sh.n_q_heads * d, sh.n_kv_heads * d
     es = 2 if sh.dtype == "bf16" else 4
-    asm_bytes = 2 * 2 * sh.n_layers * (wl.prefix_len + wl.n_chunk_rows) * kvd * es
+    asm_bytes = 2 * 2 * sh.n_layers * wl.batch * (wl.prefix_len + wl.n_chunk_rows) * kvd * es
     return {
         "gemm_qkv": ("tensor", 2.0 * rows * H * (qd + 2 * kvd), es * (H * (qd + 2 * kvd) + rows * H + rows * (qd + 2 * kvd))),
         "gemm_o": ("tensor", 2.0 * rows * qd * H, es * (qd * H + rows * qd) + rows * H * (8 + es)),
         "gemm_gate_up": ("tensor", 2.0 * rows * H * 2 * F, es * (H * 2 * F + rows * H + rows * F)),
         "gemm_down": ("tensor", 2.0 * rows * F * H, es * (F * H + rows * F) + rows * H * (8 + es)),
-        "attention": ("tensor", 4.0 * d * sh.n_q_heads * pairs, es * (2 * wl.n_ctx * kvd + 2 * rows * qd)),
+        "attention": ("tensor", 4.0 * d * sh.n_q_heads * pairs, es * (2 * wl.batch * wl.n_ctx * kvd + 2 * rows * qd)),
         "assemble": ("hbm", float(asm_bytes), float(asm_bytes)),
     }
 
@@ -296,24 +349,23 @@ def ideal_launch_ms(entry) -> float:
     return max(t_cmp, t_mem) * 1e3
 
 
-def step_work(wl: synth.Workload, rows0: int, pairs0: int, rows1: int, pairs1: int, aux_rp=None) -> dict:
+def step_work(wl: synth.Workload, layers: list, aux_rp=None) -> dict:
     """{stage: (bound, algorithmic units per step, launches per step, roofline ms per step)}
-    for one step.  Layers before the focus layer run the first set (rows0, pairs0), later
-    ones the filtered set; the focus layer projects K/V for the first set and runs attention
-    and MLP on the second.  aux_rp = (rows, pairs) of the auxiliary model's layers, counted
-    under aux_* names."""
+    for one step.  layers[l] = (rows whose K/V layer l projects, rows of its attention and
+    MLP, their causal pairs), summed over the batch.  aux_rp = (rows, pairs) of the
+    auxiliary model's layers, counted under aux_* names."""
     sh = wl.model
     L = sh.n_layers
-    fl = wl.focus_layer if wl.focus_bp else L
-    w0, w1 = algorithmic(sh, rows0, pairs0, wl), algorithmic(sh, rows1, pairs1, wl)
     out = {}
-    for k in w0:
-        if k == "assemble":
-            out[k] = (w0[k][0], w0[k][1], 1, ideal_launch_ms(w0[k]))
-            continue
-        n0 = min(L, fl + 1) if k == "gemm_qkv" else min(L, fl)
-        out[k] = (w0[k][0], n0 * w0[k][1] + (L - n0) * w1[k][1], L,
-                  n0 * ideal_launch_ms(w0[k]) + (L - n0) * ideal_launch_ms(w1[k]))
+    for l, (rows_kv, rows, pairs) in enumerate(layers):
+        wkv, w = algorithmic(sh, rows_kv, 0, wl), algorithmic(sh, rows, pairs, wl)
+        for k in w:
+            if k == "assemble":
+                out[k] = (w[k][0], w[k][1], 1, ideal_launch_ms(w[k]))
+                continue
+            e = wkv[k] if k == "gemm_qkv" else w[k]
+            b0, u0, n0, t0 = out.get(k, (e[0], 0.0, 0, 0.0))
+            out[k] = (b0, u0 + e[1], n0 + 1, t0 + ideal_launch_ms(e))
     if aux_rp is not None:
         ash = wl.aux_model
         wa = algorithmic(ash, aux_rp[0], aux_rp[1], wl)
@@ -334,34 +386,49 @@ def run_ours(args, wl, rank, world):
         S.step()
     torch.cuda.synchronize()
     rows, pairs = S.rows_and_pairs()
-    rows0, pairs0 = rows, pairs
+    focus_rp = None
     if wl.focus_bp:
         # the set before the focus filter: the same request without it
-        nofocus = dataclasses.replace(wl, focus_bp=0)
-        S.req = b.RequestRef(S.req_tok.chunk_ids, S.query, mode=wl.mode, rho_bp=wl.rho_bp, r1_bp=wl.r1_bp,
-                             window=wl.window, tau=wl.tau, budget_mode=wl.budget_mode, scores=S.scores,
-                             group_rule=wl.group_rule, epic_m=wl.epic_m)
+        S.step(S.make_reqs(focus_layer=0, focus_bp=0))
+        torch.cuda.synchronize()
+        focus_rp = S.rows_and_pairs()
         S.step()
         torch.cuda.synchronize()
-        rows0, pairs0 = S.rows_and_pairs()
-        S.req = b.RequestRef(S.req_tok.chunk_ids, S.query, mode=wl.mode, rho_bp=wl.rho_bp, r1_bp=wl.r1_bp,
-                             window=wl.window, tau=wl.tau, budget_mode=wl.budget_mode, scores=S.scores,
-                             group_rule=wl.group_rule, epic_m=wl.epic_m, focus_layer=wl.focus_layer,
-                             focus_bp=wl.focus_bp)
-        del nofocus
+    layers = S.layer_sets(focus_rp)
     aux_rp = None
     if S.aux is not None:
         nq = len(S.req_tok.chunk_ids) * S.Q
         ctx = sum(wl.prefix_len + wl.chunk_len for _ in S.req_tok.chunk_ids)
         aux_rp = (nq, S.Q * ctx + len(S.req_tok.chunk_ids) * S.Q * (S.Q + 1) // 2)
-    # timed region: K steps between barriers, per-stage events recorded live
+    # stage shares: K untimed steps with an event pair around every stage of every layer
+    # (the pairs add small gaps between kernels, so the timed region below records only
+    # the dominant stage)
+    b.blend_profile(S.h, True)
+    if S.aux is not None:
+        b.blend_profile(S.aux_h, True)
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    p0.record()
+    for _ in range(args.steps):
+        S.step()
+    p1.record()
+    torch.cuda.synchronize()
+    ms_all_stages = p0.elapsed_time(p1) / args.steps
+    prof = b.blend_profile_read(S.h)
+    b.blend_profile(S.h, False)
+    if S.aux is not None:
+        for k, v in b.blend_profile_read(S.aux_h).items():
+            prof["aux_" + k] = v
+        b.blend_profile(S.aux_h, False)
+    shares = {k: v[0] for k, v in prof.items()}
+    dom = max(shares, key=shares.get)
+    dom_h, dom_name = (S.aux_h, dom[4:]) if dom.startswith("aux_") else (S.h, dom)
+
+    # timed region: K steps between barriers; the dominant stage's launches timed live
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     l0 = b.blend_launch_count()
-    b.blend_profile(S.h, True)
-    if S.aux is not None:
-        b.blend_profile(S.aux_h, True)
+    b.blend_profile_stages(dom_h, [dom_name])
     stream = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(dev.index) as clk:
@@ -372,43 +439,39 @@ def run_ours(args, wl, rank, world):
         torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / args.steps
     launches = b.blend_launch_count() - l0
-    prof = b.blend_profile_read(S.h)
-    b.blend_profile(S.h, False)
-    if S.aux is not None:
-        for k, v in b.blend_profile_read(S.aux_h).items():
-            prof["aux_" + k] = v
-        b.blend_profile(S.aux_h, False)
+    dom_ms = b.blend_profile_read(dom_h)[dom_name][0]
+    b.blend_profile(dom_h, False)
     if world > 1:
         t = torch.tensor([ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms = float(t.item())
         torch.distributed.barrier()
-    value = world * S.N / (ms / 1e3)
+    value = world * S.batch * S.N / (ms / 1e3)
 
-    # roofline of the stage with the largest share of device time
-    work = step_work(wl, rows0, pairs0, rows, pairs, aux_rp)
-    shares = {k: v[0] for k, v in prof.items()}
+    # roofline of the stage with the largest share of device time, from its launches in
+    # the timed region
+    work = step_work(wl, layers, aux_rp)
     total = sum(shares.values()) or 1.0
-    dom = max(shares, key=shares.get)
     roof = None
     if dom in work:
         kind, step_units, per_step, _ = work[dom]
         units = step_units / per_step  # average work of one launch
         n_launch = args.steps * per_step
-        avg_ms = prof[dom][0] / n_launch
+        avg_ms = dom_ms / n_launch
         if kind == "tensor":
             peak = PEAKS["bf16_tflops_sustained"] if sh.dtype == "bf16" else None
             ach = units / (avg_ms / 1e3) / 1e12
             roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
-                    "frac": (ach / peak) if peak else None, "traffic": traffic_for(dom),
+                    "frac": (ach / peak) if peak else None, "traffic": traffic_for(dom, wl.name),
                     "peak_source": f"{PEAKS_SRC} bf16 sustained", "avg_launch_ms": avg_ms}
         else:
             ach = units / (avg_ms / 1e3) / 1e9
             roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": PEAKS["hbm_gbs"], "unit": "GB/s",
-                    "frac": ach / PEAKS["hbm_gbs"], "traffic": traffic_for(dom), "peak_source": f"{PEAKS_SRC} hbm",
+                    "frac": ach / PEAKS["hbm_gbs"], "traffic": traffic_for(dom, wl.name), "peak_source": f"{PEAKS_SRC} hbm",
                     "avg_launch_ms": avg_ms}
     stages = {k: {"ms_per_step": v[0] / args.steps, "share": v[0] / total, "launches": v[1]}
               for k, v in prof.items() if v[1]}
+
     # whole-step roofline: every GEMM/attention launch at max(FLOP / tensor peak, bytes /
     # HBM bandwidth) plus the assembly at the HBM peak, over the measured step
     tflop = sum(w[1] for k, w in work.items() if w[0] == "tensor")
@@ -425,7 +488,9 @@ def run_ours(args, wl, rank, world):
                    "group_rule": wl.group_rule, "pool": args.pool, "epic_m": wl.epic_m,
                    "focus": [wl.focus_layer, wl.focus_bp] if wl.focus_bp else None,
                    "aux_model": wl.aux_model.name if wl.aux_model else None,
-                   "rows_per_layer": rows, "rows_before_focus": rows0 if wl.focus_bp else None,
+                   "batch": S.batch, "rows_per_layer": rows,
+                   "rows_before_focus": focus_rp[0] if focus_rp else None,
+                   "rows_first_layers": [x[1] for x in layers[:3]] if wl.mode == "hkvd" else None,
                    "layers": sh.n_layers, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (weights %.1f GB, chunk pool %.1f GB)" % (
                        sum(t.numel() * t.element_size() for t in S.packed.values()) / 1e9,
@@ -437,27 +502,30 @@ def run_ours(args, wl, rank, world):
                           "peaks": f"{PEAKS_SRC}: bf16 sustained {PEAKS['bf16_tflops_sustained']} TF/s, "
                                    f"HBM {PEAKS['hbm_gbs']} GB/s"},
         "stages": stages,
+        "stages_pass": {"ms_per_step": ms_all_stages, "how": "stage times from a separate pass of K steps with an "
+                        "event pair around every stage; the timed region records only the dominant stage"},
         "tensor_cores": bool(b.blend_set_tensor_cores(S.h, True)),
     }
     if not args.no_e2e:
         line["e2e"] = e2e(S, args, world)
     if args.full_prefill_steps > 0 and world == 1:
         # the same input with every row recomputed, on a handle sized for all N rows
-        hf = b.blend_init(S.cfg, S.packed, b.Limits(S.N, S.N, S.n_c, 1))
-        full = b.RequestRef(S.req_tok.chunk_ids, S.query, mode="full")
-        b.blend_prefill(hf, [full], S.pool, S.out)
+        Bn = S.batch
+        hf = b.blend_init(S.cfg, S.packed, b.Limits(Bn * S.N, Bn * S.N, S.n_c, Bn))
+        full = S.make_reqs(mode="full")
+        b.blend_prefill(hf, full, S.pool, S.out)
         torch.cuda.synchronize()
         f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         f0.record()
         for _ in range(args.full_prefill_steps):
-            b.blend_prefill(hf, [full], S.pool, S.out)
+            b.blend_prefill(hf, full, S.pool, S.out)
         f1.record()
         torch.cuda.synchronize()
         b.blend_device_status(hf)
         del hf
         torch.cuda.empty_cache()
         fms = f0.elapsed_time(f1) / args.full_prefill_steps
-        line["full_prefill"] = {"ttft_ms": fms, "tokens_per_s": S.N / (fms / 1e3), "speedup_of_blend": fms / ms,
+        line["full_prefill"] = {"ttft_ms": fms, "tokens_per_s": Bn * S.N / (fms / 1e3), "speedup_of_blend": fms / ms,
                                 "steps": args.full_prefill_steps}
         line["loading"] = loading(S, args, fms)
     return line, S
@@ -470,7 +538,7 @@ def loading(S: Setup, args, full_ms: float) -> dict:
     b = S.b
     sh = S.wl.model
     es = 2 if sh.dtype == "bf16" else 4
-    kv_bytes = 2.0 * sh.n_layers * (S.wl.prefix_len + S.n_c) * sh.n_kv_heads * sh.head_dim * es
+    kv_bytes = 2.0 * sh.n_layers * S.batch * (S.wl.prefix_len + S.n_c) * sh.n_kv_heads * sh.head_dim * es
     a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if S.pool_loc == "host":
         # what the pipelined path does: copy-engine transfers of the pool into HBM
@@ -482,7 +550,7 @@ def loading(S: Setup, args, full_ms: float) -> dict:
     else:
         kind = "assembly of every layer from the HBM pool"
         def once():
-            b.blend_assemble(S.h, [S.req], S.pool, S.out)
+            b.blend_assemble(S.h, S.reqs, S.pool, S.out)
     once()
     torch.cuda.synchronize()
     a0.record()
@@ -506,7 +574,8 @@ def e2e(S: Setup, args, world):
     """Same step through the C ABI with host inputs: pinned H2D of query tokens and the
     small model's hidden states, D2H of the first-token hidden state, every step."""
     b = S.b
-    aux = S.aux is not None  # the auxiliary model scores on the GPU: no hidden states come in
+    # the auxiliary model scores on the GPU, and HKVD / EPIC use no scores: no hidden states come in
+    aux = S.aux is not None or not S.uses_scores
     hs_host = None if aux else S.hidden_states.cpu().pin_memory()
     q_host = S.query.cpu().pin_memory()
     out_host = torch.empty_like(S.out["hidden"], device="cpu").pin_memory()
@@ -533,7 +602,7 @@ def e2e(S: Setup, args, world):
         t = torch.tensor([dt], device=S.dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         dt = float(t.item())
-    return {"value": world * S.N / dt, "unit": "tokens/s", "ttft_ms": dt * 1e3, "h2d_bytes_per_step": h2d,
+    return {"value": world * S.batch * S.N / dt, "unit": "tokens/s", "ttft_ms": dt * 1e3, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h}
 
 
@@ -557,8 +626,7 @@ def run_sweep(args):
         packed = S.packed
         for rho in rhos:
             wl = synth.sweep_workload(nc, rho)
-            req = b.RequestRef(S.req_tok.chunk_ids, S.query, mode=wl.mode, rho_bp=wl.rho_bp, window=wl.window,
-                               tau=wl.tau, budget_mode=wl.budget_mode, scores=S.scores)
+            req = S.make_reqs(rho_bp=wl.rho_bp)
             for _ in range(args.warmup):
                 S.step(req)
             torch.cuda.synchronize()
@@ -572,7 +640,7 @@ def run_sweep(args):
                 torch.cuda.synchronize()
             ms = e0.elapsed_time(e1) / args.steps
             b.blend_device_status(S.h)
-            work = step_work(wl, rows, pairs, rows, pairs)
+            work = step_work(wl, [(rows, rows, pairs)] * wl.model.n_layers)
             tflop = sum(w[1] for w in work.values() if w[0] == "tensor")
             ideal_ms = sum(w[3] for w in work.values())
             print(json.dumps({
@@ -680,7 +748,10 @@ class OracleSample:
             sample += f"; auxiliary scoring of 1 of {wl.n_chunks} chunks (x{wl.n_chunks})"
         if wl.focus_bp:
             sample += "; the focus filter is not modelled (every layer at the first set)"
-        return {"est_step_s": est, "sample_s": t_asm + t_sel + t_layer, "N": N, "sample": sample}
+        if wl.batch > 1:
+            sample += f"; request 1 of the batch of {wl.batch} (x{wl.batch})"
+        return {"est_step_s": est * wl.batch, "sample_s": t_asm + t_sel + t_layer, "N": N * wl.batch,
+                "sample": sample}
 
     def rows_for(self, target_s: float) -> int:
         """Row subset that makes one sample take about target_s seconds (after calibrate)."""

@@ -248,11 +248,15 @@ int topk_select_dilate_noalloc(const float* scores, int32_t n, int32_t base, int
  * of blend_prefill / selective_layer (assemble, select, plan_gather, rmsnorm,
  * gemm_qkv, rope_kv, attention, gemm_o, gemm_gate_up, gemm_down, final_norm).
  * blend_profile(h, 1) clears the record and starts recording; (h, 0) stops.
- * blend_profile_read waits for the recorded events, writes per-stage total ms and
+ * blend_profile_stages(h, mask) does the same for only the stages whose bit
+ * (1 << stage index, the order above) is set in mask (0 stops): every recorded stage
+ * adds an event pair on the stream, so timing one stage this way disturbs the step
+ * least.  blend_profile_read waits for the recorded events, writes per-stage total ms and
  * kernel launch counts for the first n stages, clears the record and returns the
  * number of stages.  blend_launch_count() is the process-wide number of kernels the
- * library has launched. */
+ * library has launched.  Errors: BLEND_EINVAL for a NULL handle. */
 int blend_profile(blend_handle* h, int enable);
+int blend_profile_stages(blend_handle* h, uint32_t stage_mask);
 int blend_profile_read(blend_handle* h, double* ms, int64_t* launches, int32_t n);
 const char* blend_profile_name(int32_t i);
 int64_t blend_launch_count(void);

@@ -114,6 +114,7 @@ def lib() -> C.CDLL:
                                         C.POINTER(Outputs), vp]),
             "importance_scores": (C.c_int, [vp, i32, i32, i32, i32, vp, vp]),
             "blend_profile": (C.c_int, [vp, C.c_int]),
+            "blend_profile_stages": (C.c_int, [vp, C.c_uint32]),
             "blend_profile_read": (C.c_int, [vp, C.POINTER(C.c_double), C.POINTER(C.c_int64), i32]),
             "blend_profile_name": (C.c_char_p, [i32]),
             "blend_launch_count": (C.c_int64, []),
@@ -137,7 +138,7 @@ def lib() -> C.CDLL:
 EXPORTED = ("blend_workspace_size", "blend_init", "blend_destroy", "blend_last_error",
             "blend_device_status", "blend_set_tensor_cores", "rope_realign", "blend_assemble",
             "kv_deviation", "topk_select_dilate", "gather_rows", "scatter_kv", "selective_layer",
-            "blend_prefill", "importance_scores", "blend_profile", "blend_profile_read",
+            "blend_prefill", "importance_scores", "blend_profile", "blend_profile_stages", "blend_profile_read",
             "blend_profile_name", "blend_launch_count", "topk_select_dilate_noalloc", "span_select",
             "align_expand", "aux_attention_scores", "blend_ratio_controller", "blend_pick_storage")
 
@@ -219,6 +220,17 @@ def blend_set_tensor_cores(h: Handle, on: bool) -> int:
 
 def blend_profile(h: Handle, enable: bool):
     _check(lib().blend_profile(h.ptr, 1 if enable else 0), h)
+
+
+def blend_profile_stages(h: Handle, stages: Sequence[str]):
+    """Record only the named stages (an empty list stops recording)."""
+    names = [lib().blend_profile_name(i).decode() for i in range(32)]
+    mask = 0
+    for st in stages:
+        if st not in names:
+            raise ValueError(f"unknown profiler stage {st!r}")
+        mask |= 1 << names.index(st)
+    _check(lib().blend_profile_stages(h.ptr, mask), h)
 
 
 def blend_profile_read(h: Handle) -> dict:

@@ -101,6 +101,7 @@ struct blend_handle {
     std::string last_error;
     // profiler
     bool prof_on = false;
+    uint32_t prof_mask = 0xffffffffu;  // stages recorded while prof_on (bit = stage)
     std::vector<ProfRec> prof;            // events recorded since the last read
     std::vector<cudaEvent_t> ev_pool;     // reusable events
     size_t ev_used = 0;
@@ -131,7 +132,7 @@ struct ProfScope {
     cudaEvent_t a = nullptr;
     long long l0 = 0;
     ProfScope(blend_handle* h_, int cat_, cudaStream_t s_) : h(h_), s(s_), cat(cat_) {
-        if (h && h->prof_on && h->prof.size() < 100000) {
+        if (h && h->prof_on && ((h->prof_mask >> cat) & 1u) && h->prof.size() < 100000) {
             a = h->next_event();
             if (a) cudaEventRecord(a, s);
             l0 = g_launches.load();
@@ -527,10 +528,15 @@ int blend_set_tensor_cores(blend_handle* h, int on) {
 }
 
 int blend_profile(blend_handle* h, int enable) {
+    return blend_profile_stages(h, enable != 0 ? 0xffffffffu : 0u);
+}
+
+int blend_profile_stages(blend_handle* h, uint32_t stage_mask) {
     if (!h) return fail(nullptr, BLEND_EINVAL, "handle is NULL");
     h->prof.clear();
     h->ev_used = 0;
-    h->prof_on = enable != 0;
+    h->prof_on = stage_mask != 0;
+    h->prof_mask = stage_mask;
     return BLEND_OK;
 }
 
