@@ -165,6 +165,18 @@ class ClockSampler:
                 "samples": len(sm), "power_w": statistics.median(pw) if pw else None}
 
 
+# ---------------------------------------------------------------- ranks
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest of every rank's x (the slowest replica sets the job's time); the
+    identity on one rank.  device: where the collective's buffer lives (cuda for NCCL,
+    cpu for gloo)."""
+    if world <= 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ---------------------------------------------------------------- our arm
 class Setup:
     """Device-resident inputs, weights, handle and outputs for one replica."""
@@ -441,10 +453,8 @@ def run_ours(args, wl, rank, world):
     launches = b.blend_launch_count() - l0
     dom_ms = b.blend_profile_read(dom_h)[dom_name][0]
     b.blend_profile(dom_h, False)
+    ms = max_over_ranks(ms, world, dev)
     if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
         torch.distributed.barrier()
     value = world * S.batch * S.N / (ms / 1e3)
 
@@ -598,10 +608,7 @@ def e2e(S: Setup, args, world):
     for _ in range(args.steps):
         one()
     dt = (time.perf_counter() - t0) / args.steps
-    if world > 1:
-        t = torch.tensor([dt], device=S.dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        dt = float(t.item())
+    dt = max_over_ranks(dt, world, S.dev)
     return {"value": world * S.batch * S.N / dt, "unit": "tokens/s", "ttft_ms": dt * 1e3, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h}
 
