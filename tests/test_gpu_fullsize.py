@@ -231,3 +231,100 @@ def test_qwen14b_sweep_100_percent_equals_full_prefill():
         check(f"14B 4K rho100 {mode} hidden", o["hidden"], hf[-fc.Q:])
         check(f"14B 4K rho100 {mode} K", o["k"], kf)
         check(f"14B 4K rho100 {mode} V", o["v"], vf)
+
+
+def test_qwen14b_16k_ext20_full_depth_sampled():
+    """All 48 layers, in the launch configuration bench.py times (a handle sized for the
+    chunk rows plus the query, scores from the GPU's own importance kernel), checked on
+    outputs the oracle computes row by row: the selected set exactly (the oracle's
+    selection on the GPU's score array), every layer's reused rows against the oracle's
+    realignment of the pool rows (V and the one prefix copy bit for bit), layer 0's
+    recomputed K/V of sampled selected and query rows against the oracle's projection,
+    and, on every layer, that the selected and query rows were overwritten.  The final
+    hidden rows must have unit RMS (final RMSNorm with unit gains) at any size."""
+    wl = synth.WORKLOADS["qwen14b-16k-ext20"]
+    sh = wl.model
+    d = dev()
+    L, H, hkv, hd = sh.n_layers, sh.hidden, sh.n_kv_heads, sh.head_dim
+    P, N, n_c, Q = wl.prefix_len, wl.n_ctx, wl.n_chunk_rows, wl.query_len
+    w = synth.model_weights(sh, wl.seed, device=d)
+    w0 = {k: f64(w[k][0]) for k in ("attn_norm", "wk", "wv")}
+    embed = w["embed"]
+    packed = b.pack_weights(w)
+    del w
+    torch.cuda.empty_cache()
+    pool_tok, reqs = synth.workload_tokens(wl)
+    req = reqs[0]
+    lens = [wl.chunk_len] * len(pool_tok.chunks)
+    pk, pv, row_off = synth.random_pool_kv(sh, P, lens, wl.seed, device=d)
+    tok = torch.cat([torch.cat([pool_tok.prefix, c]) for c in pool_tok.chunks]).to(d)
+    pool = b.PoolRef(pk, pv, tok, P, lens, row_off)
+    h = b.blend_init(b.model_cfg(sh, N), packed, b.Limits(n_c + Q, N, n_c, 1))
+    hs = synth.hidden_states(n_c, wl.score_layers, wl.score_dim, wl.seed, device=d, dtype=torch.bfloat16)
+    scores = torch.empty(n_c, dtype=torch.float32, device=d)
+    b.importance_scores(hs, n_c, wl.score_layers, wl.score_dim, scores)
+    out = b.OutputsRef(k=torch.zeros(L, N, hkv, hd, dtype=torch.bfloat16, device=d),
+                       v=torch.zeros(L, N, hkv, hd, dtype=torch.bfloat16, device=d),
+                       hidden=torch.zeros(Q, H, dtype=torch.bfloat16, device=d),
+                       sel=torch.full((n_c,), -1, dtype=torch.int32, device=d),
+                       n_sel=torch.zeros(b.MAX_BATCH, dtype=torch.int32, device=d))
+    b.blend_prefill(h, [b.RequestRef(req.chunk_ids, req.query.to(d), mode="ext", rho_bp=wl.rho_bp,
+                                     window=wl.window, tau=wl.tau, budget_mode=wl.budget_mode, scores=scores)],
+                    pool, out)
+    b.blend_device_status(h)
+    torch.cuda.synchronize()
+
+    # the set, exactly
+    s64 = scores.cpu().numpy().astype(np.float64)
+    want = O.select_final_bisect(s64, O.ceil_bp(wl.rho_bp, n_c), wl.window, wl.tau, base=P)
+    n = int(out["n_sel"][0].item())
+    sel = out["sel"][:n].cpu().numpy().astype(np.int64)
+    assert sel.tolist() == want.tolist()
+
+    # reused rows of every layer: the pool row of their chunk, rotated by the chunk's shift
+    rng = np.random.default_rng(5)
+    chunk_pos = np.arange(P, P + n_c)
+    reused = np.setdiff1d(chunk_pos, sel)
+    pick = np.sort(rng.choice(reused, size=128, replace=False))
+    j, t = (pick - P) // wl.chunk_len, (pick - P) % wl.chunk_len
+    src = np.array([row_off[req.chunk_ids[jj]] for jj in j]) + P + t
+    delta = j * wl.chunk_len
+    idx_d, src_d = torch.from_numpy(pick).to(d), torch.from_numpy(src).to(d)
+    got_k, got_v = f64(out["k"][:, idx_d]), f64(out["v"][:, idx_d])
+    pool_k, pool_v = f64(pk[:, src_d]), f64(pv[:, src_d])
+    assert np.array_equal(got_v, pool_v)
+    want_k = np.stack([O.realign_keys(pool_k[l], delta, sh.rope_theta) for l in range(L)])
+    check("14B 48-layer reused K (128 rows x 48 layers)", got_k, want_k)
+    # the one prefix copy: chunk 0's entry, every layer, bit for bit
+    p0 = row_off[req.chunk_ids[0]]
+    assert torch.equal(out["k"][:, :P], pk[:, p0:p0 + P]) and torch.equal(out["v"][:, :P], pv[:, p0:p0 + P])
+
+    # layer 0's recomputed rows: RMSNorm, K/V projection, RoPE at the blended position
+    qpos = np.arange(N - Q, N)
+    rows = np.concatenate([np.sort(rng.choice(sel, size=32, replace=False)), qpos[::16]])
+    jr, tr = (rows - P) // wl.chunk_len, (rows - P) % wl.chunk_len
+    toks = np.array([int(pool_tok.chunks[req.chunk_ids[a]][b_]) if r < N - Q else int(req.query[r - (N - Q)])
+                     for a, b_, r in zip(jr, tr, rows)])
+    x = f64(embed[torch.from_numpy(toks).to(d)])
+    hn = O.rmsnorm(x, w0["attn_norm"], sh.rms_eps)
+    k0 = O.rope_rotate((hn @ w0["wk"].T).reshape(len(rows), hkv, hd), rows, sh.rope_theta)
+    v0 = (hn @ w0["wv"].T).reshape(len(rows), hkv, hd)
+    rd = torch.from_numpy(rows).to(d)
+    check("14B 48-layer layer-0 recomputed K", out["k"][0, rd], k0)
+    check("14B 48-layer layer-0 recomputed V", out["v"][0, rd], v0)
+
+    # every layer overwrote its selected and query rows: far from the realigned pool rows
+    # (random pool values), nonzero for the query rows (the outputs started at zero)
+    jj, tt = (rows[:32] - P) // wl.chunk_len, (rows[:32] - P) % wl.chunk_len
+    ssrc = torch.from_numpy(np.array([row_off[req.chunk_ids[a]] for a in jj]) + P + tt).to(d)
+    gv, pvs = f64(out["v"][:, rd[:32]]), f64(pv[:, ssrc])
+    for l in range(L):
+        assert relerr(gv[l], pvs[l]) > 0.5, l
+    qv = f64(out["v"][:, torch.from_numpy(qpos).to(d)])
+    assert np.all(np.isfinite(qv)) and np.all(np.abs(qv).reshape(L, -1).max(axis=1) > 0)
+    assert torch.isfinite(out["k"].float()).all() and torch.isfinite(out["v"].float()).all()
+
+    hid = f64(out["hidden"])
+    assert np.all(np.isfinite(hid))
+    rms = np.sqrt(np.mean(hid * hid, axis=1))
+    assert np.max(np.abs(rms - 1.0)) < 1e-2, rms

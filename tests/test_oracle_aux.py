@@ -96,3 +96,20 @@ def test_scores_are_a_share_of_each_row():
     assert np.allclose(b, np.concatenate([blocks[2], blocks[0], blocks[1]]))
     for blk in blocks:
         assert 0.0 < blk.sum() < 1.0 and np.all(blk > 0)
+
+
+def test_column_means_closed_forms():
+    """Direct pins of the column mean: a zero query attends uniformly over the keys at or
+    before its position, so every column below the smallest query position has the mean of
+    1 / (pos + 1) over the rows; and when the columns cover every key any row sees, the
+    means add up to one (each row's weights do)."""
+    rng = np.random.default_rng(3)
+    K = rng.normal(size=(20, 2, 8))
+    qpos = np.array([9, 14, 19])
+    zero = O.column_mean_scores(np.zeros((3, 4, 8)), qpos, K, 0, 10)
+    assert np.allclose(zero, np.mean(1.0 / (qpos + 1)))
+    q = rng.normal(size=(3, 4, 8))
+    full = O.column_mean_scores(q, qpos, K, 0, 20)
+    assert np.isclose(full.sum(), 1.0) and np.all(full >= 0)
+    # columns past every query position get no weight
+    assert np.all(O.column_mean_scores(q, np.array([3, 4, 5]), K, 6, 20) == 0)
