@@ -582,22 +582,28 @@ __global__ void __launch_bounds__(THREADS, 1)
 //                 each CTA's 64 keys) into the S buffer of the block's parity
 //   O += P . V    tcgen05.mma.cta_group::2 M256 N128 K16 x8 (A: each CTA's P in TMEM;
 //                 B: each CTA's 64 d columns of V, MN-major)
-// S is double-buffered in TMEM: S(j+1) is issued before P(j) is ready and S(j+2) right
-// after P.V(j), so a softmax goes from block to block without waiting for the tensor
-// core.  One commit after P.V(j) and S(j+2) both releases block j's K/V stage and tells
-// the softmax that S(j+2) is there (an item's first two S products have their own).  A softmax that must rescale O (running maximum up by more than 2^8) first waits
-// for the previous block's P.V, whose completion releases that block's K/V stage.  The
-// softmax is the single-tile one of k_attn_tc, one pair row per thread.
+// S and P each have two TMEM buffers (S: 128 fp32 columns, P: 64 columns of bf16 pairs),
+// indexed by the block's parity, and two threads of the leading CTA issue the products:
+// one issues S(j) once the softmax of block j-2 has read that S buffer (its P is ready) and
+// commits it to s_full; the other issues P.V(j) once P(j) is ready and commits it to
+// kv_empty, which frees block j's K/V stage and P buffer.  A single issuer spent about 650
+// of every 1 650 cycles per block on barrier checks and commits between its bursts while
+// the tensor core, with an issue queue about one product deep, sat idle; two issuers
+// overlap those gaps.  A softmax writes P(j) only after P.V(j-2) has read that P buffer,
+// and one that must rescale O (running maximum up by more than 2^8) first waits for
+// P.V(j-1).  The softmax is the single-tile one of k_attn_tc, one pair row per thread.
 namespace pairk {
-constexpr int THREADS2 = 192;  // warp 0 TMA, 1 TMEM + MMA issue (leader), 2..5 softmax
+constexpr int THREADS2 = 224;  // warp 0 TMA, 1 TMEM + P.V issue, 2..5 softmax, 6 S issue (leaders)
+constexpr int S_WARP = 6;
 constexpr int STAGES2 = 5;
 constexpr int KQ_BYTES = 64 * 64 * 2;                  // 64 keys x one 64-wide d half
 constexpr int VH_BYTES = BKV * 64 * 2;                 // 128 keys x this CTA's 64 d columns
 constexpr int STAGE_BYTES = 2 * KQ_BYTES + VH_BYTES;   // 32 KB
 constexpr int QT_BYTES = 2 * QH_BYTES;                 // one 128-pair tile, two d halves
 constexpr int SMEM_BYTES = 2 * QT_BYTES + STAGES2 * STAGE_BYTES + 1024;
-constexpr int COLS2 = 512;  // S buffers at 0 and 128, O at 256
+constexpr int COLS2 = 512;  // S buffers at 0 and 128, O at 256, P buffers at 384 and 448
 constexpr uint32_t O_COL = 256;
+constexpr uint32_t P_COL = 384;
 // kind::f16, bf16 inputs, fp32 accumulate, M256 (the pair) N128; P.V with B MN-major
 constexpr uint32_t IDESC_S2 = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((256u >> 4) << 24);
 constexpr uint32_t IDESC_PV2 = IDESC_S2 | (1u << 16);
@@ -813,18 +819,12 @@ __global__ void __launch_bounds__(pairk::THREADS2, 1)
                 tma_3d_pair(b + 2 * KQ_BYTES, &mapV, kf, 64 * rank, m.g, tok);
             }
         }
-    } else if (warp == 1 && lane == 0 && rank == 0) {
-        // ------------------------------------------------ MMA issuer (leader, for both CTAs)
+    } else if (warp == S_WARP && lane == 0 && rank == 0) {
+        // ------------------------------------------------ S issuer (leader, for both CTAs)
+        // S(it) goes into S buffer it & 1 once the softmax of block it - 2 has read that
+        // buffer (its P is ready), and is committed to s_full on its own
         uint32_t it = 0;
         bool ok = true;
-        auto issue_s2 = [&](uint32_t sd, uint64_t qd, uint64_t kd) {
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (kk & 3) * 32, half = kk >> 2;
-                umma_ss2(sd, qd + ((half * QH_BYTES + off) >> 4), kd + ((half * KQ_BYTES + off) >> 4), IDESC_S2,
-                         kk > 0 ? 1u : 0u);
-            }
-        };
         for (int k = 0, tl = 0; ok && !abort_flag; ++k, ++tl) {
             const int w = item_of(k);
             if (w >= total) break;
@@ -836,22 +836,44 @@ __global__ void __launch_bounds__(pairk::THREADS2, 1)
                 break;
             }
             pend_q[qb] = -1;
-            fence_after();
             const uint64_t qd = desc_k(su32(sQ + qb * QT_BYTES));
-            // S of the item's first two blocks
-            for (int j = 0; j < 2 && j < m.nblk; ++j) {
-                const uint32_t g = it + j;
-                const int st = g % STAGES2;
-                if (!wait_cl(&kv_full[st], (g / STAGES2) & 1, &abort_flag)) {
+            for (int kb = 0; kb < m.nblk; ++kb, ++it) {
+                const int b = it & 1, st = it % STAGES2;
+                if ((it >= 2 && !wait_cl(&p_full[b], ((it - 2) >> 1) & 1, &abort_flag)) ||
+                    !wait_cl(&kv_full[st], (it / STAGES2) & 1, &abort_flag)) {
                     ok = false;
                     break;
                 }
                 pend_kv[st] = -1;
                 fence_after();
-                issue_s2(tb + (g & 1) * 128, qd, desc_k(su32(sKV + st * STAGE_BYTES)));
-                commit2(&s_full[g & 1]);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk & 3) * 32, half = kk >> 2;
+                    umma_ss2(tb + b * 128, qd + ((half * QH_BYTES + off) >> 4),
+                             desc_k(su32(sKV + st * STAGE_BYTES)) + ((half * KQ_BYTES + off) >> 4), IDESC_S2,
+                             kk > 0 ? 1u : 0u);
+                }
+                commit2(&s_full[b]);
             }
-            for (int kb = 0; kb < m.nblk && ok; ++kb, ++it) {
+            if (!ok) break;
+            commit2(&q_empty[qb]);  // every S product of the item has read this Q tile
+        }
+        if (!ok) {
+            abort_flag = 1;
+            set_error(err, BLEND_ETIMEOUT);
+        }
+    } else if (warp == 1 && lane == 0 && rank == 0) {
+        // ------------------------------------------------ P.V issuer (leader, for both CTAs)
+        // P.V(it) once both CTAs' softmax warps have written P(it); its commit frees block
+        // it's K/V stage (S(it) completed before that softmax began) and its P buffer
+        uint32_t it = 0;
+        bool ok = true;
+        for (int k = 0, tl = 0; ok && !abort_flag; ++k, ++tl) {
+            const int w = item_of(k);
+            if (w >= total) break;
+            Item m;
+            get_item(w, n_req, req_row_end, row_pos, row_tok, group, hkv, m);
+            for (int kb = 0; kb < m.nblk; ++kb, ++it) {
                 const int b = it & 1, st = it % STAGES2;
                 if (!wait_cl(&p_full[b], (it >> 1) & 1, &abort_flag) ||
                     (kb == 0 && !wait_cl(&o_free, (tl & 1) ^ 1, &abort_flag))) {
@@ -859,45 +881,27 @@ __global__ void __launch_bounds__(pairk::THREADS2, 1)
                     break;
                 }
                 fence_after();
-                {
-                    const uint64_t vd = desc_mn(su32(sKV + st * STAGE_BYTES + 2 * KQ_BYTES));
-                    const uint32_t pa = tb + b * 128;
+                const uint64_t vd = desc_mn(su32(sKV + st * STAGE_BYTES + 2 * KQ_BYTES));
+                const uint32_t pa = tb + P_COL + b * 64;
 #pragma unroll
-                    for (int kk = 0; kk < BKV / 16; ++kk)
-                        umma_ts2(tb + O_COL, pa + kk * 8, vd + ((kk * 2048) >> 4), IDESC_PV2,
-                                 (kb > 0 || kk > 0) ? 1u : 0u);
-                }
-                if (kb + 2 < m.nblk) {
-                    const uint32_t g = it + 2;
-                    const int st2 = g % STAGES2;
-                    if (!wait_cl(&kv_full[st2], (g / STAGES2) & 1, &abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    pend_kv[st2] = -1;
-                    fence_after();
-                    // into the buffer P(it) occupies: the tensor core runs it after P.V(it)
-                    issue_s2(tb + b * 128, qd, desc_k(su32(sKV + st2 * STAGE_BYTES)));
-                }
-                // completes with P.V(it) and S(it + 2): block it's stage is free, S(it + 2) ready
+                for (int kk = 0; kk < BKV / 16; ++kk)
+                    umma_ts2(tb + O_COL, pa + kk * 8, vd + ((kk * 2048) >> 4), IDESC_PV2, (kb > 0 || kk > 0) ? 1u : 0u);
                 commit2(&kv_empty[st]);
             }
             if (!ok) break;
             commit2(&o_full);
-            commit2(&q_empty[qb]);
         }
         if (!ok) {
             abort_flag = 1;
             set_error(err, BLEND_ETIMEOUT);
         }
-    } else if (warp >= 2) {
+    } else if (warp >= 2 && warp < S_WARP) {
         // ------------------------------------------------ softmax of this CTA's tile + output
         const int sp = warp & 3;  // TMEM lane quarter of this warp
         const int r_in = sp * 32 + lane;
         const uint32_t lane_off = (uint32_t)(sp * 32) << 16;
         const uint32_t o_col = tb + lane_off + O_COL;
         uint32_t it = 0;
-        uint32_t s_uses0 = 0, s_uses1 = 0;  // completions of s_full[0], [1] so far (an item's first two S)
         bool ok = true;
         for (int k = 0, tl = 0; ok; ++k, ++tl) {
             const int w = item_of(k);
@@ -914,17 +918,10 @@ __global__ void __launch_bounds__(pairk::THREADS2, 1)
             for (int kb = 0; kb < m.nblk; ++kb, ++it) {
                 const int b = it & 1;
                 const uint32_t s_col = tb + lane_off + b * 128;
-                bool got;
-                if (kb < 2) {
-                    got = warp_wait_cl(&s_full[b], (b ? s_uses1 : s_uses0) & 1, &abort_flag);
-                    if (b) ++s_uses1;
-                    else ++s_uses0;
-                } else {
-                    // S(it) came with the commit after P.V(it - 2) (at most one use of that
-                    // stage behind)
-                    const uint32_t pv = it - 2;
-                    got = warp_wait_cl(&kv_empty[pv % STAGES2], (pv / STAGES2) & 1, &abort_flag);
-                }
+                const uint32_t p_col = tb + lane_off + P_COL + b * 64;
+                // S(it) is the (it / 2)-th product into S buffer b; S(it + 2) waits for this
+                // block's P, so the barrier is never a phase ahead
+                const bool got = warp_wait_cl(&s_full[b], (it >> 1) & 1, &abort_flag);
                 if (!got) {
                     ok = false;
                     break;
@@ -973,8 +970,18 @@ __global__ void __launch_bounds__(pairk::THREADS2, 1)
                     s[e] = pack_bf16x2(p0, p1);
                 }
                 const float2 accs = __fadd2_rn(acc2[0], acc2[1]);
-                TMEM_ST32(s_col, s);
-                TMEM_ST32(s_col + 32, (s + 32));
+                if (it >= 2) {
+                    // P buffer b is free once P.V(it - 2) has read it (that block's stage is
+                    // released by the same commit, at most one use of the stage behind)
+                    const uint32_t pv = it - 2;
+                    if (!warp_wait_cl(&kv_empty[pv % STAGES2], (pv / STAGES2) & 1, &abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_after();
+                }
+                TMEM_ST32(p_col, s);
+                TMEM_ST32(p_col + 32, (s + 32));
                 if (rescale && kb > 0) {
                     // O must hold every block before this one: wait for the previous P.V
                     // (the previous block's stage is released when its P.V completes, at most
