@@ -233,16 +233,16 @@ def test_qwen14b_sweep_100_percent_equals_full_prefill():
         check(f"14B 4K rho100 {mode} V", o["v"], vf)
 
 
-def test_qwen14b_16k_ext20_full_depth_sampled():
+def full_depth_sampled(wl, tag):
     """All 48 layers, in the launch configuration bench.py times (a handle sized for the
     chunk rows plus the query, scores from the GPU's own importance kernel), checked on
     outputs the oracle computes row by row: the selected set exactly (the oracle's
     selection on the GPU's score array), every layer's reused rows against the oracle's
-    realignment of the pool rows (V and the one prefix copy bit for bit), layer 0's
-    recomputed K/V of sampled selected and query rows against the oracle's projection,
-    and, on every layer, that the selected and query rows were overwritten.  The final
-    hidden rows must have unit RMS (final RMSNorm with unit gains) at any size."""
-    wl = synth.WORKLOADS["qwen14b-16k-ext20"]
+    realignment of the pool rows (V and the one prefix copy bit for bit; the sample includes
+    the context's last reused rows, the largest offsets), layer 0's recomputed K/V of
+    sampled selected and query rows against the oracle's projection, and, on every layer,
+    that the selected and query rows were overwritten.  The final hidden rows must have
+    unit RMS (final RMSNorm with unit gains) at any size."""
     sh = wl.model
     d = dev()
     L, H, hkv, hd = sh.n_layers, sh.hidden, sh.n_kv_heads, sh.head_dim
@@ -285,7 +285,7 @@ def test_qwen14b_16k_ext20_full_depth_sampled():
     rng = np.random.default_rng(5)
     chunk_pos = np.arange(P, P + n_c)
     reused = np.setdiff1d(chunk_pos, sel)
-    pick = np.sort(rng.choice(reused, size=128, replace=False))
+    pick = np.unique(np.concatenate([rng.choice(reused, size=120, replace=False), reused[-8:]]))
     j, t = (pick - P) // wl.chunk_len, (pick - P) % wl.chunk_len
     src = np.array([row_off[req.chunk_ids[jj]] for jj in j]) + P + t
     delta = j * wl.chunk_len
@@ -294,7 +294,7 @@ def test_qwen14b_16k_ext20_full_depth_sampled():
     pool_k, pool_v = f64(pk[:, src_d]), f64(pv[:, src_d])
     assert np.array_equal(got_v, pool_v)
     want_k = np.stack([O.realign_keys(pool_k[l], delta, sh.rope_theta) for l in range(L)])
-    check("14B 48-layer reused K (128 rows x 48 layers)", got_k, want_k)
+    check(f"{tag} reused K ({len(pick)} rows x 48 layers)", got_k, want_k)
     # the one prefix copy: chunk 0's entry, every layer, bit for bit
     p0 = row_off[req.chunk_ids[0]]
     assert torch.equal(out["k"][:, :P], pk[:, p0:p0 + P]) and torch.equal(out["v"][:, :P], pv[:, p0:p0 + P])
@@ -310,8 +310,8 @@ def test_qwen14b_16k_ext20_full_depth_sampled():
     k0 = O.rope_rotate((hn @ w0["wk"].T).reshape(len(rows), hkv, hd), rows, sh.rope_theta)
     v0 = (hn @ w0["wv"].T).reshape(len(rows), hkv, hd)
     rd = torch.from_numpy(rows).to(d)
-    check("14B 48-layer layer-0 recomputed K", out["k"][0, rd], k0)
-    check("14B 48-layer layer-0 recomputed V", out["v"][0, rd], v0)
+    check(f"{tag} layer-0 recomputed K", out["k"][0, rd], k0)
+    check(f"{tag} layer-0 recomputed V", out["v"][0, rd], v0)
 
     # every layer overwrote its selected and query rows: far from the realigned pool rows
     # (random pool values), nonzero for the query rows (the outputs started at zero)
@@ -328,3 +328,13 @@ def test_qwen14b_16k_ext20_full_depth_sampled():
     assert np.all(np.isfinite(hid))
     rms = np.sqrt(np.mean(hid * hid, axis=1))
     assert np.max(np.abs(rms - 1.0)) < 1e-2, rms
+
+
+def test_qwen14b_16k_ext20_full_depth_sampled():
+    full_depth_sampled(synth.WORKLOADS["qwen14b-16k-ext20"], "14B 16K 48-layer")
+
+
+def test_qwen14b_32k_ext20_full_depth_sampled():
+    """The largest context of the sweep (63 chunks, 32 448 tokens: every K and V output is
+    over 2^31 bytes at 48 layers, and the chunk rows are near the 32 768-row limit)."""
+    full_depth_sampled(synth.sweep_workload(63, 2000), "14B 32K 48-layer")
