@@ -35,6 +35,7 @@ sys.path.insert(0, ROOT)
 
 from rag_kv_cache_rope_gb300 import synth  # noqa: E402
 
+METRIC = "blended-prefill context tokens/s & TTFT ms (16K ctx, 20% recomp), % roofline"
 PEAKS = {"hbm_gbs": 6789.0, "bf16_tflops": 1874.3, "bf16_tflops_sustained": 1722.0}
 PEAKS_SRC = "fallback"
 try:
@@ -451,6 +452,7 @@ def run_ours(args, wl, rank, world):
         torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / args.steps
     launches = b.blend_launch_count() - l0
+    b.blend_device_status(S.h)  # raises if a kernel recorded an error (a bounded wait that expired, a bad index)
     dom_ms = b.blend_profile_read(dom_h)[dom_name][0]
     b.blend_profile(dom_h, False)
     ms = max_over_ranks(ms, world, dev)
@@ -487,7 +489,7 @@ def run_ours(args, wl, rank, world):
     tflop = sum(w[1] for k, w in work.items() if w[0] == "tensor")
     ideal_ms = sum(w[3] for w in work.values())
     line = {
-        "metric": "blended-prefill context tokens/s (16K ctx, 20% recompute), TTFT ms, % roofline",
+        "metric": METRIC,
         "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms, "ttft_ms": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if sh.dtype == "bf16" else "f32",
@@ -608,6 +610,7 @@ def e2e(S: Setup, args, world):
     for _ in range(args.steps):
         one()
     dt = (time.perf_counter() - t0) / args.steps
+    b.blend_device_status(S.h)
     dt = max_over_ranks(dt, world, S.dev)
     return {"value": world * S.batch * S.N / dt, "unit": "tokens/s", "ttft_ms": dt * 1e3, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h}
@@ -793,7 +796,7 @@ def run_reference(args, wl, rank, world):
     v = ests[0]["N"] / est
     return {
         "impl": "reference",
-        "metric": "blended-prefill context tokens/s (16K ctx, 20% recompute), TTFT ms, % roofline",
+        "metric": METRIC,
         "value": v, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": est * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic", "config": {"workload": wl.name},
