@@ -589,7 +589,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 // kv_empty, which frees block j's K/V stage and P buffer.  A single issuer spent about 650
 // of every 1 650 cycles per block on barrier checks and commits between its bursts while
 // the tensor core, with an issue queue about one product deep, sat idle; two issuers
-// overlap those gaps.  A softmax writes P(j) only after P.V(j-2) has read that P buffer,
+// overlap those gaps.  The softmax skips the block maximum while its running reference
+// keeps every exponential of the block below 2^50 (the block's sum says so); a row's
+// first block and any block past that bound take the exact path (maximum, conditional
+// rescale by more than 2^8).  A softmax writes P(j) only after P.V(j-2) has read that P buffer,
 // and one that must rescale O (running maximum up by more than 2^8) first waits for
 // P.V(j-1).  The softmax is the single-tile one of k_attn_tc, one pair row per thread.
 namespace pairk {
@@ -939,37 +942,74 @@ __global__ void __launch_bounds__(pairk::THREADS2, 1)
                     for (int i = 0; i < 128; ++i)
                         if (k0 + i > my_pos) s[i] = __float_as_uint(-INFINITY);
                 }
-                float mx;
-                {
-                    float a[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) a[i] = fmaxf(__uint_as_float(s[i]), __uint_as_float(s[i + 8]));
-#pragma unroll
-                    for (int i = 16; i < 128; i += 16)
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) a[c] = max3f(a[c], __uint_as_float(s[i + c]), __uint_as_float(s[i + 8 + c]));
-                    mx = max3f(max3f(a[0], a[1], a[2]), max3f(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
-                }
-                const float mxs = mx * scale_log2;
-                const bool need = mxs > m_used + RESCALE_LOG2;
-                const bool rescale = __any_sync(0xffffffffu, need);
+                const float2 sc2 = make_float2(scale_log2, scale_log2);
+                float2 accs = make_float2(0.f, 0.f);
+                bool rescale = false;
                 float corr = 1.f;
-                if (rescale) {
-                    const float m_new = need ? mxs : m_used;
-                    corr = ex2(m_used - m_new);
-                    l *= corr;
-                    m_used = m_new;
-                }
-                float2 acc2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-                const float2 sc2 = make_float2(scale_log2, scale_log2), nm2 = make_float2(-m_used, -m_used);
+                // Fast path: exponentiate against the running reference without this block's
+                // maximum.  Values up to 2^50 are exact enough in fp32 and bf16 and far from
+                // overflow in P, the row sum and O, so only a block whose sum passes 2^50 (or
+                // a row's first block) takes the exact path below with its maximum and rescale.
+                bool exact = !__all_sync(0xffffffffu, m_used != -INFINITY);
+                if (!exact) {
+                    float2 acc2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                    const float2 nm2 = make_float2(-m_used, -m_used);
 #pragma unroll
-                for (int e = 0; e < 64; ++e) {
-                    const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1])), sc2, nm2);
-                    const float p0 = ex2(x.x), p1 = ex2(x.y);
-                    acc2[e & 1] = __fadd2_rn(acc2[e & 1], make_float2(p0, p1));
-                    s[e] = pack_bf16x2(p0, p1);
+                    for (int e = 0; e < 64; ++e) {
+                        const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1])), sc2, nm2);
+                        const float p0 = ex2(x.x), p1 = ex2(x.y);
+                        acc2[e & 1] = __fadd2_rn(acc2[e & 1], make_float2(p0, p1));
+                        s[e] = pack_bf16x2(p0, p1);
+                    }
+                    accs = __fadd2_rn(acc2[0], acc2[1]);
+                    exact = __any_sync(0xffffffffu, !(accs.x + accs.y <= 0x1p50f));
+                    if (exact) {
+                        // the scores were overwritten by P: load them again
+                        TMEM_LD32(s_col, s);
+                        TMEM_LD32(s_col + 32, (s + 32));
+                        TMEM_LD32(s_col + 64, (s + 64));
+                        TMEM_LD32(s_col + 96, (s + 96));
+                        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                        if (k0 + BKV - 1 > my_pos) {
+#pragma unroll
+                            for (int i = 0; i < 128; ++i)
+                                if (k0 + i > my_pos) s[i] = __float_as_uint(-INFINITY);
+                        }
+                    }
                 }
-                const float2 accs = __fadd2_rn(acc2[0], acc2[1]);
+                if (exact) {
+                    float mx;
+                    {
+                        float a[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) a[i] = fmaxf(__uint_as_float(s[i]), __uint_as_float(s[i + 8]));
+#pragma unroll
+                        for (int i = 16; i < 128; i += 16)
+#pragma unroll
+                            for (int c = 0; c < 8; ++c)
+                                a[c] = max3f(a[c], __uint_as_float(s[i + c]), __uint_as_float(s[i + 8 + c]));
+                        mx = max3f(max3f(a[0], a[1], a[2]), max3f(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
+                    }
+                    const float mxs = mx * scale_log2;
+                    const bool need = mxs > m_used + RESCALE_LOG2;
+                    rescale = __any_sync(0xffffffffu, need);
+                    if (rescale) {
+                        const float m_new = need ? mxs : m_used;
+                        corr = ex2(m_used - m_new);
+                        l *= corr;
+                        m_used = m_new;
+                    }
+                    float2 acc2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                    const float2 nm2 = make_float2(-m_used, -m_used);
+#pragma unroll
+                    for (int e = 0; e < 64; ++e) {
+                        const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1])), sc2, nm2);
+                        const float p0 = ex2(x.x), p1 = ex2(x.y);
+                        acc2[e & 1] = __fadd2_rn(acc2[e & 1], make_float2(p0, p1));
+                        s[e] = pack_bf16x2(p0, p1);
+                    }
+                    accs = __fadd2_rn(acc2[0], acc2[1]);
+                }
                 if (it >= 2) {
                     // P buffer b is free once P.V(it - 2) has read it (that block's stage is
                     // released by the same commit, at most one use of the stage behind)
