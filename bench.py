@@ -59,8 +59,8 @@ TRAFFIC = {
                      "sha256_16": "6655236c82fc5564", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
     "gemm_down": {"bytes": 588.014336e6 + 91.328256e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
                   "sha256_16": "6655236c82fc5564", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
-    "attention": {"bytes": 139.731200e6 + 13.170688e6, "source": "rag_kv_cache_rope_gb300/csrc/attn_tc.cu",
-                  "sha256_16": "1964e8ba7635c8a6", "profile": "profiles/attn_tc_qwen14b_16k_layer.md"},
+    "attention": {"bytes": 143.852544e6 + 13.177088e6, "source": "rag_kv_cache_rope_gb300/csrc/attn_tc.cu",
+                  "sha256_16": "d6e3a54a7cce8fa0", "profile": "profiles/attn_tc_qwen14b_16k_layer.md"},
 }
 
 
