@@ -218,6 +218,21 @@ const char* blend_last_error(const blend_handle* h);
  * device-side check of an earlier call on this handle failed (bad positions in a
  * caller-given set, an out-of-range shift, an expired bounded wait).  Clears the word. */
 int blend_device_status(blend_handle* h, void* stream);
+/* Bounded device-side wait (the pages have no counterpart): enqueues on the stream a wait
+ * until *flag (device int32, 4-byte aligned) is nonzero, polling at most max_polls times
+ * with a short sleep (~64 ns) between polls.  If the flag stays 0 the handle's error word
+ * gets BLEND_ETIMEOUT and the wait ends: blend_device_status then returns BLEND_ETIMEOUT
+ * (and clears the word), and the handle and the CUDA context stay usable.  Every
+ * device-side wait inside the library's kernels is bounded the same way; this call lets
+ * a caller (or a test) exercise that timeout path on purpose, without a trap or a hang.
+ * The flag must be set by something that does not need the GPU's SMs to progress (a
+ * copy, or the host through mapped memory); a kernel queued behind this wait on the
+ * same stream never sets it.
+ * Errors: BLEND_EINVAL for a NULL handle or flag, an unaligned flag, or max_polls
+ * outside 0..BLEND_MAX_WAIT_POLLS (nothing is launched). */
+#define BLEND_MAX_WAIT_POLLS (1ll << 24)
+int blend_wait_flag(blend_handle* h, const int32_t* flag, int64_t max_polls, void* stream);
+
 /* Turns the tcgen05 tensor-core GEMM/attention on (1) or off (0) for a bf16 handle;
  * off uses the CUDA-core kernels.  Returns the setting in effect (0 for fp32 handles
  * and on GPUs without tcgen05). */

@@ -115,6 +115,7 @@ def lib() -> C.CDLL:
             "importance_scores": (C.c_int, [vp, i32, i32, i32, i32, vp, vp]),
             "blend_profile": (C.c_int, [vp, C.c_int]),
             "blend_profile_stages": (C.c_int, [vp, C.c_uint32]),
+            "blend_wait_flag": (C.c_int, [vp, vp, i64, vp]),
             "blend_profile_read": (C.c_int, [vp, C.POINTER(C.c_double), C.POINTER(C.c_int64), i32]),
             "blend_profile_name": (C.c_char_p, [i32]),
             "blend_launch_count": (C.c_int64, []),
@@ -138,7 +139,7 @@ def lib() -> C.CDLL:
 EXPORTED = ("blend_workspace_size", "blend_init", "blend_destroy", "blend_last_error",
             "blend_device_status", "blend_set_tensor_cores", "rope_realign", "blend_assemble",
             "kv_deviation", "topk_select_dilate", "gather_rows", "scatter_kv", "selective_layer",
-            "blend_prefill", "importance_scores", "blend_profile", "blend_profile_stages", "blend_profile_read",
+            "blend_prefill", "importance_scores", "blend_profile", "blend_profile_stages", "blend_wait_flag", "blend_profile_read",
             "blend_profile_name", "blend_launch_count", "topk_select_dilate_noalloc", "span_select",
             "align_expand", "aux_attention_scores", "blend_ratio_controller", "blend_pick_storage")
 
@@ -212,6 +213,12 @@ def blend_destroy(h: Handle):
 
 def blend_device_status(h: Handle, stream=None) -> int:
     return _check(lib().blend_device_status(h.ptr, _stream(stream)), h)
+
+
+def blend_wait_flag(h: Handle, flag: torch.Tensor, max_polls: int, stream=None):
+    """Bounded device-side wait until flag (device int32 scalar) is nonzero; on expiry the
+    handle's error word records BLEND_ETIMEOUT (raised by blend_device_status)."""
+    _check(lib().blend_wait_flag(h.ptr, _ptr(flag), int(max_polls), _stream(stream)), h)
 
 
 def blend_set_tensor_cores(h: Handle, on: bool) -> int:

@@ -2,6 +2,7 @@
 // blended prefill (assemble -> select -> per-layer selective recompute -> final norm).
 // Every argument is checked on the host before the first launch; nothing here
 // synchronises the device except blend_device_status.
+#include <nvtx3/nvToolsExt.h>
 #include <math.h>
 #include <stdarg.h>
 #include <stdio.h>
@@ -124,7 +125,16 @@ struct blend_handle {
 };
 
 namespace {
-// Times the launches made in its lifetime under one profiler category.
+// An NVTX range for the lifetime of a scope (shown on a profiler's timeline).
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
+
+// Times the launches made in its lifetime under one profiler category, and marks them as
+// an NVTX range named after the stage (a no-op unless a profiler is attached).
 struct ProfScope {
     blend_handle* h;
     cudaStream_t s;
@@ -132,6 +142,7 @@ struct ProfScope {
     cudaEvent_t a = nullptr;
     long long l0 = 0;
     ProfScope(blend_handle* h_, int cat_, cudaStream_t s_) : h(h_), s(s_), cat(cat_) {
+        nvtxRangePushA(kProfNames[cat]);
         if (h && h->prof_on && ((h->prof_mask >> cat) & 1u) && h->prof.size() < 100000) {
             a = h->next_event();
             if (a) cudaEventRecord(a, s);
@@ -146,6 +157,7 @@ struct ProfScope {
                 h->prof.push_back(ProfRec{a, b, cat, g_launches.load() - l0});
             }
         }
+        nvtxRangePop();
     }
 };
 }  // namespace
@@ -519,6 +531,17 @@ int blend_device_status(blend_handle* h, void* stream) {
                     "device-side check failed (code %d)", e);
     }
     return BLEND_OK;
+}
+
+int blend_wait_flag(blend_handle* h, const int32_t* flag, int64_t max_polls, void* stream) {
+    if (!h) return fail(nullptr, BLEND_EINVAL, "handle is NULL");
+    if (!flag) return fail(h, BLEND_EINVAL, "flag is NULL");
+    if (((uintptr_t)flag & 3) != 0) return fail(h, BLEND_EINVAL, "flag must be 4-byte aligned");
+    if (max_polls < 0 || max_polls > BLEND_MAX_WAIT_POLLS)
+        return fail(h, BLEND_EINVAL, "max_polls=%lld outside 0..%lld", (long long)max_polls,
+                    (long long)BLEND_MAX_WAIT_POLLS);
+    launch_wait_flag(flag, (long long)max_polls, h->err, (cudaStream_t)stream);
+    return check_cuda(h, "blend_wait_flag");
 }
 
 int blend_set_tensor_cores(blend_handle* h, int on) {
@@ -986,6 +1009,7 @@ extern "C" int blend_prefill(blend_handle* h, int32_t n_req, const blend_request
     std::vector<ReqInfo> info;
     int rc = validate_batch(h, n_req, reqs, pool, out, &info);
     if (rc != BLEND_OK) return rc;
+    NvtxRange call_range("blend_prefill");
     const blend_model_cfg& c = h->cfg;
     cudaStream_t s = (cudaStream_t)stream;
     const int mode = reqs[0].mode;
@@ -1154,6 +1178,9 @@ extern "C" int blend_prefill(blend_handle* h, int32_t n_req, const blend_request
     float* x = h->x;
     float* x_alt = h->x2;
     for (int l = 0; l < c.n_layers; ++l) {
+        char layer_name[24];
+        snprintf(layer_name, sizeof layer_name, "layer %d", l);
+        NvtxRange layer_range(layer_name);
         void* kc = (char*)out->k + (size_t)l * layer_elems * es;
         void* vc = (char*)out->v + (size_t)l * layer_elems * es;
         const Plan& p = h->plan[cur];

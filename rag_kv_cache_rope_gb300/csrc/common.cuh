@@ -164,6 +164,7 @@ struct EpicTable {
     int32_t req_n[BLEND_MAX_BATCH];
 };
 void launch_epic_set(const EpicTable& et, int32_t* set, int32_t* set_n, cudaStream_t s);
+void launch_wait_flag(const int32_t* flag, long long max_polls, int32_t* err, cudaStream_t s);
 // Cache-Craft focus filter: request r's chunks are chunk0[r] .. chunk0[r]+n_chunks[r]-1 of the
 // tables (start = blended position of the chunk's first token, len = its tokens).
 struct FocusTable {

@@ -188,6 +188,24 @@ void launch_epic_set(const EpicTable& et, int32_t* set, int32_t* set_n, cudaStre
     note_launch(1);
 }
 
+// Bounded wait on a caller's device flag: one thread polls until *flag != 0, at most
+// max_polls times with a short sleep between polls; if the flag never changes the error
+// word gets BLEND_ETIMEOUT and the kernel returns (no trap, the context stays usable).
+__global__ void k_wait_flag(const int32_t* flag, long long max_polls, int32_t* err) {
+    if (threadIdx.x != 0) return;
+    const volatile int32_t* f = flag;
+    for (long long i = 0; i < max_polls; ++i) {
+        if (*f != 0) return;
+        __nanosleep(64);
+    }
+    set_error(err, BLEND_ETIMEOUT);
+}
+
+void launch_wait_flag(const int32_t* flag, long long max_polls, int32_t* err, cudaStream_t s) {
+    k_wait_flag<<<1, 32, 0, s>>>(flag, max_polls, err);
+    note_launch(1);
+}
+
 // Token id of every blended token: prefix and chunk rows from the pool, query rows
 // from each request's query tokens.
 __global__ void k_tokens(const __grid_constant__ SegTable segs,

@@ -136,6 +136,7 @@ def test_init_rejects_bad_arguments_without_a_gpu(lib):
     vp = C.c_void_p(1 << 20)
     assert lib.span_select(None, vp, 8, 0, 4, 4, 0.4, 7000, 16, b.BUDGET_FINAL, vp, vp, None) == b.EINVAL
     assert lib.align_expand(None, vp, vp, 4, 0, vp, vp, 4, 8, 0, vp, vp, None) == b.EINVAL
+    assert lib.blend_wait_flag(None, vp, 10, None) == b.EINVAL
 
 
 def test_pack_weights_layout():
