@@ -400,3 +400,115 @@ def test_forced_schedule_reproduces_hkvd(tiny_setup):
     np.testing.assert_array_equal(a["K"], b["K"])
     np.testing.assert_array_equal(a["dev1"], b["dev1"])
     np.testing.assert_array_equal(a["dev2"], b["dev2"])
+
+
+# ---------------------------------------------------------------- layer wiring, closed forms
+# These pin the decoder layer's composition (residuals, O projection orientation, which
+# SwiGLU branch carries the SiLU, RMSNorm before the MLP) and the deviation's magnitude
+# with weights chosen so that every intermediate has a closed form (CacheBlend blog,
+# "Selective KV recompute": the recomputed rows go through the ordinary layer;
+# "Picking the tokens to recompute": the deviation between fresh and cached KV).
+
+def _layer_setup(seed=20):
+    cfg = tiny_cfg(n_layers=1)
+    w = tiny_weights(cfg, seed)
+    r = np.random.default_rng(seed)
+    N = 9
+    K = r.standard_normal((N, 2, 8))
+    V = r.standard_normal((N, 2, 8))
+    pos = np.array([2, 5, 8])
+    x = r.standard_normal((3, 32))
+    q = r.standard_normal((3, 4, 8))
+    return cfg, w, K, V, pos, x, q
+
+
+def test_layer_rest_is_identity_without_output_projections():
+    """wo = 0 and wd = 0: attention and MLP contribute nothing, so the two residual
+    connections return the input rows unchanged, bit for bit."""
+    cfg, w, K, V, pos, x, q = _layer_setup()
+    w["wo"][0] = 0.0
+    w["wd"][0] = 0.0
+    np.testing.assert_array_equal(O.layer_rest(w, cfg, 0, x, q, pos, K, V), x)
+
+
+def test_layer_rest_zero_query_adds_mean_value_through_wo():
+    """q = 0 makes every logit 0, so each row's attention output is the plain mean of
+    its kv head's values over keys 0..pos; with wo a permutation (row i picks o's column
+    perm[i]) and wd = 0, output column i gains that mean's column perm[i]."""
+    cfg, w, K, V, pos, x, q = _layer_setup(21)
+    q = np.zeros_like(q)
+    perm = np.random.default_rng(3).permutation(32)
+    wo = np.zeros((32, 32))
+    wo[np.arange(32), perm] = 1.0
+    w["wo"][0] = wo
+    w["wd"][0] = 0.0
+    out = O.layer_rest(w, cfg, 0, x, q, pos, K, V)
+    want = x.copy()
+    for i, p in enumerate(pos):
+        o = np.zeros(32)
+        for h in range(4):                          # query head h reads kv head h // 2
+            o[h * 8:(h + 1) * 8] = V[:p + 1, h // 2].sum(axis=0) / (p + 1)
+        for col in range(32):
+            want[i, col] += o[perm[col]]
+    np.testing.assert_allclose(out, want, rtol=1e-13, atol=1e-14)
+
+
+def test_layer_rest_one_hot_mlp_adds_silu_gate_times_up():
+    """wo = 0; gate row f reads input column a, up row f reads column b, down sends unit
+    f to output column j: column j gains silu(n_a) * n_b with n the RMS-normalised row
+    (unit gains), every other column is unchanged."""
+    cfg, w, K, V, pos, x, q = _layer_setup(22)
+    a, bcol, f, j = 3, 17, 5, 29
+    w["wo"][0] = 0.0
+    w["wg"][0] = 0.0
+    w["wu"][0] = 0.0
+    w["wd"][0] = 0.0
+    w["wg"][0][f, a] = 1.0
+    w["wu"][0][f, bcol] = 1.0
+    w["wd"][0][j, f] = 1.0
+    out = O.layer_rest(w, cfg, 0, x, q, pos, K, V)
+    want = x.copy()
+    for i in range(3):
+        rms = math.sqrt(sum(v * v for v in x[i]) / 32 + 1e-6)
+        na, nb = x[i, a] / rms, x[i, bcol] / rms
+        want[i, j] += na / (1.0 + math.exp(-na)) * nb
+    np.testing.assert_allclose(out, want, rtol=1e-13, atol=1e-14)
+    # the SiLU sits on the gate branch: swapping the branches changes the result
+    w["wg"][0][f, a], w["wg"][0][f, bcol] = 0.0, 1.0
+    w["wu"][0][f, bcol], w["wu"][0][f, a] = 0.0, 1.0
+    assert not np.allclose(O.layer_rest(w, cfg, 0, x, q, pos, K, V), want)
+
+
+def test_deviation_of_constant_offsets():
+    """wk = wv = 0 makes the fresh K and V rows zero at every position (a rotation of zero
+    is zero), so against caches holding the constants cK and cV the deviation is
+    hkv*d*(cK^2 + cV^2) in KV mode and hkv*d*cV^2 in V mode, taken before the overwrite
+    (the cache rows are zero afterwards); rows outside dev_rows report 0."""
+    cfg, w, K, V, pos, x, q = _layer_setup(23)
+    w["wk"][0] = 0.0
+    w["wv"][0] = 0.0
+    cK, cV = 0.75, -2.5
+    for mode, want in (("kv", 2 * 8 * (cK * cK + cV * cV)), ("v", 2 * 8 * cV * cV)):
+        Kc = np.full((9, 2, 8), cK)
+        Vc = np.full((9, 2, 8), cV)
+        rows = np.array([True, False, True])
+        _, dev = O.layer_kv(w, cfg, 0, x, pos, Kc, Vc, rows, mode)
+        np.testing.assert_allclose(dev, [want, 0.0, want], rtol=1e-15)
+        assert np.all(Kc[pos] == 0) and np.all(Vc[pos] == 0)
+        untouched = np.setdiff1d(np.arange(9), pos)
+        assert np.all(Kc[untouched] == cK) and np.all(Vc[untouched] == cV)
+
+
+def test_deviation_of_a_known_value_row():
+    """wv picks input column c for every value unit and wk = 0: the fresh V row is the
+    normalised x[c] everywhere (values are not rotated), so against a zero cache the KV
+    deviation is hkv*d*n_c^2, at any position."""
+    cfg, w, K, V, pos, x, q = _layer_setup(24)
+    c = 11
+    w["wk"][0] = 0.0
+    w["wv"][0] = 0.0
+    w["wv"][0][:, c] = 1.0
+    _, dev = O.layer_kv(w, cfg, 0, x, pos, np.zeros((9, 2, 8)), np.zeros((9, 2, 8)), np.ones(3, bool))
+    for i in range(3):
+        n_c = x[i, c] / math.sqrt(sum(v * v for v in x[i]) / 32 + 1e-6)
+        assert abs(dev[i] - 16 * n_c * n_c) <= 1e-12 * 16 * n_c * n_c
