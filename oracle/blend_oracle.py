@@ -121,20 +121,34 @@ def attention(q: np.ndarray, qpos: np.ndarray, K: np.ndarray, V: np.ndarray) -> 
     softmax(q.k / sqrt(d)).  Each row is complete even though only a few rows are
     computed (CacheBlend blog, "Selective KV recompute": expand K and V back to full
     length, then run ordinary attention).
+
+    Written as the textbook masked softmax: for each KV head and a block of query rows,
+    all logits against keys 0..max(qpos) of the block, the keys past a row's own
+    position set to -inf, the row maximum subtracted, exponentiated, normalised and
+    multiplied by V.  Blocks only bound the size of the logit array; every row is
+    computed on its own.
     """
     n, hq, d = q.shape
     hkv = K.shape[1]
     group = hq // hkv
     out = np.zeros((n, hq, d), dtype=F64)
     scale = 1.0 / math.sqrt(d)
-    for i in range(n):
-        p = int(qpos[i])
-        for g in range(hkv):
-            heads = slice(g * group, (g + 1) * group)              # query heads of kv head g
-            s = (q[i, heads, :] @ K[:p + 1, g, :].T) * scale       # [group, p+1]
-            s = s - np.max(s, axis=1, keepdims=True)
+    qpos = np.asarray(qpos, dtype=np.int64)
+    block = 256
+    for g in range(hkv):
+        heads = slice(g * group, (g + 1) * group)               # query heads of kv head g
+        Kg = np.ascontiguousarray(K[:, g, :], dtype=F64)       # [N, d]
+        Vg = np.ascontiguousarray(V[:, g, :], dtype=F64)
+        for i0 in range(0, n, block):
+            i1 = min(n, i0 + block)
+            top = int(qpos[i0:i1].max()) + 1                   # keys any row of the block sees
+            qb = np.asarray(q[i0:i1, heads, :], dtype=F64)     # [b, group, d]
+            s = (qb @ Kg[:top].T) * scale                      # [b, group, top]
+            past = np.arange(top)[None, :] > qpos[i0:i1, None]  # [b, top]: key after the row
+            s[np.broadcast_to(past[:, None, :], s.shape)] = -np.inf
+            s = s - np.max(s, axis=2, keepdims=True)
             e = np.exp(s)
-            out[i, heads, :] = (e / np.sum(e, axis=1, keepdims=True)) @ V[:p + 1, g, :]
+            out[i0:i1, heads, :] = (e / np.sum(e, axis=2, keepdims=True)) @ Vg[:top]
     return out
 
 
@@ -228,7 +242,7 @@ def full_prefill(w: dict, cfg: dict, tokens: np.ndarray):
     K = np.zeros((L, N, hkv, d), dtype=F64)
     V = np.zeros((L, N, hkv, d), dtype=F64)
     pos = np.arange(N)
-    x = np.asarray(w["embed"], dtype=F64)[np.asarray(tokens)]
+    x = np.asarray(w["embed"][np.asarray(tokens)], dtype=F64)
     for layer in range(L):
         x, _ = layer_forward(w, cfg, layer, x, pos, K[layer], V[layer])
     return rmsnorm(x, w["final_norm"], cfg["rms_eps"]), K, V
@@ -533,7 +547,7 @@ def aux_query_forward(w: dict, cfg: dict, ek, ev, P: int, query_tokens):
     K = np.concatenate([ek, np.zeros((L, Q) + ek.shape[2:], dtype=F64)], axis=1)
     V = np.concatenate([ev, np.zeros((L, Q) + ev.shape[2:], dtype=F64)], axis=1)
     pos = np.arange(P + Lc, P + Lc + Q)
-    x = np.asarray(w["embed"], dtype=F64)[np.asarray(query_tokens)]
+    x = np.asarray(w["embed"][np.asarray(query_tokens)], dtype=F64)
     q = None
     for layer in range(L):
         q, _ = layer_kv(w, cfg, layer, x, pos, K[layer], V[layer])
@@ -717,7 +731,7 @@ def blend_prefill(w: dict, cfg: dict, entries_k, entries_v, entry_tokens, prefix
 
     devs = {}
     rows = rows_at(0)
-    x = np.asarray(w["embed"], dtype=F64)[tokens[rows]]
+    x = np.asarray(w["embed"][tokens[rows]], dtype=F64)
     for layer in range(L):
         check = mode in ("hkvd", "forced") and layer in CHECK_LAYERS
         dev_rows = ((rows >= lo) & (rows < hi)) if check else None
