@@ -297,10 +297,15 @@ int blend_assemble(blend_handle* h, int32_t n_req, const blend_request* reqs,
 /* KV deviation (CacheBlend blog, "Selective KV recompute"): for row i < *n_rows,
  * dev[i] = sum over [hkv][d] of (k_new[i]-k_cache[pos[i]])^2 + (v_new[i]-v_cache[pos[i]])^2
  * (v only for BLEND_DEV_V), accumulated in fp32 in a fixed order.  k_new, v_new:
- * [rows][hkv][d]; caches: [tokens][hkv][d] (one layer).  n_rows is a device scalar. */
+ * [rows][hkv][d]; caches: [n_ctx][hkv][d] (one layer); every K/V pointer 16-byte aligned.
+ * n_rows is a device scalar, at most max_rows (host) rows are read.  Device-side checks:
+ * a position outside 0..n_ctx-1 gives dev[i] = 0 without reading the cache, and a count
+ * outside 0..max_rows is clamped; both are reported by blend_device_status as
+ * BLEND_EDEVICE.  Host errors: BLEND_EINVAL for NULL or unaligned pointers, negative
+ * sizes or a bad mode (nothing is launched). */
 int kv_deviation(blend_handle* h, const void* k_new, const void* v_new, const void* k_cache,
                  const void* v_cache, const int32_t* pos, const int32_t* n_rows, int32_t max_rows,
-                 int32_t mode, float* dev_out, void* stream);
+                 int64_t n_ctx, int32_t mode, float* dev_out, void* stream);
 
 /* Token selection: top-k by score then sliding-window grouping (CacheClip blog 6.3,
  * rule list and Figure 6; SpecCache 2.2 TopK).  scores: device [n] fp32 for positions
@@ -375,26 +380,38 @@ int blend_ratio_controller(double full_prefill_s, double kv_bytes, double load_b
 int blend_pick_storage(double full_prefill_s, double kv_bytes, int32_t floor_bp, int32_t n_dev,
                        const double* bytes_per_s, const double* cost_per_byte, int32_t* best);
 
-/* Row gather: dst[i] = src[idx[i]] for i < *n (device scalar), rows of row_bytes
- * (a multiple of 16; src, dst 16-byte aligned).  max_n bounds *n. */
-int gather_rows(const void* src, int64_t row_bytes, const int32_t* idx, const int32_t* n,
-                int32_t max_n, void* dst, void* stream);
+/* Row gather (CacheBlend blog, "Selective KV recompute": the layer input is reduced to
+ * the selected rows): dst[i] = src[idx[i]] for i < *n (device scalar, at most max_n rows),
+ * rows of row_bytes (a positive multiple of 16; src, dst 16-byte aligned); src holds
+ * src_rows rows.  Device-side checks: an index outside 0..src_rows-1 leaves dst[i]
+ * untouched and a count outside 0..max_n is clamped; both are reported by
+ * blend_device_status(h) as BLEND_EDEVICE.  The handle is used only for that error word.
+ * Host errors: BLEND_EINVAL (nothing is launched). */
+int gather_rows(blend_handle* h, const void* src, int64_t row_bytes, int64_t src_rows, const int32_t* idx,
+                const int32_t* n, int32_t max_n, void* dst, void* stream);
 
 /* KV scatter (CacheClip blog 6.3: the global KV cache entries are overwritten):
- * k_cache[pos[i]] = k_new[i], v_cache[pos[i]] = v_new[i] for i < *n (one layer). */
+ * k_cache[pos[i]] = k_new[i], v_cache[pos[i]] = v_new[i] for i < *n (one layer; caches
+ * [n_ctx][hkv][d], rows [hkv][d]; 16-byte aligned pointers).  Device-side checks: a
+ * position outside 0..n_ctx-1 is not written and a count outside 0..max_n is clamped;
+ * both are reported by blend_device_status as BLEND_EDEVICE.  Host errors: BLEND_EINVAL. */
 int scatter_kv(blend_handle* h, const void* k_new, const void* v_new, const int32_t* pos,
-               const int32_t* n, int32_t max_n, void* k_cache, void* v_cache, void* stream);
+               const int32_t* n, int32_t max_n, int64_t n_ctx, void* k_cache, void* v_cache, void* stream);
 
 /* One selective decoder layer (CacheBlend blog, "Selective KV recompute": mask the
  * input to the selected rows, project Q/K/V, expand K/V with the reused rows, run
  * attention and the rest of the layer) for one request.
- * x: device fp32 [n][H] residual rows (in/out), at strictly ascending positions pos
- * (device [n], each in 0..n_ctx-1; violations are reported by blend_device_status);
- * k_cache, v_cache: this layer's [n_ctx][hkv][d]; their rows pos[i] are overwritten
- * with the fresh K/V before attention.  dev_out: device [n] or NULL, the deviation of
- * each row against the cache before the overwrite.  n <= max_rows; n_ctx <= max_tokens. */
-int selective_layer(blend_handle* h, int32_t layer, float* x, const int32_t* pos, int32_t n,
-                    void* k_cache, void* v_cache, int32_t n_ctx, float* dev_out,
+ * x: device fp32 [max_n][H] residual rows (in/out); the first *n of them (n: device
+ * scalar, so a set size produced on the device needs no host round trip) are the rows at
+ * strictly ascending positions pos (device [*n], each in 0..n_ctx-1).  k_cache, v_cache:
+ * this layer's [n_ctx][hkv][d]; their rows pos[i] are overwritten with the fresh K/V
+ * before attention.  dev_out: device [max_n] or NULL, the deviation of each row against
+ * the cache before the overwrite.  max_n (host) <= the handle's max_rows bounds *n and
+ * sizes the launches; n_ctx <= max_tokens.  Device-side checks: a count above
+ * min(max_n, n_ctx) is clamped and a position out of range or out of order is replaced by
+ * a valid one; both are reported by blend_device_status as BLEND_EDEVICE. */
+int selective_layer(blend_handle* h, int32_t layer, float* x, const int32_t* pos, const int32_t* n,
+                    int32_t max_n, void* k_cache, void* v_cache, int32_t n_ctx, float* dev_out,
                     int32_t dev_mode, void* stream);
 
 /* The whole blended prefill for a batch of requests (all layers; assemble, select,

@@ -105,11 +105,11 @@ def lib() -> C.CDLL:
             "rope_realign": (C.c_int, [vp, vp, vp, i32, vp, i32, i64, i64, vp]),
             "blend_assemble": (C.c_int, [vp, i32, C.POINTER(Request), C.POINTER(Pool),
                                          C.POINTER(Outputs), vp]),
-            "kv_deviation": (C.c_int, [vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, vp]),
+            "kv_deviation": (C.c_int, [vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, vp, vp]),
             "topk_select_dilate": (C.c_int, [vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp]),
-            "gather_rows": (C.c_int, [vp, i64, vp, vp, i32, vp, vp]),
-            "scatter_kv": (C.c_int, [vp, vp, vp, vp, vp, i32, vp, vp, vp]),
-            "selective_layer": (C.c_int, [vp, i32, vp, vp, i32, vp, vp, i32, vp, i32, vp]),
+            "gather_rows": (C.c_int, [vp, vp, i64, i64, vp, vp, i32, vp, vp]),
+            "scatter_kv": (C.c_int, [vp, vp, vp, vp, vp, i32, i64, vp, vp, vp]),
+            "selective_layer": (C.c_int, [vp, i32, vp, vp, vp, i32, vp, vp, i32, vp, i32, vp]),
             "blend_prefill": (C.c_int, [vp, i32, C.POINTER(Request), C.POINTER(Pool),
                                         C.POINTER(Outputs), vp]),
             "importance_scores": (C.c_int, [vp, i32, i32, i32, i32, vp, vp]),
@@ -261,8 +261,9 @@ def rope_realign(h, k_src, k_dst, n_rows, delta, n_layers, src_layer_rows, dst_l
 
 
 def kv_deviation(h, k_new, v_new, k_cache, v_cache, pos, n_rows, max_rows, mode, dev_out, stream=None):
+    """n_rows: device int32 count; the cache row count is taken from k_cache's first dimension."""
     _check(lib().kv_deviation(h.ptr, _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(pos),
-                              _ptr(n_rows), max_rows, mode, _ptr(dev_out), _stream(stream)), h)
+                              _ptr(n_rows), max_rows, k_cache.shape[0], mode, _ptr(dev_out), _stream(stream)), h)
 
 
 def span_select(h, scores, n, base, budget, cap, tau_smooth, tau_cover_bp, max_span, budget_mode, idx_out,
@@ -291,19 +292,31 @@ def topk_select_dilate_noalloc(scores, n, base, budget, window, tau, budget_mode
                                             _ptr(allowed), _ptr(idx_out), _ptr(n_out), _stream(stream)))
 
 
-def gather_rows(src, row_bytes, idx, n, max_n, dst, stream=None):
-    _check(lib().gather_rows(_ptr(src), row_bytes, _ptr(idx), _ptr(n), max_n, _ptr(dst), _stream(stream)))
+def gather_rows(h, src, row_bytes, idx, n, max_n, dst, stream=None):
+    """src's first dimension is its row count (src_rows of the C call)."""
+    _check(lib().gather_rows(h.ptr, _ptr(src), row_bytes, src.shape[0], _ptr(idx), _ptr(n), max_n, _ptr(dst),
+                             _stream(stream)), h)
 
 
 def scatter_kv(h, k_new, v_new, pos, n, max_n, k_cache, v_cache, stream=None):
-    _check(lib().scatter_kv(h.ptr, _ptr(k_new), _ptr(v_new), _ptr(pos), _ptr(n), max_n, _ptr(k_cache),
-                            _ptr(v_cache), _stream(stream)), h)
+    """The cache row count (n_ctx of the C call) is k_cache's first dimension."""
+    _check(lib().scatter_kv(h.ptr, _ptr(k_new), _ptr(v_new), _ptr(pos), _ptr(n), max_n, k_cache.shape[0],
+                            _ptr(k_cache), _ptr(v_cache), _stream(stream)), h)
 
 
 def selective_layer(h, layer, x, pos, n, k_cache, v_cache, n_ctx, dev_out=None, dev_mode=DEV_KV,
-                    stream=None):
-    _check(lib().selective_layer(h.ptr, layer, _ptr(x), _ptr(pos), n, _ptr(k_cache), _ptr(v_cache),
-                                 n_ctx, _ptr(dev_out), dev_mode, _stream(stream)), h)
+                    stream=None, max_n=None):
+    """n: a device int32 count (then max_n bounds it) or a host int (copied into a device
+    scalar, max_n = n)."""
+    if isinstance(n, torch.Tensor):
+        n_dev = n
+        if max_n is None:
+            raise ValueError("max_n is required with a device count")
+    else:
+        n_dev = torch.tensor([int(n)], dtype=torch.int32, device=x.device)
+        max_n = int(n) if max_n is None else max_n
+    _check(lib().selective_layer(h.ptr, layer, _ptr(x), _ptr(pos), _ptr(n_dev), max_n, _ptr(k_cache),
+                                 _ptr(v_cache), n_ctx, _ptr(dev_out), dev_mode, _stream(stream)), h)
 
 
 def importance_scores(hidden, n, n_layers, dim, out, stream=None):

@@ -604,13 +604,16 @@ int rope_realign(blend_handle* h, const void* k_src, void* k_dst, int32_t n_rows
 
 int kv_deviation(blend_handle* h, const void* k_new, const void* v_new, const void* k_cache,
                  const void* v_cache, const int32_t* pos, const int32_t* n_rows, int32_t max_rows,
-                 int32_t mode, float* dev_out, void* stream) {
+                 int64_t n_ctx, int32_t mode, float* dev_out, void* stream) {
     if (!h) return fail(nullptr, BLEND_EINVAL, "handle is NULL");
     if (!k_new || !v_new || !k_cache || !v_cache || !pos || !n_rows || !dev_out)
         return fail(h, BLEND_EINVAL, "NULL pointer");
-    if (max_rows < 0 || (mode != BLEND_DEV_KV && mode != BLEND_DEV_V)) return fail(h, BLEND_EINVAL, "bad mode or size");
-    launch_deviation(h->cfg.dtype, k_new, v_new, k_cache, v_cache, pos, n_rows, max_rows,
-                     h->cfg.n_kv_heads * h->cfg.head_dim, mode, dev_out, (cudaStream_t)stream);
+    if (max_rows < 0 || n_ctx < 0 || (mode != BLEND_DEV_KV && mode != BLEND_DEV_V))
+        return fail(h, BLEND_EINVAL, "bad mode or size");
+    if (((uintptr_t)k_new | (uintptr_t)v_new | (uintptr_t)k_cache | (uintptr_t)v_cache) & 15)
+        return fail(h, BLEND_EINVAL, "K/V pointers must be 16-byte aligned");
+    launch_deviation(h->cfg.dtype, k_new, v_new, k_cache, v_cache, pos, n_rows, max_rows, n_ctx,
+                     h->cfg.n_kv_heads * h->cfg.head_dim, mode, dev_out, h->err, (cudaStream_t)stream);
     return check_cuda(h, "kv_deviation");
 }
 
@@ -707,24 +710,26 @@ int blend_pick_storage(double full_prefill_s, double kv_bytes, int32_t floor_bp,
     return BLEND_OK;
 }
 
-int gather_rows(const void* src, int64_t row_bytes, const int32_t* idx, const int32_t* n,
-                int32_t max_n, void* dst, void* stream) {
-    if (!src || !idx || !n || !dst) return fail(nullptr, BLEND_EINVAL, "NULL pointer");
-    if (row_bytes <= 0 || row_bytes % 16 || max_n < 0) return fail(nullptr, BLEND_EINVAL, "row_bytes must be a positive multiple of 16");
-    if (((uintptr_t)src | (uintptr_t)dst) & 15) return fail(nullptr, BLEND_EINVAL, "src/dst must be 16-byte aligned");
-    launch_gather(src, row_bytes, idx, n, max_n, dst, (cudaStream_t)stream);
-    return check_cuda(nullptr, "gather_rows");
+int gather_rows(blend_handle* h, const void* src, int64_t row_bytes, int64_t src_rows, const int32_t* idx,
+                const int32_t* n, int32_t max_n, void* dst, void* stream) {
+    if (!h) return fail(nullptr, BLEND_EINVAL, "handle is NULL");
+    if (!src || !idx || !n || !dst) return fail(h, BLEND_EINVAL, "NULL pointer");
+    if (row_bytes <= 0 || row_bytes % 16 || max_n < 0 || src_rows < 0)
+        return fail(h, BLEND_EINVAL, "row_bytes must be a positive multiple of 16, max_n and src_rows >= 0");
+    if (((uintptr_t)src | (uintptr_t)dst) & 15) return fail(h, BLEND_EINVAL, "src/dst must be 16-byte aligned");
+    launch_gather(src, row_bytes, src_rows, idx, n, max_n, dst, h->err, (cudaStream_t)stream);
+    return check_cuda(h, "gather_rows");
 }
 
 int scatter_kv(blend_handle* h, const void* k_new, const void* v_new, const int32_t* pos,
-               const int32_t* n, int32_t max_n, void* k_cache, void* v_cache, void* stream) {
+               const int32_t* n, int32_t max_n, int64_t n_ctx, void* k_cache, void* v_cache, void* stream) {
     if (!h) return fail(nullptr, BLEND_EINVAL, "handle is NULL");
     if (!k_new || !v_new || !pos || !n || !k_cache || !v_cache) return fail(h, BLEND_EINVAL, "NULL pointer");
-    if (max_n < 0) return fail(h, BLEND_EINVAL, "bad max_n");
+    if (max_n < 0 || n_ctx < 0) return fail(h, BLEND_EINVAL, "bad max_n or n_ctx");
     if (((uintptr_t)k_new | (uintptr_t)v_new | (uintptr_t)k_cache | (uintptr_t)v_cache) & 15)
         return fail(h, BLEND_EINVAL, "pointers must be 16-byte aligned");
-    launch_scatter(h->cfg.dtype, k_new, v_new, pos, n, max_n, h->cfg.n_kv_heads * h->cfg.head_dim,
-                   k_cache, v_cache, (cudaStream_t)stream);
+    launch_scatter(h->cfg.dtype, k_new, v_new, pos, n, max_n, n_ctx, h->cfg.n_kv_heads * h->cfg.head_dim,
+                   k_cache, v_cache, h->err, (cudaStream_t)stream);
     return check_cuda(h, "scatter_kv");
 }
 
@@ -737,31 +742,30 @@ int importance_scores(const void* hidden, int32_t n, int32_t n_layers, int32_t d
     return check_cuda(nullptr, "importance_scores");
 }
 
-int selective_layer(blend_handle* h, int32_t layer, float* x, const int32_t* pos, int32_t n,
-                    void* k_cache, void* v_cache, int32_t n_ctx, float* dev_out, int32_t dev_mode,
+int selective_layer(blend_handle* h, int32_t layer, float* x, const int32_t* pos, const int32_t* n,
+                    int32_t max_n, void* k_cache, void* v_cache, int32_t n_ctx, float* dev_out, int32_t dev_mode,
                     void* stream) {
     if (!h) return fail(nullptr, BLEND_EINVAL, "handle is NULL");
     const blend_model_cfg& c = h->cfg;
-    if (!x || !pos || !k_cache || !v_cache) return fail(h, BLEND_EINVAL, "NULL pointer");
+    if (!x || !pos || !n || !k_cache || !v_cache) return fail(h, BLEND_EINVAL, "NULL pointer");
     if (layer < 0 || layer >= c.n_layers) return fail(h, BLEND_EINVAL, "layer %d out of range", layer);
-    if (n < 0 || n > h->lim.max_rows || n > n_ctx || n_ctx > c.max_pos || n_ctx > h->lim.max_tokens)
-        return fail(h, BLEND_EINVAL, "n=%d / n_ctx=%d outside the handle's limits", n, n_ctx);
+    if (max_n < 0 || max_n > h->lim.max_rows || n_ctx < 0 || n_ctx > c.max_pos || n_ctx > h->lim.max_tokens)
+        return fail(h, BLEND_EINVAL, "max_n=%d / n_ctx=%d outside the handle's limits", max_n, n_ctx);
     if (dev_mode != BLEND_DEV_KV && dev_mode != BLEND_DEV_V) return fail(h, BLEND_EINVAL, "bad dev_mode");
-    if (n == 0) return BLEND_OK;
+    if (max_n == 0) return BLEND_OK;
     cudaStream_t s = (cudaStream_t)stream;
     BatchDesc bd;
     memset(&bd, 0, sizeof bd);
     bd.n_req = 1;
     bd.r[0] = ReqDesc{0, 0, n_ctx, 0, 0, 0};
-    // rows = the given positions, in order
-    launch_fill_i32(h->scratch_n, n, 1, s);
-    StageDesc st{pos, h->scratch_n, 0};
+    // rows = the given positions, in order; the device count is checked against max_n and n_ctx
+    StageDesc st{pos, n, 0, max_n};
     Plan& p = h->plan[0];
     launch_plan(bd, st, p.row_pos, p.row_tok, p.row_req, h->row_src, h->pos2row, p.M, p.req_row_end,
                 nullptr, nullptr, h->err, s);
     h->xn_scaled = false;
-    layer_kv(h, layer, x, p, p.row_req, n, bd, k_cache, v_cache, dev_out, dev_mode, 1, s);
-    layer_rest(h, layer, x, p, 1, n, k_cache, v_cache, n_ctx, s, false);
+    layer_kv(h, layer, x, p, p.row_req, max_n, bd, k_cache, v_cache, dev_out, dev_mode, 1, s);
+    layer_rest(h, layer, x, p, 1, max_n, k_cache, v_cache, n_ctx, s, false);
     return finish(h, "selective_layer");
 }
 
@@ -1247,14 +1251,14 @@ extern "C" int blend_prefill(blend_handle* h, int32_t n_req, const blend_request
             Plan& np = h->plan[1 - cur];
             launch_plan(bd, st, np.row_pos, np.row_tok, np.row_req, h->row_src, h->pos2row, np.M,
                         np.req_row_end, h->plan[cur].row_tok, h->plan[cur].M, h->err, s);
-            launch_gather(x, (long long)c.hidden * 4, h->row_src, np.M, M_max, x_alt, s);
+            launch_gather(x, (long long)c.hidden * 4, h->lim.max_rows, h->row_src, np.M, M_max, x_alt, h->err, s);
             {
                 // q is stored per kv head: compact each head's slab of [rows][group][d]
                 const int group = c.n_q_heads / c.n_kv_heads;
                 const size_t slab = (size_t)h->lim.max_rows * group * c.head_dim * es;
                 for (int g = 0; g < c.n_kv_heads; ++g)
-                    launch_gather((const char*)h->q + g * slab, (long long)group * c.head_dim * es, h->row_src,
-                                  np.M, M_max, (char*)h->q2 + g * slab, s);
+                    launch_gather((const char*)h->q + g * slab, (long long)group * c.head_dim * es,
+                                  h->lim.max_rows, h->row_src, np.M, M_max, (char*)h->q2 + g * slab, h->err, s);
             }
             float* tx = x;
             x = x_alt;

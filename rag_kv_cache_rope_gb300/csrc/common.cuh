@@ -104,10 +104,12 @@ struct QueryTable {
 
 // Stage set of every request: positions at set + nc_off[r], count at count[r];
 // iota 1: the set is every chunk row P..P+n_c-1; iota 2: every row 0..P+n_c-1.
+// max_count > 0 caps every request's count (a caller-given count above it is reported).
 struct StageDesc {
     const int32_t* set;
     const int32_t* count;
     int32_t iota;
+    int32_t max_count;
 };
 
 // ------------------------------ launchers (kernels_mem.cu) -------------------------
@@ -128,18 +130,18 @@ void launch_rmsnorm(int dtype, const float* x, const void* g, void* out, int H, 
 void launch_embed(int dtype, const void* embed, const int32_t* tokens, const int32_t* row_tok,
                   float* x, int H, int vocab, const int32_t* M_dev, int M_max, int32_t* err,
                   cudaStream_t s);
-void launch_gather(const void* src, long long row_bytes, const int32_t* idx, const int32_t* n_dev,
-                   int max_n, void* dst, cudaStream_t s);
+void launch_gather(const void* src, long long row_bytes, long long src_rows, const int32_t* idx,
+                   const int32_t* n_dev, int max_n, void* dst, int32_t* err, cudaStream_t s);
 void launch_rope_qkv(int dtype, const float* qkv, const int32_t* row_pos, const int32_t* row_tok,
                      const int32_t* row_req, const int32_t* M_dev, int M_max, const BatchDesc& bd,
                      int hq, int hkv, int d, int m_cap, const float2* tab, void* q_out, void* k_cache,
                      void* v_cache, float* dev_out, int dev_mode, int dev_by_row, cudaStream_t s);
 void launch_deviation(int dtype, const void* k_new, const void* v_new, const void* k_cache,
                       const void* v_cache, const int32_t* pos, const int32_t* n_dev, int max_rows,
-                      int kv_elems, int mode, float* dev_out, cudaStream_t s);
+                      long long n_ctx, int kv_elems, int mode, float* dev_out, int32_t* err, cudaStream_t s);
 void launch_scatter(int dtype, const void* k_new, const void* v_new, const int32_t* pos,
-                    const int32_t* n_dev, int max_n, int kv_elems, void* k_cache, void* v_cache,
-                    cudaStream_t s);
+                    const int32_t* n_dev, int max_n, long long n_ctx, int kv_elems, void* k_cache,
+                    void* v_cache, int32_t* err, cudaStream_t s);
 void launch_final_norm(int dtype, const float* x, const void* g, void* hidden, int H, float eps,
                        const BatchDesc& bd, const int32_t* req_row_end, cudaStream_t s);
 void launch_importance(int dtype, const void* hidden, int n, int n_layers, int dim, float* out,

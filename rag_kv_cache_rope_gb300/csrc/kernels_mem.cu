@@ -378,22 +378,32 @@ void launch_embed(int dtype, const void* embed, const int32_t* tokens, const int
     note_launch(1);
 }
 
-// dst[i] = src[idx[i]], rows of row_bytes (multiple of 16).
-__global__ void k_gather(const uint4* __restrict__ src, long long row_vec,
-                         const int32_t* __restrict__ idx, const int32_t* n_dev, uint4* __restrict__ dst) {
+// dst[i] = src[idx[i]], rows of row_bytes (multiple of 16).  An index outside
+// 0..src_rows-1 is reported in err and its destination row is left untouched; a count
+// above max_n is reported and clamped (the grid has max_n blocks).
+__global__ void k_gather(const uint4* __restrict__ src, long long row_vec, long long src_rows,
+                         const int32_t* __restrict__ idx, const int32_t* n_dev, int max_n,
+                         uint4* __restrict__ dst, int32_t* err) {
     const int i = blockIdx.x;
-    if (i >= *n_dev) return;
-    const long long s = (long long)idx[i] * row_vec;
+    const int n = *n_dev;
+    if (i == 0 && threadIdx.x == 0 && (n < 0 || n > max_n)) set_error(err, BLEND_EDEVICE);
+    if (i >= n) return;
+    const long long r = idx[i];
+    if (r < 0 || r >= src_rows) {
+        if (threadIdx.x == 0) set_error(err, BLEND_EDEVICE);
+        return;
+    }
+    const long long s = r * row_vec;
     const long long d = (long long)i * row_vec;
     for (long long j = threadIdx.x; j < row_vec; j += blockDim.x) dst[d + j] = src[s + j];
 }
 
-void launch_gather(const void* src, long long row_bytes, const int32_t* idx, const int32_t* n_dev,
-                   int max_n, void* dst, cudaStream_t s) {
+void launch_gather(const void* src, long long row_bytes, long long src_rows, const int32_t* idx,
+                   const int32_t* n_dev, int max_n, void* dst, int32_t* err, cudaStream_t s) {
     if (max_n <= 0) return;
     long long rv = row_bytes / 16;
     int threads = rv >= 256 ? 256 : (int)(((rv + 31) / 32) * 32);
-    k_gather<<<max_n, threads, 0, s>>>((const uint4*)src, rv, idx, n_dev, (uint4*)dst);
+    k_gather<<<max_n, threads, 0, s>>>((const uint4*)src, rv, src_rows, idx, n_dev, max_n, (uint4*)dst, err);
     note_launch(1);
 }
 
@@ -479,49 +489,89 @@ void launch_rope_qkv(int dtype, const float* qkv, const int32_t* row_pos, const 
 }
 
 // ---------------------------------------------------------------- standalone deviation / scatter
+// One warp per row, 16-byte loads of the fresh and the cached rows; each lane adds its
+// vectors in order and the lanes are combined by a fixed shuffle tree, so the result
+// does not depend on timing.  A position outside 0..n_ctx-1 is reported in err and
+// gives dev = 0 without touching the cache; a count above max_rows is reported and
+// clamped.
+constexpr int DEV_WARPS = 8;
 template <typename T>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(DEV_WARPS * 32)
     k_deviation(const T* __restrict__ kn, const T* __restrict__ vn, const T* __restrict__ kc,
                 const T* __restrict__ vc, const int32_t* __restrict__ pos, const int32_t* n_dev,
-                int kv_elems, int mode, float* __restrict__ dev) {
-    __shared__ float red[256];
-    const int i = blockIdx.x;
-    if (i >= *n_dev) return;
-    const long long a = (long long)i * kv_elems, b = (long long)pos[i] * kv_elems;
+                int max_rows, long long n_ctx, int kv_elems, int mode, float* __restrict__ dev,
+                int32_t* err) {
+    const int lane = threadIdx.x & 31;
+    const int i = blockIdx.x * DEV_WARPS + (threadIdx.x >> 5);
+    int n = *n_dev;
+    if (blockIdx.x == 0 && threadIdx.x == 0 && (n < 0 || n > max_rows)) set_error(err, BLEND_EDEVICE);
+    n = min(n, max_rows);
+    if (i >= n) return;
+    const long long p = pos[i];
+    if (p < 0 || p >= n_ctx) {
+        if (lane == 0) {
+            set_error(err, BLEND_EDEVICE);
+            dev[i] = 0.f;
+        }
+        return;
+    }
+    constexpr int E = Vec<T>::N;
+    const long long a = (long long)i * kv_elems, b = p * kv_elems;
     float acc = 0.f;
-    for (int j = threadIdx.x; j < kv_elems; j += blockDim.x) {
-        float dv = to_f<T>(vn[a + j]) - to_f<T>(vc[b + j]);
-        acc += dv * dv;
+    for (int j = lane * E; j < kv_elems; j += 32 * E) {
+        const Vec<T> x = ld16(vn + a + j), y = ld16(vc + b + j);
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            const float dv = x.get(e) - y.get(e);
+            acc = fmaf(dv, dv, acc);
+        }
         if (mode == BLEND_DEV_KV) {
-            float dk = to_f<T>(kn[a + j]) - to_f<T>(kc[b + j]);
-            acc += dk * dk;
+            const Vec<T> xk = ld16(kn + a + j), yk = ld16(kc + b + j);
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                const float dk = xk.get(e) - yk.get(e);
+                acc = fmaf(dk, dk, acc);
+            }
         }
     }
-    float s = block_sum(acc, red);
-    if (threadIdx.x == 0) dev[i] = s;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) dev[i] = acc;
 }
 
 void launch_deviation(int dtype, const void* k_new, const void* v_new, const void* k_cache,
                       const void* v_cache, const int32_t* pos, const int32_t* n_dev, int max_rows,
-                      int kv_elems, int mode, float* dev_out, cudaStream_t s) {
+                      long long n_ctx, int kv_elems, int mode, float* dev_out, int32_t* err, cudaStream_t s) {
     if (max_rows <= 0) return;
+    const int grid = (max_rows + DEV_WARPS - 1) / DEV_WARPS;
     if (dtype == BLEND_BF16)
-        k_deviation<bf16><<<max_rows, 256, 0, s>>>((const bf16*)k_new, (const bf16*)v_new,
-                                                   (const bf16*)k_cache, (const bf16*)v_cache, pos,
-                                                   n_dev, kv_elems, mode, dev_out);
+        k_deviation<bf16><<<grid, DEV_WARPS * 32, 0, s>>>((const bf16*)k_new, (const bf16*)v_new,
+                                                          (const bf16*)k_cache, (const bf16*)v_cache, pos,
+                                                          n_dev, max_rows, n_ctx, kv_elems, mode, dev_out, err);
     else
-        k_deviation<float><<<max_rows, 256, 0, s>>>((const float*)k_new, (const float*)v_new,
-                                                    (const float*)k_cache, (const float*)v_cache,
-                                                    pos, n_dev, kv_elems, mode, dev_out);
+        k_deviation<float><<<grid, DEV_WARPS * 32, 0, s>>>((const float*)k_new, (const float*)v_new,
+                                                           (const float*)k_cache, (const float*)v_cache,
+                                                           pos, n_dev, max_rows, n_ctx, kv_elems, mode, dev_out,
+                                                           err);
     note_launch(1);
 }
 
+// k_cache[pos[i]] = k_new[i], v_cache[pos[i]] = v_new[i] in 16-byte vectors; a position
+// outside 0..n_ctx-1 is reported in err and that row is not written; a count above
+// max_n is reported and clamped.
 __global__ void k_scatter(const uint4* __restrict__ kn, const uint4* __restrict__ vn,
-                          const int32_t* __restrict__ pos, const int32_t* n_dev, long long row_vec,
-                          uint4* __restrict__ kc, uint4* __restrict__ vc) {
+                          const int32_t* __restrict__ pos, const int32_t* n_dev, int max_n, long long n_ctx,
+                          long long row_vec, uint4* __restrict__ kc, uint4* __restrict__ vc, int32_t* err) {
     const int i = blockIdx.x;
-    if (i >= *n_dev) return;
-    const long long a = (long long)i * row_vec, b = (long long)pos[i] * row_vec;
+    const int n = *n_dev;
+    if (i == 0 && threadIdx.x == 0 && (n < 0 || n > max_n)) set_error(err, BLEND_EDEVICE);
+    if (i >= n) return;
+    const long long p = pos[i];
+    if (p < 0 || p >= n_ctx) {
+        if (threadIdx.x == 0) set_error(err, BLEND_EDEVICE);
+        return;
+    }
+    const long long a = (long long)i * row_vec, b = p * row_vec;
     for (long long j = threadIdx.x; j < row_vec; j += blockDim.x) {
         kc[b + j] = kn[a + j];
         vc[b + j] = vn[a + j];
@@ -529,13 +579,13 @@ __global__ void k_scatter(const uint4* __restrict__ kn, const uint4* __restrict_
 }
 
 void launch_scatter(int dtype, const void* k_new, const void* v_new, const int32_t* pos,
-                    const int32_t* n_dev, int max_n, int kv_elems, void* k_cache, void* v_cache,
-                    cudaStream_t s) {
+                    const int32_t* n_dev, int max_n, long long n_ctx, int kv_elems, void* k_cache,
+                    void* v_cache, int32_t* err, cudaStream_t s) {
     if (max_n <= 0) return;
     long long rv = (long long)kv_elems * (dtype == BLEND_BF16 ? 2 : 4) / 16;
     int threads = rv >= 128 ? 128 : (int)(((rv + 31) / 32) * 32);
-    k_scatter<<<max_n, threads, 0, s>>>((const uint4*)k_new, (const uint4*)v_new, pos, n_dev, rv,
-                                        (uint4*)k_cache, (uint4*)v_cache);
+    k_scatter<<<max_n, threads, 0, s>>>((const uint4*)k_new, (const uint4*)v_new, pos, n_dev, max_n, n_ctx, rv,
+                                        (uint4*)k_cache, (uint4*)v_cache, err);
     note_launch(1);
 }
 
@@ -618,7 +668,8 @@ __global__ void __launch_bounds__(1024)
         off[0] = 0;
         for (int r = 0; r < bd.n_req; ++r) {
             const ReqDesc rd = bd.r[r];
-            const int cap = st.iota == 2 ? (rd.P + rd.n_c) : rd.n_c;
+            int cap = st.iota == 2 ? (rd.P + rd.n_c) : rd.n_c;
+            if (st.max_count > 0 && cap > st.max_count) cap = st.max_count;
             int n = st.iota ? cap : st.count[r];
             if (n < 0 || n > cap) {
                 set_error(err, BLEND_EDEVICE);

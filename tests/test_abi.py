@@ -128,9 +128,11 @@ def test_init_rejects_bad_arguments_without_a_gpu(lib):
                         C.byref(out))
     assert rc == b.EINVAL
     assert lib.blend_destroy(None) == b.EINVAL
-    assert lib.gather_rows(None, 16, None, None, 1, None, None) == b.EINVAL
-    assert lib.gather_rows(C.c_void_p(1 << 20), 20, C.c_void_p(1 << 20), C.c_void_p(1 << 20), 1,
-                           C.c_void_p(1 << 20), None) == b.EINVAL
+    vp = C.c_void_p(1 << 20)
+    assert lib.gather_rows(None, vp, 16, 4, vp, vp, 1, vp, None) == b.EINVAL          # no handle
+    assert lib.scatter_kv(None, vp, vp, vp, vp, 1, 4, vp, vp, None) == b.EINVAL
+    assert lib.kv_deviation(None, vp, vp, vp, vp, vp, vp, 1, 4, b.DEV_KV, vp, None) == b.EINVAL
+    assert lib.selective_layer(None, 0, vp, vp, vp, 1, vp, vp, 4, None, b.DEV_KV, None) == b.EINVAL
     assert lib.importance_scores(C.c_void_p(1 << 20), 4, 0, 8, b.F32, C.c_void_p(1 << 20), None) == b.EINVAL
     assert lib.importance_scores(C.c_void_p(1 << 20), 4, 4097, 8, b.F32, C.c_void_p(1 << 20), None) == b.EINVAL
     vp = C.c_void_p(1 << 20)

@@ -164,7 +164,7 @@ def test_deviation_scatter_gather(dtype):
     want_k[pos.long()] = kn
     assert torch.equal(k2, want_k)
     rows = torch.empty_like(kn)
-    b.gather_rows(k2, kn[0].numel() * kn.element_size(), pos, nd, n, rows)
+    b.gather_rows(r.h, k2, kn[0].numel() * kn.element_size(), pos, nd, n, rows)
     torch.cuda.synchronize()
     assert torch.equal(rows, kn)
 
@@ -400,3 +400,88 @@ def test_deterministic():
     c = r.prefill([req], N, Q, n_c)
     for k in ("k", "v", "hidden", "sel", "dev1", "dev2"):
         assert torch.equal(a[k], c[k]), k
+
+
+def test_step_calls_check_positions_on_the_device():
+    """kv_deviation, scatter_kv and gather_rows take the cache / source row count: a
+    position or index outside it touches no memory and is reported as BLEND_EDEVICE, as is
+    a device count above max_n (clamped); the valid rows are still done."""
+    sh = SMALL_BF16
+    case = make_case(sh, 4, [8], pool="random")
+    r = GpuRunner(case, 64, 64, 64)
+    g = torch.Generator().manual_seed(21)
+    n_ctx, hkv, d = 300, sh.n_kv_heads, sh.head_dim
+    kc = torch.randn(n_ctx, hkv, d, generator=g).to(torch.bfloat16).to(dev())
+    vc = torch.randn(n_ctx, hkv, d, generator=g).to(torch.bfloat16).to(dev())
+    kn = torch.randn(4, hkv, d, generator=g).to(torch.bfloat16).to(dev())
+    vn = torch.randn(4, hkv, d, generator=g).to(torch.bfloat16).to(dev())
+    pos = torch.tensor([3, n_ctx, 7, -2], dtype=torch.int32, device=dev())
+    nd = torch.tensor([4], dtype=torch.int32, device=dev())
+
+    dv = torch.full((4,), -1.0, device=dev())
+    b.kv_deviation(r.h, kn, vn, kc, vc, pos, nd, 4, b.DEV_KV, dv)
+    with pytest.raises(b.BlendError) as e:
+        b.blend_device_status(r.h)
+    assert e.value.code == b.EDEVICE
+    want = [float(np.sum((f64(kn[i]) - f64(kc[p])) ** 2) + np.sum((f64(vn[i]) - f64(vc[p])) ** 2))
+            for i, p in ((0, 3), (2, 7))]
+    got = dv.cpu().numpy()
+    assert got[1] == 0.0 and got[3] == 0.0
+    np.testing.assert_allclose(got[[0, 2]], want, rtol=1e-5)
+
+    k2, v2 = kc.clone(), vc.clone()
+    b.scatter_kv(r.h, kn, vn, pos, nd, 4, k2, v2)
+    with pytest.raises(b.BlendError) as e:
+        b.blend_device_status(r.h)
+    assert e.value.code == b.EDEVICE
+    want_k, want_v = kc.clone(), vc.clone()
+    want_k[[3, 7]] = kn[[0, 2]]
+    want_v[[3, 7]] = vn[[0, 2]]
+    assert torch.equal(k2, want_k) and torch.equal(v2, want_v)
+
+    idx = torch.tensor([1, 400, 5], dtype=torch.int32, device=dev())
+    dst = torch.full((3, hkv, d), 7.0, dtype=torch.bfloat16, device=dev())
+    b.gather_rows(r.h, kc, hkv * d * 2, idx, torch.tensor([3], dtype=torch.int32, device=dev()), 3, dst)
+    with pytest.raises(b.BlendError) as e:
+        b.blend_device_status(r.h)
+    assert e.value.code == b.EDEVICE
+    assert torch.equal(dst[0], kc[1]) and torch.equal(dst[2], kc[5]) and bool((dst[1] == 7.0).all())
+
+    # a device count above max_n: clamped to max_n, reported
+    k3 = kc.clone()
+    ok_pos = torch.tensor([10, 11, 12, 13], dtype=torch.int32, device=dev())
+    b.scatter_kv(r.h, kn, vn, ok_pos, torch.tensor([9], dtype=torch.int32, device=dev()), 2, k3, vc.clone())
+    with pytest.raises(b.BlendError) as e:
+        b.blend_device_status(r.h)
+    assert e.value.code == b.EDEVICE
+    assert torch.equal(k3[[10, 11]], kn[[0, 1]]) and torch.equal(k3[[12, 13]], kc[[12, 13]])
+    b.blend_device_status(r.h)      # the word was cleared
+
+
+@pytest.mark.parametrize("shape", [synth.TINY, SMALL_BF16], ids=["f32", "bf16"])
+def test_selective_layer_with_a_device_count(shape):
+    """The row count of selective_layer can come straight from a device-side selection
+    (no host round trip): the set and its size from topk_select_dilate drive the layer,
+    with max_n above the count, and give the same rows as a call with the count on the host."""
+    case = make_case(shape, 4, [8], pool="random")
+    r = GpuRunner(case, 256, 1024, 512)
+    g = torch.Generator().manual_seed(13)
+    n_ctx, cap = 400, 200
+    dt = synth.torch_dtype(shape)
+    kc = (0.5 * torch.randn(n_ctx, shape.n_kv_heads, shape.head_dim, generator=g)).to(dt).to(dev())
+    vc = (0.5 * torch.randn(n_ctx, shape.n_kv_heads, shape.head_dim, generator=g)).to(dt).to(dev())
+    scores = torch.randn(n_ctx, generator=g).to(dev())
+    idx = torch.zeros(n_ctx, dtype=torch.int32, device=dev())
+    cnt = torch.zeros(1, dtype=torch.int32, device=dev())
+    b.topk_select_dilate(r.h, scores, n_ctx, 0, 97, 2, 1, b.BUDGET_FINAL, None, idx, cnt)
+    x = torch.randn(cap, shape.hidden, generator=g).to(dev())
+    xa, ka, va = x.clone(), kc.clone(), vc.clone()
+    b.selective_layer(r.h, 1, xa, idx, cnt, ka, va, n_ctx, max_n=cap)
+    b.blend_device_status(r.h)
+    n = int(cnt.item())
+    assert 0 < n <= 97
+    xb, kb, vb = x.clone(), kc.clone(), vc.clone()
+    b.selective_layer(r.h, 1, xb, idx[:n].clone(), n, kb, vb, n_ctx)
+    b.blend_device_status(r.h)
+    assert torch.equal(xa[:n], xb[:n]) and torch.equal(ka, kb) and torch.equal(va, vb)
+    assert torch.equal(xa[n:], x[n:])
