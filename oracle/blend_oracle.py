@@ -25,7 +25,11 @@ Parity pins (what each function is checked against, in tests/test_oracle_*.py):
   rope / realign      : rotation composition R(d)R(p)x = R(p+d)x, identity at 0, closed
                         form on basis vectors, relative-position invariance of q.k
   rmsnorm / silu      : closed forms on constant vectors
-  attention           : single key -> that value row; two keys -> closed-form softmax
+  layer_rest /        : closed forms with chosen weights: wo = wd = 0 is the identity; a zero
+  layer_kv deviation    query adds the mean value row through a permuted wo; one-hot SwiGLU
+                        weights add silu(gate) * up on one column; zero K/V projections
+                        against constant caches give hkv*d*(cK^2 + cV^2) (V only in V mode)
+  attention           : row-by-row brute force over several row blocks; single key -> that value row; two keys -> closed-form softmax
                         weights with the 1/sqrt(d) scale; GQA with duplicated K/V heads
                         equals MHA; causal mask by brute force
   full_prefill        : causality (a prefix of the input gives the same rows)
@@ -35,6 +39,10 @@ Parity pins (what each function is checked against, in tests/test_oracle_*.py):
   blend_prefill       : rho=100 % equals full prefill; rho=0 leaves every chunk row at its
                         realigned cache value; chunk 0 (shift 0) has zero layer-0 deviation
   importance_scores   : closed form on constant hidden states
+  round_bf16 /        : closed-form halfway and exponent cases, torch's float32 -> bfloat16
+  operand_round         conversion on 200 000 values; the mode's outputs are bf16 values,
+                        its residual stream is exact (only used to measure the floor of
+                        bf16 arithmetic, never as the parity reference)
   span_segments /     : a hand-worked case (tests/golden/span_completion.json), closed-form
   span_complete /       span lengths on a smooth ramp, invariants (T_init inside T, every
   span_select           covered span complete, nothing else added), degenerate thresholds,
@@ -55,6 +63,29 @@ from typing import Optional
 import numpy as np
 
 F64 = np.float64
+
+
+# ----------------------------------------------------------------------------------
+# bf16 operand rounding (used only to measure the floor of bf16 arithmetic)
+# ----------------------------------------------------------------------------------
+
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """Round to the nearest bfloat16 value, ties to even: 8 significant bits (one
+    implicit, seven stored) and the float32 exponent range.  x = m 2^e with
+    0.5 <= |m| < 1, so m 2^8 lies in [128, 256) and is rounded to an integer (half to
+    even); values below 2^-126 keep 8 significant bits instead of bf16's subnormal
+    spacing (they do not occur in the models here)."""
+    m, e = np.frexp(np.asarray(x, dtype=F64))
+    return np.ldexp(np.rint(m * 256.0), e - 8)
+
+
+def _rnd(x, operand_round):
+    """x unchanged, or rounded to bf16 when operand_round == "bf16"."""
+    if operand_round is None:
+        return x
+    if operand_round == "bf16":
+        return round_bf16(x)
+    raise ValueError(operand_round)
 
 
 # ----------------------------------------------------------------------------------
@@ -113,7 +144,8 @@ def silu(x: np.ndarray) -> np.ndarray:
     return x / (1.0 + np.exp(-x))
 
 
-def attention(q: np.ndarray, qpos: np.ndarray, K: np.ndarray, V: np.ndarray) -> np.ndarray:
+def attention(q: np.ndarray, qpos: np.ndarray, K: np.ndarray, V: np.ndarray,
+              operand_round: Optional[str] = None) -> np.ndarray:
     """Causal grouped-query attention of a set of query rows over a full KV.
 
     q[n, hq, d] at positions qpos[n]; K, V [N, hkv, d] indexed by position.  Query
@@ -126,7 +158,8 @@ def attention(q: np.ndarray, qpos: np.ndarray, K: np.ndarray, V: np.ndarray) -> 
     all logits against keys 0..max(qpos) of the block, the keys past a row's own
     position set to -inf, the row maximum subtracted, exponentiated, normalised and
     multiplied by V.  Blocks only bound the size of the logit array; every row is
-    computed on its own.
+    computed on its own.  With operand_round the exponentials are rounded before their
+    product with V (the normalising sum is taken on the unrounded ones).
     """
     n, hq, d = q.shape
     hkv = K.shape[1]
@@ -148,7 +181,7 @@ def attention(q: np.ndarray, qpos: np.ndarray, K: np.ndarray, V: np.ndarray) -> 
             s[np.broadcast_to(past[:, None, :], s.shape)] = -np.inf
             s = s - np.max(s, axis=2, keepdims=True)
             e = np.exp(s)
-            out[i0:i1, heads, :] = (e / np.sum(e, axis=2, keepdims=True)) @ Vg[:top]
+            out[i0:i1, heads, :] = (_rnd(e, operand_round) @ Vg[:top]) / np.sum(e, axis=2, keepdims=True)
     return out
 
 
@@ -172,7 +205,7 @@ def attention_probs(q: np.ndarray, qpos: np.ndarray, K: np.ndarray) -> np.ndarra
 
 def layer_kv(w: dict, cfg: dict, layer: int, x: np.ndarray, pos: np.ndarray,
              K: np.ndarray, V: np.ndarray, dev_rows: Optional[np.ndarray] = None,
-             dev_mode: str = "kv"):
+             dev_mode: str = "kv", operand_round: Optional[str] = None):
     """First half of a pre-norm decoder layer on the rows x[n, H] at positions pos[n]:
     RMSNorm, Q/K/V projection, RoPE at the blended positions, and the overwrite of this
     layer's cache rows K[pos], V[pos] with the fresh keys and values.
@@ -188,12 +221,15 @@ def layer_kv(w: dict, cfg: dict, layer: int, x: np.ndarray, pos: np.ndarray,
     how far the cached KV sits from the recomputed one; "Implementation": the largest
     deviation between newly computed and loaded KV).  dev_mode "v" compares V only
     (CacheClip paper, "Related work": CacheBlend compares the value matrix).
+    operand_round "bf16" rounds the normalised rows, q and the fresh k, v (after the
+    deviation, before the overwrite) to bf16: the operands of bf16 matrix products and
+    the cache's storage type (used only to measure the floor of bf16 arithmetic).
     Returns q [n, hq, d] and dev [n] (or None).
     """
     hq, hkv, d = cfg["n_q_heads"], cfg["n_kv_heads"], cfg["head_dim"]
     eps, theta = cfg["rms_eps"], cfg["rope_theta"]
     n = x.shape[0]
-    h = rmsnorm(x, w["attn_norm"][layer], eps)
+    h = _rnd(rmsnorm(x, w["attn_norm"][layer], eps), operand_round)
     q = (h @ w["wq"][layer].T).reshape(n, hq, d)
     k = (h @ w["wk"][layer].T).reshape(n, hkv, d)
     v = (h @ w["wv"][layer].T).reshape(n, hkv, d)
@@ -207,23 +243,27 @@ def layer_kv(w: dict, cfg: dict, layer: int, x: np.ndarray, pos: np.ndarray,
         if dev_mode == "kv":
             full = full + np.sum(dk * dk, axis=1)
         dev = np.where(dev_rows, full, 0.0)
-    K[pos] = k
-    V[pos] = v
-    return q, dev
+    K[pos] = _rnd(k, operand_round)
+    V[pos] = _rnd(v, operand_round)
+    return _rnd(q, operand_round), dev
 
 
 def layer_rest(w: dict, cfg: dict, layer: int, x: np.ndarray, q: np.ndarray, pos: np.ndarray,
-               K: np.ndarray, V: np.ndarray) -> np.ndarray:
+               K: np.ndarray, V: np.ndarray, operand_round: Optional[str] = None) -> np.ndarray:
     """Second half of the layer for the rows that continue: causal attention of their
     queries over this layer's full K, V, O-projection and residual, RMSNorm, SwiGLU MLP
-    and residual ("run the ordinary attention module to get the next layer's input")."""
+    and residual ("run the ordinary attention module to get the next layer's input").
+    operand_round "bf16" rounds the operands of the products (attention weights, the
+    attention output, the normalised rows, the SwiGLU output) to bf16; the residual
+    stream stays exact."""
     hq, d = cfg["n_q_heads"], cfg["head_dim"]
     eps = cfg["rms_eps"]
     n = x.shape[0]
-    o = attention(q, pos, K, V).reshape(n, hq * d)
+    o = _rnd(attention(q, pos, K, V, operand_round).reshape(n, hq * d), operand_round)
     x = np.asarray(x, dtype=F64) + o @ w["wo"][layer].T
-    h2 = rmsnorm(x, w["mlp_norm"][layer], eps)
-    return x + (silu(h2 @ w["wg"][layer].T) * (h2 @ w["wu"][layer].T)) @ w["wd"][layer].T
+    h2 = _rnd(rmsnorm(x, w["mlp_norm"][layer], eps), operand_round)
+    hmlp = _rnd(silu(h2 @ w["wg"][layer].T) * (h2 @ w["wu"][layer].T), operand_round)
+    return x + hmlp @ w["wd"][layer].T
 
 
 def layer_forward(w: dict, cfg: dict, layer: int, x: np.ndarray, pos: np.ndarray,
@@ -650,7 +690,7 @@ def blend_prefill(w: dict, cfg: dict, entries_k, entries_v, entry_tokens, prefix
                   scores: Optional[np.ndarray] = None, forced: Optional[list] = None,
                   dev_mode: str = "kv", group_rule: str = "window", tau_smooth: float = 0.4,
                   tau_cover_bp: int = 7000, max_span: int = 16, cap_bp: int = 0, epic_m: int = 0,
-                  focus_layer: int = 0, focus_bp: int = 0):
+                  focus_layer: int = 0, focus_bp: int = 0, operand_round: Optional[str] = None):
     """Selective KV-recompute prefill of one request.
 
     1. Assemble the blended cache (see assemble()).
@@ -682,6 +722,12 @@ def blend_prefill(w: dict, cfg: dict, entries_k, entries_v, entry_tokens, prefix
        With focus_bp > 0 (ext and epic): early termination for unfocused chunks (Cache-Craft
        notes, 3.2.2; see focused_chunks) at focus_layer, after that layer's K/V projection.
     3. Output the final RMSNorm of the query rows and the blended K, V of every layer.
+
+    operand_round None (the reference) computes every step exactly in float64.  "bf16"
+    rounds every operand of a matrix product, the cache rows written and the output to
+    bf16 (see layer_kv, layer_rest): not a reading of the method but the arithmetic of a
+    bf16 tensor-core implementation, run only to measure how far that arithmetic alone
+    moves the result away from the exact one.
 
     Positions in sets are absolute positions in the blended sequence.
     Returns a dict: hidden [Q, H], K, V [L, N, hkv, d], stages, dev1, dev2 ([N_c] each,
@@ -735,7 +781,7 @@ def blend_prefill(w: dict, cfg: dict, entries_k, entries_v, entry_tokens, prefix
     for layer in range(L):
         check = mode in ("hkvd", "forced") and layer in CHECK_LAYERS
         dev_rows = ((rows >= lo) & (rows < hi)) if check else None
-        q, dev = layer_kv(w, cfg, layer, x, rows, K[layer], V[layer], dev_rows, dev_mode)
+        q, dev = layer_kv(w, cfg, layer, x, rows, K[layer], V[layer], dev_rows, dev_mode, operand_round)
         if dev is not None:
             full = np.zeros(n_c, dtype=F64)
             full[rows[dev_rows] - lo] = dev[dev_rows]
@@ -764,9 +810,9 @@ def blend_prefill(w: dict, cfg: dict, entries_k, entries_v, entry_tokens, prefix
             where = {int(p): i for i, p in enumerate(rows)}
             keep = [where[int(p)] for p in new_rows]
             x, q, rows = x[keep], q[keep], new_rows
-        x = layer_rest(w, cfg, layer, x, q, rows, K[layer], V[layer])
+        x = layer_rest(w, cfg, layer, x, q, rows, K[layer], V[layer], operand_round)
     qi = np.searchsorted(rows, qrows)
-    hidden = rmsnorm(x[qi], w["final_norm"], cfg["rms_eps"])
+    hidden = _rnd(rmsnorm(x[qi], w["final_norm"], cfg["rms_eps"]), operand_round)
     return {"hidden": hidden, "K": K, "V": V, "stages": stages,
             "dev1": devs.get(CHECK_LAYERS[0]), "dev2": devs.get(CHECK_LAYERS[1]),
             "tokens": tokens, "N": N, "n_c": n_c}

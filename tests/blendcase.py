@@ -139,3 +139,37 @@ def set_diff_is_near_tie(got, want, score, k, rel=1e-3) -> bool:
     kth = np.sort(s)[::-1][k - 1]
     tol = rel * np.max(np.abs(s))
     return all(abs(s[p] - kth) <= tol for p in got ^ want)
+
+
+class LayerwiseF64:
+    """A stacked torch weight ([layer][...] or [vocab][H]) that the oracle reads one slice
+    at a time as float64, so a full-depth model never needs a float64 copy of every
+    layer at once.  Indexing converts only the requested rows or layer."""
+
+    def __init__(self, t: torch.Tensor):
+        self.t = t
+
+    def __getitem__(self, i):
+        if isinstance(i, np.ndarray):
+            i = torch.from_numpy(i.astype(np.int64)).to(self.t.device)
+        return f64(self.t[i])
+
+    @property
+    def shape(self):
+        return tuple(self.t.shape)
+
+
+def layerwise_weights(w: dict) -> dict:
+    """Oracle view of model_weights(): every stacked tensor converted on access; the
+    final norm gain (one vector) as float64."""
+    return {k: (f64(v) if k == "final_norm" else LayerwiseF64(v)) for k, v in w.items()}
+
+
+def per_layer_errors(got_k, got_v, ref_k, ref_v):
+    """Per layer: (2-norm relative, max-norm relative) of K and of V; got_* are device
+    tensors [L][N][hkv][d], converted one layer at a time."""
+    rows = []
+    for l in range(ref_k.shape[0]):
+        gk, gv = f64(got_k[l]), f64(got_v[l])
+        rows.append((relerr(gk, ref_k[l]), maxrel(gk, ref_k[l]), relerr(gv, ref_v[l]), maxrel(gv, ref_v[l])))
+    return rows

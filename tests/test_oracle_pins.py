@@ -534,3 +534,57 @@ def test_deviation_of_a_known_value_row():
     for i in range(3):
         n_c = x[i, c] / math.sqrt(sum(v * v for v in x[i]) / 32 + 1e-6)
         assert abs(dev[i] - 16 * n_c * n_c) <= 1e-12 * 16 * n_c * n_c
+
+
+# ---------------------------------------------------------------- bf16 operand rounding
+
+def test_round_bf16_closed_forms():
+    """bf16 keeps 8 significant bits: near 1 the spacing is 2^-7, halfway cases go to
+    the even neighbour, signs are kept, and the exponent is untouched."""
+    u = 2.0 ** -7
+    cases = [(1.0, 1.0), (1 + u / 2, 1.0), (1 + 1.5 * u, 1 + 2 * u), (1 + u / 2 + 2.0 ** -30, 1 + u),
+             (-(1 + u / 2), -1.0), (1 + u, 1 + u), (0.0, 0.0), (3.0 * 2.0 ** 100, 3.0 * 2.0 ** 100),
+             (2.0 - u / 4, 2.0), (255.5, 256.0), (254.5, 254.0), (1e-30, None)]
+    for x, want in cases:
+        got = float(O.round_bf16(np.array([x]))[0])
+        if want is None:       # any value: 8 significant bits, within half a spacing
+            m, e = math.frexp(x)
+            assert abs(got - x) <= 2.0 ** (e - 9) and float(O.round_bf16(np.array([got]))[0]) == got
+        else:
+            assert got == want, (x, got, want)
+
+
+def test_round_bf16_matches_torch_conversion():
+    """Against torch's float32 -> bfloat16 conversion (round to nearest even) on float32
+    values, which float64 holds exactly, over a wide exponent range."""
+    torch = pytest.importorskip("torch")
+    r = np.random.default_rng(30)
+    x = (r.standard_normal(200000) * np.exp2(r.integers(-60, 60, 200000))).astype(np.float32)
+    want = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(O.round_bf16(x.astype(np.float64)), want)
+
+
+def test_operand_rounding_mode(tiny_setup):
+    """operand_round="bf16": the cache rows written and the output are bf16 values, the
+    residual stream is not rounded (wo = wd = 0 returns the input exactly), and the
+    result stays within a few bf16 spacings of the exact one; None is the exact oracle."""
+    cfg, w, prefix, chunks, query, ks, vs = tiny_setup
+    order = [1, 2, 0]
+    scores = np.random.default_rng(4).standard_normal(24)
+    kw = dict(rho_bp=5000, window=2, tau=1, scores=scores)
+    ex = O.blend_prefill(w, cfg, ks, vs, chunks, prefix, order, query, "ext", **kw)
+    rb = O.blend_prefill(w, cfg, ks, vs, chunks, prefix, order, query, "ext", operand_round="bf16", **kw)
+    rows = np.concatenate([ex["stages"][0][1], np.arange(28, 32)])
+    for t in (rb["K"][:, rows], rb["V"][:, rows], rb["hidden"]):
+        np.testing.assert_array_equal(O.round_bf16(t), t)
+    for a, e in ((rb["hidden"], ex["hidden"]), (rb["K"], ex["K"]), (rb["V"], ex["V"])):
+        err = np.max(np.abs(a - e)) / np.max(np.abs(e))
+        assert 0 < err < 3e-2
+    w0 = {k: v.copy() for k, v in w.items()}
+    w0["wo"][0] = 0.0
+    w0["wd"][0] = 0.0
+    x = np.random.default_rng(5).standard_normal((3, 32)) * 7.3
+    q = np.random.default_rng(6).standard_normal((3, 4, 8))
+    Kc = np.random.default_rng(7).standard_normal((9, 2, 8))
+    np.testing.assert_array_equal(
+        O.layer_rest(w0, cfg, 0, x, q, np.array([2, 5, 8]), Kc, Kc.copy(), operand_round="bf16"), x)
