@@ -740,6 +740,7 @@ def blend_prefill(w: dict, cfg: dict, entries_k, entries_v, entry_tokens, prefix
     Q = len(query_tokens)
     N = P + n_c + Q
     K, V = assemble(entries_k, entries_v, chunk_ids, P, lens, Q, cfg["rope_theta"])
+    K = _rnd(K, operand_round)          # the realigned keys as a bf16 cache stores them
     tokens = np.concatenate([np.asarray(prefix_tokens)] + [np.asarray(entry_tokens[c]) for c in chunk_ids]
                             + [np.asarray(query_tokens)])
     lo, hi = P, P + n_c

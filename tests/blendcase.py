@@ -167,9 +167,34 @@ def layerwise_weights(w: dict) -> dict:
 
 def per_layer_errors(got_k, got_v, ref_k, ref_v):
     """Per layer: (2-norm relative, max-norm relative) of K and of V; got_* are device
-    tensors [L][N][hkv][d], converted one layer at a time."""
+    tensors [L][N][hkv][d], converted one layer at a time (or float64 arrays)."""
     rows = []
+    conv = lambda t: t if isinstance(t, np.ndarray) else f64(t)
     for l in range(ref_k.shape[0]):
-        gk, gv = f64(got_k[l]), f64(got_v[l])
+        gk, gv = conv(got_k[l]), conv(got_v[l])
         rows.append((relerr(gk, ref_k[l]), maxrel(gk, ref_k[l]), relerr(gv, ref_v[l]), maxrel(gv, ref_v[l])))
     return rows
+
+
+def assert_hkvd_sets_replay(out, P, n_c, r1_bp, rho_bp, window, tau, budget_mode, r=0):
+    """The GPU's HKVD stage sets of request r (chunk rows r*n_c.. of the outputs) equal the
+    oracle's top-k and selection run on the GPU's own deviation arrays, bit for bit: C1 =
+    topk(dev1, ceil(r1 N_c)), S = select(dev2 over C1) within C1.  Returns (c1, sel) as
+    absolute positions."""
+    c0 = r * n_c
+    n1, ns = int(out["n_c1"][r].item()), int(out["n_sel"][r].item())
+    c1 = out["c1"][c0:c0 + n1].cpu().numpy().astype(np.int64)
+    sel = out["sel"][c0:c0 + ns].cpu().numpy().astype(np.int64)
+    d1 = f64(out["dev1"][c0:c0 + n_c])
+    d2 = f64(out["dev2"][c0:c0 + n_c])
+    assert n1 == O.ceil_bp(r1_bp, n_c)
+    assert c1.tolist() == sorted(P + t for t in O.topk(d1, n1))
+    allowed = np.zeros(n_c, dtype=bool)
+    allowed[c1 - P] = True
+    assert np.all(d2[~allowed] == 0)
+    budget = O.ceil_bp(rho_bp, n_c)
+    ds = np.where(allowed, d2, -np.inf)
+    want = (O.select(ds, budget, window, tau, "candidate", allowed=allowed, base=P) if budget_mode == "candidate"
+            else O.select_final_bisect(ds, budget, window, tau, allowed=allowed, base=P))
+    assert sel.tolist() == want.tolist()
+    return c1, sel

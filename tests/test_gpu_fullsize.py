@@ -17,17 +17,14 @@ from rag_kv_cache_rope_gb300 import binding as b
 from rag_kv_cache_rope_gb300 import build as B
 from rag_kv_cache_rope_gb300 import synth
 
-from blendcase import f64, maxrel, oracle_cfg, relerr, set_diff_is_near_tie, stages_to_device
+from blendcase import (assert_hkvd_sets_replay, f64, maxrel, oracle_cfg, relerr, set_diff_is_near_tie,
+                       stages_to_device)
 
 pytestmark = pytest.mark.gpu
 
-# bf16 outputs: norm-wise relative error within the 2e-2 bar, and a max-norm guard
-# (max|d| / max|ref|) that catches a wrong row or head the 2-norm would dilute.  The
-# guard is 2e-2 up to two layers deep; three layers of bf16 intermediates reach ~2.0e-2
-# on the 8B shape (an oracle copy rounding at the same points to bf16 shows the same
-# RMS error), so there it is 3e-2.
+# bf16 outputs: the benchmark spec's 2e-2, as the norm-wise relative error and as the
+# max-norm (max|d| / max|ref|) that catches a wrong row or head the 2-norm would dilute.
 TOL_BF16 = 2e-2
-TOL_BF16_MAX_DEEP = 3e-2
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -165,21 +162,18 @@ def test_llama8b_3k_hkvd15_three_layers():
     b.blend_prefill(h, [b.RequestRef(req.chunk_ids, qd, mode="hkvd", **kw)], fc.pool, out)
     b.blend_device_status(h)
     check("8B HKVD dev1", out["dev1"], ref["dev1"])
-    c1_ref = ref["stages"][1][1]
-    n1 = int(out["n_c1"][0].item())
-    assert n1 == len(c1_ref) == O.ceil_bp(wl.r1_bp, fc.n_c)
     P = wl.prefix_len
-    assert set_diff_is_near_tie(out["c1"][:n1].cpu().numpy() - P, c1_ref - P, ref["dev1"], n1, rel=TOL_BF16)
-    ns = int(out["n_sel"][0].item())
-    assert ns <= O.ceil_bp(wl.rho_bp, fc.n_c)
-    assert set(out["sel"][:ns].cpu().numpy().tolist()) <= set(out["c1"][:n1].cpu().numpy().tolist())
+    # the GPU's sets: exactly the oracle's top-k / selection of the GPU's own deviations, and
+    # the first stage equal to the oracle's up to near-ties of the oracle's deviations
+    c1, sel = assert_hkvd_sets_replay(out, P, fc.n_c, wl.r1_bp, wl.rho_bp, wl.window, wl.tau, wl.budget_mode)
+    assert set_diff_is_near_tie(c1 - P, ref["stages"][1][1] - P, ref["dev1"], len(c1), rel=TOL_BF16)
     # values with the GPU forced onto the oracle's stage sets
     out2 = fc.outputs()
     b.blend_prefill(h, [b.RequestRef(req.chunk_ids, qd, mode="forced",
                                      stages=stages_to_device(ref["stages"], dev()))], fc.pool, out2)
     b.blend_device_status(h)
     for k, rk in (("k", "K"), ("v", "V"), ("hidden", "hidden")):
-        check(f"8B HKVD forced {k}", out2[k], ref[rk], tol_max=TOL_BF16_MAX_DEEP)
+        check(f"8B HKVD forced {k}", out2[k], ref[rk])
     check("8B HKVD forced dev2", out2["dev2"], ref["dev2"])
 
 
