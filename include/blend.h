@@ -243,13 +243,14 @@ int blend_set_tensor_cores(blend_handle* h, int on);
  * allocate device memory when they select tokens - for example a serving loop that
  * reserves all HBM for its KV pool at start-up, or one that must not call cudaMalloc /
  * cudaFree on its hot path because those calls can synchronise the device or fail
- * under fragmentation.  The call uses a fixed scratch array of 32768 ranks (128 KB)
- * in device memory that every GPU which loads the library holds until the process
- * exits; it never allocates or frees memory.
+ * under fragmentation.  The call uses fixed scratch arrays in device memory (32768 ranks
+ * and 32768 sorted 64-bit keys, 384 KB) that every GPU which loads the library holds
+ * until the process exits; it never allocates or frees memory.
  *   - n above 32768 is rejected with BLEND_EINVAL (nothing is launched).
- *   - The first call on each device looks up the array's device address (with that
- *     device current); make that first call before any stream capture.
- *   - Every call shares the one array: calls whose work overlaps on the GPU (on
+ *   - Every call looks up the arrays' device addresses on the current device (a
+ *     host-side query; the first one on a device may load the library's device code, so
+ *     make the first call on each device before any stream capture).
+ *   - Every call shares the one set of arrays: calls whose work overlaps on the GPU (on
  *     different streams, or on several host threads) race and give wrong sets.
  *     Each call rewrites every scratch entry it reads, so nothing needs clearing.
  * Errors: as topk_select_dilate; the text is in blend_last_error(NULL). */

@@ -80,6 +80,7 @@ struct blend_handle {
     int32_t* tokens;
     int32_t* err;
     int32_t* rank;
+    unsigned long long* rank_keys;  // selection: sorted 64-bit keys per 2048-position tile
     int32_t* set[3];
     int32_t* set_n[3];
     uint8_t* mask;
@@ -278,6 +279,7 @@ Layout make_layout(const blend_model_cfg* c, const blend_limits* l) {
     for (int b = 0; b < 4; ++b)                            // 36..39 host-pool staging: K, V x 2 buffers
         L.add((size_t)l->max_tokens * kvd * es);
     L.add(M * NORM_PARTS_MAX * sizeof(float));             // 40 folded-RMSNorm partial sums of squares
+    L.add((size_t)l->max_batch * ((l->max_chunk_rows + 2047) / 2048 * 2048) * 8);  // 41 sorted rank keys
     return L;
 }
 
@@ -497,6 +499,7 @@ int blend_init(const blend_model_cfg* cfg, const blend_weights* w, const blend_l
     ++i;
     for (int q = 0; q < 4; ++q) h->stage[q] = b + L.off[i++];
     h->ssq = (float*)(b + L.off[i++]);
+    h->rank_keys = (unsigned long long*)(b + L.off[i++]);
     h->use_tc = cfg->dtype == BLEND_BF16 ? tc_available() : 0;
     cudaStream_t s = (cudaStream_t)stream;
     cudaMemsetAsync(h->err, 0, 16, s);
@@ -635,7 +638,7 @@ int topk_select_dilate(blend_handle* h, const float* scores, int32_t n, int32_t 
     sb.tau = tau;
     sb.budget_mode = budget_mode;
     sb.j[0] = SelectJob{scores, allowed, idx_out, n_out, n, base, budget, 0};
-    launch_select(sb, h->rank, n, (cudaStream_t)stream);
+    launch_select(sb, h->rank, h->rank_keys, n, (cudaStream_t)stream);
     return check_cuda(h, "topk_select_dilate");
 }
 
@@ -662,7 +665,7 @@ int span_select(blend_handle* h, const float* scores, int32_t n, int32_t base, i
     sb.tau_cover_bp = tau_cover_bp;
     sb.max_span = max_span;
     sb.j[0] = SelectJob{scores, nullptr, idx_out, n_out, n, base, budget, 0, cap};
-    launch_select(sb, h->rank, n, (cudaStream_t)stream);
+    launch_select(sb, h->rank, h->rank_keys, n, (cudaStream_t)stream);
     return check_cuda(h, "span_select");
 }
 
@@ -1101,7 +1104,7 @@ extern "C" int blend_prefill(blend_handle* h, int32_t n_req, const blend_request
             max_n = info[r].n_c > max_n ? info[r].n_c : max_n;
         }
         ProfScope ps(h, PROF_SELECT, s);
-        launch_select(sb, h->rank, max_n, s);
+        launch_select(sb, h->rank, h->rank_keys, max_n, s);
     } else if (mode == BLEND_SEL_HKVD) {
         st0.iota = 1;
         n_stage = 3;
@@ -1234,7 +1237,7 @@ extern "C" int blend_prefill(blend_handle* h, int32_t n_req, const blend_request
                     max_n = info[r].n_c > max_n ? info[r].n_c : max_n;
                 }
                 ProfScope ps(h, PROF_SELECT, s);
-                launch_select(sb, h->rank, max_n, s);
+                launch_select(sb, h->rank, h->rank_keys, max_n, s);
             } else if (focus) {
                 // the query rows' attention at this layer, per chunk: their q (into the free
                 // attention-output buffer), column means over chunk tokens, then the filter

@@ -203,8 +203,11 @@ struct SelectBatch {
     SelectJob j[BLEND_MAX_BATCH];
 };
 // Ranks (select.cu), then the window rule (select.cu) or the span rule (span.cu).
-void launch_select(const SelectBatch& sb, int32_t* rank_scratch, int max_n, cudaStream_t s);
-void launch_rank(const SelectBatch& sb, int32_t* rank_scratch, int max_n, cudaStream_t s);
+// sort_scratch: n_job * roundup(max_n, 2048) keys (select.cu, RANK_TILE).
+void launch_select(const SelectBatch& sb, int32_t* rank_scratch, unsigned long long* sort_scratch, int max_n,
+                   cudaStream_t s);
+void launch_rank(const SelectBatch& sb, int32_t* rank_scratch, unsigned long long* sort_scratch, int max_n,
+                 cudaStream_t s);
 void launch_span_finish(const SelectBatch& sb, const int32_t* rank_scratch, int max_n, cudaStream_t s);
 // CacheClip 6.2 auxiliary scores (aux.cu): the query rows' last-layer q out of the per-kv-head
 // slab, then per chunk column the mean attention weight over query rows and heads.

@@ -16,7 +16,6 @@
 // value.  All arithmetic is integer, so the result is exact.
 #include <climits>
 #include <cstring>
-#include <mutex>
 
 #include "common.cuh"
 
@@ -39,65 +38,121 @@ __device__ __forceinline__ unsigned long long sel_key(float s, int t) {
     return ((unsigned long long)k << 32) | (uint32_t)t;
 }
 
-// rank[t] = #{u allowed : key(u) < key(t)} for allowed t, INT_MAX otherwise.
-__global__ void __launch_bounds__(256)
-    k_rank(const __grid_constant__ SelectBatch sb, int32_t* __restrict__ rank) {
+// rank[t] = #{u allowed : key(u) < key(t)} for allowed t, INT_MAX otherwise, in two
+// steps over tiles of RANK_TILE positions:
+//   k_rank_tiles  one CTA per tile bitonic-sorts the tile's 64-bit keys (disallowed and
+//                 padding positions get ~0, which sorts after every real key) in shared
+//                 memory and stores the sorted tile;
+//   k_rank_merge  one CTA per tile takes its sorted keys and, for every sorted tile in
+//                 turn, counts the keys below each of them by binary search in shared
+//                 memory; the sum over tiles is the rank (keys are distinct: the position
+//                 is part of the key).
+// O(n log n) work instead of the n^2 comparisons of a direct count.
+constexpr int RANK_THREADS = 1024;  // RANK_TILE = 2 keys per thread
+
+__global__ void __launch_bounds__(RANK_THREADS)
+    k_rank_tiles(const __grid_constant__ SelectBatch sb, unsigned long long* __restrict__ sorted,
+                 int sorted_stride, int32_t* __restrict__ rank) {
+    __shared__ unsigned long long key[RANK_TILE];
+    const SelectJob& jb = sb.j[blockIdx.y];
+    const int n = jb.n;
+    const int base = blockIdx.x * RANK_TILE;
+    if (base >= n) return;
+    for (int i = threadIdx.x; i < RANK_TILE; i += RANK_THREADS) {
+        const int t = base + i;
+        unsigned long long k = ~0ull;
+        if (t < n) {
+            if (jb.allowed == nullptr || jb.allowed[t] != 0) k = sel_key(jb.scores[t], t);
+            else rank[jb.rank_off + t] = INT_MAX;
+        }
+        key[i] = k;
+    }
+    __syncthreads();
+    // bitonic network, ascending: one compare-exchange per thread and stage
+    const int i = threadIdx.x;
+    for (int k = 2; k <= RANK_TILE; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            const int l = 2 * i - (i & (j - 1));
+            const int r = l + j;
+            const unsigned long long a = key[l], b = key[r];
+            if ((a > b) == ((l & k) == 0)) {
+                key[l] = b;
+                key[r] = a;
+            }
+            __syncthreads();
+        }
+    }
+    unsigned long long* dst = sorted + (long long)blockIdx.y * sorted_stride + base;
+    for (int e = threadIdx.x; e < RANK_TILE; e += RANK_THREADS) dst[e] = key[e];
+}
+
+__global__ void __launch_bounds__(RANK_THREADS)
+    k_rank_merge(const __grid_constant__ SelectBatch sb, const unsigned long long* __restrict__ sorted,
+                 int sorted_stride, int32_t* __restrict__ rank) {
     __shared__ unsigned long long tile[RANK_TILE];
     const SelectJob& jb = sb.j[blockIdx.y];
     const int n = jb.n;
-    if (blockIdx.x * blockDim.x >= n) return;
-    const int t = blockIdx.x * blockDim.x + threadIdx.x;
-    const bool mine_ok = t < n && (jb.allowed == nullptr || jb.allowed[t] != 0);
-    const unsigned long long mine = mine_ok ? sel_key(jb.scores[t], t) : ~0ull;
-    int cnt = 0;
-    for (int base = 0; base < n; base += RANK_TILE) {
-        for (int i = threadIdx.x; i < RANK_TILE; i += blockDim.x) {
-            int u = base + i;
-            unsigned long long key = ~0ull;
-            if (u < n && (jb.allowed == nullptr || jb.allowed[u] != 0)) key = sel_key(jb.scores[u], u);
-            tile[i] = key;
+    const int a0 = blockIdx.x * RANK_TILE;
+    if (a0 >= n) return;
+    const unsigned long long* srt = sorted + (long long)blockIdx.y * sorted_stride;
+    const unsigned long long q0 = srt[a0 + threadIdx.x], q1 = srt[a0 + RANK_THREADS + threadIdx.x];
+    int c0 = 0, c1 = 0;
+    const int n_tiles = (n + RANK_TILE - 1) / RANK_TILE;
+    for (int bt = 0; bt < n_tiles; ++bt) {
+        __syncthreads();
+        for (int e = threadIdx.x; e < RANK_TILE; e += RANK_THREADS) tile[e] = srt[bt * RANK_TILE + e];
+        __syncthreads();
+        // number of keys below q in the sorted tile (lower bound)
+        int l0 = 0, l1 = 0;
+#pragma unroll
+        for (int step = RANK_TILE / 2; step > 0; step >>= 1) {
+            if (tile[l0 + step - 1] < q0) l0 += step;
+            if (tile[l1 + step - 1] < q1) l1 += step;
         }
-        __syncthreads();
-        const int lim = min(RANK_TILE, n - base);
-#pragma unroll 8
-        for (int i = 0; i < lim; ++i) cnt += (tile[i] < mine) ? 1 : 0;
-        __syncthreads();
+        c0 += l0 + (tile[l0] < q0 ? 1 : 0);
+        c1 += l1 + (tile[l1] < q1 ? 1 : 0);
     }
-    if (t < n) rank[jb.rank_off + t] = mine_ok ? cnt : INT_MAX;
+    if (q0 != ~0ull) rank[jb.rank_off + (int)(uint32_t)q0] = c0;
+    if (q1 != ~0ull) rank[jb.rank_off + (int)(uint32_t)q1] = c1;
 }
 
-__device__ __forceinline__ int block_sum_int(int v, int* red) {
-    const int t = threadIdx.x;
-    red[t] = v;
+// Deterministic block-wide integer sum (warp reductions, then one warp over the warp
+// totals); every thread gets the result.  Two barriers.
+__device__ __forceinline__ int block_sum_i32(int v, int* warp_tot, int* bcast) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    v = __reduce_add_sync(0xffffffffu, v);
+    if (lane == 0) warp_tot[warp] = v;
     __syncthreads();
-    for (int s = blockDim.x >> 1; s > 0; s >>= 1) {
-        if (t < s) red[t] += red[t + s];
-        __syncthreads();
+    if (warp == 0) {
+        int x = lane < (int)(blockDim.x >> 5) ? warp_tot[lane] : 0;
+        x = __reduce_add_sync(0xffffffffu, x);
+        if (lane == 0) *bcast = x;
     }
-    int r = red[0];
     __syncthreads();
-    return r;
+    return *bcast;
 }
 
-// One CTA per job.  Thread i owns the contiguous positions [i*per, (i+1)*per).
+// One CTA per job.  Positions are walked in rounds of SEL_THREADS consecutive positions
+// (round e, thread i: p = e * SEL_THREADS + i), so the accesses of a warp to shared and
+// global memory are consecutive.
 __global__ void __launch_bounds__(SEL_THREADS)
     k_select_finish(const __grid_constant__ SelectBatch sb, const int32_t* __restrict__ rank_all) {
     extern __shared__ int32_t cov[];  // n ints: qual, then cover
-    __shared__ int red[SEL_THREADS];
+    __shared__ int warp_tot[SEL_THREADS / 32];
+    __shared__ int bcast;
     const SelectJob& jb = sb.j[blockIdx.x];
     const int n = jb.n;
     const int w = sb.window, tau = sb.tau;
     const int* rank = rank_all + jb.rank_off;
-    const int per = (n + SEL_THREADS - 1) / SEL_THREADS;
-    const int p0 = min(n, threadIdx.x * per), p1 = min(n, p0 + per);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
     int loc = 0;
-    for (int t = p0; t < p1; ++t) loc += rank[t] != INT_MAX;
-    const int n_ok = block_sum_int(loc, red);
+    for (int t = tid; t < n; t += SEL_THREADS) loc += rank[t] != INT_MAX;
+    const int n_ok = block_sum_i32(loc, warp_tot, &bcast);
     const int kmax = min(jb.budget, n_ok);
 
     // qual(t); ranks >= kmax can never be candidates and count as infinite.
-    for (int t = p0; t < p1; ++t) {
+    for (int t = tid; t < n; t += SEL_THREADS) {
         int q = INT_MAX;
         const int rt = rank[t];
         if (t <= n - w && rt < kmax) {
@@ -123,38 +178,42 @@ __global__ void __launch_bounds__(SEL_THREADS)
         cov[t] = q;
     }
     __syncthreads();
+    // cover(p) = min of qual over the windows (p-w, p] covering p; kept in registers until
+    // every thread has read the qual values it needs
     int cl[SEL_MAX_PER_THREAD];
 #pragma unroll
     for (int e = 0; e < SEL_MAX_PER_THREAD; ++e) {
-        const int p = p0 + e;
+        const int p = e * SEL_THREADS + tid;
         int c = INT_MAX;
-        if (p < p1) {
-            if (jb.allowed == nullptr || jb.allowed[p] != 0) {
-                const int lo = max(0, p - w + 1);
-                for (int t = lo; t <= p; ++t) c = min(c, cov[t]);
-            }
+        if (p < n && (jb.allowed == nullptr || jb.allowed[p] != 0)) {
+            const int lo = max(0, p - w + 1);
+            for (int t = lo; t <= p; ++t) c = min(c, cov[t]);
         }
         cl[e] = c;
     }
     __syncthreads();
 #pragma unroll
-    for (int e = 0; e < SEL_MAX_PER_THREAD; ++e)
-        if (p0 + e < p1) cov[p0 + e] = cl[e];
+    for (int e = 0; e < SEL_MAX_PER_THREAD; ++e) {
+        const int p = e * SEL_THREADS + tid;
+        if (p < n) cov[p] = cl[e];
+    }
     __syncthreads();
 
     int k = kmax;
     if (sb.budget_mode == BLEND_BUDGET_FINAL && kmax > 0) {
         loc = 0;
-        for (int p = p0; p < p1; ++p) loc += cov[p] < kmax;
-        const int f = block_sum_int(loc, red);
+#pragma unroll
+        for (int e = 0; e < SEL_MAX_PER_THREAD; ++e) loc += cl[e] < kmax;
+        const int f = block_sum_i32(loc, warp_tot, &bcast);
         if (f > jb.budget) {
             // smallest v with #{cover <= v} >= budget + 1
             int lo = 0, hi = kmax - 1;
             while (lo < hi) {
                 const int mid = (lo + hi) >> 1;
                 loc = 0;
-                for (int p = p0; p < p1; ++p) loc += cov[p] <= mid;
-                const int c = block_sum_int(loc, red);
+#pragma unroll
+                for (int e = 0; e < SEL_MAX_PER_THREAD; ++e) loc += cl[e] <= mid;
+                const int c = block_sum_i32(loc, warp_tot, &bcast);
                 if (c >= jb.budget + 1) hi = mid;
                 else lo = mid + 1;
             }
@@ -162,35 +221,51 @@ __global__ void __launch_bounds__(SEL_THREADS)
         }
     }
 
-    // ordered compaction of {p : cover(p) < k}
-    loc = 0;
-    for (int p = p0; p < p1; ++p) loc += cov[p] < k;
-    red[threadIdx.x] = loc;
-    __syncthreads();
-    for (int s = 1; s < SEL_THREADS; s <<= 1) {  // inclusive Hillis-Steele scan
-        int v = threadIdx.x >= s ? red[threadIdx.x - s] : 0;
+    // ordered compaction of {p : cover(p) < k}, one round of SEL_THREADS positions at a time
+    int written = 0;
+    for (int e = 0; e * SEL_THREADS < n; ++e) {
+        const int p = e * SEL_THREADS + tid;
+        const bool take = p < n && cov[p] < k;
+        const unsigned m = __ballot_sync(0xffffffffu, take);
+        if (lane == 0) warp_tot[warp] = __popc(m);
         __syncthreads();
-        red[threadIdx.x] += v;
+        if (warp == 0) {
+            // exclusive scan of the warp totals
+            const int v = warp_tot[lane];
+            int incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            warp_tot[lane] = incl - v;
+            if (lane == 31) bcast = incl;
+        }
+        __syncthreads();
+        if (take) jb.out[written + warp_tot[warp] + __popc(m & ((1u << lane) - 1u))] = jb.base + p;
+        written += bcast;
         __syncthreads();
     }
-    int o = red[threadIdx.x] - loc;
-    for (int p = p0; p < p1; ++p)
-        if (cov[p] < k) jb.out[o++] = jb.base + p;
-    if (threadIdx.x == SEL_THREADS - 1) *jb.out_n = red[SEL_THREADS - 1];
+    if (tid == 0) *jb.out_n = written;
 }
 
-void launch_rank(const SelectBatch& sb, int32_t* rank_scratch, int max_n, cudaStream_t s) {
+void launch_rank(const SelectBatch& sb, int32_t* rank_scratch, unsigned long long* sort_scratch, int max_n,
+                 cudaStream_t s) {
     if (sb.n_job <= 0) return;
     if (max_n <= 0) max_n = 1;
-    dim3 g1((max_n + 255) / 256, sb.n_job);
-    k_rank<<<g1, 256, 0, s>>>(sb, rank_scratch);
-    note_launch(1);
+    const int tiles = (max_n + RANK_TILE - 1) / RANK_TILE;
+    const int stride = tiles * RANK_TILE;
+    dim3 g(tiles, sb.n_job);
+    k_rank_tiles<<<g, RANK_THREADS, 0, s>>>(sb, sort_scratch, stride, rank_scratch);
+    k_rank_merge<<<g, RANK_THREADS, 0, s>>>(sb, sort_scratch, stride, rank_scratch);
+    note_launch(2);
 }
 
-void launch_select(const SelectBatch& sb, int32_t* rank_scratch, int max_n, cudaStream_t s) {
+void launch_select(const SelectBatch& sb, int32_t* rank_scratch, unsigned long long* sort_scratch, int max_n,
+                   cudaStream_t s) {
     if (sb.n_job <= 0) return;
     if (max_n <= 0) max_n = 1;
-    launch_rank(sb, rank_scratch, max_n, s);
+    launch_rank(sb, rank_scratch, sort_scratch, max_n, s);
     if (sb.rule == BLEND_GROUP_SPAN) {
         launch_span_finish(sb, rank_scratch, max_n, s);
         return;
@@ -203,30 +278,31 @@ void launch_select(const SelectBatch& sb, int32_t* rank_scratch, int max_n, cuda
 }
 
 // ---------------------------------------------------------------- allocation-free variant
-// Rank scratch of topk_select_dilate_noalloc: a fixed array in device memory, so the
-// call needs neither a handle nor any allocation.  Every GPU that loads the library
-// holds these 128 KB until the process exits.
+// Scratch of topk_select_dilate_noalloc: fixed arrays in device memory, so the call needs
+// neither a handle nor any allocation.  Every GPU that loads the library holds these
+// 384 KB (32768 ranks and 32768 sorted 64-bit keys) until the process exits.
 constexpr int NOALLOC_MAX_N = 32768;
 static __device__ __align__(256) int32_t g_noalloc_rank[NOALLOC_MAX_N];
+static __device__ __align__(256) unsigned long long g_noalloc_sorted[NOALLOC_MAX_N];
 
 namespace {
-constexpr int NOALLOC_MAX_DEVICES = 64;
-std::mutex g_noalloc_mu;
-int32_t* g_noalloc_ptr[NOALLOC_MAX_DEVICES] = {};
+struct NoallocScratch {
+    int32_t* rank = nullptr;
+    unsigned long long* sorted = nullptr;
+};
 
-// Device address of g_noalloc_rank on the current device (looked up once per device;
-// the host-side name of the array is only a stand-in and must not reach a kernel).
-int noalloc_scratch(int32_t** out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return BLEND_ECUDA;
-    if (dev < 0 || dev >= NOALLOC_MAX_DEVICES) return BLEND_EUNSUPPORTED;
-    std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_ptr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_rank) != cudaSuccess || p == nullptr) return BLEND_ECUDA;
-        g_noalloc_ptr[dev] = static_cast<int32_t*>(p);
-    }
-    *out = g_noalloc_ptr[dev];
+// Device addresses of the scratch arrays on the current device, looked up on every call
+// with that device current (a host-side query that allocates nothing), so no address
+// outlives the module instance it came from (after cudaDeviceReset the module may load
+// at another address).  The host-side names of the arrays are only stand-ins and must
+// not reach a kernel.
+int noalloc_scratch(NoallocScratch* out) {
+    void* pr = nullptr;
+    void* ps = nullptr;
+    if (cudaGetSymbolAddress(&pr, g_noalloc_rank) != cudaSuccess || pr == nullptr) return BLEND_ECUDA;
+    if (cudaGetSymbolAddress(&ps, g_noalloc_sorted) != cudaSuccess || ps == nullptr) return BLEND_ECUDA;
+    out->rank = static_cast<int32_t*>(pr);
+    out->sorted = static_cast<unsigned long long*>(ps);
     return BLEND_OK;
 }
 }  // namespace
@@ -245,8 +321,8 @@ extern "C" int topk_select_dilate_noalloc(const float* scores, int32_t n, int32_
         return report_error(BLEND_EINVAL, "topk_select_dilate_noalloc: bad budget/window/tau");
     if (budget_mode != BLEND_BUDGET_FINAL && budget_mode != BLEND_BUDGET_CANDIDATE)
         return report_error(BLEND_EINVAL, "topk_select_dilate_noalloc: bad budget_mode");
-    int32_t* rank = nullptr;
-    int rc = noalloc_scratch(&rank);
+    NoallocScratch scr;
+    int rc = noalloc_scratch(&scr);
     if (rc != BLEND_OK) {
         cudaGetLastError();
         return report_error(rc, "topk_select_dilate_noalloc: cannot get the device address of the fixed scratch");
@@ -259,7 +335,7 @@ extern "C" int topk_select_dilate_noalloc(const float* scores, int32_t n, int32_
     sb.budget_mode = budget_mode;
     sb.j[0] = SelectJob{scores, allowed, idx_out, n_out, n, base, budget, 0, 0};
     // every rank entry the call reads is written by the call first: nothing to clear
-    launch_select(sb, rank, n, (cudaStream_t)stream);
+    launch_select(sb, scr.rank, scr.sorted, n, (cudaStream_t)stream);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return report_error(BLEND_ECUDA, cudaGetErrorString(e));
     return BLEND_OK;
