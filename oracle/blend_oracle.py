@@ -58,6 +58,7 @@ Parity pins (what each function is checked against, in tests/test_oracle_*.py):
 from __future__ import annotations
 
 import math
+from concurrent.futures import ThreadPoolExecutor
 from typing import Optional
 
 import numpy as np
@@ -168,20 +169,34 @@ def attention(q: np.ndarray, qpos: np.ndarray, K: np.ndarray, V: np.ndarray,
     scale = 1.0 / math.sqrt(d)
     qpos = np.asarray(qpos, dtype=np.int64)
     block = 256
-    for g in range(hkv):
+    Ks = [np.ascontiguousarray(K[:, g, :], dtype=F64) for g in range(hkv)]   # [N, d] per kv head
+    Vs = [np.ascontiguousarray(V[:, g, :], dtype=F64) for g in range(hkv)]
+
+    def piece(g, i0):
         heads = slice(g * group, (g + 1) * group)               # query heads of kv head g
-        Kg = np.ascontiguousarray(K[:, g, :], dtype=F64)       # [N, d]
-        Vg = np.ascontiguousarray(V[:, g, :], dtype=F64)
-        for i0 in range(0, n, block):
-            i1 = min(n, i0 + block)
-            top = int(qpos[i0:i1].max()) + 1                   # keys any row of the block sees
-            qb = np.asarray(q[i0:i1, heads, :], dtype=F64)     # [b, group, d]
-            s = (qb @ Kg[:top].T) * scale                      # [b, group, top]
-            past = np.arange(top)[None, :] > qpos[i0:i1, None]  # [b, top]: key after the row
-            s[np.broadcast_to(past[:, None, :], s.shape)] = -np.inf
-            s = s - np.max(s, axis=2, keepdims=True)
-            e = np.exp(s)
-            out[i0:i1, heads, :] = (_rnd(e, operand_round) @ Vg[:top]) / np.sum(e, axis=2, keepdims=True)
+        i1 = min(n, i0 + block)
+        b = i1 - i0
+        top = int(qpos[i0:i1].max()) + 1                       # keys any row of the block sees
+        qb = np.asarray(q[i0:i1, heads, :], dtype=F64).reshape(b * group, d)
+        s = ((qb @ Ks[g][:top].T) * scale).reshape(b, group, top)
+        # keys after the row's own position: -inf
+        for r in range(b):
+            s[r, :, int(qpos[i0 + r]) + 1:] = -np.inf
+        s -= np.max(s, axis=2, keepdims=True)
+        e = np.exp(s, out=s)
+        pv = (_rnd(e, operand_round).reshape(b * group, top) @ Vs[g][:top]).reshape(b, group, d)
+        out[i0:i1, heads, :] = pv / np.sum(e, axis=2, keepdims=True)
+
+    # the (kv head, row block) pieces are independent and write disjoint parts of out; large
+    # ones run four at a time (numpy releases the interpreter lock on large arrays), which
+    # changes nothing in the arithmetic of any piece
+    tasks = [(g, i0) for g in range(hkv) for i0 in range(0, n, block)]
+    if len(tasks) > 1 and n * K.shape[0] >= (1 << 22):
+        with ThreadPoolExecutor(max_workers=4) as ex:
+            list(ex.map(lambda t: piece(*t), tasks))
+    else:
+        for t in tasks:
+            piece(*t)
     return out
 
 

@@ -407,6 +407,20 @@ void launch_gather(const void* src, long long row_bytes, long long src_rows, con
     note_launch(1);
 }
 
+// Two consecutive elements of T (8 bytes of fp32 or 4 of bf16) as floats, and back.
+template <typename T> __device__ __forceinline__ float2 load2(const T* p);
+template <> __device__ __forceinline__ float2 load2<float>(const float* p) { return *reinterpret_cast<const float2*>(p); }
+template <> __device__ __forceinline__ float2 load2<bf16>(const bf16* p) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+}
+template <typename T> __device__ __forceinline__ void store2(T* p, float a, float b);
+template <> __device__ __forceinline__ void store2<float>(float* p, float a, float b) {
+    *reinterpret_cast<float2*>(p) = make_float2(a, b);
+}
+template <> __device__ __forceinline__ void store2<bf16>(bf16* p, float a, float b) {
+    *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(a, b);
+}
+
 // ---------------------------------------------------------------- fused RoPE + deviation + scatter
 // For each recomputed row (one CTA per row): rotate q and k at the row's blended
 // position, store q for attention, compare the fresh k, v (fp32, before rounding) with
@@ -427,40 +441,48 @@ __global__ void __launch_bounds__(256)
     const int width = (hq + 2 * hkv) * d;
     const float* src = qkv + (long long)row * width;
     const float2* cs = tab + (long long)pos * half;
-    // q layout: per kv head g a slab of [m_cap rows][group][d] (pair = row * group + j)
+    // q layout: per kv head g a slab of [m_cap rows][group][d] (pair = row * group + j).
+    // Each thread takes two neighbouring rotate-half pairs (i, i+1) and (i+d/2, i+1+d/2):
+    // 8-byte loads of the fp32 projection, one 16-byte (cos, sin) load, paired stores.
     const int group = hq / hkv;
-    for (int j = threadIdx.x; j < hq * half; j += blockDim.x) {
-        int h = j / half, i = j % half;
-        float x1 = src[h * d + i], x2 = src[h * d + i + half];
-        float2 t = cs[i];
+    const int hp = half / 2;  // pairs of pairs per head
+    for (int j = threadIdx.x; j < hq * hp; j += blockDim.x) {
+        const int h = j / hp, i = 2 * (j % hp);
+        const float2 a = *reinterpret_cast<const float2*>(src + h * d + i);
+        const float2 b = *reinterpret_cast<const float2*>(src + h * d + i + half);
+        const float4 t = *reinterpret_cast<const float4*>(cs + i);  // (cos, sin) of i and i+1
         T* qo = q_out + (((long long)(h / group) * m_cap + row) * group + (h % group)) * d;
-        qo[i] = from_f<T>(x1 * t.x - x2 * t.y);
-        qo[i + half] = from_f<T>(x2 * t.x + x1 * t.y);
+        store2<T>(qo + i, a.x * t.x - b.x * t.y, a.y * t.z - b.y * t.w);
+        store2<T>(qo + i + half, b.x * t.x + a.x * t.y, b.y * t.z + a.y * t.w);
     }
     float acc = 0.f;
     const float* ks = src + hq * d;
     T* kr = kc + tok * hkv * d;
-    for (int j = threadIdx.x; j < hkv * half; j += blockDim.x) {
-        int g = j / half, i = j % half;
-        float x1 = ks[g * d + i], x2 = ks[g * d + i + half];
-        float2 t = cs[i];
-        float r1 = x1 * t.x - x2 * t.y, r2 = x2 * t.x + x1 * t.y;
+    for (int j = threadIdx.x; j < hkv * hp; j += blockDim.x) {
+        const int g = j / hp, i = 2 * (j % hp);
+        const float2 a = *reinterpret_cast<const float2*>(ks + g * d + i);
+        const float2 b = *reinterpret_cast<const float2*>(ks + g * d + i + half);
+        const float4 t = *reinterpret_cast<const float4*>(cs + i);
+        const float r1a = a.x * t.x - b.x * t.y, r1b = a.y * t.z - b.y * t.w;
+        const float r2a = b.x * t.x + a.x * t.y, r2b = b.y * t.z + a.y * t.w;
         if (dev_out && dev_mode == BLEND_DEV_KV) {
-            float o1 = to_f<T>(kr[g * d + i]) - r1, o2 = to_f<T>(kr[g * d + i + half]) - r2;
-            acc += o1 * o1 + o2 * o2;
+            const float2 c1 = load2<T>(kr + g * d + i), c2 = load2<T>(kr + g * d + i + half);
+            const float o1 = c1.x - r1a, o2 = c1.y - r1b, o3 = c2.x - r2a, o4 = c2.y - r2b;
+            acc += o1 * o1 + o2 * o2 + o3 * o3 + o4 * o4;
         }
-        kr[g * d + i] = from_f<T>(r1);
-        kr[g * d + i + half] = from_f<T>(r2);
+        store2<T>(kr + g * d + i, r1a, r1b);
+        store2<T>(kr + g * d + i + half, r2a, r2b);
     }
     const float* vs = src + (hq + hkv) * d;
     T* vr = vc + tok * hkv * d;
-    for (int j = threadIdx.x; j < hkv * d; j += blockDim.x) {
-        float v = vs[j];
+    for (int j = threadIdx.x; j < hkv * d / 2; j += blockDim.x) {
+        const float2 v = *reinterpret_cast<const float2*>(vs + 2 * j);
         if (dev_out) {
-            float o = to_f<T>(vr[j]) - v;
-            acc += o * o;
+            const float2 c = load2<T>(vr + 2 * j);
+            const float o1 = c.x - v.x, o2 = c.y - v.y;
+            acc += o1 * o1 + o2 * o2;
         }
-        vr[j] = from_f<T>(v);
+        store2<T>(vr + 2 * j, v.x, v.y);
     }
     if (dev_out) {
         float dv = block_sum(acc, red);

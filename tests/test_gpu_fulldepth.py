@@ -1,6 +1,8 @@
-"""Parity at full depth: every layer of the Llama-3-8B-shaped HKVD request (32 layers) and
-of the Mistral-7B-shaped batch (32 layers), through blend_prefill in the configuration the
-benchmark times, against the CPU oracle, with the error reported per layer.
+"""Parity at full depth: every layer of the Llama-3-8B-shaped HKVD request (32 layers), of
+the Mistral-7B-shaped batch (32 layers), of the 14B-shaped sweep's 4K context at 10 % (48
+layers) and, behind BLEND_FULL_DEPTH_48, of the 14B-shaped 16K request (48 layers), through
+blend_prefill in the configuration the benchmark times, against the CPU oracle, with the
+error reported per layer.
 
 What is checked, and against what:
   * integer outputs exactly: the HKVD stage sets are the oracle's top-k and selection
@@ -333,5 +335,49 @@ def test_qwen14b_16k_48_layers_set_and_floor(qwen14b):
                                        "(the oracle's operand_round run) exceeds it at 48 layers")
 def test_qwen14b_16k_48_layers_north_star_bar(qwen14b):
     gpu = qwen14b["gpu"]
+    for k in ("hidden", "K", "V"):
+        assert gpu[k][0] <= TOL and gpu[k][1] <= TOL, (k, gpu[k])
+
+
+# ---------------------------------------------------------------- the sweep's 4K context at 10 %, all 48 layers
+
+@pytest.fixture(scope="module")
+def sweep4k():
+    wl = synth.sweep_workload(7, 1000)
+    rq = Request(wl)
+    req = rq.reqs[0]
+    s = ext_scores(rq.n_c, 9)
+    h = rq.handle(rq.n_c + rq.Q)
+    out = rq.outputs()
+    b.blend_prefill(h, [b.RequestRef(req.chunk_ids, req.query.to(dev()), mode="ext", rho_bp=wl.rho_bp,
+                                     window=wl.window, tau=wl.tau, budget_mode=wl.budget_mode,
+                                     scores=torch.from_numpy(s).to(dev()))], rq.pool, out)
+    b.blend_device_status(h)
+    torch.cuda.synchronize()
+    kw = dict(mode="ext", rho_bp=wl.rho_bp, window=wl.window, tau=wl.tau, budget_mode=wl.budget_mode,
+              scores=s.astype(np.float64))
+    ref = rq.oracle(0, **kw)
+    floor = rq.oracle(0, operand_round="bf16", **kw)
+    res = dict(rq=rq, out=out, ref=ref, gpu=whole_errors(out["k"], out["v"], out["hidden"], ref),
+               floor=whole_errors(floor["K"], floor["V"], floor["hidden"], ref))
+    report("14B 4K 10 % 48 layers", res["gpu"], res["floor"])
+    return res
+
+
+def test_sweep_4k_10pct_48_layers_set_and_floor(sweep4k):
+    """The context x ratio sweep's 4K context at 10 % on the 14B shape, every layer: the
+    set exactly, values within FLOOR_RATIO of the bf16-operand floor."""
+    out, ref = sweep4k["out"], sweep4k["ref"]
+    ns = int(out["n_sel"][0].item())
+    assert out["sel"][:ns].cpu().numpy().tolist() == ref["stages"][0][1].tolist()
+    gpu, floor = sweep4k["gpu"], sweep4k["floor"]
+    for k in ("hidden", "K", "V"):
+        assert gpu[k][0] <= FLOOR_RATIO * floor[k][0], (k, gpu[k], floor[k])
+
+
+@pytest.mark.xfail(strict=True, reason="fails north star's 2e-2 at full depth: bf16 operand rounding alone "
+                                       "(the oracle's operand_round run) exceeds it at 48 layers")
+def test_sweep_4k_10pct_48_layers_north_star_bar(sweep4k):
+    gpu = sweep4k["gpu"]
     for k in ("hidden", "K", "V"):
         assert gpu[k][0] <= TOL and gpu[k][1] <= TOL, (k, gpu[k])
