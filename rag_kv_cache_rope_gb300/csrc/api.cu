@@ -779,6 +779,7 @@ namespace {
 
 struct ReqInfo {
     int P, n_c, Q, N, B, k1, max_rows, cap;
+    int stage_rows[3];  // most chunk rows each stage can hold (stage 0 = max_rows - Q)
 };
 
 int validate_batch(blend_handle* h, int n_req, const blend_request* reqs, const blend_pool* pool,
@@ -878,6 +879,9 @@ int validate_batch(blend_handle* h, int n_req, const blend_request* reqs, const 
             if (q.r1_bp < q.rho_bp || q.r1_bp > 10000) return fail(h, BLEND_EINVAL, "request %d: r1_bp must be in rho_bp..10000", r);
             ri.k1 = ceil_bp(q.r1_bp, ri.n_c);
             chunk_rows = ri.n_c;
+            // C1 holds exactly k1 rows; S lies within C1 and, with the final budget, holds at most B
+            ri.stage_rows[1] = ri.k1;
+            ri.stage_rows[2] = q.budget_mode == BLEND_BUDGET_FINAL && ri.B < ri.k1 ? ri.B : ri.k1;
         } else if (mode == BLEND_SEL_FORCED) {
             if (q.n_stages < 1 || q.n_stages > 3 || q.stage_layer[0] != 0)
                 return fail(h, BLEND_EINVAL, "request %d: FORCED needs 1..3 stages, the first at layer 0", r);
@@ -890,6 +894,7 @@ int validate_batch(blend_handle* h, int n_req, const blend_request* reqs, const 
                 if (q.n_stages != reqs[0].n_stages) return fail(h, BLEND_EINVAL, "requests must have the same number of stages");
             }
             chunk_rows = q.stage_n[0];
+            for (int s = 1; s < q.n_stages; ++s) ri.stage_rows[s] = q.stage_n[s];
         } else if (mode == BLEND_SEL_EPIC) {
             if (q.epic_m < 0) return fail(h, BLEND_EINVAL, "request %d: epic_m must be >= 0", r);
             for (int j = 0; j < q.n_chunks; ++j) {
@@ -900,6 +905,8 @@ int validate_batch(blend_handle* h, int n_req, const blend_request* reqs, const 
             chunk_rows = ri.P + ri.n_c;
         }
         ri.max_rows = chunk_rows + ri.Q;
+        ri.stage_rows[0] = chunk_rows;
+        if (mode != BLEND_SEL_HKVD && mode != BLEND_SEL_FORCED) ri.stage_rows[1] = ri.stage_rows[2] = chunk_rows;
         tot_tok += ri.N;
         tot_rows += ri.max_rows;
         info->push_back(ri);
@@ -1026,12 +1033,14 @@ extern "C" int blend_prefill(blend_handle* h, int32_t n_req, const blend_request
     memset(&bd, 0, sizeof bd);
     bd.n_req = n_req;
     int tok = 0, nc = 0, qo = 0, M_max = 0;
+    int M_stage[3] = {0, 0, 0};  // most rows of each stage over the batch (launch sizes)
     for (int r = 0; r < n_req; ++r) {
         bd.r[r] = ReqDesc{tok, info[r].P, info[r].n_c, info[r].Q, nc, qo};
         tok += info[r].N;
         nc += info[r].n_c;
         qo += info[r].Q;
         M_max += info[r].max_rows;
+        for (int st = 0; st < 3; ++st) M_stage[st] += info[r].stage_rows[st] + info[r].Q;
     }
     const int nc_total = nc;
     const size_t layer_elems = (size_t)tok * c.n_kv_heads * c.head_dim;
@@ -1184,6 +1193,7 @@ extern "C" int blend_prefill(blend_handle* h, int32_t n_req, const blend_request
     h->xn_scaled = false;
     float* x = h->x;
     float* x_alt = h->x2;
+    int M_cur = M_stage[0];  // bound of the current stage's rows (sizes the launches)
     for (int l = 0; l < c.n_layers; ++l) {
         char layer_name[24];
         snprintf(layer_name, sizeof layer_name, "layer %d", l);
@@ -1207,7 +1217,7 @@ extern "C" int blend_prefill(blend_handle* h, int32_t n_req, const blend_request
             }
         }
         float* dev = (checks && (l == 1 || l == 2)) ? h->dev[l - 1] : nullptr;
-        layer_kv(h, l, x, p, p.row_req, M_max, bd, kc, vc, dev, reqs[0].dev_mode, 0, s);
+        layer_kv(h, l, x, p, p.row_req, M_cur, bd, kc, vc, dev, reqs[0].dev_mode, 0, s);
         int new_stage = -1;
         for (int sidx = 1; sidx < n_stage; ++sidx)
             if (stage_layer[sidx] == l) new_stage = sidx;
@@ -1254,14 +1264,17 @@ extern "C" int blend_prefill(blend_handle* h, int32_t n_req, const blend_request
             Plan& np = h->plan[1 - cur];
             launch_plan(bd, st, np.row_pos, np.row_tok, np.row_req, h->row_src, h->pos2row, np.M,
                         np.req_row_end, h->plan[cur].row_tok, h->plan[cur].M, h->err, s);
-            launch_gather(x, (long long)c.hidden * 4, h->lim.max_rows, h->row_src, np.M, M_max, x_alt, h->err, s);
+            // the new set is at most as large as its stage's bound (the focus filter only
+            // removes rows of the current stage)
+            if (!focus) M_cur = M_stage[new_stage];
+            launch_gather(x, (long long)c.hidden * 4, h->lim.max_rows, h->row_src, np.M, M_cur, x_alt, h->err, s);
             {
                 // q is stored per kv head: compact each head's slab of [rows][group][d]
                 const int group = c.n_q_heads / c.n_kv_heads;
                 const size_t slab = (size_t)h->lim.max_rows * group * c.head_dim * es;
                 for (int g = 0; g < c.n_kv_heads; ++g)
                     launch_gather((const char*)h->q + g * slab, (long long)group * c.head_dim * es,
-                                  h->lim.max_rows, h->row_src, np.M, M_max, (char*)h->q2 + g * slab, h->err, s);
+                                  h->lim.max_rows, h->row_src, np.M, M_cur, (char*)h->q2 + g * slab, h->err, s);
             }
             float* tx = x;
             x = x_alt;
@@ -1274,7 +1287,7 @@ extern "C" int blend_prefill(blend_handle* h, int32_t n_req, const blend_request
         if (l == c.n_layers - 1 && out->q_last)
             launch_gather_qlast(c.dtype, h->q, h->lim.max_rows, c.n_q_heads / c.n_kv_heads, c.n_kv_heads,
                                 c.head_dim, bd, h->plan[cur].req_row_end, out->q_last, qo, s);
-        layer_rest(h, l, x, h->plan[cur], n_req, M_max, kc, vc, tok, s, true);
+        layer_rest(h, l, x, h->plan[cur], n_req, M_cur, kc, vc, tok, s, true);
     }
     // ---- 4. final norm of the query rows
     ProfScope ps_final(h, PROF_FINAL, s);

@@ -199,22 +199,53 @@ __device__ __forceinline__ bool mbar_wait_t(uint64_t* b, uint32_t parity, volati
     return false;
 }
 
-// Work unit u -> tile, its K-block range and, for a unit of a split tile, which K half
+// Work unit u -> tile, its K-block range and, for a unit of a split tile, which K part
 // (-1: whole tile) and the split tile's index.
 struct Unit {
     int t, half, sidx, k0, k1;
 };
+// Splitting (allowed for the non-QKV epilogues with 256-wide tiles and a workspace) is
+// decided on the device from the device row count, identically in the GEMM and in
+// k_split_combine:
+//   n_total >= grid: the tiles of a last wave that is at most half full run as two K halves;
+//   n_total <  grid: every tile may run as S = 2..4 K parts, in ceil(S n_total / grid) rounds
+//                    of 1/S of a tile; S is the one with the fewest tile-times (ties: fewer
+//                    parts), used only if that beats one whole round, and its partials fit
+//                    the workspace (ws_blocks TM-row blocks).
+// A split tile's parts are finished by k_split_combine.
 struct Sched {
     int full;   // units dealt as whole tiles
-    int split;  // split tiles (each two units), 0 when the last wave is more than half full
+    int split;  // split tiles
+    int parts;  // K parts of a split tile
     int units;
 };
-__device__ __forceinline__ Sched make_sched(int n_total, int grid, bool can_split) {
+__device__ __forceinline__ Sched make_sched(int n_total, int grid, bool can_split, int kblocks, int ws_blocks) {
     Sched sc;
-    const int rem = n_total % grid;
-    sc.split = (can_split && rem > 0 && 2 * rem <= grid) ? rem : 0;
+    sc.parts = 2;
+    sc.split = 0;
+    if (can_split && kblocks >= 2 && n_total > 0) {
+        if (n_total >= grid) {
+            const int rem = n_total % grid;
+            if (rem > 0 && 2 * rem <= grid) sc.split = rem;
+        } else {
+            int best_s = 1;
+            long long best_num = 1, best_den = 1;  // tile-times of the best S: num / den
+            for (int S = 2; S <= 4 && S <= kblocks && S * n_total <= ws_blocks; ++S) {
+                const long long rounds = (S * n_total + grid - 1) / grid;
+                if (rounds * best_den < best_num * S) {
+                    best_num = rounds;
+                    best_den = S;
+                    best_s = S;
+                }
+            }
+            if (best_s > 1) {
+                sc.parts = best_s;
+                sc.split = n_total;
+            }
+        }
+    }
     sc.full = n_total - sc.split;
-    sc.units = sc.full + 2 * sc.split;
+    sc.units = sc.full + sc.parts * sc.split;
     return sc;
 }
 __device__ __forceinline__ Unit unit_of(int u, const Sched& sc, int kblocks) {
@@ -227,11 +258,11 @@ __device__ __forceinline__ Unit unit_of(int u, const Sched& sc, int kblocks) {
         r.k1 = kblocks;
     } else {
         const int v = u - sc.full;
-        r.sidx = v >> 1;
+        r.sidx = v / sc.parts;
         r.t = sc.full + r.sidx;
-        r.half = v & 1;
-        r.k0 = r.half ? kblocks / 2 : 0;
-        r.k1 = r.half ? kblocks : kblocks / 2;
+        r.half = v % sc.parts;
+        r.k0 = r.half * kblocks / sc.parts;
+        r.k1 = (r.half + 1) * kblocks / sc.parts;
     }
     return r;
 }
@@ -438,7 +469,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int n_total = m_tiles * n_tiles;
     const int kblocks = K / BK;
     constexpr int HALF = BN / 2;
-    const Sched sc = make_sched(n_total, n_grp, EPI != EPI_QKV_ROPE && BN == 256 && kblocks >= 2 && can_split != 0);
+    const Sched sc = make_sched(n_total, n_grp, EPI != EPI_QKV_ROPE && BN == 256 && can_split != 0, kblocks,
+                                (int)(GEMM_SPLIT_WS_FLOATS / 256 / TC::TM));
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -651,9 +683,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                 }
             } else if (un.half >= 0) {
-                // a K half of a split tile: its raw partial goes to the workspace rows of
-                // (split tile, half); k_split_combine finishes the tile
-                const int ws_row0 = (un.sidx * 2 + un.half) * TC::TM + rank * BM + sp * 32;
+                // a K part of a split tile: its raw partial goes to the workspace rows of
+                // (split tile, part); k_split_combine finishes the tile
+                const int ws_row0 = (un.sidx * sc.parts + un.half) * TC::TM + rank * BM + sp * 32;
 #pragma unroll 1
                 for (int c = 0; c < BN; c += 32) {
                     uint32_t r[32];
@@ -761,21 +793,31 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 }
 
-// Finishes the split tiles of a k_gemm_tc launch (BN = 256): the two K-half partials of
-// every row of a split tile are added in a fixed order (half 0 + half 1), scaled by the
-// row's folded-norm factor, and the tile's epilogue runs on the sum: fp32 store, residual
+// Finishes the split tiles of a k_gemm_tc launch (BN = 256): the K-part partials of
+// every row of a split tile are added in a fixed order (part 0 + part 1 + ...), scaled by
+// the row's folded-norm factor, and the tile's epilogue runs on the sum: fp32 store, residual
 // add (with bf16(x * g) and the two per-128-column sums of squares of a norm producer) or
 // SwiGLU.  One warp per row, eight consecutive columns per lane.  The split set is the
 // kernel's own (same schedule from the device row count).
+template <int EPI, int TM>
+__device__ __forceinline__ void combine_tile(const float* __restrict__ ws, int N, int M, int m_tiles, const Sched& sc,
+                                             int sidx, void* __restrict__ Cv, int ldc, const NormEpi& ne);
+
 template <int EPI, int TM>
 __global__ void __launch_bounds__(128)
     k_split_combine(const float* __restrict__ ws, int K, int N, const int32_t* __restrict__ M_dev, int n_grp,
                     void* __restrict__ Cv, int ldc, const __grid_constant__ NormEpi ne) {
     const int M = *M_dev;
     const int m_tiles = (M + TM - 1) / TM, n_tiles = (N + 255) / 256;
-    const Sched sc = make_sched(m_tiles * n_tiles, n_grp, K / BK >= 2);
-    const int sidx = blockIdx.x;
-    if (sidx >= sc.split) return;
+    const Sched sc = make_sched(m_tiles * n_tiles, n_grp, true, K / BK, (int)(GEMM_SPLIT_WS_FLOATS / 256 / TM));
+    // split tiles blockIdx.x, blockIdx.x + gridDim.x, ...
+    for (int sidx = blockIdx.x; sidx < sc.split; sidx += gridDim.x)
+        combine_tile<EPI, TM>(ws, N, M, m_tiles, sc, sidx, Cv, ldc, ne);
+}
+
+template <int EPI, int TM>
+__device__ __forceinline__ void combine_tile(const float* __restrict__ ws, int N, int M, int m_tiles, const Sched& sc,
+                                             int sidx, void* __restrict__ Cv, int ldc, const NormEpi& ne) {
     const int t = sc.full + sidx, mt = t % m_tiles, nt = t / m_tiles;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int r_t = blockIdx.y * 4 + warp;  // row within the tile
@@ -786,16 +828,28 @@ __global__ void __launch_bounds__(128)
     const bool live = col < N;  // N % 32 == 0: a lane's eight columns are all in or all out
     float v[8];
     if (live) {
-        const float4* p0 = reinterpret_cast<const float4*>(ws + ((long long)(sidx * 2) * TM + r_t) * 256 + c0);
-        const float4* p1 = reinterpret_cast<const float4*>(ws + ((long long)(sidx * 2 + 1) * TM + r_t) * 256 + c0);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const float4 a = __ldcg(p0 + h), b = __ldcg(p1 + h);
-            v[4 * h] = (a.x + b.x) * rs;
-            v[4 * h + 1] = (a.y + b.y) * rs;
-            v[4 * h + 2] = (a.z + b.z) * rs;
-            v[4 * h + 3] = (a.w + b.w) * rs;
+        const float4* p0 = reinterpret_cast<const float4*>(ws + ((long long)(sidx * sc.parts) * TM + r_t) * 256 + c0);
+        float4 a0 = __ldcg(p0), a1 = __ldcg(p0 + 1);
+        for (int q = 1; q < sc.parts; ++q) {
+            const float4* pq = p0 + (long long)q * TM * 64;  // next part: TM rows of 256 floats on
+            const float4 b0 = __ldcg(pq), b1 = __ldcg(pq + 1);
+            a0.x += b0.x;
+            a0.y += b0.y;
+            a0.z += b0.z;
+            a0.w += b0.w;
+            a1.x += b1.x;
+            a1.y += b1.y;
+            a1.z += b1.z;
+            a1.w += b1.w;
         }
+        v[0] = a0.x * rs;
+        v[1] = a0.y * rs;
+        v[2] = a0.z * rs;
+        v[3] = a0.w * rs;
+        v[4] = a1.x * rs;
+        v[5] = a1.y * rs;
+        v[6] = a1.z * rs;
+        v[7] = a1.w * rs;
     } else {
 #pragma unroll
         for (int e = 0; e < 8; ++e) v[e] = 0.f;
@@ -1000,8 +1054,9 @@ void launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, int K, int N, const
     const int tiles = ((M_max + TileCfg<BN, PAIR>::TM - 1) / TileCfg<BN, PAIR>::TM) * ((N + BN - 1) / BN);
     int groups = tiles < slots ? tiles : slots;
     const bool split = split_ws != nullptr && epi != EPI_QKV_ROPE && BN == 256 && K / BK >= 2;
-    // fewer tiles than half the slots: every tile runs as two K halves
-    if (split && 2 * tiles <= slots) groups = 2 * tiles;
+    // with splitting allowed the device may run each of few tiles as up to four K parts
+    // (make_sched): give it up to four units per tile of the host's bound
+    if (split) groups = 4 * tiles < slots ? 4 * tiles : slots;
     const int cs = split ? 1 : 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(PAIR ? 2 * groups : groups);
@@ -1043,6 +1098,25 @@ void launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, int K, int N, const
     }
 }
 
+// Tile-times of T tiles on `slots` units under make_sched's rules (workspace limit aside):
+// whole waves, a last wave at most half full as K halves, or fewer tiles than slots as up
+// to four K parts.
+double est_tile_times(int T, int slots, bool can_split, int kblocks) {
+    if (T <= 0 || slots <= 0) return 0.0;
+    if (T >= slots) {
+        const int full = T / slots, rem = T % slots;
+        if (rem == 0) return full;
+        return full + ((can_split && kblocks >= 2 && 2 * rem <= slots) ? 0.5 : 1.0);
+    }
+    double best = 1.0;
+    if (can_split)
+        for (int S = 2; S <= 4 && S <= kblocks; ++S) {
+            const double t = (double)((S * T + slots - 1) / slots) / S;
+            if (t < best) best = t;
+        }
+    return best;
+}
+
 int launch_gemm_tc(const void* A, int K, int M_cap, const void* B, int N, const int32_t* M_dev, int M_max,
                    int epi, void* C, int ldc, int32_t* err, cudaStream_t s, const QkvEpi* qkv, float* split_ws,
                    const NormEpi* norm) {
@@ -1056,9 +1130,20 @@ int launch_gemm_tc(const void* A, int K, int M_cap, const void* B, int N, const 
     if (ne.x_out && (epi != EPI_ADD_F32 || ne.ssq_out == nullptr || ne.g == nullptr || ne.ldx % 8 != 0 ||
                      ne.ssq_stride != gemm_tc_norm_parts(N)))
         return BLEND_EUNSUPPORTED;
-    // 256-wide tiles over more than one 128-row block run on CTA pairs (256x256 tiles);
-    // each CTA of a pair stages half of a tile's weight rows
-    const bool pair = bn == 256 && M_max > BM && g_num_sms >= 2;
+    // 256-wide tiles over more than one 128-row block run on CTA pairs (256x256 tiles; each
+    // CTA of a pair stages half of a tile's weight rows, a third less operand traffic per
+    // SM), unless single-CTA 128-row tiles take clearly fewer tile-times: few rows, where
+    // 256-row tiles pad more and the waves fill worse (both sides with the device's split
+    // rules).  A single tile-time measured ~15 % longer than a pair's at ~500 rows (8B
+    // gate/up: 4.0 single waves took longer than 4.5 pair waves), hence the margin.
+    bool pair = bn == 256 && M_max > BM && g_num_sms >= 2;
+    if (pair) {
+        const bool can_split = split_ws != nullptr && epi != EPI_QKV_ROPE;
+        const int nt = (N + bn - 1) / bn, kb = K / BK;
+        const double t_pair = est_tile_times((M_max + 2 * BM - 1) / (2 * BM) * nt, g_num_sms / 2, can_split, kb);
+        const double t_one = est_tile_times((M_max + BM - 1) / BM * nt, g_num_sms, can_split, kb);
+        if (t_one * 1.15 < t_pair) pair = false;
+    }
     const uint32_t brows = pair ? (uint32_t)bn / 2 : (uint32_t)bn;
     CUtensorMap ma, mb;
     if (!encode_2d(&ma, A, (uint64_t)K, (uint64_t)M_cap, BK, BM) ||

@@ -10,12 +10,14 @@ int tc_available();
 // Shapes the tensor-core kernel takes: K % 64 == 0, N >= 128 and N % 32 == 0 (N % 256 == 0
 // for EPI_QKV_ROPE), ldc % 8 == 0, and an A buffer of at least 128 rows (M_cap).
 bool tc_gemm_supported(int K, int N, int epi, int ldc, int M_cap);
-// Split-tile workspace of launch_gemm_tc (fp32): two K-half partials of up to 80 split
-// tiles of 128 x 256 (CTA-pair tiles of 256 rows count twice).
-constexpr size_t GEMM_SPLIT_WS_FLOATS = (size_t)160 * 128 * 256;
+// Split-tile workspace of launch_gemm_tc (fp32): the K-part partials of the split tiles,
+// 640 blocks of 128 x 256 (a CTA-pair tile of 256 rows takes two per part), e.g. four
+// parts of 76 CTA-pair tiles.
+constexpr size_t GEMM_SPLIT_WS_FLOATS = (size_t)640 * 128 * 256;
 // A: [M_cap][K] bf16 buffer whose first *M_dev rows are used; B: [N][K] bf16.  With
 // split_ws (GEMM_SPLIT_WS_FLOATS, not for EPI_QKV_ROPE) a last wave that is at most half
-// full runs as K halves, finished by a second small kernel.  A folded-norm producer (norm->x_out) writes gemm_tc_norm_parts(N) partial sums
+// full runs as K halves, and a launch with fewer tiles than slots may run every tile as
+// 2-4 K parts; a second small kernel finishes the split tiles.  A folded-norm producer (norm->x_out) writes gemm_tc_norm_parts(N) partial sums
 // of squares per row (norm->ssq_stride must equal it).  Returns BLEND_OK or
 // BLEND_EUNSUPPORTED (operands not describable by a tensor map).
 int launch_gemm_tc(const void* A, int K, int M_cap, const void* B, int N, const int32_t* M_dev, int M_max,
