@@ -58,14 +58,14 @@ except OSError:
 # that request and while the kernel's source is unchanged.
 TRAFFIC_WORKLOAD = "qwen14b-16k-ext20"
 TRAFFIC = {
-    "gemm_qkv": {"bytes": 128.005888e6 + 31.630080e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
-                 "sha256_16": "6655236c82fc5564", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
-    "gemm_o": {"bytes": 201.848576e6 + 63.539712e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
-               "sha256_16": "6655236c82fc5564", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
-    "gemm_gate_up": {"bytes": 376.398848e6 + 86.185472e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
-                     "sha256_16": "6655236c82fc5564", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
-    "gemm_down": {"bytes": 588.014336e6 + 91.328256e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
-                  "sha256_16": "6655236c82fc5564", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
+    "gemm_qkv": {"bytes": 135.681792e6 + 30.760448e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
+                 "sha256_16": "d4fd9b3fc329cbbd", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
+    "gemm_o": {"bytes": 200.751616e6 + 63.799296e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
+               "sha256_16": "d4fd9b3fc329cbbd", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
+    "gemm_gate_up": {"bytes": 386.310144e6 + 86.436608e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
+                     "sha256_16": "d4fd9b3fc329cbbd", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
+    "gemm_down": {"bytes": 591.331072e6 + 61.410816e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
+                  "sha256_16": "d4fd9b3fc329cbbd", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
     "attention": {"bytes": 143.852544e6 + 13.177088e6, "source": "rag_kv_cache_rope_gb300/csrc/attn_tc.cu",
                   "sha256_16": "d6e3a54a7cce8fa0", "profile": "profiles/attn_tc_qwen14b_16k_layer.md"},
 }
