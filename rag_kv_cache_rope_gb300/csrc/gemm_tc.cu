@@ -685,13 +685,17 @@ __global__ void __launch_bounds__(THREADS, 1)
             } else if (un.half >= 0) {
                 // a K part of a split tile: its raw partial goes to the workspace rows of
                 // (split tile, part); k_split_combine finishes the tile
+                // (a warp whose 32 rows all lie past the device row count has nothing to keep:
+                // the combine reads live rows only)
                 const int ws_row0 = (un.sidx * sc.parts + un.half) * TC::TM + rank * BM + sp * 32;
+                if (row0 < M) {
 #pragma unroll 1
-                for (int c = 0; c < BN; c += 32) {
-                    uint32_t r[32];
-                    TMEM_LD32(tl + c, r);
-                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-                    part_chunk_tma(r, ws_row0, c, cb, &mapW);
+                    for (int c = 0; c < BN; c += 32) {
+                        uint32_t r[32];
+                        TMEM_LD32(tl + c, r);
+                        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                        part_chunk_tma(r, ws_row0, c, cb, &mapW);
+                    }
                 }
             } else {
                 // a whole tile; the folded-norm sums of squares are kept per BN/2 columns

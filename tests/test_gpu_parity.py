@@ -134,6 +134,35 @@ def test_topk_select_dilate_matches_oracle_exactly():
         assert got == want.tolist(), (n, w, tau, budget, mode, use_mask)
 
 
+def test_topk_select_tile_boundaries_and_ties_across_tiles():
+    """The rank kernels sort 2048-position tiles and merge them: sizes around a tile edge and
+    the 32768 maximum, with integer scores (exact ties in every tile, broken by position
+    across tiles), NaN and -0, with and without a mask, both budget modes."""
+    sh = synth.ModelShape("t", 1, 256, 4, 2, 64, 688, 64, 1e4, dtype="f32")
+    case = make_case(sh, 4, [8], pool="random")
+    r = GpuRunner(case, 64, 64, 32768)
+    rng = np.random.default_rng(7)
+    for n, w, tau, mode, use_mask in ((2047, 4, 1, "final", False), (2048, 4, 2, "candidate", True),
+                                      (2049, 3, 1, "final", True), (6144, 8, 5, "final", False),
+                                      (32768, 4, 1, "final", False), (32768, 2, 1, "candidate", True)):
+        s = rng.integers(0, 5, n).astype(np.float32)
+        s[rng.random(n) < 0.01] = np.nan
+        s[rng.random(n) < 0.05] = -0.0
+        budget = int(rng.integers(n // 10, n // 4))
+        allowed = (rng.random(n) < 0.7) if use_mask else None
+        st = torch.from_numpy(s).to(dev())
+        al = None if allowed is None else torch.from_numpy(allowed.astype(np.uint8)).to(dev())
+        idx = torch.full((n,), -7, dtype=torch.int32, device=dev())
+        cnt = torch.zeros(1, dtype=torch.int32, device=dev())
+        b.topk_select_dilate(r.h, st, n, 11, budget, w, tau, b.BUDGETS[mode], al, idx, cnt)
+        torch.cuda.synchronize()
+        got = idx[:int(cnt.item())].cpu().numpy().tolist()
+        sd = s.astype(np.float64)
+        want = (O.select(sd, budget, w, tau, "candidate", allowed=allowed, base=11) if mode == "candidate"
+                else O.select_final_bisect(sd, budget, w, tau, allowed=allowed, base=11))
+        assert got == want.tolist(), (n, w, tau, budget, mode, use_mask)
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_deviation_scatter_gather(dtype):
     sh = synth.ModelShape("t", 1, 256, 4, 2, 128, 688, 64, 1e4, dtype=dtype)

@@ -3,10 +3,10 @@
 topk_select_dilate_noalloc serves callers that cannot allocate device memory while
 they select tokens (a serving loop that reserved all HBM up front, or a hot path that
 must not call cudaMalloc/cudaFree because they may synchronise the device).  It keeps
-its rank scratch in a fixed device array instead of a handle's workspace.  Here it is
-called through the C ABI twice in a row, with different inputs, and each result must
-equal topk_select_dilate's exactly (index sets are compared bit for bit, as in the
-other selection tests).  This file is collected last on purpose.
+its scratch (ranks and sorted keys) in fixed device arrays instead of a handle's
+workspace.  Here it is called through the C ABI several times in a row, with different
+inputs, and each result must equal topk_select_dilate's exactly (index sets are compared
+bit for bit, as in the other selection tests).  This file is collected last on purpose.
 """
 import numpy as np
 import pytest
@@ -60,6 +60,10 @@ def test_noalloc_selection_equals_workspace_selection_on_two_calls():
     allowed = (torch.rand(9000, generator=g) < 0.7).to(torch.uint8)
     k2 = _run_both(r, s2, allowed, 7, 1800, 8, 5, b.BUDGET_CANDIDATE)
     assert k2 > 0
+    # call 3: the largest size the fixed scratch holds, every entry of it in use
+    s3 = torch.randn(32768, generator=g).to(dev)
+    k3 = _run_both(r, s3, None, 0, 6554, 2, 1, b.BUDGET_FINAL)
+    assert 0 < k3 <= 6554
 
 
 def test_noalloc_rejects_sizes_above_its_scratch():
