@@ -1091,7 +1091,10 @@ void launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, int K, int N, const
     if (split) {
         // the split tiles (if the device row count gives any) are finished here
         constexpr int TM = TileCfg<BN, PAIR>::TM;
-        const dim3 grid(groups / 2 > 0 ? groups / 2 : 1, TM / 4);
+        // the tail rule splits at most groups / 2 tiles; with fewer tiles than slots every
+        // tile may be split: one column of CTAs per tile, so none takes two
+        const int n_split = tiles < slots ? tiles : (groups / 2 > 0 ? groups / 2 : 1);
+        const dim3 grid(n_split, TM / 4);
         if (epi == EPI_STORE_F32)
             k_split_combine<EPI_STORE_F32, TM><<<grid, 128, 0, s>>>(split_ws, K, N, M_dev, groups, C, ldc, ne);
         else if (epi == EPI_ADD_F32)
