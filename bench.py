@@ -535,7 +535,8 @@ def run_ours(args, wl, rank, world):
         # the same input with every row recomputed, on a handle sized for all N rows
         Bn = S.batch
         hf = b.blend_init(S.cfg, S.packed, b.Limits(Bn * S.N, Bn * S.N, S.n_c, Bn))
-        full = S.make_reqs(mode="full")
+        # (a full prefill selects nothing: no grouping rule, static set or focus filter)
+        full = S.make_reqs(mode="full", group_rule="window", epic_m=0, focus_bp=0)
         b.blend_prefill(hf, full, S.pool, S.out)
         torch.cuda.synchronize()
         f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
