@@ -54,18 +54,19 @@ except OSError:
 
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
-# capture of each kernel (profiles/) on the 14B 16K 20 % request's shapes, valid only for
-# that request and while the kernel's source is unchanged.
+# capture of each kernel on the 14B 16K 20 % request's shapes (layer 1 of a 2-layer
+# truncation: the GEMMs with a one-pass metrics capture, attention with its full-set capture
+# in profiles/), valid only for that request and while the kernel's source is unchanged.
 TRAFFIC_WORKLOAD = "qwen14b-16k-ext20"
 TRAFFIC = {
-    "gemm_qkv": {"bytes": 135.681792e6 + 30.760448e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
-                 "sha256_16": "d4fd9b3fc329cbbd", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
-    "gemm_o": {"bytes": 200.751616e6 + 63.799296e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
-               "sha256_16": "d4fd9b3fc329cbbd", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
-    "gemm_gate_up": {"bytes": 386.310144e6 + 86.436608e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
-                     "sha256_16": "d4fd9b3fc329cbbd", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
-    "gemm_down": {"bytes": 591.331072e6 + 61.410816e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
-                  "sha256_16": "d4fd9b3fc329cbbd", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
+    "gemm_qkv": {"bytes": 134.033408e6 + 30.628864e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
+                 "sha256_16": "75793d0568ee62b3", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
+    "gemm_o": {"bytes": 197.148672e6 + 60.701696e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
+               "sha256_16": "75793d0568ee62b3", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
+    "gemm_gate_up": {"bytes": 379.461120e6 + 83.251456e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
+                     "sha256_16": "75793d0568ee62b3", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
+    "gemm_down": {"bytes": 590.889984e6 + 58.893056e6, "source": "rag_kv_cache_rope_gb300/csrc/gemm_tc.cu",
+                  "sha256_16": "75793d0568ee62b3", "profile": "profiles/gemm_tc_qwen14b_16k_layer.md"},
     "attention": {"bytes": 143.852544e6 + 13.177088e6, "source": "rag_kv_cache_rope_gb300/csrc/attn_tc.cu",
                   "sha256_16": "d6e3a54a7cce8fa0", "profile": "profiles/attn_tc_qwen14b_16k_layer.md"},
 }

@@ -85,7 +85,6 @@ struct blend_handle {
     int32_t* set_n[3];
     uint8_t* mask;
     float* dev[2];
-    int32_t* scratch_n;
     float2* aux_stats;   // aux_attention_scores: softmax (max, sum) per query row, head and key span
     float* ssq;          // folded RMSNorm: per-row partial sums of squares [rows][ssq_parts]
     bool xn_scaled = false;  // xn holds bf16(x * g) of the next layer's attention norm, ssq its partials
@@ -273,13 +272,12 @@ Layout make_layout(const blend_model_cfg* c, const blend_limits* l) {
     L.add(nc);                                             // 30 mask
     L.add(nc * 4);                                         // 31 dev1
     L.add(nc * 4);                                         // 32 dev2
-    L.add(16);                                             // 33 scratch count
-    L.add(M * (size_t)c->n_q_heads * tc_score_spans(l->max_tokens) * sizeof(float2));  // 34 aux score row statistics
-    L.add(c->dtype == BLEND_BF16 ? GEMM_SPLIT_WS_FLOATS * 4 : 0);  // 35 GEMM split partials
-    for (int b = 0; b < 4; ++b)                            // 36..39 host-pool staging: K, V x 2 buffers
+    L.add(M * (size_t)c->n_q_heads * tc_score_spans(l->max_tokens) * sizeof(float2));  // 33 aux score row statistics
+    L.add(c->dtype == BLEND_BF16 ? GEMM_SPLIT_WS_FLOATS * 4 : 0);  // 34 GEMM split partials
+    for (int b = 0; b < 4; ++b)                            // 35..38 host-pool staging: K, V x 2 buffers
         L.add((size_t)l->max_tokens * kvd * es);
-    L.add(M * NORM_PARTS_MAX * sizeof(float));             // 40 folded-RMSNorm partial sums of squares
-    L.add((size_t)l->max_batch * ((l->max_chunk_rows + 2047) / 2048 * 2048) * 8);  // 41 sorted rank keys
+    L.add(M * NORM_PARTS_MAX * sizeof(float));             // 39 folded-RMSNorm partial sums of squares
+    L.add((size_t)l->max_batch * ((l->max_chunk_rows + 2047) / 2048 * 2048) * 8);  // 40 sorted rank keys
     return L;
 }
 
@@ -493,7 +491,6 @@ int blend_init(const blend_model_cfg* cfg, const blend_weights* w, const blend_l
     h->mask = (uint8_t*)(b + L.off[i++]);
     h->dev[0] = (float*)(b + L.off[i++]);
     h->dev[1] = (float*)(b + L.off[i++]);
-    h->scratch_n = (int32_t*)(b + L.off[i++]);
     h->aux_stats = (float2*)(b + L.off[i++]);
     h->split_ws = cfg->dtype == BLEND_BF16 ? (float*)(b + L.off[i]) : nullptr;
     ++i;

@@ -507,3 +507,9 @@ def test_selective_layer_with_a_device_count(shape):
     b.blend_device_status(r.h)
     assert torch.equal(xa[:n], xb[:n]) and torch.equal(ka, kb) and torch.equal(va, vb)
     assert torch.equal(xa[n:], x[n:])
+    # an empty selection on the device (count 0 under a positive bound) changes nothing
+    xc, kc2, vc2 = x.clone(), kc.clone(), vc.clone()
+    b.selective_layer(r.h, 1, xc, idx, torch.zeros(1, dtype=torch.int32, device=dev()), kc2, vc2, n_ctx,
+                      max_n=cap)
+    b.blend_device_status(r.h)
+    assert torch.equal(xc, x) and torch.equal(kc2, kc) and torch.equal(vc2, vc)
