@@ -67,6 +67,55 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
     return r;
 }
 
+// Deterministic block-wide integer sum (warp reductions, then one warp over the warp
+// totals); every thread gets the result.  Two barriers.
+__device__ __forceinline__ int block_sum_i32(int v, int* warp_tot, int* bcast) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    v = __reduce_add_sync(0xffffffffu, v);
+    if (lane == 0) warp_tot[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        int x = lane < (int)(blockDim.x >> 5) ? warp_tot[lane] : 0;
+        x = __reduce_add_sync(0xffffffffu, x);
+        if (lane == 0) *bcast = x;
+    }
+    __syncthreads();
+    return *bcast;
+}
+
+// Ordered compaction for one CTA: out[j] = base + p for the positions p < n with keep(p),
+// in ascending order, walked in rounds of blockDim.x consecutive positions (ballots within a
+// warp, a scan of the warp counts); returns the count to every thread.  warp_tot holds
+// blockDim.x / 32 ints (blockDim.x a multiple of 32, at most 1024).
+template <typename Keep>
+__device__ __forceinline__ int compact_in_order(int n, int base, int32_t* out, Keep keep, int* warp_tot, int* bcast) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+    int written = 0;
+    for (int r0 = 0; r0 < n; r0 += blockDim.x) {
+        const int p = r0 + tid;
+        const bool take = p < n && keep(p);
+        const unsigned m = __ballot_sync(0xffffffffu, take);
+        if (lane == 0) warp_tot[warp] = __popc(m);
+        __syncthreads();
+        if (warp == 0) {
+            const int v = lane < nw ? warp_tot[lane] : 0;
+            int incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            if (lane < nw) warp_tot[lane] = incl - v;
+            if (lane == 31) *bcast = incl;
+        }
+        __syncthreads();
+        if (take) out[written + warp_tot[warp] + __popc(m & ((1u << lane) - 1u))] = base + p;
+        written += *bcast;
+        __syncthreads();
+    }
+    return written;
+}
+
 // Per-request description of a batch, passed to kernels by value.
 struct ReqDesc {
     int32_t tok_off;  // first blended token of the request in the batch K/V

@@ -116,22 +116,6 @@ __global__ void __launch_bounds__(RANK_THREADS)
     if (q1 != ~0ull) rank[jb.rank_off + (int)(uint32_t)q1] = c1;
 }
 
-// Deterministic block-wide integer sum (warp reductions, then one warp over the warp
-// totals); every thread gets the result.  Two barriers.
-__device__ __forceinline__ int block_sum_i32(int v, int* warp_tot, int* bcast) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    v = __reduce_add_sync(0xffffffffu, v);
-    if (lane == 0) warp_tot[warp] = v;
-    __syncthreads();
-    if (warp == 0) {
-        int x = lane < (int)(blockDim.x >> 5) ? warp_tot[lane] : 0;
-        x = __reduce_add_sync(0xffffffffu, x);
-        if (lane == 0) *bcast = x;
-    }
-    __syncthreads();
-    return *bcast;
-}
-
 // One CTA per job.  Positions are walked in rounds of SEL_THREADS consecutive positions
 // (round e, thread i: p = e * SEL_THREADS + i), so the accesses of a warp to shared and
 // global memory are consecutive.
@@ -221,31 +205,8 @@ __global__ void __launch_bounds__(SEL_THREADS)
         }
     }
 
-    // ordered compaction of {p : cover(p) < k}, one round of SEL_THREADS positions at a time
-    int written = 0;
-    for (int e = 0; e * SEL_THREADS < n; ++e) {
-        const int p = e * SEL_THREADS + tid;
-        const bool take = p < n && cov[p] < k;
-        const unsigned m = __ballot_sync(0xffffffffu, take);
-        if (lane == 0) warp_tot[warp] = __popc(m);
-        __syncthreads();
-        if (warp == 0) {
-            // exclusive scan of the warp totals
-            const int v = warp_tot[lane];
-            int incl = v;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
-            }
-            warp_tot[lane] = incl - v;
-            if (lane == 31) bcast = incl;
-        }
-        __syncthreads();
-        if (take) jb.out[written + warp_tot[warp] + __popc(m & ((1u << lane) - 1u))] = jb.base + p;
-        written += bcast;
-        __syncthreads();
-    }
+    // ordered compaction of {p : cover(p) < k}
+    const int written = compact_in_order(n, jb.base, jb.out, [&](int p) { return cov[p] < k; }, warp_tot, &bcast);
     if (tid == 0) *jb.out_n = written;
 }
 

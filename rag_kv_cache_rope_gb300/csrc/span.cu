@@ -1,7 +1,7 @@
 // SpecCache token selection on the device (SpecCache notes, "2.3 Semantic span
 // completion" with its global budget control, and "2.4 Cross-tokenizer alignment").
 //
-// Span completion through ranks (rank from k_rank: score descending, ties by position):
+// Span completion through ranks (from k_rank_tiles / k_rank_merge: score descending, ties by position):
 //   * scores are min-max normalised, n~ = (s - min) / (max - min), and token i+1 joins
 //     token i's span while |n~(i+1) - n~(i)| / n~(i) < tau_smooth, at most max_span tokens
 //     per span.  Every step is one fp32 operation rounded to nearest (no contraction),
@@ -25,30 +25,6 @@ constexpr int SP_THREADS = 1024;
 constexpr int SP_MAX_PER_THREAD = 32;  // n <= 32768
 constexpr int SP_MAX_N = SP_THREADS * SP_MAX_PER_THREAD;
 
-__device__ __forceinline__ int block_reduce_sum(int v, int* red) {
-    const int t = threadIdx.x;
-    red[t] = v;
-    __syncthreads();
-    for (int s = blockDim.x >> 1; s > 0; s >>= 1) {
-        if (t < s) red[t] += red[t + s];
-        __syncthreads();
-    }
-    const int r = red[0];
-    __syncthreads();
-    return r;
-}
-__device__ __forceinline__ int block_reduce_max(int v, int* red) {
-    const int t = threadIdx.x;
-    red[t] = v;
-    __syncthreads();
-    for (int s = blockDim.x >> 1; s > 0; s >>= 1) {
-        if (t < s) red[t] = max(red[t], red[t + s]);
-        __syncthreads();
-    }
-    const int r = red[0];
-    __syncthreads();
-    return r;
-}
 __device__ __forceinline__ float canon(float x) { return x == 0.f ? 0.f : x; }  // -0 -> +0
 
 // Normalised score of position p.
@@ -68,6 +44,8 @@ __global__ void __launch_bounds__(SP_THREADS)
     extern __shared__ int32_t cov[];  // n ints (cover values), then n bytes of span-start flags
     __shared__ int red[SP_THREADS];
     __shared__ float fred[2][SP_THREADS / 32];
+    __shared__ int warp_tot[SP_THREADS / 32];
+    __shared__ int bcast;
     const SelectJob& jb = sb.j[blockIdx.x];
     const int n = jb.n;
     uint8_t* start = reinterpret_cast<uint8_t*>(cov + n);
@@ -144,12 +122,14 @@ __global__ void __launch_bounds__(SP_THREADS)
     }
     __syncthreads();
 
-    // 4. TopK size and the budget
+    // 4. TopK size and the budget (counts walk rounds of SP_THREADS consecutive positions:
+    //    conflict-free shared-memory reads)
+    const int tid = threadIdx.x;
     const int kmax = min(jb.budget, n);
     int k = kmax, vcap = INT_MAX;
     int loc = 0;
-    for (int p = p0; p < p1; ++p) loc += cov[p] < kmax;
-    const int f = block_reduce_sum(loc, red);
+    for (int p = tid; p < n; p += SP_THREADS) loc += cov[p] < kmax;
+    const int f = block_sum_i32(loc, warp_tot, &bcast);
     if (sb.budget_mode == BLEND_BUDGET_FINAL) {
         if (f > jb.budget) {
             // smallest v with #{cover <= v} >= budget + 1
@@ -157,8 +137,8 @@ __global__ void __launch_bounds__(SP_THREADS)
             while (a < b) {
                 const int mid = (a + b) >> 1;
                 loc = 0;
-                for (int p = p0; p < p1; ++p) loc += cov[p] <= mid;
-                if (block_reduce_sum(loc, red) >= jb.budget + 1) b = mid;
+                for (int p = tid; p < n; p += SP_THREADS) loc += cov[p] <= mid;
+                if (block_sum_i32(loc, warp_tot, &bcast) >= jb.budget + 1) b = mid;
                 else a = mid + 1;
             }
             k = a;
@@ -169,28 +149,17 @@ __global__ void __launch_bounds__(SP_THREADS)
         while (a < b) {
             const int mid = (a + b) >> 1;
             loc = 0;
-            for (int p = p0; p < p1; ++p) loc += cov[p] < k && rank[p] <= mid;
-            if (block_reduce_sum(loc, red) >= jb.cap) b = mid;
+            for (int p = tid; p < n; p += SP_THREADS) loc += cov[p] < k && rank[p] <= mid;
+            if (block_sum_i32(loc, warp_tot, &bcast) >= jb.cap) b = mid;
             else a = mid + 1;
         }
         vcap = jb.cap > 0 ? a : -1;
     }
 
     // 5. ordered compaction of the members
-    loc = 0;
-    for (int p = p0; p < p1; ++p) loc += cov[p] < k && rank[p] <= vcap;
-    red[threadIdx.x] = loc;
-    __syncthreads();
-    for (int s = 1; s < SP_THREADS; s <<= 1) {  // inclusive scan
-        const int v = threadIdx.x >= s ? red[threadIdx.x - s] : 0;
-        __syncthreads();
-        red[threadIdx.x] += v;
-        __syncthreads();
-    }
-    int o = red[threadIdx.x] - loc;
-    for (int p = p0; p < p1; ++p)
-        if (cov[p] < k && rank[p] <= vcap) jb.out[o++] = jb.base + p;
-    if (threadIdx.x == SP_THREADS - 1) *jb.out_n = red[SP_THREADS - 1];
+    const int written =
+        compact_in_order(n, jb.base, jb.out, [&](int p) { return cov[p] < k && rank[p] <= vcap; }, warp_tot, &bcast);
+    if (tid == 0) *jb.out_n = written;
 }
 
 // SpecCache 2.4: mark every target token of every selected speculative token, then write
