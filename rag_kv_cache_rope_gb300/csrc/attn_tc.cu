@@ -579,22 +579,24 @@ __global__ void __launch_bounds__(THREADS, 1)
 // V's d columns (for P.V), so every block is loaded once for both tiles and each SM
 // reads a third less operand data per FLOP.  The leading CTA issues, for both:
 //   S = Q . K^T   tcgen05.mma.cta_group::2 M256 N128 K16 x8 (A: each CTA's Q tile; B:
-//                 each CTA's 64 keys) into the S buffer of the block's parity
+//                 each CTA's 64 keys) into S buffer j % 3
 //   O += P . V    tcgen05.mma.cta_group::2 M256 N128 K16 x8 (A: each CTA's P in TMEM;
 //                 B: each CTA's 64 d columns of V, MN-major)
-// S and P each have two TMEM buffers (S: 128 fp32 columns, P: 64 columns of bf16 pairs),
-// indexed by the block's parity, and two threads of the leading CTA issue the products:
-// one issues S(j) once the softmax of block j-2 has read that S buffer (its P is ready) and
-// commits it to s_full; the other issues P.V(j) once P(j) is ready and commits it to
-// kv_empty, which frees block j's K/V stage and P buffer.  A single issuer spent about 650
-// of every 1 650 cycles per block on barrier checks and commits between its bursts while
-// the tensor core, with an issue queue about one product deep, sat idle; two issuers
-// overlap those gaps.  The softmax skips the block maximum while its running reference
-// keeps every exponential of the block below 2^50 (the block's sum says so); a row's
-// first block and any block past that bound take the exact path (maximum, conditional
-// rescale by more than 2^8).  A softmax writes P(j) only after P.V(j-2) has read that P buffer,
-// and one that must rescale O (running maximum up by more than 2^8) first waits for
-// P.V(j-1).  The softmax is the single-tile one of k_attn_tc, one pair row per thread.
+// S has three TMEM buffers of 128 fp32 columns, and each block's P (64 columns of bf16
+// pairs) is written over the first half of its own S buffer, so S, P and O take all 512
+// columns.  Two threads of the leading CTA issue the products: one issues S(j) once
+// P.V(j-3) has read the P over that buffer and commits it to s_full; the other issues
+// P.V(j) once P(j) is ready and commits it to kv_empty, which frees block j's K/V stage
+// and S buffer.  A single issuer spent about 650 of every 1 650 cycles per block on
+// barrier checks and commits between its bursts while the tensor core, with an issue
+// queue about one product deep, sat idle; two issuers overlap those gaps.  The softmax
+// skips the block maximum while its running reference keeps every exponential of the
+// block below 2^50 (the block's sum says so); a row's first block and any block past that
+// bound take the exact path (maximum, conditional rescale by more than 2^8).  With three
+// S buffers, S(j) runs up to two blocks ahead of the softmax and the softmax never waits
+// for a P buffer (two buffers for S plus two for P measured about 6 % slower); one that
+// must rescale O first waits for P.V(j-1).  The softmax is the single-tile one of
+// k_attn_tc, one pair row per thread.
 namespace pairk {
 constexpr int THREADS2 = 224;  // warp 0 TMA, 1 TMEM + P.V issue, 2..5 softmax, 6 S issue (leaders)
 constexpr int S_WARP = 6;
@@ -604,9 +606,9 @@ constexpr int VH_BYTES = BKV * 64 * 2;                 // 128 keys x this CTA's 
 constexpr int STAGE_BYTES = 2 * KQ_BYTES + VH_BYTES;   // 32 KB
 constexpr int QT_BYTES = 2 * QH_BYTES;                 // one 128-pair tile, two d halves
 constexpr int SMEM_BYTES = 2 * QT_BYTES + STAGES2 * STAGE_BYTES + 1024;
-constexpr int COLS2 = 512;  // S buffers at 0 and 128, O at 256, P buffers at 384 and 448
-constexpr uint32_t O_COL = 256;
-constexpr uint32_t P_COL = 384;
+constexpr int COLS2 = 512;  // S buffers at 0, 128 and 256 (each block's P goes over its S), O at 384
+constexpr int NSBUF = 3;
+constexpr uint32_t O_COL = 384;
 // kind::f16, bf16 inputs, fp32 accumulate, M256 (the pair) N128; P.V with B MN-major
 constexpr uint32_t IDESC_S2 = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((256u >> 4) << 24);
 constexpr uint32_t IDESC_PV2 = IDESC_S2 | (1u << 16);
@@ -718,8 +720,8 @@ __global__ void __launch_bounds__(pairk::THREADS2, 1)
     using namespace pairk;
     constexpr int D = 128;
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t q_full[2], q_empty[2], kv_full[STAGES2], kv_empty[STAGES2], s_full[2],
-        p_full[2], o_full, o_free;
+    __shared__ __align__(8) uint64_t q_full[2], q_empty[2], kv_full[STAGES2], kv_empty[STAGES2], s_full[NSBUF],
+        p_full[NSBUF], o_full, o_free;
     __shared__ uint32_t tmem_sh;
     __shared__ volatile int abort_flag;
     __shared__ int pend_kv[STAGES2];
@@ -746,9 +748,11 @@ __global__ void __launch_bounds__(pairk::THREADS2, 1)
         for (int b = 0; b < 2; ++b) {
             mbar_init(&q_full[b], 1);
             mbar_init(&q_empty[b], 1);
+            pend_q[b] = -1;
+        }
+        for (int b = 0; b < NSBUF; ++b) {
             mbar_init(&s_full[b], 1);
             mbar_init(&p_full[b], 8);  // 4 softmax warps in each CTA
-            pend_q[b] = -1;
         }
         for (int s = 0; s < STAGES2; ++s) {
             mbar_init(&kv_full[s], 1);
@@ -824,8 +828,8 @@ __global__ void __launch_bounds__(pairk::THREADS2, 1)
         }
     } else if (warp == S_WARP && lane == 0 && rank == 0) {
         // ------------------------------------------------ S issuer (leader, for both CTAs)
-        // S(it) goes into S buffer it & 1 once the softmax of block it - 2 has read that
-        // buffer (its P is ready), and is committed to s_full on its own
+        // S(it) goes into S buffer it % 3 once P.V(it - 3) has read the P that its softmax
+        // wrote over that buffer, and is committed to s_full on its own
         uint32_t it = 0;
         bool ok = true;
         for (int k = 0, tl = 0; ok && !abort_flag; ++k, ++tl) {
@@ -841,8 +845,9 @@ __global__ void __launch_bounds__(pairk::THREADS2, 1)
             pend_q[qb] = -1;
             const uint64_t qd = desc_k(su32(sQ + qb * QT_BYTES));
             for (int kb = 0; kb < m.nblk; ++kb, ++it) {
-                const int b = it & 1, st = it % STAGES2;
-                if ((it >= 2 && !wait_cl(&p_full[b], ((it - 2) >> 1) & 1, &abort_flag)) ||
+                const int b = it % NSBUF, st = it % STAGES2;
+                const uint32_t pv = it - NSBUF;  // the P.V that last read this buffer
+                if ((it >= NSBUF && !wait_cl(&kv_empty[pv % STAGES2], (pv / STAGES2) & 1, &abort_flag)) ||
                     !wait_cl(&kv_full[st], (it / STAGES2) & 1, &abort_flag)) {
                     ok = false;
                     break;
@@ -877,15 +882,15 @@ __global__ void __launch_bounds__(pairk::THREADS2, 1)
             Item m;
             get_item(w, n_req, req_row_end, row_pos, row_tok, group, hkv, m);
             for (int kb = 0; kb < m.nblk; ++kb, ++it) {
-                const int b = it & 1, st = it % STAGES2;
-                if (!wait_cl(&p_full[b], (it >> 1) & 1, &abort_flag) ||
+                const int b = it % NSBUF, st = it % STAGES2;
+                if (!wait_cl(&p_full[b], (it / NSBUF) & 1, &abort_flag) ||
                     (kb == 0 && !wait_cl(&o_free, (tl & 1) ^ 1, &abort_flag))) {
                     ok = false;
                     break;
                 }
                 fence_after();
                 const uint64_t vd = desc_mn(su32(sKV + st * STAGE_BYTES + 2 * KQ_BYTES));
-                const uint32_t pa = tb + P_COL + b * 64;
+                const uint32_t pa = tb + b * 128;  // P over its block's S columns
 #pragma unroll
                 for (int kk = 0; kk < BKV / 16; ++kk)
                     umma_ts2(tb + O_COL, pa + kk * 8, vd + ((kk * 2048) >> 4), IDESC_PV2, (kb > 0 || kk > 0) ? 1u : 0u);
@@ -919,12 +924,11 @@ __global__ void __launch_bounds__(pairk::THREADS2, 1)
             const int my_pos = valid ? row_pos[row] : m.max_pos;
             float m_used = -INFINITY, l = 0.f;
             for (int kb = 0; kb < m.nblk; ++kb, ++it) {
-                const int b = it & 1;
+                const int b = it % NSBUF;
                 const uint32_t s_col = tb + lane_off + b * 128;
-                const uint32_t p_col = tb + lane_off + P_COL + b * 64;
-                // S(it) is the (it / 2)-th product into S buffer b; S(it + 2) waits for this
-                // block's P, so the barrier is never a phase ahead
-                const bool got = warp_wait_cl(&s_full[b], (it >> 1) & 1, &abort_flag);
+                // S(it) is the (it / 3)-th product into S buffer b; S(it + 3) waits for
+                // P.V(it), which waits for this block's P, so the barrier is never a phase ahead
+                const bool got = warp_wait_cl(&s_full[b], (it / NSBUF) & 1, &abort_flag);
                 if (!got) {
                     ok = false;
                     break;
@@ -1010,18 +1014,10 @@ __global__ void __launch_bounds__(pairk::THREADS2, 1)
                     }
                     accs = __fadd2_rn(acc2[0], acc2[1]);
                 }
-                if (it >= 2) {
-                    // P buffer b is free once P.V(it - 2) has read it (that block's stage is
-                    // released by the same commit, at most one use of the stage behind)
-                    const uint32_t pv = it - 2;
-                    if (!warp_wait_cl(&kv_empty[pv % STAGES2], (pv / STAGES2) & 1, &abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    fence_after();
-                }
-                TMEM_ST32(p_col, s);
-                TMEM_ST32(p_col + 32, (s + 32));
+                // P goes over the first 64 columns of its own S buffer (the scores are in
+                // registers; the buffer's next product waits for this block's P.V)
+                TMEM_ST32(s_col, s);
+                TMEM_ST32(s_col + 32, (s + 32));
                 if (rescale && kb > 0) {
                     // O must hold every block before this one: wait for the previous P.V
                     // (the previous block's stage is released when its P.V completes, at most
