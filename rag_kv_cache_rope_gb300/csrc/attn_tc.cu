@@ -873,7 +873,7 @@ __global__ void __launch_bounds__(pairk::THREADS2, 1)
     } else if (warp == 1 && lane == 0 && rank == 0) {
         // ------------------------------------------------ P.V issuer (leader, for both CTAs)
         // P.V(it) once both CTAs' softmax warps have written P(it); its commit frees block
-        // it's K/V stage (S(it) completed before that softmax began) and its P buffer
+        // it's K/V stage (S(it) completed before that softmax began) and its S buffer
         uint32_t it = 0;
         bool ok = true;
         for (int k = 0, tl = 0; ok && !abort_flag; ++k, ++tl) {
