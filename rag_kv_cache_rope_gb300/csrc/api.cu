@@ -1086,7 +1086,8 @@ extern "C" int blend_prefill(blend_handle* h, int32_t n_req, const blend_request
         cudaStreamWaitEvent(h->side, h->ev_start, 0);
         for (int l = 0; l < c.n_layers && l < 2; ++l) stage_layer_copy(h, pool, l);
         rc = check_cuda(h, "blend_prefill (pool loading)");
-    }    if (rc != BLEND_OK) return rc;
+    }
+    if (rc != BLEND_OK) return rc;
 
     // ---- 2. stage-0 rows
     StageDesc st0{h->set[0], h->set_n[0], 0};
