@@ -49,7 +49,7 @@ extern "C" {
 #define BLEND_EMISS (-4)        /* a requested pool entry has no cache (fetch miss) */
 #define BLEND_ETIMEOUT (-5)     /* a bounded device wait expired */
 #define BLEND_EDEVICE (-6)      /* a device-side check failed (error word set) */
-#define BLEND_EUNSUPPORTED (-7) /* shape or dtype this build does not handle */
+#define BLEND_EUNSUPPORTED (-7) /* shape or dtype the library does not handle */
 
 /* ---- enums ----------------------------------------------------------------- */
 #define BLEND_F32 0

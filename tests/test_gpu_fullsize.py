@@ -22,7 +22,7 @@ from blendcase import (assert_hkvd_sets_replay, f64, maxrel, oracle_cfg, relerr,
 
 pytestmark = pytest.mark.gpu
 
-# bf16 outputs: the benchmark spec's 2e-2, as the norm-wise relative error and as the
+# bf16 outputs: a 2e-2 bar on the norm-wise relative error and on the
 # max-norm (max|d| / max|ref|) that catches a wrong row or head the 2-norm would dilute.
 TOL_BF16 = 2e-2
 
