@@ -44,6 +44,10 @@ SHAPES = [
     (synth.ModelShape("tc-pair-odd", 2, 512, 8, 2, 128, 1024, 300, 1e6), 90, 300),
     (synth.ModelShape("tc-pair-129", 2, 512, 8, 2, 128, 1024, 300, 1e6), 129, 500),
     (synth.ModelShape("tc-pair-257", 2, 1280, 10, 2, 128, 2560, 300, 1e6), 257, 2000),
+    # one query head per kv head (plain multi-head attention) and eight (a tile of 128 pairs
+    # then holds 16 rows)
+    (synth.ModelShape("tc-mha", 2, 512, 4, 4, 128, 1024, 300, 1e6), 300, 900),
+    (synth.ModelShape("tc-gqa8", 2, 2048, 16, 2, 128, 2048, 300, 1e6), 200, 1200),
 ]
 
 
