@@ -48,6 +48,9 @@ SHAPES = [
     # then holds 16 rows)
     (synth.ModelShape("tc-mha", 2, 512, 4, 4, 128, 1024, 300, 1e6), 300, 900),
     (synth.ModelShape("tc-gqa8", 2, 2048, 16, 2, 128, 2048, 300, 1e6), 200, 1200),
+    # 525 rows with an 8B-wide MLP (the few-row regime of the 8B HKVD request: 336 CTA-pair
+    # gate/up tiles, a last wave run as K halves)
+    (synth.ModelShape("tc-mlp-525", 2, 512, 8, 2, 128, 14336, 300, 1e6), 525, 900),
 ]
 
 
